@@ -1,0 +1,162 @@
+"""Float64 CPU oracle of the WKV operator (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library
+and ``rwkv_linear_attention_backward_b300``) never does.
+
+The arithmetic lives in ``wkv_oracle.c`` (plain C, float64, OpenMP over
+independent channels); this module compiles it with gcc when needed and
+wraps each entry point for numpy arrays.  Inputs of any float dtype are
+widened to float64 before the call, so the oracle sees exactly the values
+handed to the GPU (fp32, or bf16 rounded values).
+"""
+from __future__ import annotations
+
+import ctypes
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+SOURCE = _HERE / "wkv_oracle.c"
+LIBRARY = _HERE / "liboracle.so"
+
+_DP = ctypes.POINTER(ctypes.c_double)
+
+
+def build(source: Path = SOURCE, output: Path = LIBRARY, quiet: bool = True) -> Path:
+    """Compile the oracle C source into a shared library with gcc."""
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-Wall", "-o", str(output), str(source), "-lm"]
+    subprocess.run(cmd, check=True, capture_output=quiet)
+    return output
+
+
+def _stale(lib: Path, src: Path) -> bool:
+    return (not lib.exists()) or lib.stat().st_mtime < src.stat().st_mtime
+
+
+class Oracle:
+    """ctypes handle on one compiled copy of the oracle library."""
+
+    def __init__(self, library: Path | str):
+        self.path = str(library)
+        self._lib = ctypes.CDLL(self.path)
+        i, p = ctypes.c_int, _DP
+        sigs = {
+            "wkv_oracle_forward_direct": [i, i, i, p, p, p, p, p],
+            "wkv_oracle_forward_recurrent": [i, i, i, p, p, p, p, p],
+            "wkv_oracle_backward_adjoint": [i, i, i, p, p, p, p, p, p, p, p, p],
+            "wkv_oracle_backward_direct": [i, i, i, p, p, p, p, p, p, p, p, p],
+            "wkv_oracle_state": [i, i, i, p, p, p, i, p, p, p],
+            "wkv_oracle_decode_step": [i, i, i] + [p] * 17,
+        }
+        for name, args in sigs.items():
+            fn = getattr(self._lib, name)
+            fn.argtypes = args
+            fn.restype = None
+        self._lib.wkv_oracle_num_threads.restype = ctypes.c_int
+
+    # ------------------------------------------------------------------ utils
+    @staticmethod
+    def _in(a) -> np.ndarray:
+        if hasattr(a, "detach"):  # torch tensor (CPU); bf16 widened via float32
+            import torch
+
+            a = a.detach().to("cpu")
+            if a.dtype == torch.bfloat16:
+                a = a.float()
+            a = a.numpy()
+        return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+    @staticmethod
+    def _ptr(a: np.ndarray | None):
+        if a is None:
+            return ctypes.cast(None, _DP)
+        return a.ctypes.data_as(_DP)
+
+    def num_threads(self) -> int:
+        return int(self._lib.wkv_oracle_num_threads())
+
+    # -------------------------------------------------------------- forward
+    def forward_direct(self, w, u, k, v) -> np.ndarray:
+        w, u, k, v = map(self._in, (w, u, k, v))
+        B, T, C = k.shape
+        y = np.empty_like(k)
+        self._lib.wkv_oracle_forward_direct(B, T, C, *map(self._ptr, (w, u, k, v, y)))
+        return y
+
+    def forward_recurrent(self, w, u, k, v) -> np.ndarray:
+        w, u, k, v = map(self._in, (w, u, k, v))
+        B, T, C = k.shape
+        y = np.empty_like(k)
+        self._lib.wkv_oracle_forward_recurrent(B, T, C, *map(self._ptr, (w, u, k, v, y)))
+        return y
+
+    # ------------------------------------------------------------- backward
+    def _backward(self, fn, w, u, k, v, gy):
+        w, u, k, v, gy = map(self._in, (w, u, k, v, gy))
+        B, T, C = k.shape
+        gw = np.empty(C)
+        gu = np.empty(C)
+        gk = np.empty_like(k)
+        gv = np.empty_like(k)
+        fn(B, T, C, *map(self._ptr, (w, u, k, v, gy, gw, gu, gk, gv)))
+        return gw, gu, gk, gv
+
+    def backward_adjoint(self, w, u, k, v, gy):
+        """Returns (gw, gu, gk, gv) by reverse-mode of the recurrence."""
+        return self._backward(self._lib.wkv_oracle_backward_adjoint, w, u, k, v, gy)
+
+    def backward_direct(self, w, u, k, v, gy):
+        """Returns (gw, gu, gk, gv) by differentiating the O(T^2) sum."""
+        return self._backward(self._lib.wkv_oracle_backward_direct, w, u, k, v, gy)
+
+    # ---------------------------------------------------------------- state
+    def state(self, w, k, v, t: int):
+        """(num, den, pp), each [B, C], after the first t tokens."""
+        w, k, v = map(self._in, (w, k, v))
+        B, T, C = k.shape
+        num = np.empty((B, C))
+        den = np.empty((B, C))
+        pp = np.empty((B, C))
+        self._lib.wkv_oracle_state(B, T, C, *map(self._ptr, (w, k, v)), int(t), *map(self._ptr, (num, den, pp)))
+        return num, den, pp
+
+    # --------------------------------------------------------------- decode
+    def decode_step(self, x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u, num, den, pp, mix: bool = True):
+        """One RNN-mode step of L layers.  Returns (y, num, den, pp, xk, xv, xr)
+        with the state arrays new (inputs are not modified); the mix outputs
+        are None when ``mix`` is False."""
+        x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u = map(self._in, (x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u))
+        num, den, pp = (self._in(a).copy() for a in (num, den, pp))
+        L, B, C = x.shape
+        y = np.empty_like(x)
+        xk = np.empty_like(x) if mix else None
+        xv = np.empty_like(x) if mix else None
+        xr = np.empty_like(x) if mix else None
+        self._lib.wkv_oracle_decode_step(
+            L, B, C,
+            *map(self._ptr, (x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u, num, den, pp, y, xk, xv, xr)),
+        )
+        return y, num, den, pp, xk, xv, xr
+
+
+_DEFAULT: Oracle | None = None
+
+
+def load() -> Oracle:
+    """The oracle built from ``wkv_oracle.c`` (compiled on first use)."""
+    global _DEFAULT
+    if _DEFAULT is None:
+        if _stale(LIBRARY, SOURCE):
+            build()
+        _DEFAULT = Oracle(LIBRARY)
+    return _DEFAULT
+
+
+def __getattr__(name):  # convenience: oracle.forward_direct(...) etc.
+    if name.startswith("_"):
+        raise AttributeError(name)
+    return getattr(load(), name)
+

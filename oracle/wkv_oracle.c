@@ -1,0 +1,309 @@
+/*
+ * wkv_oracle.c -- plain, slow, float64 CPU reference of the WKV operator.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library
+ * and its Python binding) may call, link or load this file.  It is used by
+ * the tests, by __graft_entry__.smoke() and by bench.py's CPU baseline leg.
+ * It shares no code, header, table or helper with the CUDA sources.
+ *
+ * What it computes (sources, by page title and section):
+ *
+ *  - "RWKV解读：在Transformer的时代的新RNN" (segmentfault), section
+ *    "3、RWKV的网络架构", equation (8): the time-mixing "attention" wkv.  The
+ *    page says the absolute-position bias of AFT is replaced by a relative
+ *    one driven by a single trained vector w, the current position gets its
+ *    own parameter u, and that eq. (8) can be written recursively.
+ *  - "RWKV についての調査記録" (qiita), section "wkvとは": wkv is a weighted
+ *    average of v with weights from k; the current v receives a bonus u;
+ *    past v are decayed more the further back they are, through one
+ *    channel-wise decay vector w; all channels are computed independently.
+ *  - Same page, section "Trainingについて": all parameters get gradients
+ *    from the loss, so w, u, k and v all need gradients.
+ *  - "RWKV解读" section "3、RWKV的网络架构", equations (7) and (9): the
+ *    token shift (input is a weighted sum of the current and the previous
+ *    token) and the sigmoid(r) gate on the time-mixing output.
+ *  - "介绍RWKV – 具有Transformer优势的RNN" (xiaozhuai), section
+ *    "RWKV作为RNN和transformer的结合体", and qiita "RWKVとは？": in
+ *    inference the layer takes a token and a state and returns an output
+ *    and a new state (the decode step).
+ *
+ * The pages lost the bodies of every equation, so the exact form used here
+ * is the standard RWKV-4 definition, which matches every property the
+ * pages state.  Per batch row b and channel c (both dropped), t in [0,T):
+ *
+ *     wkv_t = ( sum_{i<t} e^{-(t-1-i) w + k_i} v_i  +  e^{u + k_t} v_t )
+ *           / ( sum_{i<t} e^{-(t-1-i) w + k_i}      +  e^{u + k_t}     )
+ *
+ * w > 0 is the decay (passed in directly), u the bonus.  The most recent
+ * past token (i = t-1) carries factor e^0: it is not decayed.
+ *
+ * Layout: k, v, y, gy, gk, gv are [B, T, C] row-major with C fastest;
+ * w, u, gw, gu are [C].  Decode tensors are [L, B, C]; per-layer
+ * parameters are [L, C].
+ *
+ * Every function here is pinned by tests under tests/ against values that
+ * do not come from this file (closed forms, brute force finite differences,
+ * limits, invariants); see tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define IDX(b, t, c) (((size_t)(b) * (size_t)T + (size_t)(t)) * (size_t)C + (size_t)(c))
+
+int wkv_oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Forward, direct O(T^2) form: the definition above written out.  Each
+ * exponent is formed first and exponentiated once. */
+void wkv_oracle_forward_direct(int B, int T, int C, const double *w, const double *u,
+                               const double *k, const double *v, double *y)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int c = 0; c < C; ++c) {
+            for (int t = 0; t < T; ++t) {
+                double num = 0.0, den = 0.0;
+                for (int i = 0; i < t; ++i) {
+                    double e = exp(-(double)(t - 1 - i) * w[c] + k[IDX(b, i, c)]);
+                    num += e * v[IDX(b, i, c)];
+                    den += e;
+                }
+                double e = exp(u[c] + k[IDX(b, t, c)]);
+                num += e * v[IDX(b, t, c)];
+                den += e;
+                y[IDX(b, t, c)] = num / den;
+            }
+        }
+}
+
+/* Forward, recurrent form ("eq. (8) can be written recursively").  Two
+ * accumulators per channel: a_t = sum_{i<t} e^{-(t-1-i)w + k_i} v_i and
+ * b_t likewise without v.  a_0 = b_0 = 0, and
+ *     wkv_t   = (a_t + e^{u+k_t} v_t) / (b_t + e^{u+k_t})
+ *     a_{t+1} = e^{-w} a_t + e^{k_t} v_t,   b_{t+1} = e^{-w} b_t + e^{k_t}.
+ * No rescaling: in float64 the accumulators stay far from overflow for
+ * |k| up to several hundred. */
+void wkv_oracle_forward_recurrent(int B, int T, int C, const double *w, const double *u,
+                                  const double *k, const double *v, double *y)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int c = 0; c < C; ++c) {
+            double a = 0.0, bb = 0.0;
+            double decay = exp(-w[c]);
+            for (int t = 0; t < T; ++t) {
+                double kt = k[IDX(b, t, c)], vt = v[IDX(b, t, c)];
+                double e = exp(u[c] + kt);
+                y[IDX(b, t, c)] = (a + e * vt) / (bb + e);
+                double ek = exp(kt);
+                a = decay * a + ek * vt;
+                bb = decay * bb + ek;
+            }
+        }
+}
+
+/* Backward, reverse-mode differentiation of the recurrent form.  Given the
+ * upstream gradient gy = dLoss/dwkv, returns gk, gv ([B,T,C]) and gw, gu
+ * ([C], summed over b and t).  With N_t, D_t the numerator and denominator
+ * of wkv_t, e_t = e^{u+k_t}, gN_t = gy_t / D_t and gD_t = -gy_t wkv_t / D_t,
+ * and adjoints la_t = dLoss/da_t, lb_t = dLoss/db_t (la_T = lb_T = 0):
+ *     gk_t = (gN_t v_t + gD_t) e_t + (la_{t+1} v_t + lb_{t+1}) e^{k_t}
+ *     gv_t = gN_t e_t + la_{t+1} e^{k_t}
+ *     gu  += (gN_t v_t + gD_t) e_t
+ *     gw  += -e^{-w} (la_{t+1} a_t + lb_{t+1} b_t)
+ *     la_t = gN_t + e^{-w} la_{t+1},    lb_t = gD_t + e^{-w} lb_{t+1}.
+ * The forward accumulators are kept per step (O(T) memory per channel). */
+void wkv_oracle_backward_adjoint(int B, int T, int C, const double *w, const double *u,
+                                 const double *k, const double *v, const double *gy,
+                                 double *gw, double *gu, double *gk, double *gv)
+{
+    /* per-(b, c) partial sums of gw, gu, reduced over b in a fixed order
+     * afterwards so the result does not depend on the thread count */
+    double *pw = (double *)malloc(sizeof(double) * (size_t)B * (size_t)C);
+    double *pu = (double *)malloc(sizeof(double) * (size_t)B * (size_t)C);
+#pragma omp parallel
+    {
+        /* per-thread storage of the forward accumulators a_t, b_t */
+        double *a = (double *)malloc(sizeof(double) * (size_t)(T + 1));
+        double *bb = (double *)malloc(sizeof(double) * (size_t)(T + 1));
+#pragma omp for collapse(2) schedule(static)
+        for (int b = 0; b < B; ++b)
+            for (int c = 0; c < C; ++c) {
+                double decay = exp(-w[c]);
+                a[0] = 0.0;
+                bb[0] = 0.0;
+                for (int t = 0; t < T; ++t) {
+                    double ek = exp(k[IDX(b, t, c)]);
+                    a[t + 1] = decay * a[t] + ek * v[IDX(b, t, c)];
+                    bb[t + 1] = decay * bb[t] + ek;
+                }
+                double la = 0.0, lb = 0.0, sgw = 0.0, sgu = 0.0;
+                for (int t = T - 1; t >= 0; --t) {
+                    double kt = k[IDX(b, t, c)], vt = v[IDX(b, t, c)], g = gy[IDX(b, t, c)];
+                    double e = exp(u[c] + kt), ek = exp(kt);
+                    double D = bb[t] + e;
+                    double N = a[t] + e * vt;
+                    double yt = N / D;
+                    double gN = g / D;
+                    double gD = -g * yt / D;
+                    gk[IDX(b, t, c)] = (gN * vt + gD) * e + (la * vt + lb) * ek;
+                    gv[IDX(b, t, c)] = gN * e + la * ek;
+                    sgu += (gN * vt + gD) * e;
+                    sgw += -decay * (la * a[t] + lb * bb[t]);
+                    la = gN + decay * la;
+                    lb = gD + decay * lb;
+                }
+                pw[(size_t)b * (size_t)C + (size_t)c] = sgw;
+                pu[(size_t)b * (size_t)C + (size_t)c] = sgu;
+            }
+        free(a);
+        free(bb);
+    }
+    for (int c = 0; c < C; ++c) {
+        double sw = 0.0, su = 0.0;
+        for (int b = 0; b < B; ++b) {
+            sw += pw[(size_t)b * (size_t)C + (size_t)c];
+            su += pu[(size_t)b * (size_t)C + (size_t)c];
+        }
+        gw[c] = sw;
+        gu[c] = su;
+    }
+    free(pw);
+    free(pu);
+}
+
+/* Backward, direct O(T^2) derivative of the definition.  For i < t the
+ * weight of token i in wkv_t is W_ti = e^{-(t-1-i)w + k_i}; for i = t it is
+ * e^{u+k_t}.  Then, with D_t the denominator:
+ *     d wkv_t / d v_i = W_ti / D_t
+ *     d wkv_t / d k_i = W_ti (v_i - wkv_t) / D_t
+ *     d wkv_t / d u   = e^{u+k_t} (v_t - wkv_t) / D_t
+ *     d wkv_t / d w   = -sum_{i<t} (t-1-i) W_ti (v_i - wkv_t) / D_t
+ * and each is contracted with gy_t.  Shares nothing with the adjoint form. */
+void wkv_oracle_backward_direct(int B, int T, int C, const double *w, const double *u,
+                                const double *k, const double *v, const double *gy,
+                                double *gw, double *gu, double *gk, double *gv)
+{
+    for (int c = 0; c < C; ++c) {
+        gw[c] = 0.0;
+        gu[c] = 0.0;
+    }
+    for (size_t n = 0; n < (size_t)B * (size_t)T * (size_t)C; ++n) {
+        gk[n] = 0.0;
+        gv[n] = 0.0;
+    }
+#pragma omp parallel for schedule(static)
+    for (int c = 0; c < C; ++c)
+        for (int b = 0; b < B; ++b)
+            for (int t = 0; t < T; ++t) {
+                double D = 0.0, N = 0.0;
+                for (int i = 0; i < t; ++i) {
+                    double W = exp(-(double)(t - 1 - i) * w[c] + k[IDX(b, i, c)]);
+                    D += W;
+                    N += W * v[IDX(b, i, c)];
+                }
+                double Wt = exp(u[c] + k[IDX(b, t, c)]);
+                D += Wt;
+                N += Wt * v[IDX(b, t, c)];
+                double yt = N / D, g = gy[IDX(b, t, c)];
+                for (int i = 0; i < t; ++i) {
+                    double W = exp(-(double)(t - 1 - i) * w[c] + k[IDX(b, i, c)]);
+                    double vi = v[IDX(b, i, c)];
+                    gv[IDX(b, i, c)] += g * W / D;
+                    gk[IDX(b, i, c)] += g * W * (vi - yt) / D;
+                    gw[c] += -g * (double)(t - 1 - i) * W * (vi - yt) / D;
+                }
+                double vt = v[IDX(b, t, c)];
+                gv[IDX(b, t, c)] += g * Wt / D;
+                gk[IDX(b, t, c)] += g * Wt * (vt - yt) / D;
+                gu[c] += g * Wt * (vt - yt) / D;
+            }
+}
+
+/* The carried state after the first t tokens (t in [0, T]) in the
+ * (num, den, pp) convention of the decode step: a_t = num * e^{pp},
+ * b_t = den * e^{pp}, where pp is the exact running maximum of the
+ * exponents, pp_t = max_{i<t} (k_i - (t-1-i) w), and pp_0 = -1e38 with
+ * num = den = 0 (no token seen).  Written from the definition (direct sum),
+ * not from a recurrence.  Outputs are [B, C]. */
+void wkv_oracle_state(int B, int T, int C, const double *w, const double *k, const double *v,
+                      int t, double *num, double *den, double *pp)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int c = 0; c < C; ++c) {
+            size_t o = (size_t)b * (size_t)C + (size_t)c;
+            if (t <= 0) {
+                num[o] = 0.0;
+                den[o] = 0.0;
+                pp[o] = -1e38;
+                continue;
+            }
+            double m = -INFINITY;
+            for (int i = 0; i < t; ++i) {
+                double ex = k[IDX(b, i, c)] - (double)(t - 1 - i) * w[c];
+                if (ex > m) m = ex;
+            }
+            double sa = 0.0, sb = 0.0;
+            for (int i = 0; i < t; ++i) {
+                double W = exp(k[IDX(b, i, c)] - (double)(t - 1 - i) * w[c] - m);
+                sa += W * v[IDX(b, i, c)];
+                sb += W;
+            }
+            num[o] = sa;
+            den[o] = sb;
+            pp[o] = m;
+        }
+}
+
+/* One decode step of L independent time-mixing layers (RNN mode).  Per
+ * (l, b, c), with per-layer parameters indexed (l, c):
+ *   token shift, eq. (7):  xk = mu_k x + (1 - mu_k) x_prev  (xv, xr alike)
+ *   wkv from the carried state and this token's k, v:
+ *        a = num e^{pp}, b = den e^{pp},
+ *        wkv = (a + e^{u+k} v) / (b + e^{u+k})
+ *   gate, eq. (9):  y = sigmoid(r) * wkv = wkv / (1 + e^{-r})
+ *   state update:   a' = e^{-w} a + e^{k} v,  b' = e^{-w} b + e^{k},
+ *                   pp' = max(pp - w, k),  num' = a' e^{-pp'},  den' = b' e^{-pp'}.
+ * num, den, pp are updated in place.  xk, xv, xr may be NULL. */
+void wkv_oracle_decode_step(int L, int B, int C, const double *x, const double *x_prev,
+                            const double *mu_k, const double *mu_v, const double *mu_r,
+                            const double *r, const double *k, const double *v,
+                            const double *w, const double *u, double *num, double *den,
+                            double *pp, double *y, double *xk, double *xv, double *xr)
+{
+#pragma omp parallel for collapse(3) schedule(static)
+    for (int l = 0; l < L; ++l)
+        for (int b = 0; b < B; ++b)
+            for (int c = 0; c < C; ++c) {
+                size_t o = ((size_t)l * (size_t)B + (size_t)b) * (size_t)C + (size_t)c;
+                size_t p = (size_t)l * (size_t)C + (size_t)c;
+                if (xk) xk[o] = mu_k[p] * x[o] + (1.0 - mu_k[p]) * x_prev[o];
+                if (xv) xv[o] = mu_v[p] * x[o] + (1.0 - mu_v[p]) * x_prev[o];
+                if (xr) xr[o] = mu_r[p] * x[o] + (1.0 - mu_r[p]) * x_prev[o];
+                double scale = exp(pp[o]);
+                double a = num[o] * scale, bb = den[o] * scale;
+                double e = exp(u[p] + k[o]);
+                double wkv = (a + e * v[o]) / (bb + e);
+                y[o] = wkv / (1.0 + exp(-r[o]));
+                double ek = exp(k[o]);
+                double a2 = exp(-w[p]) * a + ek * v[o];
+                double b2 = exp(-w[p]) * bb + ek;
+                double pp2 = pp[o] - w[p] > k[o] ? pp[o] - w[p] : k[o];
+                num[o] = a2 * exp(-pp2);
+                den[o] = b2 * exp(-pp2);
+                pp[o] = pp2;
+            }
+}

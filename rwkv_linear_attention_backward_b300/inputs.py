@@ -1,0 +1,146 @@
+"""Seeded synthetic inputs shared by the tests, the oracle checks and bench.py.
+
+This module draws random numbers and nothing else: it holds none of the WKV
+arithmetic.  Every tensor is drawn on the CPU with ``torch.Generator`` so
+that the same seed gives the same values on any machine, in a fixed draw
+order (documented per function).  bf16 tensors are drawn in fp32 and then
+rounded to nearest-even by ``Tensor.to(torch.bfloat16)``; the oracle is
+handed the rounded values.
+
+Named workloads (sizes and distributions of the training / inference
+shapes this library targets):
+
+=========  ==========================================================
+name       shape and distributions
+=========  ==========================================================
+tiny       fwd+bwd fp32, B=1 T=64 C=64; k,v ~ N(0,1); w=exp(d),
+           d ~ U(-5,1); u ~ U(-1,1); gy ~ N(0,1)
+l169m      fwd+bwd fp32, B=8 T=1024 C=768 (one layer of a 169M RWKV-4);
+           k ~ N(0,3^2), v ~ N(0,1); d ~ U(-6,2); u ~ U(-1,1); gy ~ N(0,1)
+l1b5       fwd+bwd fp32, B=16 T=4096 C=2048 (1.5B-class layer); as l169m
+long       fwd only, bf16 k,v, fp32 state and output, B=1 T=131072
+           C=2560; k ~ N(0,5^2), v ~ N(0,1); d ~ U(-8,1); u ~ U(-1,1)
+decode     RNN decode, L=32 layers, B=256, C=4096, 1024 steps; x, x_prev,
+           r, k, v ~ N(0,1); mu_k, mu_v, mu_r ~ U(0,1); d ~ U(-6,2),
+           u ~ U(-1,1) per layer; state starts at (0, 0, -1e38)
+=========  ==========================================================
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class TrainingWorkload:
+    name: str
+    B: int
+    T: int
+    C: int
+    k_std: float
+    d_lo: float
+    d_hi: float
+    kv_dtype: str  # "f32" or "bf16"
+    backward: bool
+    seed: int
+
+    @property
+    def elements(self) -> int:
+        return self.B * self.T * self.C
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    L: int
+    B: int
+    C: int
+    steps: int
+    d_lo: float
+    d_hi: float
+    seed: int
+
+    @property
+    def elements_per_step(self) -> int:
+        return self.L * self.B * self.C
+
+
+WORKLOADS = {
+    "tiny": TrainingWorkload("tiny", 1, 64, 64, 1.0, -5.0, 1.0, "f32", True, 1001),
+    "l169m": TrainingWorkload("l169m", 8, 1024, 768, 3.0, -6.0, 2.0, "f32", True, 1002),
+    "l1b5": TrainingWorkload("l1b5", 16, 4096, 2048, 3.0, -6.0, 2.0, "f32", True, 1003),
+    "long": TrainingWorkload("long", 1, 131072, 2560, 5.0, -8.0, 1.0, "bf16", False, 1004),
+}
+DECODE = DecodeWorkload("decode", 32, 256, 4096, 1024, -6.0, 2.0, 1005)
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def training_inputs(B: int, T: int, C: int, *, seed: int, k_std: float = 1.0, d_lo: float = -5.0,
+                    d_hi: float = 1.0, kv_dtype: str = "f32", k_shift: float = 0.0):
+    """Draw (w, u, k, v, gy) on the CPU.
+
+    Draw order: d [C], u [C], k [B,T,C], v [B,T,C], gy [B,T,C].
+    w = exp(d) in fp32 (the decay is handed to the operator directly).
+    ``k_shift`` adds a constant to every k after drawing (used by the
+    shift-invariance checks).  k and v are rounded to bf16 when
+    ``kv_dtype == "bf16"``; w, u and gy stay fp32.
+    """
+    g = _gen(seed)
+    d = torch.rand(C, generator=g, dtype=torch.float32) * (d_hi - d_lo) + d_lo
+    u = torch.rand(C, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    k = torch.randn(B, T, C, generator=g, dtype=torch.float32) * k_std
+    v = torch.randn(B, T, C, generator=g, dtype=torch.float32)
+    gy = torch.randn(B, T, C, generator=g, dtype=torch.float32)
+    if k_shift:
+        k = k + k_shift
+    w = torch.exp(d)
+    if kv_dtype == "bf16":
+        k = k.to(torch.bfloat16)
+        v = v.to(torch.bfloat16)
+    elif kv_dtype != "f32":
+        raise ValueError(f"kv_dtype must be 'f32' or 'bf16', got {kv_dtype!r}")
+    return w, u, k, v, gy
+
+
+def workload_inputs(name: str):
+    wl = WORKLOADS[name]
+    return training_inputs(wl.B, wl.T, wl.C, seed=wl.seed, k_std=wl.k_std, d_lo=wl.d_lo, d_hi=wl.d_hi,
+                           kv_dtype=wl.kv_dtype)
+
+
+def decode_params(L: int, C: int, *, seed: int, d_lo: float = -6.0, d_hi: float = 2.0):
+    """Per-layer decode parameters, each [L, C]: (mu_k, mu_v, mu_r, w, u).
+
+    Draw order: d, u, mu_k, mu_v, mu_r.  w = exp(d).
+    """
+    g = _gen(seed)
+    d = torch.rand(L, C, generator=g, dtype=torch.float32) * (d_hi - d_lo) + d_lo
+    u = torch.rand(L, C, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    mu_k = torch.rand(L, C, generator=g, dtype=torch.float32)
+    mu_v = torch.rand(L, C, generator=g, dtype=torch.float32)
+    mu_r = torch.rand(L, C, generator=g, dtype=torch.float32)
+    return mu_k, mu_v, mu_r, torch.exp(d), u
+
+
+def decode_step_inputs(L: int, B: int, C: int, *, seed: int, step: int):
+    """Per-step decode inputs, each [L, B, C]: (x, x_prev, r, k, v) ~ N(0,1).
+
+    Each step index has its own generator (seed * 1_000_003 + step), so any
+    step can be drawn without drawing the ones before it.  Draw order: x,
+    x_prev, r, k, v.
+    """
+    g = _gen(int(seed) * 1_000_003 + int(step))
+    shape = (L, B, C)
+    return tuple(torch.randn(shape, generator=g, dtype=torch.float32) for _ in range(5))
+
+
+def initial_state(L: int, B: int, C: int):
+    """Decode state before any token: num = den = 0, pp = -1e38."""
+    z = torch.zeros(L, B, C, dtype=torch.float32)
+    return z.clone(), z.clone(), torch.full((L, B, C), -1e38, dtype=torch.float32)

@@ -1,0 +1,338 @@
+"""Pins of the float64 oracle against facts that do not come from the oracle.
+
+Each ``pin_*`` function takes an oracle handle (``oracle.Oracle``) and raises
+``AssertionError`` when the oracle disagrees with what the definition of the
+operator fixes: hand-derived values (``golden/hand_cases.json``), closed
+forms of special cases, limits, invariants and brute-force finite
+differences.  ``test_oracle_pins.py`` runs them on the real oracle;
+``test_oracle_mutants.py`` runs them on deliberately broken copies and
+checks that every broken copy fails at least one pin.
+
+Sources (page title, section):
+  * "RWKV についての調査記録" (qiita), "wkvとは": wkv is a weighted average of
+    v with weights from k, a bonus u for the current token, a decay that
+    grows with distance through one channel-wise vector w, and independent
+    channels.
+  * "RWKV解读：在Transformer的时代的新RNN" (segmentfault),
+    "3、RWKV的网络架构": eq. (8) and its recursive form, token shift eq. (7),
+    sigmoid(r) gate eq. (9).
+  * qiita "Trainingについて": gradients for every parameter.
+"""
+from __future__ import annotations
+
+import json
+from pathlib import Path
+
+import numpy as np
+from scipy.special import expit
+
+GOLDEN = json.loads((Path(__file__).parent / "golden" / "hand_cases.json").read_text())
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _rand_inputs(seed, B=2, T=37, C=5, k_std=1.0, w_lo=-3.0, w_hi=1.0):
+    r = _rng(seed)
+    w = np.exp(r.uniform(w_lo, w_hi, C))
+    u = r.uniform(-1, 1, C)
+    k = r.normal(0, k_std, (B, T, C))
+    v = r.normal(0, 1, (B, T, C))
+    gy = r.normal(0, 1, (B, T, C))
+    return w, u, k, v, gy
+
+
+def _close(a, b, rtol, atol=0.0, what=""):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    err = np.abs(a - b)
+    bound = atol + rtol * np.abs(b)
+    assert np.all(err <= bound), f"{what}: max err {err.max():.3e} (rtol {rtol}, atol {atol})"
+
+
+def _col(vals, T):
+    return np.asarray(vals, dtype=np.float64).reshape(1, T, 1)
+
+
+# --------------------------------------------------------------------------
+# forward
+# --------------------------------------------------------------------------
+def pin_forward_hand_values(o):
+    """Hand-derived values of small cases, both forms."""
+    for case in GOLDEN["forward"]:
+        T = len(case["k"])
+        w, u = np.array(case["w"]), np.array(case["u"])
+        k, v = _col(case["k"], T), _col(case["v"], T)
+        want = _col(case["y"], T)
+        for fn in (o.forward_direct, o.forward_recurrent):
+            _close(fn(w, u, k, v), want, 1e-13, 1e-13, f"{case['name']}/{fn.__name__}")
+
+
+def pin_forward_forms_agree(o):
+    """The direct sum and the recurrence are two independent formulations."""
+    for seed, kstd in ((1, 1.0), (2, 3.0), (3, 0.1)):
+        w, u, k, v, _ = _rand_inputs(seed, k_std=kstd)
+        yd = o.forward_direct(w, u, k, v)
+        yr = o.forward_recurrent(w, u, k, v)
+        _close(yr, yd, 1e-12, 1e-13, f"direct vs recurrent seed {seed}")
+
+
+def pin_forward_t1_is_v(o):
+    """T = 1: only the current token, wkv_0 = v_0."""
+    w, u, k, v, _ = _rand_inputs(4, T=1, C=7)
+    for fn in (o.forward_direct, o.forward_recurrent):
+        _close(fn(w, u, k, v), v, 1e-15, 0.0, f"T=1 {fn.__name__}")
+
+
+def pin_forward_constant_v(o):
+    """A weighted average of a constant is that constant."""
+    w, u, k, _, _ = _rand_inputs(5)
+    v = np.full(k.shape, -1.75)
+    for fn in (o.forward_direct, o.forward_recurrent):
+        _close(fn(w, u, k, v), v, 1e-14, 0.0, f"constant v {fn.__name__}")
+
+
+def pin_forward_convex(o):
+    """wkv_t lies between min and max of v_0..v_t (weighted average)."""
+    w, u, k, v, _ = _rand_inputs(6, k_std=2.0)
+    for fn in (o.forward_direct, o.forward_recurrent):
+        y = fn(w, u, k, v)
+        lo = np.minimum.accumulate(v, axis=1)
+        hi = np.maximum.accumulate(v, axis=1)
+        assert np.all(y >= lo - 1e-12) and np.all(y <= hi + 1e-12), f"convexity {fn.__name__}"
+
+
+def pin_forward_affine(o):
+    """wkv(alpha v + beta) = alpha wkv(v) + beta (weights do not depend on v)."""
+    w, u, k, v, _ = _rand_inputs(7)
+    for fn in (o.forward_direct, o.forward_recurrent):
+        y = fn(w, u, k, v)
+        _close(fn(w, u, k, -2.5 * v + 0.75), -2.5 * y + 0.75, 1e-12, 1e-12, f"affine {fn.__name__}")
+
+
+def pin_forward_k_shift(o):
+    """Adding one constant to every k of a channel scales all weights alike."""
+    w, u, k, v, _ = _rand_inputs(8, T=24)
+    for fn in (o.forward_direct, o.forward_recurrent):
+        y = fn(w, u, k, v)
+        for s in (-300.0, -40.0, 40.0, 300.0):
+            _close(fn(w, u, k + s, v), y, 1e-11, 1e-12, f"k shift {s} {fn.__name__}")
+
+
+def pin_forward_causal_and_independent(o):
+    """Future tokens do not change the past; channels and rows do not mix."""
+    w, u, k, v, _ = _rand_inputs(9, B=3, T=20, C=6)
+    for fn in (o.forward_direct, o.forward_recurrent):
+        y = fn(w, u, k, v)
+        k2, v2 = k.copy(), v.copy()
+        k2[:, 11:, :] += 5.0
+        v2[:, 11:, :] -= 3.0
+        y2 = fn(w, u, k2, v2)
+        assert np.array_equal(y2[:, :11], y[:, :11]), "causality"
+        pc = _rng(10).permutation(6)
+        pb = _rng(11).permutation(3)
+        yp = fn(w[pc], u[pc], k[pb][:, :, pc], v[pb][:, :, pc])
+        _close(yp, y[pb][:, :, pc], 1e-15, 0.0, "permutation")
+
+
+def pin_forward_limits(o):
+    """Closed forms of limits of w and u."""
+    w, u, k, v, _ = _rand_inputs(12, T=30, C=4)
+    ew = np.exp(k)
+    for fn in (o.forward_direct, o.forward_recurrent):
+        # w = 0: no decay -> a cumulative e^k-weighted mean with the bonus on t
+        zero = np.zeros_like(w)
+        past_n = np.concatenate([np.zeros_like(k[:, :1]), np.cumsum(ew * v, axis=1)[:, :-1]], axis=1)
+        past_d = np.concatenate([np.zeros_like(k[:, :1]), np.cumsum(ew, axis=1)[:, :-1]], axis=1)
+        cur = np.exp(u[None, None, :] + k)
+        _close(fn(zero, u, k, v), (past_n + cur * v) / (past_d + cur), 1e-12, 1e-13, "w=0")
+        # u -> +inf: the current token dominates, wkv_t -> v_t
+        _close(fn(w, np.full_like(u, 60.0), k, v), v, 1e-12, 1e-13, "u=+60")
+        # w -> inf: only token t-1 (undecayed) and token t survive, for t >= 1
+        big = np.full_like(w, 80.0)
+        y = fn(big, u, k, v)
+        e1 = np.exp(k[:, :-1])
+        e2 = np.exp(u[None, None, :] + k[:, 1:])
+        _close(y[:, 1:], (e1 * v[:, :-1] + e2 * v[:, 1:]) / (e1 + e2), 1e-12, 1e-13, "w=80")
+        _close(y[:, 0], v[:, 0], 1e-15, 0.0, "w=80 t=0")
+        # u -> -inf, w = 0, t >= 1: e^k-weighted mean of the past only
+        y = fn(zero, np.full_like(u, -80.0), k, v)
+        for t in (1, 7, 29):
+            want = np.stack([np.average(v[b, :t], axis=0, weights=ew[b, :t]) for b in range(v.shape[0])])
+            _close(y[:, t], want, 1e-12, 1e-13, f"u=-80 w=0 t={t}")
+
+
+# --------------------------------------------------------------------------
+# backward
+# --------------------------------------------------------------------------
+def _loss(o, w, u, k, v, gy):
+    return float(np.sum(gy * o.forward_direct(w, u, k, v)))
+
+
+def pin_backward_hand_values(o):
+    for case in GOLDEN["backward"]:
+        T = len(case["k"])
+        args = (np.array(case["w"]), np.array(case["u"]), _col(case["k"], T), _col(case["v"], T), _col(case["gy"], T))
+        for fn in (o.backward_adjoint, o.backward_direct):
+            gw, gu, gk, gv = fn(*args)
+            _close(gw, case["gw"], 1e-12, 1e-14, f"{case['name']} gw {fn.__name__}")
+            _close(gu, case["gu"], 1e-12, 1e-14, f"{case['name']} gu {fn.__name__}")
+            _close(gk, _col(case["gk"], T), 1e-12, 1e-14, f"{case['name']} gk {fn.__name__}")
+            _close(gv, _col(case["gv"], T), 1e-12, 1e-14, f"{case['name']} gv {fn.__name__}")
+
+
+def pin_backward_finite_differences(o):
+    """Central differences of sum(gy * wkv) in float64 on tiny inputs."""
+    for seed in (20, 21):
+        w, u, k, v, gy = _rand_inputs(seed, B=2, T=6, C=3, k_std=1.5)
+        grads = {fn.__name__: fn(w, u, k, v, gy) for fn in (o.backward_adjoint, o.backward_direct)}
+        fd = {"w": np.zeros_like(w), "u": np.zeros_like(u), "k": np.zeros_like(k), "v": np.zeros_like(v)}
+        params = {"w": w, "u": u, "k": k, "v": v}
+        for name, arr in params.items():
+            it = np.nditer(arr, flags=["multi_index"])
+            for _ in it:
+                idx = it.multi_index
+                h = 1e-6 * max(1.0, abs(arr[idx]))
+                plus = {n: a.copy() for n, a in params.items()}
+                minus = {n: a.copy() for n, a in params.items()}
+                plus[name][idx] += h
+                minus[name][idx] -= h
+                fd[name][idx] = (_loss(o, plus["w"], plus["u"], plus["k"], plus["v"], gy)
+                                 - _loss(o, minus["w"], minus["u"], minus["k"], minus["v"], gy)) / (2 * h)
+        for fname, (gw, gu, gk, gv) in grads.items():
+            for got, want, what in ((gw, fd["w"], "gw"), (gu, fd["u"], "gu"), (gk, fd["k"], "gk"), (gv, fd["v"], "gv")):
+                scale = max(1.0, float(np.max(np.abs(want))))
+                _close(got, want, 0.0, 1e-7 * scale, f"FD {what} {fname} seed {seed}")
+
+
+def pin_backward_forms_agree(o):
+    for seed, kstd in ((30, 1.0), (31, 3.0)):
+        w, u, k, v, gy = _rand_inputs(seed, B=2, T=48, C=4, k_std=kstd)
+        a = o.backward_adjoint(w, u, k, v, gy)
+        d = o.backward_direct(w, u, k, v, gy)
+        for x, y_, n in zip(a, d, ("gw", "gu", "gk", "gv")):
+            scale = float(np.max(np.abs(y_)))
+            _close(x, y_, 0.0, 1e-12 * max(scale, 1.0), f"adjoint vs direct {n} seed {seed}")
+
+
+def pin_backward_identities(o):
+    """Identities that follow from invariances of the forward pass:
+    k-shift invariance => sum_t gk_t = 0 per (b, c); v -> v + beta shifts
+    wkv by beta => sum_t gv_t = sum_t gy_t per (b, c); w never enters for
+    T <= 2 => gw = 0; T = 1 => wkv = v so gv = gy and gk = gu = gw = 0."""
+    w, u, k, v, gy = _rand_inputs(40, B=2, T=33, C=5, k_std=2.0)
+    for fn in (o.backward_adjoint, o.backward_direct):
+        gw, gu, gk, gv = fn(w, u, k, v, gy)
+        _close(gk.sum(axis=1), np.zeros_like(gk[:, 0]), 0.0, 1e-12 * max(1.0, np.abs(gk).max()), "sum gk")
+        _close(gv.sum(axis=1), gy.sum(axis=1), 1e-12, 1e-12, "sum gv")
+        for T in (1, 2):
+            gw2, gu2, gk2, gv2 = fn(w, u, k[:, :T], v[:, :T], gy[:, :T])
+            assert np.all(np.abs(gw2) < 1e-14), f"gw != 0 at T={T}"
+            if T == 1:
+                _close(gv2, gy[:, :1], 1e-15, 0.0, "T=1 gv")
+                assert np.all(np.abs(gk2) < 1e-15) and np.all(np.abs(gu2) < 1e-15), "T=1 gk/gu"
+
+
+# --------------------------------------------------------------------------
+# state and decode
+# --------------------------------------------------------------------------
+def pin_state_definition(o):
+    """state(t) combined with token t through the definition gives wkv_t,
+    and pp is the running maximum max_{i<t}(k_i - (t-1-i) w)."""
+    w, u, k, v, _ = _rand_inputs(50, B=2, T=25, C=3, k_std=2.0)
+    y = o.forward_direct(w, u, k, v)
+    for t in (0, 1, 5, 24):
+        num, den, pp = o.state(w, k, v, t)
+        if t == 0:
+            assert np.all(num == 0) and np.all(den == 0) and np.all(pp == -1e38), "empty state"
+            continue
+        ex = k[:, :t] - (t - 1 - np.arange(t))[None, :, None] * w[None, None, :]
+        _close(pp, ex.max(axis=1), 1e-15, 1e-15, f"pp t={t}")
+        cur = np.exp(u + k[:, t])
+        got = (num * np.exp(pp) + cur * v[:, t]) / (den * np.exp(pp) + cur)
+        _close(got, y[:, t], 1e-12, 1e-13, f"state -> wkv t={t}")
+        assert np.all(den >= 1.0 - 1e-12), "den >= 1 (the max term is exactly 1)"
+
+
+def pin_decode_hand_values(o):
+    for case in GOLDEN["decode"]:
+        for s in case["steps"]:
+            f = lambda x: np.array([[[x]]], dtype=np.float64)  # noqa: E731
+            p = lambda x: np.array([[x]], dtype=np.float64)  # noqa: E731
+            num, den, pp = (f(x) for x in s["state_in"])
+            y, num2, den2, pp2, xk, xv, xr = o.decode_step(
+                f(s["x"]), f(s["x_prev"]), p(s["mu_k"]), p(s["mu_v"]), p(s["mu_r"]), f(s["r"]), f(s["k"]),
+                f(s["v"]), p(s["w"]), p(s["u"]), num, den, pp)
+            _close(y, f(s["y"]), 1e-13, 1e-15, "decode y")
+            _close(np.concatenate([num2, den2, pp2]).ravel(), s["state_out"], 1e-13, 1e-15, "decode state")
+            _close(np.concatenate([xk, xv, xr]).ravel(), [s["xk"], s["xv"], s["xr"]], 1e-15, 0.0, "decode mix")
+
+
+def pin_decode_matches_forward(o):
+    """Running the decode step token by token from the empty state gives
+    sigmoid(r) * wkv of the parallel form, and ends in state(T)."""
+    r_ = _rng(60)
+    L, B, C, T = 2, 3, 4, 17
+    w = np.exp(r_.uniform(-3, 1, (L, C)))
+    u = r_.uniform(-1, 1, (L, C))
+    mu = [r_.uniform(0, 1, (L, C)) for _ in range(3)]
+    k = r_.normal(0, 2, (L, B, T, C))
+    v = r_.normal(0, 1, (L, B, T, C))
+    rr = r_.normal(0, 1, (L, B, T, C))
+    x = r_.normal(0, 1, (L, B, T + 1, C))
+    num = np.zeros((L, B, C))
+    den = np.zeros((L, B, C))
+    pp = np.full((L, B, C), -1e38)
+    ys = []
+    for t in range(T):
+        y, num, den, pp, xk, xv, xr = o.decode_step(x[:, :, t + 1], x[:, :, t], mu[0], mu[1], mu[2], rr[:, :, t],
+                                                    k[:, :, t], v[:, :, t], w, u, num, den, pp)
+        for m, got in zip(mu, (xk, xv, xr)):
+            # mu = 1 keeps the current token, mu = 0 the previous one
+            want = x[:, :, t] + m[:, None, :] * (x[:, :, t + 1] - x[:, :, t])
+            _close(got, want, 1e-14, 1e-14, "mix")
+        ys.append(y)
+    ys = np.stack(ys, axis=2)
+    for l in range(L):
+        yf = o.forward_direct(w[l], u[l], k[l], v[l])
+        _close(ys[l], yf * expit(rr[l]), 1e-12, 1e-13, f"decode vs forward layer {l}")
+        n2, d2, p2 = o.state(w[l], k[l], v[l], T)
+        _close(pp[l], p2, 1e-13, 1e-13, "decode pp vs state")
+        _close(num[l], n2, 1e-12, 1e-13, "decode num vs state")
+        _close(den[l], d2, 1e-12, 1e-13, "decode den vs state")
+
+
+ALL_PINS = [
+    pin_forward_hand_values,
+    pin_forward_forms_agree,
+    pin_forward_t1_is_v,
+    pin_forward_constant_v,
+    pin_forward_convex,
+    pin_forward_affine,
+    pin_forward_k_shift,
+    pin_forward_causal_and_independent,
+    pin_forward_limits,
+    pin_backward_hand_values,
+    pin_backward_finite_differences,
+    pin_backward_forms_agree,
+    pin_backward_identities,
+    pin_state_definition,
+    pin_decode_hand_values,
+    pin_decode_matches_forward,
+]
+
+
+def failing_pins(o):
+    """Names of the pins that fail on oracle handle ``o``."""
+    bad = []
+    for pin in ALL_PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            bad.append(pin.__name__)
+        except (FloatingPointError, ValueError, ZeroDivisionError, OverflowError):
+            bad.append(pin.__name__)
+    return bad
+
