@@ -1,0 +1,622 @@
+#!/usr/bin/env python3
+"""Benchmark of the WKV operator on one or more B300 GPUs (one process per GPU).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  A step is one pass of the training hot path
+over one batch of seeded synthetic input already resident in HBM: the
+forward call (which also writes the chunk checkpoints) followed by the
+backward call (gradients of w, u, k, v), for the named workload (default
+``l169m``: B=8, T=1024, C=768, fp32, one layer of a 169M RWKV-4).  Other
+workloads: ``tiny``, ``l1b5`` (B=16 T=4096 C=2048), ``long`` (forward only,
+bf16 k/v, B=1 T=131072 C=2560) and ``decode`` (one fused decode step of
+L=32 layers, B=256, C=4096, state carried across steps).
+
+Timing: W untimed warm-up steps, then K steps.  L2 is flushed (a write of
+twice its size) before every timed step, outside the step's CUDA-event pair;
+the value is the elements of all ranks over the max over ranks of the summed
+per-step device times.  The dominant kernel's launches are timed with their
+own events on the launching stream for the roofline entry.  SM clocks and
+clock-event reasons are sampled through NVML during the timed steps.
+
+``--impl reference`` times the float64 CPU oracle (oracle/) on this
+machine's host cores instead: each step is a bounded sample of the same
+workload (a subset of channels), so the whole run ends within minutes.
+Under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "WKV fwd+bwd B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
+METRIC_FWD = "WKV forward B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
+METRIC_DEC = "WKV decode step L·B·C elements/s and achieved HBM GB/s fraction on 1 B300"
+
+# Algorithmic HBM bytes per element (what the method must move with the
+# separate forward / backward calls; O(1/chunk) checkpoint and workspace
+# traffic excluded).
+BYTES_FWD_F32 = 12   # read k, v; write y
+BYTES_FWD_BF16 = 8   # read bf16 k, v; write fp32 y
+BYTES_BWD = 20       # read k, v, gy; write gk, gv
+BYTES_DECODE = 60    # read x, x_prev, r, k, v; read+write num, den, pp; write y, xk, xv, xr
+
+REJECT_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default depends on the workload)")
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="l169m", choices=["tiny", "l169m", "l1b5", "long", "decode"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return args
+
+
+DEFAULT_STEPS = {"tiny": 2000, "l169m": 4000, "l1b5": 200, "long": 200, "decode": 256}
+
+
+# ------------------------------------------------------------------ ranks
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Max over ranks of a float (host value; torch.distributed for N > 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def aggregate(per_rank_seconds: float, units_per_rank: float, world: int, device=None):
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    t = reduce_max(per_rank_seconds, world, device)
+    return world * units_per_rank / t, t
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read only)."""
+
+    NAMES = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+        0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+        0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+    }
+
+    def __init__(self, index: int, period_s: float = 0.02):
+        self.period = period_s
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            import pynvml
+
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # NVML missing: report that instead of clocks
+            self.nv = None
+            self.error = str(e)
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for bit, name in self.NAMES.items():
+                    if mask & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            self._stop.wait(self.period)
+
+    def __enter__(self):
+        if self.nv is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+
+    def summary(self):
+        if self.nv is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.error}
+        med = statistics.median(self.samples) if self.samples else None
+        reasons = sorted(self.reasons - {"gpu_idle"})
+        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples)}
+
+    def rejected(self) -> bool:
+        s = self.summary()
+        if any(r in s["reasons"] for r in REJECT_REASONS):
+            return True
+        # clocks stuck well below max with no reason: a leftover clock lock
+        return bool(s["sm_mhz"] and s["sm_max_mhz"] and s["sm_mhz"] < 0.6 * s["sm_max_mhz"] and not s["reasons"])
+
+
+# ---------------------------------------------------------------- helpers
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = ROOT / "rwkv_linear_attention_backward_b300" / "csrc"
+    for p in sorted(csrc.glob("*")):
+        h.update(p.name.encode())
+        h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    f = ROOT / "profiles" / "ncu_traffic.json"
+    if not f.exists():
+        return None
+    try:
+        rec = json.loads(f.read_text()).get(f"{kernel}@{workload}")
+    except ValueError:
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+# ------------------------------------------------------------- ours: setup
+class TrainingRun:
+    def __init__(self, name: str, device):
+        import torch
+        from rwkv_linear_attention_backward_b300 import binding, inputs
+
+        self.torch, self.wkv = torch, binding
+        self.wl = inputs.WORKLOADS[name]
+        wl = self.wl
+        self.host = inputs.workload_inputs(name)  # (w, u, k, v, gy) on the CPU
+        self.dev = tuple(t.to(device).contiguous() for t in self.host)
+        B, T, C = wl.B, wl.T, wl.C
+        self.elements = wl.elements
+        self.y = torch.empty(B, T, C, device=device)
+        self.ckpt = torch.empty(binding.checkpoint_floats(B, T, C), device=device)
+        self.gw = torch.empty(C, device=device)
+        self.gu = torch.empty(C, device=device)
+        self.gk = torch.empty(B, T, C, device=device)
+        self.gv = torch.empty(B, T, C, device=device)
+        self.ws_f = binding.Workspace(binding.forward_workspace_bytes(B, T, C), device)
+        self.ws_b = binding.Workspace(binding.backward_workspace_bytes(B, T, C), device)
+        kv_bytes = BYTES_FWD_BF16 if wl.kv_dtype == "bf16" else BYTES_FWD_F32
+        self.bytes_fwd = kv_bytes * self.elements
+        self.bytes_bwd = BYTES_BWD * self.elements if wl.backward else 0
+        self.launches_per_step = 1 + (2 if wl.backward else 0)
+        self.dominant = "bwd_scan_kernel" if wl.backward else "fwd_scan_kernel"
+        self.dominant_bytes = self.bytes_bwd if wl.backward else self.bytes_fwd
+
+    def step(self, ev=None):
+        w, u, k, v, gy = self.dev
+        self.wkv.forward(w, u, k, v, y=self.y, ckpt=self.ckpt, workspace=self.ws_f)
+        if self.wl.backward:
+            if ev is not None:
+                ev[0].record()
+            self.wkv.backward(w, u, k, v, gy, ckpt=self.ckpt, gw=self.gw, gu=self.gu, gk=self.gk, gv=self.gv,
+                              workspace=self.ws_b)
+            if ev is not None:
+                ev[1].record()
+
+    def step_dominant_events(self, ev):
+        """A step with the dominant call bracketed by the events `ev`."""
+        w, u, k, v, gy = self.dev
+        if self.wl.backward:
+            self.step(ev)
+        else:
+            ev[0].record()
+            self.wkv.forward(w, u, k, v, y=self.y, ckpt=self.ckpt, workspace=self.ws_f)
+            ev[1].record()
+
+    def check(self):
+        self.wkv.workspace_check(self.ws_f)
+        self.wkv.workspace_check(self.ws_b)
+
+    # end to end through the public API with host buffers
+    def e2e_setup(self):
+        torch = self.torch
+        self.pin_in = tuple(t.pin_memory() for t in self.host)
+        self.pin_out = tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                             for t in ([self.y] + ([self.gk, self.gv, self.gw, self.gu] if self.wl.backward else [])))
+        self.h2d = sum(t.numel() * t.element_size() for t in self.pin_in)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out)
+
+    def e2e_step(self):
+        for d, h in zip(self.dev, self.pin_in):
+            d.copy_(h, non_blocking=True)
+        self.step()
+        outs = [self.y] + ([self.gk, self.gv, self.gw, self.gu] if self.wl.backward else [])
+        for h, d in zip(self.pin_out, outs):
+            h.copy_(d, non_blocking=True)
+
+
+class DecodeRun:
+    def __init__(self, device):
+        import torch
+        from rwkv_linear_attention_backward_b300 import binding, inputs
+
+        self.torch, self.wkv = torch, binding
+        D = inputs.DECODE
+        self.D = D
+        L, B, C = D.L, D.B, D.C
+        self.elements = D.elements_per_step
+        self.params = tuple(t.to(device) for t in inputs.decode_params(L, C, seed=D.seed, d_lo=D.d_lo, d_hi=D.d_hi))
+        self.pool = inputs.decode_pool(L, B, C, seed=D.seed, n_sets=16, device=device)
+        self.state = tuple(t.to(device) for t in inputs.initial_state(L, B, C))
+        self.out = tuple(torch.empty(L, B, C, device=device) for _ in range(4))
+        self.t = 0
+        self.bytes_fwd = BYTES_DECODE * self.elements
+        self.bytes_bwd = 0
+        self.launches_per_step = 1
+        self.dominant = "decode_kernel_vec4"
+        self.dominant_bytes = self.bytes_fwd
+
+    def step(self, ev=None):
+        x, xp, r, k, v = self.pool[self.t % len(self.pool)]
+        mk, mv, mr, w, u = self.params
+        y, xk, xv, xr = self.out
+        if ev is not None:
+            ev[0].record()
+        self.wkv.decode_step(x, xp, mk, mv, mr, r, k, v, w, u, *self.state, y=y, xk=xk, xv=xv, xr=xr)
+        if ev is not None:
+            ev[1].record()
+        self.t += 1
+
+    step_dominant_events = step
+
+    def check(self):
+        pass
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.pin_in = tuple(t.to("cpu").pin_memory() for t in self.pool[0])
+        self.pin_out = (torch.empty(self.out[0].shape, pin_memory=True),)
+        self.h2d = sum(t.numel() * t.element_size() for t in self.pin_in)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out)
+
+    def e2e_step(self):
+        bufs = self.pool[0]
+        for d, h in zip(bufs, self.pin_in):
+            d.copy_(h, non_blocking=True)
+        x, xp, r, k, v = bufs
+        mk, mv, mr, w, u = self.params
+        y, xk, xv, xr = self.out
+        self.wkv.decode_step(x, xp, mk, mv, mr, r, k, v, w, u, *self.state, y=y, xk=xk, xv=xv, xr=xr)
+        self.pin_out[0].copy_(y, non_blocking=True)
+
+
+# --------------------------------------------------------------- ours: run
+def time_steps(run, steps: int, flush, stream):
+    """Per-step device times (s) of `steps` steps, L2 flushed before each;
+    also the dominant call's per-launch times."""
+    torch = run.torch
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev_dom = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        ev_step[i][0].record(stream)
+        run.step_dominant_events(ev_dom[i])
+        ev_step[i][1].record(stream)
+    torch.cuda.synchronize()
+    step_s = [a.elapsed_time(b) / 1e3 for a, b in ev_step]
+    dom_s = [a.elapsed_time(b) / 1e3 for a, b in ev_dom]
+    return step_s, dom_s
+
+
+def cpu_baseline(workload: str, target_s: float = 12.0):
+    """Time the float64 oracle (recurrent forward + adjoint backward, or the
+    decode step) on this host's cores on a bounded sample of the workload:
+    a subset of channels (decode: of batch rows), grown until about
+    target_s of CPU work."""
+    import numpy as np
+
+    import oracle
+    from rwkv_linear_attention_backward_b300 import inputs
+
+    o = oracle.load()
+    if workload == "decode":
+        D = inputs.DECODE
+        L, B, C = D.L, D.B, D.C
+        params = [p.numpy() for p in inputs.decode_params(L, C, seed=D.seed, d_lo=D.d_lo, d_hi=D.d_hi)]
+        rows = 16
+        x, xp, r, k, v = (t.numpy()[:, :rows] for t in inputs.decode_step_inputs(L, B, C, seed=D.seed, step=0))
+        st = [t.numpy()[:, :rows] for t in inputs.initial_state(L, B, C)]
+        done, t0, steps = 0, time.perf_counter(), 0
+        while time.perf_counter() - t0 < target_s:
+            y, *st, _, _, _ = o.decode_step(x, xp, *params[:3], r, k, v, *params[3:], *st)
+            done += L * rows * C
+            steps += 1
+        el = time.perf_counter() - t0
+        return {"value": done / el, "unit": "elements/s", "cores": o.num_threads(), "kind": "oracle",
+                "sample": f"decode step on batch rows 0..{rows - 1} of {B} (all {L} layers, all {C} channels), "
+                          f"{steps} steps in {el:.1f} s"}
+    wl = inputs.WORKLOADS[workload]
+    w, u, k, v, gy = inputs.workload_inputs(workload)
+    C = wl.C
+    nchan = C
+    # calibrate on a few channels, then size the sample for ~target_s
+    cs = np.arange(min(8, C))
+    t0 = time.perf_counter()
+    _oracle_pass(o, wl, w, u, k, v, gy, cs)
+    per_chan = (time.perf_counter() - t0) / len(cs)
+    nchan = int(max(1, min(C, target_s / max(per_chan, 1e-9) / 2)))
+    cs = np.linspace(0, C - 1, nchan).astype(int)
+    reps, done, t0 = 0, 0, time.perf_counter()
+    while True:
+        _oracle_pass(o, wl, w, u, k, v, gy, cs)
+        reps += 1
+        done += wl.B * wl.T * len(cs)
+        if time.perf_counter() - t0 >= target_s or reps >= 50:
+            break
+    el = time.perf_counter() - t0
+    what = "recurrent forward + adjoint backward" if wl.backward else "recurrent forward"
+    return {"value": done / el, "unit": "elements/s", "cores": o.num_threads(), "kind": "oracle",
+            "sample": f"{what} on {len(cs)} of {C} channels (all B={wl.B}, T={wl.T}), {reps} pass(es) in {el:.1f} s"}
+
+
+def _oracle_pass(o, wl, w, u, k, v, gy, cs):
+    ks, vs = k[:, :, cs], v[:, :, cs]
+    o.forward_recurrent(w[cs], u[cs], ks, vs)
+    if wl.backward:
+        o.backward_adjoint(w[cs], u[cs], ks, vs, gy[:, :, cs])
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    from rwkv_linear_attention_backward_b300 import build
+
+    build.build()
+    steps = args.steps or DEFAULT_STEPS[args.workload]
+    run = DecodeRun(device) if args.workload == "decode" else TrainingRun(args.workload, device)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    scratch = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+    flush = lambda: scratch.fill_(1.0)  # noqa: E731  (a write larger than L2)
+
+    for _ in range(args.warmup):
+        flush()
+        run.step()
+    torch.cuda.synchronize()
+    run.check()
+
+    attempts = []
+    for attempt in range(2):
+        barrier(world)
+        torch.cuda.synchronize()
+        with ClockSampler(device.index) as clocks:
+            step_s, dom_s = time_steps(run, steps, flush, stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        attempts.append((step_s, dom_s, clocks))
+        if not clocks.rejected():
+            break
+    step_s, dom_s, clocks = attempts[-1]
+    run.check()
+
+    total = sum(step_s)
+    value, tmax = aggregate(total, run.elements * steps, world, device)
+    ms_per_step = 1e3 * tmax / steps
+    peak, peak_kind = peaks()
+    dom_avg = sum(dom_s) / len(dom_s)
+    achieved = run.dominant_bytes / dom_avg / 1e9
+    step_bytes = run.bytes_fwd + run.bytes_bwd
+    wl_cfg = ({"workload": "decode", "L": run.D.L, "B": run.D.B, "C": run.D.C, "state": "fp32"}
+              if args.workload == "decode" else
+              {"workload": args.workload, "B": run.wl.B, "T": run.wl.T, "C": run.wl.C, "kv_dtype": run.wl.kv_dtype,
+               "pass": "forward+backward" if run.wl.backward else "forward"})
+    wl_cfg.update({"l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}",
+                   "checkpoints": "forward writes chunk checkpoints, backward reads them"
+                   if args.workload != "decode" else "n/a"})
+    out = {
+        "metric": METRIC if args.workload not in ("long", "decode") else (METRIC_FWD if args.workload == "long"
+                                                                           else METRIC_DEC),
+        "value": value,
+        "unit": "elements/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; see rwkv_linear_attention_backward_b300/inputs.py)",
+        "config": wl_cfg,
+        "achieved_hbm_gbs": step_bytes * steps / total / 1e9,
+        "hbm_frac": step_bytes * steps / total / 1e9 / peak,
+        "roofline": {
+            "kernel": run.dominant,
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": ncu_traffic(run.dominant, args.workload),
+            "algorithmic_bytes_per_launch": run.dominant_bytes,
+            "launch_ms": dom_avg * 1e3,
+        },
+        "gpu_launches": run.launches_per_step * steps,
+        "clocks": clocks.summary(),
+    }
+    if len(attempts) > 1:
+        out["clocks"]["remeasured"] = True
+    if world == 1 and not args.no_e2e:
+        out["e2e"] = e2e(run, steps=max(3, min(steps, 50)))
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.workload)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def e2e(run, steps: int):
+    """Same metric through the public API with pinned host buffers: every
+    step copies its inputs host->device, runs the step, copies the results
+    device->host."""
+    torch = run.torch
+    run.e2e_setup()
+    for _ in range(2):
+        run.e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        run.e2e_step()
+    b.record()
+    torch.cuda.synchronize()
+    dt = a.elapsed_time(b) / 1e3
+    return {"value": run.elements * steps / dt, "unit": "elements/s", "h2d_bytes_per_step": run.h2d,
+            "d2h_bytes_per_step": run.d2h, "steps": steps}
+
+
+# -------------------------------------------------------------- reference
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from rwkv_linear_attention_backward_b300 import inputs
+
+    steps = args.steps or DEFAULT_STEPS[args.workload]
+    total_budget = 120.0  # seconds for warm-up + timed steps together
+    per_step = total_budget / (steps + args.warmup)
+    o = oracle.load()
+    if args.workload == "decode":
+        D = inputs.DECODE
+        L, B, C = D.L, D.B, D.C
+        params = [p.numpy() for p in inputs.decode_params(L, C, seed=D.seed, d_lo=D.d_lo, d_hi=D.d_hi)]
+        x, xp, r, k, v = (t.numpy() for t in inputs.decode_step_inputs(L, B, C, seed=D.seed, step=0))
+        t0 = time.perf_counter()
+        o.decode_step(x[:, :1], xp[:, :1], *params[:3], r[:, :1], k[:, :1], v[:, :1], *params[3:],
+                      *[t.numpy()[:, :1] for t in inputs.initial_state(L, 1, C)])
+        per_row = time.perf_counter() - t0
+        rows = int(max(1, min(B, per_step / max(per_row, 1e-9))))
+        st = [t.numpy()[:, :rows] for t in inputs.initial_state(L, B, C)]
+
+        def one():
+            nonlocal st
+            y, *st, _, _, _ = o.decode_step(x[:, :rows], xp[:, :rows], *params[:3], r[:, :rows], k[:, :rows],
+                                            v[:, :rows], *params[3:], *st)
+            return L * rows * C
+
+        sample = f"decode step on batch rows 0..{rows - 1} of {B} (all {L} layers, {C} channels)"
+        metric = METRIC_DEC
+    else:
+        wl = inputs.WORKLOADS[args.workload]
+        w, u, k, v, gy = inputs.workload_inputs(args.workload)
+        cs = np.arange(min(4, wl.C))
+        t0 = time.perf_counter()
+        _oracle_pass(o, wl, w, u, k, v, gy, cs)
+        per_chan = (time.perf_counter() - t0) / len(cs)
+        nchan = int(max(1, min(wl.C, per_step / max(per_chan, 1e-9))))
+        cs = np.linspace(0, wl.C - 1, nchan).astype(int)
+
+        def one():
+            _oracle_pass(o, wl, w, u, k, v, gy, cs)
+            return wl.B * wl.T * len(cs)
+
+        what = "recurrent forward + adjoint backward" if wl.backward else "recurrent forward"
+        sample = f"{what} on {len(cs)} of {wl.C} channels (all B={wl.B}, T={wl.T})"
+        metric = METRIC if wl.backward else METRIC_FWD
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    done = sum(one() for _ in range(steps))
+    el = time.perf_counter() - t0
+    value = done / el
+    cfg = ({"workload": args.workload} if args.workload == "decode" else
+           {"workload": args.workload, "B": inputs.WORKLOADS[args.workload].B,
+            "T": inputs.WORKLOADS[args.workload].T, "C": inputs.WORKLOADS[args.workload].C})
+    out = {
+        "impl": "reference",
+        "metric": metric,
+        "value": value,
+        "unit": "elements/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded; see rwkv_linear_attention_backward_b300/inputs.py)",
+        "config": cfg,
+        "cpu_baseline": {"value": value, "unit": "elements/s", "cores": o.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

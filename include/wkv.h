@@ -1,0 +1,180 @@
+/*
+ * wkv.h -- C ABI of libwkv.so, the B300 (sm_103a) WKV operator of RWKV.
+ *
+ * The operator is the time-mixing "attention" of RWKV.  Sources, by page
+ * title and section:
+ *   "RWKV解读：在Transformer的时代的新RNN" (segmentfault), section
+ *     "3、RWKV的网络架构": eq. (7) token shift, eq. (8) wkv and its
+ *     recursive form, eq. (9) the sigmoid(r) gate;
+ *   "RWKV についての調査記録" (qiita), section "wkvとは": a weighted average of
+ *     v with weights from k, a bonus u for the current token, a decay growing
+ *     with distance through one channel-wise vector w, channels independent;
+ *     section "Trainingについて": gradients for every parameter, and time
+ *     parallel training because the decay is data independent; section
+ *     "RWKVとは？": in inference a token and a state go in, an output and a
+ *     new state come out.
+ * The pages lost every equation body; the exact form implemented is, per
+ * batch row b and channel c, t in [0, T):
+ *
+ *   wkv_t = ( sum_{i<t} e^{-(t-1-i) w_c + k_i} v_i  +  e^{u_c + k_t} v_t )
+ *         / ( sum_{i<t} e^{-(t-1-i) w_c + k_i}      +  e^{u_c + k_t}     )
+ *
+ * with decay w_c > 0 (passed directly; a caller holding w = exp(d) applies
+ * gd = gw * w itself) and bonus u_c.
+ *
+ * Conventions for every entry point
+ *   - Tensor arguments are DEVICE pointers owned by the caller (no host
+ *     pointers).  The library allocates nothing and keeps no per-call state;
+ *     all scratch lives in the caller's workspace.
+ *   - k, v, y, gy, gk, gv are [B, T, C] row-major, C fastest.  w, u, gw, gu
+ *     are [C].  Decode tensors are [L, B, C]; decode parameters [L, C].
+ *   - stream is a cudaStream_t cast to void*; NULL is the legacy default
+ *     stream.  Calls are asynchronous on that stream: a return of WKV_OK means
+ *     the work was enqueued.
+ *   - Invalid arguments are rejected on the host before anything is
+ *     launched; outputs are then untouched.
+ *   - Values must be finite and w >= 0; otherwise results are undefined
+ *     (no device-side value checks).  Outputs must not alias inputs, except
+ *     the decode state, which is updated in place.
+ *   - Any element alignment is accepted; 16-byte aligned decode tensors with
+ *     C % 4 == 0 take a vectorised path.
+ *   - Results are bitwise reproducible for the same inputs and shapes (no
+ *     floating-point atomics; gw, gu are reduced in a fixed order).
+ */
+#ifndef WKV_H_
+#define WKV_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WKV_OK = 0,
+  WKV_ERR_INVALID_ARG = 1, /* a size <= 0, a null required pointer, an unknown dtype */
+  WKV_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement */
+  WKV_ERR_MISALIGNED = 3,  /* reserved */
+  WKV_ERR_WORKSPACE = 4,   /* workspace null or smaller than the *_workspace_bytes query */
+  WKV_ERR_CUDA = 5,        /* a CUDA call failed; see wkv_last_error_string() */
+  WKV_ERR_TIMEOUT = 6      /* a bounded device-side wait expired (see wkv_workspace_check) */
+} wkv_status;
+
+typedef enum { WKV_F32 = 0, WKV_BF16 = 1 } wkv_dtype;
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* wkv_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread in a wkv_* call ("" if
+ * none).  Valid until the next wkv_* call on the same thread. */
+const char* wkv_last_error_string(void);
+
+/* ABI version, currently 1. */
+int wkv_version(void);
+
+/* Length in tokens of the time chunks of the chunked scans (the same for
+ * every shape).  The checkpoint array of wkv_forward / wkv_backward holds
+ * one state per chunk. */
+int wkv_chunk_len(void);
+
+/* Number of floats of a checkpoint array for shape (B, T, C):
+ * 3 * ceil(T / wkv_chunk_len()) * B * C.  Layout [3][nchunks][B][C]: planes
+ * num, den, pp of the state after each chunk (chunk j covers tokens
+ * [j*Lc, min((j+1)*Lc, T)) ), so plane entry j is the state after token
+ * min((j+1)*Lc, T) - 1, in the (num, den, pp) convention of
+ * wkv_decode_step.  Returns 0 for invalid sizes. */
+size_t wkv_checkpoint_floats(int B, int T, int C);
+
+/* Workspace sizes in bytes (0 for invalid sizes).  A workspace must be
+ * zero-filled before its first use (wkv_workspace_init, or any zeroing);
+ * every call leaves it ready for the next one.  One workspace may be reused
+ * by any number of calls in stream order, but not by two calls that run
+ * concurrently. */
+size_t wkv_forward_workspace_bytes(int B, int T, int C);
+size_t wkv_backward_workspace_bytes(int B, int T, int C);
+
+/* Zero-fills `bytes` bytes of `workspace` on `stream`. */
+wkv_status wkv_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* Synchronises `stream`, then reports whether a kernel that used this
+ * workspace since the last check gave up a bounded wait (WKV_ERR_TIMEOUT;
+ * its outputs are then invalid) and clears that record.  WKV_OK otherwise. */
+wkv_status wkv_workspace_check(void* workspace, void* stream);
+
+/*
+ * wkv_forward -- the training (time-parallel) form: y[b,t,c] = wkv_t for all
+ * t at once, by a single-pass chunked scan over T (chunk summaries combined
+ * through a bounded decoupled look-back), so k and v are read once.
+ *   kv_dtype  WKV_F32 (k, v are float) or WKV_BF16 (k, v are bf16); w, u, y
+ *             are float in both cases and all arithmetic is fp32.
+ *   ckpt      optional output (may be NULL): wkv_checkpoint_floats(B,T,C)
+ *             floats receiving the state after each chunk.  Passing it to
+ *             wkv_backward with the same w, k, v saves that call a pass over
+ *             k and v.  The last entry is the state after the whole sequence.
+ *   workspace at least wkv_forward_workspace_bytes(B, T, C) bytes.
+ * Errors: WKV_ERR_INVALID_ARG (B, T or C <= 0, B*T*C >= 2^40, null w, u, k,
+ * v or y, unknown kv_dtype), WKV_ERR_WORKSPACE, WKV_ERR_CUDA.
+ */
+wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                       const void* v, float* y, float* ckpt, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/*
+ * wkv_backward -- gradients of sum(gy * wkv) with respect to w, u, k, v.
+ *   gy          upstream gradient [B, T, C], float.
+ *   ckpt        optional (may be NULL): the checkpoint array written by
+ *               wkv_forward for the same w, k, v.  When NULL the call first
+ *               recomputes it (one extra pass over k and v).
+ *   gw, gu      [C] outputs, summed over b and t (overwritten, not
+ *               accumulated).  gk, gv [B, T, C] outputs.
+ *   workspace   at least wkv_backward_workspace_bytes(B, T, C) bytes.
+ * The reverse-time adjoint recurrence is scanned in chunks from the last
+ * chunk backwards; the forward states are recomputed per chunk from the
+ * checkpoints.  Errors: as wkv_forward; kv_dtype must be WKV_F32
+ * (WKV_ERR_UNSUPPORTED otherwise).
+ */
+wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                        const void* v, const float* gy, const float* ckpt, float* gw, float* gu, float* gk,
+                        float* gv, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * wkv_decode_step -- one RNN-mode step of L independent time-mixing layers,
+ * fused: token shift (eq. 7) -> wkv from the carried state -> sigmoid(r)
+ * gate (eq. 9) -> state update.  Per (l, b, c), with parameters at (l, c):
+ *   xk = mu_k x + (1 - mu_k) x_prev   (xv with mu_v, xr with mu_r)
+ *   wkv = (num e^{pp} + e^{u+k} v) / (den e^{pp} + e^{u+k})
+ *   y = wkv / (1 + e^{-r})
+ *   state <- state after token (k, v): a' = e^{-w} a + e^{k} v,
+ *            b' = e^{-w} b + e^{k}, pp' = max(pp - w, k)
+ * The empty state (no token yet) is num = den = 0, pp = -1e38.  The mix
+ * outputs feed the caller's R, K, V projections for the next step; r, k, v
+ * here are that step's projected inputs.
+ *   x, x_prev, r, k, v         [L, B, C] inputs
+ *   mu_k, mu_v, mu_r, w, u     [L, C] inputs
+ *   num, den, pp               [L, B, C] state, read and updated in place
+ *   y                          [L, B, C] output (required)
+ *   xk, xv, xr                 [L, B, C] outputs, each may be NULL
+ * Errors: WKV_ERR_INVALID_ARG (L, B or C <= 0, a required pointer NULL),
+ * WKV_ERR_CUDA.
+ */
+wkv_status wkv_decode_step(int L, int B, int C, const float* x, const float* x_prev, const float* mu_k,
+                           const float* mu_v, const float* mu_r, const float* r, const float* k, const float* v,
+                           const float* w, const float* u, float* num, float* den, float* pp, float* y, float* xk,
+                           float* xv, float* xr, void* stream);
+
+/*
+ * Test hooks (process-wide; not for production use).
+ * wkv_debug_set_wait_budget_ns: limit of each bounded device-side wait of
+ *   the scans, in ns of %globaltimer; <= 0 restores the default (500 ms).
+ * wkv_debug_set_skip_chunk: tiles of time chunk `chunk` skip publishing
+ *   their results, so the waits of later tiles expire and the call reports
+ *   WKV_ERR_TIMEOUT through wkv_workspace_check; -1 turns this off.
+ */
+wkv_status wkv_debug_set_wait_budget_ns(long long ns);
+wkv_status wkv_debug_set_skip_chunk(int chunk);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WKV_H_ */

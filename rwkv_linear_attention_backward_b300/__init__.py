@@ -7,16 +7,12 @@ tensors; importing it loads the library and raises if it is missing.  The
 """
 from __future__ import annotations
 
-__all__ = ["binding", "inputs"]
+import importlib
+
+__all__ = ["binding", "inputs", "build"]
 
 
 def __getattr__(name):
-    if name == "binding":
-        from . import binding as _b
-
-        return _b
-    if name == "inputs":
-        from . import inputs as _i
-
-        return _i
+    if name in __all__:
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

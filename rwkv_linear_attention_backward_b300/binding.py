@@ -1,0 +1,259 @@
+"""Thin Python binding of libwkv.so (the C ABI in include/wkv.h) for torch tensors.
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  torch provides device memory and streams.  Importing
+this module loads ``libwkv.so`` from this package directory and raises
+``ImportError`` if it is missing (build it with
+``python -m rwkv_linear_attention_backward_b300.build``); there is no
+fallback implementation.
+
+Entry points mirror the ABI names: ``forward``, ``backward``,
+``decode_step``, ``workspace_check``, plus size queries.  All tensors must be
+contiguous CUDA tensors on the current device; calls are enqueued on the
+current torch stream (or ``stream=``) and return without synchronising.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+LIBRARY = Path(__file__).resolve().parent / "libwkv.so"
+
+if not LIBRARY.exists():
+    raise ImportError(f"{LIBRARY} is missing: build it with `python -m rwkv_linear_attention_backward_b300.build`")
+
+_lib = ctypes.CDLL(str(LIBRARY))
+
+_vp, _i, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
+
+_SIGNATURES = {
+    "wkv_status_string": ([_i], ctypes.c_char_p),
+    "wkv_last_error_string": ([], ctypes.c_char_p),
+    "wkv_version": ([], _i),
+    "wkv_chunk_len": ([], _i),
+    "wkv_checkpoint_floats": ([_i, _i, _i], _sz),
+    "wkv_forward_workspace_bytes": ([_i, _i, _i], _sz),
+    "wkv_backward_workspace_bytes": ([_i, _i, _i], _sz),
+    "wkv_workspace_init": ([_vp, _sz, _vp], _i),
+    "wkv_workspace_check": ([_vp, _vp], _i),
+    "wkv_forward": ([_i, _i, _i, _i] + [_vp] * 6 + [_vp, _sz, _vp], _i),
+    "wkv_backward": ([_i, _i, _i, _i] + [_vp] * 10 + [_vp, _sz, _vp], _i),
+    "wkv_decode_step": ([_i, _i, _i] + [_vp] * 17 + [_vp], _i),
+    "wkv_debug_set_wait_budget_ns": ([_ll], _i),
+    "wkv_debug_set_skip_chunk": ([_i], _i),
+}
+for _name, (_args, _res) in _SIGNATURES.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+WKV_OK, WKV_F32, WKV_BF16 = 0, 0, 1
+EXPORTED = tuple(_SIGNATURES)
+
+
+class WKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.wkv_status_string(status).decode()
+        detail = _lib.wkv_last_error_string().decode()
+        super().__init__(f"{where}: {msg}" + (f" ({detail})" if detail else ""))
+
+
+def _check(status: int, where: str) -> None:
+    if status != WKV_OK:
+        raise WKVError(status, where)
+
+
+def _p(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtypes=(torch.float32,), shape=None) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+# ----------------------------------------------------------------- queries
+def version() -> int:
+    return int(_lib.wkv_version())
+
+
+def chunk_len() -> int:
+    return int(_lib.wkv_chunk_len())
+
+
+def checkpoint_floats(B: int, T: int, C: int) -> int:
+    return int(_lib.wkv_checkpoint_floats(B, T, C))
+
+
+def forward_workspace_bytes(B: int, T: int, C: int) -> int:
+    return int(_lib.wkv_forward_workspace_bytes(B, T, C))
+
+
+def backward_workspace_bytes(B: int, T: int, C: int) -> int:
+    return int(_lib.wkv_backward_workspace_bytes(B, T, C))
+
+
+# -------------------------------------------------------------- workspace
+class Workspace:
+    """A zero-filled device buffer reused across calls in stream order."""
+
+    def __init__(self, nbytes: int, device=None):
+        self.tensor = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+    @property
+    def nbytes(self) -> int:
+        return self.tensor.numel()
+
+    def ptr(self):
+        return ctypes.c_void_p(self.tensor.data_ptr())
+
+
+_WS_CACHE: dict = {}
+
+
+def _workspace(kind: str, nbytes: int, device: torch.device) -> Workspace:
+    key = (kind, device.index)
+    ws = _WS_CACHE.get(key)
+    if ws is None or ws.nbytes < nbytes:
+        ws = Workspace(nbytes, device)
+        _WS_CACHE[key] = ws
+    return ws
+
+
+def workspace_check(ws: Workspace, stream=None) -> None:
+    """Synchronise and raise WKVError if a bounded device wait expired."""
+    _check(_lib.wkv_workspace_check(ws.ptr(), _stream(stream)), "wkv_workspace_check")
+
+
+# ---------------------------------------------------------------- forward
+def forward(w, u, k, v, *, y=None, ckpt=None, want_ckpt: bool = False, workspace: Workspace | None = None,
+            stream=None):
+    """wkv for all t of k, v [B, T, C] (fp32 or bf16); w, u [C] fp32.
+
+    Returns ``y`` (fp32 [B, T, C]), or ``(y, ckpt)`` when ``want_ckpt`` or a
+    ``ckpt`` buffer is given (the chunk-boundary states for ``backward``).
+    """
+    if k.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("k must be float32 or bfloat16")
+    B, T, C = k.shape
+    _need(k, "k", (k.dtype,))
+    _need(v, "v", (k.dtype,), k.shape)
+    _need(w, "w", shape=(C,))
+    _need(u, "u", shape=(C,))
+    if y is None:
+        y = torch.empty((B, T, C), dtype=torch.float32, device=k.device)
+    _need(y, "y", shape=(B, T, C))
+    if ckpt is None and want_ckpt:
+        ckpt = torch.empty(checkpoint_floats(B, T, C), dtype=torch.float32, device=k.device)
+    if ckpt is not None:
+        _need(ckpt, "ckpt")
+        if ckpt.numel() < checkpoint_floats(B, T, C):
+            raise ValueError("ckpt is too small")
+    need = forward_workspace_bytes(B, T, C)
+    ws = workspace or _workspace("fwd", need, k.device)
+    dt = WKV_BF16 if k.dtype == torch.bfloat16 else WKV_F32
+    _check(_lib.wkv_forward(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(y), _p(ckpt), ws.ptr(), ws.nbytes,
+                            _stream(stream)), "wkv_forward")
+    return (y, ckpt) if ckpt is not None else y
+
+
+# --------------------------------------------------------------- backward
+def backward(w, u, k, v, gy, *, ckpt=None, gw=None, gu=None, gk=None, gv=None, workspace: Workspace | None = None,
+             stream=None):
+    """Gradients (gw, gu, gk, gv) of sum(gy * wkv); fp32 inputs."""
+    B, T, C = k.shape
+    _need(k, "k")
+    _need(v, "v", shape=k.shape)
+    _need(gy, "gy", shape=k.shape)
+    _need(w, "w", shape=(C,))
+    _need(u, "u", shape=(C,))
+    if ckpt is not None:
+        _need(ckpt, "ckpt")
+        if ckpt.numel() < checkpoint_floats(B, T, C):
+            raise ValueError("ckpt is too small")
+    dev = k.device
+    gw = torch.empty(C, dtype=torch.float32, device=dev) if gw is None else gw
+    gu = torch.empty(C, dtype=torch.float32, device=dev) if gu is None else gu
+    gk = torch.empty((B, T, C), dtype=torch.float32, device=dev) if gk is None else gk
+    gv = torch.empty((B, T, C), dtype=torch.float32, device=dev) if gv is None else gv
+    for t, n, s in ((gw, "gw", (C,)), (gu, "gu", (C,)), (gk, "gk", (B, T, C)), (gv, "gv", (B, T, C))):
+        _need(t, n, shape=s)
+    need = backward_workspace_bytes(B, T, C)
+    ws = workspace or _workspace("bwd", need, dev)
+    _check(_lib.wkv_backward(B, T, C, WKV_F32, _p(w), _p(u), _p(k), _p(v), _p(gy), _p(ckpt), _p(gw), _p(gu),
+                             _p(gk), _p(gv), ws.ptr(), ws.nbytes, _stream(stream)), "wkv_backward")
+    return gw, gu, gk, gv
+
+
+# ----------------------------------------------------------------- decode
+def decode_step(x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u, num, den, pp, *, y=None, xk=None, xv=None, xr=None,
+                mix: bool = True, stream=None):
+    """One fused RNN-mode step of L layers; num, den, pp [L, B, C] update in place.
+
+    Returns (y, xk, xv, xr); the mix outputs are None when ``mix`` is False
+    and no buffers are passed.
+    """
+    L, B, C = x.shape
+    for t, n in ((x, "x"), (x_prev, "x_prev"), (r, "r"), (k, "k"), (v, "v"), (num, "num"), (den, "den"),
+                 (pp, "pp")):
+        _need(t, n, shape=(L, B, C))
+    for t, n in ((mu_k, "mu_k"), (mu_v, "mu_v"), (mu_r, "mu_r"), (w, "w"), (u, "u")):
+        _need(t, n, shape=(L, C))
+    if y is None:
+        y = torch.empty_like(x)
+    if mix:
+        xk = torch.empty_like(x) if xk is None else xk
+        xv = torch.empty_like(x) if xv is None else xv
+        xr = torch.empty_like(x) if xr is None else xr
+    for t, n in ((y, "y"), (xk, "xk"), (xv, "xv"), (xr, "xr")):
+        if t is not None:
+            _need(t, n, shape=(L, B, C))
+    _check(_lib.wkv_decode_step(L, B, C, *map(_p, (x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u, num, den, pp, y, xk,
+                                                     xv, xr)), _stream(stream)), "wkv_decode_step")
+    return y, xk, xv, xr
+
+
+# ------------------------------------------------------------- test hooks
+def set_wait_budget_ns(ns: int) -> None:
+    _check(_lib.wkv_debug_set_wait_budget_ns(int(ns)), "wkv_debug_set_wait_budget_ns")
+
+
+def set_skip_chunk(chunk: int) -> None:
+    _check(_lib.wkv_debug_set_skip_chunk(int(chunk)), "wkv_debug_set_skip_chunk")
+
+
+# -------------------------------------------------------------- autograd
+class WKVFunction(torch.autograd.Function):
+    """torch.autograd wrapper: forward saves the chunk checkpoints so the
+    backward call skips its own pass over k and v."""
+
+    @staticmethod
+    def forward(ctx, w, u, k, v):
+        y, ckpt = forward(w, u, k, v, want_ckpt=True)
+        ctx.save_for_backward(w, u, k, v, ckpt)
+        return y
+
+    @staticmethod
+    def backward(ctx, gy):
+        w, u, k, v, ckpt = ctx.saved_tensors
+        gw, gu, gk, gv = backward(w, u, k, v, gy.contiguous(), ckpt=ckpt)
+        return gw, gu, gk, gv
+
+
+def wkv(w, u, k, v):
+    """Differentiable WKV (fp32 k, v for the backward)."""
+    return WKVFunction.apply(w, u, k, v)

@@ -1,0 +1,233 @@
+// wkv_common.cuh -- device helpers shared by the WKV kernels (sm_103a).
+//
+// The operator (RWKV time mixing, "RWKV解读：在Transformer的时代的新RNN",
+// section "3、RWKV的网络架构", eq. (8); qiita "RWKV についての調査記録",
+// section "wkvとは"): per batch row and channel, with decay w > 0 and bonus u,
+//
+//   wkv_t = (sum_{i<t} e^{-(t-1-i)w + k_i} v_i + e^{u+k_t} v_t)
+//         / (sum_{i<t} e^{-(t-1-i)w + k_i}     + e^{u+k_t}),
+//
+// computed through a carried state.  The state after t tokens is the triple
+// (num, den, pp) with a_t = num e^{pp}, b_t = den e^{pp}, where
+// a_t = sum_{i<t} e^{-(t-1-i)w+k_i} v_i, b_t likewise without v, and pp is
+// the running maximum of the exponents, so den >= 1 once a token is seen and
+// no exponential overflows.  The empty state is (0, 0, -1e38).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace wkv {
+
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
+constexpr float kEmptyPP = -1e38f;             // pp of the empty state
+
+// A flag word is (launch epoch << 2) | status, so flags left by earlier
+// launches in the same workspace never read as published.
+
+// Error codes written to the workspace header by a kernel.
+constexpr unsigned int kDevErrTimeout = 6;
+
+// ---------------------------------------------------------------- math
+// 2^x with the MUFU unit.  Flushes subnormal results to zero, which only
+// ever drops weights below 2^-126 relative to the running maximum.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// e^{-|d|}: the one exponential needed for a pair e^{x-q}, e^{y-q} with
+// q = max(x, y) and d = x - y (the larger one gets exactly 1).
+__device__ __forceinline__ float exp_neg_abs(float d) { return ex2(-fabsf(d) * kLog2e); }
+
+__device__ __forceinline__ float exp_nat(float x) { return ex2(x * kLog2e); }
+
+struct State {
+  float num, den, pp;
+};
+
+__device__ __forceinline__ State empty_state() { return State{0.f, 0.f, kEmptyPP}; }
+
+// Consume one token (k, v): a' = e^{-w} a + e^{k} v, b' = e^{-w} b + e^{k},
+// pp' = max(pp - w, k).  The rounding residual of fl(pp - w) is folded back
+// into the decay factor (Fast2Sum), so a long run of steps where the decayed
+// past stays the maximum does not drift the scale of old tokens.
+__device__ __forceinline__ void step(State& s, float k, float v, float w) {
+  const float sw = s.pp - w;
+  const float res = (s.pp - sw) - w;  // (pp - w) - fl(pp - w)
+  const float d = sw - k;
+  const float e = exp_neg_abs(d);
+  const bool keep = d >= 0.f;  // decayed past is still the maximum
+  float dec = keep ? 1.f : e;
+  const float kap = keep ? e : 1.f;
+  dec = fmaf(dec, res, dec);  // e^{(pp - w) - pp'}
+  s.num = fmaf(dec, s.num, kap * v);
+  s.den = fmaf(dec, s.den, kap);
+  s.pp = keep ? sw : k;
+}
+
+// wkv for the current token (k, v) given the state before it.
+__device__ __forceinline__ float output(const State& s, float k, float v, float u) {
+  const float d = s.pp - (u + k);
+  const float e = exp_neg_abs(d);
+  const bool past = d >= 0.f;
+  const float cp = past ? 1.f : e;  // weight of the carried past
+  const float cc = past ? e : 1.f;  // weight of the current token (bonus u)
+  const float n = fmaf(cp, s.num, cc * v);
+  const float dd = fmaf(cp, s.den, cc);
+  return n * rcp(dd);
+}
+
+// x decayed over `decay` (= steps * w) followed by y: the associative combine
+// of chunk summaries (the decay is data independent, so a chunk's effect on
+// the carried state is "decay by its length, then add its own summary").
+__device__ __forceinline__ State combine(const State& x, float decay, const State& y) {
+  const float px = x.pp - decay;
+  const float q = fmaxf(px, y.pp);
+  const float ex = exp_nat(px - q);
+  const float ey = exp_nat(y.pp - q);
+  return State{fmaf(ex, x.num, ey * y.num), fmaf(ex, x.den, ey * y.den), q};
+}
+
+// ------------------------------------------------------- memory ordering
+__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Loads of data published by other CTAs: bypass L1 (not coherent).
+__device__ __forceinline__ float ld_cg(const float* p) { return __ldcg(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint64_t flag_status(uint64_t word, uint64_t epoch) {
+  return (word >> 2) == epoch ? (word & 3u) : 0u;
+}
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+  unsigned int ticket;       // dynamic tile counter (reset by the last tile)
+  unsigned int error;        // first device error code since the last check, 0 if none
+  unsigned long long abort;  // epoch of the last launch that gave up a wait
+  unsigned int pad[60];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+
+// Takes a tile ticket for the CTA.  Tickets are handed out in the order CTAs
+// start, so a tile only ever waits on tiles whose CTAs are already running:
+// the look-back below cannot deadlock however the hardware schedules CTAs.
+__device__ __forceinline__ unsigned int take_ticket(WsHeader* h, unsigned int ntiles) {
+  __shared__ unsigned int s_ticket;
+  if (threadIdx.x == 0) {
+    unsigned int t = atomicAdd(&h->ticket, 1u);
+    if (t == ntiles - 1) atomicExch(&h->ticket, 0u);  // every ticket is out: ready for the next launch
+    s_ticket = t;
+  }
+  __syncthreads();
+  return s_ticket;
+}
+
+// Records that this launch (epoch) gave up: the code for the host, the epoch
+// so the launch's other waits stop at once.
+__device__ __forceinline__ void record_error(WsHeader* h, unsigned int code, uint64_t epoch) {
+  atomicCAS(&h->error, 0u, code);
+  atomicExch(&h->abort, (unsigned long long)epoch);
+}
+
+}  // namespace wkv
+
+namespace wkv {
+
+// Chunk summaries are combined across tiles through a binary-indexed
+// (Fenwick) tree over the chunk index.  Node (e, s) exists when
+// (e + 1) % 2^s == 0 and summarises the 2^s chunks ending at chunk e; node
+// (e, 0) is chunk e's own summary and node (e, s) = node (e - 2^{s-1}, s-1)
+// followed by node (e, s-1), computed and published by the tile of chunk e.
+// The prefix before chunk j is the fixed list of nodes given by the binary
+// digits of j (nearest first: end j-1 with level ctz(j), then strip the
+// lowest set bit and repeat).  Every tile therefore combines the same values
+// in the same order on every run (bitwise reproducible), waits on at most
+// popcount(j) nodes, and the longest chain of waits is log2(nchunks) hops.
+// The first ctz(~j) nodes of j's list are exactly the left children of the
+// nodes (j, 1..), so one wait serves both.
+
+// i-th node (0 = nearest) of the prefix list of chunk j: end chunk and level.
+__device__ __forceinline__ void fenwick_node(int j, int i, int& end, int& level) {
+  int x = j;
+  for (int q = 0; q < i; ++q) x &= x - 1;
+  level = __ffs(x) - 1;
+  end = x - 1;
+}
+
+// Index of node (end, level) in the node arrays (levels stored one after
+// the other; level s holds nchunks >> s nodes).
+__device__ __forceinline__ int node_index(const int* level_off, int end, int level) {
+  return level_off[level] + ((end + 1) >> level) - 1;
+}
+
+constexpr uint64_t kNodeReady = 1;  // flag status: node data published
+constexpr uint64_t kNodeErr = 3;    // flag status: producer gave up
+
+constexpr int kWaitOk = 0;
+constexpr int kWaitTimeout = 1;
+constexpr int kWaitError = 2;
+
+// Waits (one warp) until the n <= 32 flags flag_of(0..n-1) are published in
+// this launch's epoch.  Lane i polls flag i, so all waits overlap.  Bounded:
+// past budget_ns of %globaltimer returns kWaitTimeout; a producer that gave
+// up, or an expired wait anywhere in the same launch (h->abort == epoch),
+// gives kWaitError, so one expired wait ends every other wait at once.  The warp barrier after a
+// successful wait orders the acquiring loads before every lane's reads of
+// the published data.
+template <class FlagOf>
+__device__ __forceinline__ int wait_flags(FlagOf flag_of, int n, uint64_t epoch, uint64_t budget_ns,
+                                          const WsHeader* h) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const uint64_t* fp = lane < n ? flag_of(lane) : nullptr;
+  uint64_t st = lane < n ? 0 : kNodeReady;
+  uint64_t t0 = 0;
+  bool timing = false;
+  while (true) {
+    if (st == 0) st = flag_status(ld_acquire(fp), epoch);
+    if (__any_sync(full, st == kNodeErr)) return kWaitError;
+    if (__all_sync(full, st != 0)) break;
+    if (__shfl_sync(full, *(volatile const unsigned long long*)&h->abort, 0) == epoch) return kWaitError;
+    const uint64_t now = __shfl_sync(full, globaltimer(), 0);
+    if (!timing) {
+      t0 = now;
+      timing = true;
+    } else if (now - t0 > budget_ns) {
+      return kWaitTimeout;
+    }
+    __nanosleep(64);
+  }
+  __syncwarp();
+  return kWaitOk;
+}
+
+// Publishes data every lane has written for its channel: the fence orders
+// those writes before the flag, which lane 0 then releases.
+__device__ __forceinline__ void publish(uint64_t* flag, uint64_t epoch, uint64_t status) {
+  __threadfence();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) st_release(flag, (epoch << 2) | status);
+}
+
+}  // namespace wkv

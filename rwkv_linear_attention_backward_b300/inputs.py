@@ -1,9 +1,10 @@
 """Seeded synthetic inputs shared by the tests, the oracle checks and bench.py.
 
 This module draws random numbers and nothing else: it holds none of the WKV
-arithmetic.  Every tensor is drawn on the CPU with ``torch.Generator`` so
-that the same seed gives the same values on any machine, in a fixed draw
-order (documented per function).  bf16 tensors are drawn in fp32 and then
+arithmetic.  Tensors are drawn with a seeded ``torch.Generator`` in a fixed
+draw order (documented per function): on the CPU, so the same seed gives the
+same values on any machine, except the large decode input pools, which are
+drawn on the device that uses them (``decode_pool``).  bf16 tensors are drawn in fp32 and then
 rounded to nearest-even by ``Tensor.to(torch.bfloat16)``; the oracle is
 handed the rounded values.
 
@@ -144,3 +145,15 @@ def initial_state(L: int, B: int, C: int):
     """Decode state before any token: num = den = 0, pp = -1e38."""
     z = torch.zeros(L, B, C, dtype=torch.float32)
     return z.clone(), z.clone(), torch.full((L, B, C), -1e38, dtype=torch.float32)
+
+
+def decode_pool(L: int, B: int, C: int, *, seed: int, n_sets: int, device="cpu"):
+    """A pool of ``n_sets`` per-step decode input sets (x, x_prev, r, k, v),
+    each [L, B, C] ~ N(0,1), drawn directly on ``device`` from one generator
+    seeded with ``seed`` (set after set, in that order within a set).  A run
+    of more steps than sets uses set ``step % n_sets`` at each step."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    shape = (L, B, C)
+    return [tuple(torch.randn(shape, generator=g, dtype=torch.float32, device=device) for _ in range(5))
+            for _ in range(n_sets)]

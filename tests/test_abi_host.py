@@ -1,0 +1,126 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function include/wkv.h declares, sizes its buffers as documented, and
+rejects invalid arguments before launching anything."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "wkv.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rwkv_linear_attention_backward_b300 import build
+
+    path = build.build()
+    lib = ctypes.CDLL(str(path))
+    lib.wkv_status_string.restype = ctypes.c_char_p
+    lib.wkv_last_error_string.restype = ctypes.c_char_p
+    for n in ("wkv_checkpoint_floats", "wkv_forward_workspace_bytes", "wkv_backward_workspace_bytes"):
+        getattr(lib, n).restype = ctypes.c_size_t
+    return lib
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    return sorted(set(re.findall(r"\b(wkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("wkv_forward", "wkv_backward", "wkv_decode_step", "wkv_forward_workspace_bytes",
+              "wkv_backward_workspace_bytes", "wkv_checkpoint_floats", "wkv_workspace_check"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in wkv.h but not exported"
+
+
+def test_binding_names_match_header():
+    src = (ROOT / "rwkv_linear_attention_backward_b300" / "binding.py").read_text()
+    for n in declared_functions():
+        assert f'"{n}"' in src, f"binding does not wrap {n}"
+
+
+def test_version_and_chunk(lib):
+    assert lib.wkv_version() == 1
+    assert lib.wkv_chunk_len() == 32
+
+
+@pytest.mark.parametrize("B,T,C", [(1, 1, 1), (1, 64, 64), (8, 1024, 768), (3, 33, 129), (1, 131072, 2560)])
+def test_sizes(lib, B, T, C):
+    L = lib.wkv_chunk_len()
+    nch = -(-T // L)
+    assert lib.wkv_checkpoint_floats(B, T, C) == 3 * nch * B * C
+    f = lib.wkv_forward_workspace_bytes(B, T, C)
+    b = lib.wkv_backward_workspace_bytes(B, T, C)
+    # header + flags + two [3, nchunks, B, C] fp32 arrays at least
+    assert f >= 256 + 2 * 3 * nch * B * C * 4
+    # + adjoint tree nodes (>= 3 planes) + gw, gu partials (2 planes)
+    assert b >= f + 256 + 5 * nch * B * C * 4
+    assert f % 256 == 0 and b % 256 == 0
+
+
+def test_invalid_sizes_give_zero(lib):
+    for B, T, C in ((0, 1, 1), (1, 0, 1), (1, 1, 0), (-1, 5, 5), (1 << 20, 1 << 20, 2)):
+        assert lib.wkv_forward_workspace_bytes(B, T, C) == 0
+        assert lib.wkv_checkpoint_floats(B, T, C) == 0
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["WKV_OK", "WKV_ERR_INVALID_ARG", "WKV_ERR_UNSUPPORTED", "WKV_ERR_MISALIGNED",
+                                 "WKV_ERR_WORKSPACE", "WKV_ERR_CUDA", "WKV_ERR_TIMEOUT"]):
+        assert lib.wkv_status_string(code).decode() == name
+    assert lib.wkv_status_string(99).decode() == "WKV_ERR_UNKNOWN"
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails validation first
+NULL = ctypes.c_void_p(0)
+
+
+def _fwd(lib, B=2, T=40, C=64, dtype=0, w=FAKE, u=FAKE, k=FAKE, v=FAKE, y=FAKE, ws=FAKE, wsb=None):
+    if wsb is None:
+        wsb = lib.wkv_forward_workspace_bytes(max(B, 1), max(T, 1), max(C, 1))
+    return lib.wkv_forward(B, T, C, dtype, w, u, k, v, y, NULL, ws, ctypes.c_size_t(wsb), NULL)
+
+
+def test_forward_rejects_before_launch(lib):
+    assert _fwd(lib, B=0) == 1
+    assert _fwd(lib, T=-3) == 1
+    assert _fwd(lib, dtype=7) == 1
+    for name in ("w", "u", "k", "v", "y"):
+        assert _fwd(lib, **{name: NULL}) == 1
+    assert _fwd(lib, ws=NULL) == 4
+    assert _fwd(lib, wsb=100) == 4
+
+
+def _bwd(lib, B=2, T=40, C=64, dtype=0, ws=FAKE, wsb=None, **nulls):
+    p = {n: FAKE for n in ("w", "u", "k", "v", "gy", "gw", "gu", "gk", "gv")}
+    p.update(nulls)
+    if wsb is None:
+        wsb = lib.wkv_backward_workspace_bytes(max(B, 1), max(T, 1), max(C, 1))
+    return lib.wkv_backward(B, T, C, dtype, p["w"], p["u"], p["k"], p["v"], p["gy"], NULL, p["gw"], p["gu"],
+                            p["gk"], p["gv"], ws, ctypes.c_size_t(wsb), NULL)
+
+
+def test_backward_rejects_before_launch(lib):
+    assert _bwd(lib, C=0) == 1
+    assert _bwd(lib, dtype=5) == 1
+    assert _bwd(lib, dtype=1) == 2  # bf16 backward: valid request, not implemented
+    for name in ("w", "u", "k", "v", "gy", "gw", "gu", "gk", "gv"):
+        assert _bwd(lib, **{name: NULL}) == 1
+    assert _bwd(lib, wsb=256) == 4
+
+
+def test_decode_rejects_before_launch(lib):
+    args = [FAKE] * 17
+    assert lib.wkv_decode_step(0, 1, 1, *args, NULL) == 1
+    for i in range(14):  # the 14 required pointers; the mix outputs may be NULL
+        a = list(args)
+        a[i] = NULL
+        assert lib.wkv_decode_step(2, 3, 4, *a, NULL) == 1

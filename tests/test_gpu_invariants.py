@@ -1,0 +1,134 @@
+"""Properties of the CUDA path that hold at any size: bitwise run-to-run
+reproducibility, causality, agreement of the checkpoint and recompute paths,
+workspace reuse, streams, and the bounded-wait error report."""
+import pytest
+import torch
+
+from parity import TOL_GRAD, TOL_Y, assert_close, cuda
+from rwkv_linear_attention_backward_b300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def wkv():
+    from rwkv_linear_attention_backward_b300 import binding
+
+    return binding
+
+
+def _run(wkv, w, u, k, v, gy, ckpt_to_bwd=True):
+    y, ckpt = wkv.forward(w, u, k, v, want_ckpt=True)
+    g = wkv.backward(w, u, k, v, gy, ckpt=ckpt if ckpt_to_bwd else None)
+    torch.cuda.synchronize()
+    return (y, ckpt) + tuple(g)
+
+
+def test_bitwise_reproducible(wkv):
+    t = cuda(*inputs.training_inputs(3, 3000, 200, seed=21, k_std=3.0))
+    a = _run(wkv, *t)
+    for _ in range(3):
+        b = _run(wkv, *t)
+        for x, y_ in zip(a, b):
+            assert torch.equal(x, y_)
+
+
+def test_checkpoint_and_recompute_agree_bitwise(wkv):
+    t = cuda(*inputs.training_inputs(2, 1500, 130, seed=22, k_std=3.0))
+    a = _run(wkv, *t, ckpt_to_bwd=True)
+    b = _run(wkv, *t, ckpt_to_bwd=False)
+    for x, y_ in zip(a[2:], b[2:]):
+        assert torch.equal(x, y_)
+
+
+def test_forward_causal(wkv):
+    w, u, k, v, gy = cuda(*inputs.training_inputs(2, 777, 96, seed=23, k_std=2.0))
+    y = wkv.forward(w, u, k, v)
+    t0 = 333
+    k2, v2 = k.clone(), v.clone()
+    k2[:, t0:] += 3.0
+    v2[:, t0:] -= 1.0
+    y2 = wkv.forward(w, u, k2, v2)
+    torch.cuda.synchronize()
+    assert torch.equal(y[:, :t0], y2[:, :t0])
+    assert not torch.equal(y[:, t0:], y2[:, t0:])
+
+
+def test_backward_anticausal(wkv):
+    """gk_t, gv_t depend on gy_s for s >= t only."""
+    w, u, k, v, gy = cuda(*inputs.training_inputs(2, 777, 96, seed=24, k_std=2.0))
+    _, _, _, _, gk, gv = _run(wkv, w, u, k, v, gy)
+    t0 = 400
+    gy2 = gy.clone()
+    gy2[:, :t0] *= -2.0
+    _, _, _, _, gk2, gv2 = _run(wkv, w, u, k, v, gy2)
+    assert torch.equal(gk[:, t0:], gk2[:, t0:]) and torch.equal(gv[:, t0:], gv2[:, t0:])
+
+
+def test_k_shift_invariance(wkv):
+    w, u, k, v, gy = cuda(*inputs.training_inputs(2, 600, 64, seed=25, k_std=2.0))
+    a = _run(wkv, w, u, k, v, gy)
+    b = _run(wkv, w, u, k + 30.0, v, gy)
+    assert_close(b[0], a[0], TOL_Y, "y(k+30)")
+    for x, y_, n in zip(b[2:], a[2:], ("gw", "gu", "gk", "gv")):
+        assert_close(x, y_, TOL_GRAD, n)
+    s = a[4].double().sum(dim=1).abs().max().item()  # sum_t gk_t = 0 per (b, c)
+    assert s <= 1e-4 * a[4].abs().max().item() * 600 ** 0.5
+
+
+def test_workspace_reused_across_shapes(oracle, wkv):
+    ws = wkv.Workspace(wkv.backward_workspace_bytes(4, 2000, 300))
+    for (B, T, C), seed in (((4, 2000, 300), 1), ((1, 50, 7), 2), ((3, 999, 129), 3), ((4, 2000, 300), 4)):
+        w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=seed, k_std=2.0)
+        wc, uc, kc, vc, gyc = cuda(w, u, k, v, gy)
+        y = wkv.forward(wc, uc, kc, vc, workspace=ws)
+        gw, gu, gk, gv = wkv.backward(wc, uc, kc, vc, gyc, workspace=ws)
+        torch.cuda.synchronize()
+        assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "y")
+        ow, ou, ok, ov = oracle.backward_adjoint(w, u, k, v, gy)
+        assert_close(gk, ok, TOL_GRAD, "gk")
+        assert_close(gw, ow, TOL_GRAD, "gw")
+        wkv.workspace_check(ws)
+
+
+def test_side_stream(oracle, wkv):
+    w, u, k, v, gy = inputs.training_inputs(2, 400, 80, seed=26)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        tw = cuda(w, u, k, v, gy)
+        y = wkv.forward(*tw[:4], stream=s)
+        gw, gu, gk, gv = wkv.backward(*tw, stream=s)
+    s.synchronize()
+    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "y")
+    assert_close(gv, oracle.backward_adjoint(w, u, k, v, gy)[3], TOL_GRAD, "gv")
+
+
+@pytest.mark.parametrize("which", ["forward", "backward"])
+def test_expired_wait_is_reported(oracle, wkv, which):
+    """A chunk whose tiles never publish makes the later tiles' bounded waits
+    expire: the call reports WKV_ERR_TIMEOUT through wkv_workspace_check and
+    the device stays usable."""
+    B, T, C = 1, 32 * 40, 64
+    w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=27)
+    tw = cuda(w, u, k, v, gy)
+    ws = wkv.Workspace(wkv.backward_workspace_bytes(B, T, C))
+    try:
+        wkv.set_wait_budget_ns(2_000_000)  # 2 ms
+        wkv.set_skip_chunk(0 if which == "forward" else T // 32 - 1)
+        if which == "forward":
+            wkv.forward(*tw[:4], workspace=ws)
+        else:
+            y, ckpt = wkv.forward(*tw[:4], want_ckpt=True)
+            wkv.backward(*tw, ckpt=ckpt, workspace=ws)
+        with pytest.raises(wkv.WKVError) as exc:
+            wkv.workspace_check(ws)
+        assert exc.value.status == 6
+    finally:
+        wkv.set_skip_chunk(-1)
+        wkv.set_wait_budget_ns(0)
+    wkv.workspace_check(ws)  # the record was cleared
+    y = wkv.forward(*tw[:4], workspace=ws)
+    gw, gu, gk, gv = wkv.backward(*tw, workspace=ws)
+    wkv.workspace_check(ws)
+    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "y after timeout")
+    assert_close(gk, oracle.backward_adjoint(w, u, k, v, gy)[2], TOL_GRAD, "gk after timeout")

@@ -1,0 +1,150 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle,
+element by element, on seeded inputs (module rwkv_linear_attention_backward_b300.inputs).
+
+Small shapes cover several chunks, ragged chunk and channel-block tails,
+T = 1, deep look-back chains and stress values; the named workloads run at
+full size (the oracle computes sampled channels exactly, since channels are
+independent)."""
+import numpy as np
+import pytest
+import torch
+
+from parity import TOL_BF16, TOL_GRAD, TOL_Y, assert_close, cuda, sample_channels, to_np
+from rwkv_linear_attention_backward_b300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def wkv():
+    from rwkv_linear_attention_backward_b300 import binding
+
+    return binding
+
+
+def run_fwd_bwd(wkv, w, u, k, v, gy, use_ckpt=True):
+    w, u, k, v, gy = cuda(w, u, k, v, gy)
+    y, ckpt = wkv.forward(w, u, k, v, want_ckpt=True)
+    gw, gu, gk, gv = wkv.backward(w, u, k, v, gy, ckpt=ckpt if use_ckpt else None)
+    torch.cuda.synchronize()
+    return y, ckpt, gw, gu, gk, gv
+
+
+def check_all(oracle, wkv, w, u, k, v, gy, use_ckpt=True, what=""):
+    y, ckpt, gw, gu, gk, gv = run_fwd_bwd(wkv, w, u, k, v, gy, use_ckpt)
+    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, f"{what} y")
+    ow, ou, ok, ov = oracle.backward_adjoint(w, u, k, v, gy)
+    assert_close(gk, ok, TOL_GRAD, f"{what} gk")
+    assert_close(gv, ov, TOL_GRAD, f"{what} gv")
+    assert_close(gw, ow, TOL_GRAD, f"{what} gw")
+    assert_close(gu, ou, TOL_GRAD, f"{what} gu")
+    return y, ckpt
+
+
+SHAPES = [
+    (1, 1, 1), (1, 1, 64), (1, 31, 5), (1, 32, 33), (2, 33, 129), (3, 65, 100), (1, 64, 64),
+    (2, 200, 256), (1, 257, 130), (4, 96, 7), (1, 1000, 32), (2, 513, 384),
+]
+
+
+@pytest.mark.parametrize("B,T,C", SHAPES, ids=[f"B{b}T{t}C{c}" for b, t, c in SHAPES])
+def test_small_shapes(oracle, wkv, B, T, C):
+    w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=100 + B * 7 + T + C, k_std=2.0, d_lo=-5.0, d_hi=1.5)
+    check_all(oracle, wkv, w, u, k, v, gy, what=f"B{B}T{T}C{C}")
+
+
+def test_without_checkpoint_matches(oracle, wkv):
+    w, u, k, v, gy = inputs.training_inputs(2, 300, 160, seed=5, k_std=2.0)
+    check_all(oracle, wkv, w, u, k, v, gy, use_ckpt=False, what="no ckpt")
+
+
+def test_checkpoint_is_the_carried_state(oracle, wkv):
+    B, T, C = 2, 150, 70
+    w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=6, k_std=3.0)
+    y, ckpt = wkv.forward(*cuda(w, u, k, v), want_ckpt=True)
+    L = wkv.chunk_len()
+    nch = -(-T // L)
+    ck = to_np(ckpt).reshape(3, nch, B, C)
+    for j in range(nch):
+        t = min((j + 1) * L, T)
+        num, den, pp = oracle.state(w, k, v, t)
+        assert_close(ck[2, j], pp, TOL_Y, f"pp after chunk {j}")
+        assert_close(ck[0, j], num, TOL_Y, f"num after chunk {j}")
+        assert_close(ck[1, j], den, TOL_Y, f"den after chunk {j}")
+
+
+@pytest.mark.parametrize("case", ["k_shift_64", "tiny_w", "huge_w", "big_u", "k_std_8"])
+def test_stress_values(oracle, wkv, case):
+    B, T, C = 2, 400, 96
+    kw = dict(k_std=2.0, d_lo=-5.0, d_hi=1.0)
+    if case == "tiny_w":
+        kw.update(d_lo=-12.0, d_hi=-9.0)
+    if case == "huge_w":
+        kw.update(d_lo=2.0, d_hi=3.5)
+    if case == "k_std_8":
+        kw.update(k_std=8.0)
+    w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=7, **kw)
+    if case == "k_shift_64":
+        k = k + 64.0
+    if case == "big_u":
+        u = u + 20.0
+    check_all(oracle, wkv, w, u, k, v, gy, what=case)
+
+
+def test_deep_lookback_chain(oracle, wkv):
+    """One 32-channel group and 2048 chunks: every tile of a row waits on a
+    long chain of predecessors in both directions."""
+    B, T, C = 1, 65536, 32
+    w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=8, k_std=3.0, d_lo=-9.0, d_hi=0.0)
+    check_all(oracle, wkv, w, u, k, v, gy, what="deep chain")
+
+
+def test_bf16_forward(oracle, wkv):
+    B, T, C = 2, 777, 136
+    w, u, k, v, _ = inputs.training_inputs(B, T, C, seed=9, k_std=5.0, d_lo=-8.0, d_hi=1.0, kv_dtype="bf16")
+    y = wkv.forward(*cuda(w, u, k, v))
+    torch.cuda.synchronize()
+    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_BF16, "bf16 y")
+    # far inside the loose bf16 tolerance: the oracle sees the same rounded inputs
+    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "bf16 y (fp32-level)")
+
+
+# ------------------------------------------------------------ named workloads
+def test_workload_tiny(oracle, wkv):
+    w, u, k, v, gy = inputs.workload_inputs("tiny")
+    y, _ = check_all(oracle, wkv, w, u, k, v, gy, what="tiny")
+    assert_close(y, oracle.forward_direct(w, u, k, v), TOL_Y, "tiny y vs direct form")
+
+
+def test_workload_l169m_full(oracle, wkv):
+    w, u, k, v, gy = inputs.workload_inputs("l169m")
+    check_all(oracle, wkv, w, u, k, v, gy, what="l169m")
+
+
+def _sampled(oracle, wkv, name, nchan, seed):
+    w, u, k, v, gy = inputs.workload_inputs(name)
+    wl = inputs.WORKLOADS[name]
+    cs = sample_channels(wl.C, nchan, seed)
+    ks, vs = k[:, :, cs].contiguous(), v[:, :, cs].contiguous()
+    if wl.backward:
+        y, _, gw, gu, gk, gv = run_fwd_bwd(wkv, w, u, k, v, gy)
+        ow, ou, ok, ov = oracle.backward_adjoint(w[cs], u[cs], ks, vs, gy[:, :, cs].contiguous())
+        cst = torch.as_tensor(cs, device="cuda")
+        assert_close(gk.index_select(2, cst), ok, TOL_GRAD, f"{name} gk")
+        assert_close(gv.index_select(2, cst), ov, TOL_GRAD, f"{name} gv")
+        assert_close(gw.index_select(0, cst), ow, TOL_GRAD, f"{name} gw")
+        assert_close(gu.index_select(0, cst), ou, TOL_GRAD, f"{name} gu")
+    else:
+        y = wkv.forward(*cuda(w, u, k, v))
+        torch.cuda.synchronize()
+        cst = torch.as_tensor(cs, device="cuda")
+    tol = TOL_BF16 if wl.kv_dtype == "bf16" else TOL_Y
+    assert_close(y.index_select(2, cst), oracle.forward_recurrent(w[cs], u[cs], ks, vs), tol, f"{name} y")
+
+
+def test_workload_l1b5_sampled(oracle, wkv):
+    _sampled(oracle, wkv, "l1b5", 48, 11)
+
+
+def test_workload_long_sampled(oracle, wkv):
+    _sampled(oracle, wkv, "long", 48, 12)
