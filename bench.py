@@ -17,7 +17,7 @@ twice its size) before every timed step, outside the step's CUDA-event pair;
 the value is the elements of all ranks over the max over ranks of the summed
 per-step device times.  The dominant kernel's launches are timed with their
 own events on the launching stream for the roofline entry.  SM clocks and
-clock-event reasons are sampled through NVML during the timed steps.
+clock-event reasons are sampled (NVML, else nvidia-smi) during the timed steps.
 
 ``--impl reference`` times the float64 CPU oracle (oracle/) on this
 machine's host cores instead: each step is a bounded sample of the same
@@ -107,21 +107,30 @@ def aggregate(per_rank_seconds: float, units_per_rank: float, world: int, device
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML (read only)."""
+    """Samples the SM clock and clock-event reasons during a timed region
+    (read only): through NVML when pynvml imports, else by running
+    ``nvidia-smi --query-gpu=... -lms 50`` and reading its output."""
 
     NAMES = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
         0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
         0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
     }
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int, period_s: float = 0.02):
+        self.index = index
         self.period = period_s
         self.samples = []
         self.reasons = set()
         self.max_mhz = None
+        self.source = None
+        self.error = None
         self._stop = threading.Event()
         self._thread = None
+        self._proc = None
         try:
             import pynvml
 
@@ -129,11 +138,12 @@ class ClockSampler:
             self.nv = pynvml
             self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # NVML missing: report that instead of clocks
+            self.source = "nvml"
+        except Exception as e:
             self.nv = None
-            self.error = str(e)
+            self.error = f"pynvml: {e}"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
@@ -146,23 +156,65 @@ class ClockSampler:
                 pass
             self._stop.wait(self.period)
 
+    def _run_smi(self):
+        for line in self._proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                self.samples.append(float(parts[0]))
+                self.max_mhz = float(parts[1])
+                mask = int(parts[2], 16)
+            except ValueError:
+                continue
+            for bit, name in self.NAMES.items():
+                if mask & bit:
+                    self.reasons.add(name)
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 parts[3:7]):
+                if val.lower() == "active":
+                    self.reasons.add(name)
+
     def __enter__(self):
         if self.nv is not None:
-            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread = threading.Thread(target=self._run_nvml, daemon=True)
             self._thread.start()
+            return self
+        import subprocess
+
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
+        except OSError as e:
+            self.error = f"{self.error}; nvidia-smi: {e}"
+            return self
+        self._thread = threading.Thread(target=self._run_smi, daemon=True)
+        self._thread.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 5.0:  # first sample before the timed region
+            time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):
         self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
         if self._thread is not None:
-            self._thread.join()
+            self._thread.join(timeout=5)
 
     def summary(self):
-        if self.nv is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.error}
-        med = statistics.median(self.samples) if self.samples else None
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "source": self.source,
+                    "error": self.error}
         reasons = sorted(self.reasons - {"gpu_idle"})
-        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples)}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "source": self.source}
 
     def rejected(self) -> bool:
         s = self.summary()

@@ -37,7 +37,8 @@ bool sizes_ok(int B, int T, int C) {
   return (double)g.nchunks * g.B * g.ncb <= (double)INT_MAX;
 }
 
-// Forward workspace: header | flags [B][nwg][nnodes] u64 | tree nodes
+// Forward workspace: header (tile counters, error record) | flags
+// [B][nwg][nnodes] u64 | tree nodes
 // [3][nnodes][B][C] f32 | checkpoints [3][nchunks][B][C] f32 (used when the
 // caller passes none).
 struct FwdLayout {
@@ -191,8 +192,8 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
   a.nodes = reinterpret_cast<float*>(bytes(workspace) + l.nodes);
   a.incl = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.incl);
   a.flags = reinterpret_cast<uint64_t*>(bytes(workspace) + l.flags);
-  a.hdr = static_cast<WsHeader*>(workspace);
-  a.eh = a.hdr;
+  a.eh = static_cast<WsHeader*>(workspace);
+  a.ticket = &a.eh->ticket[0];
   a.g = g;
   a.epoch = next_epoch();
   a.budget_ns = (uint64_t)g_budget_ns.load();
@@ -230,7 +231,7 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
     f.nodes = reinterpret_cast<float*>(fws + fl.nodes);
     f.incl = reinterpret_cast<float*>(fws + fl.incl);
     f.flags = reinterpret_cast<uint64_t*>(fws + fl.flags);
-    f.hdr = reinterpret_cast<WsHeader*>(fws);
+    f.ticket = &hdr->ticket[1];  // counters stay in the outer header: its place never moves
     f.eh = hdr;
     f.g = g;
     f.epoch = next_epoch();
@@ -253,7 +254,7 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
   a.rnodes = reinterpret_cast<float*>(bytes(workspace) + l.rnodes);
   a.part = reinterpret_cast<float*>(bytes(workspace) + l.part);
   a.flags = reinterpret_cast<uint64_t*>(bytes(workspace) + l.flags);
-  a.hdr = hdr;
+  a.ticket = &hdr->ticket[2];
   a.eh = hdr;
   a.g = g;
   a.epoch = next_epoch();

@@ -43,11 +43,11 @@ namespace {
 
 // Everything the reverse pass needs at one token, from the state before it.
 struct Local {
-  float gb;   // gy e^{pp-q} / Dhat : scaled gN
-  float gc;   // gy e^{u+k-q} / Dhat : gN e^{u+k}
-  float y;    // wkv_t
-  float dec;  // e^{pp_t - w - pp_{t+1}} (compensated as in the forward step)
-  float kap;  // e^{k_t - pp_{t+1}}
+  float gb;  // gy e^{pp-q} / Dhat : scaled gN
+  float gc;  // gy e^{u+k-q} / Dhat : gN e^{u+k}
+  float y;   // wkv_t
+  float vmy; // v_t - wkv_t, formed without subtracting the two
+  Decay t;   // carry factors of the forward step (same as the forward pass)
 };
 
 __device__ __forceinline__ Local local_terms(const State& s, float k, float v, float g, float w, float u) {
@@ -59,17 +59,13 @@ __device__ __forceinline__ Local local_terms(const State& s, float k, float v, f
   const float cc = past ? e1 : 1.f;
   const float inv = rcp(fmaf(cp, s.den, cc));
   o.y = fmaf(cp, s.num, cc * v) * inv;
+  // v - wkv = cp (den v - num) / Dhat: exact cancellation of the current
+  // token's own share, so no rounding noise when the bonus dominates
+  o.vmy = cp * fmaf(s.den, v, -s.num) * inv;
   const float gi = g * inv;
   o.gb = gi * cp;
   o.gc = gi * cc;
-  const float sw = s.pp - w;
-  const float res = (s.pp - sw) - w;
-  const float d2 = sw - k;
-  const float e2 = exp_neg_abs(d2);
-  const bool keep = d2 >= 0.f;
-  const float dec = keep ? 1.f : e2;
-  o.kap = keep ? e2 : 1.f;
-  o.dec = fmaf(dec, res, dec);
+  o.t = decay_terms(s.pp, k, w);
   return o;
 }
 
@@ -79,7 +75,8 @@ template <int L>
 __global__ void __launch_bounds__(kCtaChannels, 3) bwd_scan_kernel(const BwdArgs a) {
   extern __shared__ float sm[];  // [3][L][kCtaChannels]: num, den, pp before each token
   const ScanGeometry& g = a.g;
-  const unsigned int ticket = take_ticket(a.hdr, g.ntiles);
+  const unsigned int ticket = take_ticket(a.ticket, g.ntiles);
+  if (ticket >= g.ntiles) return;  // only if the counter was not zeroed: never touch memory then
   const int per_j = g.B * g.ncb;
   const int jr = ticket / per_j;
   const int j = g.nchunks - 1 - jr;  // last chunk first
@@ -141,8 +138,9 @@ __global__ void __launch_bounds__(kCtaChannels, 3) bwd_scan_kernel(const BwdArgs
     if (i < len) {
       const State si{sm_num[i * kCtaChannels + tid], sm_den[i * kCtaChannels + tid], sm_pp[i * kCtaChannels + tid]};
       const Local o = local_terms(si, kr[i], vr[i], gr[i], w, u);
-      la = fmaf(o.dec, la, o.gb);
-      lb = fmaf(o.dec, lb, -o.gb * o.y);
+      // the adjoint is carried back by the transpose of the forward step
+      la = carry(o.t, la, o.gb);
+      lb = carry(o.t, lb, -o.gb * o.y);
     }
   }
 
@@ -246,13 +244,14 @@ __global__ void __launch_bounds__(kCtaChannels, 3) bwd_scan_kernel(const BwdArgs
       const State si{sm_num[i * kCtaChannels + tid], sm_den[i * kCtaChannels + tid], sm_pp[i * kCtaChannels + tid]};
       const float k = kr[i], v = vr[i];
       const Local o = local_terms(si, k, v, gr[i], w, u);
-      const float cur = o.gc * (v - o.y);
-      const float gk = fmaf(o.kap, fmaf(la, v, lb), cur);
-      const float gv = fmaf(o.kap, la, o.gc);
+      const float cur = o.gc * o.vmy;
+      const float gk = fmaf(o.t.kap, fmaf(la, v, lb), cur);
+      const float gv = fmaf(o.t.kap, la, o.gc);
       gu_acc += cur;
-      gw_acc = fmaf(-o.dec, fmaf(la, si.num, lb * si.den), gw_acc);
-      la = fmaf(o.dec, la, o.gb);
-      lb = fmaf(o.dec, lb, -o.gb * o.y);
+      gw_acc = fmaf(-(o.t.dec + o.t.cor), fmaf(la, si.num, lb * si.den), gw_acc);
+      // the adjoint is carried back by the transpose of the forward step
+      la = carry(o.t, la, o.gb);
+      lb = carry(o.t, lb, -o.gb * o.y);
       if (valid) {
         const int64_t off = base + (int64_t)i * g.C;
         __stcs(a.gk + off, gk);

@@ -56,21 +56,43 @@ struct State {
 __device__ __forceinline__ State empty_state() { return State{0.f, 0.f, kEmptyPP}; }
 
 // Consume one token (k, v): a' = e^{-w} a + e^{k} v, b' = e^{-w} b + e^{k},
-// pp' = max(pp - w, k).  The rounding residual of fl(pp - w) is folded back
-// into the decay factor (Fast2Sum), so a long run of steps where the decayed
-// past stays the maximum does not drift the scale of old tokens.
-__device__ __forceinline__ void step(State& s, float k, float v, float w) {
-  const float sw = s.pp - w;
-  const float res = (s.pp - sw) - w;  // (pp - w) - fl(pp - w)
+// pp' = max(pp - w, k).  The old state is carried over by the factor
+// e^{(pp - w) - pp'} = dec * (1 + res), where res = (pp - w) - fl(pp - w) is
+// the rounding residual of the new exponent (Fast2Sum).  Adding the term
+// dec * res * num separately keeps that correction at full precision (1 + res
+// itself would round to 1), so a long run of steps where the decayed past
+// stays the maximum does not drift the carried sums.
+struct Decay {
+  float dec;  // e^{fl(pp - w) - pp'}
+  float cor;  // dec * res
+  float kap;  // e^{k - pp'}
+  float pp;   // pp'
+};
+
+__device__ __forceinline__ Decay decay_terms(float pp, float k, float w) {
+  Decay o;
+  const float sw = pp - w;
+  const float res = (pp - sw) - w;
   const float d = sw - k;
   const float e = exp_neg_abs(d);
   const bool keep = d >= 0.f;  // decayed past is still the maximum
-  float dec = keep ? 1.f : e;
-  const float kap = keep ? e : 1.f;
-  dec = fmaf(dec, res, dec);  // e^{(pp - w) - pp'}
-  s.num = fmaf(dec, s.num, kap * v);
-  s.den = fmaf(dec, s.den, kap);
-  s.pp = keep ? sw : k;
+  o.dec = keep ? 1.f : e;
+  o.kap = keep ? e : 1.f;
+  o.cor = o.dec * res;
+  o.pp = keep ? sw : k;
+  return o;
+}
+
+// x' = e^{(pp - w) - pp'} x + add, with the correction term kept separate.
+__device__ __forceinline__ float carry(const Decay& t, float x, float add) {
+  return fmaf(t.dec, x, fmaf(t.cor, x, add));
+}
+
+__device__ __forceinline__ void step(State& s, float k, float v, float w) {
+  const Decay t = decay_terms(s.pp, k, w);
+  s.num = carry(t, s.num, t.kap * v);
+  s.den = carry(t, s.den, t.kap);
+  s.pp = t.pp;
 }
 
 // wkv for the current token (k, v) given the state before it.
@@ -120,23 +142,29 @@ __device__ __forceinline__ uint64_t flag_status(uint64_t word, uint64_t epoch) {
   return (word >> 2) == epoch ? (word & 3u) : 0u;
 }
 
-// Workspace header (first 256 bytes of every workspace).
+// Workspace header: the first 256 bytes of a workspace, at the same place for
+// every shape, so a workspace zero-filled once stays valid when it is reused
+// for other shapes (everything after the header is either epoch-tagged or
+// written before it is read within a call).
 struct WsHeader {
-  unsigned int ticket;       // dynamic tile counter (reset by the last tile)
+  unsigned int ticket[4];    // dynamic tile counters, one per kind of launch (each reset by its last tile)
   unsigned int error;        // first device error code since the last check, 0 if none
+  unsigned int pad0;
   unsigned long long abort;  // epoch of the last launch that gave up a wait
-  unsigned int pad[60];
+  unsigned int pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
 // Takes a tile ticket for the CTA.  Tickets are handed out in the order CTAs
 // start, so a tile only ever waits on tiles whose CTAs are already running:
-// the look-back below cannot deadlock however the hardware schedules CTAs.
-__device__ __forceinline__ unsigned int take_ticket(WsHeader* h, unsigned int ntiles) {
+// the waits below cannot deadlock however the hardware schedules CTAs.  The
+// grid has exactly ntiles CTAs, so the CTA that draws ntiles - 1 knows every
+// ticket is out and resets the counter for the next launch.
+__device__ __forceinline__ unsigned int take_ticket(unsigned int* counter, unsigned int ntiles) {
   __shared__ unsigned int s_ticket;
   if (threadIdx.x == 0) {
-    unsigned int t = atomicAdd(&h->ticket, 1u);
-    if (t == ntiles - 1) atomicExch(&h->ticket, 0u);  // every ticket is out: ready for the next launch
+    unsigned int t = atomicAdd(counter, 1u);
+    if (t == ntiles - 1) atomicExch(counter, 0u);
     s_ticket = t;
   }
   __syncthreads();

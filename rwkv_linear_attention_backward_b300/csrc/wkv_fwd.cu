@@ -41,7 +41,8 @@ __device__ __forceinline__ float load_kv<__nv_bfloat16>(const __nv_bfloat16* p) 
 template <typename KV, int L, bool WRITE_Y>
 __global__ void __launch_bounds__(kCtaChannels, 4) fwd_scan_kernel(const FwdArgs a) {
   const ScanGeometry& g = a.g;
-  const unsigned int ticket = take_ticket(a.hdr, g.ntiles);
+  const unsigned int ticket = take_ticket(a.ticket, g.ntiles);
+  if (ticket >= g.ntiles) return;  // only if the counter was not zeroed: never touch memory then
   const int per_j = g.B * g.ncb;
   const int j = ticket / per_j;
   const int rem = ticket - j * per_j;

@@ -42,7 +42,7 @@ struct FwdArgs {
   float* nodes;      // [3][nnodes][B][C] tree nodes: (num, den, pp)
   float* incl;       // [3][nchunks][B][C] state after each chunk (checkpoints)
   uint64_t* flags;   // [B][nwg][nnodes]
-  WsHeader* hdr;          // ticket counter of this launch
+  unsigned int* ticket;   // tile counter of this launch (in a workspace header)
   WsHeader* eh;           // where an expired wait is recorded (checked by the host)
   ScanGeometry g;
   uint64_t epoch;
@@ -62,7 +62,7 @@ struct BwdArgs {
   float* rnodes;       // [3][nnodes][B][C] tree nodes of the adjoint: (la, lb, exponent)
   float* part;         // [2][nchunks][B][C] per-tile gw, gu partial sums
   uint64_t* flags;     // [B][nwg][nnodes]
-  WsHeader* hdr;
+  unsigned int* ticket;
   WsHeader* eh;
   ScanGeometry g;
   uint64_t epoch;

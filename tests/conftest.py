@@ -19,3 +19,18 @@ def oracle():
     import oracle as _oracle
 
     return _oracle.load()
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write every parity measurement of the run to gpurun_out/ when that
+    folder exists (GPU runs), for the records kept under profiles/."""
+    import json
+
+    try:
+        from parity import PARITY_LOG
+    except ImportError:
+        return
+    out = os.path.join(ROOT, "gpurun_out")
+    if PARITY_LOG and os.path.isdir(out):
+        with open(os.path.join(out, "parity_errors.json"), "w") as f:
+            json.dump(PARITY_LOG, f, indent=0)

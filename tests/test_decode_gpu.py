@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 import torch
 
-from parity import TOL_Y, assert_close, cuda, to_np
+from parity import TOL_Y, assert_close, assert_state_close, cuda, to_np
 from rwkv_linear_attention_backward_b300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -39,9 +39,7 @@ def _run_steps(oracle, wkv, L, B, C, steps, seed, mix=True, offset=0):
                                                                 opp, mix=mix)
         torch.cuda.synchronize()
         assert_close(y, oy, TOL_Y, f"step {s} y")
-        assert_close(gpp, opp, TOL_Y, f"step {s} pp")
-        assert_close(gnum, onum, TOL_Y, f"step {s} num")
-        assert_close(gden, oden, TOL_Y, f"step {s} den")
+        assert_state_close(gnum, gden, gpp, onum, oden, opp, TOL_Y, f"step {s}")
         if mix:
             for a_, b_, n in ((xk, oxk, "xk"), (xv, oxv, "xv"), (xr, oxr, "xr")):
                 assert_close(a_, b_, TOL_Y, f"step {s} {n}")
@@ -91,9 +89,7 @@ def test_decode_workload(oracle, wkv):
             oy, n1, d1, p1, oxk, oxv, oxr = oracle.decode_step(x, xp, mu_k, mu_v, mu_r, r, k, v, w, u, *ofull)
             ofull = [n1, d1, p1]
             assert_close(y, oy, TOL_Y, f"full step {s} y")
-            assert_close(pp, p1, TOL_Y, f"full step {s} pp")
-            assert_close(num, n1, TOL_Y, f"full step {s} num")
-            assert_close(den, d1, TOL_Y, f"full step {s} den")
+            assert_state_close(num, den, pp, n1, d1, p1, TOL_Y, f"full step {s}")
             assert_close(xk, oxk, TOL_Y, f"full step {s} xk")
         sx, sxp, sr, sk, sv = pool_sl[s % 16]
         oy, n2, d2, p2, _, _, _ = oracle.decode_step(sx, sxp, *psl[:3], sr, sk, sv, *psl[3:], *osl, mix=False)
@@ -101,6 +97,4 @@ def test_decode_workload(oracle, wkv):
         if s % 128 == 127 or s == D.steps - 1:
             torch.cuda.synchronize()
             assert_close(slice_(y), oy, TOL_Y, f"slice step {s} y")
-            assert_close(slice_(pp), osl[2], TOL_Y, f"slice step {s} pp")
-            assert_close(slice_(num), osl[0], TOL_Y, f"slice step {s} num")
-            assert_close(slice_(den), osl[1], TOL_Y, f"slice step {s} den")
+            assert_state_close(slice_(num), slice_(den), slice_(pp), *osl, TOL_Y, f"slice step {s}")

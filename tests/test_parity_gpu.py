@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from parity import TOL_BF16, TOL_GRAD, TOL_Y, assert_close, cuda, sample_channels, to_np
+from parity import TOL_BF16, TOL_GRAD, TOL_Y, assert_close, assert_state_close, cuda, sample_channels, to_np
 from rwkv_linear_attention_backward_b300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -68,9 +68,7 @@ def test_checkpoint_is_the_carried_state(oracle, wkv):
     for j in range(nch):
         t = min((j + 1) * L, T)
         num, den, pp = oracle.state(w, k, v, t)
-        assert_close(ck[2, j], pp, TOL_Y, f"pp after chunk {j}")
-        assert_close(ck[0, j], num, TOL_Y, f"num after chunk {j}")
-        assert_close(ck[1, j], den, TOL_Y, f"den after chunk {j}")
+        assert_state_close(ck[0, j], ck[1, j], ck[2, j], num, den, pp, TOL_Y, f"after chunk {j}")
 
 
 @pytest.mark.parametrize("case", ["k_shift_64", "tiny_w", "huge_w", "big_u", "k_std_8"])
