@@ -163,6 +163,33 @@ wkv_status wkv_decode_step(int L, int B, int C, const float* x, const float* x_p
                            float* xv, float* xr, void* stream);
 
 /*
+ * wkv_forward_noalloc -- wkv_forward without a caller-provided workspace.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot call cudaMalloc, such as a plugin or embedded host whose device
+ * memory belongs to another allocator, or a latency-bound loop that must
+ * never allocate (cudaMalloc can synchronise the device and stall every
+ * stream).  Inputs and outputs are passed exactly as for wkv_forward (y and
+ * the optional ckpt are caller-owned device memory); the scratch comes from
+ * one 32 MiB array compiled into the library, which every GPU that loads the
+ * library holds until the process exits.  Nothing is allocated.
+ *   - Shapes whose wkv_forward_workspace_bytes exceed 32 MiB are rejected
+ *     with WKV_ERR_WORKSPACE and a message in wkv_last_error_string().
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the array and it keeps the last call's
+ *     contents; each call clears its first 256 bytes (tile counters, error
+ *     record) on `stream` before the kernel.  Calls that overlap on the GPU
+ *     (different streams without ordering, or different host threads)
+ *     race on the array: serialise them.
+ *   - A bounded device-side wait that expires cannot be reported here (there
+ *     is no workspace to check); use wkv_forward where that matters.
+ * Errors: as wkv_forward, plus WKV_ERR_WORKSPACE for shapes too large.
+ */
+wkv_status wkv_forward_noalloc(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                               const void* v, float* y, float* ckpt, void* stream);
+
+/*
  * Test hooks (process-wide; not for production use).
  * wkv_debug_set_wait_budget_ns: limit of each bounded device-side wait of
  *   the scans, in ns of %globaltimer; <= 0 restores the default (500 ms).

@@ -41,6 +41,7 @@ _SIGNATURES = {
     "wkv_forward": ([_i, _i, _i, _i] + [_vp] * 6 + [_vp, _sz, _vp], _i),
     "wkv_backward": ([_i, _i, _i, _i] + [_vp] * 10 + [_vp, _sz, _vp], _i),
     "wkv_decode_step": ([_i, _i, _i] + [_vp] * 17 + [_vp], _i),
+    "wkv_forward_noalloc": ([_i, _i, _i, _i] + [_vp] * 6 + [_vp], _i),
     "wkv_debug_set_wait_budget_ns": ([_ll], _i),
     "wkv_debug_set_skip_chunk": ([_i], _i),
 }
@@ -169,6 +170,25 @@ def forward(w, u, k, v, *, y=None, ckpt=None, want_ckpt: bool = False, workspace
     _check(_lib.wkv_forward(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(y), _p(ckpt), ws.ptr(), ws.nbytes,
                             _stream(stream)), "wkv_forward")
     return (y, ckpt) if ckpt is not None else y
+
+
+def forward_noalloc(w, u, k, v, *, y=None, ckpt=None, stream=None):
+    """wkv_forward with the library's built-in scratch instead of a
+    workspace, for callers that cannot allocate device memory (see
+    wkv_forward_noalloc in include/wkv.h).  Shapes needing more than 32 MiB
+    of scratch raise WKVError."""
+    B, T, C = k.shape
+    _need(k, "k", (torch.float32, torch.bfloat16))
+    _need(v, "v", (k.dtype,), k.shape)
+    _need(w, "w", shape=(C,))
+    _need(u, "u", shape=(C,))
+    if y is None:
+        y = torch.empty((B, T, C), dtype=torch.float32, device=k.device)
+    _need(y, "y", shape=(B, T, C))
+    dt = WKV_BF16 if k.dtype == torch.bfloat16 else WKV_F32
+    _check(_lib.wkv_forward_noalloc(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(y), _p(ckpt), _stream(stream)),
+           "wkv_forward_noalloc")
+    return y
 
 
 # --------------------------------------------------------------- backward

@@ -86,6 +86,10 @@ char* bytes(void* p) { return static_cast<char*>(p); }
 
 }  // namespace
 
+void set_last_error(const char* msg) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+}
+
 ScanGeometry make_geometry(int B, int T, int C) {
   ScanGeometry g;
   g.B = B;

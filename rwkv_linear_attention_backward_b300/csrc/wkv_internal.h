@@ -84,6 +84,9 @@ struct DecodeArgs {
   int L, B, C;
 };
 
+// Sets the text returned by wkv_last_error_string() on this thread.
+void set_last_error(const char* msg);
+
 cudaError_t launch_forward(const FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
 cudaError_t launch_backward(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s);
