@@ -1,6 +1,8 @@
 // wkv_abi.cu -- the extern "C" boundary of libwkv.so (declared in
 // include/wkv.h): argument checks, workspace layout, launch plans.
 #include <atomic>
+#include <mutex>
+#include <cudaTypedefs.h>
 #include <climits>
 #include <cstdio>
 #include <cstring>
@@ -38,42 +40,51 @@ bool sizes_ok(int B, int T, int C) {
 }
 
 // Forward workspace: header (tile counters, error record) | flags
-// [B][nwg][nnodes] u64 | tree nodes
-// [3][nnodes][B][C] f32 | checkpoints [3][nchunks][B][C] f32 (used when the
-// caller passes none).
+// [nchunks][B][nwg] u64 | chunk summaries [3][nchunks][B][C] f32 |
+// checkpoints [3][nchunks][B][C] f32 (used when the caller passes none).
 struct FwdLayout {
-  size_t flags, nodes, incl, total;
+  size_t flags, agg, inc, total;
 };
 
 FwdLayout fwd_layout(const ScanGeometry& g) {
   FwdLayout l;
   size_t off = sizeof(WsHeader);
   l.flags = off;
-  off += align256((size_t)g.B * g.nwg * g.nnodes * sizeof(uint64_t));
-  l.nodes = off;
-  off += align256(3 * g.nplane * sizeof(float));
-  l.incl = off;
+  off += align256((size_t)g.nchunks * g.B * g.nwg * sizeof(uint64_t));
+  l.agg = off;
+  off += align256(3 * g.plane * sizeof(float));
+  l.inc = off;
   off += align256(3 * g.plane * sizeof(float));
   l.total = off;
   return l;
 }
 
-// Backward workspace: header | flags [B][nwg][nnodes] u64 | adjoint tree
-// nodes [3][nnodes][B][C] f32 | gw, gu partials [2][nchunks][B][C] f32 |
-// a forward workspace for recomputing the checkpoints when none are given.
+// Backward workspace: header | flags [nchunks][B][nwg] u64 | adjoint
+// records, zero-carry and inclusive, [3][nchunks][B][C] f32 each | gw, gu
+// partials [2][nchunks][B][C] f32 | reduction slices [nslice][2][C] f32 |
+// launch-tagged reduction counters [ceil(C/32)] u64 | a forward workspace
+// for recomputing the checkpoints when none are given.
 struct BwdLayout {
-  size_t flags, rnodes, part, fwd, total;
+  size_t flags, ragg, rinc, part, slices, count, fwd, total;
+  int nslice;
 };
 
 BwdLayout bwd_layout(const ScanGeometry& g) {
   BwdLayout l;
   size_t off = sizeof(WsHeader);
   l.flags = off;
-  off += align256((size_t)g.B * g.nwg * g.nnodes * sizeof(uint64_t));
-  l.rnodes = off;
-  off += align256(3 * g.nplane * sizeof(float));
+  off += align256((size_t)g.nchunks * g.B * g.nwg * sizeof(uint64_t));
+  l.ragg = off;
+  off += align256(3 * g.plane * sizeof(float));
+  l.rinc = off;
+  off += align256(3 * g.plane * sizeof(float));
   l.part = off;
   off += align256(2 * g.plane * sizeof(float));
+  l.nslice = reduce_slices(g.nchunks * g.B, g.C);
+  l.slices = off;
+  off += align256((size_t)l.nslice * 2 * g.C * sizeof(float));
+  l.count = off;
+  off += align256((size_t)((g.C + 31) / 32) * sizeof(unsigned long long));
   l.fwd = off;  // nested forward workspace, used when no checkpoint is given
   off += fwd_layout(g).total;
   l.total = off;
@@ -100,18 +111,40 @@ ScanGeometry make_geometry(int B, int T, int C) {
   g.nwg = g.ncb * (kCtaChannels / 32);
   g.ntiles = (unsigned int)((size_t)g.nchunks * B * g.ncb);
   g.plane = (size_t)g.nchunks * B * C;
-  g.nnodes = 0;
-  g.nlevels = 0;
-  for (int s = 0; s < 32; ++s) {
-    g.level_off[s] = g.nnodes;
-    const int cnt = g.nchunks >> s;
-    if (cnt > 0) {
-      g.nnodes += cnt;
-      g.nlevels = s + 1;
-    }
-  }
-  g.nplane = (size_t)g.nnodes * B * C;
   return g;
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int elem_bytes) {
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
+  if (((size_t)C * elem_bytes) % 16 != 0) return false;
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)C * elem_bytes, (cuuint64_t)T * C * elem_bytes};
+  const cuuint32_t box[3] = {(cuuint32_t)kCtaChannels, (cuuint32_t)kChunk, 1u};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  const CUresult r = fn(map, elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 }  // namespace wkv
@@ -188,20 +221,24 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
   const FwdLayout l = fwd_layout(g);
   if (!workspace || workspace_bytes < l.total) return WKV_ERR_WORKSPACE;
   FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
   a.w = w;
   a.u = u;
   a.k = k;
   a.v = v;
   a.y = y;
-  a.nodes = reinterpret_cast<float*>(bytes(workspace) + l.nodes);
-  a.incl = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.incl);
+  a.agg = reinterpret_cast<float*>(bytes(workspace) + l.agg);
+  a.inc = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.inc);
   a.flags = reinterpret_cast<uint64_t*>(bytes(workspace) + l.flags);
   a.eh = static_cast<WsHeader*>(workspace);
   a.ticket = &a.eh->ticket[0];
+  a.exited = &a.eh->exited[0];
   a.g = g;
   a.epoch = next_epoch();
   a.budget_ns = (uint64_t)g_budget_ns.load();
   a.debug_skip_chunk = g_skip_chunk.load();
+  const int eb = kv_dtype == WKV_F32 ? 4 : 2;
+  a.use_tma = make_tile_map(&a.tk, k, B, T, C, eb) && make_tile_map(&a.tv, v, B, T, C, eb);
   cudaError_t e = launch_forward(a, kv_dtype, true, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
 }
@@ -227,26 +264,30 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
     char* fws = bytes(workspace) + l.fwd;
     const FwdLayout fl = fwd_layout(g);
     FwdArgs f;
+    std::memset(&f, 0, sizeof(f));
     f.w = w;
     f.u = u;
     f.k = k;
     f.v = v;
     f.y = nullptr;
-    f.nodes = reinterpret_cast<float*>(fws + fl.nodes);
-    f.incl = reinterpret_cast<float*>(fws + fl.incl);
+    f.agg = reinterpret_cast<float*>(fws + fl.agg);
+    f.inc = reinterpret_cast<float*>(fws + fl.inc);
     f.flags = reinterpret_cast<uint64_t*>(fws + fl.flags);
     f.ticket = &hdr->ticket[1];  // counters stay in the outer header: its place never moves
+    f.exited = &hdr->exited[1];
     f.eh = hdr;
     f.g = g;
     f.epoch = next_epoch();
     f.budget_ns = budget;
     f.debug_skip_chunk = -1;
+    f.use_tma = make_tile_map(&f.tk, k, B, T, C, 4) && make_tile_map(&f.tv, v, B, T, C, 4);
     cudaError_t e = launch_forward(f, WKV_F32, false, s);
     if (e != cudaSuccess) return cuda_fail(e, "wkv_backward: state pass");
-    states = f.incl;
+    states = f.inc;
   }
 
   BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
   a.w = w;
   a.u = u;
   a.k = static_cast<const float*>(k);
@@ -255,24 +296,32 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
   a.ckpt = states;
   a.gk = gk;
   a.gv = gv;
-  a.rnodes = reinterpret_cast<float*>(bytes(workspace) + l.rnodes);
+  a.ragg = reinterpret_cast<float*>(bytes(workspace) + l.ragg);
+  a.rinc = reinterpret_cast<float*>(bytes(workspace) + l.rinc);
   a.part = reinterpret_cast<float*>(bytes(workspace) + l.part);
   a.flags = reinterpret_cast<uint64_t*>(bytes(workspace) + l.flags);
   a.ticket = &hdr->ticket[2];
+  a.exited = &hdr->exited[2];
   a.eh = hdr;
   a.g = g;
   a.epoch = next_epoch();
   a.budget_ns = budget;
   a.debug_skip_chunk = skip;
+  a.use_tma = make_tile_map(&a.tk, k, B, T, C, 4) && make_tile_map(&a.tv, v, B, T, C, 4) &&
+              make_tile_map(&a.tg, gy, B, T, C, 4);
   cudaError_t e = launch_backward(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
 
   ReduceArgs r;
   r.part = a.part;
+  r.slices = reinterpret_cast<float*>(bytes(workspace) + l.slices);
+  r.count = reinterpret_cast<unsigned long long*>(bytes(workspace) + l.count);
+  r.tag = (unsigned int)a.epoch;
   r.gw = gw;
   r.gu = gu;
   r.rows = g.nchunks * g.B;
   r.C = C;
+  r.nslice = l.nslice;
   e = launch_reduce(r, s);
   return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_backward: reduce");
 }

@@ -108,14 +108,19 @@ __device__ __forceinline__ float output(const State& s, float k, float v, float 
 }
 
 // x decayed over `decay` (= steps * w) followed by y: the associative combine
-// of chunk summaries (the decay is data independent, so a chunk's effect on
+// of chunk results (the decay is data independent, so a chunk's effect on
 // the carried state is "decay by its length, then add its own summary").
+// One exponential: the larger of the two scales gets exactly 1.  Written with
+// explicit fmaf so that every caller performs the same roundings (the
+// look-back relies on bitwise equal folds).
 __device__ __forceinline__ State combine(const State& x, float decay, const State& y) {
   const float px = x.pp - decay;
-  const float q = fmaxf(px, y.pp);
-  const float ex = exp_nat(px - q);
-  const float ey = exp_nat(y.pp - q);
-  return State{fmaf(ex, x.num, ey * y.num), fmaf(ex, x.den, ey * y.den), q};
+  const float d = px - y.pp;
+  const float e = exp_neg_abs(d);
+  const bool keep = d >= 0.f;
+  const float ex = keep ? 1.f : e;
+  const float ey = keep ? e : 1.f;
+  return State{fmaf(ex, x.num, ey * y.num), fmaf(ex, x.den, ey * y.den), keep ? px : y.pp};
 }
 
 // ------------------------------------------------------- memory ordering
@@ -147,29 +152,14 @@ __device__ __forceinline__ uint64_t flag_status(uint64_t word, uint64_t epoch) {
 // for other shapes (everything after the header is either epoch-tagged or
 // written before it is read within a call).
 struct WsHeader {
-  unsigned int ticket[4];    // dynamic tile counters, one per kind of launch (each reset by its last tile)
+  unsigned int ticket[4];    // dynamic tile counters, one per kind of launch
+  unsigned int exited[4];    // CTAs of that launch that have finished (the last one resets both)
   unsigned int error;        // first device error code since the last check, 0 if none
   unsigned int pad0;
   unsigned long long abort;  // epoch of the last launch that gave up a wait
-  unsigned int pad[56];
+  unsigned int pad[52];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
-
-// Takes a tile ticket for the CTA.  Tickets are handed out in the order CTAs
-// start, so a tile only ever waits on tiles whose CTAs are already running:
-// the waits below cannot deadlock however the hardware schedules CTAs.  The
-// grid has exactly ntiles CTAs, so the CTA that draws ntiles - 1 knows every
-// ticket is out and resets the counter for the next launch.
-__device__ __forceinline__ unsigned int take_ticket(unsigned int* counter, unsigned int ntiles) {
-  __shared__ unsigned int s_ticket;
-  if (threadIdx.x == 0) {
-    unsigned int t = atomicAdd(counter, 1u);
-    if (t == ntiles - 1) atomicExch(counter, 0u);
-    s_ticket = t;
-  }
-  __syncthreads();
-  return s_ticket;
-}
 
 // Records that this launch (epoch) gave up: the code for the host, the epoch
 // so the launch's other waits stop at once.
@@ -182,60 +172,55 @@ __device__ __forceinline__ void record_error(WsHeader* h, unsigned int code, uin
 
 namespace wkv {
 
-// Chunk summaries are combined across tiles through a binary-indexed
-// (Fenwick) tree over the chunk index.  Node (e, s) exists when
-// (e + 1) % 2^s == 0 and summarises the 2^s chunks ending at chunk e; node
-// (e, 0) is chunk e's own summary and node (e, s) = node (e - 2^{s-1}, s-1)
-// followed by node (e, s-1), computed and published by the tile of chunk e.
-// The prefix before chunk j is the fixed list of nodes given by the binary
-// digits of j (nearest first: end j-1 with level ctz(j), then strip the
-// lowest set bit and repeat).  Every tile therefore combines the same values
-// in the same order on every run (bitwise reproducible), waits on at most
-// popcount(j) nodes, and the longest chain of waits is log2(nchunks) hops.
-// The first ctz(~j) nodes of j's list are exactly the left children of the
-// nodes (j, 1..), so one wait serves both.
-
-// i-th node (0 = nearest) of the prefix list of chunk j: end chunk and level.
-__device__ __forceinline__ void fenwick_node(int j, int i, int& end, int& level) {
-  int x = j;
-  for (int q = 0; q < i; ++q) x &= x - 1;
-  level = __ffs(x) - 1;
-  end = x - 1;
-}
-
-// Index of node (end, level) in the node arrays (levels stored one after
-// the other; level s holds nchunks >> s nodes).
-__device__ __forceinline__ int node_index(const int* level_off, int end, int level) {
-  return level_off[level] + ((end + 1) >> level) - 1;
-}
-
-constexpr uint64_t kNodeReady = 1;  // flag status: node data published
-constexpr uint64_t kNodeErr = 3;    // flag status: producer gave up
+// ------------------------------------------------------------ look-back
+// Chunk results are passed between tiles through per-(chunk, row, 32-channel
+// group) flags.  A tile first publishes its chunk's own summary (kAgg), and
+// once it knows the result carried into its chunk, the inclusive result
+// (kIncl).  A tile finds the result carried into its chunk by looking at its
+// neighbours in scan order: the nearest one with an inclusive record, whose
+// value it then folds forward through the summaries of the chunks in
+// between, oldest first.  The fold is a left fold in a fixed order, the same
+// one the chain of inclusive records follows, so every tile obtains the same
+// bits whichever neighbour it found first: results are reproducible.
+constexpr uint64_t kAgg = 1;   // flag status: chunk summary published
+constexpr uint64_t kIncl = 2;  // flag status: inclusive result published
+constexpr uint64_t kErr = 3;   // flag status: producer gave up
 
 constexpr int kWaitOk = 0;
 constexpr int kWaitTimeout = 1;
 constexpr int kWaitError = 2;
 
-// Waits (one warp) until the n <= 32 flags flag_of(0..n-1) are published in
-// this launch's epoch.  Lane i polls flag i, so all waits overlap.  Bounded:
-// past budget_ns of %globaltimer returns kWaitTimeout; a producer that gave
-// up, or an expired wait anywhere in the same launch (h->abort == epoch),
-// gives kWaitError, so one expired wait ends every other wait at once.  The warp barrier after a
-// successful wait orders the acquiring loads before every lane's reads of
+// Waits (one warp) until, among the nwin <= 32 neighbours whose flags are
+// flag_at(0) (nearest) .. flag_at(nwin - 1), the nearest one with an
+// inclusive record is known and every nearer one has published its summary.
+// Sets `base` to that neighbour's index.  Lane i polls neighbour i, so all
+// polls overlap.  Bounded: past budget_ns of %globaltimer returns
+// kWaitTimeout; a neighbour that gave up, or an expired wait anywhere in the
+// same launch (h->abort == epoch), gives kWaitError.  The warp barrier after
+// a successful wait orders the acquiring loads before every lane's reads of
 // the published data.
-template <class FlagOf>
-__device__ __forceinline__ int wait_flags(FlagOf flag_of, int n, uint64_t epoch, uint64_t budget_ns,
-                                          const WsHeader* h) {
+template <class FlagAt>
+__device__ __forceinline__ int lookback_wait(FlagAt flag_at, int nwin, uint64_t epoch, uint64_t budget_ns,
+                                             const WsHeader* h, int& base) {
   const unsigned full = 0xffffffffu;
   const int lane = threadIdx.x & 31;
-  const uint64_t* fp = lane < n ? flag_of(lane) : nullptr;
-  uint64_t st = lane < n ? 0 : kNodeReady;
+  const uint64_t* fp = lane < nwin ? flag_at(lane) : nullptr;
+  uint64_t st = 0;
   uint64_t t0 = 0;
   bool timing = false;
   while (true) {
-    if (st == 0) st = flag_status(ld_acquire(fp), epoch);
-    if (__any_sync(full, st == kNodeErr)) return kWaitError;
-    if (__all_sync(full, st != 0)) break;
+    if (fp != nullptr && st != kIncl) st = flag_status(ld_acquire(fp), epoch);
+    if (__any_sync(full, st == kErr)) return kWaitError;
+    const unsigned incl = __ballot_sync(full, st == kIncl);
+    const unsigned rdy = __ballot_sync(full, st != 0);
+    if (incl != 0u) {
+      const int f = __ffs(incl) - 1;
+      const unsigned need = (1u << f) - 1u;
+      if ((rdy & need) == need) {
+        base = f;
+        break;
+      }
+    }
     if (__shfl_sync(full, *(volatile const unsigned long long*)&h->abort, 0) == epoch) return kWaitError;
     const uint64_t now = __shfl_sync(full, globaltimer(), 0);
     if (!timing) {
@@ -244,7 +229,7 @@ __device__ __forceinline__ int wait_flags(FlagOf flag_of, int n, uint64_t epoch,
     } else if (now - t0 > budget_ns) {
       return kWaitTimeout;
     }
-    __nanosleep(64);
+    __nanosleep(32);
   }
   __syncwarp();
   return kWaitOk;

@@ -2,6 +2,7 @@
 // Not part of the public ABI (that is include/wkv.h).
 #pragma once
 
+#include <cuda.h>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -14,43 +15,47 @@ struct WsHeader;
 // chunk-boundary states written by the forward pass line up with the chunks
 // of the backward pass.
 constexpr int kChunk = 32;
-// Channels per CTA of the scan kernels (4 warps x 32 lanes, one channel per
-// lane).
+// Channels per tile of the scan kernels (4 consumer warps x 32 lanes, one
+// channel per lane).
 constexpr int kCtaChannels = 128;
 
 struct ScanGeometry {
   int B, T, C;
-  int nchunks;   // ceil(T / kChunk)
-  int ncb;       // ceil(C / kCtaChannels): channel blocks (CTAs) per (chunk, row)
-  int nwg;       // ncb * 4: 32-channel groups per row (one flag each per node)
+  int nchunks;          // ceil(T / kChunk)
+  int ncb;              // ceil(C / kCtaChannels): channel blocks per (chunk, row)
+  int nwg;              // ncb * 4: 32-channel groups per row (one flag each per chunk)
   unsigned int ntiles;  // nchunks * B * ncb
-  size_t plane;  // nchunks * B * C: floats per checkpoint plane
-  int nnodes;    // nodes of the binary-indexed tree over chunks
-  int nlevels;   // levels of that tree (level s holds nchunks >> s nodes)
-  int level_off[32];
-  size_t nplane; // nnodes * B * C: floats per node plane
+  size_t plane;         // nchunks * B * C: floats per record plane
 };
 
 ScanGeometry make_geometry(int B, int T, int C);
 
+// Forward scan.  Records [3][nchunks][B][C] hold states (num, den, pp).
 struct FwdArgs {
+  CUtensorMap tk, tv;  // rank-3 maps {C, T, B} of k and v, box {128, kChunk, 1} (when use_tma)
   const float* w;
   const float* u;
   const void* k;
   const void* v;
-  float* y;          // may be null (state-only pass)
-  float* nodes;      // [3][nnodes][B][C] tree nodes: (num, den, pp)
-  float* incl;       // [3][nchunks][B][C] state after each chunk (checkpoints)
-  uint64_t* flags;   // [B][nwg][nnodes]
-  unsigned int* ticket;   // tile counter of this launch (in a workspace header)
-  WsHeader* eh;           // where an expired wait is recorded (checked by the host)
+  float* y;            // may be null (state-only pass)
+  float* agg;          // chunk summaries (each chunk from the empty state)
+  float* inc;          // state after each chunk (the checkpoints)
+  uint64_t* flags;     // [nchunks][B][nwg]
+  unsigned int* ticket;  // tile counter of this launch (in a workspace header)
+  unsigned int* exited;  // CTAs of this launch that have finished
+  WsHeader* eh;          // where an expired wait is recorded (checked by the host)
   ScanGeometry g;
   uint64_t epoch;
   uint64_t budget_ns;
   int debug_skip_chunk;  // -1: off
+  int use_tma;
 };
 
+// Backward scan.  Adjoint records [3][nchunks][B][C] hold (la, lb, f): the
+// adjoints of the sums a, b at a chunk's first token, scaled by e^{f}, with f
+// the forward state's pp there.
 struct BwdArgs {
+  CUtensorMap tk, tv, tg;  // rank-3 maps of k, v, gy (when use_tma)
   const float* w;
   const float* u;
   const float* k;
@@ -59,23 +64,30 @@ struct BwdArgs {
   const float* ckpt;   // [3][nchunks][B][C] state after each chunk (forward)
   float* gk;
   float* gv;
-  float* rnodes;       // [3][nnodes][B][C] tree nodes of the adjoint: (la, lb, exponent)
+  float* ragg;         // zero-carry adjoint of each chunk
+  float* rinc;         // adjoint at each chunk's start with everything after it
   float* part;         // [2][nchunks][B][C] per-tile gw, gu partial sums
-  uint64_t* flags;     // [B][nwg][nnodes]
+  uint64_t* flags;     // [nchunks][B][nwg]
   unsigned int* ticket;
+  unsigned int* exited;
   WsHeader* eh;
   ScanGeometry g;
   uint64_t epoch;
   uint64_t budget_ns;
   int debug_skip_chunk;
+  int use_tma;
 };
 
 struct ReduceArgs {
-  const float* part;  // [2][rows][C]
+  const float* part;    // [2][rows][C]
+  float* slices;        // [nslice][2][C] per-slice sums
+  unsigned long long* count;  // [ceil(C / 32)] arrival counters, (tag << 32) | arrivals
+  unsigned int tag;           // this launch's tag: a counter with another tag reads as zero
   float* gw;
   float* gu;
-  int rows;           // nchunks * B
+  int rows;             // nchunks * B
   int C;
+  int nslice;           // row slices (blockIdx.y)
 };
 
 struct DecodeArgs {
@@ -87,9 +99,20 @@ struct DecodeArgs {
 // Sets the text returned by wkv_last_error_string() on this thread.
 void set_last_error(const char* msg);
 
-cudaError_t launch_forward(const FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
-cudaError_t launch_backward(const BwdArgs& a, cudaStream_t s);
+// Rank-3 TMA descriptor of a [B, T, C] tensor with a {128, kChunk, 1} box
+// (elem_bytes 4 = fp32, 2 = bf16).  False when TMA cannot address it (the
+// base not 16-byte aligned or C * elem_bytes not a multiple of 16) or the
+// driver has no encoder; the kernels then stage tiles with plain loads.
+bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int elem_bytes);
+
+// Grid of a persistent scan kernel: resident CTAs per SM x SMs, at most ntiles.
+cudaError_t launch_forward(FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
+cudaError_t launch_backward(BwdArgs& a, cudaStream_t s);
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, bool vec4, cudaStream_t s);
+
+// Row slices of the gw/gu reduction for `rows` partial rows over C channels
+// (a function of the shape only, so the summation order is fixed).
+int reduce_slices(int rows, int C);
 
 }  // namespace wkv
