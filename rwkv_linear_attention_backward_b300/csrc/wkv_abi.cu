@@ -39,45 +39,44 @@ bool sizes_ok(int B, int T, int C) {
   return (double)g.nchunks * g.B * g.ncb <= (double)INT_MAX;
 }
 
-// Forward workspace: header (tile counters, error record) | flags
-// [nchunks][B][nwg] u64 | chunk summaries [3][nchunks][B][C] f32 |
-// checkpoints [3][nchunks][B][C] f32 (used when the caller passes none).
+// Forward workspace: header (tile counters, error record) | chunk summaries
+// [nchunks][B][C] tagged 16-byte records | carried states [nchunks][B][C]
+// records | checkpoints [3][nchunks][B][C] f32 (used when the caller passes
+// none).
 struct FwdLayout {
-  size_t flags, agg, inc, total;
+  size_t agg, inc, ckpt, total;
 };
 
 FwdLayout fwd_layout(const ScanGeometry& g) {
   FwdLayout l;
   size_t off = sizeof(WsHeader);
-  l.flags = off;
-  off += align256((size_t)g.nchunks * g.B * g.nwg * sizeof(uint64_t));
   l.agg = off;
-  off += align256(3 * g.plane * sizeof(float));
+  off += align256(g.plane * sizeof(Rec));
   l.inc = off;
+  off += align256(g.plane * sizeof(Rec));
+  l.ckpt = off;
   off += align256(3 * g.plane * sizeof(float));
   l.total = off;
   return l;
 }
 
-// Backward workspace: header | flags [nchunks][B][nwg] u64 | adjoint
-// records, zero-carry and inclusive, [3][nchunks][B][C] f32 each | gw, gu
-// partials [2][nchunks][B][C] f32 | reduction slices [nslice][2][C] f32 |
-// launch-tagged reduction counters [ceil(C/32)] u64 | a forward workspace
-// for recomputing the checkpoints when none are given.
+// Backward workspace: header | adjoint records, zero-carry and carried,
+// [nchunks][B][C] tagged 16-byte records each | gw, gu partials [2][nchunks][B][C]
+// f32 | reduction slices [nslice][2][C] f32 | launch-tagged reduction
+// counters [ceil(C/32)] u64 | a forward workspace for recomputing the
+// checkpoints when none are given.
 struct BwdLayout {
-  size_t flags, ragg, rinc, part, slices, count, fwd, total;
+  size_t ragg, rinc, part, slices, count, fwd, total;
   int nslice;
 };
 
 BwdLayout bwd_layout(const ScanGeometry& g) {
   BwdLayout l;
   size_t off = sizeof(WsHeader);
-  l.flags = off;
-  off += align256((size_t)g.nchunks * g.B * g.nwg * sizeof(uint64_t));
   l.ragg = off;
-  off += align256(3 * g.plane * sizeof(float));
+  off += align256(g.plane * sizeof(Rec));
   l.rinc = off;
-  off += align256(3 * g.plane * sizeof(float));
+  off += align256(g.plane * sizeof(Rec));
   l.part = off;
   off += align256(2 * g.plane * sizeof(float));
   l.nslice = reduce_slices(g.nchunks * g.B, g.C);
@@ -92,6 +91,9 @@ BwdLayout bwd_layout(const ScanGeometry& g) {
 }
 
 uint64_t next_epoch() { return g_epoch.fetch_add(1) + 1; }
+
+// Record tag of a launch: never 0 (the tag of a zero-filled workspace).
+uint32_t tag_of(uint64_t epoch) { return (uint32_t)((epoch - 1) % 0xFFFFFFFFull) + 1u; }
 
 char* bytes(void* p) { return static_cast<char*>(p); }
 
@@ -108,7 +110,7 @@ ScanGeometry make_geometry(int B, int T, int C) {
   g.C = C;
   g.nchunks = (T + kChunk - 1) / kChunk;
   g.ncb = (C + kCtaChannels - 1) / kCtaChannels;
-  g.nwg = g.ncb * (kCtaChannels / 32);
+  g.nwg = (C + 31) / 32;
   g.ntiles = (unsigned int)((size_t)g.nchunks * B * g.ncb);
   g.plane = (size_t)g.nchunks * B * C;
   return g;
@@ -227,14 +229,15 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
   a.k = k;
   a.v = v;
   a.y = y;
-  a.agg = reinterpret_cast<float*>(bytes(workspace) + l.agg);
-  a.inc = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.inc);
-  a.flags = reinterpret_cast<uint64_t*>(bytes(workspace) + l.flags);
+  a.agg = reinterpret_cast<Rec*>(bytes(workspace) + l.agg);
+  a.inc = reinterpret_cast<Rec*>(bytes(workspace) + l.inc);
+  a.ckpt = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.ckpt);
   a.eh = static_cast<WsHeader*>(workspace);
   a.ticket = &a.eh->ticket[0];
   a.exited = &a.eh->exited[0];
   a.g = g;
   a.epoch = next_epoch();
+  a.tag = tag_of(a.epoch);
   a.budget_ns = (uint64_t)g_budget_ns.load();
   a.debug_skip_chunk = g_skip_chunk.load();
   const int eb = kv_dtype == WKV_F32 ? 4 : 2;
@@ -270,20 +273,21 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
     f.k = k;
     f.v = v;
     f.y = nullptr;
-    f.agg = reinterpret_cast<float*>(fws + fl.agg);
-    f.inc = reinterpret_cast<float*>(fws + fl.inc);
-    f.flags = reinterpret_cast<uint64_t*>(fws + fl.flags);
+    f.agg = reinterpret_cast<Rec*>(fws + fl.agg);
+    f.inc = reinterpret_cast<Rec*>(fws + fl.inc);
+    f.ckpt = reinterpret_cast<float*>(fws + fl.ckpt);
     f.ticket = &hdr->ticket[1];  // counters stay in the outer header: its place never moves
     f.exited = &hdr->exited[1];
     f.eh = hdr;
     f.g = g;
     f.epoch = next_epoch();
+    f.tag = tag_of(f.epoch);
     f.budget_ns = budget;
     f.debug_skip_chunk = -1;
     f.use_tma = make_tile_map(&f.tk, k, B, T, C, 4) && make_tile_map(&f.tv, v, B, T, C, 4);
     cudaError_t e = launch_forward(f, WKV_F32, false, s);
     if (e != cudaSuccess) return cuda_fail(e, "wkv_backward: state pass");
-    states = f.inc;
+    states = f.ckpt;
   }
 
   BwdArgs a;
@@ -296,15 +300,15 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
   a.ckpt = states;
   a.gk = gk;
   a.gv = gv;
-  a.ragg = reinterpret_cast<float*>(bytes(workspace) + l.ragg);
-  a.rinc = reinterpret_cast<float*>(bytes(workspace) + l.rinc);
+  a.ragg = reinterpret_cast<Rec*>(bytes(workspace) + l.ragg);
+  a.rinc = reinterpret_cast<Rec*>(bytes(workspace) + l.rinc);
   a.part = reinterpret_cast<float*>(bytes(workspace) + l.part);
-  a.flags = reinterpret_cast<uint64_t*>(bytes(workspace) + l.flags);
   a.ticket = &hdr->ticket[2];
   a.exited = &hdr->exited[2];
   a.eh = hdr;
   a.g = g;
   a.epoch = next_epoch();
+  a.tag = tag_of(a.epoch);
   a.budget_ns = budget;
   a.debug_skip_chunk = skip;
   a.use_tma = make_tile_map(&a.tk, k, B, T, C, 4) && make_tile_map(&a.tv, v, B, T, C, 4) &&

@@ -18,17 +18,19 @@
 // tile is (chunk j, batch row b, 128 channels) with k, v, gy staged in
 // shared memory by the producer warp (wkv_pipe.cuh).  Per tile and lane:
 //
-//   1. the forward state before every token of the chunk, recomputed from
-//      the forward pass's checkpoint at the fixed scale e^{F}, F = max k of
-//      the chunk (a kept in shared memory in place of k, b in registers);
-//   2. reverse pass with a zero carry: gN per token (kept in shared memory
-//      in place of gy) and the chunk's own adjoint summary, published for
-//      the look-back (wkv_common.cuh);
-//   3. look-back over the later chunks: the adjoint carried into the chunk's
-//      end, and the inclusive record of this chunk;
-//   4. reverse pass with the carry: gk, gv, and this tile's partial sums of
-//      gw, gu; a second kernel adds the partials in a fixed order, so the
-//      result is deterministic.
+//   summary  the forward state from the forward pass's checkpoint at the
+//            fixed scale e^{F}, F = max k of the chunk; in the same forward
+//            sweep the chunk's zero-carry adjoint at its first token,
+//            la = sum_t e^{-(t-t0) w} gN_t (lb likewise with gD), published
+//            as a tagged record (ek = e^{k - F} is kept in place of k);
+//   finish   the adjoint carried into the chunk's end, from the walker; the
+//            forward states again (b in registers, a in registers), then the
+//            reverse pass with the carry: gk, gv, and this tile's partial
+//            sums of gw, gu (a second kernel adds the partials in a fixed
+//            order, so the result is deterministic).
+// Walker warps carry the adjoint along each chain from the last chunk:
+// X_j = zero-carry_j + e^{-Lw} X_{j+1}, a fold in a fixed order, written as
+// tagged records for the previous chunk's tiles.
 //
 // At the fixed scale e^{F} (la carried as la e^{F}), every factor is a plain
 // product: e^{u+k} = ek e^{u}, la e^{k} = (la e^{F}) ek, la a = (la e^{F})
@@ -46,6 +48,12 @@ namespace {
 constexpr int kBwdStages = 2;
 constexpr float kFastRange = 69.f;
 constexpr float kFastCeil = 60.f;
+constexpr int kWalkCap = 16;   // chains per walker whose state stays in shared memory
+constexpr int kWalkRing = 8;   // records requested together by a walker
+// walker shared memory (see bwd_walker)
+constexpr size_t kWalkSmem = (size_t)kWalkCap * (96 + 32 + 32) * sizeof(float) + (size_t)kWalkRing * 32 * 16;
+static_assert((kWalkCap * (96 + 32 + 32) * sizeof(float)) % 16 == 0, "the record ring must be 16-byte aligned");
+static_assert(2 * 3 * kChunk * kCtaChannels * 4 + kWalkSmem + 1024 <= 114 * 1024, "two backward CTAs per SM");
 
 // Everything the per-token reverse pass needs at one token, from the state
 // before it (running-maximum form).
@@ -91,23 +99,12 @@ __device__ __forceinline__ Adj fold_adj(const Adj& A, float Lw, const Adj& X) {
   return Adj{fmaf(e, X.la, A.la), fmaf(e, X.lb, A.lb), A.f};
 }
 
-__device__ __forceinline__ Adj load_adj(const float* rec, size_t plane, size_t o) {
-  return Adj{__ldcg(rec + o), __ldcg(rec + o + plane), __ldcg(rec + o + 2 * plane)};
-}
-
-__device__ __forceinline__ void store_adj(float* rec, size_t plane, size_t o, const Adj& x) {
-  rec[o] = x.la;
-  rec[o + plane] = x.lb;
-  rec[o + 2 * plane] = x.f;
-}
-
 // The per-token (running-maximum) form for lanes outside the fixed scale's
 // bounds.  Rare, so its loops stay rolled with the per-token states (num,
 // den, pp before each token) in local memory, leaving the fast form's
-// registers alone.  Pass 1: the states and the zero-carry adjoint at the chunk start,
-// scaled by e^{P.pp}.
-__device__ __forceinline__ void exact_prepass(const float* sk, const float* sv, const float* sg, int len, State s,
-                                           float w, float u, float* xa, float* xb, float* xp, float* out) {
+// registers alone.  The states from P; returns pp after the chunk.
+__device__ __forceinline__ float exact_states(const float* sk, const float* sv, int len, State s, float w,
+                                              float* xa, float* xb, float* xp) {
   constexpr int S = kCtaChannels;
 #pragma unroll 1
   for (int i = 0; i < len; ++i) {
@@ -116,23 +113,29 @@ __device__ __forceinline__ void exact_prepass(const float* sk, const float* sv, 
     xp[i] = s.pp;
     step(s, sk[i * S], sv[i * S], w);
   }
-  float la = 0.f, lb = 0.f;
+  return s.pp;
+}
+
+// The zero-carry adjoint at the chunk start, scaled by e^{pp there}.
+__device__ __forceinline__ void exact_zero_adjoint(const float* sk, const float* sv, const float* sg, int len,
+                                                   float w, float u, const float* xa, const float* xb,
+                                                   const float* xp, float& la, float& lb) {
+  constexpr int S = kCtaChannels;
+  la = 0.f;
+  lb = 0.f;
 #pragma unroll 1
   for (int i = len - 1; i >= 0; --i) {
     const Local o = local_terms(State{xa[i], xb[i], xp[i]}, sk[i * S], sv[i * S], sg[i * S], w, u);
     la = carry(o.t, la, o.gb);
     lb = carry(o.t, lb, -o.gb * o.y);
   }
-  out[0] = la;
-  out[1] = lb;
-  out[2] = s.pp;  // pp after the chunk
 }
 
-// Pass 2: gk, gv with the carry (la, lb, scaled by e^{pp after the chunk});
+// gk, gv with the carry (la, lb, scaled by e^{pp after the chunk});
 // out[0..1] receive the gw, gu partial sums.
-__device__ __forceinline__ void exact_final(const float* sk, const float* sv, const float* sg, int len, float w, float u,
-                                         const float* xa, const float* xb, const float* xp, float la, float lb,
-                                         float* gkp, float* gvp, int64_t C, bool valid, float* out) {
+__device__ __forceinline__ void exact_final(const float* sk, const float* sv, const float* sg, int len, float w,
+                                            float u, const float* xa, const float* xb, const float* xp, float la,
+                                            float lb, float* gkp, float* gvp, int64_t C, bool valid, float* out) {
   constexpr int S = kCtaChannels;
   float gw_acc = 0.f, gu_acc = 0.f;
 #pragma unroll 1
@@ -157,178 +160,257 @@ __device__ __forceinline__ void exact_final(const float* sk, const float* sv, co
   out[1] = gu_acc;
 }
 
-// One consumer warp's share (32 channels) of one tile.  The fast form also
-// writes into the stage: the forward sum a in place of k, gN in place of gy.
+// What a consumer lane keeps of a tile between its summary and its finish.
+struct BwdPend {
+  int j, b, c, len;
+  bool live;  // the warp has channels in this tile
+  bool fast;
+  float w, u, ew, eu, F, s0;
+  State P;
+};
+
+__device__ __forceinline__ void bwd_summary(const BwdArgs& a, float* __restrict__ sk, const float* __restrict__ sv,
+                                            const float* __restrict__ sg, BwdPend& p, float* xa, float* xb,
+                                            float* xp) {
+  constexpr int S = kCtaChannels;
+  const ScanGeometry& g = a.g;
+  const int cc = p.c < g.C ? p.c : g.C - 1;
+  p.P = empty_state();
+  if (p.j > 0) {
+    const size_t o = ((size_t)(p.j - 1) * g.B + p.b) * g.C + cc;
+    p.P = State{__ldg(a.ckpt + o), __ldg(a.ckpt + o + g.plane), __ldg(a.ckpt + o + 2 * g.plane)};
+  }
+  float F = -3.0e38f, kmin = 3.0e38f;
+#pragma unroll 8
+  for (int i = 0; i < p.len; ++i) {
+    const float k = sk[i * S];
+    F = fmaxf(F, k);
+    kmin = fminf(kmin, k);
+  }
+  p.F = F;
+  p.fast = (kmin + fminf(p.u, 0.f) >= F - kFastRange) && (p.u <= kFastCeil) && (p.P.pp - F <= kFastCeil);
+  float la, lb;
+  if (p.fast) {
+    // forward states at scale e^{F}; the zero-carry adjoint at the chunk
+    // start accumulates in the same sweep, each token's gN, gD weighted by
+    // e^{-(t - t0) w}
+    const float F2 = F * kLog2e;
+    p.s0 = exp_nat(p.P.pp - F);
+    float na = p.P.num * p.s0, nb = p.P.den * p.s0, pw = 1.f;
+    la = 0.f;
+    lb = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < p.len; ++i) {
+      const float ek = ex2(fmaf(sk[i * S], kLog2e, -F2));
+      sk[i * S] = ek;
+      const float vv = sv[i * S];
+      const float ec = ek * p.eu;
+      const float rr = rcp(nb + ec);
+      const float gi = sg[i * S] * rr;         // gN at scale e^{F}
+      const float y = fmaf(ec, vv, na) * rr;   // wkv_t
+      la = fmaf(pw, gi, la);
+      lb = fmaf(-pw, gi * y, lb);
+      pw *= p.ew;
+      na = fmaf(na, p.ew, ek * vv);
+      nb = fmaf(nb, p.ew, ek);
+    }
+    // from scale e^{F} to the record's scale e^{P.pp}
+    la *= p.s0;
+    lb *= p.s0;
+  } else {
+    exact_states(sk, sv, p.len, p.P, p.w, xa, xb, xp);
+    exact_zero_adjoint(sk, sv, sg, p.len, p.w, p.u, xa, xb, xp, la, lb);
+  }
+  if (p.j > 0 && p.j != a.debug_skip_chunk && p.c < g.C)  // chunk 0's adjoint is never needed
+    rec_store(a.ragg + ((size_t)p.j * g.B + p.b) * g.C + p.c, a.tag, la, lb, p.P.pp);
+}
+
+// gk, gv and the gw, gu partials of a tile, given the adjoint X carried
+// into its chunk's end (ignored for the last chunk).
 template <bool FULL>
-__device__ __forceinline__ void bwd_tile(const BwdArgs& a, float* sk, const float* sv, float* sg, int j, int b, int wg,
-                                         int c, int len) {
+__device__ __forceinline__ void bwd_finish(const BwdArgs& a, const float* __restrict__ sk,
+                                           const float* __restrict__ sv, const float* __restrict__ sg,
+                                           const BwdPend& p, const Adj& X, float* xa, float* xb, float* xp) {
   constexpr int L = kChunk;
   constexpr int S = kCtaChannels;
   const ScanGeometry& g = a.g;
-  const int lane = threadIdx.x & 31;
-  const bool valid = c < g.C;
-  const int cc = valid ? c : g.C - 1;
-  const float w = __ldg(a.w + cc);
-  const float u = __ldg(a.u + cc);
-  sk += lane;
-  sv += lane;
-  sg += lane;
-  const size_t P3 = g.plane;
-  const size_t jstride = (size_t)g.B * g.C;
-  const size_t row = (size_t)b * g.C + cc;
-  const size_t slot = (size_t)j * jstride + row;
-
-  State P = empty_state();
-  if (j > 0) {
-    const size_t o = (size_t)(j - 1) * jstride + row;
-    P = State{__ldg(a.ckpt + o), __ldg(a.ckpt + o + P3), __ldg(a.ckpt + o + 2 * P3)};
-  }
-
-  float kr[L];
-  float F = -3.0e38f, kmin = 3.0e38f;
-#pragma unroll
-  for (int i = 0; i < L; ++i) {
-    if (FULL || i < len) {
-      kr[i] = sk[i * S];
-      F = fmaxf(F, kr[i]);
-      kmin = fminf(kmin, kr[i]);
-    }
-  }
-  const float ew = expf(-w);
-  const float eu = expf(u);
-  const bool fast = (kmin + fminf(u, 0.f) >= F - kFastRange) && (u <= kFastCeil) && (P.pp - F <= kFastCeil);
-
-  float Bd[L];                // fast form: forward sum b before each token at scale e^{F}
-  float xa[L], xb[L], xp[L];  // per-token form: (num, den, pp) before each token (local memory)
-  float la = 0.f, lb = 0.f;
-  float pp_end = 0.f;
-  float s0 = 0.f;
-  if (fast) {
-    // 1. forward states at scale e^{F}: b in registers, a in place of k
-    const float F2 = F * kLog2e;
-    s0 = exp_nat(P.pp - F);
-    float na = P.num * s0, nb = P.den * s0;
+  const bool valid = p.c < g.C;
+  const size_t slot = ((size_t)p.j * g.B + p.b) * g.C + (valid ? p.c : g.C - 1);
+  const bool has_succ = p.j < g.nchunks - 1;
+  float gw_acc = 0.f, gu_acc = 0.f;
+  float* __restrict__ gkp = a.gk + ((int64_t)p.b * g.T + (int64_t)p.j * L) * g.C + p.c;
+  float* __restrict__ gvp = a.gv + ((int64_t)p.b * g.T + (int64_t)p.j * L) * g.C + p.c;
+  if (p.fast) {
+    // forward sums before each token at scale e^{F}, from the stored ek
+    float A[L], Bd[L];
+    float na = p.P.num * p.s0, nb = p.P.den * p.s0;
 #pragma unroll
     for (int i = 0; i < L; ++i) {
-      if (FULL || i < len) {
-        const float ek = ex2(fmaf(kr[i], kLog2e, -F2));
-        kr[i] = ek;
+      if (FULL || i < p.len) {
+        const float ek = sk[i * S];
         const float vv = sv[i * S];
-        sk[i * S] = na;
+        A[i] = na;
         Bd[i] = nb;
-        na = fmaf(na, ew, ek * vv);
-        nb = fmaf(nb, ew, ek);
+        na = fmaf(na, p.ew, ek * vv);
+        nb = fmaf(nb, p.ew, ek);
       }
     }
-    // 2. reverse pass with a zero carry; gN kept in place of gy
+    // reverse pass with the carry (at scale e^{F})
+    const float f = has_succ ? exp_nat(p.F - X.f) : 0.f;
+    float la = X.la * f, lb = X.lb * f;
 #pragma unroll
     for (int i = L - 1; i >= 0; --i) {
-      if (FULL || i < len) {
-        const float ek = kr[i];
+      if (FULL || i < p.len) {
+        const float ek = sk[i * S];
         const float vv = sv[i * S];
-        const float ai = sk[i * S];
-        const float rr = rcp(fmaf(ek, eu, Bd[i]));
-        const float gi = sg[i * S] * rr;             // gN at scale e^{F}
-        const float vmy = fmaf(vv, Bd[i], -ai) * rr;  // v - wkv
-        sg[i * S] = gi;
-        la = fmaf(la, ew, gi);
-        lb = fmaf(lb, ew, -gi * (vv - vmy));
-      }
-    }
-    // from scale e^{F} to the record's scale e^{P.pp}
-    la *= s0;
-    lb *= s0;
-  } else {
-    float res[3];
-    exact_prepass(sk, sv, sg, len, P, w, u, xa, xb, xp, res);
-    la = res[0];
-    lb = res[1];
-    pp_end = res[2];
-  }
-
-  const float Lw = (float)L * w;
-  const Adj own{la, lb, P.pp};
-  uint64_t* flag = a.flags + ((size_t)j * g.B + b) * g.nwg + wg;
-  const bool has_pred = j > 0;
-  const bool has_succ = j < g.nchunks - 1;
-  const bool skip = j == a.debug_skip_chunk;  // fault injection: this tile never publishes
-
-  // 3. look-back over the later chunks
-  Adj X{0.f, 0.f, 0.f};
-  if (has_succ) {
-    if (has_pred && !skip) {
-      if (valid) store_adj(a.ragg, P3, slot, own);
-      publish(flag, a.epoch, kAgg);
-    }
-    const int nwin = min(g.nchunks - 1 - j, 32);
-    int base = 0;
-    const int rc = lookback_wait(
-        [&](int i) { return a.flags + ((size_t)(j + 1 + i) * g.B + b) * g.nwg + wg; }, nwin, a.epoch, a.budget_ns,
-        a.eh, base);
-    if (rc != kWaitOk) {
-      if (rc == kWaitTimeout && lane == 0) record_error(a.eh, kDevErrTimeout, a.epoch);
-      if (has_pred && !skip) publish(flag, a.epoch, kErr);
-      return;
-    }
-    X = load_adj(a.rinc, P3, (size_t)(j + 1 + base) * jstride + row);
-    // fold the records of chunks j + base .. j + 1, the furthest first
-    for (int i = base - 1; i >= 0; i -= 4) {
-      Adj q[4];
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        if (i - m >= 0) q[m] = load_adj(a.ragg, P3, (size_t)(j + 1 + (i - m)) * jstride + row);
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        if (i - m >= 0) X = fold_adj(q[m], Lw, X);
-    }
-  }
-  if (has_pred && !skip) {
-    const Adj incl = has_succ ? fold_adj(own, Lw, X) : own;
-    if (valid) store_adj(a.rinc, P3, slot, incl);
-    publish(flag, a.epoch, kIncl);
-  }
-
-  // 4. reverse pass with the carry
-  float gw_acc = 0.f, gu_acc = 0.f;
-  float* gkp = a.gk + ((int64_t)b * g.T + (int64_t)j * L) * g.C + cc;
-  float* gvp = a.gv + ((int64_t)b * g.T + (int64_t)j * L) * g.C + cc;
-  if (fast) {
-    const float f = has_succ ? exp_nat(F - X.f) : 0.f;
-    la = X.la * f;
-    lb = X.lb * f;
-#pragma unroll
-    for (int i = L - 1; i >= 0; --i) {
-      if (FULL || i < len) {
-        const float ek = kr[i];
-        const float vv = sv[i * S];
-        const float gi = sg[i * S];
-        const float ai = sk[i * S];
-        const float ec = ek * eu;
-        const float vmy = fmaf(vv, Bd[i], -ai) * rcp(Bd[i] + ec);  // v - wkv
-        const float cur = gi * vmy * ec;  // (gN v + gD) e^{u+k}
+        const float ec = ek * p.eu;
+        const float rr = rcp(Bd[i] + ec);
+        const float gi = sg[i * S] * rr;
+        const float vmy = fmaf(vv, Bd[i], -A[i]) * rr;  // v - wkv
+        const float cur = gi * vmy * ec;                // (gN v + gD) e^{u+k}
         const float gk = fmaf(fmaf(la, vv, lb), ek, cur);
         const float gv = fmaf(gi, ec, la * ek);
         gu_acc += cur;
-        gw_acc = fmaf(la, ai, fmaf(lb, Bd[i], gw_acc));
-        la = fmaf(la, ew, gi);
-        lb = fmaf(lb, ew, -gi * (vv - vmy));
+        gw_acc = fmaf(la, A[i], fmaf(lb, Bd[i], gw_acc));
+        la = fmaf(la, p.ew, gi);
+        lb = fmaf(lb, p.ew, -gi * (vv - vmy));
         if (valid) {
           __stcs(gkp + (int64_t)i * g.C, gk);
           __stcs(gvp + (int64_t)i * g.C, gv);
         }
       }
     }
-    gw_acc *= -ew;
+    gw_acc *= -p.ew;
   } else {
+    const float pp_end = exact_states(sk, sv, p.len, p.P, p.w, xa, xb, xp);
     const float f = has_succ ? exp_nat(pp_end - X.f) : 0.f;
     float res[2];
-    exact_final(sk, sv, sg, len, w, u, xa, xb, xp, X.la * f, X.lb * f, gkp, gvp, g.C, valid, res);
+    exact_final(sk, sv, sg, p.len, p.w, p.u, xa, xb, xp, X.la * f, X.lb * f, gkp, gvp, g.C, valid, res);
     gw_acc = res[0];
     gu_acc = res[1];
   }
   if (valid) {
     a.part[slot] = gw_acc;
-    a.part[slot + P3] = gu_acc;
+    a.part[slot + g.plane] = gu_acc;
+  }
+}
+
+// The walkers (see the forward pass): walker x owns the chains q = x + m *
+// gridDim.x and takes them chunk by chunk from the last chunk (for each
+// chunk, each of its chains).  Chunk 0's adjoint is never needed, so chunks
+// nchunks-1 .. 1.  Walker shared memory, per chain qi < kWalkCap: adjoint
+// [3][32] f32 (la, lb, f), chunk decay L*w [32] f32, this lane's element
+// offset [32] i32 (bit 31 set when the lane's channel is past C); then the
+// record ring [kWalkRing][32].
+__device__ __forceinline__ float* walk_state(float* pst, int qi) { return pst + qi * 96; }
+__device__ __forceinline__ float* walk_w(float* pst) { return pst + kWalkCap * 96; }
+__device__ __forceinline__ int* walk_off(float* pst) { return reinterpret_cast<int*>(pst + kWalkCap * 128); }
+
+__device__ __noinline__ int walk_off_slow(const ScanGeometry& g, int qi) {
+  const int q = (int)blockIdx.x + qi * (int)gridDim.x;
+  const int b = q / g.nwg;
+  const int c = (q - b * g.nwg) * 32 + (int)(threadIdx.x & 31);
+  return c < g.C ? b * g.C + c : (b * g.C + g.C - 1) | (int)0x80000000;
+}
+
+__device__ __forceinline__ int walk_offset(const ScanGeometry& g, float* pst, int mq, int qi) {
+  return mq <= kWalkCap ? walk_off(pst)[qi * 32 + (threadIdx.x & 31)] : walk_off_slow(g, qi);
+}
+
+// One item: the adjoint at the start of chunk j of chain qi from the chunk's
+// zero-carry record s and the adjoint at the start of chunk j + 1.  Kept
+// out of line so that the walker's code stays small.
+__device__ __noinline__ void bwd_walk_item(const BwdArgs& a, float* pst, int mq, int j, int qi, Rec s) {
+  const ScanGeometry& g = a.g;
+  const int lane = threadIdx.x & 31;
+  const int eo = walk_offset(g, pst, mq, qi);
+  const bool valid = eo >= 0;
+  const size_t o = (size_t)j * g.B * g.C + (eo & 0x7fffffff);
+  const bool in_smem = mq <= kWalkCap;
+  float* ps = walk_state(pst, qi) + lane;
+  Adj X{rec_x(s), rec_y(s), rec_z(s)};
+  if (j < g.nchunks - 1) {
+    Adj nx;
+    if (in_smem) {
+      nx = Adj{ps[0], ps[32], ps[64]};
+    } else {
+      const Rec r = rec_load(a.rinc + o + (size_t)g.B * g.C);  // written by this lane mq items ago
+      nx = Adj{rec_x(r), rec_y(r), rec_z(r)};
+    }
+    const float Lw = in_smem ? walk_w(pst)[qi * 32 + lane] : (float)kChunk * __ldg(a.w + (eo & 0x7fffffff) % g.C);
+    X = fold_adj(X, Lw, nx);
+  }
+  if (valid) rec_store(a.rinc + o, a.tag, X.la, X.lb, X.f);
+  if (in_smem) {
+    ps[0] = X.la;
+    ps[32] = X.lb;
+    ps[64] = X.f;
+  }
+}
+
+__device__ __forceinline__ void bwd_walker(const BwdArgs& a, float* pst) {
+  const ScanGeometry& g = a.g;
+  const int lane = threadIdx.x & 31;
+  const int nchain = g.B * g.nwg;
+  const int x = blockIdx.x, G = gridDim.x;
+  if (x >= nchain || g.nchunks < 2) return;
+  const int mq = (nchain - 1 - x) / G + 1;
+  const bool in_smem = mq <= kWalkCap;
+  const long nitems = (long)(g.nchunks - 1) * mq;
+  const size_t jstride = (size_t)g.B * g.C;
+  if (in_smem) {
+    for (int qi = 0; qi < mq; ++qi) {
+      const int eo = walk_off_slow(g, qi);
+      walk_off(pst)[qi * 32 + lane] = eo;
+      walk_w(pst)[qi * 32 + lane] = (float)kChunk * __ldg(a.w + (eo & 0x7fffffff) % g.C);
+    }
+  }
+  Rec* ring = reinterpret_cast<Rec*>(walk_off(pst) + kWalkCap * 32);  // [kWalkRing][32]
+  __syncwarp();
+  const uint32_t tag = a.tag;
+  // Blocks of kWalkRing items, as in the forward walker.
+  int bj = g.nchunks - 1, bq = 0;  // first item of the block
+  for (long base = 0; base < nitems; base += kWalkRing) {
+    const int nb = (int)min((long)kWalkRing, nitems - base);
+    int done = 0, cj = bj, cq = bq;
+    bool first = true;
+    uint64_t t0 = globaltimer();
+    while (done < nb) {
+      int j = cj, qi = cq;
+      for (int r = done; r < nb; ++r) {
+        Rec* slot = ring + r * 32 + lane;
+        if (first || !rec_ok(*slot, tag))
+          cp_async16(slot, a.ragg + (size_t)j * jstride + (walk_offset(g, pst, mq, qi) & 0x7fffffff));
+        if (++qi == mq) {
+          qi = 0;
+          --j;
+        }
+      }
+      cp_async_wait_all();
+      __syncwarp();
+      first = false;
+      const int before = done;
+      for (; done < nb; ++done) {
+        const Rec rr = ring[done * 32 + lane];
+        if (!__all_sync(0xffffffffu, walk_offset(g, pst, mq, cq) < 0 || rec_ok(rr, tag))) break;
+        bwd_walk_item(a, pst, mq, cj, cq, rr);
+        if (++cq == mq) {
+          cq = 0;
+          --cj;
+        }
+      }
+      if (done > before) {
+        t0 = globaltimer();
+        continue;
+      }
+      if (__shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == a.epoch) return;
+      if (__shfl_sync(0xffffffffu, globaltimer(), 0) - t0 > a.budget_ns) {
+        if (lane == 0) record_error(a.eh, kDevErrTimeout, a.epoch);
+        return;
+      }
+    }
+    bj = cj;
+    bq = cq;
   }
 }
 
@@ -338,6 +420,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) bwd_scan_kernel(const __grid_
   extern __shared__ __align__(1024) unsigned char smem[];
   float* stages = reinterpret_cast<float*>(smem);  // stage s: k, v, gy at (3s + 0..2) * TILE
   auto* ctl = reinterpret_cast<PipeCtl<NS>*>(smem + (size_t)NS * 3 * TILE * sizeof(float));
+  // walker shared memory (kWalkSmem bytes), 128-byte aligned
+  float* pst = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(ctl) + pipe_ctl_bytes<NS>());
   pipe_init(ctl);
   const ScanGeometry& g = a.g;
   const int warp = threadIdx.x >> 5;
@@ -371,39 +455,99 @@ __global__ void __launch_bounds__(kPipeThreads, 2) bwd_scan_kernel(const __grid_
                                           kChunk);
                         }
                       });
+  } else if (warp == kWalkerWarp) {
+    bwd_walker(a, pst);
   } else {
-    int s = 0;
-    uint32_t phase = 0;
+    // Consumer: a tile is summarised as soon as its stage lands, and the
+    // oldest summarised tile is finished once its carried adjoint is
+    // published; neither step blocks the other (see the forward kernel).
+    float xa[kChunk], xb[kChunk], xp[kChunk];  // per-token form's states (local memory)
+    BwdPend pend[NS];                           // per stage (local memory)
+    int ns = 0, nf = 0, count = 0;
+    uint32_t ps = 0;
+    bool end = false, failed = false, idle = false;
+    uint64_t idle_since = 0;
     while (true) {
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl->full[s], phase, a.budget_ns));
-      if (!ok) {
-        if (lane == 0) pipe_fail(ctl, a.eh, kDevErrTimeout, a.epoch);
-        break;
+      bool progress = false;
+      while (!end && count < NS && __all_sync(0xffffffffu, mbar_test(&ctl->full[ns], ps))) {
+        const int t = *(volatile int*)&ctl->tile[ns];
+        if (t < 0) {
+          end = true;
+          break;
+        }
+        BwdPend p;  // in registers while in use; parked in pend[] between summary and finish
+        const int jr = t / per_j;
+        const int rem = t - jr * per_j;
+        p.j = g.nchunks - 1 - jr;
+        p.b = rem / g.ncb;
+        const int cb = rem - p.b * g.ncb;
+        const int c0 = cb * kCtaChannels + warp * 32;
+        p.live = c0 < g.C;
+        p.c = c0 + lane;
+        p.len = min(kChunk, g.T - p.j * kChunk);
+        if (p.live && !failed) {
+          const int cc = p.c < g.C ? p.c : g.C - 1;
+          p.w = __ldg(a.w + cc);
+          p.u = __ldg(a.u + cc);
+          p.ew = expf(-p.w);
+          p.eu = expf(p.u);
+          float* sk = stages + (size_t)(3 * ns) * TILE + warp * 32 + lane;
+          bwd_summary(a, sk, sk + TILE, sk + 2 * TILE, p, xa, xb, xp);
+        }
+        pend[ns] = p;
+        ++count;
+        if (++ns == NS) {
+          ns = 0;
+          ps ^= 1u;
+        }
+        progress = true;
       }
-      const int t = *(volatile int*)&ctl->tile[s];
-      if (t < 0) break;
-      const int jr = t / per_j;
-      const int j = g.nchunks - 1 - jr;
-      const int rem = t - jr * per_j;
-      const int b = rem / g.ncb;
-      const int cb = rem - b * g.ncb;
-      const int c0 = cb * kCtaChannels + warp * 32;
-      if (c0 < g.C) {
-        float* sk = stages + (size_t)(3 * s) * TILE + warp * 32;
-        const int len = min(kChunk, g.T - j * kChunk);
-        const int wg = cb * kConsumerWarps + warp;
-        // one predicated body for full and partial chunks: the full-chunk
-        // specialisation schedules more loads ahead than the register file
-        // of two resident CTAs holds (it spills)
-        bwd_tile<false>(a, sk, sk + TILE, sk + 2 * TILE, j, b, wg, c0 + lane, len);
-        // this warp wrote into the stage; the next TMA fill must come after
-        fence_proxy_async_smem();
+      if (count > 0) {
+        const BwdPend p = pend[nf];
+        bool ready = true;
+        Adj X{0.f, 0.f, 0.f};
+        if (p.live && !failed && p.j < g.nchunks - 1) {
+          const bool valid = p.c < g.C;
+          const Rec r = rec_load(a.rinc + ((size_t)(p.j + 1) * g.B + p.b) * g.C + (valid ? p.c : 0));
+          ready = __all_sync(0xffffffffu, !valid || rec_ok(r, a.tag));
+          X = Adj{rec_x(r), rec_y(r), rec_z(r)};
+        }
+        if (ready) {
+          if (p.live && !failed) {
+            float* sk = stages + (size_t)(3 * nf) * TILE + warp * 32 + lane;
+            bwd_finish<false>(a, sk, sk + TILE, sk + 2 * TILE, p, X, xa, xb, xp);
+            // this warp wrote into the stage; the next TMA fill must come after
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->empty[nf]);
+          --count;
+          if (++nf == NS) nf = 0;
+          progress = true;
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->empty[s]);
-      if (++s == NS) {
-        s = 0;
-        phase ^= 1u;
+      if (end && count == 0) break;
+      if (progress) {
+        idle = false;
+        continue;
+      }
+      // nothing to do: bounded wait for a stage or a carried adjoint
+      const uint64_t now = __shfl_sync(0xffffffffu, globaltimer(), 0);
+      if (!idle) {
+        idle = true;
+        idle_since = now;
+      } else if (now - idle_since > a.budget_ns) {
+        if (failed) break;  // nothing more will arrive
+        if (lane == 0) {
+          record_error(a.eh, kDevErrTimeout, a.epoch);
+          *(volatile int*)&ctl->abort = 1;
+        }
+        failed = true;  // later tiles are only drained
+        idle_since = now;
+      }
+      if (!failed && __shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == a.epoch) {
+        failed = true;
+        if (lane == 0) *(volatile int*)&ctl->abort = 1;
       }
     }
   }
@@ -498,7 +642,7 @@ int reduce_slices(int rows, int C) {
 
 cudaError_t launch_backward(BwdArgs& a, cudaStream_t s) {
   constexpr int NS = kBwdStages;
-  const size_t smem = (size_t)NS * 3 * kChunk * kCtaChannels * sizeof(float) + sizeof(PipeCtl<NS>);
+  const size_t smem = (size_t)NS * 3 * kChunk * kCtaChannels * sizeof(float) + pipe_ctl_bytes<NS>() + kWalkSmem;
   static int grid_per_dev[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -516,8 +660,7 @@ cudaError_t launch_backward(BwdArgs& a, cudaStream_t s) {
     if (dev >= 0 && dev < 64) grid_per_dev[dev] = grid;
   }
   const unsigned int nblk = a.g.ntiles < (unsigned)grid ? a.g.ntiles : (unsigned)grid;
-  bwd_scan_kernel<<<dim3(nblk), dim3(kPipeThreads), smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_cooperative(bwd_scan_kernel, nblk, smem, s, a);
 }
 
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s) {

@@ -22,9 +22,6 @@ namespace wkv {
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 constexpr float kEmptyPP = -1e38f;             // pp of the empty state
 
-// A flag word is (launch epoch << 2) | status, so flags left by earlier
-// launches in the same workspace never read as published.
-
 // Error codes written to the workspace header by a kernel.
 constexpr unsigned int kDevErrTimeout = 6;
 
@@ -123,28 +120,11 @@ __device__ __forceinline__ State combine(const State& x, float decay, const Stat
   return State{fmaf(ex, x.num, ey * y.num), fmaf(ex, x.den, ey * y.den), keep ? px : y.pp};
 }
 
-// ------------------------------------------------------- memory ordering
-__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Loads of data published by other CTAs: bypass L1 (not coherent).
-__device__ __forceinline__ float ld_cg(const float* p) { return __ldcg(p); }
-
+// ------------------------------------------------------------- timing
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
-}
-
-__device__ __forceinline__ uint64_t flag_status(uint64_t word, uint64_t epoch) {
-  return (word >> 2) == epoch ? (word & 3u) : 0u;
 }
 
 // Workspace header: the first 256 bytes of a workspace, at the same place for
@@ -172,75 +152,49 @@ __device__ __forceinline__ void record_error(WsHeader* h, unsigned int code, uin
 
 namespace wkv {
 
-// ------------------------------------------------------------ look-back
-// Chunk results are passed between tiles through per-(chunk, row, 32-channel
-// group) flags.  A tile first publishes its chunk's own summary (kAgg), and
-// once it knows the result carried into its chunk, the inclusive result
-// (kIncl).  A tile finds the result carried into its chunk by looking at its
-// neighbours in scan order: the nearest one with an inclusive record, whose
-// value it then folds forward through the summaries of the chunks in
-// between, oldest first.  The fold is a left fold in a fixed order, the same
-// one the chain of inclusive records follows, so every tile obtains the same
-// bits whichever neighbour it found first: results are reproducible.
-constexpr uint64_t kAgg = 1;   // flag status: chunk summary published
-constexpr uint64_t kIncl = 2;  // flag status: inclusive result published
-constexpr uint64_t kErr = 3;   // flag status: producer gave up
+// ------------------------------------------------------ tagged records
+// Chunk results pass between warps of different CTAs as 16-byte records, one
+// per channel: three values and the launch tag, read and written as single
+// 128-bit accesses (single-copy atomic), so a reader that sees its launch's
+// tag sees the values written with it: no fence and no separate flag is
+// needed.  The tag is derived from the launch epoch and is never 0 (the tag
+// of a zero-filled workspace), so records left by earlier launches in a
+// reused workspace never read as current.
+struct Rec {
+  unsigned long long lo;  // value 0 | value 1 << 32
+  unsigned long long hi;  // value 2 | tag << 32
+};
+
+__device__ __forceinline__ Rec rec_load(const Rec* p) {
+  Rec r;
+  asm volatile(
+      "{\n\t.reg .b128 t;\n\t"
+      "ld.relaxed.gpu.global.b128 t, [%2];\n\t"
+      "mov.b128 {%0, %1}, t;\n\t}"
+      : "=l"(r.lo), "=l"(r.hi)
+      : "l"(p)
+      : "memory");
+  return r;
+}
+
+__device__ __forceinline__ void rec_store(Rec* p, uint32_t tag, float x, float y, float z) {
+  const unsigned long long lo = ((unsigned long long)__float_as_uint(y) << 32) | __float_as_uint(x);
+  const unsigned long long hi = ((unsigned long long)tag << 32) | __float_as_uint(z);
+  asm volatile(
+      "{\n\t.reg .b128 t;\n\t"
+      "mov.b128 t, {%0, %1};\n\t"
+      "st.relaxed.gpu.global.b128 [%2], t;\n\t}" ::"l"(lo),
+      "l"(hi), "l"(p)
+      : "memory");
+}
+
+__device__ __forceinline__ bool rec_ok(const Rec& r, uint32_t tag) { return (uint32_t)(r.hi >> 32) == tag; }
+__device__ __forceinline__ float rec_x(const Rec& r) { return __uint_as_float((uint32_t)r.lo); }
+__device__ __forceinline__ float rec_y(const Rec& r) { return __uint_as_float((uint32_t)(r.lo >> 32)); }
+__device__ __forceinline__ float rec_z(const Rec& r) { return __uint_as_float((uint32_t)r.hi); }
 
 constexpr int kWaitOk = 0;
 constexpr int kWaitTimeout = 1;
 constexpr int kWaitError = 2;
-
-// Waits (one warp) until, among the nwin <= 32 neighbours whose flags are
-// flag_at(0) (nearest) .. flag_at(nwin - 1), the nearest one with an
-// inclusive record is known and every nearer one has published its summary.
-// Sets `base` to that neighbour's index.  Lane i polls neighbour i, so all
-// polls overlap.  Bounded: past budget_ns of %globaltimer returns
-// kWaitTimeout; a neighbour that gave up, or an expired wait anywhere in the
-// same launch (h->abort == epoch), gives kWaitError.  The warp barrier after
-// a successful wait orders the acquiring loads before every lane's reads of
-// the published data.
-template <class FlagAt>
-__device__ __forceinline__ int lookback_wait(FlagAt flag_at, int nwin, uint64_t epoch, uint64_t budget_ns,
-                                             const WsHeader* h, int& base) {
-  const unsigned full = 0xffffffffu;
-  const int lane = threadIdx.x & 31;
-  const uint64_t* fp = lane < nwin ? flag_at(lane) : nullptr;
-  uint64_t st = 0;
-  uint64_t t0 = 0;
-  bool timing = false;
-  while (true) {
-    if (fp != nullptr && st != kIncl) st = flag_status(ld_acquire(fp), epoch);
-    if (__any_sync(full, st == kErr)) return kWaitError;
-    const unsigned incl = __ballot_sync(full, st == kIncl);
-    const unsigned rdy = __ballot_sync(full, st != 0);
-    if (incl != 0u) {
-      const int f = __ffs(incl) - 1;
-      const unsigned need = (1u << f) - 1u;
-      if ((rdy & need) == need) {
-        base = f;
-        break;
-      }
-    }
-    if (__shfl_sync(full, *(volatile const unsigned long long*)&h->abort, 0) == epoch) return kWaitError;
-    const uint64_t now = __shfl_sync(full, globaltimer(), 0);
-    if (!timing) {
-      t0 = now;
-      timing = true;
-    } else if (now - t0 > budget_ns) {
-      return kWaitTimeout;
-    }
-    __nanosleep(32);
-  }
-  __syncwarp();
-  return kWaitOk;
-}
-
-// Publishes data every lane has written for its channel: the fence orders
-// those writes before the flag, which lane 0 then releases.
-__device__ __forceinline__ void publish(uint64_t* flag, uint64_t epoch, uint64_t status) {
-  __threadfence();
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) st_release(flag, (epoch << 2) | status);
-}
 
 }  // namespace wkv

@@ -6,22 +6,27 @@
 // training form time-parallel (qiita "RWKV についての調査記録", section
 // "Trainingについて").  Time is cut into chunks of kChunk tokens; a tile is
 // (chunk j, batch row b, 128 channels), one channel per consumer lane, its k
-// and v staged in shared memory by the producer warp (wkv_pipe.cuh).  Per
-// tile and lane:
+// and v staged in shared memory by the producer warp (wkv_pipe.cuh).
 //
-//   1. chunk statistics: F = max k, the smallest k, and the state's running
-//      maximum at the chunk end r = max_i (k_i - (n-1-i) w);
-//   2. the chunk's own summary (its tokens from the empty state), computed at
-//      the fixed scale e^{F}: ek_i = e^{k_i - F} <= 1, num = num e^{-w} +
-//      ek v, den = den e^{-w} + ek, then rescaled to the canonical scale
-//      e^{r}; published for the look-back (wkv_common.cuh);
-//   3. look-back: the state carried into the chunk, P;
-//   4. the state after the chunk, P (+) summary, written as the checkpoint
-//      and published as the inclusive record;
-//   5. the outputs: the chunk re-run from P at scale e^{F}:
-//      y = (a + e^{u} ek v) / (b + e^{u} ek).
+// Consumer warps, per tile and lane:
+//   summary  chunk statistics F = max k, the smallest k and the running
+//            maximum at the chunk end r = max_i (k_i - (n-1-i) w); the
+//            chunk's own summary (its tokens from the empty state) at the
+//            fixed scale e^{F}: ek_i = e^{k_i - F} <= 1, num = num e^{-w} +
+//            ek v, den = den e^{-w} + ek, rescaled to the canonical scale
+//            e^{r}; published as a tagged record;
+//   re-run   (after the summary of the next tile, so that waiting overlaps
+//            work) the state P carried into the chunk, from the walker; the
+//            outputs y = (a + e^{u} ek v) / (b + e^{u} ek) from P at scale
+//            e^{F}.
+// Walker warps carry the state along each chain (batch row, 32 channels)
+// of chunks: P_{j+1} = P_j (+) summary_j, a left fold in chunk order (so the
+// result is bitwise reproducible), written as the checkpoints and as tagged
+// records for the next chunk's tiles.  A walker reads its summaries through
+// a ring of prefetched records, so a long chain advances at several chunks
+// per memory round trip.
 //
-// The fixed scale makes each element cost one exponential and a few FMAs.  It
+// The fixed scale makes each element cost a few FMAs and exponentials.  It
 // is exact in fp32 as long as every value the chunk handles stays within the
 // fp32 range: here when every token's bonus weight ek e^{min(u,0)} is at
 // least e^{-69} (then the current token's own term bounds the denominator
@@ -55,162 +60,246 @@ struct FwdStages {
   static constexpr int value = sizeof(KV) == 4 ? 3 : 4;
 };
 
-constexpr float kFastRange = 69.f;   // smallest bonus weight of the fixed scale: e^{-69}
-constexpr float kFastCeil = 60.f;    // largest scale-up of the fixed scale: e^{60}
+constexpr float kFastRange = 69.f;  // smallest bonus weight of the fixed scale: e^{-69}
+constexpr float kFastCeil = 60.f;   // largest scale-up of the fixed scale: e^{60}
+constexpr int kWalkCap = 16;        // chains per walker whose state stays in shared memory
+constexpr int kWalkRing = 8;        // summaries requested together by a walker
+// walker shared memory: chain states [kWalkCap][3][32] f32, decays [kWalkCap][32] f32, offsets [kWalkCap][32] i32,
+// record ring [kWalkRing][32] of 16-byte records
+constexpr size_t kWalkSmem = (size_t)kWalkCap * (96 + 32 + 32) * sizeof(float) + (size_t)kWalkRing * 32 * 16;
+static_assert((kWalkCap * (96 + 32 + 32) * sizeof(float)) % 16 == 0, "the record ring must be 16-byte aligned");
+static_assert(3 * 2 * kChunk * kCtaChannels * 4 + kWalkSmem + 1024 <= 114 * 1024, "two fp32 forward CTAs per SM");
 
-__device__ __forceinline__ State load_state(const float* rec, size_t plane, size_t o) {
-  return State{__ldcg(rec + o), __ldcg(rec + o + plane), __ldcg(rec + o + 2 * plane)};
-}
+// What a consumer lane keeps of a tile between its summary and its re-run.
+struct FwdPend {
+  int j, b, c, len, stage;
+  bool live;   // the warp has channels in this tile
+  bool fast;   // the summary used the fixed scale
+  float w, u, ew, F, kmin;
+};
 
-__device__ __forceinline__ void store_state(float* rec, size_t plane, size_t o, const State& s) {
-  rec[o] = s.num;
-  rec[o + plane] = s.den;
-  rec[o + 2 * plane] = s.pp;
-}
-
-// One consumer warp's share (32 channels) of one tile.
-template <typename KV, bool WRITE_Y, bool FULL>
-__device__ __forceinline__ void fwd_tile(const FwdArgs& a, const KV* sk, const KV* sv, int j, int b, int wg, int c,
-                                         int len) {
+template <typename KV>
+__device__ __forceinline__ void fwd_summary(const FwdArgs& a, const KV* __restrict__ sk, const KV* __restrict__ sv,
+                                            FwdPend& p) {
   constexpr int L = kChunk;
+  constexpr int S = kCtaChannels;
   const ScanGeometry& g = a.g;
-  const int lane = threadIdx.x & 31;
-  const bool valid = c < g.C;
-  const int cc = valid ? c : g.C - 1;  // out-of-range lanes shadow the last channel, never store
-  const int n = FULL ? L : len;
-  const float w = __ldg(a.w + cc);
-  const float u = __ldg(a.u + cc);
-  sk += lane;
-  sv += lane;
-
-  // 1. chunk statistics
-  float kr[L];
+  const int n = p.len;
   float F = -3.0e38f, kmin = 3.0e38f, r = -3.0e38f;
-#pragma unroll
-  for (int i = 0; i < L; ++i) {
-    if (FULL || i < len) {
-      kr[i] = to_f32<KV>(sk[i * kCtaChannels]);
-      F = fmaxf(F, kr[i]);
-      kmin = fminf(kmin, kr[i]);
-      r = fmaxf(r, fmaf(-(float)(n - 1 - i), w, kr[i]));
-    }
+#pragma unroll 8
+  for (int i = 0; i < n; ++i) {
+    const float k = to_f32<KV>(sk[i * S]);
+    F = fmaxf(F, k);
+    kmin = fminf(kmin, k);
+    r = fmaxf(r, fmaf(-(float)(n - 1 - i), p.w, k));
   }
-
-  // 2. the chunk's own summary
-  const bool fast_sum = kmin >= F - kFastRange;
-  const float ew = expf(-w);
-  State S;
-  if (fast_sum) {
+  p.F = F;
+  p.kmin = kmin;
+  p.fast = kmin >= F - kFastRange;
+  State s;
+  if (p.fast) {
     const float F2 = F * kLog2e;
     float num = 0.f, den = 0.f;
-#pragma unroll
-    for (int i = 0; i < L; ++i) {
-      if (FULL || i < len) {
-        const float ek = ex2(fmaf(kr[i], kLog2e, -F2));
-        kr[i] = ek;
-        const float vv = to_f32<KV>(sv[i * kCtaChannels]);
-        num = fmaf(num, ew, ek * vv);
-        den = fmaf(den, ew, ek);
-      }
+#pragma unroll 8
+    for (int i = 0; i < n; ++i) {
+      const float ek = ex2(fmaf(to_f32<KV>(sk[i * S]), kLog2e, -F2));
+      const float vv = to_f32<KV>(sv[i * S]);
+      num = fmaf(num, p.ew, ek * vv);
+      den = fmaf(den, p.ew, ek);
     }
     const float sc = exp_nat(F - r);  // >= 1: from scale e^{F} to e^{r}
-    S = State{num * sc, den * sc, r};
+    s = State{num * sc, den * sc, r};
   } else {
-    State s = empty_state();
-#pragma unroll
-    for (int i = 0; i < L; ++i)
-      if (FULL || i < len) step(s, kr[i], to_f32<KV>(sv[i * kCtaChannels]), w);
-    S = s;
+    s = empty_state();
+#pragma unroll 1
+    for (int i = 0; i < p.len; ++i) step(s, to_f32<KV>(sk[i * S]), to_f32<KV>(sv[i * S]), p.w);
   }
+  if (p.j == a.debug_skip_chunk) return;  // fault injection: this chunk's summaries are never published
+  if (p.c < g.C) rec_store(a.agg + ((size_t)p.j * g.B + p.b) * g.C + p.c, a.tag, s.num, s.den, s.pp);
+}
 
-  const size_t P3 = g.plane;
-  const size_t slot = ((size_t)j * g.B + b) * g.C + cc;
-  uint64_t* flag = a.flags + ((size_t)j * g.B + b) * g.nwg + wg;
-  const bool has_succ = j < g.nchunks - 1;
-  const bool skip = j == a.debug_skip_chunk;  // fault injection: this tile never publishes
-  const float Lw = (float)L * w;              // decay over a whole chunk
-
-  // 3. look-back for the state carried into the chunk
-  State P = empty_state();
-  if (j > 0) {
-    if (has_succ && !skip) {
-      if (valid) store_state(a.agg, P3, slot, S);
-      publish(flag, a.epoch, kAgg);
-    }
-    const int nwin = min(j, 32);
-    int base = 0;
-    const int rc = lookback_wait(
-        [&](int i) { return a.flags + ((size_t)(j - 1 - i) * g.B + b) * g.nwg + wg; }, nwin, a.epoch, a.budget_ns,
-        a.eh, base);
-    if (rc != kWaitOk) {
-      if (rc == kWaitTimeout && lane == 0) record_error(a.eh, kDevErrTimeout, a.epoch);
-      if (has_succ && !skip) publish(flag, a.epoch, kErr);
-      return;
-    }
-    const size_t row = (size_t)b * g.C + cc;
-    const size_t jstride = (size_t)g.B * g.C;
-    P = load_state(a.inc, P3, (size_t)(j - 1 - base) * jstride + row);
-    // fold the summaries of chunks j - base .. j - 1, oldest first, four loads in flight
-    for (int i = base - 1; i >= 0; i -= 4) {
-      State q[4];
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        if (i - m >= 0) q[m] = load_state(a.agg, P3, (size_t)(j - 1 - (i - m)) * jstride + row);
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        if (i - m >= 0) P = combine(P, Lw, q[m]);
-    }
-  }
-
-  // 4. the state after the chunk: checkpoint and inclusive record
-  const State incl = combine(P, (float)n * w, S);
-  if (valid) store_state(a.inc, P3, slot, incl);
-  if (has_succ && !skip) publish(flag, a.epoch, kIncl);
-
+// The outputs of a tile from the state P carried into its chunk.
+template <typename KV, bool WRITE_Y>
+__device__ __forceinline__ void fwd_rerun(const FwdArgs& a, const KV* __restrict__ sk, const KV* __restrict__ sv,
+                                          const FwdPend& p, const State& P) {
+  constexpr int L = kChunk;
+  constexpr int S = kCtaChannels;
+  const ScanGeometry& g = a.g;
+  const bool valid = p.c < g.C;
   if constexpr (WRITE_Y) {
-    // 5. outputs
-    float* yp = a.y + ((int64_t)b * g.T + (int64_t)j * L) * g.C + cc;
-    const bool fast_run = fast_sum && (kmin + fminf(u, 0.f) >= F - kFastRange) && (u <= kFastCeil) &&
-                          (P.pp - F <= kFastCeil);
-    if (fast_run) {
+    float* __restrict__ yp = a.y + ((int64_t)p.b * g.T + (int64_t)p.j * L) * g.C + p.c;
+    const float u = p.u;
+    const bool fast = p.fast && (p.kmin + fminf(u, 0.f) >= p.F - kFastRange) && (u <= kFastCeil) &&
+                      (P.pp - p.F <= kFastCeil);
+    if (fast) {
       const float eu = expf(u);
-      const float s0 = exp_nat(P.pp - F);  // P at scale e^{F}; 0 for the empty state
+      const float F2 = p.F * kLog2e;
+      const float s0 = exp_nat(P.pp - p.F);  // P at scale e^{F}; 0 for the empty state
       float na = P.num * s0, nb = P.den * s0;
-#pragma unroll
-      for (int i = 0; i < L; ++i) {
-        if (FULL || i < len) {
-          const float ek = kr[i];
-          const float vv = to_f32<KV>(sv[i * kCtaChannels]);
-          const float ec = ek * eu;
-          const float yv = fmaf(ec, vv, na) * rcp(nb + ec);
-          if (valid) __stcs(yp + (int64_t)i * g.C, yv);
-          na = fmaf(na, ew, ek * vv);
-          nb = fmaf(nb, ew, ek);
-        }
+#pragma unroll 8
+      for (int i = 0; i < p.len; ++i) {
+        const float ek = ex2(fmaf(to_f32<KV>(sk[i * S]), kLog2e, -F2));
+        const float vv = to_f32<KV>(sv[i * S]);
+        const float ec = ek * eu;
+        const float yv = fmaf(ec, vv, na) * rcp(nb + ec);
+        if (valid) __stcs(yp + (int64_t)i * g.C, yv);
+        na = fmaf(na, p.ew, ek * vv);
+        nb = fmaf(nb, p.ew, ek);
       }
     } else {
       State s = P;
-#pragma unroll
-      for (int i = 0; i < L; ++i) {
-        if (FULL || i < len) {
-          const float kk = to_f32<KV>(sk[i * kCtaChannels]);
-          const float vv = to_f32<KV>(sv[i * kCtaChannels]);
-          const float yv = output(s, kk, vv, u);
-          if (valid) __stcs(yp + (int64_t)i * g.C, yv);
-          step(s, kk, vv, w);
-        }
+#pragma unroll 1
+      for (int i = 0; i < p.len; ++i) {
+        const float kk = to_f32<KV>(sk[i * S]);
+        const float vv = to_f32<KV>(sv[i * S]);
+        const float yv = output(s, kk, vv, u);
+        if (valid) __stcs(yp + (int64_t)i * g.C, yv);
+        step(s, kk, vv, p.w);
       }
     }
+  }
+}
+
+// The walkers.  Walker x (one warp per CTA) owns the chains q = x + m * G
+// (G = gridDim.x, q = b * nwg + group of 32 channels) and takes their chunks
+// chunk by chunk (for each chunk, each of its chains), so it never waits on
+// a chunk before the chunks it still has to deliver.  With at most kWalkCap
+// chains, a chain's state, decay and row offset stay in shared memory (each
+// lane reads back only what it wrote); beyond that the state is read back
+// from the checkpoints it wrote, kWalkRing items ahead.
+
+// Walker shared memory, per chain qi < kWalkCap: state [3][32] f32 (num,
+// den, pp), decay w [32] f32, and this lane's element offset within a chunk
+// [32] i32 (b * C + channel; bit 31 set when the lane's channel is past C).
+__device__ __forceinline__ float* walk_state(float* pst, int qi) { return pst + qi * 96; }
+__device__ __forceinline__ float* walk_w(float* pst) { return pst + kWalkCap * 96; }
+__device__ __forceinline__ int* walk_off(float* pst) { return reinterpret_cast<int*>(pst + kWalkCap * 128); }
+
+// Element offset (bit 31: lane past C) of chain qi for this lane, computed.
+__device__ __noinline__ int walk_off_slow(const ScanGeometry& g, int qi) {
+  const int q = (int)blockIdx.x + qi * (int)gridDim.x;
+  const int b = q / g.nwg;
+  const int c = (q - b * g.nwg) * 32 + (int)(threadIdx.x & 31);
+  return c < g.C ? b * g.C + c : (b * g.C + g.C - 1) | (int)0x80000000;
+}
+
+__device__ __forceinline__ int walk_offset(const ScanGeometry& g, float* pst, int mq, int qi) {
+  return mq <= kWalkCap ? walk_off(pst)[qi * 32 + (threadIdx.x & 31)] : walk_off_slow(g, qi);
+}
+
+// One item: the state after chunk j of chain qi from the one before it and
+// the chunk's summary s.  Kept out of line so that the walker's code stays
+// small (the instruction cache is shared with the consumer warps).
+__device__ __noinline__ void fwd_walk_item(const FwdArgs& a, float* pst, int mq, int j, int qi, Rec s, State P) {
+  const ScanGeometry& g = a.g;
+  const int lane = threadIdx.x & 31;
+  const int eo = walk_offset(g, pst, mq, qi);
+  const bool valid = eo >= 0;
+  const size_t o = (size_t)j * g.B * g.C + (eo & 0x7fffffff);
+  const bool in_smem = mq <= kWalkCap;
+  float* ps = walk_state(pst, qi) + lane;
+  if (j == 0) {
+    P = empty_state();
+  } else if (in_smem) {
+    P = State{ps[0], ps[32], ps[64]};
+  } else {
+    const size_t op = o - (size_t)g.B * g.C;  // written by this lane mq items ago
+    P = State{__ldcg(a.ckpt + op), __ldcg(a.ckpt + op + g.plane), __ldcg(a.ckpt + op + 2 * g.plane)};
+  }
+  const float w = in_smem ? walk_w(pst)[qi * 32 + lane] : __ldg(a.w + (eo & 0x7fffffff) % g.C);
+  const int n = j == g.nchunks - 1 ? g.T - j * kChunk : kChunk;
+  P = combine(P, (float)n * w, State{rec_x(s), rec_y(s), rec_z(s)});
+  if (valid) {
+    const size_t P3 = g.plane;
+    a.ckpt[o] = P.num;
+    a.ckpt[o + P3] = P.den;
+    a.ckpt[o + 2 * P3] = P.pp;
+    if (j < g.nchunks - 1) rec_store(a.inc + o, a.tag, P.num, P.den, P.pp);
+  }
+  if (in_smem) {
+    ps[0] = P.num;
+    ps[32] = P.den;
+    ps[64] = P.pp;
+  }
+}
+
+__device__ __forceinline__ void fwd_walker(const FwdArgs& a, float* pst) {
+  const ScanGeometry& g = a.g;
+  const int lane = threadIdx.x & 31;
+  const int nchain = g.B * g.nwg;
+  const int x = blockIdx.x, G = gridDim.x;
+  if (x >= nchain) return;
+  const int mq = (nchain - 1 - x) / G + 1;
+  const bool in_smem = mq <= kWalkCap;
+  const long nitems = (long)g.nchunks * mq;
+  const size_t jstride = (size_t)g.B * g.C;
+  if (in_smem) {
+    for (int qi = 0; qi < mq; ++qi) {
+      const int eo = walk_off_slow(g, qi);
+      walk_off(pst)[qi * 32 + lane] = eo;
+      walk_w(pst)[qi * 32 + lane] = __ldg(a.w + (eo & 0x7fffffff) % g.C);
+    }
+  }
+  Rec* ring = reinterpret_cast<Rec*>(walk_off(pst) + kWalkCap * 32);  // [kWalkRing][32]
+  __syncwarp();
+  const uint32_t tag = a.tag;
+  // Items are taken in blocks of kWalkRing: every record of the block not yet
+  // current is copied into the ring together (one memory round trip), then
+  // the current prefix is folded in order; the rest is copied again.
+  int bj = 0, bq = 0;  // first item of the block
+  for (long base = 0; base < nitems; base += kWalkRing) {
+    const int nb = (int)min((long)kWalkRing, nitems - base);
+    int done = 0, cj = bj, cq = bq;
+    bool first = true;
+    uint64_t t0 = globaltimer();
+    while (done < nb) {
+      int j = cj, qi = cq;
+      for (int r = done; r < nb; ++r) {
+        Rec* slot = ring + r * 32 + lane;
+        if (first || !rec_ok(*slot, tag))
+          cp_async16(slot, a.agg + (size_t)j * jstride + (walk_offset(g, pst, mq, qi) & 0x7fffffff));
+        if (++qi == mq) {
+          qi = 0;
+          ++j;
+        }
+      }
+      cp_async_wait_all();
+      __syncwarp();
+      first = false;
+      const int before = done;
+      for (; done < nb; ++done) {
+        const Rec rr = ring[done * 32 + lane];
+        if (!__all_sync(0xffffffffu, walk_offset(g, pst, mq, cq) < 0 || rec_ok(rr, tag))) break;
+        fwd_walk_item(a, pst, mq, cj, cq, rr, State{0.f, 0.f, 0.f});
+        if (++cq == mq) {
+          cq = 0;
+          ++cj;
+        }
+      }
+      if (done > before) {
+        t0 = globaltimer();
+        continue;
+      }
+      if (__shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == a.epoch) return;
+      if (__shfl_sync(0xffffffffu, globaltimer(), 0) - t0 > a.budget_ns) {
+        if (lane == 0) record_error(a.eh, kDevErrTimeout, a.epoch);
+        return;
+      }
+    }
+    bj = cj;
+    bq = cq;
   }
 }
 
 template <typename KV, bool WRITE_Y>
-__global__ void __launch_bounds__(kPipeThreads, 1) fwd_scan_kernel(const __grid_constant__ FwdArgs a) {
+__global__ void __launch_bounds__(kPipeThreads, 2) fwd_scan_kernel(const __grid_constant__ FwdArgs a) {
   constexpr int NS = FwdStages<KV>::value;
   constexpr int TILE = kChunk * kCtaChannels;
   extern __shared__ __align__(1024) unsigned char smem[];
   KV* stages = reinterpret_cast<KV*>(smem);  // stage s: k at 2s*TILE, v at (2s+1)*TILE
   auto* ctl = reinterpret_cast<PipeCtl<NS>*>(smem + (size_t)NS * 2 * TILE * sizeof(KV));
+  // walker shared memory (kWalkSmem bytes), 128-byte aligned
+  float* pst = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(ctl) + pipe_ctl_bytes<NS>());
   pipe_init(ctl);
   const ScanGeometry& g = a.g;
   const int warp = threadIdx.x >> 5;
@@ -242,37 +331,96 @@ __global__ void __launch_bounds__(kPipeThreads, 1) fwd_scan_kernel(const __grid_
                                           cb * kCtaChannels, kChunk);
                         }
                       });
+  } else if (warp == kWalkerWarp) {
+    fwd_walker(a, pst);
   } else {
-    int s = 0;
-    uint32_t phase = 0;
+    // Consumer: a tile is summarised as soon as its stage lands (every
+    // ticketed tile's summary reaches the walkers without waiting on other
+    // tiles), and the oldest summarised tile is re-run once its carried state
+    // is published; neither step blocks the other.
+    FwdPend pend[NS];  // per stage (local memory)
+    int ns = 0, nf = 0, count = 0;
+    uint32_t ps = 0;
+    bool end = false, failed = false, idle = false;
+    uint64_t idle_since = 0;
     while (true) {
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl->full[s], phase, a.budget_ns));
-      if (!ok) {
-        if (lane == 0) pipe_fail(ctl, a.eh, kDevErrTimeout, a.epoch);
-        break;
+      bool progress = false;
+      while (!end && count < NS && __all_sync(0xffffffffu, mbar_test(&ctl->full[ns], ps))) {
+        const int t = *(volatile int*)&ctl->tile[ns];
+        if (t < 0) {
+          end = true;
+          break;
+        }
+        FwdPend p;  // in registers while in use; parked in pend[] between summary and re-run
+        const int j = t / per_j;
+        const int rem = t - j * per_j;
+        p.j = j;
+        p.b = rem / g.ncb;
+        const int cb = rem - p.b * g.ncb;
+        const int c0 = cb * kCtaChannels + warp * 32;
+        p.live = c0 < g.C;
+        p.c = c0 + lane;
+        p.len = min(kChunk, g.T - j * kChunk);
+        if (p.live && !failed) {
+          const int cc = p.c < g.C ? p.c : g.C - 1;
+          p.w = __ldg(a.w + cc);
+          p.u = __ldg(a.u + cc);
+          p.ew = expf(-p.w);
+          const KV* sk = stages + (size_t)(2 * ns) * TILE + warp * 32 + lane;
+          fwd_summary<KV>(a, sk, sk + TILE, p);
+        }
+        pend[ns] = p;
+        ++count;
+        if (++ns == NS) {
+          ns = 0;
+          ps ^= 1u;
+        }
+        progress = true;
       }
-      const int t = *(volatile int*)&ctl->tile[s];
-      if (t < 0) break;
-      const int j = t / per_j;
-      const int rem = t - j * per_j;
-      const int b = rem / g.ncb;
-      const int cb = rem - b * g.ncb;
-      const int c0 = cb * kCtaChannels + warp * 32;
-      if (c0 < g.C) {
-        const KV* sk = stages + (size_t)(2 * s) * TILE + warp * 32;
-        const KV* sv = sk + TILE;
-        const int len = min(kChunk, g.T - j * kChunk);
-        const int wg = cb * kConsumerWarps + warp;
-        if (len == kChunk)
-          fwd_tile<KV, WRITE_Y, true>(a, sk, sv, j, b, wg, c0 + lane, len);
-        else
-          fwd_tile<KV, WRITE_Y, false>(a, sk, sv, j, b, wg, c0 + lane, len);
+      if (count > 0) {
+        const FwdPend p = pend[nf];
+        bool ready = true;
+        State P = empty_state();
+        if (p.live && !failed && p.j > 0) {
+          const bool valid = p.c < g.C;
+          const Rec r = rec_load(a.inc + ((size_t)(p.j - 1) * g.B + p.b) * g.C + (valid ? p.c : 0));
+          ready = __all_sync(0xffffffffu, !valid || rec_ok(r, a.tag));
+          P = State{rec_x(r), rec_y(r), rec_z(r)};
+        }
+        if (ready) {
+          if (p.live && !failed) {
+            const KV* sk = stages + (size_t)(2 * nf) * TILE + warp * 32 + lane;
+            fwd_rerun<KV, WRITE_Y>(a, sk, sk + TILE, p, P);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->empty[nf]);
+          --count;
+          if (++nf == NS) nf = 0;
+          progress = true;
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->empty[s]);
-      if (++s == NS) {
-        s = 0;
-        phase ^= 1u;
+      if (end && count == 0) break;
+      if (progress) {
+        idle = false;
+        continue;
+      }
+      // nothing to do: bounded wait for a stage or a carried state
+      const uint64_t now = __shfl_sync(0xffffffffu, globaltimer(), 0);
+      if (!idle) {
+        idle = true;
+        idle_since = now;
+      } else if (now - idle_since > a.budget_ns) {
+        if (failed) break;  // nothing more will arrive
+        if (lane == 0) {
+          record_error(a.eh, kDevErrTimeout, a.epoch);
+          *(volatile int*)&ctl->abort = 1;
+        }
+        failed = true;  // later tiles are only drained
+        idle_since = now;
+      }
+      if (!failed && __shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == a.epoch) {
+        failed = true;
+        if (lane == 0) *(volatile int*)&ctl->abort = 1;
       }
     }
   }
@@ -282,7 +430,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) fwd_scan_kernel(const __grid_
 template <typename KV, bool WRITE_Y>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   constexpr int NS = FwdStages<KV>::value;
-  const size_t smem = (size_t)NS * 2 * kChunk * kCtaChannels * sizeof(KV) + sizeof(PipeCtl<NS>);
+  const size_t smem = (size_t)NS * 2 * kChunk * kCtaChannels * sizeof(KV) + pipe_ctl_bytes<NS>() + kWalkSmem;
   auto kern = fwd_scan_kernel<KV, WRITE_Y>;
   // per device: the opt-in to large dynamic shared memory and the resident CTAs per SM
   static int grid_per_dev[64] = {};
@@ -302,8 +450,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
     if (dev >= 0 && dev < 64) grid_per_dev[dev] = grid;
   }
   const unsigned int nblk = a.g.ntiles < (unsigned)grid ? a.g.ntiles : (unsigned)grid;
-  kern<<<dim3(nblk), dim3(kPipeThreads), smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_cooperative(kern, nblk, smem, s, a);
 }
 
 }  // namespace

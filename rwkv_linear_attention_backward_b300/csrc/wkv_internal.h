@@ -23,14 +23,17 @@ struct ScanGeometry {
   int B, T, C;
   int nchunks;          // ceil(T / kChunk)
   int ncb;              // ceil(C / kCtaChannels): channel blocks per (chunk, row)
-  int nwg;              // ncb * 4: 32-channel groups per row (one flag each per chunk)
+  int nwg;              // ceil(C / 32): 32-channel groups per row (one chain of chunks each)
   unsigned int ntiles;  // nchunks * B * ncb
   size_t plane;         // nchunks * B * C: floats per record plane
 };
 
 ScanGeometry make_geometry(int B, int T, int C);
 
-// Forward scan.  Records [3][nchunks][B][C] hold states (num, den, pp).
+struct Rec;  // a 16-byte tagged record (wkv_common.cuh)
+
+// Forward scan.  Records are [nchunks][B][C] arrays of tagged 16-byte
+// records (wkv_common.cuh) holding states (num, den, pp).
 struct FwdArgs {
   CUtensorMap tk, tv;  // rank-3 maps {C, T, B} of k and v, box {128, kChunk, 1} (when use_tma)
   const float* w;
@@ -38,22 +41,23 @@ struct FwdArgs {
   const void* k;
   const void* v;
   float* y;            // may be null (state-only pass)
-  float* agg;          // chunk summaries (each chunk from the empty state)
-  float* inc;          // state after each chunk (the checkpoints)
-  uint64_t* flags;     // [nchunks][B][nwg]
+  Rec* agg;            // each chunk's own summary (from the empty state), written by the tiles
+  Rec* inc;            // the state after each chunk, written by the walkers for the next chunk's tiles
+  float* ckpt;         // [3][nchunks][B][C] f32: the state after each chunk (the checkpoints)
   unsigned int* ticket;  // tile counter of this launch (in a workspace header)
   unsigned int* exited;  // CTAs of this launch that have finished
   WsHeader* eh;          // where an expired wait is recorded (checked by the host)
   ScanGeometry g;
   uint64_t epoch;
+  uint32_t tag;          // record tag of this launch (never 0)
   uint64_t budget_ns;
   int debug_skip_chunk;  // -1: off
   int use_tma;
 };
 
-// Backward scan.  Adjoint records [3][nchunks][B][C] hold (la, lb, f): the
-// adjoints of the sums a, b at a chunk's first token, scaled by e^{f}, with f
-// the forward state's pp there.
+// Backward scan.  Adjoint records (tagged, [nchunks][B][C]) hold (la, lb,
+// f): the adjoints of the sums a, b at a chunk's first token, scaled by
+// e^{f}, with f the forward state's pp there.
 struct BwdArgs {
   CUtensorMap tk, tv, tg;  // rank-3 maps of k, v, gy (when use_tma)
   const float* w;
@@ -64,15 +68,15 @@ struct BwdArgs {
   const float* ckpt;   // [3][nchunks][B][C] state after each chunk (forward)
   float* gk;
   float* gv;
-  float* ragg;         // zero-carry adjoint of each chunk
-  float* rinc;         // adjoint at each chunk's start with everything after it
+  Rec* ragg;           // zero-carry adjoint of each chunk, written by the tiles
+  Rec* rinc;           // adjoint at each chunk's start with everything after it, written by the walkers
   float* part;         // [2][nchunks][B][C] per-tile gw, gu partial sums
-  uint64_t* flags;     // [nchunks][B][nwg]
   unsigned int* ticket;
   unsigned int* exited;
   WsHeader* eh;
   ScanGeometry g;
   uint64_t epoch;
+  uint32_t tag;
   uint64_t budget_ns;
   int debug_skip_chunk;
   int use_tma;

@@ -1,17 +1,21 @@
 // wkv_pipe.cuh -- the tile pipeline of the persistent scan kernels (sm_103a).
 //
 // A scan kernel runs a fixed number of CTAs (a multiple of the SM count's
-// resident capacity), each with one producer warp and kConsumerWarps
-// consumer warps.  The producer takes tile tickets from a counter in the
+// resident capacity), each with one producer warp, kConsumerWarps consumer
+// warps and one walker warp (the walkers carry chunk results from chunk to
+// chunk; see the scan kernels).  The producer takes tile tickets from a counter in the
 // workspace header, in increasing order, and stages every tile's input
 // arrays ([chunk of tokens] x [128 channels] each) into a ring of shared
 // memory stages: by TMA (cp.async.bulk.tensor, completion counted on the
 // stage's `full` mbarrier) when the tensors meet TMA's alignment rules, else
 // by plain loads.  Consumer warps take the stages in the same order, and
-// release each one on its `empty` mbarrier.  Since each CTA handles its
-// tickets in increasing order and a tile only ever waits on tiles with
-// smaller tickets (whose CTAs are running), the kernels cannot deadlock
-// however CTAs are scheduled.
+// release each one on its `empty` mbarrier.  Tickets are handed out in scan
+// order and each CTA handles its tickets in increasing order; a tile only
+// waits on results of earlier chunks, which the walkers (one warp per CTA,
+// each with a fixed set of chains, all resident: the kernels are launched
+// cooperatively) derive from tiles with smaller tickets.  The oldest
+// unfinished tile can therefore always progress: the kernels cannot
+// deadlock.
 //
 // Every wait is bounded (%globaltimer budget); an expired wait records
 // WKV_ERR_TIMEOUT in the workspace header and the kernel winds down.
@@ -25,8 +29,9 @@
 namespace wkv {
 
 constexpr int kConsumerWarps = 4;                       // one channel per lane: 128 channels per tile
-constexpr int kPipeThreads = (kConsumerWarps + 1) * 32;  // + the producer warp
-constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kProducerWarp = kConsumerWarps;            // stages the tiles
+constexpr int kWalkerWarp = kConsumerWarps + 1;          // carries chunk results along the chains
+constexpr int kPipeThreads = (kConsumerWarps + 2) * 32;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -61,6 +66,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking: whether the phase of `bar` with the given parity completed.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `bar` with the given parity to complete, for at
 // most budget_ns.  Returns false on expiry.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
@@ -70,6 +88,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer() - t0 > budget_ns) return false;
   }
+}
+
+// 16-byte asynchronous copy global -> shared that bypasses L1 (so a copy
+// issued again reads the current value in L2), and the wait for all of this
+// thread's copies.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 // Orders this thread's generic-proxy accesses to shared memory before later
@@ -100,6 +129,13 @@ struct PipeCtl {
   int tile[NSTAGE];        // ticket staged in the stage, -1 = no more tiles
   int abort;               // set when this CTA gave up a wait
 };
+
+// Bytes reserved for the control block: a multiple of 128, so that what
+// follows it in shared memory (16-byte records) stays aligned.
+template <int NSTAGE>
+__host__ __device__ constexpr size_t pipe_ctl_bytes() {
+  return (sizeof(PipeCtl<NSTAGE>) + 127) / 128 * 128;
+}
 
 template <int NSTAGE>
 __device__ __forceinline__ void pipe_init(PipeCtl<NSTAGE>* ctl) {
@@ -200,6 +236,24 @@ __device__ __forceinline__ void copy_tile_plain(E* dst, const E* src, int B, int
       dst[i * 128 + q] = val;
     }
   }
+}
+
+// Launches a scan kernel cooperatively: all its CTAs are resident at once
+// (or the launch fails), which the walkers' fixed chain assignment needs.
+template <class Args>
+inline cudaError_t launch_cooperative(void (*kern)(Args), unsigned int nblk, size_t smem, cudaStream_t s,
+                                      const Args& args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nblk);
+  cfg.blockDim = dim3(kPipeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 }  // namespace wkv
