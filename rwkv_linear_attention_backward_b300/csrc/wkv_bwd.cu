@@ -318,12 +318,21 @@ __device__ __forceinline__ int walk_offset(const ScanGeometry& g, float* pst, in
 }
 
 // One item: the adjoint at the start of chunk j of chain qi from the chunk's
-// zero-carry record s and the adjoint at the start of chunk j + 1.  Kept
-// out of line so that the walker's code stays small.
-__device__ __noinline__ void bwd_walk_item(const BwdArgs& a, float* pst, int mq, int j, int qi, Rec s) {
+// zero-carry record s and the adjoint at the start of chunk j + 1.
+// Inlined once into the walker's rolled loop (see the forward walker).
+// A walker with a single chain keeps its adjoint, chunk decay and offset
+// here, in registers (the common case: fewer chains than CTAs).
+struct WalkOne {
+  Adj X;
+  float Lw;
+  int eo;
+};
+
+__device__ __forceinline__ void bwd_walk_item(const BwdArgs& a, float* pst, int mq, int j, int qi, Rec s,
+                                              WalkOne& one) {
   const ScanGeometry& g = a.g;
   const int lane = threadIdx.x & 31;
-  const int eo = walk_offset(g, pst, mq, qi);
+  const int eo = mq == 1 ? one.eo : walk_offset(g, pst, mq, qi);
   const bool valid = eo >= 0;
   const size_t o = (size_t)j * g.B * g.C + (eo & 0x7fffffff);
   const bool in_smem = mq <= kWalkCap;
@@ -331,17 +340,22 @@ __device__ __noinline__ void bwd_walk_item(const BwdArgs& a, float* pst, int mq,
   Adj X{rec_x(s), rec_y(s), rec_z(s)};
   if (j < g.nchunks - 1) {
     Adj nx;
-    if (in_smem) {
+    if (mq == 1) {
+      nx = one.X;
+    } else if (in_smem) {
       nx = Adj{ps[0], ps[32], ps[64]};
     } else {
       const Rec r = rec_load(a.rinc + o + (size_t)g.B * g.C);  // written by this lane mq items ago
       nx = Adj{rec_x(r), rec_y(r), rec_z(r)};
     }
-    const float Lw = in_smem ? walk_w(pst)[qi * 32 + lane] : (float)kChunk * __ldg(a.w + (eo & 0x7fffffff) % g.C);
+    const float Lw = mq == 1 ? one.Lw
+                             : (in_smem ? walk_w(pst)[qi * 32 + lane] : (float)kChunk * __ldg(a.w + (eo & 0x7fffffff) % g.C));
     X = fold_adj(X, Lw, nx);
   }
   if (valid) rec_store(a.rinc + o, a.tag, X.la, X.lb, X.f);
-  if (in_smem) {
+  if (mq == 1) {
+    one.X = X;
+  } else if (in_smem) {
     ps[0] = X.la;
     ps[32] = X.lb;
     ps[64] = X.f;
@@ -367,6 +381,11 @@ __device__ __forceinline__ void bwd_walker(const BwdArgs& a, float* pst) {
   }
   Rec* ring = reinterpret_cast<Rec*>(walk_off(pst) + kWalkCap * 32);  // [kWalkRing][32]
   __syncwarp();
+  WalkOne one;
+  one.eo = walk_off_slow(g, 0);
+  one.Lw = (float)kChunk * __ldg(a.w + (one.eo & 0x7fffffff) % g.C);
+  one.X = Adj{0.f, 0.f, 0.f};
+  auto offset_of = [&](int qi) { return mq == 1 ? one.eo : walk_offset(g, pst, mq, qi); };
   const uint32_t tag = a.tag;
   // Blocks of kWalkRing items, as in the forward walker.
   int bj = g.nchunks - 1, bq = 0;  // first item of the block
@@ -380,7 +399,7 @@ __device__ __forceinline__ void bwd_walker(const BwdArgs& a, float* pst) {
       for (int r = done; r < nb; ++r) {
         Rec* slot = ring + r * 32 + lane;
         if (first || !rec_ok(*slot, tag))
-          cp_async16(slot, a.ragg + (size_t)j * jstride + (walk_offset(g, pst, mq, qi) & 0x7fffffff));
+          cp_async16(slot, a.ragg + (size_t)j * jstride + (offset_of(qi) & 0x7fffffff));
         if (++qi == mq) {
           qi = 0;
           --j;
@@ -392,8 +411,8 @@ __device__ __forceinline__ void bwd_walker(const BwdArgs& a, float* pst) {
       const int before = done;
       for (; done < nb; ++done) {
         const Rec rr = ring[done * 32 + lane];
-        if (!__all_sync(0xffffffffu, walk_offset(g, pst, mq, cq) < 0 || rec_ok(rr, tag))) break;
-        bwd_walk_item(a, pst, mq, cj, cq, rr);
+        if (!__all_sync(0xffffffffu, offset_of(cq) < 0 || rec_ok(rr, tag))) break;
+        bwd_walk_item(a, pst, mq, cj, cq, rr, one);
         if (++cq == mq) {
           cq = 0;
           --cj;

@@ -81,7 +81,6 @@ struct FwdPend {
 template <typename KV>
 __device__ __forceinline__ void fwd_summary(const FwdArgs& a, const KV* __restrict__ sk, const KV* __restrict__ sv,
                                             FwdPend& p) {
-  constexpr int L = kChunk;
   constexpr int S = kCtaChannels;
   const ScanGeometry& g = a.g;
   const int n = p.len;
@@ -187,26 +186,39 @@ __device__ __forceinline__ int walk_offset(const ScanGeometry& g, float* pst, in
   return mq <= kWalkCap ? walk_off(pst)[qi * 32 + (threadIdx.x & 31)] : walk_off_slow(g, qi);
 }
 
+// A walker with a single chain keeps its state, decay and offset here, in
+// registers (the common case: fewer chains than CTAs).
+struct WalkOne {
+  State P;
+  float w;
+  int eo;
+};
+
 // One item: the state after chunk j of chain qi from the one before it and
-// the chunk's summary s.  Kept out of line so that the walker's code stays
-// small (the instruction cache is shared with the consumer warps).
-__device__ __noinline__ void fwd_walk_item(const FwdArgs& a, float* pst, int mq, int j, int qi, Rec s, State P) {
+// the chunk's summary s.  Inlined once into the walker's rolled loop (a call
+// would save registers to local memory, which misses the small L1 left
+// beside the shared memory).
+__device__ __forceinline__ void fwd_walk_item(const FwdArgs& a, float* pst, int mq, int j, int qi, Rec s,
+                                              WalkOne& one) {
   const ScanGeometry& g = a.g;
   const int lane = threadIdx.x & 31;
-  const int eo = walk_offset(g, pst, mq, qi);
+  const int eo = mq == 1 ? one.eo : walk_offset(g, pst, mq, qi);
   const bool valid = eo >= 0;
   const size_t o = (size_t)j * g.B * g.C + (eo & 0x7fffffff);
   const bool in_smem = mq <= kWalkCap;
   float* ps = walk_state(pst, qi) + lane;
+  State P;
   if (j == 0) {
     P = empty_state();
+  } else if (mq == 1) {
+    P = one.P;
   } else if (in_smem) {
     P = State{ps[0], ps[32], ps[64]};
   } else {
     const size_t op = o - (size_t)g.B * g.C;  // written by this lane mq items ago
     P = State{__ldcg(a.ckpt + op), __ldcg(a.ckpt + op + g.plane), __ldcg(a.ckpt + op + 2 * g.plane)};
   }
-  const float w = in_smem ? walk_w(pst)[qi * 32 + lane] : __ldg(a.w + (eo & 0x7fffffff) % g.C);
+  const float w = mq == 1 ? one.w : (in_smem ? walk_w(pst)[qi * 32 + lane] : __ldg(a.w + (eo & 0x7fffffff) % g.C));
   const int n = j == g.nchunks - 1 ? g.T - j * kChunk : kChunk;
   P = combine(P, (float)n * w, State{rec_x(s), rec_y(s), rec_z(s)});
   if (valid) {
@@ -216,7 +228,9 @@ __device__ __noinline__ void fwd_walk_item(const FwdArgs& a, float* pst, int mq,
     a.ckpt[o + 2 * P3] = P.pp;
     if (j < g.nchunks - 1) rec_store(a.inc + o, a.tag, P.num, P.den, P.pp);
   }
-  if (in_smem) {
+  if (mq == 1) {
+    one.P = P;
+  } else if (in_smem) {
     ps[0] = P.num;
     ps[32] = P.den;
     ps[64] = P.pp;
@@ -242,6 +256,11 @@ __device__ __forceinline__ void fwd_walker(const FwdArgs& a, float* pst) {
   }
   Rec* ring = reinterpret_cast<Rec*>(walk_off(pst) + kWalkCap * 32);  // [kWalkRing][32]
   __syncwarp();
+  WalkOne one;
+  one.eo = walk_off_slow(g, 0);
+  one.w = __ldg(a.w + (one.eo & 0x7fffffff) % g.C);
+  one.P = empty_state();
+  auto offset_of = [&](int qi) { return mq == 1 ? one.eo : walk_offset(g, pst, mq, qi); };
   const uint32_t tag = a.tag;
   // Items are taken in blocks of kWalkRing: every record of the block not yet
   // current is copied into the ring together (one memory round trip), then
@@ -257,7 +276,7 @@ __device__ __forceinline__ void fwd_walker(const FwdArgs& a, float* pst) {
       for (int r = done; r < nb; ++r) {
         Rec* slot = ring + r * 32 + lane;
         if (first || !rec_ok(*slot, tag))
-          cp_async16(slot, a.agg + (size_t)j * jstride + (walk_offset(g, pst, mq, qi) & 0x7fffffff));
+          cp_async16(slot, a.agg + (size_t)j * jstride + (offset_of(qi) & 0x7fffffff));
         if (++qi == mq) {
           qi = 0;
           ++j;
@@ -269,8 +288,8 @@ __device__ __forceinline__ void fwd_walker(const FwdArgs& a, float* pst) {
       const int before = done;
       for (; done < nb; ++done) {
         const Rec rr = ring[done * 32 + lane];
-        if (!__all_sync(0xffffffffu, walk_offset(g, pst, mq, cq) < 0 || rec_ok(rr, tag))) break;
-        fwd_walk_item(a, pst, mq, cj, cq, rr, State{0.f, 0.f, 0.f});
+        if (!__all_sync(0xffffffffu, offset_of(cq) < 0 || rec_ok(rr, tag))) break;
+        fwd_walk_item(a, pst, mq, cj, cq, rr, one);
         if (++cq == mq) {
           cq = 0;
           ++cj;
