@@ -12,8 +12,10 @@ workloads: ``tiny``, ``l1b5`` (B=16 T=4096 C=2048), ``long`` (forward only,
 bf16 k/v, B=1 T=131072 C=2560) and ``decode`` (one fused decode step of
 L=32 layers, B=256, C=4096, state carried across steps).
 
-Timing: W untimed warm-up steps, then K steps.  L2 is flushed (a write of
-twice its size) before every timed step, outside the step's CUDA-event pair;
+Timing: W untimed warm-up steps; then the forward and the backward call are
+captured once as CUDA graphs (as a training loop would run them; ``--no-graph``
+calls the API every step instead) and K steps replay them.  L2 is flushed (a
+write of twice its size) before every timed step, outside the step's CUDA-event pair;
 the value is the elements of all ranks over the max over ranks of the summed
 per-step device times.  The dominant kernel's launches are timed with their
 own events on the launching stream for the roofline entry.  SM clocks and
@@ -63,6 +65,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="call the API every step instead of replaying CUDA graphs of the calls")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -285,25 +289,47 @@ class TrainingRun:
         self.dominant = "bwd_scan_kernel" if wl.backward else "fwd_scan_kernel"
         self.dominant_bytes = self.bytes_bwd if wl.backward else self.bytes_fwd
 
-    def step(self, ev=None):
-        w, u, k, v, gy = self.dev
+    def _forward(self):
+        w, u, k, v, _ = self.dev
         self.wkv.forward(w, u, k, v, y=self.y, ckpt=self.ckpt, workspace=self.ws_f)
+
+    def _backward(self):
+        w, u, k, v, gy = self.dev
+        self.wkv.backward(w, u, k, v, gy, ckpt=self.ckpt, gw=self.gw, gu=self.gu, gk=self.gk, gv=self.gv,
+                          workspace=self.ws_b)
+
+    def capture(self):
+        """CUDA graphs of the forward and the backward call on the run's
+        buffers (after warm-up: per-device set-up stays out of the capture),
+        replayed by the timed steps as a training loop would."""
+        torch = self.torch
+        self.g_fwd = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_fwd):
+            self._forward()
+        self.g_bwd = None
+        if self.wl.backward:
+            self.g_bwd = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.g_bwd):
+                self._backward()
+        torch.cuda.synchronize()
+
+    def step(self, ev=None):
+        graphs = getattr(self, "g_fwd", None) is not None
+        self.g_fwd.replay() if graphs else self._forward()
         if self.wl.backward:
             if ev is not None:
                 ev[0].record()
-            self.wkv.backward(w, u, k, v, gy, ckpt=self.ckpt, gw=self.gw, gu=self.gu, gk=self.gk, gv=self.gv,
-                              workspace=self.ws_b)
+            self.g_bwd.replay() if graphs else self._backward()
             if ev is not None:
                 ev[1].record()
 
     def step_dominant_events(self, ev):
         """A step with the dominant call bracketed by the events `ev`."""
-        w, u, k, v, gy = self.dev
         if self.wl.backward:
             self.step(ev)
         else:
             ev[0].record()
-            self.wkv.forward(w, u, k, v, y=self.y, ckpt=self.ckpt, workspace=self.ws_f)
+            self.g_fwd.replay() if getattr(self, "g_fwd", None) is not None else self._forward()
             ev[1].record()
 
     def check(self):
@@ -322,7 +348,9 @@ class TrainingRun:
     def e2e_step(self):
         for d, h in zip(self.dev, self.pin_in):
             d.copy_(h, non_blocking=True)
-        self.step()
+        self._forward()
+        if self.wl.backward:
+            self._backward()
         outs = [self.y] + ([self.gk, self.gv, self.gw, self.gu] if self.wl.backward else [])
         for h, d in zip(self.pin_out, outs):
             h.copy_(d, non_blocking=True)
@@ -361,6 +389,9 @@ class DecodeRun:
         self.t += 1
 
     step_dominant_events = step
+
+    def capture(self):
+        pass  # one launch per step, on a rotating input set: called directly
 
     def check(self):
         pass
@@ -485,6 +516,13 @@ def run_ours(args):
         run.step()
     torch.cuda.synchronize()
     run.check()
+    if not args.no_graph:
+        run.capture()
+        for _ in range(2):
+            flush()
+            run.step()
+        torch.cuda.synchronize()
+        run.check()
 
     attempts = []
     for attempt in range(2):
@@ -511,7 +549,9 @@ def run_ours(args):
               if args.workload == "decode" else
               {"workload": args.workload, "B": run.wl.B, "T": run.wl.T, "C": run.wl.C, "kv_dtype": run.wl.kv_dtype,
                "pass": "forward+backward" if run.wl.backward else "forward"})
-    wl_cfg.update({"l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}",
+    wl_cfg.update({"launch": "api calls per step" if (args.no_graph or args.workload == "decode") else
+                   "CUDA graphs of the forward and backward calls, captured once and replayed per step",
+                   "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}",
                    "checkpoints": "forward writes chunk checkpoints, backward reads them"
                    if args.workload != "decode" else "n/a"})
     out = {

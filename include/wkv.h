@@ -178,10 +178,11 @@ wkv_status wkv_decode_step(int L, int B, int C, const float* x, const float* x_p
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
  *   - Every call on a device shares the array and it keeps the last call's
- *     contents; each call clears its first 256 bytes (tile counters, error
- *     record) on `stream` before the kernel.  Calls that overlap on the GPU
- *     (different streams without ordering, or different host threads)
- *     race on the array: serialise them.
+ *     contents, which the next call relies on (its tile counters are back at
+ *     zero; a launch counter in it tags each call's intermediate results so
+ *     that an earlier call's are never taken for the current one's).  Calls
+ *     that overlap on the GPU (different streams without ordering, or
+ *     different host threads) race on the array: serialise them.
  *   - A bounded device-side wait that expires cannot be reported here (there
  *     is no workspace to check); use wkv_forward where that matters.
  * Errors: as wkv_forward, plus WKV_ERR_WORKSPACE for shapes too large.

@@ -17,7 +17,6 @@ namespace {
 
 constexpr long long kDefaultBudgetNs = 500LL * 1000 * 1000;
 
-std::atomic<uint64_t> g_epoch{0};
 std::atomic<long long> g_budget_ns{kDefaultBudgetNs};
 std::atomic<int> g_skip_chunk{-1};
 thread_local char g_last_error[256] = "";
@@ -90,10 +89,7 @@ BwdLayout bwd_layout(const ScanGeometry& g) {
   return l;
 }
 
-uint64_t next_epoch() { return g_epoch.fetch_add(1) + 1; }
 
-// Record tag of a launch: never 0 (the tag of a zero-filled workspace).
-uint32_t tag_of(uint64_t epoch) { return (uint32_t)((epoch - 1) % 0xFFFFFFFFull) + 1u; }
 
 char* bytes(void* p) { return static_cast<char*>(p); }
 
@@ -236,8 +232,6 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
   a.ticket = &a.eh->ticket[0];
   a.exited = &a.eh->exited[0];
   a.g = g;
-  a.epoch = next_epoch();
-  a.tag = tag_of(a.epoch);
   a.budget_ns = (uint64_t)g_budget_ns.load();
   a.debug_skip_chunk = g_skip_chunk.load();
   const int eb = kv_dtype == WKV_F32 ? 4 : 2;
@@ -280,8 +274,6 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
     f.exited = &hdr->exited[1];
     f.eh = hdr;
     f.g = g;
-    f.epoch = next_epoch();
-    f.tag = tag_of(f.epoch);
     f.budget_ns = budget;
     f.debug_skip_chunk = -1;
     f.use_tma = make_tile_map(&f.tk, k, B, T, C, 4) && make_tile_map(&f.tv, v, B, T, C, 4);
@@ -307,8 +299,6 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
   a.exited = &hdr->exited[2];
   a.eh = hdr;
   a.g = g;
-  a.epoch = next_epoch();
-  a.tag = tag_of(a.epoch);
   a.budget_ns = budget;
   a.debug_skip_chunk = skip;
   a.use_tma = make_tile_map(&a.tk, k, B, T, C, 4) && make_tile_map(&a.tv, v, B, T, C, 4) &&
@@ -320,7 +310,7 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
   r.part = a.part;
   r.slices = reinterpret_cast<float*>(bytes(workspace) + l.slices);
   r.count = reinterpret_cast<unsigned long long*>(bytes(workspace) + l.count);
-  r.tag = (unsigned int)a.epoch;
+  r.eh = hdr;
   r.gw = gw;
   r.gu = gu;
   r.rows = g.nchunks * g.B;

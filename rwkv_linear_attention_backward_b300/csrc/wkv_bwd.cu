@@ -169,7 +169,8 @@ struct BwdPend {
   State P;
 };
 
-__device__ __forceinline__ void bwd_summary(const BwdArgs& a, float* __restrict__ sk, const float* __restrict__ sv,
+__device__ __forceinline__ void bwd_summary(const BwdArgs& a, const Launch& L, float* __restrict__ sk,
+                                            const float* __restrict__ sv,
                                             const float* __restrict__ sg, BwdPend& p, float* xa, float* xb,
                                             float* xp) {
   constexpr int S = kCtaChannels;
@@ -222,7 +223,7 @@ __device__ __forceinline__ void bwd_summary(const BwdArgs& a, float* __restrict_
     exact_zero_adjoint(sk, sv, sg, p.len, p.w, p.u, xa, xb, xp, la, lb);
   }
   if (p.j > 0 && p.j != a.debug_skip_chunk && p.c < g.C)  // chunk 0's adjoint is never needed
-    rec_store(a.ragg + ((size_t)p.j * g.B + p.b) * g.C + p.c, a.tag, la, lb, p.P.pp);
+    rec_store(a.ragg + ((size_t)p.j * g.B + p.b) * g.C + p.c, L.tag, la, lb, p.P.pp);
 }
 
 // gk, gv and the gw, gu partials of a tile, given the adjoint X carried
@@ -328,8 +329,8 @@ struct WalkOne {
   int eo;
 };
 
-__device__ __forceinline__ void bwd_walk_item(const BwdArgs& a, float* pst, int mq, int j, int qi, Rec s,
-                                              WalkOne& one) {
+__device__ __forceinline__ void bwd_walk_item(const BwdArgs& a, const Launch& L, float* pst, int mq, int j, int qi,
+                                              Rec s, WalkOne& one) {
   const ScanGeometry& g = a.g;
   const int lane = threadIdx.x & 31;
   const int eo = mq == 1 ? one.eo : walk_offset(g, pst, mq, qi);
@@ -352,7 +353,7 @@ __device__ __forceinline__ void bwd_walk_item(const BwdArgs& a, float* pst, int 
                              : (in_smem ? walk_w(pst)[qi * 32 + lane] : (float)kChunk * __ldg(a.w + (eo & 0x7fffffff) % g.C));
     X = fold_adj(X, Lw, nx);
   }
-  if (valid) rec_store(a.rinc + o, a.tag, X.la, X.lb, X.f);
+  if (valid) rec_store(a.rinc + o, L.tag, X.la, X.lb, X.f);
   if (mq == 1) {
     one.X = X;
   } else if (in_smem) {
@@ -362,7 +363,7 @@ __device__ __forceinline__ void bwd_walk_item(const BwdArgs& a, float* pst, int 
   }
 }
 
-__device__ __forceinline__ void bwd_walker(const BwdArgs& a, float* pst) {
+__device__ __forceinline__ void bwd_walker(const BwdArgs& a, const Launch& L, float* pst) {
   const ScanGeometry& g = a.g;
   const int lane = threadIdx.x & 31;
   const int nchain = g.B * g.nwg;
@@ -386,7 +387,7 @@ __device__ __forceinline__ void bwd_walker(const BwdArgs& a, float* pst) {
   one.Lw = (float)kChunk * __ldg(a.w + (one.eo & 0x7fffffff) % g.C);
   one.X = Adj{0.f, 0.f, 0.f};
   auto offset_of = [&](int qi) { return mq == 1 ? one.eo : walk_offset(g, pst, mq, qi); };
-  const uint32_t tag = a.tag;
+  const uint32_t tag = L.tag;
   // Blocks of kWalkRing items, as in the forward walker.
   int bj = g.nchunks - 1, bq = 0;  // first item of the block
   for (long base = 0; base < nitems; base += kWalkRing) {
@@ -412,7 +413,7 @@ __device__ __forceinline__ void bwd_walker(const BwdArgs& a, float* pst) {
       for (; done < nb; ++done) {
         const Rec rr = ring[done * 32 + lane];
         if (!__all_sync(0xffffffffu, offset_of(cq) < 0 || rec_ok(rr, tag))) break;
-        bwd_walk_item(a, pst, mq, cj, cq, rr, one);
+        bwd_walk_item(a, L, pst, mq, cj, cq, rr, one);
         if (++cq == mq) {
           cq = 0;
           --cj;
@@ -422,9 +423,9 @@ __device__ __forceinline__ void bwd_walker(const BwdArgs& a, float* pst) {
         t0 = globaltimer();
         continue;
       }
-      if (__shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == a.epoch) return;
+      if (__shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == L.epoch) return;
       if (__shfl_sync(0xffffffffu, globaltimer(), 0) - t0 > a.budget_ns) {
-        if (lane == 0) record_error(a.eh, kDevErrTimeout, a.epoch);
+        if (lane == 0) record_error(a.eh, kDevErrTimeout, L.epoch);
         return;
       }
     }
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) bwd_scan_kernel(const __grid_
   auto* ctl = reinterpret_cast<PipeCtl<NS>*>(smem + (size_t)NS * 3 * TILE * sizeof(float));
   // walker shared memory (kWalkSmem bytes), 128-byte aligned
   float* pst = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(ctl) + pipe_ctl_bytes<NS>());
-  pipe_init(ctl);
+  const Launch L = pipe_init(ctl, a.eh);
   const ScanGeometry& g = a.g;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) bwd_scan_kernel(const __grid_
       tma_prefetch_desc(&a.tg);
     }
     producer_loop<NS>(ctl, a.ticket, g.ntiles, a.use_tma != 0, (uint32_t)(3 * TILE * sizeof(float)), a.budget_ns,
-                      a.eh, a.epoch, [&](unsigned int t, int s, uint64_t* bar) {
+                      a.eh, L.epoch, [&](unsigned int t, int s, uint64_t* bar) {
                         const int jr = t / per_j;
                         const int j = g.nchunks - 1 - jr;  // last chunk first
                         const int rem = t - jr * per_j;
@@ -475,13 +476,32 @@ __global__ void __launch_bounds__(kPipeThreads, 2) bwd_scan_kernel(const __grid_
                         }
                       });
   } else if (warp == kWalkerWarp) {
-    bwd_walker(a, pst);
+    bwd_walker(a, L, pst);
   } else {
     // Consumer: a tile is summarised as soon as its stage lands, and the
     // oldest summarised tile is finished once its carried adjoint is
     // published; neither step blocks the other (see the forward kernel).
     float xa[kChunk], xb[kChunk], xp[kChunk];  // per-token form's states (local memory)
-    BwdPend pend[NS];                           // per stage (local memory)
+    // Per-lane results of a tile's summary wait for its finish in registers,
+    // one set per stage, selected with constant indices (a stage-indexed
+    // array would live in local memory); the tile's coordinates come back
+    // from its ticket, still in the control block until the stage is
+    // released.
+    float sF[NS], sS0[NS], sEw[NS], sEu[NS], sPn[NS], sPd[NS], sPp[NS];
+    bool sFast[NS];
+    auto decode = [&](int t, BwdPend& p) {
+      const int jr = t / per_j;
+      const int rem = t - jr * per_j;
+      p.j = g.nchunks - 1 - jr;
+      p.b = rem / g.ncb;
+      const int c0 = (rem - p.b * g.ncb) * kCtaChannels + warp * 32;
+      p.live = c0 < g.C;
+      p.c = c0 + lane;
+      p.len = min(kChunk, g.T - p.j * kChunk);
+      const int cc = p.c < g.C ? p.c : g.C - 1;
+      p.w = __ldg(a.w + cc);
+      p.u = __ldg(a.u + cc);
+    };
     int ns = 0, nf = 0, count = 0;
     uint32_t ps = 0;
     bool end = false, failed = false, idle = false;
@@ -494,26 +514,27 @@ __global__ void __launch_bounds__(kPipeThreads, 2) bwd_scan_kernel(const __grid_
           end = true;
           break;
         }
-        BwdPend p;  // in registers while in use; parked in pend[] between summary and finish
-        const int jr = t / per_j;
-        const int rem = t - jr * per_j;
-        p.j = g.nchunks - 1 - jr;
-        p.b = rem / g.ncb;
-        const int cb = rem - p.b * g.ncb;
-        const int c0 = cb * kCtaChannels + warp * 32;
-        p.live = c0 < g.C;
-        p.c = c0 + lane;
-        p.len = min(kChunk, g.T - p.j * kChunk);
+        BwdPend p;
+        decode(t, p);
         if (p.live && !failed) {
-          const int cc = p.c < g.C ? p.c : g.C - 1;
-          p.w = __ldg(a.w + cc);
-          p.u = __ldg(a.u + cc);
           p.ew = expf(-p.w);
           p.eu = expf(p.u);
           float* sk = stages + (size_t)(3 * ns) * TILE + warp * 32 + lane;
-          bwd_summary(a, sk, sk + TILE, sk + 2 * TILE, p, xa, xb, xp);
+          bwd_summary(a, L, sk, sk + TILE, sk + 2 * TILE, p, xa, xb, xp);
+#pragma unroll
+          for (int q = 0; q < NS; ++q) {
+            if (q == ns) {
+              sF[q] = p.F;
+              sS0[q] = p.s0;
+              sEw[q] = p.ew;
+              sEu[q] = p.eu;
+              sPn[q] = p.P.num;
+              sPd[q] = p.P.den;
+              sPp[q] = p.P.pp;
+              sFast[q] = p.fast;
+            }
+          }
         }
-        pend[ns] = p;
         ++count;
         if (++ns == NS) {
           ns = 0;
@@ -522,18 +543,32 @@ __global__ void __launch_bounds__(kPipeThreads, 2) bwd_scan_kernel(const __grid_
         progress = true;
       }
       if (count > 0) {
-        const BwdPend p = pend[nf];
+        BwdPend p;
+        decode(*(volatile int*)&ctl->tile[nf], p);
         bool ready = true;
         Adj X{0.f, 0.f, 0.f};
         if (p.live && !failed && p.j < g.nchunks - 1) {
           const bool valid = p.c < g.C;
           const Rec r = rec_load(a.rinc + ((size_t)(p.j + 1) * g.B + p.b) * g.C + (valid ? p.c : 0));
-          ready = __all_sync(0xffffffffu, !valid || rec_ok(r, a.tag));
+          ready = __all_sync(0xffffffffu, !valid || rec_ok(r, L.tag));
           X = Adj{rec_x(r), rec_y(r), rec_z(r)};
         }
         if (ready) {
           if (p.live && !failed) {
+#pragma unroll
+            for (int q = 0; q < NS; ++q) {
+              if (q == nf) {
+                p.F = sF[q];
+                p.s0 = sS0[q];
+                p.ew = sEw[q];
+                p.eu = sEu[q];
+                p.P = State{sPn[q], sPd[q], sPp[q]};
+                p.fast = sFast[q];
+              }
+            }
             float* sk = stages + (size_t)(3 * nf) * TILE + warp * 32 + lane;
+            // one predicated body for full and partial chunks: a full-chunk
+            // specialisation would not fit two CTAs' registers (it spills)
             bwd_finish<false>(a, sk, sk + TILE, sk + 2 * TILE, p, X, xa, xb, xp);
             // this warp wrote into the stage; the next TMA fill must come after
             fence_proxy_async_smem();
@@ -558,19 +593,19 @@ __global__ void __launch_bounds__(kPipeThreads, 2) bwd_scan_kernel(const __grid_
       } else if (now - idle_since > a.budget_ns) {
         if (failed) break;  // nothing more will arrive
         if (lane == 0) {
-          record_error(a.eh, kDevErrTimeout, a.epoch);
+          record_error(a.eh, kDevErrTimeout, L.epoch);
           *(volatile int*)&ctl->abort = 1;
         }
         failed = true;  // later tiles are only drained
         idle_since = now;
       }
-      if (!failed && __shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == a.epoch) {
+      if (!failed && __shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == L.epoch) {
         failed = true;
         if (lane == 0) *(volatile int*)&ctl->abort = 1;
       }
     }
   }
-  pipe_exit(a.ticket, a.exited);
+  pipe_exit(a.ticket, a.exited, a.eh, L.epoch);
 }
 
 // gw[c] = sum over the partial rows of part[0][.][c], gu likewise from
@@ -620,15 +655,18 @@ __global__ void __launch_bounds__(256) reduce_kernel(const ReduceArgs a) {
     __threadfence();
     __syncwarp();
     if (lane == 0) {
-      // arrivals of this launch; a word left by another launch (another tag)
-      // counts as zero, so the counters need no reset between launches
+      // arrivals of this launch, tagged with the workspace's sequence number
+      // (advanced by the backward scan before this kernel runs); a word left
+      // by another launch (another tag) counts as zero, so the counters need
+      // no reset between launches
+      const uint32_t tag = tag_of(*(volatile const unsigned long long*)&a.eh->seq);
       unsigned long long old = *(volatile unsigned long long*)(a.count + grp), seen;
       do {
         seen = old;
-        const unsigned long long mine = (seen >> 32) == a.tag ? seen + 1ull : ((unsigned long long)a.tag << 32) | 1ull;
+        const unsigned long long mine = (seen >> 32) == tag ? seen + 1ull : ((unsigned long long)tag << 32) | 1ull;
         old = atomicCAS(a.count + grp, seen, mine);
       } while (old != seen);
-      const unsigned int n = (seen >> 32) == a.tag ? (unsigned int)(seen & 0xffffffffu) + 1u : 1u;
+      const unsigned int n = (seen >> 32) == tag ? (unsigned int)(seen & 0xffffffffu) + 1u : 1u;
       last = n == (unsigned int)a.nslice;
     }
     __syncwarp();

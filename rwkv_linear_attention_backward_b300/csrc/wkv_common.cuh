@@ -137,9 +137,22 @@ struct WsHeader {
   unsigned int error;        // first device error code since the last check, 0 if none
   unsigned int pad0;
   unsigned long long abort;  // epoch of the last launch that gave up a wait
-  unsigned int pad[52];
+  unsigned long long seq;    // epoch of the last launch that used this workspace
+  unsigned int pad[50];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
+
+// A launch's identity: its epoch (1 + the workspace's sequence number when
+// the launch starts, read on the device, so that a launch replayed from a
+// CUDA graph still gets a new one) and the record tag derived from it.
+struct Launch {
+  unsigned long long epoch;
+  uint32_t tag;
+};
+
+__host__ __device__ __forceinline__ uint32_t tag_of(unsigned long long epoch) {
+  return (uint32_t)((epoch - 1) % 0xFFFFFFFFull) + 1u;  // never 0: the tag of a zero-filled workspace
+}
 
 // Records that this launch (epoch) gave up: the code for the host, the epoch
 // so the launch's other waits stop at once.
@@ -158,8 +171,8 @@ namespace wkv {
 // 128-bit accesses (single-copy atomic), so a reader that sees its launch's
 // tag sees the values written with it: no fence and no separate flag is
 // needed.  The tag is derived from the launch epoch and is never 0 (the tag
-// of a zero-filled workspace), so records left by earlier launches in a
-// reused workspace never read as current.
+// of a zero-filled workspace); epochs increase from launch to launch on a
+// workspace, so records left by earlier launches never read as current.
 struct Rec {
   unsigned long long lo;  // value 0 | value 1 << 32
   unsigned long long hi;  // value 2 | tag << 32

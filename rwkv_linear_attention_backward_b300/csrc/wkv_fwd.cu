@@ -79,8 +79,8 @@ struct FwdPend {
 };
 
 template <typename KV>
-__device__ __forceinline__ void fwd_summary(const FwdArgs& a, const KV* __restrict__ sk, const KV* __restrict__ sv,
-                                            FwdPend& p) {
+__device__ __forceinline__ void fwd_summary(const FwdArgs& a, const Launch& L, const KV* __restrict__ sk,
+                                            const KV* __restrict__ sv, FwdPend& p) {
   constexpr int S = kCtaChannels;
   const ScanGeometry& g = a.g;
   const int n = p.len;
@@ -114,7 +114,7 @@ __device__ __forceinline__ void fwd_summary(const FwdArgs& a, const KV* __restri
     for (int i = 0; i < p.len; ++i) step(s, to_f32<KV>(sk[i * S]), to_f32<KV>(sv[i * S]), p.w);
   }
   if (p.j == a.debug_skip_chunk) return;  // fault injection: this chunk's summaries are never published
-  if (p.c < g.C) rec_store(a.agg + ((size_t)p.j * g.B + p.b) * g.C + p.c, a.tag, s.num, s.den, s.pp);
+  if (p.c < g.C) rec_store(a.agg + ((size_t)p.j * g.B + p.b) * g.C + p.c, L.tag, s.num, s.den, s.pp);
 }
 
 // The outputs of a tile from the state P carried into its chunk.
@@ -198,8 +198,8 @@ struct WalkOne {
 // the chunk's summary s.  Inlined once into the walker's rolled loop (a call
 // would save registers to local memory, which misses the small L1 left
 // beside the shared memory).
-__device__ __forceinline__ void fwd_walk_item(const FwdArgs& a, float* pst, int mq, int j, int qi, Rec s,
-                                              WalkOne& one) {
+__device__ __forceinline__ void fwd_walk_item(const FwdArgs& a, const Launch& L, float* pst, int mq, int j, int qi,
+                                              Rec s, WalkOne& one) {
   const ScanGeometry& g = a.g;
   const int lane = threadIdx.x & 31;
   const int eo = mq == 1 ? one.eo : walk_offset(g, pst, mq, qi);
@@ -226,7 +226,7 @@ __device__ __forceinline__ void fwd_walk_item(const FwdArgs& a, float* pst, int 
     a.ckpt[o] = P.num;
     a.ckpt[o + P3] = P.den;
     a.ckpt[o + 2 * P3] = P.pp;
-    if (j < g.nchunks - 1) rec_store(a.inc + o, a.tag, P.num, P.den, P.pp);
+    if (j < g.nchunks - 1) rec_store(a.inc + o, L.tag, P.num, P.den, P.pp);
   }
   if (mq == 1) {
     one.P = P;
@@ -237,7 +237,7 @@ __device__ __forceinline__ void fwd_walk_item(const FwdArgs& a, float* pst, int 
   }
 }
 
-__device__ __forceinline__ void fwd_walker(const FwdArgs& a, float* pst) {
+__device__ __forceinline__ void fwd_walker(const FwdArgs& a, const Launch& L, float* pst) {
   const ScanGeometry& g = a.g;
   const int lane = threadIdx.x & 31;
   const int nchain = g.B * g.nwg;
@@ -261,7 +261,7 @@ __device__ __forceinline__ void fwd_walker(const FwdArgs& a, float* pst) {
   one.w = __ldg(a.w + (one.eo & 0x7fffffff) % g.C);
   one.P = empty_state();
   auto offset_of = [&](int qi) { return mq == 1 ? one.eo : walk_offset(g, pst, mq, qi); };
-  const uint32_t tag = a.tag;
+  const uint32_t tag = L.tag;
   // Items are taken in blocks of kWalkRing: every record of the block not yet
   // current is copied into the ring together (one memory round trip), then
   // the current prefix is folded in order; the rest is copied again.
@@ -289,7 +289,7 @@ __device__ __forceinline__ void fwd_walker(const FwdArgs& a, float* pst) {
       for (; done < nb; ++done) {
         const Rec rr = ring[done * 32 + lane];
         if (!__all_sync(0xffffffffu, offset_of(cq) < 0 || rec_ok(rr, tag))) break;
-        fwd_walk_item(a, pst, mq, cj, cq, rr, one);
+        fwd_walk_item(a, L, pst, mq, cj, cq, rr, one);
         if (++cq == mq) {
           cq = 0;
           ++cj;
@@ -299,9 +299,9 @@ __device__ __forceinline__ void fwd_walker(const FwdArgs& a, float* pst) {
         t0 = globaltimer();
         continue;
       }
-      if (__shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == a.epoch) return;
+      if (__shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == L.epoch) return;
       if (__shfl_sync(0xffffffffu, globaltimer(), 0) - t0 > a.budget_ns) {
-        if (lane == 0) record_error(a.eh, kDevErrTimeout, a.epoch);
+        if (lane == 0) record_error(a.eh, kDevErrTimeout, L.epoch);
         return;
       }
     }
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) fwd_scan_kernel(const __grid_
   auto* ctl = reinterpret_cast<PipeCtl<NS>*>(smem + (size_t)NS * 2 * TILE * sizeof(KV));
   // walker shared memory (kWalkSmem bytes), 128-byte aligned
   float* pst = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(ctl) + pipe_ctl_bytes<NS>());
-  pipe_init(ctl);
+  const Launch L = pipe_init(ctl, a.eh);
   const ScanGeometry& g = a.g;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) fwd_scan_kernel(const __grid_
       tma_prefetch_desc(&a.tv);
     }
     producer_loop<NS>(ctl, a.ticket, g.ntiles, a.use_tma != 0, (uint32_t)(2 * TILE * sizeof(KV)), a.budget_ns, a.eh,
-                      a.epoch, [&](unsigned int t, int s, uint64_t* bar) {
+                      L.epoch, [&](unsigned int t, int s, uint64_t* bar) {
                         const int j = t / per_j;
                         const int rem = t - j * per_j;
                         const int b = rem / g.ncb;
@@ -351,13 +351,32 @@ __global__ void __launch_bounds__(kPipeThreads, 2) fwd_scan_kernel(const __grid_
                         }
                       });
   } else if (warp == kWalkerWarp) {
-    fwd_walker(a, pst);
+    fwd_walker(a, L, pst);
   } else {
     // Consumer: a tile is summarised as soon as its stage lands (every
     // ticketed tile's summary reaches the walkers without waiting on other
     // tiles), and the oldest summarised tile is re-run once its carried state
     // is published; neither step blocks the other.
-    FwdPend pend[NS];  // per stage (local memory)
+    // Per-lane results of a tile's summary wait for its re-run in registers,
+    // one set per stage, selected with constant indices (a stage-indexed
+    // array would live in local memory).  The tile's coordinates come back
+    // from its ticket, still in the control block until the stage is
+    // released.
+    float sF[NS], sK[NS], sE[NS];
+    bool sFast[NS];
+    auto decode = [&](int t, FwdPend& p) {
+      const int j = t / per_j;
+      const int rem = t - j * per_j;
+      p.j = j;
+      p.b = rem / g.ncb;
+      const int c0 = (rem - p.b * g.ncb) * kCtaChannels + warp * 32;
+      p.live = c0 < g.C;
+      p.c = c0 + lane;
+      p.len = min(kChunk, g.T - j * kChunk);
+      const int cc = p.c < g.C ? p.c : g.C - 1;
+      p.w = __ldg(a.w + cc);
+      p.u = __ldg(a.u + cc);
+    };
     int ns = 0, nf = 0, count = 0;
     uint32_t ps = 0;
     bool end = false, failed = false, idle = false;
@@ -370,25 +389,22 @@ __global__ void __launch_bounds__(kPipeThreads, 2) fwd_scan_kernel(const __grid_
           end = true;
           break;
         }
-        FwdPend p;  // in registers while in use; parked in pend[] between summary and re-run
-        const int j = t / per_j;
-        const int rem = t - j * per_j;
-        p.j = j;
-        p.b = rem / g.ncb;
-        const int cb = rem - p.b * g.ncb;
-        const int c0 = cb * kCtaChannels + warp * 32;
-        p.live = c0 < g.C;
-        p.c = c0 + lane;
-        p.len = min(kChunk, g.T - j * kChunk);
+        FwdPend p;
+        decode(t, p);
         if (p.live && !failed) {
-          const int cc = p.c < g.C ? p.c : g.C - 1;
-          p.w = __ldg(a.w + cc);
-          p.u = __ldg(a.u + cc);
           p.ew = expf(-p.w);
           const KV* sk = stages + (size_t)(2 * ns) * TILE + warp * 32 + lane;
-          fwd_summary<KV>(a, sk, sk + TILE, p);
+          fwd_summary<KV>(a, L, sk, sk + TILE, p);
+#pragma unroll
+          for (int q = 0; q < NS; ++q) {
+            if (q == ns) {
+              sF[q] = p.F;
+              sK[q] = p.kmin;
+              sE[q] = p.ew;
+              sFast[q] = p.fast;
+            }
+          }
         }
-        pend[ns] = p;
         ++count;
         if (++ns == NS) {
           ns = 0;
@@ -397,17 +413,27 @@ __global__ void __launch_bounds__(kPipeThreads, 2) fwd_scan_kernel(const __grid_
         progress = true;
       }
       if (count > 0) {
-        const FwdPend p = pend[nf];
+        FwdPend p;
+        decode(*(volatile int*)&ctl->tile[nf], p);
         bool ready = true;
         State P = empty_state();
         if (p.live && !failed && p.j > 0) {
           const bool valid = p.c < g.C;
           const Rec r = rec_load(a.inc + ((size_t)(p.j - 1) * g.B + p.b) * g.C + (valid ? p.c : 0));
-          ready = __all_sync(0xffffffffu, !valid || rec_ok(r, a.tag));
+          ready = __all_sync(0xffffffffu, !valid || rec_ok(r, L.tag));
           P = State{rec_x(r), rec_y(r), rec_z(r)};
         }
         if (ready) {
           if (p.live && !failed) {
+#pragma unroll
+            for (int q = 0; q < NS; ++q) {
+              if (q == nf) {
+                p.F = sF[q];
+                p.kmin = sK[q];
+                p.ew = sE[q];
+                p.fast = sFast[q];
+              }
+            }
             const KV* sk = stages + (size_t)(2 * nf) * TILE + warp * 32 + lane;
             fwd_rerun<KV, WRITE_Y>(a, sk, sk + TILE, p, P);
           }
@@ -431,19 +457,19 @@ __global__ void __launch_bounds__(kPipeThreads, 2) fwd_scan_kernel(const __grid_
       } else if (now - idle_since > a.budget_ns) {
         if (failed) break;  // nothing more will arrive
         if (lane == 0) {
-          record_error(a.eh, kDevErrTimeout, a.epoch);
+          record_error(a.eh, kDevErrTimeout, L.epoch);
           *(volatile int*)&ctl->abort = 1;
         }
         failed = true;  // later tiles are only drained
         idle_since = now;
       }
-      if (!failed && __shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == a.epoch) {
+      if (!failed && __shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&a.eh->abort, 0) == L.epoch) {
         failed = true;
         if (lane == 0) *(volatile int*)&ctl->abort = 1;
       }
     }
   }
-  pipe_exit(a.ticket, a.exited);
+  pipe_exit(a.ticket, a.exited, a.eh, L.epoch);
 }
 
 template <typename KV, bool WRITE_Y>

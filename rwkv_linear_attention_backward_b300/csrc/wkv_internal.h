@@ -48,8 +48,6 @@ struct FwdArgs {
   unsigned int* exited;  // CTAs of this launch that have finished
   WsHeader* eh;          // where an expired wait is recorded (checked by the host)
   ScanGeometry g;
-  uint64_t epoch;
-  uint32_t tag;          // record tag of this launch (never 0)
   uint64_t budget_ns;
   int debug_skip_chunk;  // -1: off
   int use_tma;
@@ -75,8 +73,6 @@ struct BwdArgs {
   unsigned int* exited;
   WsHeader* eh;
   ScanGeometry g;
-  uint64_t epoch;
-  uint32_t tag;
   uint64_t budget_ns;
   int debug_skip_chunk;
   int use_tma;
@@ -86,7 +82,7 @@ struct ReduceArgs {
   const float* part;    // [2][rows][C]
   float* slices;        // [nslice][2][C] per-slice sums
   unsigned long long* count;  // [ceil(C / 32)] arrival counters, (tag << 32) | arrivals
-  unsigned int tag;           // this launch's tag: a counter with another tag reads as zero
+  const WsHeader* eh;         // its sequence number tags the counters: another tag reads as zero
   float* gw;
   float* gu;
   int rows;             // nchunks * B

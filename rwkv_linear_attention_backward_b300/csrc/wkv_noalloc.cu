@@ -79,16 +79,10 @@ extern "C" wkv_status wkv_forward_noalloc(int B, int T, int C, int kv_dtype, con
   void* scratch = nullptr;
   const wkv_status st = scratch_address(&scratch);
   if (st != WKV_OK) return st;
-  // The array keeps the previous call's contents.  The tile counters and the
-  // error record in its first 256 bytes must start at zero; everything else
-  // is tagged with the launch or written before it is read.
-  cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(WsHeader), static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) {
-    char msg[200];
-    std::snprintf(msg, sizeof(msg), "wkv_forward_noalloc: clearing the scratch header failed: %s",
-                  cudaGetErrorString(e));
-    set_last_error(msg);
-    return WKV_ERR_CUDA;
-  }
+  // The array keeps the previous call's contents, and nothing in it needs
+  // clearing: it is zero when the library loads, every launch leaves its
+  // tile counters at zero, and the sequence number in its header must carry
+  // on from call to call (the tag of each call's records comes from it, so
+  // records of an earlier call never read as current).
   return wkv_forward(B, T, C, kv_dtype, w, u, k, v, y, ckpt, scratch, kNoAllocScratchBytes, stream);
 }

@@ -128,6 +128,7 @@ struct PipeCtl {
   uint64_t empty[NSTAGE];  // one arrival per consumer warp
   int tile[NSTAGE];        // ticket staged in the stage, -1 = no more tiles
   int abort;               // set when this CTA gave up a wait
+  unsigned long long epoch;  // this launch's epoch (see Launch)
 };
 
 // Bytes reserved for the control block: a multiple of 128, so that what
@@ -137,17 +138,23 @@ __host__ __device__ constexpr size_t pipe_ctl_bytes() {
   return (sizeof(PipeCtl<NSTAGE>) + 127) / 128 * 128;
 }
 
+// Initialises the control block and returns this launch's identity: every
+// CTA reads the workspace's sequence number before any CTA of the launch can
+// advance it (that happens in pipe_exit, after every CTA has finished).
 template <int NSTAGE>
-__device__ __forceinline__ void pipe_init(PipeCtl<NSTAGE>* ctl) {
+__device__ __forceinline__ Launch pipe_init(PipeCtl<NSTAGE>* ctl, const WsHeader* h) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&ctl->full[s], 1);
       mbar_init(&ctl->empty[s], kConsumerWarps);
     }
     ctl->abort = 0;
+    ctl->epoch = *(volatile const unsigned long long*)&h->seq + 1ull;
     mbar_init_fence();
   }
   __syncthreads();
+  const unsigned long long e = ctl->epoch;
+  return Launch{e, tag_of(e)};
 }
 
 // Records that this launch (epoch) gave up a wait, CTA-wide and device-wide.
@@ -208,14 +215,17 @@ __device__ __forceinline__ void producer_loop(PipeCtl<NSTAGE>* ctl, unsigned int
 }
 
 // Last CTA out resets the launch's ticket counter for the next launch that
-// uses the same workspace (every CTA has stopped taking tickets by then).
-__device__ __forceinline__ void pipe_exit(unsigned int* ticket, unsigned int* exited) {
+// uses the same workspace (every CTA has stopped taking tickets by then) and
+// advances the workspace's sequence number to this launch's epoch.
+__device__ __forceinline__ void pipe_exit(unsigned int* ticket, unsigned int* exited, WsHeader* h,
+                                          unsigned long long epoch) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(exited, 1u) == gridDim.x - 1) {
       atomicExch(ticket, 0u);
       atomicExch(exited, 0u);
+      atomicExch(&h->seq, epoch);
     }
   }
 }

@@ -140,3 +140,41 @@ def test_expired_wait_is_reported(oracle, wkv, which):
     wkv.workspace_check(ws)
     assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "y after timeout")
     assert_close(gk, oracle.backward_adjoint(w, u, k, v, gy)[2], TOL_GRAD, "gk after timeout")
+
+
+def test_graph_replay_with_new_inputs(wkv):
+    """Forward + backward captured once in a CUDA graph and replayed after the
+    inputs change in place give the results of direct calls on the new
+    inputs (every launch takes a fresh tag on the device, so results carried
+    between CTAs by an earlier replay are never taken for the current one)."""
+    B, T, C = 2, 700, 160
+    a = cuda(*inputs.training_inputs(B, T, C, seed=31, k_std=3.0))
+    b = cuda(*inputs.training_inputs(B, T, C, seed=32, k_std=3.0))
+    w, u, k, v, gy = (t.clone() for t in a)
+    y = torch.empty(B, T, C, device="cuda")
+    ck = torch.empty(wkv.checkpoint_floats(B, T, C), device="cuda")
+    gw, gu = torch.empty(C, device="cuda"), torch.empty(C, device="cuda")
+    gk, gv = torch.empty(B, T, C, device="cuda"), torch.empty(B, T, C, device="cuda")
+    wsf = wkv.Workspace(wkv.forward_workspace_bytes(B, T, C))
+    wsb = wkv.Workspace(wkv.backward_workspace_bytes(B, T, C))
+
+    def step():
+        wkv.forward(w, u, k, v, y=y, ckpt=ck, workspace=wsf)
+        wkv.backward(w, u, k, v, gy, ckpt=ck, gw=gw, gu=gu, gk=gk, gv=gv, workspace=wsb)
+
+    step()  # first calls: per-device set-up happens outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for src in (a, b, a, b):
+        for dst, s in zip((w, u, k, v, gy), src):
+            dst.copy_(s)
+        g.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in (y, ck, gw, gu, gk, gv)]
+        ref = _run(wkv, *src)
+        for x, r_, n in zip(got, ref, ("y", "ckpt", "gw", "gu", "gk", "gv")):
+            assert torch.equal(x, r_), n
+    wkv.workspace_check(wsf)
+    wkv.workspace_check(wsb)
