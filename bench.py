@@ -67,6 +67,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-graph", action="store_true",
                     help="call the API every step instead of replaying CUDA graphs of the calls")
+    ap.add_argument("--scan-mode", default="auto", choices=["auto", "chunked", "sequential"],
+                    help="scan strategy of the forward/backward calls (default: the library's choice by shape)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -504,6 +506,10 @@ def run_ours(args):
     from rwkv_linear_attention_backward_b300 import build
 
     build.build()
+    if args.scan_mode != "auto":
+        from rwkv_linear_attention_backward_b300 import binding
+
+        binding.set_scan_mode(args.scan_mode)
     steps = args.steps or DEFAULT_STEPS[args.workload]
     run = DecodeRun(device) if args.workload == "decode" else TrainingRun(args.workload, device)
     stream = torch.cuda.current_stream()
@@ -552,6 +558,7 @@ def run_ours(args):
     wl_cfg.update({"launch": "api calls per step" if (args.no_graph or args.workload == "decode") else
                    "CUDA graphs of the forward and backward calls, captured once and replayed per step",
                    "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}",
+                   "scan_mode": args.scan_mode,
                    "checkpoints": "forward writes chunk checkpoints, backward reads them"
                    if args.workload != "decode" else "n/a"})
     out = {

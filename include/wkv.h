@@ -62,6 +62,9 @@ typedef enum {
 
 typedef enum { WKV_F32 = 0, WKV_BF16 = 1 } wkv_dtype;
 
+/* Scan strategies of wkv_forward / wkv_backward (see wkv_debug_set_scan_mode). */
+typedef enum { WKV_SCAN_AUTO = 0, WKV_SCAN_CHUNKED = 1, WKV_SCAN_SEQUENTIAL = 2 } wkv_scan_mode;
+
 /* Human-readable name of a status code.  Never NULL. */
 const char* wkv_status_string(int status);
 
@@ -200,6 +203,22 @@ wkv_status wkv_forward_noalloc(int B, int T, int C, int kv_dtype, const float* w
  */
 wkv_status wkv_debug_set_wait_budget_ns(long long ns);
 wkv_status wkv_debug_set_skip_chunk(int chunk);
+
+/*
+ * wkv_debug_set_scan_mode: which kernels wkv_forward and wkv_backward run
+ * (process-wide; for tests and measurements).
+ *   WKV_SCAN_AUTO (default): sequential when the shape has at least as many
+ *     columns (B x ceil(C / 32)) as the GPU has SMs, else chunked.
+ *   WKV_SCAN_CHUNKED: time cut into chunks spread over all CTAs, chunk
+ *     results carried between CTAs (every shape).
+ *   WKV_SCAN_SEQUENTIAL: one warp per column walking its chunks in order,
+ *     nothing exchanged between CTAs (every shape; slow when columns are few).
+ * Both strategies compute the same recurrence with the same per-chunk
+ * arithmetic; outputs agree to rounding (bitwise on lanes whose chunks all
+ * stay on the fixed-scale form).  wkv_debug_set_skip_chunk affects the
+ * chunked kernels only.  Errors: WKV_ERR_INVALID_ARG for another value.
+ */
+wkv_status wkv_debug_set_scan_mode(int mode);
 
 #ifdef __cplusplus
 }

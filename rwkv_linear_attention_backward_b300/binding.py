@@ -44,6 +44,7 @@ _SIGNATURES = {
     "wkv_forward_noalloc": ([_i, _i, _i, _i] + [_vp] * 6 + [_vp], _i),
     "wkv_debug_set_wait_budget_ns": ([_ll], _i),
     "wkv_debug_set_skip_chunk": ([_i], _i),
+    "wkv_debug_set_scan_mode": ([_i], _i),
 }
 for _name, (_args, _res) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -254,6 +255,15 @@ def set_wait_budget_ns(ns: int) -> None:
 
 def set_skip_chunk(chunk: int) -> None:
     _check(_lib.wkv_debug_set_skip_chunk(int(chunk)), "wkv_debug_set_skip_chunk")
+
+
+SCAN_MODES = {"auto": 0, "chunked": 1, "sequential": 2}
+
+
+def set_scan_mode(mode: str) -> None:
+    """Which kernels forward/backward run: "auto" (by shape), "chunked" or
+    "sequential" (process-wide, for tests and measurements)."""
+    _check(_lib.wkv_debug_set_scan_mode(SCAN_MODES[mode]), "wkv_debug_set_scan_mode")
 
 
 # -------------------------------------------------------------- autograd

@@ -19,6 +19,7 @@ constexpr long long kDefaultBudgetNs = 500LL * 1000 * 1000;
 
 std::atomic<long long> g_budget_ns{kDefaultBudgetNs};
 std::atomic<int> g_skip_chunk{-1};
+std::atomic<int> g_scan_mode{WKV_SCAN_AUTO};
 thread_local char g_last_error[256] = "";
 
 void clear_error() { g_last_error[0] = '\0'; }
@@ -93,6 +94,30 @@ BwdLayout bwd_layout(const ScanGeometry& g) {
 
 char* bytes(void* p) { return static_cast<char*>(p); }
 
+// Whether a shape takes the sequential column kernels (wkv_seq.cu): when its
+// columns (batch rows x 32-channel groups) fill every SM at least once, the
+// columns alone keep the GPU busy and a column's chunks need no exchange
+// between CTAs; fewer columns leave SMs idle, and the chunked scans split
+// time across CTAs instead.
+// nseg receives the runs per column of the sequential kernels.
+cudaError_t sequential_mode(const ScanGeometry& g, bool& seq, int& nseg) {
+  static int sms_per_dev[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int sms = (dev >= 0 && dev < 64) ? sms_per_dev[dev] : 0;
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) sms_per_dev[dev] = sms;
+  }
+  const long long cols = (long long)g.B * g.nwg;
+  const int mode = g_scan_mode.load();
+  seq = mode == WKV_SCAN_AUTO ? cols >= sms : mode == WKV_SCAN_SEQUENTIAL;
+  nseg = seq_segments((int)(cols < INT_MAX ? cols : INT_MAX), g.nchunks, sms);
+  return cudaSuccess;
+}
+
 }  // namespace
 
 void set_last_error(const char* msg) {
@@ -129,14 +154,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace
 
-bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int elem_bytes) {
+bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int elem_bytes, int box_c) {
   if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
   if (((size_t)C * elem_bytes) % 16 != 0) return false;
   PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)T, (cuuint64_t)B};
   const cuuint64_t strides[2] = {(cuuint64_t)C * elem_bytes, (cuuint64_t)T * C * elem_bytes};
-  const cuuint32_t box[3] = {(cuuint32_t)kCtaChannels, (cuuint32_t)kChunk, 1u};
+  const cuuint32_t box[3] = {(cuuint32_t)box_c, (cuuint32_t)kChunk, 1u};
   const cuuint32_t estride[3] = {1u, 1u, 1u};
   const CUresult r = fn(map, elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                         const_cast<void*>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -145,6 +170,73 @@ bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int 
   return r == CUDA_SUCCESS;
 }
 
+}  // namespace wkv
+
+namespace wkv {
+namespace {
+
+// The backward pass with the sequential column kernels: the checkpoints
+// (recomputed by a state-only forward walk when the caller has none), the
+// reverse walk writing gk, gv and one gw, gu row per batch row, then the
+// reduction of those B rows.
+wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int nseg, const float* w, const float* u,
+                               const void* k, const void* v, const float* gy, const float* ckpt, float* gw,
+                               float* gu, float* gk, float* gv, WsHeader* hdr, void* workspace, uint64_t budget,
+                               cudaStream_t s) {
+  const int B = g.B, T = g.T, C = g.C;
+  const float* states = ckpt;
+  if (!states) {
+    SeqFwdArgs f;
+    std::memset(&f, 0, sizeof(f));
+    f.w = w;
+    f.u = u;
+    f.k = k;
+    f.v = v;
+    f.y = nullptr;
+    f.ckpt = reinterpret_cast<float*>(bytes(workspace) + l.fwd + fwd_layout(g).ckpt);
+    f.eh = hdr;
+    f.g = g;
+    f.budget_ns = budget;
+    f.nseg = nseg;
+    f.use_tma = make_tile_map(&f.tk, k, B, T, C, 4, kSeqChannels) && make_tile_map(&f.tv, v, B, T, C, 4, kSeqChannels);
+    cudaError_t e = launch_seq_forward(f, WKV_F32, false, s);
+    if (e != cudaSuccess) return cuda_fail(e, "wkv_backward: state pass");
+    states = f.ckpt;
+  }
+  SeqBwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.w = w;
+  a.u = u;
+  a.k = static_cast<const float*>(k);
+  a.v = static_cast<const float*>(v);
+  a.gy = gy;
+  a.ckpt = states;
+  a.gk = gk;
+  a.gv = gv;
+  a.part = reinterpret_cast<float*>(bytes(workspace) + l.part);  // [2][nseg * B][C]
+  a.eh = hdr;
+  a.g = g;
+  a.budget_ns = budget;
+  a.nseg = nseg;
+  a.use_tma = make_tile_map(&a.tk, k, B, T, C, 4, kSeqChannels) && make_tile_map(&a.tv, v, B, T, C, 4, kSeqChannels) &&
+              make_tile_map(&a.tg, gy, B, T, C, 4, kSeqChannels);
+  cudaError_t e = launch_seq_backward(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
+  ReduceArgs r;
+  r.part = a.part;
+  r.slices = reinterpret_cast<float*>(bytes(workspace) + l.slices);
+  r.count = reinterpret_cast<unsigned long long*>(bytes(workspace) + l.count);
+  r.eh = hdr;
+  r.gw = gw;
+  r.gu = gu;
+  r.rows = nseg * B;
+  r.C = C;
+  r.nslice = reduce_slices(nseg * B, C);
+  e = launch_reduce(r, s);
+  return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_backward: reduce");
+}
+
+}  // namespace
 }  // namespace wkv
 
 using namespace wkv;
@@ -218,6 +310,28 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
   const ScanGeometry g = make_geometry(B, T, C);
   const FwdLayout l = fwd_layout(g);
   if (!workspace || workspace_bytes < l.total) return WKV_ERR_WORKSPACE;
+  const int eb = kv_dtype == WKV_F32 ? 4 : 2;
+  bool seq = false;
+  int nseg = 1;
+  cudaError_t e = sequential_mode(g, seq, nseg);
+  if (e != cudaSuccess) return cuda_fail(e, "wkv_forward");
+  if (seq) {
+    SeqFwdArgs q;
+    std::memset(&q, 0, sizeof(q));
+    q.w = w;
+    q.u = u;
+    q.k = k;
+    q.v = v;
+    q.y = y;
+    q.ckpt = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.ckpt);
+    q.eh = static_cast<WsHeader*>(workspace);
+    q.g = g;
+    q.budget_ns = (uint64_t)g_budget_ns.load();
+    q.nseg = nseg;
+    q.use_tma = make_tile_map(&q.tk, k, B, T, C, eb, kSeqChannels) && make_tile_map(&q.tv, v, B, T, C, eb, kSeqChannels);
+    e = launch_seq_forward(q, kv_dtype, true, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
+  }
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
   a.w = w;
@@ -234,9 +348,8 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
   a.g = g;
   a.budget_ns = (uint64_t)g_budget_ns.load();
   a.debug_skip_chunk = g_skip_chunk.load();
-  const int eb = kv_dtype == WKV_F32 ? 4 : 2;
-  a.use_tma = make_tile_map(&a.tk, k, B, T, C, eb) && make_tile_map(&a.tv, v, B, T, C, eb);
-  cudaError_t e = launch_forward(a, kv_dtype, true, static_cast<cudaStream_t>(stream));
+  a.use_tma = make_tile_map(&a.tk, k, B, T, C, eb, kCtaChannels) && make_tile_map(&a.tv, v, B, T, C, eb, kCtaChannels);
+  e = launch_forward(a, kv_dtype, true, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
 }
 
@@ -254,6 +367,11 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
   WsHeader* hdr = static_cast<WsHeader*>(workspace);
   const int skip = g_skip_chunk.load();
   const uint64_t budget = (uint64_t)g_budget_ns.load();
+  bool seq = false;
+  int nseg = 1;
+  cudaError_t e = sequential_mode(g, seq, nseg);
+  if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
+  if (seq) return backward_sequential(g, l, nseg, w, u, k, v, gy, ckpt, gw, gu, gk, gv, hdr, workspace, budget, s);
 
   const float* states = ckpt;
   if (!states) {
@@ -276,8 +394,8 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
     f.g = g;
     f.budget_ns = budget;
     f.debug_skip_chunk = -1;
-    f.use_tma = make_tile_map(&f.tk, k, B, T, C, 4) && make_tile_map(&f.tv, v, B, T, C, 4);
-    cudaError_t e = launch_forward(f, WKV_F32, false, s);
+    f.use_tma = make_tile_map(&f.tk, k, B, T, C, 4, kCtaChannels) && make_tile_map(&f.tv, v, B, T, C, 4, kCtaChannels);
+    e = launch_forward(f, WKV_F32, false, s);
     if (e != cudaSuccess) return cuda_fail(e, "wkv_backward: state pass");
     states = f.ckpt;
   }
@@ -301,9 +419,9 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
   a.g = g;
   a.budget_ns = budget;
   a.debug_skip_chunk = skip;
-  a.use_tma = make_tile_map(&a.tk, k, B, T, C, 4) && make_tile_map(&a.tv, v, B, T, C, 4) &&
-              make_tile_map(&a.tg, gy, B, T, C, 4);
-  cudaError_t e = launch_backward(a, s);
+  a.use_tma = make_tile_map(&a.tk, k, B, T, C, 4, kCtaChannels) && make_tile_map(&a.tv, v, B, T, C, 4, kCtaChannels) &&
+              make_tile_map(&a.tg, gy, B, T, C, 4, kCtaChannels);
+  e = launch_backward(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
 
   ReduceArgs r;
@@ -345,6 +463,12 @@ wkv_status wkv_debug_set_wait_budget_ns(long long ns) {
 
 wkv_status wkv_debug_set_skip_chunk(int chunk) {
   g_skip_chunk.store(chunk < 0 ? -1 : chunk);
+  return WKV_OK;
+}
+
+wkv_status wkv_debug_set_scan_mode(int mode) {
+  if (mode != WKV_SCAN_AUTO && mode != WKV_SCAN_CHUNKED && mode != WKV_SCAN_SEQUENTIAL) return WKV_ERR_INVALID_ARG;
+  g_scan_mode.store(mode);
   return WKV_OK;
 }
 

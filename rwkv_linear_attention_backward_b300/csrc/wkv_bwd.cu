@@ -37,6 +37,7 @@
 // (a e^{-F}).  The bounds that keep it exact in fp32 are those of the forward
 // pass (wkv_fwd.cu); lanes outside them take the per-token running-maximum
 // form, with the adjoints scaled by e^{pp_t} per token.
+#include "wkv_adjoint.cuh"
 #include "wkv_common.cuh"
 #include "wkv_internal.h"
 #include "wkv_pipe.cuh"
@@ -54,111 +55,6 @@ constexpr int kWalkRing = 8;   // records requested together by a walker
 constexpr size_t kWalkSmem = (size_t)kWalkCap * (96 + 32 + 32) * sizeof(float) + (size_t)kWalkRing * 32 * 16;
 static_assert((kWalkCap * (96 + 32 + 32) * sizeof(float)) % 16 == 0, "the record ring must be 16-byte aligned");
 static_assert(2 * 3 * kChunk * kCtaChannels * 4 + kWalkSmem + 1024 <= 114 * 1024, "two backward CTAs per SM");
-
-// Everything the per-token reverse pass needs at one token, from the state
-// before it (running-maximum form).
-struct Local {
-  float gb;  // gy e^{pp-q} / Dhat : scaled gN
-  float gc;  // gy e^{u+k-q} / Dhat : gN e^{u+k}
-  float y;   // wkv_t
-  float vmy; // v_t - wkv_t, formed without subtracting the two
-  Decay t;   // carry factors of the forward step (same as the forward pass)
-};
-
-__device__ __forceinline__ Local local_terms(const State& s, float k, float v, float g, float w, float u) {
-  Local o;
-  const float d1 = s.pp - (u + k);
-  const float e1 = exp_neg_abs(d1);
-  const bool past = d1 >= 0.f;
-  const float cp = past ? 1.f : e1;
-  const float cc = past ? e1 : 1.f;
-  const float inv = rcp(fmaf(cp, s.den, cc));
-  o.y = fmaf(cp, s.num, cc * v) * inv;
-  // v - wkv = cp (den v - num) / Dhat: exact cancellation of the current
-  // token's own share, so no rounding noise when the bonus dominates
-  o.vmy = cp * fmaf(s.den, v, -s.num) * inv;
-  const float gi = g * inv;
-  o.gb = gi * cp;
-  o.gc = gi * cc;
-  o.t = decay_terms(s.pp, k, w);
-  return o;
-}
-
-// An adjoint record: la_true = la e^{-f}, lb_true = lb e^{-f}.
-struct Adj {
-  float la, lb, f;
-};
-
-// The adjoint at the start of a chunk from its own zero-carry record `A` and
-// the adjoint at the start of the next chunk `X`: A + e^{-Lw} X.  The scale
-// of X never exceeds A's decayed by the chunk ((A.f - Lw) - X.f <= 0: the
-// forward states are running maxima), so one exponential of a non-positive
-// number.
-__device__ __forceinline__ Adj fold_adj(const Adj& A, float Lw, const Adj& X) {
-  const float e = exp_nat((A.f - Lw) - X.f);
-  return Adj{fmaf(e, X.la, A.la), fmaf(e, X.lb, A.lb), A.f};
-}
-
-// The per-token (running-maximum) form for lanes outside the fixed scale's
-// bounds.  Rare, so its loops stay rolled with the per-token states (num,
-// den, pp before each token) in local memory, leaving the fast form's
-// registers alone.  The states from P; returns pp after the chunk.
-__device__ __forceinline__ float exact_states(const float* sk, const float* sv, int len, State s, float w,
-                                              float* xa, float* xb, float* xp) {
-  constexpr int S = kCtaChannels;
-#pragma unroll 1
-  for (int i = 0; i < len; ++i) {
-    xa[i] = s.num;
-    xb[i] = s.den;
-    xp[i] = s.pp;
-    step(s, sk[i * S], sv[i * S], w);
-  }
-  return s.pp;
-}
-
-// The zero-carry adjoint at the chunk start, scaled by e^{pp there}.
-__device__ __forceinline__ void exact_zero_adjoint(const float* sk, const float* sv, const float* sg, int len,
-                                                   float w, float u, const float* xa, const float* xb,
-                                                   const float* xp, float& la, float& lb) {
-  constexpr int S = kCtaChannels;
-  la = 0.f;
-  lb = 0.f;
-#pragma unroll 1
-  for (int i = len - 1; i >= 0; --i) {
-    const Local o = local_terms(State{xa[i], xb[i], xp[i]}, sk[i * S], sv[i * S], sg[i * S], w, u);
-    la = carry(o.t, la, o.gb);
-    lb = carry(o.t, lb, -o.gb * o.y);
-  }
-}
-
-// gk, gv with the carry (la, lb, scaled by e^{pp after the chunk});
-// out[0..1] receive the gw, gu partial sums.
-__device__ __forceinline__ void exact_final(const float* sk, const float* sv, const float* sg, int len, float w,
-                                            float u, const float* xa, const float* xb, const float* xp, float la,
-                                            float lb, float* gkp, float* gvp, int64_t C, bool valid, float* out) {
-  constexpr int S = kCtaChannels;
-  float gw_acc = 0.f, gu_acc = 0.f;
-#pragma unroll 1
-  for (int i = len - 1; i >= 0; --i) {
-    const State si{xa[i], xb[i], xp[i]};
-    const float k = sk[i * S], v = sv[i * S];
-    const Local o = local_terms(si, k, v, sg[i * S], w, u);
-    const float cur = o.gc * o.vmy;
-    const float gk = fmaf(o.t.kap, fmaf(la, v, lb), cur);
-    const float gv = fmaf(o.t.kap, la, o.gc);
-    gu_acc += cur;
-    gw_acc = fmaf(-(o.t.dec + o.t.cor), fmaf(la, si.num, lb * si.den), gw_acc);
-    // the adjoint is carried back by the transpose of the forward step
-    la = carry(o.t, la, o.gb);
-    lb = carry(o.t, lb, -o.gb * o.y);
-    if (valid) {
-      __stcs(gkp + (int64_t)i * C, gk);
-      __stcs(gvp + (int64_t)i * C, gv);
-    }
-  }
-  out[0] = gw_acc;
-  out[1] = gu_acc;
-}
 
 // What a consumer lane keeps of a tile between its summary and its finish.
 struct BwdPend {
@@ -219,8 +115,8 @@ __device__ __forceinline__ void bwd_summary(const BwdArgs& a, const Launch& L, f
     la *= p.s0;
     lb *= p.s0;
   } else {
-    exact_states(sk, sv, p.len, p.P, p.w, xa, xb, xp);
-    exact_zero_adjoint(sk, sv, sg, p.len, p.w, p.u, xa, xb, xp, la, lb);
+    exact_states<kCtaChannels>(sk, sv, p.len, p.P, p.w, xa, xb, xp);
+    exact_zero_adjoint<kCtaChannels>(sk, sv, sg, p.len, p.w, p.u, xa, xb, xp, la, lb);
   }
   if (p.j > 0 && p.j != a.debug_skip_chunk && p.c < g.C)  // chunk 0's adjoint is never needed
     rec_store(a.ragg + ((size_t)p.j * g.B + p.b) * g.C + p.c, L.tag, la, lb, p.P.pp);
@@ -283,10 +179,10 @@ __device__ __forceinline__ void bwd_finish(const BwdArgs& a, const float* __rest
     }
     gw_acc *= -p.ew;
   } else {
-    const float pp_end = exact_states(sk, sv, p.len, p.P, p.w, xa, xb, xp);
+    const float pp_end = exact_states<kCtaChannels>(sk, sv, p.len, p.P, p.w, xa, xb, xp);
     const float f = has_succ ? exp_nat(pp_end - X.f) : 0.f;
-    float res[2];
-    exact_final(sk, sv, sg, p.len, p.w, p.u, xa, xb, xp, X.la * f, X.lb * f, gkp, gvp, g.C, valid, res);
+    float res[4];
+    exact_final<kCtaChannels>(sk, sv, sg, p.len, p.w, p.u, xa, xb, xp, X.la * f, X.lb * f, gkp, gvp, g.C, valid, res);
     gw_acc = res[0];
     gu_acc = res[1];
   }

@@ -99,11 +99,56 @@ struct DecodeArgs {
 // Sets the text returned by wkv_last_error_string() on this thread.
 void set_last_error(const char* msg);
 
-// Rank-3 TMA descriptor of a [B, T, C] tensor with a {128, kChunk, 1} box
+// Rank-3 TMA descriptor of a [B, T, C] tensor with a {box_c, kChunk, 1} box
 // (elem_bytes 4 = fp32, 2 = bf16).  False when TMA cannot address it (the
 // base not 16-byte aligned or C * elem_bytes not a multiple of 16) or the
 // driver has no encoder; the kernels then stage tiles with plain loads.
-bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int elem_bytes);
+bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int elem_bytes, int box_c);
+
+// Sequential column kernels (wkv_seq.cu): one warp per column of 32
+// channels of one batch row, walking the time chunks in order; used when
+// there are at least as many columns as SMs (no chunk results cross CTAs).
+constexpr int kSeqChannels = 32;
+constexpr int kSeqMaxWarps = 8;  // runs (warps) per column's CTA
+
+struct SeqFwdArgs {
+  CUtensorMap tk, tv;  // box {32, kChunk, 1} (when use_tma)
+  const float* w;
+  const float* u;
+  const void* k;
+  const void* v;
+  float* y;     // may be null (state-only pass)
+  float* ckpt;  // [3][nchunks][B][C] state after each chunk
+  WsHeader* eh;
+  ScanGeometry g;
+  uint64_t budget_ns;
+  int nseg;  // warps per column, each walking one run of its chunks (seq_segments)
+  int use_tma;
+};
+
+struct SeqBwdArgs {
+  CUtensorMap tk, tv, tg;
+  const float* w;
+  const float* u;
+  const float* k;
+  const float* v;
+  const float* gy;
+  const float* ckpt;
+  float* gk;
+  float* gv;
+  float* part;  // [2][nseg * B][C] gw, gu sums per (run, batch row)
+  WsHeader* eh;
+  ScanGeometry g;
+  uint64_t budget_ns;
+  int nseg;
+  int use_tma;
+};
+
+cudaError_t launch_seq_forward(const SeqFwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
+// Runs per column (warps per CTA) of the sequential kernels: enough for about
+// four warps per SM, at most kSeqMaxWarps and at most one per chunk.
+int seq_segments(int cols, int nchunks, int sms);
+cudaError_t launch_seq_backward(const SeqBwdArgs& a, cudaStream_t s);
 
 // Grid of a persistent scan kernel: resident CTAs per SM x SMs, at most ntiles.
 cudaError_t launch_forward(FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);

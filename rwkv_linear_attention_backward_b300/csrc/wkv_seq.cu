@@ -1,0 +1,890 @@
+// wkv_seq.cu -- WKV forward and backward as one sequential walk over time
+// per column, for shapes with enough independent columns to fill the GPU.
+//
+// Channels and batch rows are independent (the recurrence of
+// "RWKV解读：在Transformer的时代的新RNN", section "3、RWKV的网络架构",
+// eq. (8), runs per channel), so a column -- one batch row and 32
+// consecutive channels, one channel per lane -- needs nothing from any other
+// column.  One warp (one CTA) walks a column's time chunks in order (the
+// forward pass) or in reverse order (the backward pass) and carries the
+// state, or the adjoint, from chunk to chunk in registers: there is no chunk
+// summary to publish and no wait on another CTA.  The warp stages its own
+// chunks, k and v (and gy) as [kChunk tokens x 32 channels] boxes, into a
+// ring of shared-memory stages by TMA, several chunks ahead, so each column
+// keeps its next loads in flight while it computes.
+//
+// The per-chunk arithmetic is that of the chunked scans (wkv_fwd.cu,
+// wkv_bwd.cu): the fixed scale e^{F}, F = the chunk's largest k, under the
+// same bounds, and the per-token running-maximum form for lanes outside
+// them.  The carried state crosses a chunk boundary the way the chunked
+// scan's walkers carry it -- the chunk's own summary combined with the
+// state before it decayed by e^{-n w} in one exponential -- not through n
+// products of the rounded e^{-w}, whose rounding error would otherwise grow
+// with T.  The adjoint crosses chunk boundaries the same way.  Outputs and
+// checkpoints of fixed-scale lanes therefore match the chunked forward
+// pass's bit for bit.
+#include <cuda_bf16.h>
+
+#include <type_traits>
+
+#include "wkv_adjoint.cuh"
+#include "wkv_common.cuh"
+#include "wkv_internal.h"
+#include "wkv_pipe.cuh"
+
+namespace wkv {
+
+namespace {
+
+constexpr int kSeqTile = kChunk * kSeqChannels;  // elements of one array in one stage
+constexpr float kFastRange = 69.f;  // smallest bonus weight of the fixed scale: e^{-69}
+constexpr float kFastCeil = 60.f;   // largest scale-up of the fixed scale: e^{60}
+
+template <typename KV>
+__device__ __forceinline__ float to_f32(KV x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+// Records an expired wait: the code only (these kernels have no launch epoch
+// and other launches' waits must not stop on their account).
+__device__ __forceinline__ void seq_record_timeout(WsHeader* h) { atomicCAS(&h->error, 0u, kDevErrTimeout); }
+
+// Bytes of the stage ring's control block (one mbarrier per stage), a
+// multiple of 128.
+template <int NS>
+__host__ __device__ constexpr size_t seq_ctl_bytes() {
+  return ((size_t)NS * 8 + 127) / 128 * 128;
+}
+
+// The column of this CTA: batch row, first channel, this lane's channel
+// (every warp of the CTA covers the same 32 channels).
+struct Column {
+  int b, c0, c;
+  bool valid;  // c < C
+  int cc;      // c clamped into [0, C)
+};
+
+__device__ __forceinline__ Column column_of(const ScanGeometry& g) {
+  Column o;
+  const int q = blockIdx.x;
+  o.b = q / g.nwg;
+  o.c0 = (q - o.b * g.nwg) * kSeqChannels;
+  o.c = o.c0 + (int)(threadIdx.x & 31);
+  o.valid = o.c < g.C;
+  o.cc = o.valid ? o.c : g.C - 1;
+  return o;
+}
+
+// Plain-load copy of one [kChunk x 32] box of a [B, T, C] tensor, zero
+// outside the tensor (TMA's fill value); the whole warp takes part, lane l
+// writing column l of the box.
+template <typename E>
+__device__ __forceinline__ void copy_box_plain(E* dst, const E* src, const ScanGeometry& g, const Column& col,
+                                               int t0) {
+#pragma unroll 4
+  for (int i = 0; i < kChunk; ++i) {
+    const int t = t0 + i;
+    E val = E(0.f);
+    if (t < g.T && col.valid) val = src[((int64_t)col.b * g.T + t) * g.C + col.c];
+    dst[i * kSeqChannels + (threadIdx.x & 31)] = val;
+  }
+}
+
+// Waits (bounded) for stage s's TMA bytes of phase `parity`; every lane
+// waits, so every lane's later reads see the copied bytes.
+__device__ __forceinline__ bool stage_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+  const bool ok = mbar_wait(bar, parity, budget_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// After an expired wait: give the copies still in flight into this CTA's
+// shared memory (stages of chunks issued after the one that expired) one
+// more shared, bounded chance to land before the CTA exits.  The limit is
+// fixed (not the adjustable wait budget), long against any copy.
+constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
+
+template <int NS>
+__device__ __forceinline__ void drain_stages(uint64_t* full, int first, int issued) {
+  const uint64_t t0 = globaltimer();
+  for (int it = first + 1; it < issued; ++it) {
+    const int s = it % NS;
+    const uint32_t parity = (uint32_t)((it / NS) & 1);
+    while (!mbar_try_wait(&full[s], parity)) {
+      if (globaltimer() - t0 > kDrainNs) return;
+    }
+  }
+}
+
+// Largest / smallest of x[0..N): a balanced tree (max and min are exact, so
+// the result is that of any order), with N/2 independent operations per
+// level instead of a chain of N.
+template <int N>
+__device__ __forceinline__ float tree_max(const float* x) {
+  if constexpr (N == 1) {
+    return x[0];
+  } else {
+    return fmaxf(tree_max<N / 2>(x), tree_max<N - N / 2>(x + N / 2));
+  }
+}
+
+template <int N>
+__device__ __forceinline__ float tree_min(const float* x) {
+  if constexpr (N == 1) {
+    return x[0];
+  } else {
+    return fminf(tree_min<N / 2>(x), tree_min<N - N / 2>(x + N / 2));
+  }
+}
+
+// ------------------------------------------------------------------ forward
+// A whole chunk of the forward pass for this lane, with every loop fully
+// unrolled and no per-token branch: the one warp of a column has no other
+// warp to hide latencies behind, so each phase is written as independent
+// work per token (the k values and then ek in registers; the statistics by
+// trees) and only the carried sums form chains.  Same arithmetic, in the
+// same order per value, as the generic form below.
+template <typename KV, bool WRITE_Y>
+__device__ __forceinline__ void seq_fwd_full(const KV* __restrict__ sk, const KV* __restrict__ sv, float w, float u,
+                                             float ew, float eu, State& P, float* __restrict__ yp, int64_t ystride,
+                                             bool valid) {
+  constexpr int L = kChunk;
+  constexpr int S = kSeqChannels;
+  float kr[L], rr[L];
+#pragma unroll
+  for (int i = 0; i < L; ++i) {
+    kr[i] = to_f32<KV>(sk[i * S]);
+    rr[i] = fmaf(-(float)(L - 1 - i), w, kr[i]);
+  }
+  const float F = tree_max<L>(kr);
+  const float kmin = tree_min<L>(kr);
+  const float r = tree_max<L>(rr);
+  const bool fast = (kmin + fminf(u, 0.f) >= F - kFastRange) && (u <= kFastCeil) && (P.pp - F <= kFastCeil);
+  if (fast) {
+    const float F2 = F * kLog2e;
+    const float s0 = exp_nat(P.pp - F);
+    float na = P.num * s0, nb = P.den * s0;
+    float on = 0.f, od = 0.f;
+#pragma unroll
+    for (int i = 0; i < L; ++i) kr[i] = ex2(fmaf(kr[i], kLog2e, -F2));  // ek
+#pragma unroll
+    for (int i = 0; i < L; ++i) {
+      const float ek = kr[i];
+      const float vv = to_f32<KV>(sv[i * S]);
+      const float ekv = ek * vv;
+      if constexpr (WRITE_Y) {
+        const float ec = ek * eu;
+        const float yv = fmaf(ec, vv, na) * rcp(nb + ec);
+        if (valid) __stcs(yp + (int64_t)i * ystride, yv);
+        na = fmaf(na, ew, ekv);
+        nb = fmaf(nb, ew, ek);
+      }
+      on = fmaf(on, ew, ekv);
+      od = fmaf(od, ew, ek);
+    }
+    const float sc = exp_nat(F - r);
+    P = combine(P, (float)L * w, State{on * sc, od * sc, r});
+  } else {
+#pragma unroll 1
+    for (int i = 0; i < L; ++i) {
+      const float kk = to_f32<KV>(sk[i * S]);
+      const float vv = to_f32<KV>(sv[i * S]);
+      if constexpr (WRITE_Y) {
+        const float yv = output(P, kk, vv, u);
+        if (valid) __stcs(yp + (int64_t)i * ystride, yv);
+      }
+      step(P, kk, vv, w);
+    }
+  }
+}
+
+// One chunk of n <= kChunk tokens (the generic form, for the partial last
+// chunk): outputs from the carried state P (when WRITE_Y), then P advanced
+// past the chunk.
+template <typename KV, bool WRITE_Y>
+__device__ __forceinline__ void seq_fwd_chunk(const KV* __restrict__ sk, const KV* __restrict__ sv, int n, float w,
+                                              float u, float ew, float eu, State& P, float* __restrict__ yp,
+                                              int64_t ystride, bool valid) {
+  constexpr int S = kSeqChannels;
+  float F = -3.0e38f, kmin = 3.0e38f, r = -3.0e38f;
+#pragma unroll 8
+  for (int i = 0; i < n; ++i) {
+    const float k = to_f32<KV>(sk[i * S]);
+    F = fmaxf(F, k);
+    kmin = fminf(kmin, k);
+    r = fmaxf(r, fmaf(-(float)(n - 1 - i), w, k));
+  }
+  const bool fast = (kmin + fminf(u, 0.f) >= F - kFastRange) && (u <= kFastCeil) && (P.pp - F <= kFastCeil);
+  if (fast) {
+    const float F2 = F * kLog2e;
+    const float s0 = exp_nat(P.pp - F);  // P at scale e^{F}; 0 for the empty state
+    float na = P.num * s0, nb = P.den * s0;  // sums before each token, with P (for the outputs)
+    float on = 0.f, od = 0.f;                // the chunk's own sums (for the carried state)
+#pragma unroll 8
+    for (int i = 0; i < n; ++i) {
+      const float ek = ex2(fmaf(to_f32<KV>(sk[i * S]), kLog2e, -F2));
+      const float vv = to_f32<KV>(sv[i * S]);
+      const float ekv = ek * vv;
+      if constexpr (WRITE_Y) {
+        const float ec = ek * eu;
+        const float yv = fmaf(ec, vv, na) * rcp(nb + ec);
+        if (valid) __stcs(yp + (int64_t)i * ystride, yv);
+        na = fmaf(na, ew, ekv);
+        nb = fmaf(nb, ew, ek);
+      }
+      on = fmaf(on, ew, ekv);
+      od = fmaf(od, ew, ek);
+    }
+    // the chunk's own summary at its running-maximum scale e^{r}, then
+    // P decayed by the chunk's length combined with it
+    const float sc = exp_nat(F - r);
+    P = combine(P, (float)n * w, State{on * sc, od * sc, r});
+  } else {
+#pragma unroll 1
+    for (int i = 0; i < n; ++i) {
+      const float kk = to_f32<KV>(sk[i * S]);
+      const float vv = to_f32<KV>(sv[i * S]);
+      if constexpr (WRITE_Y) {
+        const float yv = output(P, kk, vv, u);
+        if (valid) __stcs(yp + (int64_t)i * ystride, yv);
+      }
+      step(P, kk, vv, w);
+    }
+  }
+}
+
+// Segments of a column's walk, one per warp of the CTA: the chunks in walk
+// order (time order for the forward pass, reverse time order for the
+// backward pass) cut into nseg contiguous runs.  Every warp but the last
+// first summarises its run (phase 1: the state, or the adjoint, it carries
+// from the empty one); after one CTA barrier each warp folds the summaries
+// of the runs before its own into its carry and walks its run again with it
+// (phase 2, reading the run a second time, from L2).  The last warp has no
+// phase 1, so it takes about 1.5 times the chunks of the others (a summary
+// costs about half a full walk).  With nseg == 1 this is the plain
+// sequential walk.
+__device__ __forceinline__ void segment_of(int nchunks, int nseg, int s, int& first, int& count) {
+  const int c = nseg > 1 ? (2 * nchunks) / (2 * nseg + 1) : 0;
+  first = s * c;
+  count = s < nseg - 1 ? c : nchunks - first;  // >= 1 for the last warp
+}
+
+// Shared memory of a CTA of nseg warps: each warp's ring of NS stages of
+// `arrays` [kChunk x 32] boxes of E, the warps' stage mbarriers [nseg][NS],
+// then the run summaries [nseg][3][32] f32.
+template <typename E, int NS>
+__host__ __device__ constexpr size_t seq_ring_elems(int arrays) {
+  return (size_t)NS * arrays * kSeqTile;
+}
+
+template <typename E, int NS>
+__host__ __device__ constexpr size_t seq_smem_bytes(int nseg, int arrays) {
+  return (size_t)nseg * seq_ring_elems<E, NS>(arrays) * sizeof(E) + ((size_t)nseg * NS * 8 + 127) / 128 * 128 +
+         (size_t)nseg * 3 * 32 * sizeof(float);
+}
+
+template <typename KV, int NS, bool WRITE_Y>
+__global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_fwd_kernel(const __grid_constant__ SeqFwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int nseg = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr size_t kRing = seq_ring_elems<KV, NS>(2);  // stage s: k at 2s*kSeqTile, v at (2s+1)*kSeqTile
+  KV* ring = reinterpret_cast<KV*>(smem) + (size_t)warp * kRing;
+  unsigned char* ctl = smem + (size_t)nseg * kRing * sizeof(KV);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctl) + warp * NS;
+  float* summ = reinterpret_cast<float*>(ctl + ((size_t)nseg * NS * 8 + 127) / 128 * 128);  // [nseg][3][32]
+  const ScanGeometry& g = a.g;
+  const Column col = column_of(g);
+  const float w = __ldg(a.w + col.cc), u = __ldg(a.u + col.cc);
+  const float ew = expf(-w), eu = expf(u);
+  const bool tma = a.use_tma != 0;
+  constexpr uint32_t kStageBytes = 2 * kSeqTile * sizeof(KV);
+
+  int first, count;
+  segment_of(g.nchunks, nseg, warp, first, count);
+  const int n1 = warp < nseg - 1 ? count : 0;  // phase-1 items, then the same chunks again
+  const int nitems = n1 + count;
+  auto chunk_of = [&](int it) { return first + (it < n1 ? it : it - n1); };
+  auto issue = [&](int it) {  // lane 0: item it into its stage
+    const int s = it % NS;
+    const int j = chunk_of(it);
+    KV* dk = ring + (size_t)(2 * s) * kSeqTile;
+    mbar_arrive_expect_tx(&full[s], kStageBytes);
+    tma_load_3d(dk, &a.tk, &full[s], col.c0, j * kChunk, col.b);
+    tma_load_3d(dk + kSeqTile, &a.tv, &full[s], col.c0, j * kChunk, col.b);
+  };
+  int issued = 0;
+  if (tma) {
+    if (lane == 0) {
+      for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+      mbar_init_fence();
+      tma_prefetch_desc(&a.tk);
+      tma_prefetch_desc(&a.tv);
+      for (int it = 0; it < NS && it < nitems; ++it) issue(it);
+    }
+    issued = min(NS, nitems);
+    __syncwarp();
+  }
+  // Takes item it's stage (false: the wait expired); `release` after use.
+  auto acquire = [&](int it, KV*& dk) {
+    const int s = it % NS;
+    dk = ring + (size_t)(2 * s) * kSeqTile;
+    if (tma) return stage_wait(&full[s], (uint32_t)((it / NS) & 1), a.budget_ns);
+    const int j = chunk_of(it);
+    copy_box_plain(dk, static_cast<const KV*>(a.k), g, col, j * kChunk);
+    copy_box_plain(dk + kSeqTile, static_cast<const KV*>(a.v), g, col, j * kChunk);
+    __syncwarp();
+    return true;
+  };
+  auto release = [&](int it) {
+    // every lane's reads of the stage come before the copy that refills it
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (tma && it + NS < nitems) {
+      if (lane == 0) issue(it + NS);
+      ++issued;
+    }
+  };
+
+  // phase 1: this run's own summary (the state it carries from the empty one)
+  int failed = -1;
+  State P = empty_state();
+  int it = 0;
+  for (; it < n1; ++it) {
+    KV* dk;
+    if (!acquire(it, dk)) {
+      failed = it;
+      break;
+    }
+    const int j = chunk_of(it);
+    const int n = min(kChunk, g.T - j * kChunk);
+    if (n == kChunk)
+      seq_fwd_full<KV, false>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, P, nullptr, 0, false);
+    else
+      seq_fwd_chunk<KV, false>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, nullptr, 0, false);
+    release(it);
+  }
+  if (n1 > 0) {
+    summ[(warp * 3 + 0) * 32 + lane] = P.num;
+    summ[(warp * 3 + 1) * 32 + lane] = P.den;
+    summ[(warp * 3 + 2) * 32 + lane] = P.pp;
+  }
+  __syncthreads();
+  if (failed >= 0) {
+    if (lane == 0) seq_record_timeout(a.eh);
+    drain_stages<NS>(full, failed, issued);
+    return;
+  }
+  // the carry into this run: the runs before it, in order
+  P = empty_state();
+  for (int q = 0; q < warp; ++q) {
+    int fq, cq;
+    segment_of(g.nchunks, nseg, q, fq, cq);
+    if (cq == 0) continue;
+    const State Sq{summ[(q * 3 + 0) * 32 + lane], summ[(q * 3 + 1) * 32 + lane], summ[(q * 3 + 2) * 32 + lane]};
+    P = combine(P, (float)(cq * kChunk) * w, Sq);
+  }
+
+  // phase 2: outputs and checkpoints
+  const size_t o0 = (size_t)col.b * g.C + col.cc;
+  const size_t jstride = (size_t)g.B * g.C;
+  for (; it < nitems; ++it) {
+    KV* dk;
+    if (!acquire(it, dk)) {
+      if (lane == 0) seq_record_timeout(a.eh);
+      drain_stages<NS>(full, it, issued);
+      return;
+    }
+    const int j = chunk_of(it);
+    const int n = min(kChunk, g.T - j * kChunk);
+    float* yp = WRITE_Y ? a.y + ((int64_t)col.b * g.T + (int64_t)j * kChunk) * g.C + col.c : nullptr;
+    if (n == kChunk)
+      seq_fwd_full<KV, WRITE_Y>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, P, yp, g.C, col.valid);
+    else
+      seq_fwd_chunk<KV, WRITE_Y>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, yp, g.C, col.valid);
+    if (col.valid) {
+      const size_t o = (size_t)j * jstride + o0;
+      a.ckpt[o] = P.num;
+      a.ckpt[o + g.plane] = P.den;
+      a.ckpt[o + 2 * g.plane] = P.pp;
+    }
+    release(it);
+  }
+}
+
+// ----------------------------------------------------------------- backward
+// The adjoint recurrence and the gradients are those of the chunked
+// backward pass (wkv_bwd.cu).  Per chunk, last chunk first: the forward
+// sums before each token from the checkpoint before the chunk (the sums in
+// registers, ek written over k in the stage), then the reverse sweep with
+// the adjoint X carried in from the next chunk.  The sweep keeps the
+// chunk's zero-carry adjoint (la0, lb0) apart from X's decayed share, so X
+// crosses the chunk in one exponential (fold_adj) rather than n products of
+// the rounded e^{-w}.
+struct BwdColumn {
+  float w, u, ew, eu;
+  float gw_s, gw_k, gu_s, gu_k;  // compensated sums over the chunks
+};
+
+__device__ __forceinline__ void kahan_add(float& s, float& k, float x) {
+  const float y = x - k;
+  const float t = s + y;
+  k = (t - s) - y;
+  s = t;
+}
+
+// FULL: a whole chunk (n == kChunk), every loop fully unrolled with no
+// per-token branch and ek kept in registers (see seq_fwd_full); otherwise
+// the first n tokens, each token under its own predicate, ek stored over k
+// in the stage.
+template <bool FULL>
+__device__ __forceinline__ void seq_bwd_chunk(float* __restrict__ sk, const float* __restrict__ sv,
+                                              const float* __restrict__ sg, int n, const BwdColumn& cw,
+                                              const State& P, bool has_succ, Adj& X, float* __restrict__ gkp,
+                                              float* __restrict__ gvp, int64_t stride, bool valid, float& gw_acc,
+                                              float& gu_acc, float* xa, float* xb, float* xp) {
+  constexpr int L = kChunk;
+  constexpr int S = kSeqChannels;
+  if constexpr (FULL) n = L;
+  float kr[L];
+  float F, kmin;
+  if constexpr (FULL) {
+#pragma unroll
+    for (int i = 0; i < L; ++i) kr[i] = sk[i * S];
+    F = tree_max<L>(kr);
+    kmin = tree_min<L>(kr);
+  } else {
+    F = -3.0e38f;
+    kmin = 3.0e38f;
+#pragma unroll 8
+    for (int i = 0; i < n; ++i) {
+      const float k = sk[i * S];
+      F = fmaxf(F, k);
+      kmin = fminf(kmin, k);
+    }
+  }
+  const bool fast =
+      (kmin + fminf(cw.u, 0.f) >= F - kFastRange) && (cw.u <= kFastCeil) && (P.pp - F <= kFastCeil);
+  gw_acc = 0.f;
+  gu_acc = 0.f;
+  if (fast) {
+    const float F2 = F * kLog2e;
+    const float s0 = exp_nat(P.pp - F);
+    float A[L], Bd[L];
+    float na = P.num * s0, nb = P.den * s0;
+    if constexpr (FULL) {
+#pragma unroll
+      for (int i = 0; i < L; ++i) kr[i] = ex2(fmaf(kr[i], kLog2e, -F2));  // ek
+    }
+#pragma unroll
+    for (int i = 0; i < L; ++i) {
+      if (FULL || i < n) {
+        float ek;
+        if constexpr (FULL) {
+          ek = kr[i];
+        } else {
+          ek = ex2(fmaf(sk[i * S], kLog2e, -F2));
+          sk[i * S] = ek;
+        }
+        const float vv = sv[i * S];
+        A[i] = na;
+        Bd[i] = nb;
+        na = fmaf(na, cw.ew, ek * vv);
+        nb = fmaf(nb, cw.ew, ek);
+      }
+    }
+    // X at scale e^{F}; its share of the adjoint after token i is
+    // X e^{-(n-1-i) w} (pw)
+    const float f = has_succ ? exp_nat(F - X.f) : 0.f;
+    const float xla = X.la * f, xlb = X.lb * f;
+    float la0 = 0.f, lb0 = 0.f, pw = 1.f;
+    float gwb = 0.f;  // gw's lb share: a second chain beside gw_acc's la share
+#pragma unroll
+    for (int i = L - 1; i >= 0; --i) {
+      if (FULL || i < n) {
+        const float la = fmaf(xla, pw, la0);  // adjoints after token i, at scale e^{F}
+        const float lb = fmaf(xlb, pw, lb0);
+        const float ek = FULL ? kr[i] : sk[i * S];
+        const float vv = sv[i * S];
+        const float ec = ek * cw.eu;
+        const float rr = rcp(Bd[i] + ec);
+        const float gi = sg[i * S] * rr;
+        const float vmy = fmaf(vv, Bd[i], -A[i]) * rr;  // v - wkv
+        const float cur = gi * vmy * ec;                // (gN v + gD) e^{u+k}
+        const float gk = fmaf(fmaf(la, vv, lb), ek, cur);
+        const float gv = fmaf(gi, ec, la * ek);
+        gu_acc += cur;
+        gw_acc = fmaf(la, A[i], gw_acc);
+        gwb = fmaf(lb, Bd[i], gwb);
+        la0 = fmaf(la0, cw.ew, gi);
+        lb0 = fmaf(lb0, cw.ew, -gi * (vv - vmy));
+        pw *= cw.ew;
+        if (valid) {
+          __stcs(gkp + (int64_t)i * stride, gk);
+          __stcs(gvp + (int64_t)i * stride, gv);
+        }
+      }
+    }
+    gw_acc = -cw.ew * (gw_acc + gwb);
+    // the adjoint at the chunk start, at the scale of P (the record form)
+    const Adj A0{la0 * s0, lb0 * s0, P.pp};
+    X = has_succ ? fold_adj(A0, (float)n * cw.w, X) : A0;
+  } else {
+    const float pp_end = exact_states<kSeqChannels>(sk, sv, n, P, cw.w, xa, xb, xp);
+    const float f = has_succ ? exp_nat(pp_end - X.f) : 0.f;
+    float res[4];
+    exact_final<kSeqChannels>(sk, sv, sg, n, cw.w, cw.u, xa, xb, xp, X.la * f, X.lb * f, gkp, gvp, stride, valid,
+                              res);
+    gw_acc = res[0];
+    gu_acc = res[1];
+    X = Adj{res[2], res[3], P.pp};
+  }
+}
+
+// Phase 1 of the backward walk for one chunk: the chunk's zero-carry
+// adjoint at its first token (its own gy only), in the record form: scaled
+// by e^{P.pp}, P the state before the chunk.  The forward sums and the
+// adjoint accumulate in one forward sweep, each token's gN, gD weighted by
+// e^{-(t - t0) w} (pw), as in the chunked backward pass's summary.
+template <bool FULL>
+__device__ __forceinline__ Adj seq_bwd_summary(const float* __restrict__ sk, const float* __restrict__ sv,
+                                               const float* __restrict__ sg, int n, const BwdColumn& cw,
+                                               const State& P, float* xa, float* xb, float* xp) {
+  constexpr int L = kChunk;
+  constexpr int S = kSeqChannels;
+  if constexpr (FULL) n = L;
+  float kr[L];
+  float F, kmin;
+  if constexpr (FULL) {
+#pragma unroll
+    for (int i = 0; i < L; ++i) kr[i] = sk[i * S];
+    F = tree_max<L>(kr);
+    kmin = tree_min<L>(kr);
+  } else {
+    F = -3.0e38f;
+    kmin = 3.0e38f;
+#pragma unroll 8
+    for (int i = 0; i < n; ++i) {
+      const float k = sk[i * S];
+      F = fmaxf(F, k);
+      kmin = fminf(kmin, k);
+    }
+  }
+  const bool fast =
+      (kmin + fminf(cw.u, 0.f) >= F - kFastRange) && (cw.u <= kFastCeil) && (P.pp - F <= kFastCeil);
+  float la = 0.f, lb = 0.f;
+  if (fast) {
+    const float F2 = F * kLog2e;
+    const float s0 = exp_nat(P.pp - F);
+    float na = P.num * s0, nb = P.den * s0, pw = 1.f;
+    if constexpr (FULL) {
+#pragma unroll
+      for (int i = 0; i < L; ++i) kr[i] = ex2(fmaf(kr[i], kLog2e, -F2));  // ek
+#pragma unroll
+      for (int i = 0; i < L; ++i) {
+        const float ek = kr[i];
+        const float vv = sv[i * S];
+        const float ec = ek * cw.eu;
+        const float rr = rcp(nb + ec);
+        const float gi = sg[i * S] * rr;        // gN at scale e^{F}
+        const float y = fmaf(ec, vv, na) * rr;  // wkv_t
+        la = fmaf(pw, gi, la);
+        lb = fmaf(-pw, gi * y, lb);
+        pw *= cw.ew;
+        na = fmaf(na, cw.ew, ek * vv);
+        nb = fmaf(nb, cw.ew, ek);
+      }
+    } else {
+#pragma unroll 8
+      for (int i = 0; i < n; ++i) {
+        const float ek = ex2(fmaf(sk[i * S], kLog2e, -F2));
+        const float vv = sv[i * S];
+        const float ec = ek * cw.eu;
+        const float rr = rcp(nb + ec);
+        const float gi = sg[i * S] * rr;
+        const float y = fmaf(ec, vv, na) * rr;
+        la = fmaf(pw, gi, la);
+        lb = fmaf(-pw, gi * y, lb);
+        pw *= cw.ew;
+        na = fmaf(na, cw.ew, ek * vv);
+        nb = fmaf(nb, cw.ew, ek);
+      }
+    }
+    la *= s0;  // from scale e^{F} to the record's e^{P.pp}
+    lb *= s0;
+  } else {
+    exact_states<kSeqChannels>(sk, sv, n, P, cw.w, xa, xb, xp);
+    exact_zero_adjoint<kSeqChannels>(sk, sv, sg, n, cw.w, cw.u, xa, xb, xp, la, lb);
+  }
+  return Adj{la, lb, P.pp};
+}
+
+template <int NS>
+__global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_bwd_kernel(const __grid_constant__ SeqBwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int nseg = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr size_t kRing = seq_ring_elems<float, NS>(3);  // stage s: k, v, gy at (3s + 0..2) * kSeqTile
+  float* ring = reinterpret_cast<float*>(smem) + (size_t)warp * kRing;
+  unsigned char* ctl = smem + (size_t)nseg * kRing * sizeof(float);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctl) + warp * NS;
+  float* summ = reinterpret_cast<float*>(ctl + ((size_t)nseg * NS * 8 + 127) / 128 * 128);  // [nseg][3][32]
+  const ScanGeometry& g = a.g;
+  const Column col = column_of(g);
+  BwdColumn cw;
+  cw.w = __ldg(a.w + col.cc);
+  cw.u = __ldg(a.u + col.cc);
+  cw.ew = expf(-cw.w);
+  cw.eu = expf(cw.u);
+  cw.gw_s = cw.gw_k = cw.gu_s = cw.gu_k = 0.f;
+  const bool tma = a.use_tma != 0;
+  constexpr uint32_t kStageBytes = 3 * kSeqTile * sizeof(float);
+  const int last = g.nchunks - 1;
+
+  // The reduction of the gw, gu rows that follows this kernel tags its
+  // counters with the workspace's sequence number: advance it once per call.
+  if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(&a.eh->seq, 1ull);
+
+  int first, count;  // in walk order: position p is chunk last - p
+  segment_of(g.nchunks, nseg, warp, first, count);
+  const int n1 = warp < nseg - 1 ? count : 0;
+  const int nitems = n1 + count;
+  auto chunk_of = [&](int it) { return last - (first + (it < n1 ? it : it - n1)); };
+  auto issue = [&](int it) {  // lane 0: item it into its stage
+    const int s = it % NS;
+    const int j = chunk_of(it);
+    float* dk = ring + (size_t)(3 * s) * kSeqTile;
+    mbar_arrive_expect_tx(&full[s], kStageBytes);
+    tma_load_3d(dk, &a.tk, &full[s], col.c0, j * kChunk, col.b);
+    tma_load_3d(dk + kSeqTile, &a.tv, &full[s], col.c0, j * kChunk, col.b);
+    tma_load_3d(dk + 2 * kSeqTile, &a.tg, &full[s], col.c0, j * kChunk, col.b);
+  };
+  int issued = 0;
+  if (tma) {
+    if (lane == 0) {
+      for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+      mbar_init_fence();
+      tma_prefetch_desc(&a.tk);
+      tma_prefetch_desc(&a.tv);
+      tma_prefetch_desc(&a.tg);
+      for (int it = 0; it < NS && it < nitems; ++it) issue(it);
+    }
+    issued = min(NS, nitems);
+    __syncwarp();
+  }
+  auto acquire = [&](int it, float*& dk) {
+    const int s = it % NS;
+    dk = ring + (size_t)(3 * s) * kSeqTile;
+    if (tma) return stage_wait(&full[s], (uint32_t)((it / NS) & 1), a.budget_ns);
+    const int j = chunk_of(it);
+    copy_box_plain(dk, a.k, g, col, j * kChunk);
+    copy_box_plain(dk + kSeqTile, a.v, g, col, j * kChunk);
+    copy_box_plain(dk + 2 * kSeqTile, a.gy, g, col, j * kChunk);
+    __syncwarp();
+    return true;
+  };
+  auto release = [&](int it) {
+    // this warp may have written into the stage: order its accesses before
+    // the async-proxy copy that refills it
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (tma && it + NS < nitems) {
+      if (lane == 0) issue(it + NS);
+      ++issued;
+    }
+  };
+
+  float xa[kChunk], xb[kChunk], xp[kChunk];  // per-token form's states (local memory)
+  const size_t o0 = (size_t)col.b * g.C + col.cc;
+  const size_t jstride = (size_t)g.B * g.C;
+  auto load_state = [&](int j) {  // the checkpoint before chunk j
+    if (j <= 0) return empty_state();
+    const size_t o = (size_t)(j - 1) * jstride + o0;
+    return State{__ldg(a.ckpt + o), __ldg(a.ckpt + o + g.plane), __ldg(a.ckpt + o + 2 * g.plane)};
+  };
+
+  // phase 1: this run's zero-carry adjoint at its first token
+  int failed = -1;
+  State Pn = nitems > 0 ? load_state(chunk_of(0)) : empty_state();
+  Adj X{0.f, 0.f, 0.f};
+  int it = 0;
+  for (; it < n1; ++it) {
+    const State P = Pn;
+    if (it + 1 < nitems) Pn = load_state(chunk_of(it + 1));  // one chunk ahead
+    float* dk;
+    if (!acquire(it, dk)) {
+      failed = it;
+      break;
+    }
+    const int j = chunk_of(it);
+    const int n = min(kChunk, g.T - j * kChunk);
+    const Adj A = n == kChunk
+                      ? seq_bwd_summary<true>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P,
+                                              xa, xb, xp)
+                      : seq_bwd_summary<false>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P,
+                                               xa, xb, xp);
+    X = it == 0 ? A : fold_adj(A, (float)n * cw.w, X);
+    release(it);
+  }
+  if (n1 > 0) {
+    summ[(warp * 3 + 0) * 32 + lane] = X.la;
+    summ[(warp * 3 + 1) * 32 + lane] = X.lb;
+    summ[(warp * 3 + 2) * 32 + lane] = X.f;
+  }
+  __syncthreads();
+  if (failed >= 0) {
+    if (lane == 0) seq_record_timeout(a.eh);
+    drain_stages<NS>(full, failed, issued);
+    return;
+  }
+  // the carry into this run's end: the runs after it in time, nearest last
+  // (none for the run holding the last chunk)
+  bool has_x = false;
+  X = Adj{0.f, 0.f, 0.f};
+  for (int q = 0; q < warp; ++q) {
+    int fq, cq;
+    segment_of(g.nchunks, nseg, q, fq, cq);
+    if (cq == 0) continue;
+    const Adj Aq{summ[(q * 3 + 0) * 32 + lane], summ[(q * 3 + 1) * 32 + lane], summ[(q * 3 + 2) * 32 + lane]};
+    X = has_x ? fold_adj(Aq, (float)(cq * kChunk) * cw.w, X) : Aq;
+    has_x = true;
+  }
+
+  // phase 2: gk, gv, and this run's gw, gu
+  for (; it < nitems; ++it) {
+    const State P = Pn;
+    if (it + 1 < nitems) Pn = load_state(chunk_of(it + 1));
+    float* dk;
+    if (!acquire(it, dk)) {
+      if (lane == 0) seq_record_timeout(a.eh);
+      drain_stages<NS>(full, it, issued);
+      return;
+    }
+    const int j = chunk_of(it);
+    const int n = min(kChunk, g.T - j * kChunk);
+    const int64_t row = ((int64_t)col.b * g.T + (int64_t)j * kChunk) * g.C + col.c;
+    float gw_acc, gu_acc;
+    if (n == kChunk)
+      seq_bwd_chunk<true>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last, X,
+                          a.gk + row, a.gv + row, g.C, col.valid, gw_acc, gu_acc, xa, xb, xp);
+    else
+      seq_bwd_chunk<false>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last, X,
+                           a.gk + row, a.gv + row, g.C, col.valid, gw_acc, gu_acc, xa, xb, xp);
+    kahan_add(cw.gw_s, cw.gw_k, gw_acc);
+    kahan_add(cw.gu_s, cw.gu_k, gu_acc);
+    release(it);
+  }
+  // one gw, gu row per (warp, batch row): row warp * B + b of [2][nseg * B][C]
+  if (col.valid) {
+    const size_t o = (size_t)warp * jstride + o0;
+    a.part[o] = cw.gw_s;
+    a.part[(size_t)nseg * jstride + o] = cw.gu_s;
+  }
+}
+
+// ------------------------------------------------------------------ launch
+struct DevInfo {
+  int sms = 0;
+  size_t smem_per_sm = 0;
+};
+
+cudaError_t dev_info(DevInfo& d) {
+  static DevInfo cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && cache[dev].sms > 0) {
+    d = cache[dev];
+    return cudaSuccess;
+  }
+  int sms = 0, smem = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e != cudaSuccess) return e;
+  d.sms = sms;
+  d.smem_per_sm = (size_t)smem;
+  if (dev >= 0 && dev < 64) cache[dev] = d;
+  return cudaSuccess;
+}
+
+// The opt-in to the kernel's shared memory is made once per device and size
+// (the first call, before any stream capture, as for the other kernels),
+// then every call only launches.
+template <class Args, void (*K)(Args)>
+cudaError_t launch_seq(unsigned int cols, int nseg, size_t smem, cudaStream_t s, const Args& a) {
+  static size_t configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || configured[dev] < smem) {
+    e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = smem;
+  }
+  K<<<dim3(cols), dim3(32 * nseg), smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+// Stage counts compiled: 8, 4, 3, 2.  The launcher takes the largest that
+// lets every column's CTA be resident at once (the shared memory of an SM
+// divided by the columns it has to hold), so that no column waits for a
+// second wave; `run(std::integral_constant<int, NS>, smem)` launches.
+template <typename E, class Run>
+cudaError_t launch_staged(const DevInfo& d, unsigned int cols, int nseg, int arrays, bool tma, Run run) {
+  const unsigned int per_sm = (cols + d.sms - 1) / d.sms;
+  const size_t budget = d.smem_per_sm / (per_sm > 0 ? per_sm : 1);
+  auto fits = [&](size_t bytes) { return tma && bytes + 1024 <= budget; };  // 1 KB: the per-CTA reservation
+  if (fits(seq_smem_bytes<E, 8>(nseg, arrays)))
+    return run(std::integral_constant<int, 8>{}, seq_smem_bytes<E, 8>(nseg, arrays));
+  if (fits(seq_smem_bytes<E, 4>(nseg, arrays)))
+    return run(std::integral_constant<int, 4>{}, seq_smem_bytes<E, 4>(nseg, arrays));
+  if (fits(seq_smem_bytes<E, 3>(nseg, arrays)))
+    return run(std::integral_constant<int, 3>{}, seq_smem_bytes<E, 3>(nseg, arrays));
+  return run(std::integral_constant<int, 2>{}, seq_smem_bytes<E, 2>(nseg, arrays));
+}
+
+template <typename KV, bool WRITE_Y>
+cudaError_t launch_seq_fwd_t(const SeqFwdArgs& a, cudaStream_t s) {
+  DevInfo d;
+  cudaError_t e = dev_info(d);
+  if (e != cudaSuccess) return e;
+  const unsigned int cols = (unsigned int)a.g.B * a.g.nwg;
+  return launch_staged<KV>(d, cols, a.nseg, 2, a.use_tma != 0, [&](auto ns, size_t smem) {
+    return launch_seq<SeqFwdArgs, seq_fwd_kernel<KV, decltype(ns)::value, WRITE_Y>>(cols, a.nseg, smem, s, a);
+  });
+}
+
+}  // namespace
+
+cudaError_t launch_seq_forward(const SeqFwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s) {
+  if (kv_dtype == 0)
+    return write_y ? launch_seq_fwd_t<float, true>(a, s) : launch_seq_fwd_t<float, false>(a, s);
+  return write_y ? launch_seq_fwd_t<__nv_bfloat16, true>(a, s) : launch_seq_fwd_t<__nv_bfloat16, false>(a, s);
+}
+
+cudaError_t launch_seq_backward(const SeqBwdArgs& a, cudaStream_t s) {
+  DevInfo d;
+  cudaError_t e = dev_info(d);
+  if (e != cudaSuccess) return e;
+  const unsigned int cols = (unsigned int)a.g.B * a.g.nwg;
+  return launch_staged<float>(d, cols, a.nseg, 3, a.use_tma != 0, [&](auto ns, size_t smem) {
+    return launch_seq<SeqBwdArgs, seq_bwd_kernel<decltype(ns)::value>>(cols, a.nseg, smem, s, a);
+  });
+}
+
+int seq_segments(int cols, int nchunks, int sms) {
+  int nseg = (4 * sms + cols - 1) / (cols > 0 ? cols : 1);  // at least 4 warps per SM
+  if (nseg > kSeqMaxWarps) nseg = kSeqMaxWarps;
+  if (nseg > nchunks) nseg = nchunks;
+  return nseg < 1 ? 1 : nseg;
+}
+
+}  // namespace wkv

@@ -14,6 +14,17 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (B300, sm_103a)")
 
 
+@pytest.fixture(params=["chunked", "sequential"])
+def scan_mode(request):
+    """Runs a GPU test once per scan strategy of wkv_forward / wkv_backward
+    (forced through the library's test hook; back to automatic after)."""
+    from rwkv_linear_attention_backward_b300 import binding
+
+    binding.set_scan_mode(request.param)
+    yield request.param
+    binding.set_scan_mode("auto")
+
+
 @pytest.fixture(scope="session")
 def oracle():
     import oracle as _oracle

@@ -24,7 +24,7 @@ def _run(wkv, w, u, k, v, gy, ckpt_to_bwd=True):
     return (y, ckpt) + tuple(g)
 
 
-def test_bitwise_reproducible(wkv):
+def test_bitwise_reproducible(wkv, scan_mode):
     t = cuda(*inputs.training_inputs(3, 3000, 200, seed=21, k_std=3.0))
     a = _run(wkv, *t)
     for _ in range(3):
@@ -33,7 +33,7 @@ def test_bitwise_reproducible(wkv):
             assert torch.equal(x, y_)
 
 
-def test_checkpoint_and_recompute_agree_bitwise(wkv):
+def test_checkpoint_and_recompute_agree_bitwise(wkv, scan_mode):
     t = cuda(*inputs.training_inputs(2, 1500, 130, seed=22, k_std=3.0))
     a = _run(wkv, *t, ckpt_to_bwd=True)
     b = _run(wkv, *t, ckpt_to_bwd=False)
@@ -42,7 +42,7 @@ def test_checkpoint_and_recompute_agree_bitwise(wkv):
 
 
 @pytest.mark.parametrize("t0", [333, 320])
-def test_forward_causal(wkv, t0):
+def test_forward_causal(wkv, scan_mode, t0):
     """y_t depends on tokens <= t only.  Whole chunks before the change are
     bitwise unchanged.  Inside the chunk holding the change, earlier outputs
     share the chunk's exponent reference (its largest k) with the changed
@@ -62,7 +62,7 @@ def test_forward_causal(wkv, t0):
     assert not torch.equal(y[:, t0:], y2[:, t0:])
 
 
-def test_backward_anticausal(wkv):
+def test_backward_anticausal(wkv, scan_mode):
     """gk_t, gv_t depend on gy_s for s >= t only."""
     w, u, k, v, gy = cuda(*inputs.training_inputs(2, 777, 96, seed=24, k_std=2.0))
     _, _, _, _, gk, gv = _run(wkv, w, u, k, v, gy)
@@ -73,7 +73,7 @@ def test_backward_anticausal(wkv):
     assert torch.equal(gk[:, t0:], gk2[:, t0:]) and torch.equal(gv[:, t0:], gv2[:, t0:])
 
 
-def test_k_shift_invariance(wkv):
+def test_k_shift_invariance(wkv, scan_mode):
     w, u, k, v, gy = cuda(*inputs.training_inputs(2, 600, 64, seed=25, k_std=2.0))
     a = _run(wkv, w, u, k, v, gy)
     b = _run(wkv, w, u, k + 30.0, v, gy)
@@ -84,7 +84,7 @@ def test_k_shift_invariance(wkv):
     assert s <= 1e-4 * a[4].abs().max().item() * 600 ** 0.5
 
 
-def test_workspace_reused_across_shapes(oracle, wkv):
+def test_workspace_reused_across_shapes(oracle, wkv, scan_mode):
     ws = wkv.Workspace(wkv.backward_workspace_bytes(4, 2000, 300))
     for (B, T, C), seed in (((4, 2000, 300), 1), ((1, 50, 7), 2), ((3, 999, 129), 3), ((4, 2000, 300), 4)):
         w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=seed, k_std=2.0)
@@ -99,7 +99,7 @@ def test_workspace_reused_across_shapes(oracle, wkv):
         wkv.workspace_check(ws)
 
 
-def test_side_stream(oracle, wkv):
+def test_side_stream(oracle, wkv, scan_mode):
     w, u, k, v, gy = inputs.training_inputs(2, 400, 80, seed=26)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -142,7 +142,7 @@ def test_expired_wait_is_reported(oracle, wkv, which):
     assert_close(gk, oracle.backward_adjoint(w, u, k, v, gy)[2], TOL_GRAD, "gk after timeout")
 
 
-def test_graph_replay_with_new_inputs(wkv):
+def test_graph_replay_with_new_inputs(wkv, scan_mode):
     """Forward + backward captured once in a CUDA graph and replayed after the
     inputs change in place give the results of direct calls on the new
     inputs (every launch takes a fresh tag on the device, so results carried

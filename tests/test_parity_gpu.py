@@ -2,8 +2,10 @@
 element by element, on seeded inputs (module rwkv_linear_attention_backward_b300.inputs).
 
 Small shapes cover several chunks, ragged chunk and channel-block tails,
-T = 1, deep look-back chains and stress values; the named workloads run at
-full size (the oracle computes sampled channels exactly, since channels are
+T = 1, deep look-back chains and stress values, each under both scan
+strategies (chunked across CTAs, and sequential per column); the named
+workloads run at full size in the strategy the library picks for them (the
+oracle computes sampled channels exactly, since channels are
 independent)."""
 import numpy as np
 import pytest
@@ -48,17 +50,17 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("B,T,C", SHAPES, ids=[f"B{b}T{t}C{c}" for b, t, c in SHAPES])
-def test_small_shapes(oracle, wkv, B, T, C):
+def test_small_shapes(oracle, wkv, scan_mode, B, T, C):
     w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=100 + B * 7 + T + C, k_std=2.0, d_lo=-5.0, d_hi=1.5)
     check_all(oracle, wkv, w, u, k, v, gy, what=f"B{B}T{T}C{C}")
 
 
-def test_without_checkpoint_matches(oracle, wkv):
+def test_without_checkpoint_matches(oracle, wkv, scan_mode):
     w, u, k, v, gy = inputs.training_inputs(2, 300, 160, seed=5, k_std=2.0)
     check_all(oracle, wkv, w, u, k, v, gy, use_ckpt=False, what="no ckpt")
 
 
-def test_checkpoint_is_the_carried_state(oracle, wkv):
+def test_checkpoint_is_the_carried_state(oracle, wkv, scan_mode):
     B, T, C = 2, 150, 70
     w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=6, k_std=3.0)
     y, ckpt = wkv.forward(*cuda(w, u, k, v), want_ckpt=True)
@@ -72,7 +74,7 @@ def test_checkpoint_is_the_carried_state(oracle, wkv):
 
 
 @pytest.mark.parametrize("case", ["k_shift_64", "tiny_w", "huge_w", "big_u", "k_std_8"])
-def test_stress_values(oracle, wkv, case):
+def test_stress_values(oracle, wkv, scan_mode, case):
     B, T, C = 2, 400, 96
     kw = dict(k_std=2.0, d_lo=-5.0, d_hi=1.0)
     if case == "tiny_w":
@@ -89,7 +91,7 @@ def test_stress_values(oracle, wkv, case):
     check_all(oracle, wkv, w, u, k, v, gy, what=case)
 
 
-def test_deep_lookback_chain(oracle, wkv):
+def test_deep_lookback_chain(oracle, wkv, scan_mode):
     """One 32-channel group and 2048 chunks: every tile of a row waits on a
     long chain of predecessors in both directions."""
     B, T, C = 1, 65536, 32
@@ -97,7 +99,7 @@ def test_deep_lookback_chain(oracle, wkv):
     check_all(oracle, wkv, w, u, k, v, gy, what="deep chain")
 
 
-def test_bf16_forward(oracle, wkv):
+def test_bf16_forward(oracle, wkv, scan_mode):
     B, T, C = 2, 777, 136
     w, u, k, v, _ = inputs.training_inputs(B, T, C, seed=9, k_std=5.0, d_lo=-8.0, d_hi=1.0, kv_dtype="bf16")
     y = wkv.forward(*cuda(w, u, k, v))
@@ -105,6 +107,54 @@ def test_bf16_forward(oracle, wkv):
     assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_BF16, "bf16 y")
     # far inside the loose bf16 tolerance: the oracle sees the same rounded inputs
     assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "bf16 y (fp32-level)")
+
+
+def _both_modes(wkv, w, u, k, v, gy):
+    res = {}
+    try:
+        for mode in ("chunked", "sequential"):
+            wkv.set_scan_mode(mode)
+            res[mode] = run_fwd_bwd(wkv, w, u, k, v, gy)
+    finally:
+        wkv.set_scan_mode("auto")
+    return res["chunked"], res["sequential"]
+
+
+def test_scan_modes_agree_bitwise(wkv):
+    """With one run per column (enough columns: 640 here, four warps per SM
+    of a 148-SM part), the sequential walk carries the state across chunk
+    boundaries with the chunked scan's combine, in the same order, and
+    computes a chunk's outputs with the same fixed-scale arithmetic: on
+    inputs where every chunk stays on the fixed scale, y and the checkpoints
+    agree bit for bit.  The gradients add a chunk's carried adjoint in
+    another order: equal to rounding."""
+    w, u, k, v, gy = inputs.training_inputs(5, 300, 4096, seed=42, k_std=2.0, d_lo=-6.0, d_hi=2.0)
+    a, b = _both_modes(wkv, w, u, k, v, gy)
+    assert torch.equal(a[0], b[0]), "y"
+    assert torch.equal(a[1], b[1]), "ckpt"
+    for x, y_, n in zip(a[2:], b[2:], ("gw", "gu", "gk", "gv")):
+        assert_close(y_, x, TOL_GRAD, f"{n} sequential vs chunked")
+
+
+def test_scan_modes_agree_runs(oracle, wkv):
+    """At the 169M layer shape (192 columns) each column's walk is split into
+    runs carried through shared memory: both strategies match the oracle and
+    each other."""
+    B, T, C = 8, 1000, 768
+    w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=41, k_std=3.0, d_lo=-6.0, d_hi=2.0)
+    a, b = _both_modes(wkv, w, u, k, v, gy)
+    assert_close(b[0], a[0], TOL_Y, "y sequential vs chunked")
+    for x, y_, n in zip(a[2:], b[2:], ("gw", "gu", "gk", "gv")):
+        assert_close(y_, x, TOL_GRAD, f"{n} sequential vs chunked")
+    cs = sample_channels(C, 24, 41)
+    ks, vs = k[:, :, cs].contiguous(), v[:, :, cs].contiguous()
+    ow, ou, ok, ov = oracle.backward_adjoint(w[cs], u[cs], ks, vs, gy[:, :, cs].contiguous())
+    cst = torch.as_tensor(cs, device="cuda")
+    assert_close(b[0].index_select(2, cst), oracle.forward_recurrent(w[cs], u[cs], ks, vs), TOL_Y, "sequential y")
+    assert_close(b[4].index_select(2, cst), ok, TOL_GRAD, "sequential gk")
+    assert_close(b[5].index_select(2, cst), ov, TOL_GRAD, "sequential gv")
+    assert_close(b[2].index_select(0, cst), ow, TOL_GRAD, "sequential gw")
+    assert_close(b[3].index_select(0, cst), ou, TOL_GRAD, "sequential gu")
 
 
 # ------------------------------------------------------------ named workloads
