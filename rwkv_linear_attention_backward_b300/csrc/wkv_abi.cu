@@ -99,8 +99,7 @@ char* bytes(void* p) { return static_cast<char*>(p); }
 // columns alone keep the GPU busy and a column's chunks need no exchange
 // between CTAs; fewer columns leave SMs idle, and the chunked scans split
 // time across CTAs instead.
-// nseg receives the runs per column of the sequential kernels.
-cudaError_t sequential_mode(const ScanGeometry& g, bool& seq, int& nseg) {
+cudaError_t sequential_mode(const ScanGeometry& g, bool& seq) {
   static int sms_per_dev[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -114,7 +113,6 @@ cudaError_t sequential_mode(const ScanGeometry& g, bool& seq, int& nseg) {
   const long long cols = (long long)g.B * g.nwg;
   const int mode = g_scan_mode.load();
   seq = mode == WKV_SCAN_AUTO ? cols >= sms : mode == WKV_SCAN_SEQUENTIAL;
-  nseg = seq_segments((int)(cols < INT_MAX ? cols : INT_MAX), g.nchunks, sms);
   return cudaSuccess;
 }
 
@@ -179,7 +177,7 @@ namespace {
 // (recomputed by a state-only forward walk when the caller has none), the
 // reverse walk writing gk, gv and one gw, gu row per batch row, then the
 // reduction of those B rows.
-wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int nseg, const float* w, const float* u,
+wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const float* w, const float* u,
                                const void* k, const void* v, const float* gy, const float* ckpt, float* gw,
                                float* gu, float* gk, float* gv, WsHeader* hdr, void* workspace, uint64_t budget,
                                cudaStream_t s) {
@@ -197,7 +195,7 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int ns
     f.eh = hdr;
     f.g = g;
     f.budget_ns = budget;
-    f.nseg = nseg;
+    f.nseg = seq_segments(B, T, C, 2, 4, false);
     f.use_tma = make_tile_map(&f.tk, k, B, T, C, 4, kSeqChannels) && make_tile_map(&f.tv, v, B, T, C, 4, kSeqChannels);
     cudaError_t e = launch_seq_forward(f, WKV_F32, false, s);
     if (e != cudaSuccess) return cuda_fail(e, "wkv_backward: state pass");
@@ -217,6 +215,7 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int ns
   a.eh = hdr;
   a.g = g;
   a.budget_ns = budget;
+  const int nseg = seq_segments(B, T, C, 3, 4, true);
   a.nseg = nseg;
   a.use_tma = make_tile_map(&a.tk, k, B, T, C, 4, kSeqChannels) && make_tile_map(&a.tv, v, B, T, C, 4, kSeqChannels) &&
               make_tile_map(&a.tg, gy, B, T, C, 4, kSeqChannels);
@@ -312,8 +311,7 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
   if (!workspace || workspace_bytes < l.total) return WKV_ERR_WORKSPACE;
   const int eb = kv_dtype == WKV_F32 ? 4 : 2;
   bool seq = false;
-  int nseg = 1;
-  cudaError_t e = sequential_mode(g, seq, nseg);
+  cudaError_t e = sequential_mode(g, seq);
   if (e != cudaSuccess) return cuda_fail(e, "wkv_forward");
   if (seq) {
     SeqFwdArgs q;
@@ -327,7 +325,7 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
     q.eh = static_cast<WsHeader*>(workspace);
     q.g = g;
     q.budget_ns = (uint64_t)g_budget_ns.load();
-    q.nseg = nseg;
+    q.nseg = seq_segments(B, T, C, 2, eb, false);
     q.use_tma = make_tile_map(&q.tk, k, B, T, C, eb, kSeqChannels) && make_tile_map(&q.tv, v, B, T, C, eb, kSeqChannels);
     e = launch_seq_forward(q, kv_dtype, true, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
@@ -368,10 +366,9 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
   const int skip = g_skip_chunk.load();
   const uint64_t budget = (uint64_t)g_budget_ns.load();
   bool seq = false;
-  int nseg = 1;
-  cudaError_t e = sequential_mode(g, seq, nseg);
+  cudaError_t e = sequential_mode(g, seq);
   if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
-  if (seq) return backward_sequential(g, l, nseg, w, u, k, v, gy, ckpt, gw, gu, gk, gv, hdr, workspace, budget, s);
+  if (seq) return backward_sequential(g, l, w, u, k, v, gy, ckpt, gw, gu, gk, gv, hdr, workspace, budget, s);
 
   const float* states = ckpt;
   if (!states) {

@@ -145,9 +145,12 @@ struct SeqBwdArgs {
 };
 
 cudaError_t launch_seq_forward(const SeqFwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
-// Runs per column (warps per CTA) of the sequential kernels: enough for about
-// four warps per SM, at most kSeqMaxWarps and at most one per chunk.
-int seq_segments(int cols, int nchunks, int sms);
+// Runs per column (warps per CTA) of a sequential kernel over `arrays`
+// [B, T, C] inputs of elem_bytes each: about 8 warps per SM, within the
+// SM's shared memory (and, backward, its registers), only while the inputs
+// re-read by the runs fit in L2 (or the columns alone leave SMs idle); at
+// most kSeqMaxWarps and one per chunk.
+int seq_segments(int B, int T, int C, int arrays, int elem_bytes, bool backward);
 cudaError_t launch_seq_backward(const SeqBwdArgs& a, cudaStream_t s);
 
 // Grid of a persistent scan kernel: resident CTAs per SM x SMs, at most ntiles.

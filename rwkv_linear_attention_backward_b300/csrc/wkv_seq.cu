@@ -166,26 +166,39 @@ __device__ __forceinline__ void seq_fwd_full(const KV* __restrict__ sk, const KV
   const float r = tree_max<L>(rr);
   const bool fast = (kmin + fminf(u, 0.f) >= F - kFastRange) && (u <= kFastCeil) && (P.pp - F <= kFastCeil);
   if (fast) {
+    // Phase by phase over the whole chunk (independent work per token in
+    // each, so one warp keeps several in flight): ek; the carried sums
+    // before each token (four chains); the outputs.
     const float F2 = F * kLog2e;
     const float s0 = exp_nat(P.pp - F);
-    float na = P.num * s0, nb = P.den * s0;
-    float on = 0.f, od = 0.f;
-#pragma unroll
-    for (int i = 0; i < L; ++i) kr[i] = ex2(fmaf(kr[i], kLog2e, -F2));  // ek
+    float vr[L];
 #pragma unroll
     for (int i = 0; i < L; ++i) {
-      const float ek = kr[i];
-      const float vv = to_f32<KV>(sv[i * S]);
-      const float ekv = ek * vv;
+      vr[i] = to_f32<KV>(sv[i * S]);
+      kr[i] = ex2(fmaf(kr[i], kLog2e, -F2));  // ek
+    }
+    float na = P.num * s0, nb = P.den * s0;
+    float on = 0.f, od = 0.f;
+    float A[L], Bd[L];  // sums with P before each token (for the outputs)
+#pragma unroll
+    for (int i = 0; i < L; ++i) {
+      const float ekv = kr[i] * vr[i];
       if constexpr (WRITE_Y) {
-        const float ec = ek * eu;
-        const float yv = fmaf(ec, vv, na) * rcp(nb + ec);
-        if (valid) __stcs(yp + (int64_t)i * ystride, yv);
+        A[i] = na;
+        Bd[i] = nb;
         na = fmaf(na, ew, ekv);
-        nb = fmaf(nb, ew, ek);
+        nb = fmaf(nb, ew, kr[i]);
       }
       on = fmaf(on, ew, ekv);
-      od = fmaf(od, ew, ek);
+      od = fmaf(od, ew, kr[i]);
+    }
+    if constexpr (WRITE_Y) {
+#pragma unroll
+      for (int i = 0; i < L; ++i) {
+        const float ec = kr[i] * eu;
+        const float yv = fmaf(ec, vr[i], A[i]) * rcp(Bd[i] + ec);
+        if (valid) __stcs(yp + (int64_t)i * ystride, yv);
+      }
     }
     const float sc = exp_nat(F - r);
     P = combine(P, (float)L * w, State{on * sc, od * sc, r});
@@ -265,13 +278,13 @@ __device__ __forceinline__ void seq_fwd_chunk(const KV* __restrict__ sk, const K
 // from the empty one); after one CTA barrier each warp folds the summaries
 // of the runs before its own into its carry and walks its run again with it
 // (phase 2, reading the run a second time, from L2).  The last warp has no
-// phase 1, so it takes about 1.5 times the chunks of the others (a summary
-// costs about half a full walk).  With nseg == 1 this is the plain
-// sequential walk.
+// phase 1 but cannot start phase 2 before the barrier either, so the runs
+// are equal (the first nchunks % nseg one chunk longer).  With nseg == 1
+// this is the plain sequential walk.
 __device__ __forceinline__ void segment_of(int nchunks, int nseg, int s, int& first, int& count) {
-  const int c = nseg > 1 ? (2 * nchunks) / (2 * nseg + 1) : 0;
-  first = s * c;
-  count = s < nseg - 1 ? c : nchunks - first;  // >= 1 for the last warp
+  const int base = nchunks / nseg, rem = nchunks - base * nseg;
+  first = s * base + min(s, rem);
+  count = base + (s < rem ? 1 : 0);
 }
 
 // Shared memory of a CTA of nseg warps: each warp's ring of NS stages of
@@ -505,12 +518,46 @@ __device__ __forceinline__ void seq_bwd_chunk(float* __restrict__ sk, const floa
     const float xla = X.la * f, xlb = X.lb * f;
     float la0 = 0.f, lb0 = 0.f, pw = 1.f;
     float gwb = 0.f;  // gw's lb share: a second chain beside gw_acc's la share
+    if constexpr (FULL) {
+      // the per-token terms that need no adjoint, for the whole chunk first
+      // (independent work), then the reverse sweep's chains
+      float GI[L], VM[L];
 #pragma unroll
-    for (int i = L - 1; i >= 0; --i) {
-      if (FULL || i < n) {
+      for (int i = 0; i < L; ++i) {
+        const float ec = kr[i] * cw.eu;
+        const float rr = rcp(Bd[i] + ec);
+        GI[i] = sg[i * S] * rr;                        // gN at scale e^{F}
+        VM[i] = fmaf(sv[i * S], Bd[i], -A[i]) * rr;  // v - wkv
+      }
+#pragma unroll
+      for (int i = L - 1; i >= 0; --i) {
         const float la = fmaf(xla, pw, la0);  // adjoints after token i, at scale e^{F}
         const float lb = fmaf(xlb, pw, lb0);
-        const float ek = FULL ? kr[i] : sk[i * S];
+        const float ek = kr[i];
+        const float vv = sv[i * S];
+        const float ec = ek * cw.eu;
+        const float gi = GI[i];
+        const float cur = gi * VM[i] * ec;  // (gN v + gD) e^{u+k}
+        const float gk = fmaf(fmaf(la, vv, lb), ek, cur);
+        const float gv = fmaf(gi, ec, la * ek);
+        gu_acc += cur;
+        gw_acc = fmaf(la, A[i], gw_acc);
+        gwb = fmaf(lb, Bd[i], gwb);
+        la0 = fmaf(la0, cw.ew, gi);
+        lb0 = fmaf(lb0, cw.ew, -gi * (vv - VM[i]));
+        pw *= cw.ew;
+        if (valid) {
+          __stcs(gkp + (int64_t)i * stride, gk);
+          __stcs(gvp + (int64_t)i * stride, gv);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = L - 1; i >= 0; --i) {
+      if (!FULL && i < n) {
+        const float la = fmaf(xla, pw, la0);
+        const float lb = fmaf(xlb, pw, lb0);
+        const float ek = sk[i * S];
         const float vv = sv[i * S];
         const float ec = ek * cw.eu;
         const float rr = rcp(Bd[i] + ec);
@@ -793,6 +840,7 @@ __global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_bwd_kernel(const __grid
 struct DevInfo {
   int sms = 0;
   size_t smem_per_sm = 0;
+  size_t l2 = 0;
 };
 
 cudaError_t dev_info(DevInfo& d) {
@@ -809,8 +857,12 @@ cudaError_t dev_info(DevInfo& d) {
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   if (e != cudaSuccess) return e;
+  int l2 = 0;
+  e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+  if (e != cudaSuccess) return e;
   d.sms = sms;
   d.smem_per_sm = (size_t)smem;
+  d.l2 = (size_t)l2;
   if (dev >= 0 && dev < 64) cache[dev] = d;
   return cudaSuccess;
 }
@@ -880,11 +932,28 @@ cudaError_t launch_seq_backward(const SeqBwdArgs& a, cudaStream_t s) {
   });
 }
 
-int seq_segments(int cols, int nchunks, int sms) {
-  int nseg = (4 * sms + cols - 1) / (cols > 0 ? cols : 1);  // at least 4 warps per SM
+int seq_segments(int B, int T, int C, int arrays, int elem_bytes, bool backward) {
+  DevInfo d;
+  if (dev_info(d) != cudaSuccess || d.sms <= 0) return 1;
+  const ScanGeometry g = make_geometry(B, T, C);
+  const long long cols = (long long)g.B * g.nwg;
+  const long long per_sm = (cols + d.sms - 1) / d.sms;
+  // warps an SM can hold: two stages each in shared memory; the backward
+  // kernel's registers (up to 255 per thread) allow 8 warps per SM
+  const size_t stage = (size_t)arrays * kSeqTile * elem_bytes;
+  long long warps = (long long)(d.smem_per_sm / (2 * stage + 512));
+  if (backward && warps > 8) warps = 8;
+  long long nseg = warps / (per_sm > 0 ? per_sm : 1);
+  const long long want = (8LL * d.sms + cols - 1) / cols;  // about 8 warps per SM
+  if (nseg > want) nseg = want;
   if (nseg > kSeqMaxWarps) nseg = kSeqMaxWarps;
-  if (nseg > nchunks) nseg = nchunks;
-  return nseg < 1 ? 1 : nseg;
+  // Phase 2 re-reads what the runs but the last summarised in phase 1: only
+  // worth it while that still sits in L2 (60% of it here), unless the
+  // columns alone leave SMs idle.
+  const double reread = (double)B * T * C * arrays * elem_bytes * (double)(nseg - 1) / (double)nseg;
+  if (cols >= d.sms && reread > 0.6 * (double)d.l2) nseg = 1;
+  if (nseg > g.nchunks) nseg = g.nchunks;
+  return nseg < 1 ? 1 : (int)nseg;
 }
 
 }  // namespace wkv
