@@ -288,7 +288,13 @@ class TrainingRun:
         self.bytes_fwd = kv_bytes * self.elements
         self.bytes_bwd = BYTES_BWD * self.elements if wl.backward else 0
         self.launches_per_step = 1 + (2 if wl.backward else 0)
-        self.dominant = "bwd_scan_kernel" if wl.backward else "fwd_scan_kernel"
+        from rwkv_linear_attention_backward_b300 import binding
+
+        self.strategy = binding.scan_strategy(wl.B, wl.T, wl.C)
+        if self.strategy == "sequential":
+            self.dominant = "seq_bwd_kernel" if wl.backward else "seq_fwd_kernel"
+        else:
+            self.dominant = "bwd_scan_kernel" if wl.backward else "fwd_scan_kernel"
         self.dominant_bytes = self.bytes_bwd if wl.backward else self.bytes_fwd
 
     def _forward(self):
@@ -559,6 +565,7 @@ def run_ours(args):
                    "CUDA graphs of the forward and backward calls, captured once and replayed per step",
                    "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}",
                    "scan_mode": args.scan_mode,
+                   "strategy": getattr(run, "strategy", "n/a"),
                    "checkpoints": "forward writes chunk checkpoints, backward reads them"
                    if args.workload != "decode" else "n/a"})
     out = {

@@ -220,6 +220,14 @@ wkv_status wkv_debug_set_skip_chunk(int chunk);
  */
 wkv_status wkv_debug_set_scan_mode(int mode);
 
+/*
+ * wkv_scan_strategy: the strategy wkv_forward and wkv_backward take for a
+ * [B, T, C] call on the current device under the current scan mode:
+ * WKV_SCAN_CHUNKED or WKV_SCAN_SEQUENTIAL; -1 for invalid sizes or when the
+ * device cannot be queried.  Host only; nothing is launched.
+ */
+int wkv_scan_strategy(int B, int T, int C);
+
 #ifdef __cplusplus
 }
 #endif

@@ -45,6 +45,7 @@ _SIGNATURES = {
     "wkv_debug_set_wait_budget_ns": ([_ll], _i),
     "wkv_debug_set_skip_chunk": ([_i], _i),
     "wkv_debug_set_scan_mode": ([_i], _i),
+    "wkv_scan_strategy": ([_i, _i, _i], _i),
 }
 for _name, (_args, _res) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -258,6 +259,15 @@ def set_skip_chunk(chunk: int) -> None:
 
 
 SCAN_MODES = {"auto": 0, "chunked": 1, "sequential": 2}
+
+
+def scan_strategy(B: int, T: int, C: int) -> str:
+    """"chunked" or "sequential": the kernels forward/backward run for a
+    [B, T, C] call on the current device (under the current scan mode)."""
+    r = int(_lib.wkv_scan_strategy(B, T, C))
+    if r < 0:
+        raise WKVError(1, "wkv_scan_strategy")  # WKV_ERR_INVALID_ARG
+    return {1: "chunked", 2: "sequential"}[r]
 
 
 def set_scan_mode(mode: str) -> None:

@@ -192,10 +192,11 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const 
     f.v = v;
     f.y = nullptr;
     f.ckpt = reinterpret_cast<float*>(bytes(workspace) + l.fwd + fwd_layout(g).ckpt);
+    f.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.fwd + fwd_layout(g).agg);
+    f.exited = &hdr->exited[1];
     f.eh = hdr;
     f.g = g;
     f.budget_ns = budget;
-    f.nseg = seq_segments(B, T, C, 2, 4, false);
     f.use_tma = make_tile_map(&f.tk, k, B, T, C, 4, kSeqChannels) && make_tile_map(&f.tv, v, B, T, C, 4, kSeqChannels);
     cudaError_t e = launch_seq_forward(f, WKV_F32, false, s);
     if (e != cudaSuccess) return cuda_fail(e, "wkv_backward: state pass");
@@ -212,15 +213,16 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const 
   a.gk = gk;
   a.gv = gv;
   a.part = reinterpret_cast<float*>(bytes(workspace) + l.part);  // [2][nseg * B][C]
+  a.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.ragg);
+  a.exited = &hdr->exited[2];
   a.eh = hdr;
   a.g = g;
   a.budget_ns = budget;
-  const int nseg = seq_segments(B, T, C, 3, 4, true);
-  a.nseg = nseg;
   a.use_tma = make_tile_map(&a.tk, k, B, T, C, 4, kSeqChannels) && make_tile_map(&a.tv, v, B, T, C, 4, kSeqChannels) &&
               make_tile_map(&a.tg, gy, B, T, C, 4, kSeqChannels);
   cudaError_t e = launch_seq_backward(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
+  const int nseg = a.nseg;
   ReduceArgs r;
   r.part = a.part;
   r.slices = reinterpret_cast<float*>(bytes(workspace) + l.slices);
@@ -322,10 +324,11 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
     q.v = v;
     q.y = y;
     q.ckpt = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.ckpt);
+    q.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.agg);
     q.eh = static_cast<WsHeader*>(workspace);
+    q.exited = &q.eh->exited[0];
     q.g = g;
     q.budget_ns = (uint64_t)g_budget_ns.load();
-    q.nseg = seq_segments(B, T, C, 2, eb, false);
     q.use_tma = make_tile_map(&q.tk, k, B, T, C, eb, kSeqChannels) && make_tile_map(&q.tv, v, B, T, C, eb, kSeqChannels);
     e = launch_seq_forward(q, kv_dtype, true, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
@@ -461,6 +464,13 @@ wkv_status wkv_debug_set_wait_budget_ns(long long ns) {
 wkv_status wkv_debug_set_skip_chunk(int chunk) {
   g_skip_chunk.store(chunk < 0 ? -1 : chunk);
   return WKV_OK;
+}
+
+int wkv_scan_strategy(int B, int T, int C) {
+  if (!sizes_ok(B, T, C)) return -1;
+  bool seq = false;
+  if (sequential_mode(make_geometry(B, T, C), seq) != cudaSuccess) return -1;
+  return seq ? WKV_SCAN_SEQUENTIAL : WKV_SCAN_CHUNKED;
 }
 
 wkv_status wkv_debug_set_scan_mode(int mode) {

@@ -105,11 +105,13 @@ void set_last_error(const char* msg);
 // driver has no encoder; the kernels then stage tiles with plain loads.
 bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int elem_bytes, int box_c);
 
-// Sequential column kernels (wkv_seq.cu): one warp per column of 32
-// channels of one batch row, walking the time chunks in order; used when
-// there are at least as many columns as SMs (no chunk results cross CTAs).
+// Sequential column kernels (wkv_seq.cu): a column is one batch row and 32
+// channels; its chunks are walked in order (forward) or in reverse order
+// (backward) by nseg runs, one warp (CTA) each, which exchange one summary
+// each through tagged records.  Used when there are at least as many
+// columns as SMs (wkv_abi.cu).
 constexpr int kSeqChannels = 32;
-constexpr int kSeqMaxWarps = 8;  // runs (warps) per column's CTA
+constexpr int kSeqMaxRuns = 32;  // runs per column
 
 struct SeqFwdArgs {
   CUtensorMap tk, tv;  // box {32, kChunk, 1} (when use_tma)
@@ -117,12 +119,14 @@ struct SeqFwdArgs {
   const float* u;
   const void* k;
   const void* v;
-  float* y;     // may be null (state-only pass)
-  float* ckpt;  // [3][nchunks][B][C] state after each chunk
+  float* y;               // may be null (state-only pass)
+  float* ckpt;            // [3][nchunks][B][C] state after each chunk
+  Rec* recs;              // [nseg][B][C] run summaries (tagged records)
+  unsigned int* exited;   // CTAs of this launch that have finished (in a workspace header)
   WsHeader* eh;
   ScanGeometry g;
   uint64_t budget_ns;
-  int nseg;  // warps per column, each walking one run of its chunks (seq_segments)
+  int nseg;               // runs per column: set by launch_seq_forward
   int use_tma;
 };
 
@@ -136,22 +140,19 @@ struct SeqBwdArgs {
   const float* ckpt;
   float* gk;
   float* gv;
-  float* part;  // [2][nseg * B][C] gw, gu sums per (run, batch row)
+  float* part;            // [2][nseg * B][C] gw, gu sums per (run, batch row)
+  Rec* recs;              // [nseg][B][C] run summaries (tagged records)
+  unsigned int* exited;
   WsHeader* eh;
   ScanGeometry g;
   uint64_t budget_ns;
-  int nseg;
+  int nseg;               // runs per column: set by launch_seq_backward
   int use_tma;
 };
 
-cudaError_t launch_seq_forward(const SeqFwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
-// Runs per column (warps per CTA) of a sequential kernel over `arrays`
-// [B, T, C] inputs of elem_bytes each: about 8 warps per SM, within the
-// SM's shared memory (and, backward, its registers), only while the inputs
-// re-read by the runs fit in L2 (or the columns alone leave SMs idle); at
-// most kSeqMaxWarps and one per chunk.
-int seq_segments(int B, int T, int C, int arrays, int elem_bytes, bool backward);
-cudaError_t launch_seq_backward(const SeqBwdArgs& a, cudaStream_t s);
+// Choose the runs per column (written to a.nseg) and launch.
+cudaError_t launch_seq_forward(SeqFwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
+cudaError_t launch_seq_backward(SeqBwdArgs& a, cudaStream_t s);
 
 // Grid of a persistent scan kernel: resident CTAs per SM x SMs, at most ntiles.
 cudaError_t launch_forward(FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);

@@ -51,28 +51,16 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
   return __bfloat162float(x);
 }
 
-// Records an expired wait: the code only (these kernels have no launch epoch
-// and other launches' waits must not stop on their account).
-__device__ __forceinline__ void seq_record_timeout(WsHeader* h) { atomicCAS(&h->error, 0u, kDevErrTimeout); }
-
-// Bytes of the stage ring's control block (one mbarrier per stage), a
-// multiple of 128.
-template <int NS>
-__host__ __device__ constexpr size_t seq_ctl_bytes() {
-  return ((size_t)NS * 8 + 127) / 128 * 128;
-}
-
-// The column of this CTA: batch row, first channel, this lane's channel
-// (every warp of the CTA covers the same 32 channels).
+// Column q (batch row q / nwg, channels from 32 (q % nwg)): batch row,
+// first channel, this lane's channel.
 struct Column {
   int b, c0, c;
   bool valid;  // c < C
   int cc;      // c clamped into [0, C)
 };
 
-__device__ __forceinline__ Column column_of(const ScanGeometry& g) {
+__device__ __forceinline__ Column column_of(const ScanGeometry& g, int q) {
   Column o;
-  const int q = blockIdx.x;
   o.b = q / g.nwg;
   o.c0 = (q - o.b * g.nwg) * kSeqChannels;
   o.c = o.c0 + (int)(threadIdx.x & 31);
@@ -121,15 +109,31 @@ __device__ __forceinline__ void drain_stages(uint64_t* full, int first, int issu
   }
 }
 
-// Largest / smallest of x[0..N): a balanced tree (max and min are exact, so
-// the result is that of any order), with N/2 independent operations per
-// level instead of a chain of N.
+// Three-input max / min (single PTX instructions on sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Largest / smallest of x[0..N): a balanced ternary tree (max and min are
+// exact, so the result is that of any order), with many independent
+// operations per level instead of a chain of N.
 template <int N>
 __device__ __forceinline__ float tree_max(const float* x) {
   if constexpr (N == 1) {
     return x[0];
+  } else if constexpr (N == 2) {
+    return fmaxf(x[0], x[1]);
   } else {
-    return fmaxf(tree_max<N / 2>(x), tree_max<N - N / 2>(x + N / 2));
+    constexpr int a = N / 3, b = N / 3;
+    return max3f(tree_max<a>(x), tree_max<b>(x + a), tree_max<N - a - b>(x + a + b));
   }
 }
 
@@ -137,8 +141,11 @@ template <int N>
 __device__ __forceinline__ float tree_min(const float* x) {
   if constexpr (N == 1) {
     return x[0];
+  } else if constexpr (N == 2) {
+    return fminf(x[0], x[1]);
   } else {
-    return fminf(tree_min<N / 2>(x), tree_min<N - N / 2>(x + N / 2));
+    constexpr int a = N / 3, b = N / 3;
+    return min3f(tree_min<a>(x), tree_min<b>(x + a), tree_min<N - a - b>(x + a + b));
   }
 }
 
@@ -271,57 +278,94 @@ __device__ __forceinline__ void seq_fwd_chunk(const KV* __restrict__ sk, const K
   }
 }
 
-// Segments of a column's walk, one per warp of the CTA: the chunks in walk
-// order (time order for the forward pass, reverse time order for the
-// backward pass) cut into nseg contiguous runs.  Every warp but the last
-// first summarises its run (phase 1: the state, or the adjoint, it carries
-// from the empty one); after one CTA barrier each warp folds the summaries
-// of the runs before its own into its carry and walks its run again with it
-// (phase 2, reading the run a second time, from L2).  The last warp has no
-// phase 1 but cannot start phase 2 before the barrier either, so the runs
-// are equal (the first nchunks % nseg one chunk longer).  With nseg == 1
-// this is the plain sequential walk.
+// Runs of a column's walk: the chunks in walk order (time order for the
+// forward pass, reverse time order for the backward pass) cut into nseg
+// equal contiguous runs (the first nchunks % nseg one chunk longer); run s
+// of column q is CTA q * nseg + s, one warp.  Every run but the last first
+// summarises its chunks (phase 1: the state, or the adjoint, it carries from
+// the empty one) and publishes the summary as tagged records; then each run
+// folds the summaries of the runs before it into its carry and walks its
+// chunks again with it (phase 2, reading them a second time, from L2 while
+// they fit there).  The runs of a column wait only on phase-1 results, which
+// every run produces before it waits, and the launch is cooperative (all
+// runs resident), so the waits always end.  With nseg == 1 this is the
+// plain sequential walk and nothing is exchanged.
 __device__ __forceinline__ void segment_of(int nchunks, int nseg, int s, int& first, int& count) {
   const int base = nchunks / nseg, rem = nchunks - base * nseg;
   first = s * base + min(s, rem);
   count = base + (s < rem ? 1 : 0);
 }
 
-// Shared memory of a CTA of nseg warps: each warp's ring of NS stages of
-// `arrays` [kChunk x 32] boxes of E, the warps' stage mbarriers [nseg][NS],
-// then the run summaries [nseg][3][32] f32.
+// Shared memory of a run's CTA: its ring of NS stages of `arrays`
+// [kChunk x 32] boxes of E, then the stages' mbarriers.
 template <typename E, int NS>
 __host__ __device__ constexpr size_t seq_ring_elems(int arrays) {
   return (size_t)NS * arrays * kSeqTile;
 }
 
 template <typename E, int NS>
-__host__ __device__ constexpr size_t seq_smem_bytes(int nseg, int arrays) {
-  return (size_t)nseg * seq_ring_elems<E, NS>(arrays) * sizeof(E) + ((size_t)nseg * NS * 8 + 127) / 128 * 128 +
-         (size_t)nseg * 3 * 32 * sizeof(float);
+__host__ __device__ constexpr size_t seq_smem_bytes(int arrays) {
+  return seq_ring_elems<E, NS>(arrays) * sizeof(E) + 128;
+}
+
+// The launch's identity: 1 + the workspace's sequence number, read by every
+// CTA at its start, before the last CTA to finish can advance it (seq_exit).
+__device__ __forceinline__ Launch seq_launch(const WsHeader* h) {
+  unsigned long long e = 0;
+  if ((threadIdx.x & 31) == 0) e = *(volatile const unsigned long long*)&h->seq + 1ull;
+  e = __shfl_sync(0xffffffffu, e, 0);
+  return Launch{e, tag_of(e)};
+}
+
+// The last CTA out resets the exit counter and advances the sequence number.
+__device__ __forceinline__ void seq_exit(unsigned int* exited, WsHeader* h, unsigned long long epoch) {
+  __syncwarp();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(exited, 1u) == gridDim.x - 1) {
+      atomicExch(exited, 0u);
+      atomicExch(&h->seq, epoch);
+    }
+  }
+}
+
+// Waits (bounded) until the record at p carries this launch's tag on every
+// valid lane.  False when the wait expired (recorded) or the launch gave up
+// elsewhere.
+__device__ __forceinline__ bool wait_rec(const Rec* p, bool valid, const Launch& L, WsHeader* h, uint64_t budget_ns,
+                                         Rec& r) {
+  r = rec_load(p);
+  if (__all_sync(0xffffffffu, !valid || rec_ok(r, L.tag))) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    __nanosleep(100);
+    r = rec_load(p);
+    if (__all_sync(0xffffffffu, !valid || rec_ok(r, L.tag))) return true;
+    if (__shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&h->abort, 0) == L.epoch) return false;
+    if (__shfl_sync(0xffffffffu, globaltimer(), 0) - t0 > budget_ns) {
+      if ((threadIdx.x & 31) == 0) record_error(h, kDevErrTimeout, L.epoch);
+      return false;
+    }
+  }
 }
 
 template <typename KV, int NS, bool WRITE_Y>
-__global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_fwd_kernel(const __grid_constant__ SeqFwdArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int nseg = blockDim.x >> 5;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  constexpr size_t kRing = seq_ring_elems<KV, NS>(2);  // stage s: k at 2s*kSeqTile, v at (2s+1)*kSeqTile
-  KV* ring = reinterpret_cast<KV*>(smem) + (size_t)warp * kRing;
-  unsigned char* ctl = smem + (size_t)nseg * kRing * sizeof(KV);
-  uint64_t* full = reinterpret_cast<uint64_t*>(ctl) + warp * NS;
-  float* summ = reinterpret_cast<float*>(ctl + ((size_t)nseg * NS * 8 + 127) / 128 * 128);  // [nseg][3][32]
+__device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L, unsigned char* smem) {
+  KV* ring = reinterpret_cast<KV*>(smem);  // stage s: k at 2s*kSeqTile, v at (2s+1)*kSeqTile
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + seq_ring_elems<KV, NS>(2) * sizeof(KV));
+  const int lane = threadIdx.x;
   const ScanGeometry& g = a.g;
-  const Column col = column_of(g);
+  const int nseg = a.nseg;
+  const int q = blockIdx.x / nseg, run = blockIdx.x - q * nseg;
+  const Column col = column_of(g, q);
   const float w = __ldg(a.w + col.cc), u = __ldg(a.u + col.cc);
   const float ew = expf(-w), eu = expf(u);
   const bool tma = a.use_tma != 0;
   constexpr uint32_t kStageBytes = 2 * kSeqTile * sizeof(KV);
 
   int first, count;
-  segment_of(g.nchunks, nseg, warp, first, count);
-  const int n1 = warp < nseg - 1 ? count : 0;  // phase-1 items, then the same chunks again
+  segment_of(g.nchunks, nseg, run, first, count);
+  const int n1 = run < nseg - 1 ? count : 0;  // phase-1 items, then the same chunks again
   const int nitems = n1 + count;
   auto chunk_of = [&](int it) { return first + (it < n1 ? it : it - n1); };
   auto issue = [&](int it) {  // lane 0: item it into its stage
@@ -364,17 +408,19 @@ __global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_fwd_kernel(const __grid
       ++issued;
     }
   };
+  auto fail = [&](int it) {
+    if (lane == 0) record_error(a.eh, kDevErrTimeout, L.epoch);
+    drain_stages<NS>(full, it, issued);
+  };
+  const size_t rec0 = (size_t)col.b * g.C + col.cc;  // + run * B * C
+  const size_t jstride = (size_t)g.B * g.C;
 
   // phase 1: this run's own summary (the state it carries from the empty one)
-  int failed = -1;
   State P = empty_state();
   int it = 0;
   for (; it < n1; ++it) {
     KV* dk;
-    if (!acquire(it, dk)) {
-      failed = it;
-      break;
-    }
+    if (!acquire(it, dk)) return fail(it);
     const int j = chunk_of(it);
     const int n = min(kChunk, g.T - j * kChunk);
     if (n == kChunk)
@@ -383,37 +429,22 @@ __global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_fwd_kernel(const __grid
       seq_fwd_chunk<KV, false>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, nullptr, 0, false);
     release(it);
   }
-  if (n1 > 0) {
-    summ[(warp * 3 + 0) * 32 + lane] = P.num;
-    summ[(warp * 3 + 1) * 32 + lane] = P.den;
-    summ[(warp * 3 + 2) * 32 + lane] = P.pp;
-  }
-  __syncthreads();
-  if (failed >= 0) {
-    if (lane == 0) seq_record_timeout(a.eh);
-    drain_stages<NS>(full, failed, issued);
-    return;
-  }
+  if (n1 > 0 && col.valid) rec_store(a.recs + (size_t)run * jstride + rec0, L.tag, P.num, P.den, P.pp);
+
   // the carry into this run: the runs before it, in order
   P = empty_state();
-  for (int q = 0; q < warp; ++q) {
-    int fq, cq;
-    segment_of(g.nchunks, nseg, q, fq, cq);
-    if (cq == 0) continue;
-    const State Sq{summ[(q * 3 + 0) * 32 + lane], summ[(q * 3 + 1) * 32 + lane], summ[(q * 3 + 2) * 32 + lane]};
-    P = combine(P, (float)(cq * kChunk) * w, Sq);
+  for (int r = 0; r < run; ++r) {
+    int fr, cr;
+    segment_of(g.nchunks, nseg, r, fr, cr);
+    Rec rec;
+    if (!wait_rec(a.recs + (size_t)r * jstride + rec0, col.valid, L, a.eh, a.budget_ns, rec)) return fail(it - 1);
+    P = combine(P, (float)(cr * kChunk) * w, State{rec_x(rec), rec_y(rec), rec_z(rec)});
   }
 
   // phase 2: outputs and checkpoints
-  const size_t o0 = (size_t)col.b * g.C + col.cc;
-  const size_t jstride = (size_t)g.B * g.C;
   for (; it < nitems; ++it) {
     KV* dk;
-    if (!acquire(it, dk)) {
-      if (lane == 0) seq_record_timeout(a.eh);
-      drain_stages<NS>(full, it, issued);
-      return;
-    }
+    if (!acquire(it, dk)) return fail(it);
     const int j = chunk_of(it);
     const int n = min(kChunk, g.T - j * kChunk);
     float* yp = WRITE_Y ? a.y + ((int64_t)col.b * g.T + (int64_t)j * kChunk) * g.C + col.c : nullptr;
@@ -422,13 +453,21 @@ __global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_fwd_kernel(const __grid
     else
       seq_fwd_chunk<KV, WRITE_Y>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, yp, g.C, col.valid);
     if (col.valid) {
-      const size_t o = (size_t)j * jstride + o0;
+      const size_t o = (size_t)j * jstride + rec0;
       a.ckpt[o] = P.num;
       a.ckpt[o + g.plane] = P.den;
       a.ckpt[o + 2 * g.plane] = P.pp;
     }
     release(it);
   }
+}
+
+template <typename KV, int NS, bool WRITE_Y>
+__global__ void __launch_bounds__(kSeqChannels) seq_fwd_kernel(const __grid_constant__ SeqFwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Launch L = seq_launch(a.eh);
+  seq_fwd_run<KV, NS, WRITE_Y>(a, L, smem);
+  seq_exit(a.exited, a.eh, L.epoch);
 }
 
 // ----------------------------------------------------------------- backward
@@ -673,18 +712,14 @@ __device__ __forceinline__ Adj seq_bwd_summary(const float* __restrict__ sk, con
 }
 
 template <int NS>
-__global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_bwd_kernel(const __grid_constant__ SeqBwdArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int nseg = blockDim.x >> 5;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  constexpr size_t kRing = seq_ring_elems<float, NS>(3);  // stage s: k, v, gy at (3s + 0..2) * kSeqTile
-  float* ring = reinterpret_cast<float*>(smem) + (size_t)warp * kRing;
-  unsigned char* ctl = smem + (size_t)nseg * kRing * sizeof(float);
-  uint64_t* full = reinterpret_cast<uint64_t*>(ctl) + warp * NS;
-  float* summ = reinterpret_cast<float*>(ctl + ((size_t)nseg * NS * 8 + 127) / 128 * 128);  // [nseg][3][32]
+__device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L, unsigned char* smem) {
+  float* ring = reinterpret_cast<float*>(smem);  // stage s: k, v, gy at (3s + 0..2) * kSeqTile
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + seq_ring_elems<float, NS>(3) * sizeof(float));
+  const int lane = threadIdx.x;
   const ScanGeometry& g = a.g;
-  const Column col = column_of(g);
+  const int nseg = a.nseg;
+  const int q = blockIdx.x / nseg, run = blockIdx.x - q * nseg;
+  const Column col = column_of(g, q);
   BwdColumn cw;
   cw.w = __ldg(a.w + col.cc);
   cw.u = __ldg(a.u + col.cc);
@@ -695,13 +730,9 @@ __global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_bwd_kernel(const __grid
   constexpr uint32_t kStageBytes = 3 * kSeqTile * sizeof(float);
   const int last = g.nchunks - 1;
 
-  // The reduction of the gw, gu rows that follows this kernel tags its
-  // counters with the workspace's sequence number: advance it once per call.
-  if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(&a.eh->seq, 1ull);
-
   int first, count;  // in walk order: position p is chunk last - p
-  segment_of(g.nchunks, nseg, warp, first, count);
-  const int n1 = warp < nseg - 1 ? count : 0;
+  segment_of(g.nchunks, nseg, run, first, count);
+  const int n1 = run < nseg - 1 ? count : 0;
   const int nitems = n1 + count;
   auto chunk_of = [&](int it) { return last - (first + (it < n1 ? it : it - n1)); };
   auto issue = [&](int it) {  // lane 0: item it into its stage
@@ -747,6 +778,10 @@ __global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_bwd_kernel(const __grid
       ++issued;
     }
   };
+  auto fail = [&](int it) {
+    if (lane == 0) record_error(a.eh, kDevErrTimeout, L.epoch);
+    drain_stages<NS>(full, it, issued);
+  };
 
   float xa[kChunk], xb[kChunk], xp[kChunk];  // per-token form's states (local memory)
   const size_t o0 = (size_t)col.b * g.C + col.cc;
@@ -757,8 +792,7 @@ __global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_bwd_kernel(const __grid
     return State{__ldg(a.ckpt + o), __ldg(a.ckpt + o + g.plane), __ldg(a.ckpt + o + 2 * g.plane)};
   };
 
-  // phase 1: this run's zero-carry adjoint at its first token
-  int failed = -1;
+  // phase 1: this run's zero-carry adjoint at its first token (in time)
   State Pn = nitems > 0 ? load_state(chunk_of(0)) : empty_state();
   Adj X{0.f, 0.f, 0.f};
   int it = 0;
@@ -766,10 +800,7 @@ __global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_bwd_kernel(const __grid
     const State P = Pn;
     if (it + 1 < nitems) Pn = load_state(chunk_of(it + 1));  // one chunk ahead
     float* dk;
-    if (!acquire(it, dk)) {
-      failed = it;
-      break;
-    }
+    if (!acquire(it, dk)) return fail(it);
     const int j = chunk_of(it);
     const int n = min(kChunk, g.T - j * kChunk);
     const Adj A = n == kChunk
@@ -780,28 +811,18 @@ __global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_bwd_kernel(const __grid
     X = it == 0 ? A : fold_adj(A, (float)n * cw.w, X);
     release(it);
   }
-  if (n1 > 0) {
-    summ[(warp * 3 + 0) * 32 + lane] = X.la;
-    summ[(warp * 3 + 1) * 32 + lane] = X.lb;
-    summ[(warp * 3 + 2) * 32 + lane] = X.f;
-  }
-  __syncthreads();
-  if (failed >= 0) {
-    if (lane == 0) seq_record_timeout(a.eh);
-    drain_stages<NS>(full, failed, issued);
-    return;
-  }
-  // the carry into this run's end: the runs after it in time, nearest last
-  // (none for the run holding the last chunk)
-  bool has_x = false;
+  if (n1 > 0 && col.valid) rec_store(a.recs + (size_t)run * jstride + o0, L.tag, X.la, X.lb, X.f);
+
+  // the carry into this run's end (in time): the runs after it, nearest
+  // last (none for the run holding the last chunk)
   X = Adj{0.f, 0.f, 0.f};
-  for (int q = 0; q < warp; ++q) {
-    int fq, cq;
-    segment_of(g.nchunks, nseg, q, fq, cq);
-    if (cq == 0) continue;
-    const Adj Aq{summ[(q * 3 + 0) * 32 + lane], summ[(q * 3 + 1) * 32 + lane], summ[(q * 3 + 2) * 32 + lane]};
-    X = has_x ? fold_adj(Aq, (float)(cq * kChunk) * cw.w, X) : Aq;
-    has_x = true;
+  for (int r = 0; r < run; ++r) {
+    int fr, cr;
+    segment_of(g.nchunks, nseg, r, fr, cr);
+    Rec rec;
+    if (!wait_rec(a.recs + (size_t)r * jstride + o0, col.valid, L, a.eh, a.budget_ns, rec)) return fail(it - 1);
+    const Adj Ar{rec_x(rec), rec_y(rec), rec_z(rec)};
+    X = r == 0 ? Ar : fold_adj(Ar, (float)(cr * kChunk) * cw.w, X);
   }
 
   // phase 2: gk, gv, and this run's gw, gu
@@ -809,11 +830,7 @@ __global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_bwd_kernel(const __grid
     const State P = Pn;
     if (it + 1 < nitems) Pn = load_state(chunk_of(it + 1));
     float* dk;
-    if (!acquire(it, dk)) {
-      if (lane == 0) seq_record_timeout(a.eh);
-      drain_stages<NS>(full, it, issued);
-      return;
-    }
+    if (!acquire(it, dk)) return fail(it);
     const int j = chunk_of(it);
     const int n = min(kChunk, g.T - j * kChunk);
     const int64_t row = ((int64_t)col.b * g.T + (int64_t)j * kChunk) * g.C + col.c;
@@ -828,12 +845,22 @@ __global__ void __launch_bounds__(kSeqMaxWarps * 32) seq_bwd_kernel(const __grid
     kahan_add(cw.gu_s, cw.gu_k, gu_acc);
     release(it);
   }
-  // one gw, gu row per (warp, batch row): row warp * B + b of [2][nseg * B][C]
+  // one gw, gu row per (run, batch row): row run * B + b of [2][nseg * B][C]
   if (col.valid) {
-    const size_t o = (size_t)warp * jstride + o0;
+    const size_t o = (size_t)run * jstride + o0;
     a.part[o] = cw.gw_s;
     a.part[(size_t)nseg * jstride + o] = cw.gu_s;
   }
+}
+
+template <int NS>
+__global__ void __launch_bounds__(kSeqChannels) seq_bwd_kernel(const __grid_constant__ SeqBwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Launch L = seq_launch(a.eh);
+  seq_bwd_run<NS>(a, L, smem);
+  // the last CTA advances the sequence number, which also tags the counters
+  // of the gw, gu reduction that follows
+  seq_exit(a.exited, a.eh, L.epoch);
 }
 
 // ------------------------------------------------------------------ launch
@@ -867,93 +894,132 @@ cudaError_t dev_info(DevInfo& d) {
   return cudaSuccess;
 }
 
-// The opt-in to the kernel's shared memory is made once per device and size
-// (the first call, before any stream capture, as for the other kernels),
-// then every call only launches.
+// Per device and kernel: the opt-in to the kernel's shared memory and its
+// resident CTAs per SM at that size (one warp each), queried once (the first
+// call on a device, before any stream capture, as for the other kernels).
 template <class Args, void (*K)(Args)>
-cudaError_t launch_seq(unsigned int cols, int nseg, size_t smem, cudaStream_t s, const Args& a) {
-  static size_t configured[64] = {};
+cudaError_t resident_per_sm(size_t smem, int& per_sm) {
+  static int cache[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || configured[dev] < smem) {
-    e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = smem;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+    per_sm = cache[dev];
+    return cudaSuccess;
   }
-  K<<<dim3(cols), dim3(32 * nseg), smem, s>>>(a);
-  return cudaGetLastError();
+  e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, K, kSeqChannels, smem);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cache[dev] = per_sm;
+  return cudaSuccess;
 }
 
-// Stage counts compiled: 8, 4, 3, 2.  The launcher takes the largest that
-// lets every column's CTA be resident at once (the shared memory of an SM
-// divided by the columns it has to hold), so that no column waits for a
-// second wave; `run(std::integral_constant<int, NS>, smem)` launches.
-template <typename E, class Run>
-cudaError_t launch_staged(const DevInfo& d, unsigned int cols, int nseg, int arrays, bool tma, Run run) {
-  const unsigned int per_sm = (cols + d.sms - 1) / d.sms;
-  const size_t budget = d.smem_per_sm / (per_sm > 0 ? per_sm : 1);
-  auto fits = [&](size_t bytes) { return tma && bytes + 1024 <= budget; };  // 1 KB: the per-CTA reservation
-  if (fits(seq_smem_bytes<E, 8>(nseg, arrays)))
-    return run(std::integral_constant<int, 8>{}, seq_smem_bytes<E, 8>(nseg, arrays));
-  if (fits(seq_smem_bytes<E, 4>(nseg, arrays)))
-    return run(std::integral_constant<int, 4>{}, seq_smem_bytes<E, 4>(nseg, arrays));
-  if (fits(seq_smem_bytes<E, 3>(nseg, arrays)))
-    return run(std::integral_constant<int, 3>{}, seq_smem_bytes<E, 3>(nseg, arrays));
-  return run(std::integral_constant<int, 2>{}, seq_smem_bytes<E, 2>(nseg, arrays));
+template <class Args>
+cudaError_t launch_runs(void (*kern)(Args), unsigned int nblk, size_t smem, bool cooperative, cudaStream_t s,
+                        const Args& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nblk);
+  cfg.blockDim = dim3(kSeqChannels);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cooperative ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// Runs per column: about `warps` warps per SM in all (every run is
+// resident, so no more than the SMs hold at two stages per run), at most
+// kSeqMaxRuns and one per chunk; and 1 when the inputs that phase 2
+// re-reads would not fit in L2 (60% of it) while the columns alone fill
+// every SM.
+int choose_runs(const DevInfo& d, const ScanGeometry& g, int per_sm2, size_t input_bytes, int warps) {
+  const long long cols = (long long)g.B * g.nwg;
+  const long long cap = (long long)per_sm2 * d.sms;
+  // when phase 2 re-reads from DRAM anyway, more runs only add phase-1 work
+  if ((double)input_bytes > 0.6 * (double)d.l2 && warps > 8) warps = 8;
+  const long long target = cap < (long long)warps * d.sms ? cap : (long long)warps * d.sms;
+  long long nseg = target / cols;
+  if (nseg > kSeqMaxRuns) nseg = kSeqMaxRuns;
+  if (nseg > g.nchunks) nseg = g.nchunks;
+  if (nseg < 1) nseg = 1;
+  const double reread = (double)input_bytes * (double)(nseg - 1) / (double)nseg;
+  if (cols >= d.sms && reread > 0.6 * (double)d.l2) nseg = 1;
+  return (int)nseg;
+}
+
+// Launches `kern<NS>` for the largest NS of 8, 4, 3, 2 at which all the
+// launch's CTAs are resident at once (needed when runs wait on each other,
+// and it spares a second wave otherwise).
+template <class Args, template <int> class Kern>
+cudaError_t launch_planned(const DevInfo& d, Args& a, int arrays, size_t elem, size_t input_bytes, int warps,
+                           cudaStream_t s) {
+  const unsigned int cols = (unsigned int)a.g.B * a.g.nwg;
+  const size_t stage = (size_t)arrays * kSeqTile * elem;
+  int per_sm2 = 0;
+  cudaError_t e = resident_per_sm<Args, Kern<2>::fn>(2 * stage + 128, per_sm2);
+  if (e != cudaSuccess) return e;
+  a.nseg = choose_runs(d, a.g, per_sm2, input_bytes, warps);
+  const unsigned int nblk = cols * (unsigned int)a.nseg;
+  const unsigned int need = (nblk + d.sms - 1) / d.sms;
+  const bool coop = a.nseg > 1;
+  if (a.use_tma) {
+    int per_sm = 0;
+    e = resident_per_sm<Args, Kern<8>::fn>(8 * stage + 128, per_sm);
+    if (e != cudaSuccess) return e;
+    if ((unsigned)per_sm >= need) return launch_runs(Kern<8>::fn, nblk, 8 * stage + 128, coop, s, a);
+    e = resident_per_sm<Args, Kern<4>::fn>(4 * stage + 128, per_sm);
+    if (e != cudaSuccess) return e;
+    if ((unsigned)per_sm >= need) return launch_runs(Kern<4>::fn, nblk, 4 * stage + 128, coop, s, a);
+    e = resident_per_sm<Args, Kern<3>::fn>(3 * stage + 128, per_sm);
+    if (e != cudaSuccess) return e;
+    if ((unsigned)per_sm >= need) return launch_runs(Kern<3>::fn, nblk, 3 * stage + 128, coop, s, a);
+  }
+  return launch_runs(Kern<2>::fn, nblk, 2 * stage + 128, coop, s, a);
 }
 
 template <typename KV, bool WRITE_Y>
-cudaError_t launch_seq_fwd_t(const SeqFwdArgs& a, cudaStream_t s) {
+struct FwdKern {
+  template <int NS>
+  struct At {
+    static constexpr void (*fn)(SeqFwdArgs) = seq_fwd_kernel<KV, NS, WRITE_Y>;
+  };
+};
+
+template <int NS>
+struct BwdKern {
+  static constexpr void (*fn)(SeqBwdArgs) = seq_bwd_kernel<NS>;
+};
+
+template <typename KV, bool WRITE_Y>
+cudaError_t launch_seq_fwd_t(SeqFwdArgs& a, cudaStream_t s) {
   DevInfo d;
   cudaError_t e = dev_info(d);
   if (e != cudaSuccess) return e;
-  const unsigned int cols = (unsigned int)a.g.B * a.g.nwg;
-  return launch_staged<KV>(d, cols, a.nseg, 2, a.use_tma != 0, [&](auto ns, size_t smem) {
-    return launch_seq<SeqFwdArgs, seq_fwd_kernel<KV, decltype(ns)::value, WRITE_Y>>(cols, a.nseg, smem, s, a);
-  });
+  const size_t input_bytes = (size_t)a.g.B * a.g.T * a.g.C * 2 * sizeof(KV);
+  // the forward kernel's registers allow more warps than its two stages of
+  // shared memory: aim at 12 per SM
+  return launch_planned<SeqFwdArgs, FwdKern<KV, WRITE_Y>::template At>(d, a, 2, sizeof(KV), input_bytes, 12, s);
 }
 
 }  // namespace
 
-cudaError_t launch_seq_forward(const SeqFwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s) {
+cudaError_t launch_seq_forward(SeqFwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s) {
   if (kv_dtype == 0)
     return write_y ? launch_seq_fwd_t<float, true>(a, s) : launch_seq_fwd_t<float, false>(a, s);
   return write_y ? launch_seq_fwd_t<__nv_bfloat16, true>(a, s) : launch_seq_fwd_t<__nv_bfloat16, false>(a, s);
 }
 
-cudaError_t launch_seq_backward(const SeqBwdArgs& a, cudaStream_t s) {
+cudaError_t launch_seq_backward(SeqBwdArgs& a, cudaStream_t s) {
   DevInfo d;
   cudaError_t e = dev_info(d);
   if (e != cudaSuccess) return e;
-  const unsigned int cols = (unsigned int)a.g.B * a.g.nwg;
-  return launch_staged<float>(d, cols, a.nseg, 3, a.use_tma != 0, [&](auto ns, size_t smem) {
-    return launch_seq<SeqBwdArgs, seq_bwd_kernel<decltype(ns)::value>>(cols, a.nseg, smem, s, a);
-  });
-}
-
-int seq_segments(int B, int T, int C, int arrays, int elem_bytes, bool backward) {
-  DevInfo d;
-  if (dev_info(d) != cudaSuccess || d.sms <= 0) return 1;
-  const ScanGeometry g = make_geometry(B, T, C);
-  const long long cols = (long long)g.B * g.nwg;
-  const long long per_sm = (cols + d.sms - 1) / d.sms;
-  // warps an SM can hold: two stages each in shared memory; the backward
-  // kernel's registers (up to 255 per thread) allow 8 warps per SM
-  const size_t stage = (size_t)arrays * kSeqTile * elem_bytes;
-  long long warps = (long long)(d.smem_per_sm / (2 * stage + 512));
-  if (backward && warps > 8) warps = 8;
-  long long nseg = warps / (per_sm > 0 ? per_sm : 1);
-  const long long want = (8LL * d.sms + cols - 1) / cols;  // about 8 warps per SM
-  if (nseg > want) nseg = want;
-  if (nseg > kSeqMaxWarps) nseg = kSeqMaxWarps;
-  // Phase 2 re-reads what the runs but the last summarised in phase 1: only
-  // worth it while that still sits in L2 (60% of it here), unless the
-  // columns alone leave SMs idle.
-  const double reread = (double)B * T * C * arrays * elem_bytes * (double)(nseg - 1) / (double)nseg;
-  if (cols >= d.sms && reread > 0.6 * (double)d.l2) nseg = 1;
-  if (nseg > g.nchunks) nseg = g.nchunks;
-  return nseg < 1 ? 1 : (int)nseg;
+  const size_t input_bytes = (size_t)a.g.B * a.g.T * a.g.C * 3 * sizeof(float);
+  // the backward kernel's registers (up to 255 per thread) allow 8 warps per SM
+  return launch_planned<SeqBwdArgs, BwdKern>(d, a, 3, sizeof(float), input_bytes, 8, s);
 }
 
 }  // namespace wkv

@@ -178,3 +178,21 @@ def test_graph_replay_with_new_inputs(wkv, scan_mode):
             assert torch.equal(x, r_), n
     wkv.workspace_check(wsf)
     wkv.workspace_check(wsb)
+
+
+def test_scan_strategy_by_shape(wkv):
+    """The automatic choice: sequential when the columns (B x ceil(C/32))
+    reach the SM count, chunked otherwise; the test hook overrides it."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert wkv.scan_strategy(8, 1024, 768) == ("sequential" if 8 * 24 >= sms else "chunked")
+    assert wkv.scan_strategy(1, 131072, 2560) == ("sequential" if 80 >= sms else "chunked")
+    assert wkv.scan_strategy(1, 64, 64) == "chunked"
+    try:
+        wkv.set_scan_mode("sequential")
+        assert wkv.scan_strategy(1, 64, 64) == "sequential"
+        wkv.set_scan_mode("chunked")
+        assert wkv.scan_strategy(16, 4096, 2048) == "chunked"
+    finally:
+        wkv.set_scan_mode("auto")
+    with pytest.raises(wkv.WKVError):
+        wkv.scan_strategy(0, 1, 1)
