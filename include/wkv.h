@@ -197,9 +197,12 @@ wkv_status wkv_forward_noalloc(int B, int T, int C, int kv_dtype, const float* w
  * Test hooks (process-wide; not for production use).
  * wkv_debug_set_wait_budget_ns: limit of each bounded device-side wait of
  *   the scans, in ns of %globaltimer; <= 0 restores the default (500 ms).
- * wkv_debug_set_skip_chunk: tiles of time chunk `chunk` skip publishing
- *   their results, so the waits of later tiles expire and the call reports
- *   WKV_ERR_TIMEOUT through wkv_workspace_check; -1 turns this off.
+ * wkv_debug_set_skip_chunk: the results that carry time chunk `chunk` to
+ *   other CTAs are never published (the chunked scan: that chunk's tiles;
+ *   the sequential kernels: the summary of the run holding the chunk, when
+ *   its column has several runs), so the waits of the CTAs that need them
+ *   expire and the call reports WKV_ERR_TIMEOUT through
+ *   wkv_workspace_check; -1 turns this off.
  */
 wkv_status wkv_debug_set_wait_budget_ns(long long ns);
 wkv_status wkv_debug_set_skip_chunk(int chunk);
@@ -207,18 +210,28 @@ wkv_status wkv_debug_set_skip_chunk(int chunk);
 /*
  * wkv_debug_set_scan_mode: which kernels wkv_forward and wkv_backward run
  * (process-wide; for tests and measurements).
- *   WKV_SCAN_AUTO (default): sequential when the shape has at least as many
- *     columns (B x ceil(C / 32)) as the GPU has SMs, else chunked.
- *   WKV_SCAN_CHUNKED: time cut into chunks spread over all CTAs, chunk
- *     results carried between CTAs (every shape).
- *   WKV_SCAN_SEQUENTIAL: one warp per column walking its chunks in order,
- *     nothing exchanged between CTAs (every shape; slow when columns are few).
+ *   WKV_SCAN_AUTO (default): the sequential kernels, measured faster on
+ *     every shape tried (from B=1 T=64 C=64 to B=1 T=131072 C=2560).
+ *   WKV_SCAN_CHUNKED: time cut into 32-token chunks spread over all CTAs of
+ *     a persistent launch; chunk results carried between CTAs.
+ *   WKV_SCAN_SEQUENTIAL: a column (batch row, 32 channels) walks its chunks
+ *     in order, split into a few runs (one warp each) that exchange one
+ *     summary each.
  * Both strategies compute the same recurrence with the same per-chunk
- * arithmetic; outputs agree to rounding (bitwise on lanes whose chunks all
- * stay on the fixed-scale form).  wkv_debug_set_skip_chunk affects the
- * chunked kernels only.  Errors: WKV_ERR_INVALID_ARG for another value.
+ * arithmetic; outputs agree to rounding (bitwise, with one run per column,
+ * on lanes whose chunks all stay on the fixed-scale form).
+ * Errors: WKV_ERR_INVALID_ARG for another value.
  */
 wkv_status wkv_debug_set_scan_mode(int mode);
+
+/*
+ * wkv_debug_set_max_runs: upper bound on the runs a column's walk is split
+ * into by the sequential kernels (process-wide; for tests and
+ * measurements); <= 0 removes the bound (the default: the library's
+ * choice by shape and device).  With one run per column nothing is
+ * exchanged between CTAs.
+ */
+wkv_status wkv_debug_set_max_runs(int runs);
 
 /*
  * wkv_scan_strategy: the strategy wkv_forward and wkv_backward take for a

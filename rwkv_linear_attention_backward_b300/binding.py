@@ -46,6 +46,7 @@ _SIGNATURES = {
     "wkv_debug_set_skip_chunk": ([_i], _i),
     "wkv_debug_set_scan_mode": ([_i], _i),
     "wkv_scan_strategy": ([_i, _i, _i], _i),
+    "wkv_debug_set_max_runs": ([_i], _i),
 }
 for _name, (_args, _res) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -268,6 +269,12 @@ def scan_strategy(B: int, T: int, C: int) -> str:
     if r < 0:
         raise WKVError(1, "wkv_scan_strategy")  # WKV_ERR_INVALID_ARG
     return {1: "chunked", 2: "sequential"}[r]
+
+
+def set_max_runs(runs: int) -> None:
+    """Upper bound on the runs per column of the sequential kernels (0: the
+    library's choice); process-wide, for tests and measurements."""
+    _check(_lib.wkv_debug_set_max_runs(int(runs)), "wkv_debug_set_max_runs")
 
 
 def set_scan_mode(mode: str) -> None:

@@ -20,6 +20,7 @@ constexpr long long kDefaultBudgetNs = 500LL * 1000 * 1000;
 std::atomic<long long> g_budget_ns{kDefaultBudgetNs};
 std::atomic<int> g_skip_chunk{-1};
 std::atomic<int> g_scan_mode{WKV_SCAN_AUTO};
+std::atomic<int> g_max_runs{0};
 thread_local char g_last_error[256] = "";
 
 void clear_error() { g_last_error[0] = '\0'; }
@@ -94,25 +95,17 @@ BwdLayout bwd_layout(const ScanGeometry& g) {
 
 char* bytes(void* p) { return static_cast<char*>(p); }
 
-// Whether a shape takes the sequential column kernels (wkv_seq.cu): when its
-// columns (batch rows x 32-channel groups) fill every SM at least once, the
-// columns alone keep the GPU busy and a column's chunks need no exchange
-// between CTAs; fewer columns leave SMs idle, and the chunked scans split
-// time across CTAs instead.
+// Whether a call takes the sequential column kernels (wkv_seq.cu) or the
+// chunked scan (wkv_fwd.cu, wkv_bwd.cu).  Automatic: sequential for every
+// shape.  Measured on B300 (forward + backward per call, fp32; forward only,
+// bf16, for the last two): B=1 T=64 C=64 0.060 vs 0.061 ms; 1x1024x768 0.068
+// vs 0.074; 2x4096x512 0.080 vs 0.137; 1x65536x32 0.317 vs 1.288;
+// 4x2048x1024 0.099 vs 0.125; 8x1024x768 0.088 vs 0.102; 1x16384x2048 0.339
+// vs 0.451; 1x131072x2560 0.970 vs 1.623; 1x32768x4096 0.345 vs 0.456.  The
+// chunked scan stays selectable (wkv_debug_set_scan_mode) and tested.
 cudaError_t sequential_mode(const ScanGeometry& g, bool& seq) {
-  static int sms_per_dev[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  int sms = (dev >= 0 && dev < 64) ? sms_per_dev[dev] : 0;
-  if (sms == 0) {
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) sms_per_dev[dev] = sms;
-  }
-  const long long cols = (long long)g.B * g.nwg;
-  const int mode = g_scan_mode.load();
-  seq = mode == WKV_SCAN_AUTO ? cols >= sms : mode == WKV_SCAN_SEQUENTIAL;
+  (void)g;
+  seq = g_scan_mode.load() != WKV_SCAN_CHUNKED;
   return cudaSuccess;
 }
 
@@ -194,6 +187,8 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const 
     f.ckpt = reinterpret_cast<float*>(bytes(workspace) + l.fwd + fwd_layout(g).ckpt);
     f.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.fwd + fwd_layout(g).agg);
     f.exited = &hdr->exited[1];
+    f.nseg = g_max_runs.load();
+    f.debug_skip_chunk = -1;
     f.eh = hdr;
     f.g = g;
     f.budget_ns = budget;
@@ -215,6 +210,8 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const 
   a.part = reinterpret_cast<float*>(bytes(workspace) + l.part);  // [2][nseg * B][C]
   a.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.ragg);
   a.exited = &hdr->exited[2];
+  a.nseg = g_max_runs.load();
+  a.debug_skip_chunk = g_skip_chunk.load();
   a.eh = hdr;
   a.g = g;
   a.budget_ns = budget;
@@ -327,6 +324,8 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
     q.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.agg);
     q.eh = static_cast<WsHeader*>(workspace);
     q.exited = &q.eh->exited[0];
+    q.nseg = g_max_runs.load();  // 0: the launcher's choice
+    q.debug_skip_chunk = g_skip_chunk.load();
     q.g = g;
     q.budget_ns = (uint64_t)g_budget_ns.load();
     q.use_tma = make_tile_map(&q.tk, k, B, T, C, eb, kSeqChannels) && make_tile_map(&q.tv, v, B, T, C, eb, kSeqChannels);
@@ -471,6 +470,11 @@ int wkv_scan_strategy(int B, int T, int C) {
   bool seq = false;
   if (sequential_mode(make_geometry(B, T, C), seq) != cudaSuccess) return -1;
   return seq ? WKV_SCAN_SEQUENTIAL : WKV_SCAN_CHUNKED;
+}
+
+wkv_status wkv_debug_set_max_runs(int runs) {
+  g_max_runs.store(runs > 0 ? runs : 0);
+  return WKV_OK;
 }
 
 wkv_status wkv_debug_set_scan_mode(int mode) {

@@ -126,7 +126,8 @@ struct SeqFwdArgs {
   WsHeader* eh;
   ScanGeometry g;
   uint64_t budget_ns;
-  int nseg;               // runs per column: set by launch_seq_forward
+  int nseg;               // runs per column: in, an upper bound (0: none); out, the runs launched
+  int debug_skip_chunk;   // -1: off; else the run holding this chunk never publishes its summary
   int use_tma;
 };
 
@@ -146,7 +147,8 @@ struct SeqBwdArgs {
   WsHeader* eh;
   ScanGeometry g;
   uint64_t budget_ns;
-  int nseg;               // runs per column: set by launch_seq_backward
+  int nseg;               // as for the forward pass
+  int debug_skip_chunk;
   int use_tma;
 };
 

@@ -429,7 +429,8 @@ __device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L
       seq_fwd_chunk<KV, false>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, nullptr, 0, false);
     release(it);
   }
-  if (n1 > 0 && col.valid) rec_store(a.recs + (size_t)run * jstride + rec0, L.tag, P.num, P.den, P.pp);
+  const bool skip = a.debug_skip_chunk >= first && a.debug_skip_chunk < first + count;  // fault injection
+  if (n1 > 0 && col.valid && !skip) rec_store(a.recs + (size_t)run * jstride + rec0, L.tag, P.num, P.den, P.pp);
 
   // the carry into this run: the runs before it, in order
   P = empty_state();
@@ -811,7 +812,10 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
     X = it == 0 ? A : fold_adj(A, (float)n * cw.w, X);
     release(it);
   }
-  if (n1 > 0 && col.valid) rec_store(a.recs + (size_t)run * jstride + o0, L.tag, X.la, X.lb, X.f);
+  // fault injection: the run holding this chunk never publishes
+  const bool skip = a.debug_skip_chunk >= 0 && last - a.debug_skip_chunk >= first &&
+                    last - a.debug_skip_chunk < first + count;
+  if (n1 > 0 && col.valid && !skip) rec_store(a.recs + (size_t)run * jstride + o0, L.tag, X.la, X.lb, X.f);
 
   // the carry into this run's end (in time): the runs after it, nearest
   // last (none for the run holding the last chunk)
@@ -962,7 +966,9 @@ cudaError_t launch_planned(const DevInfo& d, Args& a, int arrays, size_t elem, s
   int per_sm2 = 0;
   cudaError_t e = resident_per_sm<Args, Kern<2>::fn>(2 * stage + 128, per_sm2);
   if (e != cudaSuccess) return e;
+  const int cap_runs = a.nseg;
   a.nseg = choose_runs(d, a.g, per_sm2, input_bytes, warps);
+  if (cap_runs > 0 && a.nseg > cap_runs) a.nseg = cap_runs;
   const unsigned int nblk = cols * (unsigned int)a.nseg;
   const unsigned int need = (nblk + d.sms - 1) / d.sms;
   const bool coop = a.nseg > 1;

@@ -111,16 +111,20 @@ def test_side_stream(oracle, wkv, scan_mode):
     assert_close(gv, oracle.backward_adjoint(w, u, k, v, gy)[3], TOL_GRAD, "gv")
 
 
+@pytest.mark.parametrize("mode", ["chunked", "sequential"])
 @pytest.mark.parametrize("which", ["forward", "backward"])
-def test_expired_wait_is_reported(oracle, wkv, which):
-    """A chunk whose tiles never publish makes the later tiles' bounded waits
-    expire: the call reports WKV_ERR_TIMEOUT through wkv_workspace_check and
-    the device stays usable."""
+def test_expired_wait_is_reported(oracle, wkv, which, mode):
+    """A chunk whose results are never published (the chunked scan: its
+    tiles; the sequential kernels: the summary of the run holding it) makes
+    the bounded waits of the CTAs that need them expire: the call reports
+    WKV_ERR_TIMEOUT through wkv_workspace_check and the device stays
+    usable."""
     B, T, C = 1, 32 * 40, 64
     w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=27)
     tw = cuda(w, u, k, v, gy)
     ws = wkv.Workspace(wkv.backward_workspace_bytes(B, T, C))
     try:
+        wkv.set_scan_mode(mode)
         wkv.set_wait_budget_ns(2_000_000)  # 2 ms
         wkv.set_skip_chunk(0 if which == "forward" else T // 32 - 1)
         if which == "forward":
@@ -135,9 +139,12 @@ def test_expired_wait_is_reported(oracle, wkv, which):
         wkv.set_skip_chunk(-1)
         wkv.set_wait_budget_ns(0)
     wkv.workspace_check(ws)  # the record was cleared
-    y = wkv.forward(*tw[:4], workspace=ws)
-    gw, gu, gk, gv = wkv.backward(*tw, workspace=ws)
-    wkv.workspace_check(ws)
+    try:
+        y = wkv.forward(*tw[:4], workspace=ws)
+        gw, gu, gk, gv = wkv.backward(*tw, workspace=ws)
+        wkv.workspace_check(ws)
+    finally:
+        wkv.set_scan_mode("auto")
     assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "y after timeout")
     assert_close(gk, oracle.backward_adjoint(w, u, k, v, gy)[2], TOL_GRAD, "gk after timeout")
 
@@ -181,17 +188,15 @@ def test_graph_replay_with_new_inputs(wkv, scan_mode):
 
 
 def test_scan_strategy_by_shape(wkv):
-    """The automatic choice: sequential when the columns (B x ceil(C/32))
-    reach the SM count, chunked otherwise; the test hook overrides it."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert wkv.scan_strategy(8, 1024, 768) == ("sequential" if 8 * 24 >= sms else "chunked")
-    assert wkv.scan_strategy(1, 131072, 2560) == ("sequential" if 80 >= sms else "chunked")
-    assert wkv.scan_strategy(1, 64, 64) == "chunked"
+    """The automatic choice is the sequential kernels for every shape; the
+    test hook overrides it."""
+    for shape in ((8, 1024, 768), (1, 131072, 2560), (1, 64, 64), (16, 4096, 2048)):
+        assert wkv.scan_strategy(*shape) == "sequential"
     try:
-        wkv.set_scan_mode("sequential")
-        assert wkv.scan_strategy(1, 64, 64) == "sequential"
         wkv.set_scan_mode("chunked")
-        assert wkv.scan_strategy(16, 4096, 2048) == "chunked"
+        assert wkv.scan_strategy(1, 64, 64) == "chunked"
+        wkv.set_scan_mode("sequential")
+        assert wkv.scan_strategy(16, 4096, 2048) == "sequential"
     finally:
         wkv.set_scan_mode("auto")
     with pytest.raises(wkv.WKVError):
