@@ -168,8 +168,8 @@ namespace {
 
 // The backward pass with the sequential column kernels: the checkpoints
 // (recomputed by a state-only forward walk when the caller has none), the
-// reverse walk writing gk, gv and one gw, gu row per batch row, then the
-// reduction of those B rows.
+// reverse walk writing gk, gv and one gw, gu row per (run, batch row), then
+// the reduction of those rows.
 wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const float* w, const float* u,
                                const void* k, const void* v, const float* gy, const float* ckpt, float* gw,
                                float* gu, float* gk, float* gv, WsHeader* hdr, void* workspace, uint64_t budget,
@@ -219,7 +219,7 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const 
               make_tile_map(&a.tg, gy, B, T, C, 4, kSeqChannels);
   cudaError_t e = launch_seq_backward(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
-  const int nseg = a.nseg;
+  const int rows = a.nseg * B;
   ReduceArgs r;
   r.part = a.part;
   r.slices = reinterpret_cast<float*>(bytes(workspace) + l.slices);
@@ -227,9 +227,9 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const 
   r.eh = hdr;
   r.gw = gw;
   r.gu = gu;
-  r.rows = nseg * B;
+  r.rows = rows;
   r.C = C;
-  r.nslice = reduce_slices(nseg * B, C);
+  r.nslice = reduce_slices(rows, C);
   e = launch_reduce(r, s);
   return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_backward: reduce");
 }

@@ -318,10 +318,12 @@ __device__ __forceinline__ Launch seq_launch(const WsHeader* h) {
 }
 
 // The last CTA out resets the exit counter and advances the sequence number.
+// Both matter only to later launches, which the end of this one orders
+// after every write of it, so no fence is needed (a fence here would wait
+// for the CTA's streaming stores to drain).
 __device__ __forceinline__ void seq_exit(unsigned int* exited, WsHeader* h, unsigned long long epoch) {
   __syncwarp();
   if (threadIdx.x == 0) {
-    __threadfence();
     if (atomicAdd(exited, 1u) == gridDim.x - 1) {
       atomicExch(exited, 0u);
       atomicExch(&h->seq, epoch);
@@ -400,8 +402,9 @@ __device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L
     return true;
   };
   auto release = [&](int it) {
-    // every lane's reads of the stage come before the copy that refills it
-    fence_proxy_async_smem();
+    // Every lane's reads of the stage come before the copy that refills it:
+    // their values have been used before this point, so the reads are
+    // complete; the stage is only read, so no proxy fence is needed.
     __syncwarp();
     if (tma && it + NS < nitems) {
       if (lane == 0) issue(it + NS);
@@ -769,10 +772,10 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
     __syncwarp();
     return true;
   };
-  auto release = [&](int it) {
-    // this warp may have written into the stage: order its accesses before
-    // the async-proxy copy that refills it
-    fence_proxy_async_smem();
+  auto release = [&](int it, bool wrote) {
+    // a stage this warp wrote into (ek over k, partial chunks): order those
+    // writes before the async-proxy copy that refills it
+    if (wrote) fence_proxy_async_smem();
     __syncwarp();
     if (tma && it + NS < nitems) {
       if (lane == 0) issue(it + NS);
@@ -810,7 +813,7 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
                       : seq_bwd_summary<false>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P,
                                                xa, xb, xp);
     X = it == 0 ? A : fold_adj(A, (float)n * cw.w, X);
-    release(it);
+    release(it, false);
   }
   // fault injection: the run holding this chunk never publishes
   const bool skip = a.debug_skip_chunk >= 0 && last - a.debug_skip_chunk >= first &&
@@ -847,9 +850,10 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
                            a.gk + row, a.gv + row, g.C, col.valid, gw_acc, gu_acc, xa, xb, xp);
     kahan_add(cw.gw_s, cw.gw_k, gw_acc);
     kahan_add(cw.gu_s, cw.gu_k, gu_acc);
-    release(it);
+    release(it, n != kChunk);
   }
   // one gw, gu row per (run, batch row): row run * B + b of [2][nseg * B][C]
+  // (added up in row order by the reduction kernel that follows)
   if (col.valid) {
     const size_t o = (size_t)run * jstride + o0;
     a.part[o] = cw.gw_s;
@@ -862,8 +866,6 @@ __global__ void __launch_bounds__(kSeqChannels) seq_bwd_kernel(const __grid_cons
   extern __shared__ __align__(128) unsigned char smem[];
   const Launch L = seq_launch(a.eh);
   seq_bwd_run<NS>(a, L, smem);
-  // the last CTA advances the sequence number, which also tags the counters
-  // of the gw, gu reduction that follows
   seq_exit(a.exited, a.eh, L.epoch);
 }
 
