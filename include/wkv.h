@@ -234,6 +234,16 @@ wkv_status wkv_debug_set_scan_mode(int mode);
 wkv_status wkv_debug_set_max_runs(int runs);
 
 /*
+ * wkv_debug_set_chain_len: > 0 makes the sequential forward pass walk each
+ * column as a chain of runs of that many chunks (each run summarised, then
+ * walked again from the state carried in from the run before it, taken
+ * from a tagged record); 0 restores the default, which chains runs only
+ * when a shape's inputs exceed the L2 cache while its columns leave SMs
+ * idle (a long sequence).  Process-wide; for tests and measurements.
+ */
+wkv_status wkv_debug_set_chain_len(int chunks);
+
+/*
  * wkv_scan_strategy: the strategy wkv_forward and wkv_backward take for a
  * [B, T, C] call on the current device under the current scan mode:
  * WKV_SCAN_CHUNKED or WKV_SCAN_SEQUENTIAL; -1 for invalid sizes or when the

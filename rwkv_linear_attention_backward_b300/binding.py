@@ -47,6 +47,7 @@ _SIGNATURES = {
     "wkv_debug_set_scan_mode": ([_i], _i),
     "wkv_scan_strategy": ([_i, _i, _i], _i),
     "wkv_debug_set_max_runs": ([_i], _i),
+    "wkv_debug_set_chain_len": ([_i], _i),
 }
 for _name, (_args, _res) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -275,6 +276,12 @@ def set_max_runs(runs: int) -> None:
     """Upper bound on the runs per column of the sequential kernels (0: the
     library's choice); process-wide, for tests and measurements."""
     _check(_lib.wkv_debug_set_max_runs(int(runs)), "wkv_debug_set_max_runs")
+
+
+def set_chain_len(chunks: int) -> None:
+    """> 0: the sequential forward walks chained runs of that many chunks;
+    0: the library's choice (process-wide, for tests and measurements)."""
+    _check(_lib.wkv_debug_set_chain_len(int(chunks)), "wkv_debug_set_chain_len")
 
 
 def set_scan_mode(mode: str) -> None:

@@ -21,6 +21,7 @@ std::atomic<long long> g_budget_ns{kDefaultBudgetNs};
 std::atomic<int> g_skip_chunk{-1};
 std::atomic<int> g_scan_mode{WKV_SCAN_AUTO};
 std::atomic<int> g_max_runs{0};
+std::atomic<int> g_chain_len{0};
 thread_local char g_last_error[256] = "";
 
 void clear_error() { g_last_error[0] = '\0'; }
@@ -188,6 +189,7 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const 
     f.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.fwd + fwd_layout(g).agg);
     f.exited = &hdr->exited[1];
     f.nseg = g_max_runs.load();
+    f.chain = g_chain_len.load();
     f.debug_skip_chunk = -1;
     f.eh = hdr;
     f.g = g;
@@ -325,6 +327,7 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
     q.eh = static_cast<WsHeader*>(workspace);
     q.exited = &q.eh->exited[0];
     q.nseg = g_max_runs.load();  // 0: the launcher's choice
+    q.chain = g_chain_len.load();
     q.debug_skip_chunk = g_skip_chunk.load();
     q.g = g;
     q.budget_ns = (uint64_t)g_budget_ns.load();
@@ -470,6 +473,11 @@ int wkv_scan_strategy(int B, int T, int C) {
   bool seq = false;
   if (sequential_mode(make_geometry(B, T, C), seq) != cudaSuccess) return -1;
   return seq ? WKV_SCAN_SEQUENTIAL : WKV_SCAN_CHUNKED;
+}
+
+wkv_status wkv_debug_set_chain_len(int chunks) {
+  g_chain_len.store(chunks > 0 ? chunks : 0);
+  return WKV_OK;
 }
 
 wkv_status wkv_debug_set_max_runs(int runs) {

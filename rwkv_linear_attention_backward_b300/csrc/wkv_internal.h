@@ -128,6 +128,7 @@ struct SeqFwdArgs {
   uint64_t budget_ns;
   int nseg;               // runs per column: in, an upper bound (0: none); out, the runs launched
   int debug_skip_chunk;   // -1: off; else the run holding this chunk never publishes its summary
+  int chain;              // 0: runs exchange summaries; > 0: chained runs of this many chunks (set by the launcher)
   int use_tma;
 };
 

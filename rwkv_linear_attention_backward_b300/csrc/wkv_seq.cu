@@ -466,11 +466,160 @@ __device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L
   }
 }
 
+// Chained runs, for columns whose inputs do not fit in L2 while the columns
+// alone leave SMs idle (a long sequence): a column's chunks are cut into R
+// short runs of `chain` chunks, and warp wi of the column's nseg warps walks
+// runs wi, wi + nseg, ... in order.  For each run the warp summarises it
+// (phase 1), waits for the state after the previous run (a tagged record
+// written by the warp that walked it), publishes the state after its own run
+// (that state combined with its summary: a fixed order of folds, so the
+// results are reproducible), and walks the run again from the carried state
+// (phase 2), a few microseconds after phase 1 read it, so from L2.  Only the
+// runs in flight sit in L2, whatever T is.  Run r waits only on run r - 1,
+// which its warp reaches before any later run of its own, and every warp is
+// resident (cooperative launch), so the waits always end.  The last run
+// publishes nothing and needs no phase 1.
 template <typename KV, int NS, bool WRITE_Y>
+__device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch& L, unsigned char* smem) {
+  KV* ring = reinterpret_cast<KV*>(smem);  // stage s: k at 2s*kSeqTile, v at (2s+1)*kSeqTile
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + seq_ring_elems<KV, NS>(2) * sizeof(KV));
+  const int lane = threadIdx.x;
+  const ScanGeometry& g = a.g;
+  const int W = a.nseg, len = a.chain;
+  const int q = blockIdx.x / W, wi = blockIdx.x - q * W;
+  const int R = (g.nchunks + len - 1) / len;
+  const Column col = column_of(g, q);
+  const float w = __ldg(a.w + col.cc), u = __ldg(a.u + col.cc);
+  const float ew = expf(-w), eu = expf(u);
+  const bool tma = a.use_tma != 0;
+  constexpr uint32_t kStageBytes = 2 * kSeqTile * sizeof(KV);
+  const size_t rec0 = (size_t)col.b * g.C + col.cc;  // + run * B * C
+  const size_t jstride = (size_t)g.B * g.C;
+
+  // The warp's item stream: per run, its chunks (phase 1) then the same
+  // chunks again (phase 2); the last run of the column has phase 2 only.
+  // Items per run: 2 len, except the last run (the warp's last).
+  const int last_len = g.nchunks - (R - 1) * len;
+  int nitems = 0;
+  for (int r = wi; r < R; r += W) nitems += r == R - 1 ? last_len : 2 * len;
+  struct Item {
+    int r, j;
+    bool p1, first, last;  // phase 1 item; first / last item of its phase
+  };
+  auto item = [&](int it) {
+    Item o;
+    const int m = it / (2 * len), off = it - m * 2 * len;
+    o.r = wi + m * W;
+    if (o.r == R - 1) {
+      o.p1 = false;
+      o.j = o.r * len + off;
+      o.first = off == 0;
+      o.last = off == last_len - 1;
+    } else {
+      o.p1 = off < len;
+      const int k = o.p1 ? off : off - len;
+      o.j = o.r * len + k;
+      o.first = k == 0;
+      o.last = k == len - 1;
+    }
+    return o;
+  };
+  auto issue = [&](int it) {  // lane 0: item it into its stage
+    const int s = it % NS;
+    const int j = item(it).j;
+    KV* dk = ring + (size_t)(2 * s) * kSeqTile;
+    mbar_arrive_expect_tx(&full[s], kStageBytes);
+    tma_load_3d(dk, &a.tk, &full[s], col.c0, j * kChunk, col.b);
+    tma_load_3d(dk + kSeqTile, &a.tv, &full[s], col.c0, j * kChunk, col.b);
+  };
+  int issued = 0;
+  if (tma) {
+    if (lane == 0) {
+      for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+      mbar_init_fence();
+      tma_prefetch_desc(&a.tk);
+      tma_prefetch_desc(&a.tv);
+      for (int it = 0; it < NS && it < nitems; ++it) issue(it);
+    }
+    issued = min(NS, nitems);
+    __syncwarp();
+  }
+  auto fail = [&](int it) {
+    if (lane == 0) record_error(a.eh, kDevErrTimeout, L.epoch);
+    drain_stages<NS>(full, it, issued);
+  };
+  // the state after run r - 1 (empty before run 0)
+  auto carry_in = [&](int r, State& P) {
+    if (r == 0) {
+      P = empty_state();
+      return true;
+    }
+    Rec rec;
+    if (!wait_rec(a.recs + (size_t)(r - 1) * jstride + rec0, col.valid, L, a.eh, a.budget_ns, rec)) return false;
+    P = State{rec_x(rec), rec_y(rec), rec_z(rec)};
+    return true;
+  };
+
+  State S = empty_state(), P = empty_state();
+  for (int it = 0; it < nitems; ++it) {
+    const Item m = item(it);
+    const int s = it % NS;
+    KV* dk = ring + (size_t)(2 * s) * kSeqTile;
+    if (tma) {
+      if (!stage_wait(&full[s], (uint32_t)((it / NS) & 1), a.budget_ns)) return fail(it);
+    } else {
+      copy_box_plain(dk, static_cast<const KV*>(a.k), g, col, m.j * kChunk);
+      copy_box_plain(dk + kSeqTile, static_cast<const KV*>(a.v), g, col, m.j * kChunk);
+      __syncwarp();
+    }
+    const int n = min(kChunk, g.T - m.j * kChunk);
+    if (m.p1) {
+      if (m.first) S = empty_state();
+      if (n == kChunk)
+        seq_fwd_full<KV, false>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, S, nullptr, 0, false);
+      else
+        seq_fwd_chunk<KV, false>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, S, nullptr, 0, false);
+    } else {
+      if (m.first && m.r == R - 1 && !carry_in(m.r, P)) return fail(it);
+      float* yp = WRITE_Y ? a.y + ((int64_t)col.b * g.T + (int64_t)m.j * kChunk) * g.C + col.c : nullptr;
+      if (n == kChunk)
+        seq_fwd_full<KV, WRITE_Y>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, P, yp, g.C, col.valid);
+      else
+        seq_fwd_chunk<KV, WRITE_Y>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, yp, g.C, col.valid);
+      if (col.valid) {
+        const size_t o = (size_t)m.j * jstride + rec0;
+        a.ckpt[o] = P.num;
+        a.ckpt[o + g.plane] = P.den;
+        a.ckpt[o + 2 * g.plane] = P.pp;
+      }
+    }
+    // release the stage (only read: see seq_fwd_run)
+    __syncwarp();
+    if (tma && it + NS < nitems) {
+      if (lane == 0) issue(it + NS);
+      ++issued;
+    }
+    if (m.p1 && m.last) {
+      // the state after the previous run, then the state after this one
+      if (!carry_in(m.r, P)) return fail(it);
+      const State I = combine(P, (float)(len * kChunk) * w, S);
+      const bool skip = a.debug_skip_chunk >= m.r * len && a.debug_skip_chunk < (m.r + 1) * len;
+      if (col.valid && !skip) rec_store(a.recs + (size_t)m.r * jstride + rec0, L.tag, I.num, I.den, I.pp);
+    }
+  }
+}
+
+// CHAIN: chained runs (seq_fwd_chain), else runs exchanging summaries
+// (seq_fwd_run); separate kernels, so that each holds only its own code
+// (both in one kernel overflowed the instruction cache).
+template <typename KV, int NS, bool WRITE_Y, bool CHAIN>
 __global__ void __launch_bounds__(kSeqChannels) seq_fwd_kernel(const __grid_constant__ SeqFwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Launch L = seq_launch(a.eh);
-  seq_fwd_run<KV, NS, WRITE_Y>(a, L, smem);
+  if constexpr (CHAIN)
+    seq_fwd_chain<KV, NS, WRITE_Y>(a, L, smem);
+  else
+    seq_fwd_run<KV, NS, WRITE_Y>(a, L, smem);
   seq_exit(a.exited, a.eh, L.epoch);
 }
 
@@ -942,11 +1091,11 @@ cudaError_t launch_runs(void (*kern)(Args), unsigned int nblk, size_t smem, bool
 // kSeqMaxRuns and one per chunk; and 1 when the inputs that phase 2
 // re-reads would not fit in L2 (60% of it) while the columns alone fill
 // every SM.
-int choose_runs(const DevInfo& d, const ScanGeometry& g, int per_sm2, size_t input_bytes, int warps) {
+int choose_runs(const DevInfo& d, const ScanGeometry& g, int per_sm2, size_t input_bytes, int warps, bool chained) {
   const long long cols = (long long)g.B * g.nwg;
   const long long cap = (long long)per_sm2 * d.sms;
   // when phase 2 re-reads from DRAM anyway, more runs only add phase-1 work
-  if ((double)input_bytes > 0.6 * (double)d.l2 && warps > 8) warps = 8;
+  if (!chained && (double)input_bytes > 0.6 * (double)d.l2 && warps > 8) warps = 8;
   const long long target = cap < (long long)warps * d.sms ? cap : (long long)warps * d.sms;
   long long nseg = target / cols;
   if (nseg > kSeqMaxRuns) nseg = kSeqMaxRuns;
@@ -957,43 +1106,87 @@ int choose_runs(const DevInfo& d, const ScanGeometry& g, int per_sm2, size_t inp
   return (int)nseg;
 }
 
-// Launches `kern<NS>` for the largest NS of 8, 4, 3, 2 at which all the
-// launch's CTAs are resident at once (needed when runs wait on each other,
-// and it spares a second wave otherwise).
-template <class Args, template <int> class Kern>
+// Launches `K<NS>::fn` for the largest NS of 8, 4, 3, 2 at which all `nblk`
+// CTAs are resident at once (needed when runs wait on each other, and it
+// spares a second wave otherwise).
+template <class Args, template <int> class K>
+cudaError_t launch_staged(const DevInfo& d, const Args& a, unsigned int nblk, size_t stage, bool coop,
+                          cudaStream_t s) {
+  const unsigned int need = (nblk + d.sms - 1) / d.sms;
+  if (a.use_tma) {
+    int per_sm = 0;
+    cudaError_t e = resident_per_sm<Args, K<8>::fn>(8 * stage + 128, per_sm);
+    if (e != cudaSuccess) return e;
+    if ((unsigned)per_sm >= need) return launch_runs(K<8>::fn, nblk, 8 * stage + 128, coop, s, a);
+    e = resident_per_sm<Args, K<4>::fn>(4 * stage + 128, per_sm);
+    if (e != cudaSuccess) return e;
+    if ((unsigned)per_sm >= need) return launch_runs(K<4>::fn, nblk, 4 * stage + 128, coop, s, a);
+    e = resident_per_sm<Args, K<3>::fn>(3 * stage + 128, per_sm);
+    if (e != cudaSuccess) return e;
+    if ((unsigned)per_sm >= need) return launch_runs(K<3>::fn, nblk, 3 * stage + 128, coop, s, a);
+  }
+  int per_sm2 = 0;
+  cudaError_t e = resident_per_sm<Args, K<2>::fn>(2 * stage + 128, per_sm2);
+  if (e != cudaSuccess) return e;
+  return launch_runs(K<2>::fn, nblk, 2 * stage + 128, coop, s, a);
+}
+
+// Plans the runs (a.nseg, and a.chain for the forward pass) and launches
+// Kern, or KernChain for chained runs.
+template <class Args, template <int> class Kern, template <int> class KernChain>
 cudaError_t launch_planned(const DevInfo& d, Args& a, int arrays, size_t elem, size_t input_bytes, int warps,
                            cudaStream_t s) {
   const unsigned int cols = (unsigned int)a.g.B * a.g.nwg;
   const size_t stage = (size_t)arrays * kSeqTile * elem;
-  int per_sm2 = 0;
-  cudaError_t e = resident_per_sm<Args, Kern<2>::fn>(2 * stage + 128, per_sm2);
-  if (e != cudaSuccess) return e;
   const int cap_runs = a.nseg;
-  a.nseg = choose_runs(d, a.g, per_sm2, input_bytes, warps);
-  if (cap_runs > 0 && a.nseg > cap_runs) a.nseg = cap_runs;
-  const unsigned int nblk = cols * (unsigned int)a.nseg;
-  const unsigned int need = (nblk + d.sms - 1) / d.sms;
-  const bool coop = a.nseg > 1;
-  if (a.use_tma) {
-    int per_sm = 0;
-    e = resident_per_sm<Args, Kern<8>::fn>(8 * stage + 128, per_sm);
-    if (e != cudaSuccess) return e;
-    if ((unsigned)per_sm >= need) return launch_runs(Kern<8>::fn, nblk, 8 * stage + 128, coop, s, a);
-    e = resident_per_sm<Args, Kern<4>::fn>(4 * stage + 128, per_sm);
-    if (e != cudaSuccess) return e;
-    if ((unsigned)per_sm >= need) return launch_runs(Kern<4>::fn, nblk, 4 * stage + 128, coop, s, a);
-    e = resident_per_sm<Args, Kern<3>::fn>(3 * stage + 128, per_sm);
-    if (e != cudaSuccess) return e;
-    if ((unsigned)per_sm >= need) return launch_runs(Kern<3>::fn, nblk, 3 * stage + 128, coop, s, a);
+  bool chained = false;
+  int forced = 0;
+  if constexpr (std::is_same<Args, SeqFwdArgs>::value) {
+    // Chained runs when phase 2 would re-read from DRAM (inputs beyond L2)
+    // while the columns alone leave SMs idle; a positive a.chain on entry
+    // forces chained runs of that length.
+    forced = a.chain;
+    chained = forced > 0 || ((long long)cols < d.sms && (double)input_bytes > 0.6 * (double)d.l2);
+    // chained runs re-read from L2, so they take more warps: 16 per SM
+    // (measured on the long-context forward: 0.73 ms at 16, 0.86 at 8, 0.9+ at 24)
+    if (chained && !forced) warps = 16;
   }
-  return launch_runs(Kern<2>::fn, nblk, 2 * stage + 128, coop, s, a);
+  // resident CTAs per SM of the kernel that will run, at two stages
+  int per_sm2 = 0;
+  cudaError_t e = chained ? resident_per_sm<Args, KernChain<2>::fn>(2 * stage + 128, per_sm2)
+                          : resident_per_sm<Args, Kern<2>::fn>(2 * stage + 128, per_sm2);
+  if (e != cudaSuccess) return e;
+  a.nseg = choose_runs(d, a.g, per_sm2, input_bytes, warps, chained);
+  if (cap_runs > 0 && a.nseg > cap_runs) a.nseg = cap_runs;
+  if constexpr (std::is_same<Args, SeqFwdArgs>::value) {
+    a.chain = 0;
+    if (chained) {
+      // runs of `len` chunks, the runs in flight (nseg per column) within 40%
+      // of L2 (longer runs fall out of L2 before phase 2; shorter ones make
+      // the chain of carried states the bound)
+      long long len = forced;
+      if (len <= 0) {
+        const double per_run_chunk = (double)cols * a.nseg * stage;  // one chunk of every run in flight
+        len = (long long)(0.4 * (double)d.l2 / per_run_chunk);
+        if (len < 4) len = 4;
+        if (len > 64) len = 64;
+      }
+      a.chain = (int)len;
+      const int R = (a.g.nchunks + a.chain - 1) / a.chain;
+      if (a.nseg > R) a.nseg = R;  // a warp per run at most
+    }
+  }
+  const unsigned int nblk = cols * (unsigned int)a.nseg;
+  const bool coop = a.nseg > 1;  // runs wait on each other
+  if (chained) return launch_staged<Args, KernChain>(d, a, nblk, stage, coop, s);
+  return launch_staged<Args, Kern>(d, a, nblk, stage, coop, s);
 }
 
-template <typename KV, bool WRITE_Y>
+template <typename KV, bool WRITE_Y, bool CHAIN>
 struct FwdKern {
   template <int NS>
   struct At {
-    static constexpr void (*fn)(SeqFwdArgs) = seq_fwd_kernel<KV, NS, WRITE_Y>;
+    static constexpr void (*fn)(SeqFwdArgs) = seq_fwd_kernel<KV, NS, WRITE_Y, CHAIN>;
   };
 };
 
@@ -1010,7 +1203,8 @@ cudaError_t launch_seq_fwd_t(SeqFwdArgs& a, cudaStream_t s) {
   const size_t input_bytes = (size_t)a.g.B * a.g.T * a.g.C * 2 * sizeof(KV);
   // the forward kernel's registers allow more warps than its two stages of
   // shared memory: aim at 12 per SM
-  return launch_planned<SeqFwdArgs, FwdKern<KV, WRITE_Y>::template At>(d, a, 2, sizeof(KV), input_bytes, 12, s);
+  return launch_planned<SeqFwdArgs, FwdKern<KV, WRITE_Y, false>::template At, FwdKern<KV, WRITE_Y, true>::template At>(
+      d, a, 2, sizeof(KV), input_bytes, 12, s);
 }
 
 }  // namespace
@@ -1027,7 +1221,7 @@ cudaError_t launch_seq_backward(SeqBwdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const size_t input_bytes = (size_t)a.g.B * a.g.T * a.g.C * 3 * sizeof(float);
   // the backward kernel's registers (up to 255 per thread) allow 8 warps per SM
-  return launch_planned<SeqBwdArgs, BwdKern>(d, a, 3, sizeof(float), input_bytes, 8, s);
+  return launch_planned<SeqBwdArgs, BwdKern, BwdKern>(d, a, 3, sizeof(float), input_bytes, 8, s);
 }
 
 }  // namespace wkv

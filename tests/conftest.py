@@ -14,19 +14,22 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (B300, sm_103a)")
 
 
-@pytest.fixture(params=["chunked", "sequential", "sequential-1run"])
+@pytest.fixture(params=["chunked", "sequential", "sequential-1run", "sequential-chain3"])
 def scan_mode(request):
     """Runs a GPU test once per scan strategy of wkv_forward / wkv_backward
     (forced through the library's test hooks; back to automatic after):
     the chunked scan, the sequential walk with its runs per column chosen by
-    the library, and the sequential walk with one run per column."""
+    the library, the sequential walk with one run per column, and the
+    sequential forward as chained runs of 3 chunks."""
     from rwkv_linear_attention_backward_b300 import binding
 
     binding.set_scan_mode(request.param.split("-")[0])
     binding.set_max_runs(1 if request.param.endswith("1run") else 0)
+    binding.set_chain_len(3 if request.param.endswith("chain3") else 0)
     yield request.param
     binding.set_scan_mode("auto")
     binding.set_max_runs(0)
+    binding.set_chain_len(0)
 
 
 @pytest.fixture(scope="session")

@@ -111,7 +111,7 @@ def test_side_stream(oracle, wkv, scan_mode):
     assert_close(gv, oracle.backward_adjoint(w, u, k, v, gy)[3], TOL_GRAD, "gv")
 
 
-@pytest.mark.parametrize("mode", ["chunked", "sequential"])
+@pytest.mark.parametrize("mode", ["chunked", "sequential", "sequential-chain3"])
 @pytest.mark.parametrize("which", ["forward", "backward"])
 def test_expired_wait_is_reported(oracle, wkv, which, mode):
     """A chunk whose results are never published (the chunked scan: its
@@ -124,7 +124,8 @@ def test_expired_wait_is_reported(oracle, wkv, which, mode):
     tw = cuda(w, u, k, v, gy)
     ws = wkv.Workspace(wkv.backward_workspace_bytes(B, T, C))
     try:
-        wkv.set_scan_mode(mode)
+        wkv.set_scan_mode(mode.split("-")[0])
+        wkv.set_chain_len(3 if mode.endswith("chain3") else 0)
         wkv.set_wait_budget_ns(2_000_000)  # 2 ms
         wkv.set_skip_chunk(0 if which == "forward" else T // 32 - 1)
         if which == "forward":
@@ -145,6 +146,7 @@ def test_expired_wait_is_reported(oracle, wkv, which, mode):
         wkv.workspace_check(ws)
     finally:
         wkv.set_scan_mode("auto")
+        wkv.set_chain_len(0)
     assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "y after timeout")
     assert_close(gk, oracle.backward_adjoint(w, u, k, v, gy)[2], TOL_GRAD, "gk after timeout")
 
