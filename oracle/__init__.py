@@ -46,6 +46,7 @@ class Oracle:
         sigs = {
             "wkv_oracle_forward_direct": [i, i, i, p, p, p, p, p],
             "wkv_oracle_forward_recurrent": [i, i, i, p, p, p, p, p],
+            "wkv_oracle_forward_state": [i, i, i] + [p] * 11,
             "wkv_oracle_backward_adjoint": [i, i, i, p, p, p, p, p, p, p, p, p],
             "wkv_oracle_backward_direct": [i, i, i, p, p, p, p, p, p, p, p, p],
             "wkv_oracle_state": [i, i, i, p, p, p, i, p, p, p],
@@ -92,6 +93,21 @@ class Oracle:
         y = np.empty_like(k)
         self._lib.wkv_oracle_forward_recurrent(B, T, C, *map(self._ptr, (w, u, k, v, y)))
         return y
+
+    def forward_state(self, w, u, k, v, state_in=None):
+        """wkv over k, v [B, T, C] continuing from ``state_in`` = (num, den,
+        pp), each [B, C] (None: the empty state).  Returns (y, (num, den, pp)),
+        the state after the T tokens."""
+        w, u, k, v = map(self._in, (w, u, k, v))
+        B, T, C = k.shape
+        y = np.empty_like(k)
+        if state_in is None:
+            sin = (None, None, None)
+        else:
+            sin = tuple(self._in(a).reshape(B, C).copy() for a in state_in)
+        out = tuple(np.empty((B, C)) for _ in range(3))
+        self._lib.wkv_oracle_forward_state(B, T, C, *map(self._ptr, (w, u, k, v) + sin + (y,) + out))
+        return y, out
 
     # ------------------------------------------------------------- backward
     def _backward(self, fn, w, u, k, v, gy):

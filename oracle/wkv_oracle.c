@@ -114,6 +114,56 @@ void wkv_oracle_forward_recurrent(int B, int T, int C, const double *w, const do
         }
 }
 
+/* Forward from a carried state: the same operator over T more tokens of a
+ * sequence whose earlier tokens are summarised by the state (num, den, pp)
+ * [B, C] in the convention of wkv_oracle_state (a = num e^{pp} and
+ * b = den e^{pp} are the sums a_0, b_0 over the earlier tokens; pp = -1e38
+ * with num = den = 0 is the empty state).  The earlier tokens decay with
+ * the distance like any others, so for t in [0, T):
+ *     a_t = e^{-t w} a_0 + sum_{i<t} e^{-(t-1-i) w + k_i} v_i  (b_t alike)
+ *     wkv_t = (a_t + e^{u+k_t} v_t) / (b_t + e^{u+k_t}).
+ * Evaluated by the recurrence of wkv_oracle_forward_recurrent with the sums
+ * kept as (A, Bs, M), a = A e^{M}, so that a state with a large pp does not
+ * overflow a double; M is the running maximum of the exponents.  num_in
+ * (with den_in, pp_in) may be NULL: the empty state.  The state after the
+ * T tokens is written to num_out, den_out, pp_out ([B, C], may be NULL) in
+ * the same convention. */
+void wkv_oracle_forward_state(int B, int T, int C, const double *w, const double *u,
+                              const double *k, const double *v, const double *num_in,
+                              const double *den_in, const double *pp_in, double *y,
+                              double *num_out, double *den_out, double *pp_out)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int c = 0; c < C; ++c) {
+            size_t o = (size_t)b * (size_t)C + (size_t)c;
+            double A = 0.0, Bs = 0.0, M = -INFINITY;
+            if (num_in && pp_in[o] > -1e37) {
+                A = num_in[o];
+                Bs = den_in[o];
+                M = pp_in[o];
+            }
+            for (int t = 0; t < T; ++t) {
+                double kt = k[IDX(b, t, c)], vt = v[IDX(b, t, c)];
+                double ek = u[c] + kt;                 /* exponent of the current token's weight */
+                double q = M > ek ? M : ek;
+                double sp = exp(M - q), sc = exp(ek - q);
+                y[IDX(b, t, c)] = (A * sp + vt * sc) / (Bs * sp + sc);
+                double m2 = (M - w[c]) > kt ? (M - w[c]) : kt;
+                double dp = exp(M - w[c] - m2), dk = exp(kt - m2);
+                A = A * dp + vt * dk;
+                Bs = Bs * dp + dk;
+                M = m2;
+            }
+            if (num_out) {
+                int seen = M > -INFINITY;
+                num_out[o] = seen ? A : 0.0;
+                den_out[o] = seen ? Bs : 0.0;
+                pp_out[o] = seen ? M : -1e38;
+            }
+        }
+}
+
 /* Backward, reverse-mode differentiation of the recurrent form.  Given the
  * upstream gradient gy = dLoss/dwkv, returns gk, gv ([B,T,C]) and gw, gu
  * ([C], summed over b and t).  With N_t, D_t the numerator and denominator

@@ -256,6 +256,31 @@ def pin_state_definition(o):
         assert np.all(den >= 1.0 - 1e-12), "den >= 1 (the max term is exactly 1)"
 
 
+def pin_forward_state_split(o):
+    """A sequence cut at t0 and continued from the state of its first t0
+    tokens (the direct-sum state) gives the parallel form's outputs for the
+    remaining tokens, and ends in the direct-sum state of all tokens; the
+    empty state is the plain forward; two cuts chained through the returned
+    state agree with one."""
+    w, u, k, v, _ = _rand_inputs(70, B=2, T=30, C=4, k_std=2.5)
+    y = o.forward_direct(w, u, k, v)
+    T = k.shape[1]
+    y0, _ = o.forward_state(w, u, k, v, None)
+    _close(y0, y, 1e-12, 1e-13, "empty state in")
+    n_all, d_all, p_all = o.state(w, k, v, T)
+    for t0 in (0, 1, 7, 29, 30):
+        sin = o.state(w, k, v, t0)
+        y2, (n2, d2, p2) = o.forward_state(w, u, k[:, t0:], v[:, t0:], sin)
+        _close(y2, y[:, t0:], 1e-12, 1e-13, f"continued outputs t0={t0}")
+        _close(p2, p_all, 1e-13, 1e-13, f"state out pp t0={t0}")
+        _close(n2, n_all, 1e-12, 1e-13, f"state out num t0={t0}")
+        _close(d2, d_all, 1e-12, 1e-13, f"state out den t0={t0}")
+    ya, sa = o.forward_state(w, u, k[:, :11], v[:, :11], None)
+    yb, sb = o.forward_state(w, u, k[:, 11:], v[:, 11:], sa)
+    _close(np.concatenate([ya, yb], axis=1), y, 1e-12, 1e-13, "two chained cuts")
+    _close(sb[2], p_all, 1e-13, 1e-13, "chained state pp")
+
+
 def pin_decode_hand_values(o):
     for case in GOLDEN["decode"]:
         for s in case["steps"]:
@@ -318,6 +343,7 @@ ALL_PINS = [
     pin_backward_finite_differences,
     pin_backward_forms_agree,
     pin_backward_identities,
+    pin_forward_state_split,
     pin_state_definition,
     pin_decode_hand_values,
     pin_decode_matches_forward,

@@ -50,6 +50,10 @@ MUTANTS = [
      "double pp2 = pp[o] - w[p] > k[o] ? pp[o] - w[p] : k[o];", "double pp2 = pp[o] > k[o] ? pp[o] : k[o];"),
     ("decode_drops_bonus", "wkv_oracle_decode_step",
      "double e = exp(u[p] + k[o]);", "double e = exp(k[o]);"),
+    ("state_in_not_decayed", "wkv_oracle_forward_state",
+     "double dp = exp(M - w[c] - m2)", "double dp = exp(M - m2)"),
+    ("state_in_scale_ignored", "wkv_oracle_forward_state",
+     "double sp = exp(M - q), sc", "double sp = exp(-q), sc"),
 ]
 
 
