@@ -106,8 +106,8 @@ wkv_status wkv_workspace_check(void* workspace, void* stream);
 
 /*
  * wkv_forward -- the training (time-parallel) form: y[b,t,c] = wkv_t for all
- * t at once, by a single-pass chunked scan over T (chunk summaries combined
- * through a bounded decoupled look-back), so k and v are read once.
+ * t at once, by a chunked associative scan over T (chunk summaries combined
+ * across chunks, runs and CTAs; see wkv_debug_set_scan_mode).
  *   kv_dtype  WKV_F32 (k, v are float) or WKV_BF16 (k, v are bf16); w, u, y
  *             are float in both cases and all arithmetic is fp32.
  *   ckpt      optional output (may be NULL): wkv_checkpoint_floats(B,T,C)
@@ -121,6 +121,34 @@ wkv_status wkv_workspace_check(void* workspace, void* stream);
 wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
                        const void* v, float* y, float* ckpt, void* workspace, size_t workspace_bytes,
                        void* stream);
+
+/*
+ * wkv_forward_with_state -- wkv_forward continuing a sequence whose earlier
+ * tokens are summarised by a carried state, and returning the state after
+ * the last token: the prefill of a prompt by the time-parallel form, handed
+ * to wkv_decode_step for the tokens that follow (the pages' two forms of
+ * the same operator: parallel for training, recurrent for inference;
+ * "RWKV解读" section "3、RWKV的网络架构": eq. (8) can be written
+ * recursively; qiita "RWKVとは？": a token and a state in, an output and a
+ * new state out).
+ *   state_in   [3][B][C] floats, or NULL for the empty state: the planes
+ *              num, den, pp of the state before token 0, in the convention
+ *              of the decode step (a = num e^{pp}, b = den e^{pp} are the
+ *              decayed sums over the earlier tokens; pp = -1e38 with
+ *              num = den = 0 is the empty state).  The earlier tokens decay
+ *              with the distance like any others.
+ *   state_out  [3][B][C] floats, or NULL: the same planes after token T-1
+ *              (pp the running maximum), ready for wkv_decode_step (its
+ *              num, den, pp for one layer are the three planes).
+ *   The other arguments are those of wkv_forward; ckpt and y describe the T
+ *   tokens of this call.  wkv_backward differentiates the forward pass from
+ *   the empty state only: the gradient with respect to a state_in is not
+ *   computed.
+ * Errors: as wkv_forward.
+ */
+wkv_status wkv_forward_with_state(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                                  const void* v, const float* state_in, float* y, float* state_out, float* ckpt,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * wkv_backward -- gradients of sum(gy * wkv) with respect to w, u, k, v.

@@ -39,6 +39,7 @@ _SIGNATURES = {
     "wkv_workspace_init": ([_vp, _sz, _vp], _i),
     "wkv_workspace_check": ([_vp, _vp], _i),
     "wkv_forward": ([_i, _i, _i, _i] + [_vp] * 6 + [_vp, _sz, _vp], _i),
+    "wkv_forward_with_state": ([_i, _i, _i, _i] + [_vp] * 8 + [_vp, _sz, _vp], _i),
     "wkv_backward": ([_i, _i, _i, _i] + [_vp] * 10 + [_vp, _sz, _vp], _i),
     "wkv_decode_step": ([_i, _i, _i] + [_vp] * 17 + [_vp], _i),
     "wkv_forward_noalloc": ([_i, _i, _i, _i] + [_vp] * 6 + [_vp], _i),
@@ -174,6 +175,41 @@ def forward(w, u, k, v, *, y=None, ckpt=None, want_ckpt: bool = False, workspace
     _check(_lib.wkv_forward(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(y), _p(ckpt), ws.ptr(), ws.nbytes,
                             _stream(stream)), "wkv_forward")
     return (y, ckpt) if ckpt is not None else y
+
+
+def forward_with_state(w, u, k, v, state_in=None, *, y=None, state_out=None, ckpt=None, want_ckpt: bool = False,
+                       workspace: Workspace | None = None, stream=None):
+    """wkv over k, v [B, T, C] continuing from ``state_in`` (fp32 [3, B, C]:
+    the planes num, den, pp; None: the empty state).  Returns
+    ``(y, state_out)``, or ``(y, state_out, ckpt)`` when ``want_ckpt`` or a
+    ``ckpt`` buffer is given; ``state_out`` is [3, B, C] (the state after the
+    last token, in the decode step's convention)."""
+    if k.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("k must be float32 or bfloat16")
+    B, T, C = k.shape
+    _need(k, "k", (k.dtype,))
+    _need(v, "v", (k.dtype,), k.shape)
+    _need(w, "w", shape=(C,))
+    _need(u, "u", shape=(C,))
+    if state_in is not None:
+        _need(state_in, "state_in", shape=(3, B, C))
+    if y is None:
+        y = torch.empty((B, T, C), dtype=torch.float32, device=k.device)
+    _need(y, "y", shape=(B, T, C))
+    if state_out is None:
+        state_out = torch.empty((3, B, C), dtype=torch.float32, device=k.device)
+    _need(state_out, "state_out", shape=(3, B, C))
+    if ckpt is None and want_ckpt:
+        ckpt = torch.empty(checkpoint_floats(B, T, C), dtype=torch.float32, device=k.device)
+    if ckpt is not None:
+        _need(ckpt, "ckpt")
+        if ckpt.numel() < checkpoint_floats(B, T, C):
+            raise ValueError("ckpt is too small")
+    ws = workspace or _workspace("fwd", forward_workspace_bytes(B, T, C), k.device)
+    dt = WKV_BF16 if k.dtype == torch.bfloat16 else WKV_F32
+    _check(_lib.wkv_forward_with_state(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(state_in), _p(y), _p(state_out),
+                                       _p(ckpt), ws.ptr(), ws.nbytes, _stream(stream)), "wkv_forward_with_state")
+    return (y, state_out, ckpt) if ckpt is not None else (y, state_out)
 
 
 def forward_noalloc(w, u, k, v, *, y=None, ckpt=None, stream=None):

@@ -304,6 +304,13 @@ wkv_status wkv_workspace_check(void* workspace, void* stream) {
 wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
                        const void* v, float* y, float* ckpt, void* workspace, size_t workspace_bytes,
                        void* stream) {
+  return wkv_forward_with_state(B, T, C, kv_dtype, w, u, k, v, nullptr, y, nullptr, ckpt, workspace,
+                                workspace_bytes, stream);
+}
+
+wkv_status wkv_forward_with_state(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                                  const void* v, const float* state_in, float* y, float* state_out, float* ckpt,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
   if (!sizes_ok(B, T, C) || !w || !u || !k || !v || !y) return WKV_ERR_INVALID_ARG;
   if (kv_dtype != WKV_F32 && kv_dtype != WKV_BF16) return WKV_ERR_INVALID_ARG;
@@ -322,6 +329,8 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
     q.k = k;
     q.v = v;
     q.y = y;
+    q.state_in = state_in;
+    q.state_out = state_out;
     q.ckpt = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.ckpt);
     q.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.agg);
     q.eh = static_cast<WsHeader*>(workspace);
@@ -342,6 +351,8 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
   a.k = k;
   a.v = v;
   a.y = y;
+  a.state_in = state_in;
+  a.state_out = state_out;
   a.agg = reinterpret_cast<Rec*>(bytes(workspace) + l.agg);
   a.inc = reinterpret_cast<Rec*>(bytes(workspace) + l.inc);
   a.ckpt = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.ckpt);

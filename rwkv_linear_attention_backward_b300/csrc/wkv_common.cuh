@@ -52,6 +52,19 @@ struct State {
 
 __device__ __forceinline__ State empty_state() { return State{0.f, 0.f, kEmptyPP}; }
 
+// A state given per (batch row, channel) as planes [3][B][C] (num, den, pp;
+// bc = B * C, o = b * C + c); NULL is the empty state.
+__device__ __forceinline__ State load_state_planes(const float* s, size_t bc, size_t o) {
+  if (s == nullptr) return empty_state();
+  return State{__ldg(s + o), __ldg(s + o + bc), __ldg(s + o + 2 * bc)};
+}
+
+__device__ __forceinline__ void store_state_planes(float* s, size_t bc, size_t o, const State& P) {
+  s[o] = P.num;
+  s[o + bc] = P.den;
+  s[o + 2 * bc] = P.pp;
+}
+
 // Consume one token (k, v): a' = e^{-w} a + e^{k} v, b' = e^{-w} b + e^{k},
 // pp' = max(pp - w, k).  The old state is carried over by the factor
 // e^{(pp - w) - pp'} = dec * (1 + res), where res = (pp - w) - fl(pp - w) is

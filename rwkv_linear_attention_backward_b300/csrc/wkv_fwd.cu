@@ -209,7 +209,7 @@ __device__ __forceinline__ void fwd_walk_item(const FwdArgs& a, const Launch& L,
   float* ps = walk_state(pst, qi) + lane;
   State P;
   if (j == 0) {
-    P = empty_state();
+    P = load_state_planes(a.state_in, (size_t)g.B * g.C, eo & 0x7fffffff);
   } else if (mq == 1) {
     P = one.P;
   } else if (in_smem) {
@@ -227,6 +227,7 @@ __device__ __forceinline__ void fwd_walk_item(const FwdArgs& a, const Launch& L,
     a.ckpt[o + P3] = P.den;
     a.ckpt[o + 2 * P3] = P.pp;
     if (j < g.nchunks - 1) rec_store(a.inc + o, L.tag, P.num, P.den, P.pp);
+    if (j == g.nchunks - 1 && a.state_out) store_state_planes(a.state_out, (size_t)g.B * g.C, eo & 0x7fffffff, P);
   }
   if (mq == 1) {
     one.P = P;
@@ -422,6 +423,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) fwd_scan_kernel(const __grid_
           const Rec r = rec_load(a.inc + ((size_t)(p.j - 1) * g.B + p.b) * g.C + (valid ? p.c : 0));
           ready = __all_sync(0xffffffffu, !valid || rec_ok(r, L.tag));
           P = State{rec_x(r), rec_y(r), rec_z(r)};
+        } else if (p.live && p.j == 0) {
+          P = load_state_planes(a.state_in, (size_t)g.B * g.C, (size_t)p.b * g.C + (p.c < g.C ? p.c : g.C - 1));
         }
         if (ready) {
           if (p.live && !failed) {

@@ -41,6 +41,8 @@ struct FwdArgs {
   const void* k;
   const void* v;
   float* y;            // may be null (state-only pass)
+  const float* state_in;  // [3][B][C] state before the first token (num, den, pp planes); null: empty
+  float* state_out;       // [3][B][C] state after the last token; may be null
   Rec* agg;            // each chunk's own summary (from the empty state), written by the tiles
   Rec* inc;            // the state after each chunk, written by the walkers for the next chunk's tiles
   float* ckpt;         // [3][nchunks][B][C] f32: the state after each chunk (the checkpoints)
@@ -121,6 +123,8 @@ struct SeqFwdArgs {
   const void* v;
   float* y;               // may be null (state-only pass)
   float* ckpt;            // [3][nchunks][B][C] state after each chunk
+  const float* state_in;  // [3][B][C] state before the first token (num, den, pp planes); null: empty
+  float* state_out;       // [3][B][C] state after the last token; may be null
   Rec* recs;              // [nseg][B][C] run summaries (tagged records)
   unsigned int* exited;   // CTAs of this launch that have finished (in a workspace header)
   WsHeader* eh;

@@ -435,8 +435,9 @@ __device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L
   const bool skip = a.debug_skip_chunk >= first && a.debug_skip_chunk < first + count;  // fault injection
   if (n1 > 0 && col.valid && !skip) rec_store(a.recs + (size_t)run * jstride + rec0, L.tag, P.num, P.den, P.pp);
 
-  // the carry into this run: the runs before it, in order
-  P = empty_state();
+  // the carry into this run: the state given before the first token, then
+  // the runs before this one, in order
+  P = load_state_planes(a.state_in, jstride, rec0);
   for (int r = 0; r < run; ++r) {
     int fr, cr;
     segment_of(g.nchunks, nseg, r, fr, cr);
@@ -461,6 +462,7 @@ __device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L
       a.ckpt[o] = P.num;
       a.ckpt[o + g.plane] = P.den;
       a.ckpt[o + 2 * g.plane] = P.pp;
+      if (j == g.nchunks - 1 && a.state_out) store_state_planes(a.state_out, jstride, rec0, P);
     }
     release(it);
   }
@@ -551,7 +553,7 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
   // the state after run r - 1 (empty before run 0)
   auto carry_in = [&](int r, State& P) {
     if (r == 0) {
-      P = empty_state();
+      P = load_state_planes(a.state_in, jstride, rec0);  // the state given before the first token
       return true;
     }
     Rec rec;
@@ -591,6 +593,7 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
         a.ckpt[o] = P.num;
         a.ckpt[o + g.plane] = P.den;
         a.ckpt[o + 2 * g.plane] = P.pp;
+        if (m.j == g.nchunks - 1 && a.state_out) store_state_planes(a.state_out, jstride, rec0, P);
       }
     }
     // release the stage (only read: see seq_fwd_run)
