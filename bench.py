@@ -51,6 +51,7 @@ METRIC_DEC = "WKV decode step L·B·C elements/s and achieved HBM GB/s fraction 
 BYTES_FWD_F32 = 12   # read k, v; write y
 BYTES_FWD_BF16 = 8   # read bf16 k, v; write fp32 y
 BYTES_BWD = 20       # read k, v, gy; write gk, gv
+BYTES_BWD_BF16 = 14  # read bf16 k, v, gy; write fp32 gk, gv
 BYTES_DECODE = 60    # read x, x_prev, r, k, v; read+write num, den, pp; write y, xk, xv, xr
 
 REJECT_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
@@ -61,7 +62,7 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default depends on the workload)")
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="l169m", choices=["tiny", "l169m", "l1b5", "long", "decode"])
+    ap.add_argument("--workload", default="l169m", choices=["tiny", "l169m", "l1b5", "long", "l169m_bf16", "decode"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -75,7 +76,7 @@ def parse_args(argv=None):
     return args
 
 
-DEFAULT_STEPS = {"tiny": 2000, "l169m": 4000, "l1b5": 200, "long": 200, "decode": 256}
+DEFAULT_STEPS = {"tiny": 2000, "l169m": 4000, "l1b5": 200, "long": 200, "l169m_bf16": 4000, "decode": 256}
 
 
 # ------------------------------------------------------------------ ranks
@@ -286,7 +287,8 @@ class TrainingRun:
         self.ws_b = binding.Workspace(binding.backward_workspace_bytes(B, T, C), device)
         kv_bytes = BYTES_FWD_BF16 if wl.kv_dtype == "bf16" else BYTES_FWD_F32
         self.bytes_fwd = kv_bytes * self.elements
-        self.bytes_bwd = BYTES_BWD * self.elements if wl.backward else 0
+        bwd_bytes = BYTES_BWD_BF16 if wl.kv_dtype == "bf16" else BYTES_BWD
+        self.bytes_bwd = bwd_bytes * self.elements if wl.backward else 0
         self.launches_per_step = 1 + (2 if wl.backward else 0)
         from rwkv_linear_attention_backward_b300 import binding
 

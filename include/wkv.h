@@ -152,7 +152,10 @@ wkv_status wkv_forward_with_state(int B, int T, int C, int kv_dtype, const float
 
 /*
  * wkv_backward -- gradients of sum(gy * wkv) with respect to w, u, k, v.
- *   gy          upstream gradient [B, T, C], float.
+ *   kv_dtype    WKV_F32: k, v, gy are float; WKV_BF16: k, v, gy are bf16
+ *               (halving the bytes read; the arithmetic stays fp32 and
+ *               gw, gu, gk, gv are float in both cases).
+ *   gy          upstream gradient [B, T, C], of kv_dtype.
  *   ckpt        optional (may be NULL): the checkpoint array written by
  *               wkv_forward for the same w, k, v.  When NULL the call first
  *               recomputes it (one extra pass over k and v).
@@ -161,11 +164,12 @@ wkv_status wkv_forward_with_state(int B, int T, int C, int kv_dtype, const float
  *   workspace   at least wkv_backward_workspace_bytes(B, T, C) bytes.
  * The reverse-time adjoint recurrence is scanned in chunks from the last
  * chunk backwards; the forward states are recomputed per chunk from the
- * checkpoints.  Errors: as wkv_forward; kv_dtype must be WKV_F32
- * (WKV_ERR_UNSUPPORTED otherwise).
+ * checkpoints.  Errors: as wkv_forward; WKV_ERR_UNSUPPORTED for WKV_BF16
+ * while wkv_debug_set_scan_mode forces the chunked scan (which takes fp32
+ * inputs only).
  */
 wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
-                        const void* v, const float* gy, const float* ckpt, float* gw, float* gu, float* gk,
+                        const void* v, const void* gy, const float* ckpt, float* gw, float* gu, float* gk,
                         float* gv, void* workspace, size_t workspace_bytes, void* stream);
 
 /*

@@ -234,11 +234,14 @@ def forward_noalloc(w, u, k, v, *, y=None, ckpt=None, stream=None):
 # --------------------------------------------------------------- backward
 def backward(w, u, k, v, gy, *, ckpt=None, gw=None, gu=None, gk=None, gv=None, workspace: Workspace | None = None,
              stream=None):
-    """Gradients (gw, gu, gk, gv) of sum(gy * wkv); fp32 inputs."""
+    """Gradients (gw, gu, gk, gv) of sum(gy * wkv); k, v, gy all fp32 or all
+    bf16 (fp32 arithmetic and fp32 gradients either way)."""
+    if k.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("k must be float32 or bfloat16")
     B, T, C = k.shape
-    _need(k, "k")
-    _need(v, "v", shape=k.shape)
-    _need(gy, "gy", shape=k.shape)
+    _need(k, "k", (k.dtype,))
+    _need(v, "v", (k.dtype,), k.shape)
+    _need(gy, "gy", (k.dtype,), k.shape)
     _need(w, "w", shape=(C,))
     _need(u, "u", shape=(C,))
     if ckpt is not None:
@@ -254,7 +257,8 @@ def backward(w, u, k, v, gy, *, ckpt=None, gw=None, gu=None, gk=None, gv=None, w
         _need(t, n, shape=s)
     need = backward_workspace_bytes(B, T, C)
     ws = workspace or _workspace("bwd", need, dev)
-    _check(_lib.wkv_backward(B, T, C, WKV_F32, _p(w), _p(u), _p(k), _p(v), _p(gy), _p(ckpt), _p(gw), _p(gu),
+    dt = WKV_BF16 if k.dtype == torch.bfloat16 else WKV_F32
+    _check(_lib.wkv_backward(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(gy), _p(ckpt), _p(gw), _p(gu),
                              _p(gk), _p(gv), ws.ptr(), ws.nbytes, _stream(stream)), "wkv_backward")
     return gw, gu, gk, gv
 

@@ -171,11 +171,12 @@ namespace {
 // (recomputed by a state-only forward walk when the caller has none), the
 // reverse walk writing gk, gv and one gw, gu row per (run, batch row), then
 // the reduction of those rows.
-wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const float* w, const float* u,
-                               const void* k, const void* v, const float* gy, const float* ckpt, float* gw,
-                               float* gu, float* gk, float* gv, WsHeader* hdr, void* workspace, uint64_t budget,
-                               cudaStream_t s) {
+wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int kv_dtype, const float* w,
+                               const float* u, const void* k, const void* v, const void* gy, const float* ckpt,
+                               float* gw, float* gu, float* gk, float* gv, WsHeader* hdr, void* workspace,
+                               uint64_t budget, cudaStream_t s) {
   const int B = g.B, T = g.T, C = g.C;
+  const int eb = kv_dtype == WKV_F32 ? 4 : 2;
   const float* states = ckpt;
   if (!states) {
     SeqFwdArgs f;
@@ -194,8 +195,8 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const 
     f.eh = hdr;
     f.g = g;
     f.budget_ns = budget;
-    f.use_tma = make_tile_map(&f.tk, k, B, T, C, 4, kSeqChannels) && make_tile_map(&f.tv, v, B, T, C, 4, kSeqChannels);
-    cudaError_t e = launch_seq_forward(f, WKV_F32, false, s);
+    f.use_tma = make_tile_map(&f.tk, k, B, T, C, eb, kSeqChannels) && make_tile_map(&f.tv, v, B, T, C, eb, kSeqChannels);
+    cudaError_t e = launch_seq_forward(f, kv_dtype, false, s);
     if (e != cudaSuccess) return cuda_fail(e, "wkv_backward: state pass");
     states = f.ckpt;
   }
@@ -203,8 +204,8 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const 
   std::memset(&a, 0, sizeof(a));
   a.w = w;
   a.u = u;
-  a.k = static_cast<const float*>(k);
-  a.v = static_cast<const float*>(v);
+  a.k = k;
+  a.v = v;
   a.gy = gy;
   a.ckpt = states;
   a.gk = gk;
@@ -217,9 +218,9 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, const 
   a.eh = hdr;
   a.g = g;
   a.budget_ns = budget;
-  a.use_tma = make_tile_map(&a.tk, k, B, T, C, 4, kSeqChannels) && make_tile_map(&a.tv, v, B, T, C, 4, kSeqChannels) &&
-              make_tile_map(&a.tg, gy, B, T, C, 4, kSeqChannels);
-  cudaError_t e = launch_seq_backward(a, s);
+  a.use_tma = make_tile_map(&a.tk, k, B, T, C, eb, kSeqChannels) &&
+              make_tile_map(&a.tv, v, B, T, C, eb, kSeqChannels) && make_tile_map(&a.tg, gy, B, T, C, eb, kSeqChannels);
+  cudaError_t e = launch_seq_backward(a, kv_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
   const int rows = a.nseg * B;
   ReduceArgs r;
@@ -368,12 +369,11 @@ wkv_status wkv_forward_with_state(int B, int T, int C, int kv_dtype, const float
 }
 
 wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
-                        const void* v, const float* gy, const float* ckpt, float* gw, float* gu, float* gk,
+                        const void* v, const void* gy, const float* ckpt, float* gw, float* gu, float* gk,
                         float* gv, void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
   if (!sizes_ok(B, T, C) || !w || !u || !k || !v || !gy || !gw || !gu || !gk || !gv) return WKV_ERR_INVALID_ARG;
   if (kv_dtype != WKV_F32 && kv_dtype != WKV_BF16) return WKV_ERR_INVALID_ARG;
-  if (kv_dtype != WKV_F32) return WKV_ERR_UNSUPPORTED;
   const ScanGeometry g = make_geometry(B, T, C);
   const BwdLayout l = bwd_layout(g);
   if (!workspace || workspace_bytes < l.total) return WKV_ERR_WORKSPACE;
@@ -384,7 +384,12 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
   bool seq = false;
   cudaError_t e = sequential_mode(g, seq);
   if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
-  if (seq) return backward_sequential(g, l, w, u, k, v, gy, ckpt, gw, gu, gk, gv, hdr, workspace, budget, s);
+  if (seq)
+    return backward_sequential(g, l, kv_dtype, w, u, k, v, gy, ckpt, gw, gu, gk, gv, hdr, workspace, budget, s);
+  if (kv_dtype != WKV_F32) {
+    set_last_error("wkv_backward: bf16 inputs are taken by the sequential kernels only (the chunked scan is forced)");
+    return WKV_ERR_UNSUPPORTED;
+  }
 
   const float* states = ckpt;
   if (!states) {
@@ -419,7 +424,7 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
   a.u = u;
   a.k = static_cast<const float*>(k);
   a.v = static_cast<const float*>(v);
-  a.gy = gy;
+  a.gy = static_cast<const float*>(gy);
   a.ckpt = states;
   a.gk = gk;
   a.gv = gv;

@@ -58,30 +58,32 @@ __device__ __forceinline__ Adj fold_adj(const Adj& A, float Lw, const Adj& X) {
 // The per-token (running-maximum) form for lanes outside the fixed scale's
 // bounds.  Rare, so its loops stay rolled with the per-token states (num,
 // den, pp before each token) in local memory, leaving the fast form's
-// registers alone.  The states from P; returns pp after the chunk.
-template <int S>
-__device__ __forceinline__ float exact_states(const float* sk, const float* sv, int len, State s, float w,
-                                              float* xa, float* xb, float* xp) {
+// registers alone.  The states from P; returns pp after the chunk.  E: the
+// element type of the staged k, v, gy (float or bf16).
+template <int S, typename E = float>
+__device__ __forceinline__ float exact_states(const E* sk, const E* sv, int len, State s, float w, float* xa,
+                                              float* xb, float* xp) {
 #pragma unroll 1
   for (int i = 0; i < len; ++i) {
     xa[i] = s.num;
     xb[i] = s.den;
     xp[i] = s.pp;
-    step(s, sk[i * S], sv[i * S], w);
+    step(s, to_f32<E>(sk[i * S]), to_f32<E>(sv[i * S]), w);
   }
   return s.pp;
 }
 
 // The zero-carry adjoint at the chunk start, scaled by e^{pp there}.
-template <int S>
-__device__ __forceinline__ void exact_zero_adjoint(const float* sk, const float* sv, const float* sg, int len,
-                                                   float w, float u, const float* xa, const float* xb,
-                                                   const float* xp, float& la, float& lb) {
+template <int S, typename E = float>
+__device__ __forceinline__ void exact_zero_adjoint(const E* sk, const E* sv, const E* sg, int len, float w, float u,
+                                                   const float* xa, const float* xb, const float* xp, float& la,
+                                                   float& lb) {
   la = 0.f;
   lb = 0.f;
 #pragma unroll 1
   for (int i = len - 1; i >= 0; --i) {
-    const Local o = local_terms(State{xa[i], xb[i], xp[i]}, sk[i * S], sv[i * S], sg[i * S], w, u);
+    const Local o = local_terms(State{xa[i], xb[i], xp[i]}, to_f32<E>(sk[i * S]), to_f32<E>(sv[i * S]),
+                                to_f32<E>(sg[i * S]), w, u);
     la = carry(o.t, la, o.gb);
     lb = carry(o.t, lb, -o.gb * o.y);
   }
@@ -90,16 +92,16 @@ __device__ __forceinline__ void exact_zero_adjoint(const float* sk, const float*
 // gk, gv with the carry (la, lb, scaled by e^{pp after the chunk});
 // out[0..1] receive the gw, gu partial sums, out[2..3] the adjoint at the
 // chunk start.
-template <int S>
-__device__ __forceinline__ void exact_final(const float* sk, const float* sv, const float* sg, int len, float w,
-                                            float u, const float* xa, const float* xb, const float* xp, float la,
-                                            float lb, float* gkp, float* gvp, int64_t C, bool valid, float* out) {
+template <int S, typename E = float>
+__device__ __forceinline__ void exact_final(const E* sk, const E* sv, const E* sg, int len, float w, float u,
+                                            const float* xa, const float* xb, const float* xp, float la, float lb,
+                                            float* gkp, float* gvp, int64_t C, bool valid, float* out) {
   float gw_acc = 0.f, gu_acc = 0.f;
 #pragma unroll 1
   for (int i = len - 1; i >= 0; --i) {
     const State si{xa[i], xb[i], xp[i]};
-    const float k = sk[i * S], v = sv[i * S];
-    const Local o = local_terms(si, k, v, sg[i * S], w, u);
+    const float k = to_f32<E>(sk[i * S]), v = to_f32<E>(sv[i * S]);
+    const Local o = local_terms(si, k, v, to_f32<E>(sg[i * S]), w, u);
     const float cur = o.gc * o.vmy;
     const float gk = fmaf(o.t.kap, fmaf(la, v, lb), cur);
     const float gv = fmaf(o.t.kap, la, o.gc);

@@ -15,9 +15,23 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace wkv {
+
+// Element of an input array (k, v, gy) as fp32: inputs may be fp32 or bf16,
+// the arithmetic is fp32.
+template <typename E>
+__device__ __forceinline__ float to_f32(E x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
 
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 constexpr float kEmptyPP = -1e38f;             // pp of the empty state

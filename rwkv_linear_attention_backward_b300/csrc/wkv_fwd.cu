@@ -44,16 +44,6 @@ namespace wkv {
 
 namespace {
 
-template <typename KV>
-__device__ __forceinline__ float to_f32(KV x);
-template <>
-__device__ __forceinline__ float to_f32<float>(float x) {
-  return x;
-}
-template <>
-__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
-  return __bfloat162float(x);
-}
 
 template <typename KV>
 struct FwdStages {

@@ -140,9 +140,9 @@ struct SeqBwdArgs {
   CUtensorMap tk, tv, tg;
   const float* w;
   const float* u;
-  const float* k;
-  const float* v;
-  const float* gy;
+  const void* k;   // k, v, gy: float or bf16 (kv_dtype of the launch)
+  const void* v;
+  const void* gy;
   const float* ckpt;
   float* gk;
   float* gv;
@@ -159,7 +159,7 @@ struct SeqBwdArgs {
 
 // Choose the runs per column (written to a.nseg) and launch.
 cudaError_t launch_seq_forward(SeqFwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
-cudaError_t launch_seq_backward(SeqBwdArgs& a, cudaStream_t s);
+cudaError_t launch_seq_backward(SeqBwdArgs& a, int kv_dtype, cudaStream_t s);
 
 // Grid of a persistent scan kernel: resident CTAs per SM x SMs, at most ntiles.
 cudaError_t launch_forward(FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);

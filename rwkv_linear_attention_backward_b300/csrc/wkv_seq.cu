@@ -40,16 +40,6 @@ constexpr int kSeqTile = kChunk * kSeqChannels;  // elements of one array in one
 constexpr float kFastRange = 69.f;  // smallest bonus weight of the fixed scale: e^{-69}
 constexpr float kFastCeil = 60.f;   // largest scale-up of the fixed scale: e^{60}
 
-template <typename KV>
-__device__ __forceinline__ float to_f32(KV x);
-template <>
-__device__ __forceinline__ float to_f32<float>(float x) {
-  return x;
-}
-template <>
-__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
-  return __bfloat162float(x);
-}
 
 // Column q (batch row q / nwg, channels from 32 (q % nwg)): batch row,
 // first channel, this lane's channel.
@@ -649,11 +639,12 @@ __device__ __forceinline__ void kahan_add(float& s, float& k, float x) {
 
 // FULL: a whole chunk (n == kChunk), every loop fully unrolled with no
 // per-token branch and ek kept in registers (see seq_fwd_full); otherwise
-// the first n tokens, each token under its own predicate, ek stored over k
-// in the stage.
-template <bool FULL>
-__device__ __forceinline__ void seq_bwd_chunk(float* __restrict__ sk, const float* __restrict__ sv,
-                                              const float* __restrict__ sg, int n, const BwdColumn& cw,
+// the first n tokens, each token under its own predicate, ek computed again
+// where the reverse sweep needs it.  KV: the staged element type (float or
+// bf16; the arithmetic is fp32).
+template <bool FULL, typename KV>
+__device__ __forceinline__ void seq_bwd_chunk(const KV* __restrict__ sk, const KV* __restrict__ sv,
+                                              const KV* __restrict__ sg, int n, const BwdColumn& cw,
                                               const State& P, bool has_succ, Adj& X, float* __restrict__ gkp,
                                               float* __restrict__ gvp, int64_t stride, bool valid, float& gw_acc,
                                               float& gu_acc, float* xa, float* xb, float* xp) {
@@ -664,7 +655,7 @@ __device__ __forceinline__ void seq_bwd_chunk(float* __restrict__ sk, const floa
   float F, kmin;
   if constexpr (FULL) {
 #pragma unroll
-    for (int i = 0; i < L; ++i) kr[i] = sk[i * S];
+    for (int i = 0; i < L; ++i) kr[i] = to_f32<KV>(sk[i * S]);
     F = tree_max<L>(kr);
     kmin = tree_min<L>(kr);
   } else {
@@ -672,7 +663,7 @@ __device__ __forceinline__ void seq_bwd_chunk(float* __restrict__ sk, const floa
     kmin = 3.0e38f;
 #pragma unroll 8
     for (int i = 0; i < n; ++i) {
-      const float k = sk[i * S];
+      const float k = to_f32<KV>(sk[i * S]);
       F = fmaxf(F, k);
       kmin = fminf(kmin, k);
     }
@@ -697,10 +688,9 @@ __device__ __forceinline__ void seq_bwd_chunk(float* __restrict__ sk, const floa
         if constexpr (FULL) {
           ek = kr[i];
         } else {
-          ek = ex2(fmaf(sk[i * S], kLog2e, -F2));
-          sk[i * S] = ek;
+          ek = ex2(fmaf(to_f32<KV>(sk[i * S]), kLog2e, -F2));
         }
-        const float vv = sv[i * S];
+        const float vv = to_f32<KV>(sv[i * S]);
         A[i] = na;
         Bd[i] = nb;
         na = fmaf(na, cw.ew, ek * vv);
@@ -721,15 +711,15 @@ __device__ __forceinline__ void seq_bwd_chunk(float* __restrict__ sk, const floa
       for (int i = 0; i < L; ++i) {
         const float ec = kr[i] * cw.eu;
         const float rr = rcp(Bd[i] + ec);
-        GI[i] = sg[i * S] * rr;                        // gN at scale e^{F}
-        VM[i] = fmaf(sv[i * S], Bd[i], -A[i]) * rr;  // v - wkv
+        GI[i] = to_f32<KV>(sg[i * S]) * rr;                        // gN at scale e^{F}
+        VM[i] = fmaf(to_f32<KV>(sv[i * S]), Bd[i], -A[i]) * rr;  // v - wkv
       }
 #pragma unroll
       for (int i = L - 1; i >= 0; --i) {
         const float la = fmaf(xla, pw, la0);  // adjoints after token i, at scale e^{F}
         const float lb = fmaf(xlb, pw, lb0);
         const float ek = kr[i];
-        const float vv = sv[i * S];
+        const float vv = to_f32<KV>(sv[i * S]);
         const float ec = ek * cw.eu;
         const float gi = GI[i];
         const float cur = gi * VM[i] * ec;  // (gN v + gD) e^{u+k}
@@ -752,11 +742,11 @@ __device__ __forceinline__ void seq_bwd_chunk(float* __restrict__ sk, const floa
       if (!FULL && i < n) {
         const float la = fmaf(xla, pw, la0);
         const float lb = fmaf(xlb, pw, lb0);
-        const float ek = sk[i * S];
-        const float vv = sv[i * S];
+        const float ek = ex2(fmaf(to_f32<KV>(sk[i * S]), kLog2e, -F2));
+        const float vv = to_f32<KV>(sv[i * S]);
         const float ec = ek * cw.eu;
         const float rr = rcp(Bd[i] + ec);
-        const float gi = sg[i * S] * rr;
+        const float gi = to_f32<KV>(sg[i * S]) * rr;
         const float vmy = fmaf(vv, Bd[i], -A[i]) * rr;  // v - wkv
         const float cur = gi * vmy * ec;                // (gN v + gD) e^{u+k}
         const float gk = fmaf(fmaf(la, vv, lb), ek, cur);
@@ -778,10 +768,10 @@ __device__ __forceinline__ void seq_bwd_chunk(float* __restrict__ sk, const floa
     const Adj A0{la0 * s0, lb0 * s0, P.pp};
     X = has_succ ? fold_adj(A0, (float)n * cw.w, X) : A0;
   } else {
-    const float pp_end = exact_states<kSeqChannels>(sk, sv, n, P, cw.w, xa, xb, xp);
+    const float pp_end = exact_states<kSeqChannels, KV>(sk, sv, n, P, cw.w, xa, xb, xp);
     const float f = has_succ ? exp_nat(pp_end - X.f) : 0.f;
     float res[4];
-    exact_final<kSeqChannels>(sk, sv, sg, n, cw.w, cw.u, xa, xb, xp, X.la * f, X.lb * f, gkp, gvp, stride, valid,
+    exact_final<kSeqChannels, KV>(sk, sv, sg, n, cw.w, cw.u, xa, xb, xp, X.la * f, X.lb * f, gkp, gvp, stride, valid,
                               res);
     gw_acc = res[0];
     gu_acc = res[1];
@@ -794,9 +784,9 @@ __device__ __forceinline__ void seq_bwd_chunk(float* __restrict__ sk, const floa
 // by e^{P.pp}, P the state before the chunk.  The forward sums and the
 // adjoint accumulate in one forward sweep, each token's gN, gD weighted by
 // e^{-(t - t0) w} (pw), as in the chunked backward pass's summary.
-template <bool FULL>
-__device__ __forceinline__ Adj seq_bwd_summary(const float* __restrict__ sk, const float* __restrict__ sv,
-                                               const float* __restrict__ sg, int n, const BwdColumn& cw,
+template <bool FULL, typename KV>
+__device__ __forceinline__ Adj seq_bwd_summary(const KV* __restrict__ sk, const KV* __restrict__ sv,
+                                               const KV* __restrict__ sg, int n, const BwdColumn& cw,
                                                const State& P, float* xa, float* xb, float* xp) {
   constexpr int L = kChunk;
   constexpr int S = kSeqChannels;
@@ -805,7 +795,7 @@ __device__ __forceinline__ Adj seq_bwd_summary(const float* __restrict__ sk, con
   float F, kmin;
   if constexpr (FULL) {
 #pragma unroll
-    for (int i = 0; i < L; ++i) kr[i] = sk[i * S];
+    for (int i = 0; i < L; ++i) kr[i] = to_f32<KV>(sk[i * S]);
     F = tree_max<L>(kr);
     kmin = tree_min<L>(kr);
   } else {
@@ -813,7 +803,7 @@ __device__ __forceinline__ Adj seq_bwd_summary(const float* __restrict__ sk, con
     kmin = 3.0e38f;
 #pragma unroll 8
     for (int i = 0; i < n; ++i) {
-      const float k = sk[i * S];
+      const float k = to_f32<KV>(sk[i * S]);
       F = fmaxf(F, k);
       kmin = fminf(kmin, k);
     }
@@ -831,10 +821,10 @@ __device__ __forceinline__ Adj seq_bwd_summary(const float* __restrict__ sk, con
 #pragma unroll
       for (int i = 0; i < L; ++i) {
         const float ek = kr[i];
-        const float vv = sv[i * S];
+        const float vv = to_f32<KV>(sv[i * S]);
         const float ec = ek * cw.eu;
         const float rr = rcp(nb + ec);
-        const float gi = sg[i * S] * rr;        // gN at scale e^{F}
+        const float gi = to_f32<KV>(sg[i * S]) * rr;        // gN at scale e^{F}
         const float y = fmaf(ec, vv, na) * rr;  // wkv_t
         la = fmaf(pw, gi, la);
         lb = fmaf(-pw, gi * y, lb);
@@ -845,11 +835,11 @@ __device__ __forceinline__ Adj seq_bwd_summary(const float* __restrict__ sk, con
     } else {
 #pragma unroll 8
       for (int i = 0; i < n; ++i) {
-        const float ek = ex2(fmaf(sk[i * S], kLog2e, -F2));
-        const float vv = sv[i * S];
+        const float ek = ex2(fmaf(to_f32<KV>(sk[i * S]), kLog2e, -F2));
+        const float vv = to_f32<KV>(sv[i * S]);
         const float ec = ek * cw.eu;
         const float rr = rcp(nb + ec);
-        const float gi = sg[i * S] * rr;
+        const float gi = to_f32<KV>(sg[i * S]) * rr;
         const float y = fmaf(ec, vv, na) * rr;
         la = fmaf(pw, gi, la);
         lb = fmaf(-pw, gi * y, lb);
@@ -861,16 +851,16 @@ __device__ __forceinline__ Adj seq_bwd_summary(const float* __restrict__ sk, con
     la *= s0;  // from scale e^{F} to the record's e^{P.pp}
     lb *= s0;
   } else {
-    exact_states<kSeqChannels>(sk, sv, n, P, cw.w, xa, xb, xp);
-    exact_zero_adjoint<kSeqChannels>(sk, sv, sg, n, cw.w, cw.u, xa, xb, xp, la, lb);
+    exact_states<kSeqChannels, KV>(sk, sv, n, P, cw.w, xa, xb, xp);
+    exact_zero_adjoint<kSeqChannels, KV>(sk, sv, sg, n, cw.w, cw.u, xa, xb, xp, la, lb);
   }
   return Adj{la, lb, P.pp};
 }
 
-template <int NS>
+template <typename KV, int NS>
 __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L, unsigned char* smem) {
-  float* ring = reinterpret_cast<float*>(smem);  // stage s: k, v, gy at (3s + 0..2) * kSeqTile
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + seq_ring_elems<float, NS>(3) * sizeof(float));
+  KV* ring = reinterpret_cast<KV*>(smem);  // stage s: k, v, gy at (3s + 0..2) * kSeqTile
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + seq_ring_elems<KV, NS>(3) * sizeof(KV));
   const int lane = threadIdx.x;
   const ScanGeometry& g = a.g;
   const int nseg = a.nseg;
@@ -883,7 +873,7 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
   cw.eu = expf(cw.u);
   cw.gw_s = cw.gw_k = cw.gu_s = cw.gu_k = 0.f;
   const bool tma = a.use_tma != 0;
-  constexpr uint32_t kStageBytes = 3 * kSeqTile * sizeof(float);
+  constexpr uint32_t kStageBytes = 3 * kSeqTile * sizeof(KV);
   const int last = g.nchunks - 1;
 
   int first, count;  // in walk order: position p is chunk last - p
@@ -894,7 +884,7 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
   auto issue = [&](int it) {  // lane 0: item it into its stage
     const int s = it % NS;
     const int j = chunk_of(it);
-    float* dk = ring + (size_t)(3 * s) * kSeqTile;
+    KV* dk = ring + (size_t)(3 * s) * kSeqTile;
     mbar_arrive_expect_tx(&full[s], kStageBytes);
     tma_load_3d(dk, &a.tk, &full[s], col.c0, j * kChunk, col.b);
     tma_load_3d(dk + kSeqTile, &a.tv, &full[s], col.c0, j * kChunk, col.b);
@@ -913,21 +903,19 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
     issued = min(NS, nitems);
     __syncwarp();
   }
-  auto acquire = [&](int it, float*& dk) {
+  auto acquire = [&](int it, KV*& dk) {
     const int s = it % NS;
     dk = ring + (size_t)(3 * s) * kSeqTile;
     if (tma) return stage_wait(&full[s], (uint32_t)((it / NS) & 1), a.budget_ns);
     const int j = chunk_of(it);
-    copy_box_plain(dk, a.k, g, col, j * kChunk);
-    copy_box_plain(dk + kSeqTile, a.v, g, col, j * kChunk);
-    copy_box_plain(dk + 2 * kSeqTile, a.gy, g, col, j * kChunk);
+    copy_box_plain(dk, static_cast<const KV*>(a.k), g, col, j * kChunk);
+    copy_box_plain(dk + kSeqTile, static_cast<const KV*>(a.v), g, col, j * kChunk);
+    copy_box_plain(dk + 2 * kSeqTile, static_cast<const KV*>(a.gy), g, col, j * kChunk);
     __syncwarp();
     return true;
   };
-  auto release = [&](int it, bool wrote) {
-    // a stage this warp wrote into (ek over k, partial chunks): order those
-    // writes before the async-proxy copy that refills it
-    if (wrote) fence_proxy_async_smem();
+  auto release = [&](int it) {
+    // the stage is only read (see seq_fwd_run): no proxy fence
     __syncwarp();
     if (tma && it + NS < nitems) {
       if (lane == 0) issue(it + NS);
@@ -955,17 +943,17 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
   for (; it < n1; ++it) {
     const State P = Pn;
     if (it + 1 < nitems) Pn = load_state(chunk_of(it + 1));  // one chunk ahead
-    float* dk;
+    KV* dk;
     if (!acquire(it, dk)) return fail(it);
     const int j = chunk_of(it);
     const int n = min(kChunk, g.T - j * kChunk);
     const Adj A = n == kChunk
-                      ? seq_bwd_summary<true>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P,
+                      ? seq_bwd_summary<true, KV>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P,
                                               xa, xb, xp)
-                      : seq_bwd_summary<false>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P,
+                      : seq_bwd_summary<false, KV>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P,
                                                xa, xb, xp);
     X = it == 0 ? A : fold_adj(A, (float)n * cw.w, X);
-    release(it, false);
+    release(it);
   }
   // fault injection: the run holding this chunk never publishes
   const bool skip = a.debug_skip_chunk >= 0 && last - a.debug_skip_chunk >= first &&
@@ -988,21 +976,21 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
   for (; it < nitems; ++it) {
     const State P = Pn;
     if (it + 1 < nitems) Pn = load_state(chunk_of(it + 1));
-    float* dk;
+    KV* dk;
     if (!acquire(it, dk)) return fail(it);
     const int j = chunk_of(it);
     const int n = min(kChunk, g.T - j * kChunk);
     const int64_t row = ((int64_t)col.b * g.T + (int64_t)j * kChunk) * g.C + col.c;
     float gw_acc, gu_acc;
     if (n == kChunk)
-      seq_bwd_chunk<true>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last, X,
+      seq_bwd_chunk<true, KV>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last, X,
                           a.gk + row, a.gv + row, g.C, col.valid, gw_acc, gu_acc, xa, xb, xp);
     else
-      seq_bwd_chunk<false>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last, X,
+      seq_bwd_chunk<false, KV>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last, X,
                            a.gk + row, a.gv + row, g.C, col.valid, gw_acc, gu_acc, xa, xb, xp);
     kahan_add(cw.gw_s, cw.gw_k, gw_acc);
     kahan_add(cw.gu_s, cw.gu_k, gu_acc);
-    release(it, n != kChunk);
+    release(it);
   }
   // one gw, gu row per (run, batch row): row run * B + b of [2][nseg * B][C]
   // (added up in row order by the reduction kernel that follows)
@@ -1013,11 +1001,11 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
   }
 }
 
-template <int NS>
+template <typename KV, int NS>
 __global__ void __launch_bounds__(kSeqChannels) seq_bwd_kernel(const __grid_constant__ SeqBwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Launch L = seq_launch(a.eh);
-  seq_bwd_run<NS>(a, L, smem);
+  seq_bwd_run<KV, NS>(a, L, smem);
   seq_exit(a.exited, a.eh, L.epoch);
 }
 
@@ -1193,9 +1181,12 @@ struct FwdKern {
   };
 };
 
-template <int NS>
+template <typename KV>
 struct BwdKern {
-  static constexpr void (*fn)(SeqBwdArgs) = seq_bwd_kernel<NS>;
+  template <int NS>
+  struct At {
+    static constexpr void (*fn)(SeqBwdArgs) = seq_bwd_kernel<KV, NS>;
+  };
 };
 
 template <typename KV, bool WRITE_Y>
@@ -1218,13 +1209,19 @@ cudaError_t launch_seq_forward(SeqFwdArgs& a, int kv_dtype, bool write_y, cudaSt
   return write_y ? launch_seq_fwd_t<__nv_bfloat16, true>(a, s) : launch_seq_fwd_t<__nv_bfloat16, false>(a, s);
 }
 
-cudaError_t launch_seq_backward(SeqBwdArgs& a, cudaStream_t s) {
+template <typename KV>
+cudaError_t launch_seq_bwd_t(SeqBwdArgs& a, cudaStream_t s) {
   DevInfo d;
   cudaError_t e = dev_info(d);
   if (e != cudaSuccess) return e;
-  const size_t input_bytes = (size_t)a.g.B * a.g.T * a.g.C * 3 * sizeof(float);
+  const size_t input_bytes = (size_t)a.g.B * a.g.T * a.g.C * 3 * sizeof(KV);
   // the backward kernel's registers (up to 255 per thread) allow 8 warps per SM
-  return launch_planned<SeqBwdArgs, BwdKern, BwdKern>(d, a, 3, sizeof(float), input_bytes, 8, s);
+  return launch_planned<SeqBwdArgs, BwdKern<KV>::template At, BwdKern<KV>::template At>(d, a, 3, sizeof(KV),
+                                                                                      input_bytes, 8, s);
+}
+
+cudaError_t launch_seq_backward(SeqBwdArgs& a, int kv_dtype, cudaStream_t s) {
+  return kv_dtype == 0 ? launch_seq_bwd_t<float>(a, s) : launch_seq_bwd_t<__nv_bfloat16>(a, s);
 }
 
 }  // namespace wkv

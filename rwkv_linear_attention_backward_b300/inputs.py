@@ -21,6 +21,8 @@ l169m      fwd+bwd fp32, B=8 T=1024 C=768 (one layer of a 169M RWKV-4);
 l1b5       fwd+bwd fp32, B=16 T=4096 C=2048 (1.5B-class layer); as l169m
 long       fwd only, bf16 k,v, fp32 state and output, B=1 T=131072
            C=2560; k ~ N(0,5^2), v ~ N(0,1); d ~ U(-8,1); u ~ U(-1,1)
+l169m_bf16 fwd+bwd with bf16 k, v, gy (fp32 arithmetic and outputs), the
+           l169m shape and distributions
 decode     RNN decode, L=32 layers, B=256, C=4096, 1024 steps; x, x_prev,
            r, k, v ~ N(0,1); mu_k, mu_v, mu_r ~ U(0,1); d ~ U(-6,2),
            u ~ U(-1,1) per layer; state starts at (0, 0, -1e38)
@@ -72,6 +74,7 @@ WORKLOADS = {
     "l169m": TrainingWorkload("l169m", 8, 1024, 768, 3.0, -6.0, 2.0, "f32", True, 1002),
     "l1b5": TrainingWorkload("l1b5", 16, 4096, 2048, 3.0, -6.0, 2.0, "f32", True, 1003),
     "long": TrainingWorkload("long", 1, 131072, 2560, 5.0, -8.0, 1.0, "bf16", False, 1004),
+    "l169m_bf16": TrainingWorkload("l169m_bf16", 8, 1024, 768, 3.0, -6.0, 2.0, "bf16", True, 1006),
 }
 DECODE = DecodeWorkload("decode", 32, 256, 4096, 1024, -6.0, 2.0, 1005)
 
@@ -89,8 +92,8 @@ def training_inputs(B: int, T: int, C: int, *, seed: int, k_std: float = 1.0, d_
     Draw order: d [C], u [C], k [B,T,C], v [B,T,C], gy [B,T,C].
     w = exp(d) in fp32 (the decay is handed to the operator directly).
     ``k_shift`` adds a constant to every k after drawing (used by the
-    shift-invariance checks).  k and v are rounded to bf16 when
-    ``kv_dtype == "bf16"``; w, u and gy stay fp32.
+    shift-invariance checks).  k, v and gy are rounded to bf16 when
+    ``kv_dtype == "bf16"``; w and u stay fp32.
     """
     g = _gen(seed)
     d = torch.rand(C, generator=g, dtype=torch.float32) * (d_hi - d_lo) + d_lo
@@ -104,6 +107,7 @@ def training_inputs(B: int, T: int, C: int, *, seed: int, k_std: float = 1.0, d_
     if kv_dtype == "bf16":
         k = k.to(torch.bfloat16)
         v = v.to(torch.bfloat16)
+        gy = gy.to(torch.bfloat16)
     elif kv_dtype != "f32":
         raise ValueError(f"kv_dtype must be 'f32' or 'bf16', got {kv_dtype!r}")
     return w, u, k, v, gy

@@ -111,7 +111,14 @@ def _bwd(lib, B=2, T=40, C=64, dtype=0, ws=FAKE, wsb=None, **nulls):
 def test_backward_rejects_before_launch(lib):
     assert _bwd(lib, C=0) == 1
     assert _bwd(lib, dtype=5) == 1
-    assert _bwd(lib, dtype=1) == 2  # bf16 backward: valid request, not implemented
+    # bf16 inputs while the chunked scan (fp32 only) is forced: refused before
+    # any launch (a bf16 call in the default mode is valid and would launch,
+    # which this host test never does)
+    lib.wkv_debug_set_scan_mode(1)
+    try:
+        assert _bwd(lib, dtype=1) == 2
+    finally:
+        lib.wkv_debug_set_scan_mode(0)
     for name in ("w", "u", "k", "v", "gy", "gw", "gu", "gk", "gv"):
         assert _bwd(lib, **{name: NULL}) == 1
     assert _bwd(lib, wsb=256) == 4

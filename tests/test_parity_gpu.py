@@ -109,6 +109,46 @@ def test_bf16_forward(oracle, wkv, scan_mode):
     assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "bf16 y (fp32-level)")
 
 
+BF16_SHAPES = [(1, 1, 8), (2, 33, 136), (3, 200, 96), (1, 1000, 40), (2, 513, 384)]
+
+
+@pytest.mark.parametrize("B,T,C", BF16_SHAPES, ids=[f"B{b}T{t}C{c}" for b, t, c in BF16_SHAPES])
+def test_bf16_backward(oracle, wkv, scan_mode, B, T, C):
+    """bf16 k, v, gy with fp32 arithmetic and fp32 gradients: the oracle sees
+    the same rounded inputs, so the gradients meet the fp32 tolerance.  The
+    chunked scan takes fp32 inputs only and refuses before launching."""
+    w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=400 + B + T + C, k_std=3.0, kv_dtype="bf16")
+    if scan_mode == "chunked":
+        with pytest.raises(wkv.WKVError) as exc:
+            wkv.backward(*cuda(w, u, k, v, gy))
+        assert exc.value.status == 2
+        return
+    for use_ckpt in (True, False):
+        y, ckpt, gw, gu, gk, gv = run_fwd_bwd(wkv, w, u, k, v, gy, use_ckpt=use_ckpt)
+        ow, ou, ok, ov = oracle.backward_adjoint(w, u, k, v, gy)
+        what = f"bf16 ckpt={use_ckpt}"
+        assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, f"{what} y")
+        assert_close(gk, ok, TOL_GRAD, f"{what} gk")
+        assert_close(gv, ov, TOL_GRAD, f"{what} gv")
+        assert_close(gw, ow, TOL_GRAD, f"{what} gw")
+        assert_close(gu, ou, TOL_GRAD, f"{what} gu")
+
+
+def test_bf16_backward_agrees_with_fp32_of_rounded_inputs(wkv):
+    """The bf16 call equals the fp32 call on the same rounded values bit for
+    bit: the only difference is the staged type, and widening bf16 to fp32
+    is exact (one run per column, so both calls split the columns alike)."""
+    w, u, k, v, gy = inputs.training_inputs(4, 600, 256, seed=410, k_std=3.0, kv_dtype="bf16")
+    try:
+        wkv.set_max_runs(1)
+        a = run_fwd_bwd(wkv, w, u, k, v, gy)
+        b = run_fwd_bwd(wkv, w, u, k.float(), v.float(), gy.float())
+    finally:
+        wkv.set_max_runs(0)
+    for x, y_, n in zip(a, b, ("y", "ckpt", "gw", "gu", "gk", "gv")):
+        assert torch.equal(x, y_), n
+
+
 def _both_modes(wkv, w, u, k, v, gy, max_runs=0):
     res = {}
     try:
@@ -197,3 +237,7 @@ def test_workload_l1b5_sampled(oracle, wkv):
 
 def test_workload_long_sampled(oracle, wkv):
     _sampled(oracle, wkv, "long", 48, 12)
+
+
+def test_workload_l169m_bf16_sampled(oracle, wkv):
+    _sampled(oracle, wkv, "l169m_bf16", 48, 13)
