@@ -47,6 +47,8 @@ class Oracle:
             "wkv_oracle_forward_direct": [i, i, i, p, p, p, p, p],
             "wkv_oracle_forward_recurrent": [i, i, i, p, p, p, p, p],
             "wkv_oracle_forward_state": [i, i, i] + [p] * 11,
+            "wkv_oracle_token_shift": [i, i, i] + [p] * 8,
+            "wkv_oracle_token_shift_backward": [i, i, i] + [p] * 13,
             "wkv_oracle_backward_adjoint": [i, i, i, p, p, p, p, p, p, p, p, p],
             "wkv_oracle_backward_direct": [i, i, i, p, p, p, p, p, p, p, p, p],
             "wkv_oracle_state": [i, i, i, p, p, p, i, p, p, p],
@@ -108,6 +110,29 @@ class Oracle:
         out = tuple(np.empty((B, C)) for _ in range(3))
         self._lib.wkv_oracle_forward_state(B, T, C, *map(self._ptr, (w, u, k, v) + sin + (y,) + out))
         return y, out
+
+    # ---------------------------------------------------------- token shift
+    def token_shift(self, x, x0, mu_k, mu_v, mu_r):
+        """(xk, xv, xr) of x [B, T, C]; x0 [B, C] is the token before the
+        sequence (None: zeros)."""
+        x, mu_k, mu_v, mu_r = map(self._in, (x, mu_k, mu_v, mu_r))
+        x0 = None if x0 is None else self._in(x0)
+        B, T, C = x.shape
+        outs = tuple(np.empty_like(x) for _ in range(3))
+        self._lib.wkv_oracle_token_shift(B, T, C, *map(self._ptr, (x, x0, mu_k, mu_v, mu_r) + outs))
+        return outs
+
+    def token_shift_backward(self, x, x0, mu_k, mu_v, mu_r, gxk, gxv, gxr):
+        """(gx, gx0, gmu_k, gmu_v, gmu_r); gx0 is None when x0 is None."""
+        x, mu_k, mu_v, mu_r, gxk, gxv, gxr = map(self._in, (x, mu_k, mu_v, mu_r, gxk, gxv, gxr))
+        x0 = None if x0 is None else self._in(x0)
+        B, T, C = x.shape
+        gx = np.empty_like(x)
+        gx0 = None if x0 is None else np.empty((B, C))
+        gm = tuple(np.empty(C) for _ in range(3))
+        self._lib.wkv_oracle_token_shift_backward(
+            B, T, C, *map(self._ptr, (x, x0, mu_k, mu_v, mu_r, gxk, gxv, gxr, gx, gx0) + gm))
+        return (gx, gx0) + gm
 
     # ------------------------------------------------------------- backward
     def _backward(self, fn, w, u, k, v, gy):

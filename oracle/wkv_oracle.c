@@ -357,3 +357,63 @@ void wkv_oracle_decode_step(int L, int B, int C, const double *x, const double *
                 pp[o] = pp2;
             }
 }
+
+/* Token shift of the training path, eq. (7) of "RWKV解读" section
+ * "3、RWKV的网络架构" (the input of each projection is a weighted sum of the
+ * current and the previous token; segmentfault and "Инновационная
+ * архитектура RWKV", "Механизмы взаимодействия"): per (b, t, c), with
+ * x_{-1} = x0 (the last token before the sequence, [B, C]; NULL: zeros),
+ *     xk_t = mu_k x_t + (1 - mu_k) x_{t-1}   (xv, xr with mu_v, mu_r).
+ * Backward, given gxk, gxv, gxr [B, T, C]: each x_t feeds its own mixes
+ * with weight mu and the next token's with weight 1 - mu, so
+ *     gx_t  = sum_m mu_m gxm_t + (1 - mu_m) gxm_{t+1}   (no t+1 term at T-1)
+ *     gx0   = sum_m (1 - mu_m) gxm_0                    ([B, C], may be NULL)
+ *     gmu_m = sum_{b,t} gxm_t (x_t - x_{t-1})           ([C]). */
+void wkv_oracle_token_shift(int B, int T, int C, const double *x, const double *x0, const double *mu_k,
+                            const double *mu_v, const double *mu_r, double *xk, double *xv, double *xr)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int c = 0; c < C; ++c)
+            for (int t = 0; t < T; ++t) {
+                double cur = x[IDX(b, t, c)];
+                double prev = t > 0 ? x[IDX(b, t - 1, c)] : (x0 ? x0[(size_t)b * C + c] : 0.0);
+                xk[IDX(b, t, c)] = mu_k[c] * cur + (1.0 - mu_k[c]) * prev;
+                xv[IDX(b, t, c)] = mu_v[c] * cur + (1.0 - mu_v[c]) * prev;
+                xr[IDX(b, t, c)] = mu_r[c] * cur + (1.0 - mu_r[c]) * prev;
+            }
+}
+
+void wkv_oracle_token_shift_backward(int B, int T, int C, const double *x, const double *x0,
+                                     const double *mu_k, const double *mu_v, const double *mu_r,
+                                     const double *gxk, const double *gxv, const double *gxr, double *gx,
+                                     double *gx0, double *gmu_k, double *gmu_v, double *gmu_r)
+{
+#pragma omp parallel for schedule(static)
+    for (int c = 0; c < C; ++c) {
+        double sk = 0.0, sv = 0.0, sr = 0.0;
+        for (int b = 0; b < B; ++b)
+            for (int t = 0; t < T; ++t) {
+                size_t i = IDX(b, t, c);
+                double g = mu_k[c] * gxk[i] + mu_v[c] * gxv[i] + mu_r[c] * gxr[i];
+                if (t + 1 < T) {
+                    size_t n = IDX(b, t + 1, c);
+                    g += (1.0 - mu_k[c]) * gxk[n] + (1.0 - mu_v[c]) * gxv[n] + (1.0 - mu_r[c]) * gxr[n];
+                }
+                gx[i] = g;
+                double prev = t > 0 ? x[IDX(b, t - 1, c)] : (x0 ? x0[(size_t)b * C + c] : 0.0);
+                double d = x[i] - prev;
+                sk += gxk[i] * d;
+                sv += gxv[i] * d;
+                sr += gxr[i] * d;
+            }
+        gmu_k[c] = sk;
+        gmu_v[c] = sv;
+        gmu_r[c] = sr;
+        if (gx0)
+            for (int b = 0; b < B; ++b) {
+                size_t i = IDX(b, 0, c);
+                gx0[(size_t)b * C + c] = (1.0 - mu_k[c]) * gxk[i] + (1.0 - mu_v[c]) * gxv[i] + (1.0 - mu_r[c]) * gxr[i];
+            }
+    }
+}

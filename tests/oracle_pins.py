@@ -281,6 +281,54 @@ def pin_forward_state_split(o):
     _close(sb[2], p_all, 1e-13, 1e-13, "chained state pp")
 
 
+def pin_token_shift(o):
+    """mu = 1 keeps the current token, mu = 0 takes the previous one (the
+    given x0 before the first), and the mix is the decode step's (which its
+    own pins tie to the definition); the backward matches central finite
+    differences of sum(g * mix) in x, x0 and every mu."""
+    r = _rng(80)
+    B, T, C = 2, 9, 3
+    x = r.normal(0, 1, (B, T, C))
+    x0 = r.normal(0, 1, (B, C))
+    one, zero = np.ones(C), np.zeros(C)
+    xk, xv, xr = o.token_shift(x, x0, one, zero, one)
+    _close(xk, x, 0, 0, "mu=1 keeps x_t")
+    prev = np.concatenate([x0[:, None], x[:, :-1]], axis=1)
+    _close(xv, prev, 0, 0, "mu=0 takes x_{t-1}")
+    _close(o.token_shift(x, None, zero, zero, zero)[0][:, 0], np.zeros((B, C)), 0, 0, "no x0: zeros")
+    mk, mv, mr = (r.uniform(0, 1, C) for _ in range(3))
+    xk, xv, xr = o.token_shift(x, x0, mk, mv, mr)
+    for t in range(T):  # the decode step's mix of (x_t, x_{t-1}) for one layer
+        p = prev[:, t]
+        y, _, _, _, dk, dv, dr = o.decode_step(x[None, :, t], p[None], mk[None], mv[None], mr[None],
+                                               np.zeros((1, B, C)), np.zeros((1, B, C)), np.zeros((1, B, C)),
+                                               np.ones((1, C)), np.zeros((1, C)), np.zeros((1, B, C)),
+                                               np.zeros((1, B, C)), np.full((1, B, C), -1e38))
+        _close(dk[0], xk[:, t], 1e-15, 1e-15, "shift vs decode mix k")
+        _close(dv[0], xv[:, t], 1e-15, 1e-15, "shift vs decode mix v")
+        _close(dr[0], xr[:, t], 1e-15, 1e-15, "shift vs decode mix r")
+    g = [r.normal(0, 1, (B, T, C)) for _ in range(3)]
+    gx, gx0, gmk, gmv, gmr = o.token_shift_backward(x, x0, mk, mv, mr, *g)
+
+    def loss(x_, x0_, mk_, mv_, mr_):
+        outs = o.token_shift(x_, x0_, mk_, mv_, mr_)
+        return sum(float(np.sum(gi * oi)) for gi, oi in zip(g, outs))
+
+    h = 1e-6
+    for arr, grad, name in ((x, gx, "x"), (x0, gx0, "x0"), (mk, gmk, "mu_k"), (mv, gmv, "mu_v"), (mr, gmr, "mu_r")):
+        flat = arr.reshape(-1)
+        num = np.empty_like(flat)
+        for i in range(flat.size):
+            keep = flat[i]
+            flat[i] = keep + h
+            lp = loss(x, x0, mk, mv, mr)
+            flat[i] = keep - h
+            lm = loss(x, x0, mk, mv, mr)
+            flat[i] = keep
+            num[i] = (lp - lm) / (2 * h)
+        _close(grad.reshape(-1), num, 1e-6, 1e-7, f"token shift d/d{name}")
+
+
 def pin_decode_hand_values(o):
     for case in GOLDEN["decode"]:
         for s in case["steps"]:
@@ -344,6 +392,7 @@ ALL_PINS = [
     pin_backward_forms_agree,
     pin_backward_identities,
     pin_forward_state_split,
+    pin_token_shift,
     pin_state_definition,
     pin_decode_hand_values,
     pin_decode_matches_forward,

@@ -54,6 +54,13 @@ MUTANTS = [
      "double dp = exp(M - w[c] - m2)", "double dp = exp(M - m2)"),
     ("state_in_scale_ignored", "wkv_oracle_forward_state",
      "double sp = exp(M - q), sc", "double sp = exp(-q), sc"),
+    ("shift_mix_transposed", "wkv_oracle_token_shift",
+     "xk[IDX(b, t, c)] = mu_k[c] * cur + (1.0 - mu_k[c]) * prev;",
+     "xk[IDX(b, t, c)] = mu_k[c] * prev + (1.0 - mu_k[c]) * cur;"),
+    ("shift_grad_misses_next_token", "wkv_oracle_token_shift_backward",
+     "g += (1.0 - mu_k[c]) * gxk[n] +", "g += 0.0 * gxk[n] +"),
+    ("shift_grad_mu_sign", "wkv_oracle_token_shift_backward",
+     "double d = x[i] - prev;", "double d = prev - x[i];"),
 ]
 
 
