@@ -44,6 +44,7 @@ sys.path.insert(0, str(ROOT))
 METRIC = "WKV fwd+bwd B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
 METRIC_FWD = "WKV forward B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
 METRIC_DEC = "WKV decode step L·B·C elements/s and achieved HBM GB/s fraction on 1 B300"
+METRIC_SHIFT = "token shift fwd+bwd B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
 
 # Algorithmic HBM bytes per element (what the method must move with the
 # separate forward / backward calls; O(1/chunk) checkpoint and workspace
@@ -53,6 +54,8 @@ BYTES_FWD_BF16 = 8   # read bf16 k, v; write fp32 y
 BYTES_BWD = 20       # read k, v, gy; write gk, gv
 BYTES_BWD_BF16 = 14  # read bf16 k, v, gy; write fp32 gk, gv
 BYTES_DECODE = 60    # read x, x_prev, r, k, v; read+write num, den, pp; write y, xk, xv, xr
+BYTES_SHIFT_FWD = 16  # read x; write xk, xv, xr
+BYTES_SHIFT_BWD = 20  # read x, gxk, gxv, gxr; write gx
 
 REJECT_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
@@ -62,7 +65,8 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default depends on the workload)")
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="l169m", choices=["tiny", "l169m", "l1b5", "long", "l169m_bf16", "decode"])
+    ap.add_argument("--workload", default="l169m", choices=["tiny", "l169m", "l1b5", "long", "l169m_bf16", "decode",
+                                                              "shift"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -76,7 +80,8 @@ def parse_args(argv=None):
     return args
 
 
-DEFAULT_STEPS = {"tiny": 2000, "l169m": 4000, "l1b5": 200, "long": 200, "l169m_bf16": 4000, "decode": 256}
+DEFAULT_STEPS = {"tiny": 2000, "l169m": 4000, "l1b5": 200, "long": 200, "l169m_bf16": 4000, "decode": 256,
+                 "shift": 200}
 
 
 # ------------------------------------------------------------------ ranks
@@ -424,6 +429,68 @@ class DecodeRun:
         self.pin_out[0].copy_(y, non_blocking=True)
 
 
+class ShiftRun:
+    """A step is the token shift's forward and backward calls (the training
+    path's mix of each token with the previous one)."""
+
+    def __init__(self, device):
+        import torch
+        from rwkv_linear_attention_backward_b300 import binding, inputs
+
+        self.torch, self.wkv = torch, binding
+        S = inputs.SHIFT
+        self.S = S
+        B, T, C = S.B, S.T, S.C
+        self.elements = S.elements
+        self.host = inputs.shift_inputs(B, T, C, seed=S.seed)
+        self.dev = tuple(t.to(device).contiguous() for t in self.host)
+        self.out = tuple(torch.empty(B, T, C, device=device) for _ in range(3))
+        self.ws = binding.Workspace(binding._lib.wkv_token_shift_backward_workspace_bytes(B, T, C), device)
+        self.bytes_fwd = BYTES_SHIFT_FWD * self.elements
+        self.bytes_bwd = BYTES_SHIFT_BWD * self.elements
+        self.launches_per_step = 3
+        self.dominant = "shift_bwd_kernel"
+        self.dominant_bytes = self.bytes_bwd
+
+    def _forward(self):
+        x, x0, mk, mv, mr = self.dev[:5]
+        self.wkv.token_shift(x, x0, mk, mv, mr, xk=self.out[0], xv=self.out[1], xr=self.out[2])
+
+    def _backward(self):
+        return self.wkv.token_shift_backward(*self.dev, workspace=self.ws)
+
+    def step(self, ev=None):
+        self._forward()
+        if ev is not None:
+            ev[0].record()
+        self._backward()
+        if ev is not None:
+            ev[1].record()
+
+    step_dominant_events = step
+
+    def capture(self):
+        pass  # two API calls per step
+
+    def check(self):
+        pass
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.pin_in = tuple(t.pin_memory() for t in self.host)
+        self.pin_out = tuple(torch.empty(self.S.B, self.S.T, self.S.C, pin_memory=True) for _ in range(4))
+        self.h2d = sum(t.numel() * t.element_size() for t in self.pin_in)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out)
+
+    def e2e_step(self):
+        for d, h in zip(self.dev, self.pin_in):
+            d.copy_(h, non_blocking=True)
+        self._forward()
+        gx = self._backward()[0]
+        for h, d in zip(self.pin_out, self.out + (gx,)):
+            h.copy_(d, non_blocking=True)
+
+
 # --------------------------------------------------------------- ours: run
 def time_steps(run, steps: int, flush, stream):
     """Per-step device times (s) of `steps` steps, L2 flushed before each;
@@ -469,6 +536,8 @@ def cpu_baseline(workload: str, target_s: float = 12.0):
         return {"value": done / el, "unit": "elements/s", "cores": o.num_threads(), "kind": "oracle",
                 "sample": f"decode step on batch rows 0..{rows - 1} of {B} (all {L} layers, all {C} channels), "
                           f"{steps} steps in {el:.1f} s"}
+    if workload == "shift":
+        return _shift_oracle_timing(o, target_s)
     wl = inputs.WORKLOADS[workload]
     w, u, k, v, gy = inputs.workload_inputs(workload)
     C = wl.C
@@ -491,6 +560,27 @@ def cpu_baseline(workload: str, target_s: float = 12.0):
     what = "recurrent forward + adjoint backward" if wl.backward else "recurrent forward"
     return {"value": done / el, "unit": "elements/s", "cores": o.num_threads(), "kind": "oracle",
             "sample": f"{what} on {len(cs)} of {C} channels (all B={wl.B}, T={wl.T}), {reps} pass(es) in {el:.1f} s"}
+
+
+def _shift_oracle_timing(o, target_s):
+    """The oracle's token shift forward + backward on batch row 0 of the
+    shift workload, repeated for about target_s."""
+    from rwkv_linear_attention_backward_b300 import inputs
+
+    S = inputs.SHIFT
+    x, x0, mk, mv, mr, gk, gv, gr = (t.numpy() for t in inputs.shift_inputs(1, S.T, S.C, seed=S.seed))
+    reps, done, t0 = 0, 0, time.perf_counter()
+    while True:
+        o.token_shift(x, x0, mk, mv, mr)
+        o.token_shift_backward(x, x0, mk, mv, mr, gk, gv, gr)
+        reps += 1
+        done += S.T * S.C
+        if time.perf_counter() - t0 >= target_s or reps >= 200:
+            break
+    el = time.perf_counter() - t0
+    return {"value": done / el, "unit": "elements/s", "cores": o.num_threads(), "kind": "oracle",
+            "sample": f"token shift forward + backward on one batch row (T={S.T}, C={S.C}) of {S.B}, "
+                      f"{reps} pass(es) in {el:.1f} s"}
 
 
 def _oracle_pass(o, wl, w, u, k, v, gy, cs):
@@ -519,7 +609,12 @@ def run_ours(args):
 
         binding.set_scan_mode(args.scan_mode)
     steps = args.steps or DEFAULT_STEPS[args.workload]
-    run = DecodeRun(device) if args.workload == "decode" else TrainingRun(args.workload, device)
+    if args.workload == "decode":
+        run = DecodeRun(device)
+    elif args.workload == "shift":
+        run = ShiftRun(device)
+    else:
+        run = TrainingRun(args.workload, device)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     scratch = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
@@ -559,20 +654,23 @@ def run_ours(args):
     dom_avg = sum(dom_s) / len(dom_s)
     achieved = run.dominant_bytes / dom_avg / 1e9
     step_bytes = run.bytes_fwd + run.bytes_bwd
-    wl_cfg = ({"workload": "decode", "L": run.D.L, "B": run.D.B, "C": run.D.C, "state": "fp32"}
-              if args.workload == "decode" else
-              {"workload": args.workload, "B": run.wl.B, "T": run.wl.T, "C": run.wl.C, "kv_dtype": run.wl.kv_dtype,
-               "pass": "forward+backward" if run.wl.backward else "forward"})
-    wl_cfg.update({"launch": "api calls per step" if (args.no_graph or args.workload == "decode") else
+    if args.workload == "decode":
+        wl_cfg = {"workload": "decode", "L": run.D.L, "B": run.D.B, "C": run.D.C, "state": "fp32"}
+    elif args.workload == "shift":
+        wl_cfg = {"workload": "shift", "B": run.S.B, "T": run.S.T, "C": run.S.C, "pass": "forward+backward"}
+    else:
+        wl_cfg = {"workload": args.workload, "B": run.wl.B, "T": run.wl.T, "C": run.wl.C,
+                  "kv_dtype": run.wl.kv_dtype, "pass": "forward+backward" if run.wl.backward else "forward"}
+    wl_cfg.update({"launch": "api calls per step" if (args.no_graph or args.workload in ("decode", "shift")) else
                    "CUDA graphs of the forward and backward calls, captured once and replayed per step",
                    "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}",
                    "scan_mode": args.scan_mode,
                    "strategy": getattr(run, "strategy", "n/a"),
                    "checkpoints": "forward writes chunk checkpoints, backward reads them"
-                   if args.workload != "decode" else "n/a"})
+                   if args.workload not in ("decode", "shift") else "n/a"})
+    metric = {"long": METRIC_FWD, "decode": METRIC_DEC, "shift": METRIC_SHIFT}.get(args.workload, METRIC)
     out = {
-        "metric": METRIC if args.workload not in ("long", "decode") else (METRIC_FWD if args.workload == "long"
-                                                                           else METRIC_DEC),
+        "metric": metric,
         "value": value,
         "unit": "elements/s",
         "n_gpus": world,
@@ -670,6 +768,17 @@ def run_reference(args):
 
         sample = f"decode step on batch rows 0..{rows - 1} of {B} (all {L} layers, {C} channels)"
         metric = METRIC_DEC
+    elif args.workload == "shift":
+        S = inputs.SHIFT
+        x, x0, mk, mv, mr, gk, gv, gr = (t.numpy() for t in inputs.shift_inputs(1, S.T, S.C, seed=S.seed))
+
+        def one():
+            o.token_shift(x, x0, mk, mv, mr)
+            o.token_shift_backward(x, x0, mk, mv, mr, gk, gv, gr)
+            return S.T * S.C
+
+        sample = f"token shift forward + backward on one batch row (T={S.T}, C={S.C}) of {S.B}"
+        metric = METRIC_SHIFT
     else:
         wl = inputs.WORKLOADS[args.workload]
         w, u, k, v, gy = inputs.workload_inputs(args.workload)
@@ -693,9 +802,13 @@ def run_reference(args):
     done = sum(one() for _ in range(steps))
     el = time.perf_counter() - t0
     value = done / el
-    cfg = ({"workload": args.workload} if args.workload == "decode" else
-           {"workload": args.workload, "B": inputs.WORKLOADS[args.workload].B,
-            "T": inputs.WORKLOADS[args.workload].T, "C": inputs.WORKLOADS[args.workload].C})
+    if args.workload == "decode":
+        cfg = {"workload": args.workload}
+    elif args.workload == "shift":
+        cfg = {"workload": "shift", "B": inputs.SHIFT.B, "T": inputs.SHIFT.T, "C": inputs.SHIFT.C}
+    else:
+        cfg = {"workload": args.workload, "B": inputs.WORKLOADS[args.workload].B,
+               "T": inputs.WORKLOADS[args.workload].T, "C": inputs.WORKLOADS[args.workload].C}
     out = {
         "impl": "reference",
         "metric": metric,

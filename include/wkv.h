@@ -198,6 +198,46 @@ wkv_status wkv_decode_step(int L, int B, int C, const float* x, const float* x_p
                            float* xv, float* xr, void* stream);
 
 /*
+ * wkv_token_shift -- the token shift of the training path, eq. (7) of
+ * "RWKV解读" section "3、RWKV的网络架构": the input of each projection is
+ * a weighted sum of the current and the previous token.  Per (b, t, c),
+ * with x_{-1} = x0[b, c] (zeros when x0 is NULL):
+ *     xk = mu_k x_t + (1 - mu_k) x_{t-1},  xv, xr alike with mu_v, mu_r.
+ *   x                [B, T, C] input; x0 [B, C] or NULL (the token before
+ *                    the sequence, e.g. the last token of the previous
+ *                    segment).
+ *   mu_k, mu_v, mu_r [C] mix vectors.
+ *   xk, xv, xr       [B, T, C] outputs, all required (written in one pass
+ *                    over x).
+ * 16-byte aligned tensors with C % 4 == 0 take a vectorised path.
+ * Errors: WKV_ERR_INVALID_ARG (a size <= 0, B*T*C >= 2^40, a required
+ * pointer NULL), WKV_ERR_CUDA.
+ */
+wkv_status wkv_token_shift(int B, int T, int C, const float* x, const float* x0, const float* mu_k,
+                           const float* mu_v, const float* mu_r, float* xk, float* xv, float* xr, void* stream);
+
+/* Workspace bytes of wkv_token_shift_backward (per-slice partial sums);
+ * 0 for invalid sizes. */
+size_t wkv_token_shift_backward_workspace_bytes(int B, int T, int C);
+
+/*
+ * wkv_token_shift_backward -- gradients of sum(gxk xk + gxv xv + gxr xr)
+ * for wkv_token_shift's inputs:
+ *     gx_t  = sum_m mu_m gxm_t + (1 - mu_m) gxm_{t+1}   (no t+1 term at T-1)
+ *     gx0   = sum_m (1 - mu_m) gxm_0                     [B, C], may be NULL
+ *     gmu_m = sum_{b,t} gxm_t (x_t - x_{t-1})            [C]
+ *   gx [B, T, C] and gmu_k, gmu_v, gmu_r [C] are required outputs
+ *   (overwritten); the gmu sums are in a fixed order (bitwise reproducible).
+ *   workspace  at least wkv_token_shift_backward_workspace_bytes(B, T, C)
+ *              bytes of device memory (no initialisation needed).
+ * Errors: as wkv_token_shift, plus WKV_ERR_WORKSPACE.
+ */
+wkv_status wkv_token_shift_backward(int B, int T, int C, const float* x, const float* x0, const float* mu_k,
+                                    const float* mu_v, const float* mu_r, const float* gxk, const float* gxv,
+                                    const float* gxr, float* gx, float* gx0, float* gmu_k, float* gmu_v,
+                                    float* gmu_r, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * wkv_forward_noalloc -- wkv_forward without a caller-provided workspace.
  * The pages have no counterpart: this entry point exists for callers that
  * cannot call cudaMalloc, such as a plugin or embedded host whose device

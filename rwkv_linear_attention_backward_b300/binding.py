@@ -49,6 +49,9 @@ _SIGNATURES = {
     "wkv_scan_strategy": ([_i, _i, _i], _i),
     "wkv_debug_set_max_runs": ([_i], _i),
     "wkv_debug_set_chain_len": ([_i], _i),
+    "wkv_token_shift": ([_i, _i, _i] + [_vp] * 8 + [_vp], _i),
+    "wkv_token_shift_backward_workspace_bytes": ([_i, _i, _i], _sz),
+    "wkv_token_shift_backward": ([_i, _i, _i] + [_vp] * 13 + [_vp, _sz, _vp], _i),
 }
 for _name, (_args, _res) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -210,6 +213,47 @@ def forward_with_state(w, u, k, v, state_in=None, *, y=None, state_out=None, ckp
     _check(_lib.wkv_forward_with_state(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(state_in), _p(y), _p(state_out),
                                        _p(ckpt), ws.ptr(), ws.nbytes, _stream(stream)), "wkv_forward_with_state")
     return (y, state_out, ckpt) if ckpt is not None else (y, state_out)
+
+
+def token_shift(x, x0, mu_k, mu_v, mu_r, *, xk=None, xv=None, xr=None, stream=None):
+    """(xk, xv, xr) = mu x_t + (1 - mu) x_{t-1} for x [B, T, C] (fp32); x0
+    [B, C] is the token before the sequence (None: zeros)."""
+    B, T, C = x.shape
+    _need(x, "x")
+    if x0 is not None:
+        _need(x0, "x0", shape=(B, C))
+    for m, n in ((mu_k, "mu_k"), (mu_v, "mu_v"), (mu_r, "mu_r")):
+        _need(m, n, shape=(C,))
+    outs = []
+    for t, n in ((xk, "xk"), (xv, "xv"), (xr, "xr")):
+        t = torch.empty_like(x) if t is None else t
+        _need(t, n, shape=(B, T, C))
+        outs.append(t)
+    _check(_lib.wkv_token_shift(B, T, C, _p(x), _p(x0), _p(mu_k), _p(mu_v), _p(mu_r), *map(_p, outs),
+                                _stream(stream)), "wkv_token_shift")
+    return tuple(outs)
+
+
+def token_shift_backward(x, x0, mu_k, mu_v, mu_r, gxk, gxv, gxr, *, workspace: Workspace | None = None,
+                         stream=None):
+    """(gx, gx0, gmu_k, gmu_v, gmu_r) of token_shift; gx0 is None when x0 is."""
+    B, T, C = x.shape
+    _need(x, "x")
+    if x0 is not None:
+        _need(x0, "x0", shape=(B, C))
+    for m, n in ((mu_k, "mu_k"), (mu_v, "mu_v"), (mu_r, "mu_r")):
+        _need(m, n, shape=(C,))
+    for g, n in ((gxk, "gxk"), (gxv, "gxv"), (gxr, "gxr")):
+        _need(g, n, shape=(B, T, C))
+    gx = torch.empty_like(x)
+    gx0 = None if x0 is None else torch.empty_like(x0)
+    gm = tuple(torch.empty(C, dtype=torch.float32, device=x.device) for _ in range(3))
+    need = int(_lib.wkv_token_shift_backward_workspace_bytes(B, T, C))
+    ws = workspace or _workspace("shift", need, x.device)
+    _check(_lib.wkv_token_shift_backward(B, T, C, _p(x), _p(x0), _p(mu_k), _p(mu_v), _p(mu_r), _p(gxk), _p(gxv),
+                                         _p(gxr), _p(gx), _p(gx0), *map(_p, gm), ws.ptr(), ws.nbytes,
+                                         _stream(stream)), "wkv_token_shift_backward")
+    return (gx, gx0) + gm
 
 
 def forward_noalloc(w, u, k, v, *, y=None, ckpt=None, stream=None):

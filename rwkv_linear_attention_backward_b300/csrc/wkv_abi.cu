@@ -1,5 +1,6 @@
 // wkv_abi.cu -- the extern "C" boundary of libwkv.so (declared in
 // include/wkv.h): argument checks, workspace layout, launch plans.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <cudaTypedefs.h>
@@ -472,6 +473,74 @@ wkv_status wkv_decode_step(int L, int B, int C, const float* x, const float* x_p
                     al16(xk) && al16(xv) && al16(xr);
   cudaError_t e = launch_decode(a, vec4, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_decode_step");
+}
+
+size_t wkv_token_shift_backward_workspace_bytes(int B, int T, int C) {
+  if (B <= 0 || T <= 0 || C <= 0 || (double)B * T * C >= 1099511627776.0) return 0;
+  const bool vec4 = C % 4 == 0;  // the larger of the two slice counts
+  const int ns = std::max(shift_slices(B, T, C, vec4), shift_slices(B, T, C, false));
+  return std::max<size_t>(align256((size_t)ns * 3 * C * sizeof(float)), 256);
+}
+
+wkv_status wkv_token_shift(int B, int T, int C, const float* x, const float* x0, const float* mu_k,
+                           const float* mu_v, const float* mu_r, float* xk, float* xv, float* xr, void* stream) {
+  clear_error();
+  if (B <= 0 || T <= 0 || C <= 0 || (double)B * T * C >= 1099511627776.0) return WKV_ERR_INVALID_ARG;
+  if (!x || !mu_k || !mu_v || !mu_r || !xk || !xv || !xr) return WKV_ERR_INVALID_ARG;
+  ShiftArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.x = x;
+  a.x0 = x0;
+  a.mu_k = mu_k;
+  a.mu_v = mu_v;
+  a.mu_r = mu_r;
+  a.xk = xk;
+  a.xv = xv;
+  a.xr = xr;
+  a.B = B;
+  a.T = T;
+  a.C = C;
+  auto al16 = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const bool vec4 = C % 4 == 0 && al16(x) && al16(x0) && al16(mu_k) && al16(mu_v) && al16(mu_r) && al16(xk) &&
+                    al16(xv) && al16(xr);
+  cudaError_t e = launch_shift_forward(a, vec4, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_token_shift");
+}
+
+wkv_status wkv_token_shift_backward(int B, int T, int C, const float* x, const float* x0, const float* mu_k,
+                                    const float* mu_v, const float* mu_r, const float* gxk, const float* gxv,
+                                    const float* gxr, float* gx, float* gx0, float* gmu_k, float* gmu_v,
+                                    float* gmu_r, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  if (B <= 0 || T <= 0 || C <= 0 || (double)B * T * C >= 1099511627776.0) return WKV_ERR_INVALID_ARG;
+  if (!x || !mu_k || !mu_v || !mu_r || !gxk || !gxv || !gxr || !gx || !gmu_k || !gmu_v || !gmu_r)
+    return WKV_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < wkv_token_shift_backward_workspace_bytes(B, T, C)) return WKV_ERR_WORKSPACE;
+  ShiftArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.x = x;
+  a.x0 = x0;
+  a.mu_k = mu_k;
+  a.mu_v = mu_v;
+  a.mu_r = mu_r;
+  a.gxk = gxk;
+  a.gxv = gxv;
+  a.gxr = gxr;
+  a.gx = gx;
+  a.gx0 = gx0;
+  a.gmu_k = gmu_k;
+  a.gmu_v = gmu_v;
+  a.gmu_r = gmu_r;
+  a.part = static_cast<float*>(workspace);
+  a.B = B;
+  a.T = T;
+  a.C = C;
+  auto al16 = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const bool vec4 = C % 4 == 0 && al16(x) && al16(x0) && al16(mu_k) && al16(mu_v) && al16(mu_r) && al16(gxk) &&
+                    al16(gxv) && al16(gxr) && al16(gx) && al16(gx0);
+  a.nslice = shift_slices(B, T, C, vec4);
+  cudaError_t e = launch_shift_backward(a, vec4, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_token_shift_backward");
 }
 
 wkv_status wkv_debug_set_wait_budget_ns(long long ns) {

@@ -161,6 +161,21 @@ struct SeqBwdArgs {
 cudaError_t launch_seq_forward(SeqFwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
 cudaError_t launch_seq_backward(SeqBwdArgs& a, int kv_dtype, cudaStream_t s);
 
+// Token shift of the training path (wkv_shift.cu).
+struct ShiftArgs {
+  const float *x, *x0, *mu_k, *mu_v, *mu_r;  // x [B, T, C]; x0 [B, C] or null (zeros); mu [C]
+  float *xk, *xv, *xr;                        // forward outputs [B, T, C]
+  const float *gxk, *gxv, *gxr;               // backward inputs [B, T, C]
+  float *gx, *gx0, *gmu_k, *gmu_v, *gmu_r;    // backward outputs; gx0 may be null
+  float* part;                                // [nslice][3][C] per-slice gmu sums
+  int B, T, C, nslice;
+};
+
+// Row slices of the backward pass (a function of the shape only).
+int shift_slices(int B, int T, int C, bool vec4);
+cudaError_t launch_shift_forward(const ShiftArgs& a, bool vec4, cudaStream_t s);
+cudaError_t launch_shift_backward(const ShiftArgs& a, bool vec4, cudaStream_t s);
+
 // Grid of a persistent scan kernel: resident CTAs per SM x SMs, at most ntiles.
 cudaError_t launch_forward(FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
 cudaError_t launch_backward(BwdArgs& a, cudaStream_t s);

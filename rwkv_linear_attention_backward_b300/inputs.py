@@ -23,6 +23,8 @@ long       fwd only, bf16 k,v, fp32 state and output, B=1 T=131072
            C=2560; k ~ N(0,5^2), v ~ N(0,1); d ~ U(-8,1); u ~ U(-1,1)
 l169m_bf16 fwd+bwd with bf16 k, v, gy (fp32 arithmetic and outputs), the
            l169m shape and distributions
+shift      token shift of the training path, fwd+bwd, B=16 T=4096 C=2048;
+           x, gxk, gxv, gxr ~ N(0,1); x0 ~ N(0,1); mu_k, mu_v, mu_r ~ U(0,1)
 decode     RNN decode, L=32 layers, B=256, C=4096, 1024 steps; x, x_prev,
            r, k, v ~ N(0,1); mu_k, mu_v, mu_r ~ U(0,1); d ~ U(-6,2),
            u ~ U(-1,1) per layer; state starts at (0, 0, -1e38)
@@ -77,6 +79,36 @@ WORKLOADS = {
     "l169m_bf16": TrainingWorkload("l169m_bf16", 8, 1024, 768, 3.0, -6.0, 2.0, "bf16", True, 1006),
 }
 DECODE = DecodeWorkload("decode", 32, 256, 4096, 1024, -6.0, 2.0, 1005)
+
+
+@dataclass(frozen=True)
+class ShiftWorkload:
+    name: str
+    B: int
+    T: int
+    C: int
+    seed: int
+
+    @property
+    def elements(self) -> int:
+        return self.B * self.T * self.C
+
+
+SHIFT = ShiftWorkload("shift", 16, 4096, 2048, 1007)
+
+
+def shift_inputs(B: int, T: int, C: int, *, seed: int):
+    """Draw (x, x0, mu_k, mu_v, mu_r, gxk, gxv, gxr) on the CPU, fp32.
+
+    Draw order: x [B,T,C] ~ N(0,1), x0 [B,C] ~ N(0,1), mu_k, mu_v, mu_r [C]
+    ~ U(0,1), gxk, gxv, gxr [B,T,C] ~ N(0,1).
+    """
+    g = _gen(seed)
+    x = torch.randn(B, T, C, generator=g, dtype=torch.float32)
+    x0 = torch.randn(B, C, generator=g, dtype=torch.float32)
+    mus = [torch.rand(C, generator=g, dtype=torch.float32) for _ in range(3)]
+    gs = [torch.randn(B, T, C, generator=g, dtype=torch.float32) for _ in range(3)]
+    return (x, x0, *mus, *gs)
 
 
 def _gen(seed: int) -> torch.Generator:

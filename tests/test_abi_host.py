@@ -19,7 +19,8 @@ def lib():
     lib = ctypes.CDLL(str(path))
     lib.wkv_status_string.restype = ctypes.c_char_p
     lib.wkv_last_error_string.restype = ctypes.c_char_p
-    for n in ("wkv_checkpoint_floats", "wkv_forward_workspace_bytes", "wkv_backward_workspace_bytes"):
+    for n in ("wkv_checkpoint_floats", "wkv_forward_workspace_bytes", "wkv_backward_workspace_bytes",
+              "wkv_token_shift_backward_workspace_bytes"):
         getattr(lib, n).restype = ctypes.c_size_t
     return lib
 
@@ -131,3 +132,22 @@ def test_decode_rejects_before_launch(lib):
         a = list(args)
         a[i] = NULL
         assert lib.wkv_decode_step(2, 3, 4, *a, NULL) == 1
+
+
+def test_token_shift_rejects_before_launch(lib):
+    args = [FAKE] * 8  # x, x0, mu_k, mu_v, mu_r, xk, xv, xr
+    assert lib.wkv_token_shift(0, 4, 4, *args, NULL) == 1
+    assert lib.wkv_token_shift(2, 4, -1, *args, NULL) == 1
+    for i in (0, 2, 3, 4, 5, 6, 7):  # every pointer but x0 is required
+        a = list(args)
+        a[i] = NULL
+        assert lib.wkv_token_shift(2, 4, 4, *a, NULL) == 1
+    bargs = [FAKE] * 13  # x, x0, mu_k, mu_v, mu_r, gxk, gxv, gxr, gx, gx0, gmu_k, gmu_v, gmu_r
+    need = lib.wkv_token_shift_backward_workspace_bytes(2, 4, 4)
+    assert need > 0 and lib.wkv_token_shift_backward_workspace_bytes(0, 4, 4) == 0
+    for i in (0, 2, 3, 4, 5, 6, 7, 8, 10, 11, 12):  # x0 and gx0 may be NULL
+        a = list(bargs)
+        a[i] = NULL
+        assert lib.wkv_token_shift_backward(2, 4, 4, *a, FAKE, ctypes.c_size_t(need), NULL) == 1
+    assert lib.wkv_token_shift_backward(2, 4, 4, *bargs, NULL, ctypes.c_size_t(need), NULL) == 4
+    assert lib.wkv_token_shift_backward(2, 4, 4, *bargs, FAKE, ctypes.c_size_t(need - 1), NULL) == 4
