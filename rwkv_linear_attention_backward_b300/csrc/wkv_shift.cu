@@ -182,16 +182,20 @@ __global__ void __launch_bounds__(256) shift_reduce_kernel(const ShiftArgs a) {
   out[c] = s;
 }
 
+// CTAs for `items` work items of a grid-stride kernel: enough for the items,
+// at most 8 CTAs of 256 threads per SM of the current device.
 int grid_for(int64_t items, int threads) {
-  static int sms = 0;
+  static int sms_per_dev[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int sms = (dev >= 0 && dev < 64) ? sms_per_dev[dev] : 0;
   if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 148;
+    if (dev >= 0 && dev < 64) sms_per_dev[dev] = sms;
   }
   const int64_t want = (items + threads - 1) / threads;
-  const int64_t cap = (int64_t)sms * 8;  // 8 CTAs of 256 threads per SM
+  const int64_t cap = (int64_t)sms * 8;
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
