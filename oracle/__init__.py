@@ -53,6 +53,8 @@ class Oracle:
             "wkv_oracle_backward_direct": [i, i, i, p, p, p, p, p, p, p, p, p],
             "wkv_oracle_state": [i, i, i, p, p, p, i, p, p, p],
             "wkv_oracle_decode_step": [i, i, i] + [p] * 17,
+            "wkv_oracle_forward_gated": [i, i, i] + [p] * 6,
+            "wkv_oracle_backward_gated": [i, i, i] + [p] * 11,
         }
         for name, args in sigs.items():
             fn = getattr(self._lib, name)
@@ -110,6 +112,25 @@ class Oracle:
         out = tuple(np.empty((B, C)) for _ in range(3))
         self._lib.wkv_oracle_forward_state(B, T, C, *map(self._ptr, (w, u, k, v) + sin + (y,) + out))
         return y, out
+
+    # ------------------------------------------------------------ gated output
+    def forward_gated(self, w, u, k, v, r) -> np.ndarray:
+        """sigmoid(r) * wkv for k, v, r [B, T, C]."""
+        w, u, k, v, r = map(self._in, (w, u, k, v, r))
+        B, T, C = k.shape
+        out = np.empty_like(k)
+        self._lib.wkv_oracle_forward_gated(B, T, C, *map(self._ptr, (w, u, k, v, r, out)))
+        return out
+
+    def backward_gated(self, w, u, k, v, r, gout):
+        """(gw, gu, gk, gv, gr): gradients of sum(gout * sigmoid(r) * wkv)."""
+        w, u, k, v, r, gout = map(self._in, (w, u, k, v, r, gout))
+        B, T, C = k.shape
+        gw = np.empty(C)
+        gu = np.empty(C)
+        gk, gv, gr = (np.empty_like(k) for _ in range(3))
+        self._lib.wkv_oracle_backward_gated(B, T, C, *map(self._ptr, (w, u, k, v, r, gout, gw, gu, gk, gv, gr)))
+        return gw, gu, gk, gv, gr
 
     # ---------------------------------------------------------- token shift
     def token_shift(self, x, x0, mu_k, mu_v, mu_r):

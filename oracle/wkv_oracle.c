@@ -358,6 +358,45 @@ void wkv_oracle_decode_step(int L, int B, int C, const double *x, const double *
             }
 }
 
+/* The time-mixing output with its receptance gate, eq. (9) of "RWKV解读"
+ * section "3、RWKV的网络架构" (the wkv result is multiplied elementwise by
+ * sigmoid of the receptance r before the output projection): per (b, t, c)
+ *     out_t = sigmoid(r_t) wkv_t,   sigmoid(r) = 1 / (1 + e^{-r}),
+ * with wkv_t the direct sum of wkv_oracle_forward_direct.  r is [B, T, C]. */
+void wkv_oracle_forward_gated(int B, int T, int C, const double *w, const double *u, const double *k,
+                              const double *v, const double *r, double *out)
+{
+    wkv_oracle_forward_direct(B, T, C, w, u, k, v, out);
+    size_t n = (size_t)B * (size_t)T * (size_t)C;
+    for (size_t i = 0; i < n; ++i)
+        out[i] = out[i] / (1.0 + exp(-r[i]));
+}
+
+/* Gradients of sum(gout * out) for the gated output above.  wkv_t reaches
+ * the loss only through out_t, with factor sigmoid(r_t), so the gradient
+ * that enters the recurrence's reverse mode is gy_t = gout_t sigmoid(r_t)
+ * (giving gw, gu, gk, gv as wkv_oracle_backward_adjoint); and, from the
+ * derivative sigmoid'(r) = sigmoid(r) (1 - sigmoid(r)),
+ *     gr_t = gout_t wkv_t sigmoid(r_t) (1 - sigmoid(r_t)).
+ * wkv_t here comes from the recurrent form (wkv_oracle_forward_recurrent). */
+void wkv_oracle_backward_gated(int B, int T, int C, const double *w, const double *u, const double *k,
+                               const double *v, const double *r, const double *gout, double *gw,
+                               double *gu, double *gk, double *gv, double *gr)
+{
+    size_t n = (size_t)B * (size_t)T * (size_t)C;
+    double *y = (double *)malloc(sizeof(double) * n);
+    double *gy = (double *)malloc(sizeof(double) * n);
+    wkv_oracle_forward_recurrent(B, T, C, w, u, k, v, y);
+    for (size_t i = 0; i < n; ++i) {
+        double s = 1.0 / (1.0 + exp(-r[i]));
+        gy[i] = gout[i] * s;
+        gr[i] = gout[i] * y[i] * s * (1.0 - s);
+    }
+    wkv_oracle_backward_adjoint(B, T, C, w, u, k, v, gy, gw, gu, gk, gv);
+    free(y);
+    free(gy);
+}
+
 /* Token shift of the training path, eq. (7) of "RWKV解读" section
  * "3、RWKV的网络架构" (the input of each projection is a weighted sum of the
  * current and the previous token; segmentfault and "Инновационная

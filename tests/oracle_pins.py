@@ -377,6 +377,50 @@ def pin_decode_matches_forward(o):
         _close(den[l], d2, 1e-12, 1e-13, "decode den vs state")
 
 
+# --------------------------------------------------------------------------
+# the receptance gate on the output (eq. (9))
+# --------------------------------------------------------------------------
+def pin_gate_special_values(o):
+    """The gate at points where sigmoid is exact: 3/4 at ln 3, 1/2 at 0, 1/4
+    at -ln 3, and 1 to within e^{-40} at 40, applied to the ungated wkv
+    (pinned above).  At r = 40 the gradients are the ungated ones with
+    gy = gout, and gr vanishes with sigmoid'(40) < 5e-18."""
+    w, u, k, v, g = _rand_inputs(50, B=2, T=21, C=4, k_std=1.5)
+    y = o.forward_direct(w, u, k, v)
+    for rv, s in ((np.log(3.0), 0.75), (0.0, 0.5), (-np.log(3.0), 0.25), (40.0, 1.0)):
+        _close(o.forward_gated(w, u, k, v, np.full_like(k, rv)), s * y, 1e-14, 1e-15, f"gate at r={rv:.3f}")
+    gw, gu, gk, gv, gr = o.backward_gated(w, u, k, v, np.full_like(k, 40.0), g)
+    for got, want, n in zip((gw, gu, gk, gv), o.backward_adjoint(w, u, k, v, g), ("gw", "gu", "gk", "gv")):
+        _close(got, want, 1e-14, 1e-15, f"r=40 {n}")
+    assert np.all(np.abs(gr) <= 5e-18 * np.abs(g * y) + 1e-300), "r=40 gr"
+
+
+def pin_gate_finite_differences(o):
+    """Central differences of sum(gout * sigmoid(r) * wkv) in float64 on tiny
+    inputs give all five gradients of the gated backward pass."""
+    names = ("w", "u", "k", "v", "r")
+    for seed in (60, 61):
+        w, u, k, v, gout = _rand_inputs(seed, B=2, T=5, C=3, k_std=1.5)
+        r = _rng(seed + 100).normal(0, 1.5, k.shape)
+        params = dict(zip(names, (w, u, k, v, r)))
+
+        def loss(p):
+            return float(np.sum(gout * o.forward_gated(*(p[n] for n in names))))
+
+        got = dict(zip(names, o.backward_gated(w, u, k, v, r, gout)))
+        for name, arr in params.items():
+            fd = np.zeros_like(arr)
+            for idx in np.ndindex(arr.shape):
+                h = 1e-6 * max(1.0, abs(arr[idx]))
+                plus = {n: a.copy() for n, a in params.items()}
+                minus = {n: a.copy() for n, a in params.items()}
+                plus[name][idx] += h
+                minus[name][idx] -= h
+                fd[idx] = (loss(plus) - loss(minus)) / (2 * h)
+            scale = max(1.0, float(np.max(np.abs(fd))))
+            _close(got[name], fd, 0.0, 1e-7 * scale, f"gated FD g{name} seed {seed}")
+
+
 ALL_PINS = [
     pin_forward_hand_values,
     pin_forward_forms_agree,
@@ -396,6 +440,8 @@ ALL_PINS = [
     pin_state_definition,
     pin_decode_hand_values,
     pin_decode_matches_forward,
+    pin_gate_special_values,
+    pin_gate_finite_differences,
 ]
 
 

@@ -59,6 +59,14 @@ MUTANTS = [
      "xk[IDX(b, t, c)] = mu_k[c] * prev + (1.0 - mu_k[c]) * cur;"),
     ("shift_grad_misses_next_token", "wkv_oracle_token_shift_backward",
      "g += (1.0 - mu_k[c]) * gxk[n] +", "g += 0.0 * gxk[n] +"),
+    ("gate_sign", "wkv_oracle_forward_gated",
+     "out[i] / (1.0 + exp(-r[i]))", "out[i] / (1.0 + exp(r[i]))"),
+    ("gated_gy_not_gated", "wkv_oracle_backward_gated",
+     "gy[i] = gout[i] * s;", "gy[i] = gout[i];"),
+    ("gated_gr_drops_one_minus_s", "wkv_oracle_backward_gated",
+     "gr[i] = gout[i] * y[i] * s * (1.0 - s);", "gr[i] = gout[i] * y[i] * s;"),
+    ("gated_gr_uses_gated_gradient", "wkv_oracle_backward_gated",
+     "gr[i] = gout[i] * y[i] * s * (1.0 - s);", "gr[i] = gy[i] * y[i] * s * (1.0 - s);"),
     ("shift_grad_mu_sign", "wkv_oracle_token_shift_backward",
      "double d = x[i] - prev;", "double d = prev - x[i];"),
 ]
