@@ -45,6 +45,7 @@ METRIC = "WKV fwd+bwd B·T·C elements/s and achieved HBM GB/s fraction on 1 B30
 METRIC_FWD = "WKV forward B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
 METRIC_DEC = "WKV decode step L·B·C elements/s and achieved HBM GB/s fraction on 1 B300"
 METRIC_SHIFT = "token shift fwd+bwd B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
+METRIC_GATED = "gated WKV sigmoid(r)*wkv fwd+bwd B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
 
 # Algorithmic HBM bytes per element (what the method must move with the
 # separate forward / backward calls; O(1/chunk) checkpoint and workspace
@@ -56,6 +57,8 @@ BYTES_BWD_BF16 = 14  # read bf16 k, v, gy; write fp32 gk, gv
 BYTES_DECODE = 60    # read x, x_prev, r, k, v; read+write num, den, pp; write y, xk, xv, xr
 BYTES_SHIFT_FWD = 16  # read x; write xk, xv, xr
 BYTES_SHIFT_BWD = 20  # read x, gxk, gxv, gxr; write gx
+BYTES_FWD_GATED = 16  # read k, v, r; write sigmoid(r) * wkv
+BYTES_BWD_GATED = 28  # read k, v, r, gout; write gk, gv, gr
 
 REJECT_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
@@ -65,8 +68,8 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default depends on the workload)")
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="l169m", choices=["tiny", "l169m", "l1b5", "long", "l169m_bf16", "decode",
-                                                              "shift"])
+    ap.add_argument("--workload", default="l169m", choices=["tiny", "l169m", "l1b5", "long", "l169m_bf16",
+                                                              "l169m_gated", "decode", "shift"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -80,8 +83,8 @@ def parse_args(argv=None):
     return args
 
 
-DEFAULT_STEPS = {"tiny": 2000, "l169m": 4000, "l1b5": 200, "long": 200, "l169m_bf16": 4000, "decode": 256,
-                 "shift": 200}
+DEFAULT_STEPS = {"tiny": 2000, "l169m": 4000, "l1b5": 200, "long": 200, "l169m_bf16": 4000, "l169m_gated": 4000,
+                 "decode": 256, "shift": 200}
 
 
 # ------------------------------------------------------------------ ranks
@@ -278,7 +281,7 @@ class TrainingRun:
         self.torch, self.wkv = torch, binding
         self.wl = inputs.WORKLOADS[name]
         wl = self.wl
-        self.host = inputs.workload_inputs(name)  # (w, u, k, v, gy) on the CPU
+        self.host = inputs.workload_inputs(name)  # (w, u, k, v, gy[, r]) on the CPU
         self.dev = tuple(t.to(device).contiguous() for t in self.host)
         B, T, C = wl.B, wl.T, wl.C
         self.elements = wl.elements
@@ -288,11 +291,15 @@ class TrainingRun:
         self.gu = torch.empty(C, device=device)
         self.gk = torch.empty(B, T, C, device=device)
         self.gv = torch.empty(B, T, C, device=device)
+        self.gr = torch.empty(B, T, C, device=device) if wl.gated else None
         self.ws_f = binding.Workspace(binding.forward_workspace_bytes(B, T, C), device)
         self.ws_b = binding.Workspace(binding.backward_workspace_bytes(B, T, C), device)
         kv_bytes = BYTES_FWD_BF16 if wl.kv_dtype == "bf16" else BYTES_FWD_F32
-        self.bytes_fwd = kv_bytes * self.elements
         bwd_bytes = BYTES_BWD_BF16 if wl.kv_dtype == "bf16" else BYTES_BWD
+        if wl.gated:
+            assert wl.kv_dtype == "f32"
+            kv_bytes, bwd_bytes = BYTES_FWD_GATED, BYTES_BWD_GATED
+        self.bytes_fwd = kv_bytes * self.elements
         self.bytes_bwd = bwd_bytes * self.elements if wl.backward else 0
         self.launches_per_step = 1 + (2 if wl.backward else 0)
         from rwkv_linear_attention_backward_b300 import binding
@@ -305,13 +312,20 @@ class TrainingRun:
         self.dominant_bytes = self.bytes_bwd if wl.backward else self.bytes_fwd
 
     def _forward(self):
-        w, u, k, v, _ = self.dev
-        self.wkv.forward(w, u, k, v, y=self.y, ckpt=self.ckpt, workspace=self.ws_f)
+        w, u, k, v = self.dev[:4]
+        if self.wl.gated:
+            self.wkv.forward_gated(w, u, k, v, self.dev[5], out=self.y, ckpt=self.ckpt, workspace=self.ws_f)
+        else:
+            self.wkv.forward(w, u, k, v, y=self.y, ckpt=self.ckpt, workspace=self.ws_f)
 
     def _backward(self):
-        w, u, k, v, gy = self.dev
-        self.wkv.backward(w, u, k, v, gy, ckpt=self.ckpt, gw=self.gw, gu=self.gu, gk=self.gk, gv=self.gv,
-                          workspace=self.ws_b)
+        w, u, k, v, gy = self.dev[:5]
+        if self.wl.gated:
+            self.wkv.backward_gated(w, u, k, v, self.dev[5], gy, ckpt=self.ckpt, gw=self.gw, gu=self.gu, gk=self.gk,
+                                    gv=self.gv, gr=self.gr, workspace=self.ws_b)
+        else:
+            self.wkv.backward(w, u, k, v, gy, ckpt=self.ckpt, gw=self.gw, gu=self.gu, gk=self.gk, gv=self.gv,
+                              workspace=self.ws_b)
 
     def capture(self):
         """CUDA graphs of the forward and the backward call on the run's
@@ -355,10 +369,13 @@ class TrainingRun:
     def e2e_setup(self):
         torch = self.torch
         self.pin_in = tuple(t.pin_memory() for t in self.host)
-        self.pin_out = tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                             for t in ([self.y] + ([self.gk, self.gv, self.gw, self.gu] if self.wl.backward else [])))
+        self.pin_out = tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in self._outputs())
         self.h2d = sum(t.numel() * t.element_size() for t in self.pin_in)
         self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out)
+
+    def _outputs(self):
+        grads = [self.gk, self.gv, self.gw, self.gu] + ([self.gr] if self.wl.gated else [])
+        return [self.y] + (grads if self.wl.backward else [])
 
     def e2e_step(self):
         for d, h in zip(self.dev, self.pin_in):
@@ -366,8 +383,7 @@ class TrainingRun:
         self._forward()
         if self.wl.backward:
             self._backward()
-        outs = [self.y] + ([self.gk, self.gv, self.gw, self.gu] if self.wl.backward else [])
-        for h, d in zip(self.pin_out, outs):
+        for h, d in zip(self.pin_out, self._outputs()):
             h.copy_(d, non_blocking=True)
 
 
@@ -539,25 +555,26 @@ def cpu_baseline(workload: str, target_s: float = 12.0):
     if workload == "shift":
         return _shift_oracle_timing(o, target_s)
     wl = inputs.WORKLOADS[workload]
-    w, u, k, v, gy = inputs.workload_inputs(workload)
+    w, u, k, v, gy, *r = inputs.workload_inputs(workload)
+    r = r[0] if r else None
     C = wl.C
     nchan = C
     # calibrate on a few channels, then size the sample for ~target_s
     cs = np.arange(min(8, C))
     t0 = time.perf_counter()
-    _oracle_pass(o, wl, w, u, k, v, gy, cs)
+    _oracle_pass(o, wl, w, u, k, v, gy, cs, r)
     per_chan = (time.perf_counter() - t0) / len(cs)
     nchan = int(max(1, min(C, target_s / max(per_chan, 1e-9) / 2)))
     cs = np.linspace(0, C - 1, nchan).astype(int)
     reps, done, t0 = 0, 0, time.perf_counter()
     while True:
-        _oracle_pass(o, wl, w, u, k, v, gy, cs)
+        _oracle_pass(o, wl, w, u, k, v, gy, cs, r)
         reps += 1
         done += wl.B * wl.T * len(cs)
         if time.perf_counter() - t0 >= target_s or reps >= 50:
             break
     el = time.perf_counter() - t0
-    what = "recurrent forward + adjoint backward" if wl.backward else "recurrent forward"
+    what = _oracle_what(wl)
     return {"value": done / el, "unit": "elements/s", "cores": o.num_threads(), "kind": "oracle",
             "sample": f"{what} on {len(cs)} of {C} channels (all B={wl.B}, T={wl.T}), {reps} pass(es) in {el:.1f} s"}
 
@@ -583,11 +600,22 @@ def _shift_oracle_timing(o, target_s):
                       f"{reps} pass(es) in {el:.1f} s"}
 
 
-def _oracle_pass(o, wl, w, u, k, v, gy, cs):
+def _oracle_pass(o, wl, w, u, k, v, gy, cs, r=None):
     ks, vs = k[:, :, cs], v[:, :, cs]
+    if wl.gated:
+        rs = r[:, :, cs]
+        o.forward_gated(w[cs], u[cs], ks, vs, rs)
+        o.backward_gated(w[cs], u[cs], ks, vs, rs, gy[:, :, cs])
+        return
     o.forward_recurrent(w[cs], u[cs], ks, vs)
     if wl.backward:
         o.backward_adjoint(w[cs], u[cs], ks, vs, gy[:, :, cs])
+
+
+def _oracle_what(wl):
+    if wl.gated:
+        return "gated direct forward + gated adjoint backward"
+    return "recurrent forward + adjoint backward" if wl.backward else "recurrent forward"
 
 
 def run_ours(args):
@@ -661,6 +689,8 @@ def run_ours(args):
     else:
         wl_cfg = {"workload": args.workload, "B": run.wl.B, "T": run.wl.T, "C": run.wl.C,
                   "kv_dtype": run.wl.kv_dtype, "pass": "forward+backward" if run.wl.backward else "forward"}
+        if run.wl.gated:
+            wl_cfg["output"] = "sigmoid(r) * wkv, the gate fused into the forward and backward kernels"
     wl_cfg.update({"launch": "api calls per step" if (args.no_graph or args.workload in ("decode", "shift")) else
                    "CUDA graphs of the forward and backward calls, captured once and replayed per step",
                    "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}",
@@ -668,7 +698,8 @@ def run_ours(args):
                    "strategy": getattr(run, "strategy", "n/a"),
                    "checkpoints": "forward writes chunk checkpoints, backward reads them"
                    if args.workload not in ("decode", "shift") else "n/a"})
-    metric = {"long": METRIC_FWD, "decode": METRIC_DEC, "shift": METRIC_SHIFT}.get(args.workload, METRIC)
+    metric = {"long": METRIC_FWD, "decode": METRIC_DEC, "shift": METRIC_SHIFT,
+              "l169m_gated": METRIC_GATED}.get(args.workload, METRIC)
     out = {
         "metric": metric,
         "value": value,
@@ -781,21 +812,21 @@ def run_reference(args):
         metric = METRIC_SHIFT
     else:
         wl = inputs.WORKLOADS[args.workload]
-        w, u, k, v, gy = inputs.workload_inputs(args.workload)
+        w, u, k, v, gy, *r = inputs.workload_inputs(args.workload)
+        r = r[0] if r else None
         cs = np.arange(min(4, wl.C))
         t0 = time.perf_counter()
-        _oracle_pass(o, wl, w, u, k, v, gy, cs)
+        _oracle_pass(o, wl, w, u, k, v, gy, cs, r)
         per_chan = (time.perf_counter() - t0) / len(cs)
         nchan = int(max(1, min(wl.C, per_step / max(per_chan, 1e-9))))
         cs = np.linspace(0, wl.C - 1, nchan).astype(int)
 
         def one():
-            _oracle_pass(o, wl, w, u, k, v, gy, cs)
+            _oracle_pass(o, wl, w, u, k, v, gy, cs, r)
             return wl.B * wl.T * len(cs)
 
-        what = "recurrent forward + adjoint backward" if wl.backward else "recurrent forward"
-        sample = f"{what} on {len(cs)} of {wl.C} channels (all B={wl.B}, T={wl.T})"
-        metric = METRIC if wl.backward else METRIC_FWD
+        sample = f"{_oracle_what(wl)} on {len(cs)} of {wl.C} channels (all B={wl.B}, T={wl.T})"
+        metric = METRIC_GATED if wl.gated else (METRIC if wl.backward else METRIC_FWD)
     for _ in range(args.warmup):
         one()
     t0 = time.perf_counter()

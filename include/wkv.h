@@ -173,6 +173,47 @@ wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const
                         float* gv, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * wkv_forward_gated -- the time-mixing output with its receptance gate fused
+ * in ("RWKV解读" section "3、RWKV的网络架构", eq. (9): the wkv result is
+ * multiplied elementwise by sigmoid of the receptance before the output
+ * projection):
+ *   out[b,t,c] = sigmoid(r[b,t,c]) * wkv_t,   sigmoid(r) = 1 / (1 + e^{-r}).
+ * The gate is applied as each output is written: wkv itself never goes to
+ * memory.
+ *   r          [B, T, C] input of kv_dtype (like k and v).
+ *   out        [B, T, C] float output.
+ *   The other arguments (state_in, state_out, ckpt, workspace) are those of
+ *   wkv_forward_with_state; ckpt serves wkv_backward_gated as it serves
+ *   wkv_backward.
+ * Errors: as wkv_forward (r NULL: WKV_ERR_INVALID_ARG); WKV_ERR_UNSUPPORTED
+ * while wkv_debug_set_scan_mode forces the chunked scan (the gate is fused
+ * into the sequential kernels only).
+ */
+wkv_status wkv_forward_gated(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                             const void* v, const void* r, const float* state_in, float* out, float* state_out,
+                             float* ckpt, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * wkv_backward_gated -- gradients of sum(gout * sigmoid(r) * wkv) with
+ * respect to w, u, k, v and r.  wkv_t reaches the output only through the
+ * gate, so the gradient entering the recurrence is gout_t sigmoid(r_t), and
+ *   gr_t = gout_t * wkv_t * sigmoid(r_t) * (1 - sigmoid(r_t)),
+ * with wkv_t recomputed inside the reverse walk (the forward pass need not
+ * keep it).  Both are formed as each chunk is read, from the r and gout
+ * planes staged beside k and v.
+ *   r, gout     [B, T, C] inputs of kv_dtype.
+ *   gr          [B, T, C] float output.
+ *   The other arguments are those of wkv_backward (ckpt from
+ *   wkv_forward_gated or wkv_forward for the same w, k, v, or NULL;
+ *   workspace at least wkv_backward_workspace_bytes(B, T, C)).
+ * Errors: as wkv_backward (r or gr NULL: WKV_ERR_INVALID_ARG);
+ * WKV_ERR_UNSUPPORTED while the chunked scan is forced.
+ */
+wkv_status wkv_backward_gated(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                              const void* v, const void* r, const void* gout, const float* ckpt, float* gw, float* gu,
+                              float* gk, float* gv, float* gr, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * wkv_decode_step -- one RNN-mode step of L independent time-mixing layers,
  * fused: token shift (eq. 7) -> wkv from the carried state -> sigmoid(r)
  * gate (eq. 9) -> state update.  Per (l, b, c), with parameters at (l, c):

@@ -7,8 +7,10 @@ this module loads ``libwkv.so`` from this package directory and raises
 ``python -m rwkv_linear_attention_backward_b300.build``); there is no
 fallback implementation.
 
-Entry points mirror the ABI names: ``forward``, ``backward``,
-``decode_step``, ``workspace_check``, plus size queries.  All tensors must be
+Entry points mirror the ABI names: ``forward``, ``forward_with_state``,
+``forward_gated``, ``backward``, ``backward_gated``, ``decode_step``,
+``token_shift``, ``token_shift_backward``, ``workspace_check``, plus size
+queries and test hooks.  All tensors must be
 contiguous CUDA tensors on the current device; calls are enqueued on the
 current torch stream (or ``stream=``) and return without synchronising.
 """
@@ -41,6 +43,8 @@ _SIGNATURES = {
     "wkv_forward": ([_i, _i, _i, _i] + [_vp] * 6 + [_vp, _sz, _vp], _i),
     "wkv_forward_with_state": ([_i, _i, _i, _i] + [_vp] * 8 + [_vp, _sz, _vp], _i),
     "wkv_backward": ([_i, _i, _i, _i] + [_vp] * 10 + [_vp, _sz, _vp], _i),
+    "wkv_forward_gated": ([_i, _i, _i, _i] + [_vp] * 9 + [_vp, _sz, _vp], _i),
+    "wkv_backward_gated": ([_i, _i, _i, _i] + [_vp] * 12 + [_vp, _sz, _vp], _i),
     "wkv_decode_step": ([_i, _i, _i] + [_vp] * 17 + [_vp], _i),
     "wkv_forward_noalloc": ([_i, _i, _i, _i] + [_vp] * 6 + [_vp], _i),
     "wkv_debug_set_wait_budget_ns": ([_ll], _i),
@@ -215,6 +219,40 @@ def forward_with_state(w, u, k, v, state_in=None, *, y=None, state_out=None, ckp
     return (y, state_out, ckpt) if ckpt is not None else (y, state_out)
 
 
+def forward_gated(w, u, k, v, r, state_in=None, *, out=None, state_out=None, ckpt=None, want_ckpt: bool = False,
+                  workspace: Workspace | None = None, stream=None):
+    """sigmoid(r) * wkv for k, v, r [B, T, C] (all fp32 or all bf16); w, u [C]
+    fp32.  Returns ``out`` (fp32 [B, T, C]), or ``(out, ckpt)`` when
+    ``want_ckpt`` or a ``ckpt`` buffer is given.  ``state_in`` / ``state_out``
+    ([3, B, C] fp32, optional) as for ``forward_with_state``."""
+    if k.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("k must be float32 or bfloat16")
+    B, T, C = k.shape
+    _need(k, "k", (k.dtype,))
+    _need(v, "v", (k.dtype,), k.shape)
+    _need(r, "r", (k.dtype,), k.shape)
+    _need(w, "w", shape=(C,))
+    _need(u, "u", shape=(C,))
+    if state_in is not None:
+        _need(state_in, "state_in", shape=(3, B, C))
+    if state_out is not None:
+        _need(state_out, "state_out", shape=(3, B, C))
+    if out is None:
+        out = torch.empty((B, T, C), dtype=torch.float32, device=k.device)
+    _need(out, "out", shape=(B, T, C))
+    if ckpt is None and want_ckpt:
+        ckpt = torch.empty(checkpoint_floats(B, T, C), dtype=torch.float32, device=k.device)
+    if ckpt is not None:
+        _need(ckpt, "ckpt")
+        if ckpt.numel() < checkpoint_floats(B, T, C):
+            raise ValueError("ckpt is too small")
+    ws = workspace or _workspace("fwd", forward_workspace_bytes(B, T, C), k.device)
+    dt = WKV_BF16 if k.dtype == torch.bfloat16 else WKV_F32
+    _check(_lib.wkv_forward_gated(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(r), _p(state_in), _p(out),
+                                  _p(state_out), _p(ckpt), ws.ptr(), ws.nbytes, _stream(stream)), "wkv_forward_gated")
+    return (out, ckpt) if ckpt is not None else out
+
+
 def token_shift(x, x0, mu_k, mu_v, mu_r, *, xk=None, xv=None, xr=None, stream=None):
     """(xk, xv, xr) = mu x_t + (1 - mu) x_{t-1} for x [B, T, C] (fp32); x0
     [B, C] is the token before the sequence (None: zeros)."""
@@ -307,6 +345,36 @@ def backward(w, u, k, v, gy, *, ckpt=None, gw=None, gu=None, gk=None, gv=None, w
     return gw, gu, gk, gv
 
 
+def backward_gated(w, u, k, v, r, gout, *, ckpt=None, gw=None, gu=None, gk=None, gv=None, gr=None,
+                   workspace: Workspace | None = None, stream=None):
+    """Gradients (gw, gu, gk, gv, gr) of sum(gout * sigmoid(r) * wkv); k, v,
+    r, gout all fp32 or all bf16 (fp32 arithmetic and gradients)."""
+    if k.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("k must be float32 or bfloat16")
+    B, T, C = k.shape
+    for t, n in ((k, "k"), (v, "v"), (r, "r"), (gout, "gout")):
+        _need(t, n, (k.dtype,), k.shape)
+    _need(w, "w", shape=(C,))
+    _need(u, "u", shape=(C,))
+    if ckpt is not None:
+        _need(ckpt, "ckpt")
+        if ckpt.numel() < checkpoint_floats(B, T, C):
+            raise ValueError("ckpt is too small")
+    dev = k.device
+    gw = torch.empty(C, dtype=torch.float32, device=dev) if gw is None else gw
+    gu = torch.empty(C, dtype=torch.float32, device=dev) if gu is None else gu
+    gk, gv, gr = (torch.empty((B, T, C), dtype=torch.float32, device=dev) if t is None else t for t in (gk, gv, gr))
+    for t, n, s in ((gw, "gw", (C,)), (gu, "gu", (C,)), (gk, "gk", (B, T, C)), (gv, "gv", (B, T, C)),
+                    (gr, "gr", (B, T, C))):
+        _need(t, n, shape=s)
+    ws = workspace or _workspace("bwd", backward_workspace_bytes(B, T, C), dev)
+    dt = WKV_BF16 if k.dtype == torch.bfloat16 else WKV_F32
+    _check(_lib.wkv_backward_gated(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(r), _p(gout), _p(ckpt), _p(gw),
+                                   _p(gu), _p(gk), _p(gv), _p(gr), ws.ptr(), ws.nbytes, _stream(stream)),
+           "wkv_backward_gated")
+    return gw, gu, gk, gv, gr
+
+
 # ----------------------------------------------------------------- decode
 def decode_step(x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u, num, den, pp, *, y=None, xk=None, xv=None, xr=None,
                 mix: bool = True, stream=None):
@@ -395,3 +463,23 @@ class WKVFunction(torch.autograd.Function):
 def wkv(w, u, k, v):
     """Differentiable WKV (fp32 k, v for the backward)."""
     return WKVFunction.apply(w, u, k, v)
+
+
+class GatedWKVFunction(torch.autograd.Function):
+    """torch.autograd wrapper of the gated output sigmoid(r) * wkv."""
+
+    @staticmethod
+    def forward(ctx, w, u, k, v, r):
+        out, ckpt = forward_gated(w, u, k, v, r, want_ckpt=True)
+        ctx.save_for_backward(w, u, k, v, r, ckpt)
+        return out
+
+    @staticmethod
+    def backward(ctx, gout):
+        w, u, k, v, r, ckpt = ctx.saved_tensors
+        return backward_gated(w, u, k, v, r, gout.contiguous(), ckpt=ckpt)
+
+
+def wkv_gated(w, u, k, v, r):
+    """Differentiable sigmoid(r) * wkv (fp32 k, v, r for the backward)."""
+    return GatedWKVFunction.apply(w, u, k, v, r)

@@ -170,12 +170,12 @@ namespace {
 
 // The backward pass with the sequential column kernels: the checkpoints
 // (recomputed by a state-only forward walk when the caller has none), the
-// reverse walk writing gk, gv and one gw, gu row per (run, batch row), then
-// the reduction of those rows.
+// reverse walk writing gk, gv (and gr for the gated output, r non-null) and
+// one gw, gu row per (run, batch row), then the reduction of those rows.
 wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int kv_dtype, const float* w,
-                               const float* u, const void* k, const void* v, const void* gy, const float* ckpt,
-                               float* gw, float* gu, float* gk, float* gv, WsHeader* hdr, void* workspace,
-                               uint64_t budget, cudaStream_t s) {
+                               const float* u, const void* k, const void* v, const void* gy, const void* r,
+                               const float* ckpt, float* gw, float* gu, float* gk, float* gv, float* gr,
+                               WsHeader* hdr, void* workspace, uint64_t budget, cudaStream_t s) {
   const int B = g.B, T = g.T, C = g.C;
   const int eb = kv_dtype == WKV_F32 ? 4 : 2;
   const float* states = ckpt;
@@ -208,9 +208,11 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int kv
   a.k = k;
   a.v = v;
   a.gy = gy;
+  a.r = r;
   a.ckpt = states;
   a.gk = gk;
   a.gv = gv;
+  a.gr = gr;
   a.part = reinterpret_cast<float*>(bytes(workspace) + l.part);  // [2][nseg * B][C]
   a.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.ragg);
   a.exited = &hdr->exited[2];
@@ -220,21 +222,22 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int kv
   a.g = g;
   a.budget_ns = budget;
   a.use_tma = make_tile_map(&a.tk, k, B, T, C, eb, kSeqChannels) &&
-              make_tile_map(&a.tv, v, B, T, C, eb, kSeqChannels) && make_tile_map(&a.tg, gy, B, T, C, eb, kSeqChannels);
+              make_tile_map(&a.tv, v, B, T, C, eb, kSeqChannels) && make_tile_map(&a.tg, gy, B, T, C, eb, kSeqChannels) &&
+              (!r || make_tile_map(&a.tr, r, B, T, C, eb, kSeqChannels));
   cudaError_t e = launch_seq_backward(a, kv_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
   const int rows = a.nseg * B;
-  ReduceArgs r;
-  r.part = a.part;
-  r.slices = reinterpret_cast<float*>(bytes(workspace) + l.slices);
-  r.count = reinterpret_cast<unsigned long long*>(bytes(workspace) + l.count);
-  r.eh = hdr;
-  r.gw = gw;
-  r.gu = gu;
-  r.rows = rows;
-  r.C = C;
-  r.nslice = reduce_slices(rows, C);
-  e = launch_reduce(r, s);
+  ReduceArgs red;
+  red.part = a.part;
+  red.slices = reinterpret_cast<float*>(bytes(workspace) + l.slices);
+  red.count = reinterpret_cast<unsigned long long*>(bytes(workspace) + l.count);
+  red.eh = hdr;
+  red.gw = gw;
+  red.gu = gu;
+  red.rows = rows;
+  red.C = C;
+  red.nslice = reduce_slices(rows, C);
+  e = launch_reduce(red, s);
   return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_backward: reduce");
 }
 
@@ -242,6 +245,176 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int kv
 }  // namespace wkv
 
 using namespace wkv;
+
+namespace wkv {
+namespace {
+
+// wkv_forward_with_state, and wkv_forward_gated when r is non-null.
+wkv_status forward_impl(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                        const void* v, const void* r, const float* state_in, float* y, float* state_out, float* ckpt,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  if (!sizes_ok(B, T, C) || !w || !u || !k || !v || !y) return WKV_ERR_INVALID_ARG;
+  if (kv_dtype != WKV_F32 && kv_dtype != WKV_BF16) return WKV_ERR_INVALID_ARG;
+  const ScanGeometry g = make_geometry(B, T, C);
+  const FwdLayout l = fwd_layout(g);
+  if (!workspace || workspace_bytes < l.total) return WKV_ERR_WORKSPACE;
+  const int eb = kv_dtype == WKV_F32 ? 4 : 2;
+  bool seq = false;
+  cudaError_t e = sequential_mode(g, seq);
+  if (e != cudaSuccess) return cuda_fail(e, "wkv_forward");
+  if (r && !seq) {
+    set_last_error("wkv_forward_gated: the gated output is written by the sequential kernels only (the chunked scan "
+                   "is forced)");
+    return WKV_ERR_UNSUPPORTED;
+  }
+  if (seq) {
+    SeqFwdArgs q;
+    std::memset(&q, 0, sizeof(q));
+    q.w = w;
+    q.u = u;
+    q.k = k;
+    q.v = v;
+    q.y = y;
+    q.r = r;
+    q.state_in = state_in;
+    q.state_out = state_out;
+    q.ckpt = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.ckpt);
+    q.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.agg);
+    q.eh = static_cast<WsHeader*>(workspace);
+    q.exited = &q.eh->exited[0];
+    q.nseg = g_max_runs.load();  // 0: the launcher's choice
+    q.chain = g_chain_len.load();
+    q.debug_skip_chunk = g_skip_chunk.load();
+    q.g = g;
+    q.budget_ns = (uint64_t)g_budget_ns.load();
+    q.use_tma = make_tile_map(&q.tk, k, B, T, C, eb, kSeqChannels) && make_tile_map(&q.tv, v, B, T, C, eb, kSeqChannels);
+    e = launch_seq_forward(q, kv_dtype, true, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
+  }
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.w = w;
+  a.u = u;
+  a.k = k;
+  a.v = v;
+  a.y = y;
+  a.state_in = state_in;
+  a.state_out = state_out;
+  a.agg = reinterpret_cast<Rec*>(bytes(workspace) + l.agg);
+  a.inc = reinterpret_cast<Rec*>(bytes(workspace) + l.inc);
+  a.ckpt = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.ckpt);
+  a.eh = static_cast<WsHeader*>(workspace);
+  a.ticket = &a.eh->ticket[0];
+  a.exited = &a.eh->exited[0];
+  a.g = g;
+  a.budget_ns = (uint64_t)g_budget_ns.load();
+  a.debug_skip_chunk = g_skip_chunk.load();
+  a.use_tma = make_tile_map(&a.tk, k, B, T, C, eb, kCtaChannels) && make_tile_map(&a.tv, v, B, T, C, eb, kCtaChannels);
+  e = launch_forward(a, kv_dtype, true, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
+}
+
+// wkv_backward, and wkv_backward_gated when r is non-null (then gy is the
+// gated output's gradient and gr receives r's).
+wkv_status backward_impl(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                         const void* v, const void* gy, const void* r, const float* ckpt, float* gw, float* gu,
+                         float* gk, float* gv, float* gr, void* workspace, size_t workspace_bytes, void* stream) {
+  clear_error();
+  if (!sizes_ok(B, T, C) || !w || !u || !k || !v || !gy || !gw || !gu || !gk || !gv) return WKV_ERR_INVALID_ARG;
+  if (r && !gr) return WKV_ERR_INVALID_ARG;
+  if (kv_dtype != WKV_F32 && kv_dtype != WKV_BF16) return WKV_ERR_INVALID_ARG;
+  const ScanGeometry g = make_geometry(B, T, C);
+  const BwdLayout l = bwd_layout(g);
+  if (!workspace || workspace_bytes < l.total) return WKV_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  const int skip = g_skip_chunk.load();
+  const uint64_t budget = (uint64_t)g_budget_ns.load();
+  bool seq = false;
+  cudaError_t e = sequential_mode(g, seq);
+  if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
+  if (seq)
+    return backward_sequential(g, l, kv_dtype, w, u, k, v, gy, r, ckpt, gw, gu, gk, gv, gr, hdr, workspace, budget,
+                               s);
+  if (r) {
+    set_last_error("wkv_backward_gated: the gated output's backward pass runs on the sequential kernels only (the "
+                   "chunked scan is forced)");
+    return WKV_ERR_UNSUPPORTED;
+  }
+  if (kv_dtype != WKV_F32) {
+    set_last_error("wkv_backward: bf16 inputs are taken by the sequential kernels only (the chunked scan is forced)");
+    return WKV_ERR_UNSUPPORTED;
+  }
+
+  const float* states = ckpt;
+  if (!states) {
+    // recompute the chunk-boundary states: forward scan without outputs
+    char* fws = bytes(workspace) + l.fwd;
+    const FwdLayout fl = fwd_layout(g);
+    FwdArgs f;
+    std::memset(&f, 0, sizeof(f));
+    f.w = w;
+    f.u = u;
+    f.k = k;
+    f.v = v;
+    f.y = nullptr;
+    f.agg = reinterpret_cast<Rec*>(fws + fl.agg);
+    f.inc = reinterpret_cast<Rec*>(fws + fl.inc);
+    f.ckpt = reinterpret_cast<float*>(fws + fl.ckpt);
+    f.ticket = &hdr->ticket[1];  // counters stay in the outer header: its place never moves
+    f.exited = &hdr->exited[1];
+    f.eh = hdr;
+    f.g = g;
+    f.budget_ns = budget;
+    f.debug_skip_chunk = -1;
+    f.use_tma = make_tile_map(&f.tk, k, B, T, C, 4, kCtaChannels) && make_tile_map(&f.tv, v, B, T, C, 4, kCtaChannels);
+    e = launch_forward(f, WKV_F32, false, s);
+    if (e != cudaSuccess) return cuda_fail(e, "wkv_backward: state pass");
+    states = f.ckpt;
+  }
+
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.w = w;
+  a.u = u;
+  a.k = static_cast<const float*>(k);
+  a.v = static_cast<const float*>(v);
+  a.gy = static_cast<const float*>(gy);
+  a.ckpt = states;
+  a.gk = gk;
+  a.gv = gv;
+  a.ragg = reinterpret_cast<Rec*>(bytes(workspace) + l.ragg);
+  a.rinc = reinterpret_cast<Rec*>(bytes(workspace) + l.rinc);
+  a.part = reinterpret_cast<float*>(bytes(workspace) + l.part);
+  a.ticket = &hdr->ticket[2];
+  a.exited = &hdr->exited[2];
+  a.eh = hdr;
+  a.g = g;
+  a.budget_ns = budget;
+  a.debug_skip_chunk = skip;
+  a.use_tma = make_tile_map(&a.tk, k, B, T, C, 4, kCtaChannels) && make_tile_map(&a.tv, v, B, T, C, 4, kCtaChannels) &&
+              make_tile_map(&a.tg, gy, B, T, C, 4, kCtaChannels);
+  e = launch_backward(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
+
+  ReduceArgs red;
+  red.part = a.part;
+  red.slices = reinterpret_cast<float*>(bytes(workspace) + l.slices);
+  red.count = reinterpret_cast<unsigned long long*>(bytes(workspace) + l.count);
+  red.eh = hdr;
+  red.gw = gw;
+  red.gu = gu;
+  red.rows = g.nchunks * g.B;
+  red.C = C;
+  red.nslice = l.nslice;
+  e = launch_reduce(red, s);
+  return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_backward: reduce");
+}
+
+}  // namespace
+}  // namespace wkv
+
 
 extern "C" {
 
@@ -313,148 +486,33 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
 wkv_status wkv_forward_with_state(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
                                   const void* v, const float* state_in, float* y, float* state_out, float* ckpt,
                                   void* workspace, size_t workspace_bytes, void* stream) {
+  return forward_impl(B, T, C, kv_dtype, w, u, k, v, nullptr, state_in, y, state_out, ckpt, workspace,
+                      workspace_bytes, stream);
+}
+
+wkv_status wkv_forward_gated(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                             const void* v, const void* r, const float* state_in, float* out, float* state_out,
+                             float* ckpt, void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
-  if (!sizes_ok(B, T, C) || !w || !u || !k || !v || !y) return WKV_ERR_INVALID_ARG;
-  if (kv_dtype != WKV_F32 && kv_dtype != WKV_BF16) return WKV_ERR_INVALID_ARG;
-  const ScanGeometry g = make_geometry(B, T, C);
-  const FwdLayout l = fwd_layout(g);
-  if (!workspace || workspace_bytes < l.total) return WKV_ERR_WORKSPACE;
-  const int eb = kv_dtype == WKV_F32 ? 4 : 2;
-  bool seq = false;
-  cudaError_t e = sequential_mode(g, seq);
-  if (e != cudaSuccess) return cuda_fail(e, "wkv_forward");
-  if (seq) {
-    SeqFwdArgs q;
-    std::memset(&q, 0, sizeof(q));
-    q.w = w;
-    q.u = u;
-    q.k = k;
-    q.v = v;
-    q.y = y;
-    q.state_in = state_in;
-    q.state_out = state_out;
-    q.ckpt = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.ckpt);
-    q.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.agg);
-    q.eh = static_cast<WsHeader*>(workspace);
-    q.exited = &q.eh->exited[0];
-    q.nseg = g_max_runs.load();  // 0: the launcher's choice
-    q.chain = g_chain_len.load();
-    q.debug_skip_chunk = g_skip_chunk.load();
-    q.g = g;
-    q.budget_ns = (uint64_t)g_budget_ns.load();
-    q.use_tma = make_tile_map(&q.tk, k, B, T, C, eb, kSeqChannels) && make_tile_map(&q.tv, v, B, T, C, eb, kSeqChannels);
-    e = launch_seq_forward(q, kv_dtype, true, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
-  }
-  FwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.w = w;
-  a.u = u;
-  a.k = k;
-  a.v = v;
-  a.y = y;
-  a.state_in = state_in;
-  a.state_out = state_out;
-  a.agg = reinterpret_cast<Rec*>(bytes(workspace) + l.agg);
-  a.inc = reinterpret_cast<Rec*>(bytes(workspace) + l.inc);
-  a.ckpt = ckpt ? ckpt : reinterpret_cast<float*>(bytes(workspace) + l.ckpt);
-  a.eh = static_cast<WsHeader*>(workspace);
-  a.ticket = &a.eh->ticket[0];
-  a.exited = &a.eh->exited[0];
-  a.g = g;
-  a.budget_ns = (uint64_t)g_budget_ns.load();
-  a.debug_skip_chunk = g_skip_chunk.load();
-  a.use_tma = make_tile_map(&a.tk, k, B, T, C, eb, kCtaChannels) && make_tile_map(&a.tv, v, B, T, C, eb, kCtaChannels);
-  e = launch_forward(a, kv_dtype, true, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
+  if (!r) return WKV_ERR_INVALID_ARG;
+  return forward_impl(B, T, C, kv_dtype, w, u, k, v, r, state_in, out, state_out, ckpt, workspace, workspace_bytes,
+                      stream);
 }
 
 wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
                         const void* v, const void* gy, const float* ckpt, float* gw, float* gu, float* gk,
                         float* gv, void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_impl(B, T, C, kv_dtype, w, u, k, v, gy, nullptr, ckpt, gw, gu, gk, gv, nullptr, workspace,
+                       workspace_bytes, stream);
+}
+
+wkv_status wkv_backward_gated(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                              const void* v, const void* r, const void* gout, const float* ckpt, float* gw, float* gu,
+                              float* gk, float* gv, float* gr, void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
-  if (!sizes_ok(B, T, C) || !w || !u || !k || !v || !gy || !gw || !gu || !gk || !gv) return WKV_ERR_INVALID_ARG;
-  if (kv_dtype != WKV_F32 && kv_dtype != WKV_BF16) return WKV_ERR_INVALID_ARG;
-  const ScanGeometry g = make_geometry(B, T, C);
-  const BwdLayout l = bwd_layout(g);
-  if (!workspace || workspace_bytes < l.total) return WKV_ERR_WORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  WsHeader* hdr = static_cast<WsHeader*>(workspace);
-  const int skip = g_skip_chunk.load();
-  const uint64_t budget = (uint64_t)g_budget_ns.load();
-  bool seq = false;
-  cudaError_t e = sequential_mode(g, seq);
-  if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
-  if (seq)
-    return backward_sequential(g, l, kv_dtype, w, u, k, v, gy, ckpt, gw, gu, gk, gv, hdr, workspace, budget, s);
-  if (kv_dtype != WKV_F32) {
-    set_last_error("wkv_backward: bf16 inputs are taken by the sequential kernels only (the chunked scan is forced)");
-    return WKV_ERR_UNSUPPORTED;
-  }
-
-  const float* states = ckpt;
-  if (!states) {
-    // recompute the chunk-boundary states: forward scan without outputs
-    char* fws = bytes(workspace) + l.fwd;
-    const FwdLayout fl = fwd_layout(g);
-    FwdArgs f;
-    std::memset(&f, 0, sizeof(f));
-    f.w = w;
-    f.u = u;
-    f.k = k;
-    f.v = v;
-    f.y = nullptr;
-    f.agg = reinterpret_cast<Rec*>(fws + fl.agg);
-    f.inc = reinterpret_cast<Rec*>(fws + fl.inc);
-    f.ckpt = reinterpret_cast<float*>(fws + fl.ckpt);
-    f.ticket = &hdr->ticket[1];  // counters stay in the outer header: its place never moves
-    f.exited = &hdr->exited[1];
-    f.eh = hdr;
-    f.g = g;
-    f.budget_ns = budget;
-    f.debug_skip_chunk = -1;
-    f.use_tma = make_tile_map(&f.tk, k, B, T, C, 4, kCtaChannels) && make_tile_map(&f.tv, v, B, T, C, 4, kCtaChannels);
-    e = launch_forward(f, WKV_F32, false, s);
-    if (e != cudaSuccess) return cuda_fail(e, "wkv_backward: state pass");
-    states = f.ckpt;
-  }
-
-  BwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.w = w;
-  a.u = u;
-  a.k = static_cast<const float*>(k);
-  a.v = static_cast<const float*>(v);
-  a.gy = static_cast<const float*>(gy);
-  a.ckpt = states;
-  a.gk = gk;
-  a.gv = gv;
-  a.ragg = reinterpret_cast<Rec*>(bytes(workspace) + l.ragg);
-  a.rinc = reinterpret_cast<Rec*>(bytes(workspace) + l.rinc);
-  a.part = reinterpret_cast<float*>(bytes(workspace) + l.part);
-  a.ticket = &hdr->ticket[2];
-  a.exited = &hdr->exited[2];
-  a.eh = hdr;
-  a.g = g;
-  a.budget_ns = budget;
-  a.debug_skip_chunk = skip;
-  a.use_tma = make_tile_map(&a.tk, k, B, T, C, 4, kCtaChannels) && make_tile_map(&a.tv, v, B, T, C, 4, kCtaChannels) &&
-              make_tile_map(&a.tg, gy, B, T, C, 4, kCtaChannels);
-  e = launch_backward(a, s);
-  if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
-
-  ReduceArgs r;
-  r.part = a.part;
-  r.slices = reinterpret_cast<float*>(bytes(workspace) + l.slices);
-  r.count = reinterpret_cast<unsigned long long*>(bytes(workspace) + l.count);
-  r.eh = hdr;
-  r.gw = gw;
-  r.gu = gu;
-  r.rows = g.nchunks * g.B;
-  r.C = C;
-  r.nslice = l.nslice;
-  e = launch_reduce(r, s);
-  return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_backward: reduce");
+  if (!r || !gr) return WKV_ERR_INVALID_ARG;
+  return backward_impl(B, T, C, kv_dtype, w, u, k, v, gout, r, ckpt, gw, gu, gk, gv, gr, workspace, workspace_bytes,
+                       stream);
 }
 
 wkv_status wkv_decode_step(int L, int B, int C, const float* x, const float* x_prev, const float* mu_k,

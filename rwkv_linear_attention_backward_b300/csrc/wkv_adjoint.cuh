@@ -73,8 +73,27 @@ __device__ __forceinline__ float exact_states(const E* sk, const E* sv, int len,
   return s.pp;
 }
 
+// The gradient reaching wkv_t from the staged plane sg at offset o: gy
+// itself (RP = 0), or, for the gated output out_t = sigmoid(r_t) wkv_t, the
+// output's gradient times sigmoid(r_t), with the r plane staged RP elements
+// after sg.  gq receives the factor that turns wkv_t into gr_t: gout
+// sigmoid'(r) = gy (1 - sigmoid(r)) (0 without the gate).
+template <int RP, typename E>
+__device__ __forceinline__ float gate_grad(const E* sg, int o, float& gq) {
+  const float g = to_f32<E>(sg[o]);
+  if constexpr (RP == 0) {
+    gq = 0.f;
+    return g;
+  } else {
+    const float s = sigmoid(to_f32<E>(sg[o + RP]));
+    const float gy = g * s;
+    gq = fmaf(-gy, s, gy);
+    return gy;
+  }
+}
+
 // The zero-carry adjoint at the chunk start, scaled by e^{pp there}.
-template <int S, typename E = float>
+template <int S, typename E = float, int RP = 0>
 __device__ __forceinline__ void exact_zero_adjoint(const E* sk, const E* sv, const E* sg, int len, float w, float u,
                                                    const float* xa, const float* xb, const float* xp, float& la,
                                                    float& lb) {
@@ -82,8 +101,9 @@ __device__ __forceinline__ void exact_zero_adjoint(const E* sk, const E* sv, con
   lb = 0.f;
 #pragma unroll 1
   for (int i = len - 1; i >= 0; --i) {
+    float gq;
     const Local o = local_terms(State{xa[i], xb[i], xp[i]}, to_f32<E>(sk[i * S]), to_f32<E>(sv[i * S]),
-                                to_f32<E>(sg[i * S]), w, u);
+                                gate_grad<RP>(sg, i * S, gq), w, u);
     la = carry(o.t, la, o.gb);
     lb = carry(o.t, lb, -o.gb * o.y);
   }
@@ -91,17 +111,19 @@ __device__ __forceinline__ void exact_zero_adjoint(const E* sk, const E* sv, con
 
 // gk, gv with the carry (la, lb, scaled by e^{pp after the chunk});
 // out[0..1] receive the gw, gu partial sums, out[2..3] the adjoint at the
-// chunk start.
-template <int S, typename E = float>
+// chunk start.  With the gate (RP != 0, see gate_grad) gr goes to grp.
+template <int S, typename E = float, int RP = 0>
 __device__ __forceinline__ void exact_final(const E* sk, const E* sv, const E* sg, int len, float w, float u,
                                             const float* xa, const float* xb, const float* xp, float la, float lb,
-                                            float* gkp, float* gvp, int64_t C, bool valid, float* out) {
+                                            float* gkp, float* gvp, int64_t C, bool valid, float* out,
+                                            float* grp = nullptr) {
   float gw_acc = 0.f, gu_acc = 0.f;
 #pragma unroll 1
   for (int i = len - 1; i >= 0; --i) {
     const State si{xa[i], xb[i], xp[i]};
     const float k = to_f32<E>(sk[i * S]), v = to_f32<E>(sv[i * S]);
-    const Local o = local_terms(si, k, v, to_f32<E>(sg[i * S]), w, u);
+    float gq;
+    const Local o = local_terms(si, k, v, gate_grad<RP>(sg, i * S, gq), w, u);
     const float cur = o.gc * o.vmy;
     const float gk = fmaf(o.t.kap, fmaf(la, v, lb), cur);
     const float gv = fmaf(o.t.kap, la, o.gc);
@@ -113,6 +135,7 @@ __device__ __forceinline__ void exact_final(const E* sk, const E* sv, const E* s
     if (valid) {
       __stcs(gkp + (int64_t)i * C, gk);
       __stcs(gvp + (int64_t)i * C, gv);
+      if constexpr (RP != 0) __stcs(grp + (int64_t)i * C, gq * o.y);
     }
   }
   out[0] = gw_acc;

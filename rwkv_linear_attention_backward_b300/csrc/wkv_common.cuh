@@ -60,6 +60,11 @@ __device__ __forceinline__ float exp_neg_abs(float d) { return ex2(-fabsf(d) * k
 
 __device__ __forceinline__ float exp_nat(float x) { return ex2(x * kLog2e); }
 
+// sigmoid(r) = 1 / (1 + e^{-r}), the receptance gate on the time-mixing
+// output: 0 once e^{-r} overflows (r below about -88), 1 once e^{-r} is
+// below half an ulp of 1.
+__device__ __forceinline__ float sigmoid(float r) { return rcp(1.f + exp_nat(-r)); }
+
 struct State {
   float num, den, pp;
 };

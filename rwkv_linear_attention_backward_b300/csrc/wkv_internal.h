@@ -122,6 +122,7 @@ struct SeqFwdArgs {
   const void* k;
   const void* v;
   float* y;               // may be null (state-only pass)
+  const void* r;          // [B, T, C] of the k, v type, or null: y = sigmoid(r) wkv (the gated output)
   float* ckpt;            // [3][nchunks][B][C] state after each chunk
   const float* state_in;  // [3][B][C] state before the first token (num, den, pp planes); null: empty
   float* state_out;       // [3][B][C] state after the last token; may be null
@@ -137,15 +138,17 @@ struct SeqFwdArgs {
 };
 
 struct SeqBwdArgs {
-  CUtensorMap tk, tv, tg;
+  CUtensorMap tk, tv, tg, tr;  // tr: of r (gated launches)
   const float* w;
   const float* u;
-  const void* k;   // k, v, gy: float or bf16 (kv_dtype of the launch)
+  const void* k;   // k, v, gy, r: float or bf16 (kv_dtype of the launch)
   const void* v;
-  const void* gy;
+  const void* gy;  // with r: the gradient of the gated output sigmoid(r) wkv
+  const void* r;   // null: ungated
   const float* ckpt;
   float* gk;
   float* gv;
+  float* gr;       // [B, T, C] (gated launches)
   float* part;            // [2][nseg * B][C] gw, gu sums per (run, batch row)
   Rec* recs;              // [nseg][B][C] run summaries (tagged records)
   unsigned int* exited;
@@ -157,7 +160,8 @@ struct SeqBwdArgs {
   int use_tma;
 };
 
-// Choose the runs per column (written to a.nseg) and launch.
+// Choose the runs per column (written to a.nseg) and launch; a.r non-null
+// selects the gated kernels.
 cudaError_t launch_seq_forward(SeqFwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
 cudaError_t launch_seq_backward(SeqBwdArgs& a, int kv_dtype, cudaStream_t s);
 

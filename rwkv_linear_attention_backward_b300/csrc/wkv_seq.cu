@@ -140,18 +140,47 @@ __device__ __forceinline__ float tree_min(const float* x) {
 }
 
 // ------------------------------------------------------------------ forward
+// What a forward walk writes per token: nothing (a state-only pass), wkv_t,
+// or the gated output sigmoid(r_t) wkv_t.
+constexpr int kYNone = 0, kYWkv = 1, kYGated = 2;
+
+// The gate's input for output i of a chunk (rp: r at the chunk's first
+// token of this lane's channel, token stride `stride`); 0 unless gated.
+template <typename KV, int YM>
+__device__ __forceinline__ float load_r(const KV* __restrict__ rp, int i, int64_t stride, bool valid) {
+  if constexpr (YM == kYGated) return valid ? to_f32<KV>(__ldg(rp + (int64_t)i * stride)) : 0.f;
+  return 0.f;
+}
+
+// Stores output i of a chunk (yp: y at the chunk's first token): wkv_t, or
+// sigmoid(r) wkv_t when gated.
+template <int YM>
+__device__ __forceinline__ void put_y(float* __restrict__ yp, int i, int64_t stride, float yv, float r, bool valid) {
+  if (!valid) return;
+  if constexpr (YM == kYGated) yv *= sigmoid(r);
+  __stcs(yp + (int64_t)i * stride, yv);
+}
+
 // A whole chunk of the forward pass for this lane, with every loop fully
 // unrolled and no per-token branch: the one warp of a column has no other
 // warp to hide latencies behind, so each phase is written as independent
 // work per token (the k values and then ek in registers; the statistics by
 // trees) and only the carried sums form chains.  Same arithmetic, in the
 // same order per value, as the generic form below.
-template <typename KV, bool WRITE_Y>
+template <typename KV, int YM>
 __device__ __forceinline__ void seq_fwd_full(const KV* __restrict__ sk, const KV* __restrict__ sv, float w, float u,
-                                             float ew, float eu, State& P, float* __restrict__ yp, int64_t ystride,
-                                             bool valid) {
+                                             float ew, float eu, State& P, float* __restrict__ yp,
+                                             const KV* __restrict__ rp, int64_t ystride, bool valid) {
   constexpr int L = kChunk;
   constexpr int S = kSeqChannels;
+  // the gate's r for the whole chunk first: independent global loads, in
+  // flight while the chunk is computed (loaded one by one next to the y
+  // stores, each would wait for the last)
+  float rg[L];
+  if constexpr (YM == kYGated) {
+#pragma unroll
+    for (int i = 0; i < L; ++i) rg[i] = load_r<KV, YM>(rp, i, ystride, valid);
+  }
   float kr[L], rr[L];
 #pragma unroll
   for (int i = 0; i < L; ++i) {
@@ -180,7 +209,7 @@ __device__ __forceinline__ void seq_fwd_full(const KV* __restrict__ sk, const KV
 #pragma unroll
     for (int i = 0; i < L; ++i) {
       const float ekv = kr[i] * vr[i];
-      if constexpr (WRITE_Y) {
+      if constexpr (YM != kYNone) {
         A[i] = na;
         Bd[i] = nb;
         na = fmaf(na, ew, ekv);
@@ -189,12 +218,12 @@ __device__ __forceinline__ void seq_fwd_full(const KV* __restrict__ sk, const KV
       on = fmaf(on, ew, ekv);
       od = fmaf(od, ew, kr[i]);
     }
-    if constexpr (WRITE_Y) {
+    if constexpr (YM != kYNone) {
 #pragma unroll
       for (int i = 0; i < L; ++i) {
         const float ec = kr[i] * eu;
         const float yv = fmaf(ec, vr[i], A[i]) * rcp(Bd[i] + ec);
-        if (valid) __stcs(yp + (int64_t)i * ystride, yv);
+        put_y<YM>(yp, i, ystride, yv, YM == kYGated ? rg[i] : 0.f, valid);
       }
     }
     const float sc = exp_nat(F - r);
@@ -204,9 +233,9 @@ __device__ __forceinline__ void seq_fwd_full(const KV* __restrict__ sk, const KV
     for (int i = 0; i < L; ++i) {
       const float kk = to_f32<KV>(sk[i * S]);
       const float vv = to_f32<KV>(sv[i * S]);
-      if constexpr (WRITE_Y) {
+      if constexpr (YM != kYNone) {
         const float yv = output(P, kk, vv, u);
-        if (valid) __stcs(yp + (int64_t)i * ystride, yv);
+        put_y<YM>(yp, i, ystride, yv, load_r<KV, YM>(rp, i, ystride, valid), valid);
       }
       step(P, kk, vv, w);
     }
@@ -214,12 +243,12 @@ __device__ __forceinline__ void seq_fwd_full(const KV* __restrict__ sk, const KV
 }
 
 // One chunk of n <= kChunk tokens (the generic form, for the partial last
-// chunk): outputs from the carried state P (when WRITE_Y), then P advanced
+// chunk): outputs from the carried state P (unless YM is kYNone), then P advanced
 // past the chunk.
-template <typename KV, bool WRITE_Y>
+template <typename KV, int YM>
 __device__ __forceinline__ void seq_fwd_chunk(const KV* __restrict__ sk, const KV* __restrict__ sv, int n, float w,
                                               float u, float ew, float eu, State& P, float* __restrict__ yp,
-                                              int64_t ystride, bool valid) {
+                                              const KV* __restrict__ rp, int64_t ystride, bool valid) {
   constexpr int S = kSeqChannels;
   float F = -3.0e38f, kmin = 3.0e38f, r = -3.0e38f;
 #pragma unroll 8
@@ -240,10 +269,10 @@ __device__ __forceinline__ void seq_fwd_chunk(const KV* __restrict__ sk, const K
       const float ek = ex2(fmaf(to_f32<KV>(sk[i * S]), kLog2e, -F2));
       const float vv = to_f32<KV>(sv[i * S]);
       const float ekv = ek * vv;
-      if constexpr (WRITE_Y) {
+      if constexpr (YM != kYNone) {
         const float ec = ek * eu;
         const float yv = fmaf(ec, vv, na) * rcp(nb + ec);
-        if (valid) __stcs(yp + (int64_t)i * ystride, yv);
+        put_y<YM>(yp, i, ystride, yv, load_r<KV, YM>(rp, i, ystride, valid), valid);
         na = fmaf(na, ew, ekv);
         nb = fmaf(nb, ew, ek);
       }
@@ -259,9 +288,9 @@ __device__ __forceinline__ void seq_fwd_chunk(const KV* __restrict__ sk, const K
     for (int i = 0; i < n; ++i) {
       const float kk = to_f32<KV>(sk[i * S]);
       const float vv = to_f32<KV>(sv[i * S]);
-      if constexpr (WRITE_Y) {
+      if constexpr (YM != kYNone) {
         const float yv = output(P, kk, vv, u);
-        if (valid) __stcs(yp + (int64_t)i * ystride, yv);
+        put_y<YM>(yp, i, ystride, yv, load_r<KV, YM>(rp, i, ystride, valid), valid);
       }
       step(P, kk, vv, w);
     }
@@ -341,7 +370,7 @@ __device__ __forceinline__ bool wait_rec(const Rec* p, bool valid, const Launch&
   }
 }
 
-template <typename KV, int NS, bool WRITE_Y>
+template <typename KV, int NS, int YM>
 __device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L, unsigned char* smem) {
   KV* ring = reinterpret_cast<KV*>(smem);  // stage s: k at 2s*kSeqTile, v at (2s+1)*kSeqTile
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + seq_ring_elems<KV, NS>(2) * sizeof(KV));
@@ -417,9 +446,9 @@ __device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L
     const int j = chunk_of(it);
     const int n = min(kChunk, g.T - j * kChunk);
     if (n == kChunk)
-      seq_fwd_full<KV, false>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, P, nullptr, 0, false);
+      seq_fwd_full<KV, kYNone>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, P, nullptr, nullptr, 0, false);
     else
-      seq_fwd_chunk<KV, false>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, nullptr, 0, false);
+      seq_fwd_chunk<KV, kYNone>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, nullptr, nullptr, 0, false);
     release(it);
   }
   const bool skip = a.debug_skip_chunk >= first && a.debug_skip_chunk < first + count;  // fault injection
@@ -442,11 +471,13 @@ __device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L
     if (!acquire(it, dk)) return fail(it);
     const int j = chunk_of(it);
     const int n = min(kChunk, g.T - j * kChunk);
-    float* yp = WRITE_Y ? a.y + ((int64_t)col.b * g.T + (int64_t)j * kChunk) * g.C + col.c : nullptr;
+    const int64_t row = ((int64_t)col.b * g.T + (int64_t)j * kChunk) * g.C + col.c;
+    float* yp = YM != kYNone ? a.y + row : nullptr;
+    const KV* rp = YM == kYGated ? static_cast<const KV*>(a.r) + row : nullptr;
     if (n == kChunk)
-      seq_fwd_full<KV, WRITE_Y>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, P, yp, g.C, col.valid);
+      seq_fwd_full<KV, YM>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, P, yp, rp, g.C, col.valid);
     else
-      seq_fwd_chunk<KV, WRITE_Y>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, yp, g.C, col.valid);
+      seq_fwd_chunk<KV, YM>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, yp, rp, g.C, col.valid);
     if (col.valid) {
       const size_t o = (size_t)j * jstride + rec0;
       a.ckpt[o] = P.num;
@@ -471,7 +502,7 @@ __device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L
 // which its warp reaches before any later run of its own, and every warp is
 // resident (cooperative launch), so the waits always end.  The last run
 // publishes nothing and needs no phase 1.
-template <typename KV, int NS, bool WRITE_Y>
+template <typename KV, int NS, int YM>
 __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch& L, unsigned char* smem) {
   KV* ring = reinterpret_cast<KV*>(smem);  // stage s: k at 2s*kSeqTile, v at (2s+1)*kSeqTile
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + seq_ring_elems<KV, NS>(2) * sizeof(KV));
@@ -568,16 +599,18 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
     if (m.p1) {
       if (m.first) S = empty_state();
       if (n == kChunk)
-        seq_fwd_full<KV, false>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, S, nullptr, 0, false);
+        seq_fwd_full<KV, kYNone>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, S, nullptr, nullptr, 0, false);
       else
-        seq_fwd_chunk<KV, false>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, S, nullptr, 0, false);
+        seq_fwd_chunk<KV, kYNone>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, S, nullptr, nullptr, 0, false);
     } else {
       if (m.first && m.r == R - 1 && !carry_in(m.r, P)) return fail(it);
-      float* yp = WRITE_Y ? a.y + ((int64_t)col.b * g.T + (int64_t)m.j * kChunk) * g.C + col.c : nullptr;
+      const int64_t row = ((int64_t)col.b * g.T + (int64_t)m.j * kChunk) * g.C + col.c;
+      float* yp = YM != kYNone ? a.y + row : nullptr;
+      const KV* rp = YM == kYGated ? static_cast<const KV*>(a.r) + row : nullptr;
       if (n == kChunk)
-        seq_fwd_full<KV, WRITE_Y>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, P, yp, g.C, col.valid);
+        seq_fwd_full<KV, YM>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, P, yp, rp, g.C, col.valid);
       else
-        seq_fwd_chunk<KV, WRITE_Y>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, yp, g.C, col.valid);
+        seq_fwd_chunk<KV, YM>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, yp, rp, g.C, col.valid);
       if (col.valid) {
         const size_t o = (size_t)m.j * jstride + rec0;
         a.ckpt[o] = P.num;
@@ -605,14 +638,14 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
 // CHAIN: chained runs (seq_fwd_chain), else runs exchanging summaries
 // (seq_fwd_run); separate kernels, so that each holds only its own code
 // (both in one kernel overflowed the instruction cache).
-template <typename KV, int NS, bool WRITE_Y, bool CHAIN>
+template <typename KV, int NS, int YM, bool CHAIN>
 __global__ void __launch_bounds__(kSeqChannels) seq_fwd_kernel(const __grid_constant__ SeqFwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Launch L = seq_launch(a.eh);
   if constexpr (CHAIN)
-    seq_fwd_chain<KV, NS, WRITE_Y>(a, L, smem);
+    seq_fwd_chain<KV, NS, YM>(a, L, smem);
   else
-    seq_fwd_run<KV, NS, WRITE_Y>(a, L, smem);
+    seq_fwd_run<KV, NS, YM>(a, L, smem);
   seq_exit(a.exited, a.eh, L.epoch);
 }
 
@@ -641,13 +674,16 @@ __device__ __forceinline__ void kahan_add(float& s, float& k, float x) {
 // per-token branch and ek kept in registers (see seq_fwd_full); otherwise
 // the first n tokens, each token under its own predicate, ek computed again
 // where the reverse sweep needs it.  KV: the staged element type (float or
-// bf16; the arithmetic is fp32).
-template <bool FULL, typename KV>
+// bf16; the arithmetic is fp32).  RP: 0, or for the gated output the offset
+// of the staged r plane from the output-gradient plane sg (gate_grad); then
+// gr_t = gout_t sigmoid'(r_t) wkv_t goes to grp.
+template <bool FULL, typename KV, int RP>
 __device__ __forceinline__ void seq_bwd_chunk(const KV* __restrict__ sk, const KV* __restrict__ sv,
                                               const KV* __restrict__ sg, int n, const BwdColumn& cw,
                                               const State& P, bool has_succ, Adj& X, float* __restrict__ gkp,
-                                              float* __restrict__ gvp, int64_t stride, bool valid, float& gw_acc,
-                                              float& gu_acc, float* xa, float* xb, float* xp) {
+                                              float* __restrict__ gvp, float* __restrict__ grp, int64_t stride,
+                                              bool valid, float& gw_acc, float& gu_acc, float* xa, float* xb,
+                                              float* xp) {
   constexpr int L = kChunk;
   constexpr int S = kSeqChannels;
   if constexpr (FULL) n = L;
@@ -711,8 +747,13 @@ __device__ __forceinline__ void seq_bwd_chunk(const KV* __restrict__ sk, const K
       for (int i = 0; i < L; ++i) {
         const float ec = kr[i] * cw.eu;
         const float rr = rcp(Bd[i] + ec);
-        GI[i] = to_f32<KV>(sg[i * S]) * rr;                        // gN at scale e^{F}
-        VM[i] = fmaf(to_f32<KV>(sv[i * S]), Bd[i], -A[i]) * rr;  // v - wkv
+        const float vv = to_f32<KV>(sv[i * S]);
+        float gq;
+        GI[i] = gate_grad<RP>(sg, i * S, gq) * rr;  // gN at scale e^{F}
+        VM[i] = fmaf(vv, Bd[i], -A[i]) * rr;        // v - wkv
+        if constexpr (RP != 0) {
+          if (valid) __stcs(grp + (int64_t)i * stride, gq * (fmaf(ec, vv, A[i]) * rr));
+        }
       }
 #pragma unroll
       for (int i = L - 1; i >= 0; --i) {
@@ -746,7 +787,8 @@ __device__ __forceinline__ void seq_bwd_chunk(const KV* __restrict__ sk, const K
         const float vv = to_f32<KV>(sv[i * S]);
         const float ec = ek * cw.eu;
         const float rr = rcp(Bd[i] + ec);
-        const float gi = to_f32<KV>(sg[i * S]) * rr;
+        float gq;
+        const float gi = gate_grad<RP>(sg, i * S, gq) * rr;
         const float vmy = fmaf(vv, Bd[i], -A[i]) * rr;  // v - wkv
         const float cur = gi * vmy * ec;                // (gN v + gD) e^{u+k}
         const float gk = fmaf(fmaf(la, vv, lb), ek, cur);
@@ -760,6 +802,7 @@ __device__ __forceinline__ void seq_bwd_chunk(const KV* __restrict__ sk, const K
         if (valid) {
           __stcs(gkp + (int64_t)i * stride, gk);
           __stcs(gvp + (int64_t)i * stride, gv);
+          if constexpr (RP != 0) __stcs(grp + (int64_t)i * stride, gq * (fmaf(ec, vv, A[i]) * rr));
         }
       }
     }
@@ -771,8 +814,8 @@ __device__ __forceinline__ void seq_bwd_chunk(const KV* __restrict__ sk, const K
     const float pp_end = exact_states<kSeqChannels, KV>(sk, sv, n, P, cw.w, xa, xb, xp);
     const float f = has_succ ? exp_nat(pp_end - X.f) : 0.f;
     float res[4];
-    exact_final<kSeqChannels, KV>(sk, sv, sg, n, cw.w, cw.u, xa, xb, xp, X.la * f, X.lb * f, gkp, gvp, stride, valid,
-                              res);
+    exact_final<kSeqChannels, KV, RP>(sk, sv, sg, n, cw.w, cw.u, xa, xb, xp, X.la * f, X.lb * f, gkp, gvp, stride,
+                                      valid, res, grp);
     gw_acc = res[0];
     gu_acc = res[1];
     X = Adj{res[2], res[3], P.pp};
@@ -784,7 +827,7 @@ __device__ __forceinline__ void seq_bwd_chunk(const KV* __restrict__ sk, const K
 // by e^{P.pp}, P the state before the chunk.  The forward sums and the
 // adjoint accumulate in one forward sweep, each token's gN, gD weighted by
 // e^{-(t - t0) w} (pw), as in the chunked backward pass's summary.
-template <bool FULL, typename KV>
+template <bool FULL, typename KV, int RP>
 __device__ __forceinline__ Adj seq_bwd_summary(const KV* __restrict__ sk, const KV* __restrict__ sv,
                                                const KV* __restrict__ sg, int n, const BwdColumn& cw,
                                                const State& P, float* xa, float* xb, float* xp) {
@@ -824,7 +867,8 @@ __device__ __forceinline__ Adj seq_bwd_summary(const KV* __restrict__ sk, const 
         const float vv = to_f32<KV>(sv[i * S]);
         const float ec = ek * cw.eu;
         const float rr = rcp(nb + ec);
-        const float gi = to_f32<KV>(sg[i * S]) * rr;        // gN at scale e^{F}
+        float gq;
+        const float gi = gate_grad<RP>(sg, i * S, gq) * rr;  // gN at scale e^{F}
         const float y = fmaf(ec, vv, na) * rr;  // wkv_t
         la = fmaf(pw, gi, la);
         lb = fmaf(-pw, gi * y, lb);
@@ -839,7 +883,8 @@ __device__ __forceinline__ Adj seq_bwd_summary(const KV* __restrict__ sk, const 
         const float vv = to_f32<KV>(sv[i * S]);
         const float ec = ek * cw.eu;
         const float rr = rcp(nb + ec);
-        const float gi = to_f32<KV>(sg[i * S]) * rr;
+        float gq;
+        const float gi = gate_grad<RP>(sg, i * S, gq) * rr;
         const float y = fmaf(ec, vv, na) * rr;
         la = fmaf(pw, gi, la);
         lb = fmaf(-pw, gi * y, lb);
@@ -852,15 +897,19 @@ __device__ __forceinline__ Adj seq_bwd_summary(const KV* __restrict__ sk, const 
     lb *= s0;
   } else {
     exact_states<kSeqChannels, KV>(sk, sv, n, P, cw.w, xa, xb, xp);
-    exact_zero_adjoint<kSeqChannels, KV>(sk, sv, sg, n, cw.w, cw.u, xa, xb, xp, la, lb);
+    exact_zero_adjoint<kSeqChannels, KV, RP>(sk, sv, sg, n, cw.w, cw.u, xa, xb, xp, la, lb);
   }
   return Adj{la, lb, P.pp};
 }
 
-template <typename KV, int NS>
+// GATE: the gated output (SeqBwdArgs::r): the staged planes are k, v, the
+// output's gradient and r.
+template <typename KV, int NS, bool GATE>
 __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L, unsigned char* smem) {
-  KV* ring = reinterpret_cast<KV*>(smem);  // stage s: k, v, gy at (3s + 0..2) * kSeqTile
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + seq_ring_elems<KV, NS>(3) * sizeof(KV));
+  constexpr int NP = GATE ? 4 : 3;              // planes per stage
+  constexpr int RP = GATE ? kSeqTile : 0;       // r's plane after the gradient's
+  KV* ring = reinterpret_cast<KV*>(smem);  // stage s: k, v, gy (, r) at (NP s + 0..NP-1) * kSeqTile
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + seq_ring_elems<KV, NS>(NP) * sizeof(KV));
   const int lane = threadIdx.x;
   const ScanGeometry& g = a.g;
   const int nseg = a.nseg;
@@ -873,7 +922,7 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
   cw.eu = expf(cw.u);
   cw.gw_s = cw.gw_k = cw.gu_s = cw.gu_k = 0.f;
   const bool tma = a.use_tma != 0;
-  constexpr uint32_t kStageBytes = 3 * kSeqTile * sizeof(KV);
+  constexpr uint32_t kStageBytes = NP * kSeqTile * sizeof(KV);
   const int last = g.nchunks - 1;
 
   int first, count;  // in walk order: position p is chunk last - p
@@ -884,11 +933,12 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
   auto issue = [&](int it) {  // lane 0: item it into its stage
     const int s = it % NS;
     const int j = chunk_of(it);
-    KV* dk = ring + (size_t)(3 * s) * kSeqTile;
+    KV* dk = ring + (size_t)(NP * s) * kSeqTile;
     mbar_arrive_expect_tx(&full[s], kStageBytes);
     tma_load_3d(dk, &a.tk, &full[s], col.c0, j * kChunk, col.b);
     tma_load_3d(dk + kSeqTile, &a.tv, &full[s], col.c0, j * kChunk, col.b);
     tma_load_3d(dk + 2 * kSeqTile, &a.tg, &full[s], col.c0, j * kChunk, col.b);
+    if constexpr (GATE) tma_load_3d(dk + 3 * kSeqTile, &a.tr, &full[s], col.c0, j * kChunk, col.b);
   };
   int issued = 0;
   if (tma) {
@@ -898,6 +948,7 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
       tma_prefetch_desc(&a.tk);
       tma_prefetch_desc(&a.tv);
       tma_prefetch_desc(&a.tg);
+      if constexpr (GATE) tma_prefetch_desc(&a.tr);
       for (int it = 0; it < NS && it < nitems; ++it) issue(it);
     }
     issued = min(NS, nitems);
@@ -905,12 +956,13 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
   }
   auto acquire = [&](int it, KV*& dk) {
     const int s = it % NS;
-    dk = ring + (size_t)(3 * s) * kSeqTile;
+    dk = ring + (size_t)(NP * s) * kSeqTile;
     if (tma) return stage_wait(&full[s], (uint32_t)((it / NS) & 1), a.budget_ns);
     const int j = chunk_of(it);
     copy_box_plain(dk, static_cast<const KV*>(a.k), g, col, j * kChunk);
     copy_box_plain(dk + kSeqTile, static_cast<const KV*>(a.v), g, col, j * kChunk);
     copy_box_plain(dk + 2 * kSeqTile, static_cast<const KV*>(a.gy), g, col, j * kChunk);
+    if constexpr (GATE) copy_box_plain(dk + 3 * kSeqTile, static_cast<const KV*>(a.r), g, col, j * kChunk);
     __syncwarp();
     return true;
   };
@@ -947,11 +999,10 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
     if (!acquire(it, dk)) return fail(it);
     const int j = chunk_of(it);
     const int n = min(kChunk, g.T - j * kChunk);
-    const Adj A = n == kChunk
-                      ? seq_bwd_summary<true, KV>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P,
-                                              xa, xb, xp)
-                      : seq_bwd_summary<false, KV>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P,
-                                               xa, xb, xp);
+    const Adj A = n == kChunk ? seq_bwd_summary<true, KV, RP>(dk + lane, dk + kSeqTile + lane,
+                                                                dk + 2 * kSeqTile + lane, n, cw, P, xa, xb, xp)
+                              : seq_bwd_summary<false, KV, RP>(dk + lane, dk + kSeqTile + lane,
+                                                                 dk + 2 * kSeqTile + lane, n, cw, P, xa, xb, xp);
     X = it == 0 ? A : fold_adj(A, (float)n * cw.w, X);
     release(it);
   }
@@ -982,12 +1033,13 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
     const int n = min(kChunk, g.T - j * kChunk);
     const int64_t row = ((int64_t)col.b * g.T + (int64_t)j * kChunk) * g.C + col.c;
     float gw_acc, gu_acc;
+    float* grp = GATE ? a.gr + row : nullptr;
     if (n == kChunk)
-      seq_bwd_chunk<true, KV>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last, X,
-                          a.gk + row, a.gv + row, g.C, col.valid, gw_acc, gu_acc, xa, xb, xp);
+      seq_bwd_chunk<true, KV, RP>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last, X,
+                                  a.gk + row, a.gv + row, grp, g.C, col.valid, gw_acc, gu_acc, xa, xb, xp);
     else
-      seq_bwd_chunk<false, KV>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last, X,
-                           a.gk + row, a.gv + row, g.C, col.valid, gw_acc, gu_acc, xa, xb, xp);
+      seq_bwd_chunk<false, KV, RP>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last,
+                                   X, a.gk + row, a.gv + row, grp, g.C, col.valid, gw_acc, gu_acc, xa, xb, xp);
     kahan_add(cw.gw_s, cw.gw_k, gw_acc);
     kahan_add(cw.gu_s, cw.gu_k, gu_acc);
     release(it);
@@ -1001,11 +1053,11 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
   }
 }
 
-template <typename KV, int NS>
+template <typename KV, int NS, bool GATE>
 __global__ void __launch_bounds__(kSeqChannels) seq_bwd_kernel(const __grid_constant__ SeqBwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Launch L = seq_launch(a.eh);
-  seq_bwd_run<KV, NS>(a, L, smem);
+  seq_bwd_run<KV, NS, GATE>(a, L, smem);
   seq_exit(a.exited, a.eh, L.epoch);
 }
 
@@ -1173,23 +1225,23 @@ cudaError_t launch_planned(const DevInfo& d, Args& a, int arrays, size_t elem, s
   return launch_staged<Args, Kern>(d, a, nblk, stage, coop, s);
 }
 
-template <typename KV, bool WRITE_Y, bool CHAIN>
+template <typename KV, int YM, bool CHAIN>
 struct FwdKern {
   template <int NS>
   struct At {
-    static constexpr void (*fn)(SeqFwdArgs) = seq_fwd_kernel<KV, NS, WRITE_Y, CHAIN>;
+    static constexpr void (*fn)(SeqFwdArgs) = seq_fwd_kernel<KV, NS, YM, CHAIN>;
   };
 };
 
-template <typename KV>
+template <typename KV, bool GATE>
 struct BwdKern {
   template <int NS>
   struct At {
-    static constexpr void (*fn)(SeqBwdArgs) = seq_bwd_kernel<KV, NS>;
+    static constexpr void (*fn)(SeqBwdArgs) = seq_bwd_kernel<KV, NS, GATE>;
   };
 };
 
-template <typename KV, bool WRITE_Y>
+template <typename KV, int YM>
 cudaError_t launch_seq_fwd_t(SeqFwdArgs& a, cudaStream_t s) {
   DevInfo d;
   cudaError_t e = dev_info(d);
@@ -1197,31 +1249,37 @@ cudaError_t launch_seq_fwd_t(SeqFwdArgs& a, cudaStream_t s) {
   const size_t input_bytes = (size_t)a.g.B * a.g.T * a.g.C * 2 * sizeof(KV);
   // the forward kernel's registers allow more warps than its two stages of
   // shared memory: aim at 12 per SM
-  return launch_planned<SeqFwdArgs, FwdKern<KV, WRITE_Y, false>::template At, FwdKern<KV, WRITE_Y, true>::template At>(
+  return launch_planned<SeqFwdArgs, FwdKern<KV, YM, false>::template At, FwdKern<KV, YM, true>::template At>(
       d, a, 2, sizeof(KV), input_bytes, 12, s);
 }
 
 }  // namespace
 
 cudaError_t launch_seq_forward(SeqFwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s) {
-  if (kv_dtype == 0)
-    return write_y ? launch_seq_fwd_t<float, true>(a, s) : launch_seq_fwd_t<float, false>(a, s);
-  return write_y ? launch_seq_fwd_t<__nv_bfloat16, true>(a, s) : launch_seq_fwd_t<__nv_bfloat16, false>(a, s);
+  const int ym = !write_y ? kYNone : (a.r ? kYGated : kYWkv);
+  if (kv_dtype == 0) {
+    if (ym == kYGated) return launch_seq_fwd_t<float, kYGated>(a, s);
+    return ym == kYWkv ? launch_seq_fwd_t<float, kYWkv>(a, s) : launch_seq_fwd_t<float, kYNone>(a, s);
+  }
+  if (ym == kYGated) return launch_seq_fwd_t<__nv_bfloat16, kYGated>(a, s);
+  return ym == kYWkv ? launch_seq_fwd_t<__nv_bfloat16, kYWkv>(a, s) : launch_seq_fwd_t<__nv_bfloat16, kYNone>(a, s);
 }
 
-template <typename KV>
+template <typename KV, bool GATE>
 cudaError_t launch_seq_bwd_t(SeqBwdArgs& a, cudaStream_t s) {
   DevInfo d;
   cudaError_t e = dev_info(d);
   if (e != cudaSuccess) return e;
-  const size_t input_bytes = (size_t)a.g.B * a.g.T * a.g.C * 3 * sizeof(KV);
+  constexpr int NP = GATE ? 4 : 3;
+  const size_t input_bytes = (size_t)a.g.B * a.g.T * a.g.C * NP * sizeof(KV);
   // the backward kernel's registers (up to 255 per thread) allow 8 warps per SM
-  return launch_planned<SeqBwdArgs, BwdKern<KV>::template At, BwdKern<KV>::template At>(d, a, 3, sizeof(KV),
-                                                                                      input_bytes, 8, s);
+  return launch_planned<SeqBwdArgs, BwdKern<KV, GATE>::template At, BwdKern<KV, GATE>::template At>(
+      d, a, NP, sizeof(KV), input_bytes, 8, s);
 }
 
 cudaError_t launch_seq_backward(SeqBwdArgs& a, int kv_dtype, cudaStream_t s) {
-  return kv_dtype == 0 ? launch_seq_bwd_t<float>(a, s) : launch_seq_bwd_t<__nv_bfloat16>(a, s);
+  if (a.r) return kv_dtype == 0 ? launch_seq_bwd_t<float, true>(a, s) : launch_seq_bwd_t<__nv_bfloat16, true>(a, s);
+  return kv_dtype == 0 ? launch_seq_bwd_t<float, false>(a, s) : launch_seq_bwd_t<__nv_bfloat16, false>(a, s);
 }
 
 }  // namespace wkv

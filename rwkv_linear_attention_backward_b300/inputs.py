@@ -23,6 +23,9 @@ long       fwd only, bf16 k,v, fp32 state and output, B=1 T=131072
            C=2560; k ~ N(0,5^2), v ~ N(0,1); d ~ U(-8,1); u ~ U(-1,1)
 l169m_bf16 fwd+bwd with bf16 k, v, gy (fp32 arithmetic and outputs), the
            l169m shape and distributions
+l169m_gated fwd+bwd of the gated output sigmoid(r) * wkv, the l169m shape
+           and distributions, r ~ N(0,2^2) (gy is the gated output's
+           gradient)
 shift      token shift of the training path, fwd+bwd, B=16 T=4096 C=2048;
            x, gxk, gxv, gxr ~ N(0,1); x0 ~ N(0,1); mu_k, mu_v, mu_r ~ U(0,1)
 decode     RNN decode, L=32 layers, B=256, C=4096, 1024 steps; x, x_prev,
@@ -49,6 +52,7 @@ class TrainingWorkload:
     kv_dtype: str  # "f32" or "bf16"
     backward: bool
     seed: int
+    gated: bool = False  # the output gate sigmoid(r) * wkv (r from gate_inputs, seed + 1)
 
     @property
     def elements(self) -> int:
@@ -77,6 +81,7 @@ WORKLOADS = {
     "l1b5": TrainingWorkload("l1b5", 16, 4096, 2048, 3.0, -6.0, 2.0, "f32", True, 1003),
     "long": TrainingWorkload("long", 1, 131072, 2560, 5.0, -8.0, 1.0, "bf16", False, 1004),
     "l169m_bf16": TrainingWorkload("l169m_bf16", 8, 1024, 768, 3.0, -6.0, 2.0, "bf16", True, 1006),
+    "l169m_gated": TrainingWorkload("l169m_gated", 8, 1024, 768, 3.0, -6.0, 2.0, "f32", True, 1008, gated=True),
 }
 DECODE = DecodeWorkload("decode", 32, 256, 4096, 1024, -6.0, 2.0, 1005)
 
@@ -146,9 +151,27 @@ def training_inputs(B: int, T: int, C: int, *, seed: int, k_std: float = 1.0, d_
 
 
 def workload_inputs(name: str):
+    """(w, u, k, v, gy) of a named workload, and r (gate_inputs, seed + 1)
+    after them when the workload is gated."""
     wl = WORKLOADS[name]
-    return training_inputs(wl.B, wl.T, wl.C, seed=wl.seed, k_std=wl.k_std, d_lo=wl.d_lo, d_hi=wl.d_hi,
+    base = training_inputs(wl.B, wl.T, wl.C, seed=wl.seed, k_std=wl.k_std, d_lo=wl.d_lo, d_hi=wl.d_hi,
                            kv_dtype=wl.kv_dtype)
+    if wl.gated:
+        return base + (gate_inputs(wl.B, wl.T, wl.C, seed=wl.seed + 1, kv_dtype=wl.kv_dtype),)
+    return base
+
+
+def gate_inputs(B: int, T: int, C: int, *, seed: int, r_std: float = 2.0, kv_dtype: str = "f32"):
+    """Draw the receptance r [B,T,C] ~ N(0, r_std^2) of the output gate on the
+    CPU, from its own generator (so the WKV inputs drawn with another seed
+    keep their values); rounded to bf16 when ``kv_dtype == "bf16"``."""
+    g = _gen(seed)
+    r = torch.randn(B, T, C, generator=g, dtype=torch.float32) * r_std
+    if kv_dtype == "bf16":
+        r = r.to(torch.bfloat16)
+    elif kv_dtype != "f32":
+        raise ValueError(f"kv_dtype must be 'f32' or 'bf16', got {kv_dtype!r}")
+    return r
 
 
 def decode_params(L: int, C: int, *, seed: int, d_lo: float = -6.0, d_hi: float = 2.0):

@@ -125,6 +125,32 @@ def test_backward_rejects_before_launch(lib):
     assert _bwd(lib, wsb=256) == 4
 
 
+def test_gated_rejects_before_launch(lib):
+    B, T, C = 2, 40, 64
+    wsf = ctypes.c_size_t(lib.wkv_forward_workspace_bytes(B, T, C))
+    wsb = ctypes.c_size_t(lib.wkv_backward_workspace_bytes(B, T, C))
+
+    def fwd(r=FAKE, out=FAKE, ws=wsf):
+        return lib.wkv_forward_gated(B, T, C, 0, FAKE, FAKE, FAKE, FAKE, r, NULL, out, NULL, NULL, FAKE, ws, NULL)
+
+    def bwd(r=FAKE, gout=FAKE, gr=FAKE, ws=wsb):
+        return lib.wkv_backward_gated(B, T, C, 0, FAKE, FAKE, FAKE, FAKE, r, gout, NULL, FAKE, FAKE, FAKE, FAKE, gr,
+                                      FAKE, ws, NULL)
+
+    assert fwd(r=NULL) == 1 and fwd(out=NULL) == 1
+    assert fwd(ws=ctypes.c_size_t(64)) == 4
+    assert bwd(r=NULL) == 1 and bwd(gout=NULL) == 1 and bwd(gr=NULL) == 1
+    assert bwd(ws=ctypes.c_size_t(64)) == 4
+    # the gate is fused into the sequential kernels only: refused before any
+    # launch while the chunked scan is forced
+    lib.wkv_debug_set_scan_mode(1)
+    try:
+        assert fwd() == 2 and bwd() == 2
+        assert b"sequential" in lib.wkv_last_error_string()
+    finally:
+        lib.wkv_debug_set_scan_mode(0)
+
+
 def test_decode_rejects_before_launch(lib):
     args = [FAKE] * 17
     assert lib.wkv_decode_step(0, 1, 1, *args, NULL) == 1
