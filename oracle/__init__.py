@@ -55,6 +55,10 @@ class Oracle:
             "wkv_oracle_decode_step": [i, i, i] + [p] * 17,
             "wkv_oracle_forward_gated": [i, i, i] + [p] * 6,
             "wkv_oracle_backward_gated": [i, i, i] + [p] * 11,
+            "wkv_oracle_sqrelu": [ctypes.c_size_t] + [p] * 2,
+            "wkv_oracle_sqrelu_backward": [ctypes.c_size_t] + [p] * 3,
+            "wkv_oracle_cmix_gate": [ctypes.c_size_t] + [p] * 3,
+            "wkv_oracle_cmix_gate_backward": [ctypes.c_size_t] + [p] * 5,
         }
         for name, args in sigs.items():
             fn = getattr(self._lib, name)
@@ -131,6 +135,32 @@ class Oracle:
         gk, gv, gr = (np.empty_like(k) for _ in range(3))
         self._lib.wkv_oracle_backward_gated(B, T, C, *map(self._ptr, (w, u, k, v, r, gout, gw, gu, gk, gv, gr)))
         return gw, gu, gk, gv, gr
+
+    # --------------------------------------------------- channel mixing
+    def _elementwise(self, fn, outs, *args):
+        args = [self._in(a) for a in args]
+        shape = args[0].shape
+        for a in args[1:]:
+            assert a.shape == shape, "elementwise inputs of different shapes"
+        res = tuple(np.empty(shape) for _ in range(outs))
+        fn(args[0].size, *map(self._ptr, tuple(args) + res))
+        return res if outs > 1 else res[0]
+
+    def sqrelu(self, k) -> np.ndarray:
+        """max(k, 0)^2, elementwise."""
+        return self._elementwise(self._lib.wkv_oracle_sqrelu, 1, k)
+
+    def sqrelu_backward(self, k, ga) -> np.ndarray:
+        """gk = 2 max(k, 0) ga."""
+        return self._elementwise(self._lib.wkv_oracle_sqrelu_backward, 1, k, ga)
+
+    def cmix_gate(self, r, vk) -> np.ndarray:
+        """sigmoid(r) * vk, elementwise."""
+        return self._elementwise(self._lib.wkv_oracle_cmix_gate, 1, r, vk)
+
+    def cmix_gate_backward(self, r, vk, gout):
+        """(gr, gvk) of sum(gout * sigmoid(r) * vk)."""
+        return self._elementwise(self._lib.wkv_oracle_cmix_gate_backward, 2, r, vk, gout)
 
     # ---------------------------------------------------------- token shift
     def token_shift(self, x, x0, mu_k, mu_v, mu_r):

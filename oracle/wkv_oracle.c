@@ -397,6 +397,48 @@ void wkv_oracle_backward_gated(int B, int T, int C, const double *w, const doubl
     free(gy);
 }
 
+/* The pointwise parts of channel mixing (segmentfault "RWKV解读" section
+ * "3、RWKV的网络架构", eq. (10), whose body the page lost; qiita "RWKV
+ * についての調査記録": channel mixing computes K, then V from it, then gates
+ * with a sigmoid; "Инновационная архитектура RWKV", section "Механизмы
+ * взаимодействия": the projected signal goes through a squared ReLU and is
+ * multiplied by a sigmoid forget gate).  Read here as: between the key and
+ * value projections
+ *     a = max(k, 0)^2,          backward  gk = 2 max(k, 0) ga,
+ * and after the value projection vk = W_v a, with r the receptance,
+ *     out = sigmoid(r) vk,      backward  gvk = gout sigmoid(r),
+ *                                         gr  = gout vk sigmoid(r) (1 - sigmoid(r)).
+ * Elementwise over n values. */
+void wkv_oracle_sqrelu(size_t n, const double *k, double *a)
+{
+    for (size_t i = 0; i < n; ++i) {
+        double p = k[i] > 0.0 ? k[i] : 0.0;
+        a[i] = p * p;
+    }
+}
+
+void wkv_oracle_sqrelu_backward(size_t n, const double *k, const double *ga, double *gk)
+{
+    for (size_t i = 0; i < n; ++i)
+        gk[i] = 2.0 * (k[i] > 0.0 ? k[i] : 0.0) * ga[i];
+}
+
+void wkv_oracle_cmix_gate(size_t n, const double *r, const double *vk, double *out)
+{
+    for (size_t i = 0; i < n; ++i)
+        out[i] = vk[i] / (1.0 + exp(-r[i]));
+}
+
+void wkv_oracle_cmix_gate_backward(size_t n, const double *r, const double *vk, const double *gout,
+                                   double *gr, double *gvk)
+{
+    for (size_t i = 0; i < n; ++i) {
+        double s = 1.0 / (1.0 + exp(-r[i]));
+        gvk[i] = gout[i] * s;
+        gr[i] = gout[i] * vk[i] * s * (1.0 - s);
+    }
+}
+
 /* Token shift of the training path, eq. (7) of "RWKV解读" section
  * "3、RWKV的网络架构" (the input of each projection is a weighted sum of the
  * current and the previous token; segmentfault and "Инновационная

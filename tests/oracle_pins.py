@@ -421,6 +421,46 @@ def pin_gate_finite_differences(o):
             _close(got[name], fd, 0.0, 1e-7 * scale, f"gated FD g{name} seed {seed}")
 
 
+def pin_channel_mix(o):
+    """Squared ReLU: zero for k <= 0 and k^2 above (hand values); the channel
+    mix's gate at the exact sigmoid points; the gate equals the time-mixing
+    output's gate applied to the pinned wkv; central finite differences of
+    sum(ga * a) and sum(gout * sigmoid(r) * vk) give both backward passes."""
+    k = np.array([-3.0, -0.5, 0.0, 0.25, 1.0, 7.0])
+    _close(o.sqrelu(k), [0.0, 0.0, 0.0, 0.0625, 1.0, 49.0], 0.0, 0.0, "sqrelu hand values")
+    rng = _rng(90)
+    vk = rng.normal(0, 1, (3, 7, 5))
+    for rv, s in ((np.log(3.0), 0.75), (0.0, 0.5), (-np.log(3.0), 0.25), (40.0, 1.0)):
+        _close(o.cmix_gate(np.full_like(vk, rv), vk), s * vk, 1e-15, 0.0, f"cmix gate at r={rv:.3f}")
+    w, u, kk, v, _ = _rand_inputs(91, B=2, T=9, C=3)
+    r = rng.normal(0, 2, kk.shape)
+    _close(o.cmix_gate(r, o.forward_direct(w, u, kk, v)), o.forward_gated(w, u, kk, v, r), 1e-15, 1e-16,
+           "cmix gate vs time-mixing gate")
+    x = rng.normal(0, 1.5, (4, 6))
+    x[np.abs(x) < 1e-3] = 0.5  # keep central differences off the kink at 0
+    g = rng.normal(0, 1, x.shape)
+    h = 1e-6
+    fd = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fd[idx] = (np.sum(g * o.sqrelu(xp)) - np.sum(g * o.sqrelu(xm))) / (2 * h)
+    _close(o.sqrelu_backward(x, g), fd, 0.0, 1e-7 * max(1.0, np.abs(fd).max()), "FD sqrelu")
+    r = rng.normal(0, 1.5, x.shape)
+    gr, gvk = o.cmix_gate_backward(r, x, g)
+    for name, arr, got in (("r", r, gr), ("vk", x, gvk)):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            ap, am = arr.copy(), arr.copy()
+            ap[idx] += h
+            am[idx] -= h
+            args_p = (ap, x) if name == "r" else (r, ap)
+            args_m = (am, x) if name == "r" else (r, am)
+            fd[idx] = (np.sum(g * o.cmix_gate(*args_p)) - np.sum(g * o.cmix_gate(*args_m))) / (2 * h)
+        _close(got, fd, 0.0, 1e-7 * max(1.0, np.abs(fd).max()), f"FD cmix gate g{name}")
+
+
 ALL_PINS = [
     pin_forward_hand_values,
     pin_forward_forms_agree,
@@ -442,6 +482,7 @@ ALL_PINS = [
     pin_decode_matches_forward,
     pin_gate_special_values,
     pin_gate_finite_differences,
+    pin_channel_mix,
 ]
 
 

@@ -67,6 +67,13 @@ MUTANTS = [
      "gr[i] = gout[i] * y[i] * s * (1.0 - s);", "gr[i] = gout[i] * y[i] * s;"),
     ("gated_gr_uses_gated_gradient", "wkv_oracle_backward_gated",
      "gr[i] = gout[i] * y[i] * s * (1.0 - s);", "gr[i] = gy[i] * y[i] * s * (1.0 - s);"),
+    ("sqrelu_not_squared", "wkv_oracle_sqrelu", "a[i] = p * p;", "a[i] = p;"),
+    ("sqrelu_grad_drops_two", "wkv_oracle_sqrelu_backward",
+     "gk[i] = 2.0 * (k[i] > 0.0 ? k[i] : 0.0) * ga[i];", "gk[i] = (k[i] > 0.0 ? k[i] : 0.0) * ga[i];"),
+    ("cmix_gate_sign", "wkv_oracle_cmix_gate", "vk[i] / (1.0 + exp(-r[i]))", "vk[i] / (1.0 + exp(r[i]))"),
+    ("cmix_gr_drops_one_minus_s", "wkv_oracle_cmix_gate_backward",
+     "gr[i] = gout[i] * vk[i] * s * (1.0 - s);", "gr[i] = gout[i] * vk[i] * s;"),
+    ("cmix_gvk_ungated", "wkv_oracle_cmix_gate_backward", "gvk[i] = gout[i] * s;", "gvk[i] = gout[i];"),
     ("shift_grad_mu_sign", "wkv_oracle_token_shift_backward",
      "double d = x[i] - prev;", "double d = prev - x[i];"),
 ]
