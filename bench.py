@@ -45,6 +45,7 @@ METRIC = "WKV fwd+bwd B·T·C elements/s and achieved HBM GB/s fraction on 1 B30
 METRIC_FWD = "WKV forward B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
 METRIC_DEC = "WKV decode step L·B·C elements/s and achieved HBM GB/s fraction on 1 B300"
 METRIC_SHIFT = "token shift fwd+bwd B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
+METRIC_CMIX = "channel-mix pointwise fwd+bwd B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
 METRIC_GATED = "gated WKV sigmoid(r)*wkv fwd+bwd B·T·C elements/s and achieved HBM GB/s fraction on 1 B300"
 
 # Algorithmic HBM bytes per element (what the method must move with the
@@ -57,6 +58,10 @@ BYTES_BWD_BF16 = 14  # read bf16 k, v, gy; write fp32 gk, gv
 BYTES_DECODE = 60    # read x, x_prev, r, k, v; read+write num, den, pp; write y, xk, xv, xr
 BYTES_SHIFT_FWD = 16  # read x; write xk, xv, xr
 BYTES_SHIFT_BWD = 20  # read x, gxk, gxv, gxr; write gx
+BYTES_SQRELU_FWD = 8    # read k; write max(k, 0)^2                 (per hidden element)
+BYTES_SQRELU_BWD = 12   # read k, ga; write gk                      (per hidden element)
+BYTES_CMIX_GATE_FWD = 12  # read r, vk; write out
+BYTES_CMIX_GATE_BWD = 20  # read r, vk, gout; write gr, gvk
 BYTES_FWD_GATED = 16  # read k, v, r; write sigmoid(r) * wkv
 BYTES_BWD_GATED = 28  # read k, v, r, gout; write gk, gv, gr
 
@@ -69,7 +74,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default depends on the workload)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="l169m", choices=["tiny", "l169m", "l1b5", "long", "l169m_bf16",
-                                                              "l169m_gated", "decode", "shift"])
+                                                              "l169m_gated", "decode", "shift", "cmix"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -84,7 +89,7 @@ def parse_args(argv=None):
 
 
 DEFAULT_STEPS = {"tiny": 2000, "l169m": 4000, "l1b5": 200, "long": 200, "l169m_bf16": 4000, "l169m_gated": 4000,
-                 "decode": 256, "shift": 200}
+                 "decode": 256, "shift": 200, "cmix": 1000}
 
 
 # ------------------------------------------------------------------ ranks
@@ -508,6 +513,78 @@ class ShiftRun:
 
 
 # --------------------------------------------------------------- ours: run
+class CmixRun:
+    """A step is channel mixing's four pointwise calls: the squared ReLU
+    and the gate forward, then the gate's and the squared ReLU's backward
+    (the projections between them are the caller's matmuls, not timed)."""
+
+    def __init__(self, device):
+        import torch
+        from rwkv_linear_attention_backward_b300 import binding, inputs
+
+        self.torch, self.wkv = torch, binding
+        M = inputs.CMIX
+        self.M = M
+        self.elements = M.elements
+        self.host = inputs.cmix_inputs(M.B, M.T, M.C, M.H, seed=M.seed)
+        self.dev = tuple(t.to(device).contiguous() for t in self.host)
+        k, _, r, _, _ = self.dev
+        self.out = (torch.empty_like(k), torch.empty_like(r), torch.empty_like(r), torch.empty_like(r),
+                    torch.empty_like(k))  # a, out, gr, gvk, gk
+        hid = M.B * M.T * M.H
+        self.bytes_fwd = BYTES_SQRELU_FWD * hid + BYTES_CMIX_GATE_FWD * self.elements
+        self.bytes_bwd = BYTES_SQRELU_BWD * hid + BYTES_CMIX_GATE_BWD * self.elements
+        self.launches_per_step = 4
+        self.dominant = "cmix_kernel<1, 4> (squared-ReLU backward)"
+        self.dominant_bytes = BYTES_SQRELU_BWD * hid
+
+    def _forward(self):
+        k, _, r, vk, _ = self.dev
+        self.wkv.channel_mix_sqrelu(k, out=self.out[0])
+        self.wkv.channel_mix_gate(r, vk, out=self.out[1])
+
+    def _gate_backward(self):
+        _, _, r, vk, gout = self.dev
+        self.wkv.channel_mix_gate_backward(r, vk, gout, gr=self.out[2], gvk=self.out[3])
+
+    def _sqrelu_backward(self):
+        k, ga = self.dev[:2]
+        self.wkv.channel_mix_sqrelu_backward(k, ga, gk=self.out[4])
+
+    def step(self, ev=None):
+        self._forward()
+        self._gate_backward()
+        if ev is not None:
+            ev[0].record()
+        self._sqrelu_backward()
+        if ev is not None:
+            ev[1].record()
+
+    step_dominant_events = step
+
+    def capture(self):
+        pass  # four API calls per step
+
+    def check(self):
+        pass
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.pin_in = tuple(t.pin_memory() for t in self.host)
+        self.pin_out = tuple(torch.empty(t.shape, pin_memory=True) for t in self.out)
+        self.h2d = sum(t.numel() * t.element_size() for t in self.pin_in)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out)
+
+    def e2e_step(self):
+        for d, h in zip(self.dev, self.pin_in):
+            d.copy_(h, non_blocking=True)
+        self._forward()
+        self._gate_backward()
+        self._sqrelu_backward()
+        for h, d in zip(self.pin_out, self.out):
+            h.copy_(d, non_blocking=True)
+
+
 def time_steps(run, steps: int, flush, stream):
     """Per-step device times (s) of `steps` steps, L2 flushed before each;
     also the dominant call's per-launch times."""
@@ -554,6 +631,8 @@ def cpu_baseline(workload: str, target_s: float = 12.0):
                           f"{steps} steps in {el:.1f} s"}
     if workload == "shift":
         return _shift_oracle_timing(o, target_s)
+    if workload == "cmix":
+        return _cmix_oracle_timing(o, target_s)
     wl = inputs.WORKLOADS[workload]
     w, u, k, v, gy, *r = inputs.workload_inputs(workload)
     r = r[0] if r else None
@@ -600,6 +679,33 @@ def _shift_oracle_timing(o, target_s):
                       f"{reps} pass(es) in {el:.1f} s"}
 
 
+def _cmix_oracle_timing(o, target_s):
+    """The oracle's channel-mix steps (forward and backward) on batch row 0
+    of the cmix workload, repeated for about target_s."""
+    from rwkv_linear_attention_backward_b300 import inputs
+
+    M = inputs.CMIX
+    k, ga, r, vk, gout = (t.numpy() for t in inputs.cmix_inputs(1, M.T, M.C, M.H, seed=M.seed))
+    reps, done, t0 = 0, 0, time.perf_counter()
+    while True:
+        _cmix_oracle_pass(o, k, ga, r, vk, gout)
+        reps += 1
+        done += M.T * M.C
+        if time.perf_counter() - t0 >= target_s or reps >= 200:
+            break
+    el = time.perf_counter() - t0
+    return {"value": done / el, "unit": "elements/s", "cores": o.num_threads(), "kind": "oracle",
+            "sample": f"channel-mix squared ReLU + gate, forward and backward, on one batch row (T={M.T}, "
+                      f"C={M.C}, H={M.H}) of {M.B}, {reps} pass(es) in {el:.1f} s"}
+
+
+def _cmix_oracle_pass(o, k, ga, r, vk, gout):
+    o.sqrelu(k)
+    o.cmix_gate(r, vk)
+    o.cmix_gate_backward(r, vk, gout)
+    o.sqrelu_backward(k, ga)
+
+
 def _oracle_pass(o, wl, w, u, k, v, gy, cs, r=None):
     ks, vs = k[:, :, cs], v[:, :, cs]
     if wl.gated:
@@ -641,6 +747,8 @@ def run_ours(args):
         run = DecodeRun(device)
     elif args.workload == "shift":
         run = ShiftRun(device)
+    elif args.workload == "cmix":
+        run = CmixRun(device)
     else:
         run = TrainingRun(args.workload, device)
     stream = torch.cuda.current_stream()
@@ -686,19 +794,22 @@ def run_ours(args):
         wl_cfg = {"workload": "decode", "L": run.D.L, "B": run.D.B, "C": run.D.C, "state": "fp32"}
     elif args.workload == "shift":
         wl_cfg = {"workload": "shift", "B": run.S.B, "T": run.S.T, "C": run.S.C, "pass": "forward+backward"}
+    elif args.workload == "cmix":
+        wl_cfg = {"workload": "cmix", "B": run.M.B, "T": run.M.T, "C": run.M.C, "H": run.M.H,
+                  "pass": "forward+backward of the squared ReLU [B,T,H] and the gate [B,T,C]"}
     else:
         wl_cfg = {"workload": args.workload, "B": run.wl.B, "T": run.wl.T, "C": run.wl.C,
                   "kv_dtype": run.wl.kv_dtype, "pass": "forward+backward" if run.wl.backward else "forward"}
         if run.wl.gated:
             wl_cfg["output"] = "sigmoid(r) * wkv, the gate fused into the forward and backward kernels"
-    wl_cfg.update({"launch": "api calls per step" if (args.no_graph or args.workload in ("decode", "shift")) else
+    wl_cfg.update({"launch": "api calls per step" if (args.no_graph or args.workload in ("decode", "shift", "cmix")) else
                    "CUDA graphs of the forward and backward calls, captured once and replayed per step",
                    "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}",
                    "scan_mode": args.scan_mode,
                    "strategy": getattr(run, "strategy", "n/a"),
                    "checkpoints": "forward writes chunk checkpoints, backward reads them"
-                   if args.workload not in ("decode", "shift") else "n/a"})
-    metric = {"long": METRIC_FWD, "decode": METRIC_DEC, "shift": METRIC_SHIFT,
+                   if args.workload not in ("decode", "shift", "cmix") else "n/a"})
+    metric = {"long": METRIC_FWD, "decode": METRIC_DEC, "shift": METRIC_SHIFT, "cmix": METRIC_CMIX,
               "l169m_gated": METRIC_GATED}.get(args.workload, METRIC)
     out = {
         "metric": metric,
@@ -810,6 +921,17 @@ def run_reference(args):
 
         sample = f"token shift forward + backward on one batch row (T={S.T}, C={S.C}) of {S.B}"
         metric = METRIC_SHIFT
+    elif args.workload == "cmix":
+        M = inputs.CMIX
+        k, ga, r, vk, gout = (t.numpy() for t in inputs.cmix_inputs(1, M.T, M.C, M.H, seed=M.seed))
+
+        def one():
+            _cmix_oracle_pass(o, k, ga, r, vk, gout)
+            return M.T * M.C
+
+        sample = f"channel-mix squared ReLU + gate, forward and backward, on one batch row (T={M.T}, C={M.C}, " \
+                 f"H={M.H}) of {M.B}"
+        metric = METRIC_CMIX
     else:
         wl = inputs.WORKLOADS[args.workload]
         w, u, k, v, gy, *r = inputs.workload_inputs(args.workload)
@@ -837,6 +959,8 @@ def run_reference(args):
         cfg = {"workload": args.workload}
     elif args.workload == "shift":
         cfg = {"workload": "shift", "B": inputs.SHIFT.B, "T": inputs.SHIFT.T, "C": inputs.SHIFT.C}
+    elif args.workload == "cmix":
+        cfg = {"workload": "cmix", "B": inputs.CMIX.B, "T": inputs.CMIX.T, "C": inputs.CMIX.C, "H": inputs.CMIX.H}
     else:
         cfg = {"workload": args.workload, "B": inputs.WORKLOADS[args.workload].B,
                "T": inputs.WORKLOADS[args.workload].T, "C": inputs.WORKLOADS[args.workload].C}

@@ -214,6 +214,31 @@ wkv_status wkv_backward_gated(int B, int T, int C, int kv_dtype, const float* w,
                               float* gk, float* gv, float* gr, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Channel mixing's pointwise parts, forward and backward.  Channel mixing
+ * computes K from the token-shifted input, V from K, and gates the result
+ * with a sigmoid of its receptance ("RWKV についての調査記録", Time Mixing /
+ * Channel Mixing walk-through); between the key and value projections sits
+ * a squared ReLU ("Инновационная архитектура RWKV", "Механизмы
+ * взаимодействия"; "RWKV解读" section "3、RWKV的网络架构", eq. (10)).  The
+ * projections are the caller's matmuls; these calls are the elementwise
+ * steps around them, over n contiguous floats of any shape:
+ *   wkv_channel_mix_sqrelu            a   = max(k, 0)^2
+ *   wkv_channel_mix_sqrelu_backward   gk  = 2 max(k, 0) ga
+ *   wkv_channel_mix_gate              out = sigmoid(r) vk
+ *   wkv_channel_mix_gate_backward     gvk = gout sigmoid(r),
+ *                                     gr  = gout vk sigmoid(r) (1 - sigmoid(r))
+ * All pointers are float device pointers of n elements; an output may be the
+ * same buffer as an input (in place), other overlaps are undefined.  n == 0
+ * does nothing.  Errors: WKV_ERR_INVALID_ARG (n < 0, or a pointer NULL with
+ * n > 0), WKV_ERR_CUDA.
+ */
+wkv_status wkv_channel_mix_sqrelu(long long n, const float* k, float* a, void* stream);
+wkv_status wkv_channel_mix_sqrelu_backward(long long n, const float* k, const float* ga, float* gk, void* stream);
+wkv_status wkv_channel_mix_gate(long long n, const float* r, const float* vk, float* out, void* stream);
+wkv_status wkv_channel_mix_gate_backward(long long n, const float* r, const float* vk, const float* gout, float* gr,
+                                         float* gvk, void* stream);
+
+/*
  * wkv_decode_step -- one RNN-mode step of L independent time-mixing layers,
  * fused: token shift (eq. 7) -> wkv from the carried state -> sigmoid(r)
  * gate (eq. 9) -> state update.  Per (l, b, c), with parameters at (l, c):

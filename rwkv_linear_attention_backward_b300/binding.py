@@ -9,8 +9,8 @@ fallback implementation.
 
 Entry points mirror the ABI names: ``forward``, ``forward_with_state``,
 ``forward_gated``, ``backward``, ``backward_gated``, ``decode_step``,
-``token_shift``, ``token_shift_backward``, ``workspace_check``, plus size
-queries and test hooks.  All tensors must be
+``token_shift``, ``token_shift_backward``, the ``channel_mix_*`` pointwise
+steps, ``workspace_check``, plus size queries and test hooks.  All tensors must be
 contiguous CUDA tensors on the current device; calls are enqueued on the
 current torch stream (or ``stream=``) and return without synchronising.
 """
@@ -56,6 +56,10 @@ _SIGNATURES = {
     "wkv_token_shift": ([_i, _i, _i] + [_vp] * 8 + [_vp], _i),
     "wkv_token_shift_backward_workspace_bytes": ([_i, _i, _i], _sz),
     "wkv_token_shift_backward": ([_i, _i, _i] + [_vp] * 13 + [_vp, _sz, _vp], _i),
+    "wkv_channel_mix_sqrelu": ([_ll] + [_vp] * 2 + [_vp], _i),
+    "wkv_channel_mix_sqrelu_backward": ([_ll] + [_vp] * 3 + [_vp], _i),
+    "wkv_channel_mix_gate": ([_ll] + [_vp] * 3 + [_vp], _i),
+    "wkv_channel_mix_gate_backward": ([_ll] + [_vp] * 5 + [_vp], _i),
 }
 for _name, (_args, _res) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -373,6 +377,57 @@ def backward_gated(w, u, k, v, r, gout, *, ckpt=None, gw=None, gu=None, gk=None,
                                    _p(gu), _p(gk), _p(gv), _p(gr), ws.ptr(), ws.nbytes, _stream(stream)),
            "wkv_backward_gated")
     return gw, gu, gk, gv, gr
+
+
+# --------------------------------------------------------- channel mixing
+def _same(name, t, like):
+    _need(t, name, shape=tuple(like.shape))
+    if t.device != like.device:
+        raise ValueError(f"{name} must be on {like.device}")
+
+
+def channel_mix_sqrelu(k, *, out=None, stream=None):
+    """max(k, 0)^2 of an fp32 tensor of any shape (``out`` may be ``k``)."""
+    _need(k, "k")
+    out = torch.empty_like(k) if out is None else out
+    _same("out", out, k)
+    _check(_lib.wkv_channel_mix_sqrelu(k.numel(), _p(k), _p(out), _stream(stream)), "wkv_channel_mix_sqrelu")
+    return out
+
+
+def channel_mix_sqrelu_backward(k, ga, *, gk=None, stream=None):
+    """gk = 2 max(k, 0) ga."""
+    _need(k, "k")
+    _same("ga", ga, k)
+    gk = torch.empty_like(k) if gk is None else gk
+    _same("gk", gk, k)
+    _check(_lib.wkv_channel_mix_sqrelu_backward(k.numel(), _p(k), _p(ga), _p(gk), _stream(stream)),
+           "wkv_channel_mix_sqrelu_backward")
+    return gk
+
+
+def channel_mix_gate(r, vk, *, out=None, stream=None):
+    """sigmoid(r) * vk, fp32 tensors of one shape."""
+    _need(r, "r")
+    _same("vk", vk, r)
+    out = torch.empty_like(r) if out is None else out
+    _same("out", out, r)
+    _check(_lib.wkv_channel_mix_gate(r.numel(), _p(r), _p(vk), _p(out), _stream(stream)), "wkv_channel_mix_gate")
+    return out
+
+
+def channel_mix_gate_backward(r, vk, gout, *, gr=None, gvk=None, stream=None):
+    """(gr, gvk) of sum(gout * sigmoid(r) * vk)."""
+    _need(r, "r")
+    _same("vk", vk, r)
+    _same("gout", gout, r)
+    gr = torch.empty_like(r) if gr is None else gr
+    gvk = torch.empty_like(r) if gvk is None else gvk
+    _same("gr", gr, r)
+    _same("gvk", gvk, r)
+    _check(_lib.wkv_channel_mix_gate_backward(r.numel(), _p(r), _p(vk), _p(gout), _p(gr), _p(gvk), _stream(stream)),
+           "wkv_channel_mix_gate_backward")
+    return gr, gvk
 
 
 # ----------------------------------------------------------------- decode

@@ -601,6 +601,44 @@ wkv_status wkv_token_shift_backward(int B, int T, int C, const float* x, const f
   return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_token_shift_backward");
 }
 
+namespace {
+// The channel-mix calls: nothing to do for n == 0; every pointer required
+// for n > 0.
+wkv_status cmix_call(int op, long long n, const float* x, const float* y, const float* z, float* o1, float* o2,
+                     void* stream, const char* who) {
+  clear_error();
+  if (n < 0) return WKV_ERR_INVALID_ARG;
+  if (n == 0) return WKV_OK;
+  if (!x || !o1 || (op != 0 && !y) || (op == 3 && (!z || !o2))) return WKV_ERR_INVALID_ARG;
+  CmixArgs a;
+  a.x = x;
+  a.y = op != 0 ? y : nullptr;
+  a.z = op == 3 ? z : nullptr;
+  a.o1 = o1;
+  a.o2 = op == 3 ? o2 : nullptr;
+  a.n = n;
+  cudaError_t e = launch_cmix(op, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WKV_OK : cuda_fail(e, who);
+}
+}  // namespace
+
+wkv_status wkv_channel_mix_sqrelu(long long n, const float* k, float* a, void* stream) {
+  return cmix_call(0, n, k, nullptr, nullptr, a, nullptr, stream, "wkv_channel_mix_sqrelu");
+}
+
+wkv_status wkv_channel_mix_sqrelu_backward(long long n, const float* k, const float* ga, float* gk, void* stream) {
+  return cmix_call(1, n, k, ga, nullptr, gk, nullptr, stream, "wkv_channel_mix_sqrelu_backward");
+}
+
+wkv_status wkv_channel_mix_gate(long long n, const float* r, const float* vk, float* out, void* stream) {
+  return cmix_call(2, n, r, vk, nullptr, out, nullptr, stream, "wkv_channel_mix_gate");
+}
+
+wkv_status wkv_channel_mix_gate_backward(long long n, const float* r, const float* vk, const float* gout, float* gr,
+                                         float* gvk, void* stream) {
+  return cmix_call(3, n, r, vk, gout, gr, gvk, stream, "wkv_channel_mix_gate_backward");
+}
+
 wkv_status wkv_debug_set_wait_budget_ns(long long ns) {
   g_budget_ns.store(ns > 0 ? ns : kDefaultBudgetNs);
   return WKV_OK;

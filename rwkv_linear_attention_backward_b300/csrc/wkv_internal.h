@@ -175,10 +175,26 @@ struct ShiftArgs {
   int B, T, C, nslice;
 };
 
+// CTAs of `threads` threads for a grid-stride kernel over `items` items: at
+// most 8 per SM of the current device (wkv_shift.cu).
+int elementwise_grid(int64_t items, int threads);
+
 // Row slices of the backward pass (a function of the shape only).
 int shift_slices(int B, int T, int C, bool vec4);
 cudaError_t launch_shift_forward(const ShiftArgs& a, bool vec4, cudaStream_t s);
 cudaError_t launch_shift_backward(const ShiftArgs& a, bool vec4, cudaStream_t s);
+
+// Pointwise parts of channel mixing (wkv_cmix.cu), elementwise over n:
+// op 0 a = max(k, 0)^2 (x = k; o1 = a); op 1 gk = 2 max(k, 0) ga (x = k,
+// y = ga; o1 = gk); op 2 out = sigmoid(r) vk (x = r, y = vk; o1 = out);
+// op 3 gvk = gout sigmoid(r), gr = gvk (1 - sigmoid(r)) vk (x = r, y = vk,
+// z = gout; o1 = gr, o2 = gvk).
+struct CmixArgs {
+  const float *x, *y, *z;
+  float *o1, *o2;
+  int64_t n;
+};
+cudaError_t launch_cmix(int op, const CmixArgs& a, cudaStream_t s);
 
 // Grid of a persistent scan kernel: resident CTAs per SM x SMs, at most ntiles.
 cudaError_t launch_forward(FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);

@@ -182,9 +182,11 @@ __global__ void __launch_bounds__(256) shift_reduce_kernel(const ShiftArgs a) {
   out[c] = s;
 }
 
+}  // namespace
+
 // CTAs for `items` work items of a grid-stride kernel: enough for the items,
-// at most 8 CTAs of 256 threads per SM of the current device.
-int grid_for(int64_t items, int threads) {
+// at most 8 CTAs of `threads` threads per SM of the current device.
+int elementwise_grid(int64_t items, int threads) {
   static int sms_per_dev[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -199,8 +201,6 @@ int grid_for(int64_t items, int threads) {
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
-}  // namespace
-
 int shift_slices(int B, int T, int C, bool vec4) {
   const int per_group = vec4 ? 128 : 32;
   const int groups = (C + per_group - 1) / per_group;
@@ -213,9 +213,9 @@ int shift_slices(int B, int T, int C, bool vec4) {
 
 cudaError_t launch_shift_forward(const ShiftArgs& a, bool vec4, cudaStream_t s) {
   if (vec4) {
-    shift_fwd_kernel<4><<<grid_for((int64_t)a.B * a.T * (a.C / 4), 256), 256, 0, s>>>(a);
+    shift_fwd_kernel<4><<<elementwise_grid((int64_t)a.B * a.T * (a.C / 4), 256), 256, 0, s>>>(a);
   } else {
-    shift_fwd_kernel<1><<<grid_for((int64_t)a.B * a.T * a.C, 256), 256, 0, s>>>(a);
+    shift_fwd_kernel<1><<<elementwise_grid((int64_t)a.B * a.T * a.C, 256), 256, 0, s>>>(a);
   }
   return cudaGetLastError();
 }

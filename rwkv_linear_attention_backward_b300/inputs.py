@@ -28,6 +28,9 @@ l169m_gated fwd+bwd of the gated output sigmoid(r) * wkv, the l169m shape
            gradient)
 shift      token shift of the training path, fwd+bwd, B=16 T=4096 C=2048;
            x, gxk, gxv, gxr ~ N(0,1); x0 ~ N(0,1); mu_k, mu_v, mu_r ~ U(0,1)
+cmix       channel mixing's pointwise steps (squared ReLU, sigmoid gate)
+           fwd+bwd at the 169M layer: B=8 T=1024 C=768, hidden H=3072;
+           k, ga [B,T,H] ~ N(0,1); r, vk, gout [B,T,C] ~ N(0,1)
 decode     RNN decode, L=32 layers, B=256, C=4096, 1024 steps; x, x_prev,
            r, k, v ~ N(0,1); mu_k, mu_v, mu_r ~ U(0,1); d ~ U(-6,2),
            u ~ U(-1,1) per layer; state starts at (0, 0, -1e38)
@@ -100,6 +103,32 @@ class ShiftWorkload:
 
 
 SHIFT = ShiftWorkload("shift", 16, 4096, 2048, 1007)
+
+
+@dataclass(frozen=True)
+class ChannelMixWorkload:
+    name: str
+    B: int
+    T: int
+    C: int
+    H: int  # hidden width of the channel mix (the key projection's outputs)
+    seed: int
+
+    @property
+    def elements(self) -> int:
+        return self.B * self.T * self.C
+
+
+CMIX = ChannelMixWorkload("cmix", 8, 1024, 768, 3072, 1010)
+
+
+def cmix_inputs(B: int, T: int, C: int, H: int, *, seed: int):
+    """Draw (k, ga) [B,T,H] and (r, vk, gout) [B,T,C] ~ N(0,1) on the CPU,
+    fp32, in that order."""
+    g = _gen(seed)
+    k, ga = (torch.randn(B, T, H, generator=g, dtype=torch.float32) for _ in range(2))
+    r, vk, gout = (torch.randn(B, T, C, generator=g, dtype=torch.float32) for _ in range(3))
+    return k, ga, r, vk, gout
 
 
 def shift_inputs(B: int, T: int, C: int, *, seed: int):

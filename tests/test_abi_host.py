@@ -151,6 +151,23 @@ def test_gated_rejects_before_launch(lib):
         lib.wkv_debug_set_scan_mode(0)
 
 
+def test_channel_mix_rejects_before_launch(lib):
+    n = ctypes.c_longlong
+    assert lib.wkv_channel_mix_sqrelu(n(-1), FAKE, FAKE, NULL) == 1
+    assert lib.wkv_channel_mix_sqrelu(n(0), NULL, NULL, NULL) == 0  # nothing to do, nothing launched
+    assert lib.wkv_channel_mix_sqrelu(n(8), NULL, FAKE, NULL) == 1
+    assert lib.wkv_channel_mix_sqrelu(n(8), FAKE, NULL, NULL) == 1
+    assert lib.wkv_channel_mix_sqrelu_backward(n(8), FAKE, NULL, FAKE, NULL) == 1
+    assert lib.wkv_channel_mix_gate(n(8), FAKE, NULL, FAKE, NULL) == 1
+    assert lib.wkv_channel_mix_gate(n(-5), FAKE, FAKE, FAKE, NULL) == 1
+    args = [FAKE] * 5  # r, vk, gout, gr, gvk
+    for i in range(5):
+        a = list(args)
+        a[i] = NULL
+        assert lib.wkv_channel_mix_gate_backward(n(8), *a, NULL) == 1
+    assert lib.wkv_channel_mix_gate_backward(n(0), *([NULL] * 5), NULL) == 0
+
+
 def test_decode_rejects_before_launch(lib):
     args = [FAKE] * 17
     assert lib.wkv_decode_step(0, 1, 1, *args, NULL) == 1
