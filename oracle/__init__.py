@@ -55,6 +55,7 @@ class Oracle:
             "wkv_oracle_decode_step": [i, i, i] + [p] * 17,
             "wkv_oracle_forward_gated": [i, i, i] + [p] * 6,
             "wkv_oracle_backward_gated": [i, i, i] + [p] * 11,
+            "wkv_oracle_state_fold": [i, i, p, i, p, ctypes.POINTER(ctypes.c_longlong), p],
             "wkv_oracle_sqrelu": [ctypes.c_size_t] + [p] * 2,
             "wkv_oracle_sqrelu_backward": [ctypes.c_size_t] + [p] * 3,
             "wkv_oracle_cmix_gate": [ctypes.c_size_t] + [p] * 3,
@@ -135,6 +136,25 @@ class Oracle:
         gk, gv, gr = (np.empty_like(k) for _ in range(3))
         self._lib.wkv_oracle_backward_gated(B, T, C, *map(self._ptr, (w, u, k, v, r, gout, gw, gu, gk, gv, gr)))
         return gw, gu, gk, gv, gr
+
+    def state_fold(self, w, states, lengths):
+        """(num, den, pp), each [B, C]: the state after consecutive segments
+        given by their own states (a sequence of (num, den, pp) triples, or
+        an array [n, 3, B, C]) and their lengths in tokens."""
+        w = self._in(w)
+        if not hasattr(states, "shape"):
+            states = np.stack([np.stack([self._in(x) for x in st]) for st in states]) if len(states) else None
+        else:
+            states = self._in(states)
+        n = 0 if states is None else states.shape[0]
+        if n == 0:
+            raise ValueError("give the shape through at least one segment")
+        B, C = states.shape[2], states.shape[3]
+        states = np.ascontiguousarray(states, dtype=np.float64)
+        lens = (ctypes.c_longlong * n)(*[int(x) for x in lengths])
+        out = np.empty((3, B, C))
+        self._lib.wkv_oracle_state_fold(B, C, self._ptr(w), n, self._ptr(states), lens, self._ptr(out))
+        return out[0], out[1], out[2]
 
     # --------------------------------------------------- channel mixing
     def _elementwise(self, fn, outs, *args):

@@ -397,6 +397,47 @@ void wkv_oracle_backward_gated(int B, int T, int C, const double *w, const doubl
     free(gy);
 }
 
+/* The state after consecutive segments of one sequence, from each segment's
+ * own state (after its tokens, from the empty state) and its length: the
+ * prefix combination that lets segments of one long sequence run apart
+ * ("RWKV解读" section "3、RWKV的网络架构": eq. (8) written recursively; qiita
+ * "Trainingについて": the decay does not depend on the data, so a segment's
+ * effect on the carried state is "decay by its length, add its own sums").
+ * In the decode step's convention a = num e^{pp}, b = den e^{pp}; a token
+ * decays once for every later token, so after a state P and a segment of n
+ * tokens with own sums a_S, b_S:
+ *     a = e^{-n w} a_P + a_S,   b = e^{-n w} b_P + b_S,
+ * kept at the scale of the larger exponent.  states is [n][3][B][C] (planes
+ * num, den, pp; pp <= -1e37 marks an empty segment), lengths [n], out
+ * [3][B][C] (the empty state, num = den = 0 and pp = -1e38, if no segment
+ * has a token). */
+void wkv_oracle_state_fold(int B, int C, const double *w, int n, const double *states,
+                           const long long *lengths, double *out)
+{
+    size_t bc = (size_t)B * (size_t)C;
+    for (size_t o = 0; o < bc; ++o) {
+        int c = (int)(o % (size_t)C);
+        double A = 0.0, Bs = 0.0, M = -INFINITY;
+        for (int i = 0; i < n; ++i) {
+            const double *st = states + (size_t)i * 3 * bc;
+            double Md = M - (double)lengths[i] * w[c];
+            if (st[2 * bc + o] <= -1e37) {
+                M = Md;
+                continue;
+            }
+            double m2 = Md > st[2 * bc + o] ? Md : st[2 * bc + o];
+            double dp = exp(Md - m2), ds = exp(st[2 * bc + o] - m2);
+            A = A * dp + st[o] * ds;
+            Bs = Bs * dp + st[bc + o] * ds;
+            M = m2;
+        }
+        int seen = M > -INFINITY;
+        out[o] = seen ? A : 0.0;
+        out[bc + o] = seen ? Bs : 0.0;
+        out[2 * bc + o] = seen ? M : -1e38;
+    }
+}
+
 /* The pointwise parts of channel mixing (segmentfault "RWKV解读" section
  * "3、RWKV的网络架构", eq. (10), whose body the page lost; qiita "RWKV
  * についての調査記録": channel mixing computes K, then V from it, then gates

@@ -281,6 +281,26 @@ def pin_forward_state_split(o):
     _close(sb[2], p_all, 1e-13, 1e-13, "chained state pp")
 
 
+def pin_state_fold(o):
+    """Segments' own states folded in order give the direct-sum state of the
+    whole sequence (oracle.state over all tokens), for uneven cuts, a
+    zero-length segment and a single segment; a state given before the
+    first segment (a leading segment of length 0) continues the same way."""
+    w, u, k, v, _ = _rand_inputs(75, B=2, T=40, C=3, k_std=2.5, w_lo=-4.0, w_hi=1.5)
+    whole = o.state(w, k, v, 40)
+    for cuts in ((0, 40), (0, 13, 40), (0, 1, 2, 17, 17, 39, 40), (0, 25, 40)):
+        segs = [o.state(w, k[:, a:b], v[:, a:b], b - a) for a, b in zip(cuts[:-1], cuts[1:])]
+        lens = [b - a for a, b in zip(cuts[:-1], cuts[1:])]
+        got = o.state_fold(w, segs, lens)
+        for g, r, name in zip(got, whole, ("num", "den", "pp")):
+            _close(g, r, 1e-12, 1e-13, f"fold {cuts} {name}")
+    head = o.state(w, k[:, :9], v[:, :9], 9)
+    tail = [o.state(w, k[:, 9:30], v[:, 9:30], 21), o.state(w, k[:, 30:], v[:, 30:], 10)]
+    got = o.state_fold(w, [head] + tail, [0, 21, 10])
+    for g, r, name in zip(got, whole, ("num", "den", "pp")):
+        _close(g, r, 1e-12, 1e-13, f"fold after a given state {name}")
+
+
 def pin_token_shift(o):
     """mu = 1 keeps the current token, mu = 0 takes the previous one (the
     given x0 before the first), and the mix is the decode step's (which its
@@ -476,6 +496,7 @@ ALL_PINS = [
     pin_backward_forms_agree,
     pin_backward_identities,
     pin_forward_state_split,
+    pin_state_fold,
     pin_token_shift,
     pin_state_definition,
     pin_decode_hand_values,

@@ -67,6 +67,10 @@ MUTANTS = [
      "gr[i] = gout[i] * y[i] * s * (1.0 - s);", "gr[i] = gout[i] * y[i] * s;"),
     ("gated_gr_uses_gated_gradient", "wkv_oracle_backward_gated",
      "gr[i] = gout[i] * y[i] * s * (1.0 - s);", "gr[i] = gy[i] * y[i] * s * (1.0 - s);"),
+    ("fold_no_decay", "wkv_oracle_state_fold",
+     "double Md = M - (double)lengths[i] * w[c];", "double Md = M;"),
+    ("fold_decays_segment", "wkv_oracle_state_fold",
+     "A = A * dp + st[o] * ds;", "A = A * dp + st[o] * ds * exp(-(double)lengths[i] * w[c]);"),
     ("sqrelu_not_squared", "wkv_oracle_sqrelu", "a[i] = p * p;", "a[i] = p;"),
     ("sqrelu_grad_drops_two", "wkv_oracle_sqrelu_backward",
      "gk[i] = 2.0 * (k[i] > 0.0 ? k[i] : 0.0) * ga[i];", "gk[i] = (k[i] > 0.0 ? k[i] : 0.0) * ga[i];"),
