@@ -140,15 +140,44 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
  *   state_out  [3][B][C] floats, or NULL: the same planes after token T-1
  *              (pp the running maximum), ready for wkv_decode_step (its
  *              num, den, pp for one layer are the three planes).
+ *   y          as for wkv_forward, or NULL for a state-only pass: nothing
+ *              but state_out and ckpt is written (one of them must be
+ *              given), and no output is read back or stored.
  *   The other arguments are those of wkv_forward; ckpt and y describe the T
  *   tokens of this call.  wkv_backward differentiates the forward pass from
  *   the empty state only: the gradient with respect to a state_in is not
  *   computed.
- * Errors: as wkv_forward.
+ * Errors: as wkv_forward (y, state_out and ckpt all NULL:
+ * WKV_ERR_INVALID_ARG).
  */
 wkv_status wkv_forward_with_state(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
                                   const void* v, const float* state_in, float* y, float* state_out, float* ckpt,
                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * wkv_state_fold -- the state after n consecutive segments of one sequence,
+ * from each segment's own state (after its tokens, from the empty state) and
+ * its length.  The decay does not depend on the data ("RWKV についての調査記録",
+ * "Trainingについて"; eq. (8) written recursively, "RWKV解读" section
+ * "3、RWKV的网络架构"): a segment acts on the carried state by decaying it by
+ * its length and adding its own sums, a = e^{-n w} a + a_seg (b alike).  This
+ * splits one long sequence over devices: each runs wkv_forward_with_state
+ * with y = NULL on its segment, the [3][B][C] states are exchanged, each
+ * folds the states of the segments before its own into its state_in, then
+ * runs wkv_forward_with_state again for its outputs.  A state given before
+ * the first segment enters as a leading segment of length 0.
+ *   w        [C] device floats (the decay).
+ *   states   [n][3][B][C] device floats: segment i's planes num, den, pp, as
+ *            wkv_forward_with_state's state_out (the empty state, pp = -1e38
+ *            with num = den = 0, for a segment without tokens).
+ *   lengths  n HOST integers: segment i's tokens (>= 0), read during the call.
+ *   out      [3][B][C] device floats: the state after the n segments (the
+ *            empty state for n == 0).
+ * Errors: WKV_ERR_INVALID_ARG (B or C <= 0, n < 0 or n > 256, a negative
+ * length, w or out NULL, states or lengths NULL with n > 0), WKV_ERR_CUDA.
+ */
+wkv_status wkv_state_fold(int B, int C, const float* w, int n, const float* states, const long long* lengths,
+                          float* out, void* stream);
 
 /*
  * wkv_backward -- gradients of sum(gy * wkv) with respect to w, u, k, v.

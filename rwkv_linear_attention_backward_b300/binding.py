@@ -56,6 +56,7 @@ _SIGNATURES = {
     "wkv_token_shift": ([_i, _i, _i] + [_vp] * 8 + [_vp], _i),
     "wkv_token_shift_backward_workspace_bytes": ([_i, _i, _i], _sz),
     "wkv_token_shift_backward": ([_i, _i, _i] + [_vp] * 13 + [_vp, _sz, _vp], _i),
+    "wkv_state_fold": ([_i, _i, _vp, _i, _vp, ctypes.POINTER(_ll), _vp, _vp], _i),
     "wkv_channel_mix_sqrelu": ([_ll] + [_vp] * 2 + [_vp], _i),
     "wkv_channel_mix_sqrelu_backward": ([_ll] + [_vp] * 3 + [_vp], _i),
     "wkv_channel_mix_gate": ([_ll] + [_vp] * 3 + [_vp], _i),
@@ -189,12 +190,13 @@ def forward(w, u, k, v, *, y=None, ckpt=None, want_ckpt: bool = False, workspace
 
 
 def forward_with_state(w, u, k, v, state_in=None, *, y=None, state_out=None, ckpt=None, want_ckpt: bool = False,
-                       workspace: Workspace | None = None, stream=None):
+                       want_y: bool = True, workspace: Workspace | None = None, stream=None):
     """wkv over k, v [B, T, C] continuing from ``state_in`` (fp32 [3, B, C]:
     the planes num, den, pp; None: the empty state).  Returns
     ``(y, state_out)``, or ``(y, state_out, ckpt)`` when ``want_ckpt`` or a
     ``ckpt`` buffer is given; ``state_out`` is [3, B, C] (the state after the
-    last token, in the decode step's convention)."""
+    last token, in the decode step's convention).  ``want_y=False`` (and no
+    ``y``): a state-only pass, y is None."""
     if k.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("k must be float32 or bfloat16")
     B, T, C = k.shape
@@ -204,9 +206,10 @@ def forward_with_state(w, u, k, v, state_in=None, *, y=None, state_out=None, ckp
     _need(u, "u", shape=(C,))
     if state_in is not None:
         _need(state_in, "state_in", shape=(3, B, C))
-    if y is None:
+    if y is None and want_y:
         y = torch.empty((B, T, C), dtype=torch.float32, device=k.device)
-    _need(y, "y", shape=(B, T, C))
+    if y is not None:
+        _need(y, "y", shape=(B, T, C))
     if state_out is None:
         state_out = torch.empty((3, B, C), dtype=torch.float32, device=k.device)
     _need(state_out, "state_out", shape=(3, B, C))
@@ -255,6 +258,27 @@ def forward_gated(w, u, k, v, r, state_in=None, *, out=None, state_out=None, ckp
     _check(_lib.wkv_forward_gated(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(r), _p(state_in), _p(out),
                                   _p(state_out), _p(ckpt), ws.ptr(), ws.nbytes, _stream(stream)), "wkv_forward_gated")
     return (out, ckpt) if ckpt is not None else out
+
+
+def state_fold(w, states, lengths, *, out=None, stream=None):
+    """The state [3, B, C] after consecutive segments: ``states`` fp32
+    [n, 3, B, C] (each segment's own state, from the empty state; n may be
+    0 with any leading size), ``lengths`` the n segments' token counts."""
+    C = w.shape[0]
+    _need(w, "w", shape=(C,))
+    _need(states, "states")
+    if states.dim() != 4 or states.shape[1] != 3 or states.shape[3] != C:
+        raise ValueError("states must be [n, 3, B, C]")
+    n, B = states.shape[0], states.shape[2]
+    lengths = [int(x) for x in lengths]
+    if len(lengths) != n:
+        raise ValueError("one length per segment")
+    out = torch.empty((3, B, C), dtype=torch.float32, device=w.device) if out is None else out
+    _need(out, "out", shape=(3, B, C))
+    lens = (ctypes.c_longlong * max(n, 1))(*lengths)
+    _check(_lib.wkv_state_fold(B, C, _p(w), n, _p(states) if n else None, lens, _p(out), _stream(stream)),
+           "wkv_state_fold")
+    return out
 
 
 def token_shift(x, x0, mu_k, mu_v, mu_r, *, xk=None, xv=None, xr=None, stream=None):

@@ -254,7 +254,9 @@ wkv_status forward_impl(int B, int T, int C, int kv_dtype, const float* w, const
                         const void* v, const void* r, const float* state_in, float* y, float* state_out, float* ckpt,
                         void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
-  if (!sizes_ok(B, T, C) || !w || !u || !k || !v || !y) return WKV_ERR_INVALID_ARG;
+  // no y: a state-only pass, which must return the state (or checkpoints)
+  if (!sizes_ok(B, T, C) || !w || !u || !k || !v || (!y && !state_out && !ckpt) || (r && !y))
+    return WKV_ERR_INVALID_ARG;
   if (kv_dtype != WKV_F32 && kv_dtype != WKV_BF16) return WKV_ERR_INVALID_ARG;
   const ScanGeometry g = make_geometry(B, T, C);
   const FwdLayout l = fwd_layout(g);
@@ -289,7 +291,7 @@ wkv_status forward_impl(int B, int T, int C, int kv_dtype, const float* w, const
     q.g = g;
     q.budget_ns = (uint64_t)g_budget_ns.load();
     q.use_tma = make_tile_map(&q.tk, k, B, T, C, eb, kSeqChannels) && make_tile_map(&q.tv, v, B, T, C, eb, kSeqChannels);
-    e = launch_seq_forward(q, kv_dtype, true, static_cast<cudaStream_t>(stream));
+    e = launch_seq_forward(q, kv_dtype, y != nullptr, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
   }
   FwdArgs a;
@@ -311,7 +313,7 @@ wkv_status forward_impl(int B, int T, int C, int kv_dtype, const float* w, const
   a.budget_ns = (uint64_t)g_budget_ns.load();
   a.debug_skip_chunk = g_skip_chunk.load();
   a.use_tma = make_tile_map(&a.tk, k, B, T, C, eb, kCtaChannels) && make_tile_map(&a.tv, v, B, T, C, eb, kCtaChannels);
-  e = launch_forward(a, kv_dtype, true, static_cast<cudaStream_t>(stream));
+  e = launch_forward(a, kv_dtype, y != nullptr, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
 }
 
@@ -479,6 +481,10 @@ wkv_status wkv_workspace_check(void* workspace, void* stream) {
 wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
                        const void* v, float* y, float* ckpt, void* workspace, size_t workspace_bytes,
                        void* stream) {
+  if (!y) {
+    clear_error();
+    return WKV_ERR_INVALID_ARG;
+  }
   return wkv_forward_with_state(B, T, C, kv_dtype, w, u, k, v, nullptr, y, nullptr, ckpt, workspace,
                                 workspace_bytes, stream);
 }
@@ -637,6 +643,28 @@ wkv_status wkv_channel_mix_gate(long long n, const float* r, const float* vk, fl
 wkv_status wkv_channel_mix_gate_backward(long long n, const float* r, const float* vk, const float* gout, float* gr,
                                          float* gvk, void* stream) {
   return cmix_call(3, n, r, vk, gout, gr, gvk, stream, "wkv_channel_mix_gate_backward");
+}
+
+wkv_status wkv_state_fold(int B, int C, const float* w, int n, const float* states, const long long* lengths,
+                          float* out, void* stream) {
+  clear_error();
+  if (B <= 0 || C <= 0 || (double)B * C >= 1099511627776.0 || !w || !out || n < 0 || n > kMaxFoldSegments)
+    return WKV_ERR_INVALID_ARG;
+  if (n > 0 && (!states || !lengths)) return WKV_ERR_INVALID_ARG;
+  FoldArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int i = 0; i < n; ++i) {
+    if (lengths[i] < 0) return WKV_ERR_INVALID_ARG;
+    a.len[i] = lengths[i];
+  }
+  a.w = w;
+  a.states = states;
+  a.out = out;
+  a.B = B;
+  a.C = C;
+  a.n = n;
+  cudaError_t e = launch_state_fold(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_state_fold");
 }
 
 wkv_status wkv_debug_set_wait_budget_ns(long long ns) {

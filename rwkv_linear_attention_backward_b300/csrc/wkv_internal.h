@@ -196,6 +196,18 @@ struct CmixArgs {
 };
 cudaError_t launch_cmix(int op, const CmixArgs& a, cudaStream_t s);
 
+// The state after n consecutive segments (wkv_state.cu): states [n][3][B][C]
+// (each segment's own state), len[i] segment i's tokens, out [3][B][C].
+constexpr int kMaxFoldSegments = 256;
+struct FoldArgs {
+  const float* w;
+  const float* states;
+  float* out;
+  int B, C, n;
+  long long len[kMaxFoldSegments];
+};
+cudaError_t launch_state_fold(const FoldArgs& a, cudaStream_t s);
+
 // Grid of a persistent scan kernel: resident CTAs per SM x SMs, at most ntiles.
 cudaError_t launch_forward(FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
 cudaError_t launch_backward(BwdArgs& a, cudaStream_t s);

@@ -168,6 +168,24 @@ def test_channel_mix_rejects_before_launch(lib):
     assert lib.wkv_channel_mix_gate_backward(n(0), *([NULL] * 5), NULL) == 0
 
 
+def test_state_fold_and_state_only_pass_reject_before_launch(lib):
+    lens = (ctypes.c_longlong * 3)(5, 0, 7)
+    bad = (ctypes.c_longlong * 3)(5, -1, 7)
+    fold = lib.wkv_state_fold
+    assert fold(0, 4, FAKE, 3, FAKE, lens, FAKE, NULL) == 1
+    assert fold(2, 4, NULL, 3, FAKE, lens, FAKE, NULL) == 1
+    assert fold(2, 4, FAKE, 3, FAKE, lens, NULL, NULL) == 1
+    assert fold(2, 4, FAKE, -1, FAKE, lens, FAKE, NULL) == 1
+    assert fold(2, 4, FAKE, 257, FAKE, lens, FAKE, NULL) == 1
+    assert fold(2, 4, FAKE, 3, NULL, lens, FAKE, NULL) == 1
+    assert fold(2, 4, FAKE, 3, FAKE, NULL, FAKE, NULL) == 1
+    assert fold(2, 4, FAKE, 3, FAKE, bad, FAKE, NULL) == 1
+    # a pass with no y must return the state or the checkpoints
+    wsb = ctypes.c_size_t(lib.wkv_forward_workspace_bytes(2, 40, 64))
+    assert lib.wkv_forward_with_state(2, 40, 64, 0, FAKE, FAKE, FAKE, FAKE, NULL, NULL, NULL, NULL, FAKE, wsb,
+                                      NULL) == 1
+
+
 def test_decode_rejects_before_launch(lib):
     args = [FAKE] * 17
     assert lib.wkv_decode_step(0, 1, 1, *args, NULL) == 1
