@@ -51,6 +51,7 @@ class Oracle:
             "wkv_oracle_token_shift_backward": [i, i, i] + [p] * 13,
             "wkv_oracle_backward_adjoint": [i, i, i, p, p, p, p, p, p, p, p, p],
             "wkv_oracle_backward_direct": [i, i, i, p, p, p, p, p, p, p, p, p],
+            "wkv_oracle_backward_state": [i, i, i] + [p] * 16,
             "wkv_oracle_state": [i, i, i, p, p, p, i, p, p, p],
             "wkv_oracle_decode_step": [i, i, i] + [p] * 17,
             "wkv_oracle_forward_gated": [i, i, i] + [p] * 6,
@@ -223,6 +224,23 @@ class Oracle:
     def backward_direct(self, w, u, k, v, gy):
         """Returns (gw, gu, gk, gv) by differentiating the O(T^2) sum."""
         return self._backward(self._lib.wkv_oracle_backward_direct, w, u, k, v, gy)
+
+    def backward_state(self, w, u, k, v, gy, state_in=None, adj_end=None):
+        """Gradients of sum(gy * wkv) + ga_end a_T + gb_end b_T for a segment
+        starting from ``state_in`` = (num, den, pp) ([B, C] each; None:
+        empty), ``adj_end`` = (ga_end, gb_end) the gradient of the unscaled
+        end sums (None: zero).  Returns (gw, gu, gk, gv, (ga_start,
+        gb_start)), the last the gradient of the unscaled start sums."""
+        w, u, k, v, gy = map(self._in, (w, u, k, v, gy))
+        B, T, C = k.shape
+        sin = (None, None, None) if state_in is None else tuple(self._in(x).reshape(B, C).copy() for x in state_in)
+        aend = (None, None) if adj_end is None else tuple(self._in(x).reshape(B, C).copy() for x in adj_end)
+        gw, gu = np.empty(C), np.empty(C)
+        gk, gv = np.empty_like(k), np.empty_like(k)
+        ga, gb = np.empty((B, C)), np.empty((B, C))
+        self._lib.wkv_oracle_backward_state(B, T, C, *map(self._ptr, (w, u, k, v, gy) + sin + aend +
+                                                          (gw, gu, gk, gv, ga, gb)))
+        return gw, gu, gk, gv, (ga, gb)
 
     # ---------------------------------------------------------------- state
     def state(self, w, k, v, t: int):

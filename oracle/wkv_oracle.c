@@ -234,6 +234,76 @@ void wkv_oracle_backward_adjoint(int B, int T, int C, const double *w, const dou
     free(pu);
 }
 
+/* Backward pass of a segment that starts from a given state and whose end
+ * sums feed later tokens: the gradient with respect to a carried state, and
+ * the piece a sequence split along time needs per segment.  The segment's
+ * sums start at a_0 = num_in e^{pp_in}, b_0 = den_in e^{pp_in} (zero for a
+ * NULL or empty state) and the loss is
+ *     L = sum_t gy_t wkv_t + ga_end a_T + gb_end b_T,
+ * ga_end, gb_end [B, C] the gradient reaching the end sums from the tokens
+ * after the segment (NULL: none).  The recurrence of
+ * wkv_oracle_backward_adjoint, started from la_T = ga_end, lb_T = gb_end,
+ * gives gw (the start state's decay through the segment included), gu, gk,
+ * gv, and the adjoint of the start sums ga_start = la_0 = dL/da_0,
+ * gb_start = lb_0 ([B, C]; NULL: not returned).  Unscaled sums: moderate k
+ * only. */
+void wkv_oracle_backward_state(int B, int T, int C, const double *w, const double *u, const double *k,
+                               const double *v, const double *gy, const double *num_in,
+                               const double *den_in, const double *pp_in, const double *ga_end,
+                               const double *gb_end, double *gw, double *gu, double *gk, double *gv,
+                               double *ga_start, double *gb_start)
+{
+    double *a = (double *)malloc(sizeof(double) * (size_t)(T + 1));
+    double *bb = (double *)malloc(sizeof(double) * (size_t)(T + 1));
+    double *pw = (double *)malloc(sizeof(double) * (size_t)B * (size_t)C);
+    double *pu = (double *)malloc(sizeof(double) * (size_t)B * (size_t)C);
+    for (int b = 0; b < B; ++b)
+        for (int c = 0; c < C; ++c) {
+            size_t o = (size_t)b * (size_t)C + (size_t)c;
+            double decay = exp(-w[c]);
+            int given = num_in && pp_in[o] > -1e37;
+            a[0] = given ? num_in[o] * exp(pp_in[o]) : 0.0;
+            bb[0] = given ? den_in[o] * exp(pp_in[o]) : 0.0;
+            for (int t = 0; t < T; ++t) {
+                double ek = exp(k[IDX(b, t, c)]);
+                a[t + 1] = decay * a[t] + ek * v[IDX(b, t, c)];
+                bb[t + 1] = decay * bb[t] + ek;
+            }
+            double la = ga_end ? ga_end[o] : 0.0, lb = gb_end ? gb_end[o] : 0.0, sgw = 0.0, sgu = 0.0;
+            for (int t = T - 1; t >= 0; --t) {
+                double kt = k[IDX(b, t, c)], vt = v[IDX(b, t, c)], g = gy[IDX(b, t, c)];
+                double e = exp(u[c] + kt), ek = exp(kt);
+                double D = bb[t] + e;
+                double yt = (a[t] + e * vt) / D;
+                double gN = g / D;
+                double gD = -g * yt / D;
+                gk[IDX(b, t, c)] = (gN * vt + gD) * e + (la * vt + lb) * ek;
+                gv[IDX(b, t, c)] = gN * e + la * ek;
+                sgu += (gN * vt + gD) * e;
+                sgw += -decay * (la * a[t] + lb * bb[t]);
+                la = gN + decay * la;
+                lb = gD + decay * lb;
+            }
+            pw[o] = sgw;
+            pu[o] = sgu;
+            if (ga_start) ga_start[o] = la;
+            if (gb_start) gb_start[o] = lb;
+        }
+    for (int c = 0; c < C; ++c) {
+        double sw = 0.0, su = 0.0;
+        for (int b = 0; b < B; ++b) {
+            sw += pw[(size_t)b * (size_t)C + (size_t)c];
+            su += pu[(size_t)b * (size_t)C + (size_t)c];
+        }
+        gw[c] = sw;
+        gu[c] = su;
+    }
+    free(a);
+    free(bb);
+    free(pw);
+    free(pu);
+}
+
 /* Backward, direct O(T^2) derivative of the definition.  For i < t the
  * weight of token i in wkv_t is W_ti = e^{-(t-1-i)w + k_i}; for i = t it is
  * e^{u+k_t}.  Then, with D_t the denominator:

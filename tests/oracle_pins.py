@@ -235,6 +235,51 @@ def pin_backward_identities(o):
                 assert np.all(np.abs(gk2) < 1e-15) and np.all(np.abs(gu2) < 1e-15), "T=1 gk/gu"
 
 
+def pin_backward_state(o):
+    """The backward pass of a segment with a carried start state and a
+    gradient on its end sums: with neither it is the plain adjoint backward;
+    central finite differences of sum(gy * wkv) + ga_end a_T + gb_end b_T
+    give gw, gu, gk, gv and the gradient of the start sums; and a sequence's
+    backward cut in two (the later half from the state at the cut, the
+    earlier half fed the later half's start gradient) gives the whole
+    sequence's gradients."""
+    names = ("gw", "gu", "gk", "gv")
+    w, u, k, v, gy = _rand_inputs(95, B=2, T=12, C=3, k_std=1.0)
+    for g, r, n in zip(o.backward_state(w, u, k, v, gy)[:4], o.backward_adjoint(w, u, k, v, gy), names):
+        _close(g, r, 1e-14, 1e-15, f"no state, no end gradient: {n}")
+    rng = _rng(96)
+    B, T, C = k.shape
+    pp_in = np.full((B, C), 0.3)
+    num_in, den_in = rng.normal(0, 1, (B, C)), rng.uniform(0.5, 2.0, (B, C))
+    ga_end, gb_end = rng.normal(0, 0.2, (B, C)), rng.normal(0, 0.2, (B, C))
+
+    def loss(p):
+        y, (n, d, pe) = o.forward_state(p["w"], p["u"], p["k"], p["v"], (p["num"], p["den"], pp_in))
+        return float(np.sum(gy * y) + np.sum(ga_end * n * np.exp(pe)) + np.sum(gb_end * d * np.exp(pe)))
+
+    params = {"w": w, "u": u, "k": k, "v": v, "num": num_in, "den": den_in}
+    gw, gu, gk, gv, (ga, gb) = o.backward_state(w, u, k, v, gy, (num_in, den_in, pp_in), (ga_end, gb_end))
+    got = {"w": gw, "u": gu, "k": gk, "v": gv, "num": ga * np.exp(pp_in), "den": gb * np.exp(pp_in)}
+    for name, arr in params.items():
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            h = 1e-6 * max(1.0, abs(arr[idx]))
+            plus = {n: a.copy() for n, a in params.items()}
+            minus = {n: a.copy() for n, a in params.items()}
+            plus[name][idx] += h
+            minus[name][idx] -= h
+            fd[idx] = (loss(plus) - loss(minus)) / (2 * h)
+        _close(got[name], fd, 0.0, 1e-7 * max(1.0, float(np.max(np.abs(fd)))), f"FD with state: d{name}")
+    whole = o.backward_adjoint(w, u, k, v, gy)
+    t0 = 5
+    late = o.backward_state(w, u, k[:, t0:], v[:, t0:], gy[:, t0:], o.state(w, k, v, t0))
+    early = o.backward_state(w, u, k[:, :t0], v[:, :t0], gy[:, :t0], None, late[4])
+    _close(np.concatenate([early[2], late[2]], axis=1), whole[2], 1e-12, 1e-14, "cut in two: gk")
+    _close(np.concatenate([early[3], late[3]], axis=1), whole[3], 1e-12, 1e-14, "cut in two: gv")
+    _close(early[0] + late[0], whole[0], 1e-12, 1e-14, "cut in two: gw")
+    _close(early[1] + late[1], whole[1], 1e-12, 1e-14, "cut in two: gu")
+
+
 # --------------------------------------------------------------------------
 # state and decode
 # --------------------------------------------------------------------------
@@ -495,6 +540,7 @@ ALL_PINS = [
     pin_backward_finite_differences,
     pin_backward_forms_agree,
     pin_backward_identities,
+    pin_backward_state,
     pin_forward_state_split,
     pin_state_fold,
     pin_token_shift,

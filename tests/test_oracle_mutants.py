@@ -67,6 +67,12 @@ MUTANTS = [
      "gr[i] = gout[i] * y[i] * s * (1.0 - s);", "gr[i] = gout[i] * y[i] * s;"),
     ("gated_gr_uses_gated_gradient", "wkv_oracle_backward_gated",
      "gr[i] = gout[i] * y[i] * s * (1.0 - s);", "gr[i] = gy[i] * y[i] * s * (1.0 - s);"),
+    ("bstate_ignores_state_in", "wkv_oracle_backward_state",
+     "a[0] = given ? num_in[o] * exp(pp_in[o]) : 0.0;", "a[0] = 0.0;"),
+    ("bstate_ignores_end_gradient", "wkv_oracle_backward_state",
+     "double la = ga_end ? ga_end[o] : 0.0,", "double la = 0.0,"),
+    ("bstate_gw_drops_decay", "wkv_oracle_backward_state",
+     "sgw += -decay * (la * a[t] + lb * bb[t]);", "sgw += -(la * a[t] + lb * bb[t]);"),
     ("fold_no_decay", "wkv_oracle_state_fold",
      "double Md = M - (double)lengths[i] * w[c];", "double Md = M;"),
     ("fold_decays_segment", "wkv_oracle_state_fold",
