@@ -268,6 +268,38 @@ wkv_status wkv_channel_mix_gate_backward(long long n, const float* r, const floa
                                          float* gvk, void* stream);
 
 /*
+ * wkv_backward_with_state -- wkv_backward for a segment whose forward pass
+ * started from a carried state (wkv_forward_with_state's state_in) and whose
+ * end state feeds tokens after it: the gradient with respect to a carried
+ * state, and the backward pass of a sequence split along time (each
+ * segment's gradient at its start is the next earlier segment's gstate_end).
+ *   state_in    [3][B][C] or NULL: the state the forward pass started from.
+ *   gstate_end  [3][B][C] or NULL: the gradient of the loss from the tokens
+ *               after the segment with respect to the state after its last
+ *               token, as planes (g_num, g_den, pp): the gradient with
+ *               respect to num and den of that state written at scale pp
+ *               (a = num e^{pp}, so any pp near the state's own serves,
+ *               e.g. state_out's pp plane, or that of the next segment's
+ *               folded start state).
+ *   gstate_in   [3][B][C] or NULL, output: the same planes for state_in:
+ *               (g_num, g_den) with respect to state_in's num and den, and
+ *               state_in's pp.  A sequence split along time passes each
+ *               segment's gstate_in as the previous segment's gstate_end.
+ *               The gradient with respect to pp follows as
+ *               g_num num + g_den den.
+ *   ckpt        as for wkv_backward, from wkv_forward_with_state with the
+ *               same state_in (or NULL: recomputed from state_in).
+ *   The other arguments, and gw (which then includes the decay of state_in
+ *   through the segment), are those of wkv_backward.
+ * Errors: as wkv_backward; WKV_ERR_UNSUPPORTED while the chunked scan is
+ * forced.
+ */
+wkv_status wkv_backward_with_state(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                                   const void* v, const void* gy, const float* state_in, const float* gstate_end,
+                                   const float* ckpt, float* gw, float* gu, float* gk, float* gv, float* gstate_in,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * wkv_decode_step -- one RNN-mode step of L independent time-mixing layers,
  * fused: token shift (eq. 7) -> wkv from the carried state -> sigmoid(r)
  * gate (eq. 9) -> state update.  Per (l, b, c), with parameters at (l, c):

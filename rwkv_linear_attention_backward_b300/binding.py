@@ -45,6 +45,7 @@ _SIGNATURES = {
     "wkv_backward": ([_i, _i, _i, _i] + [_vp] * 10 + [_vp, _sz, _vp], _i),
     "wkv_forward_gated": ([_i, _i, _i, _i] + [_vp] * 9 + [_vp, _sz, _vp], _i),
     "wkv_backward_gated": ([_i, _i, _i, _i] + [_vp] * 12 + [_vp, _sz, _vp], _i),
+    "wkv_backward_with_state": ([_i, _i, _i, _i] + [_vp] * 13 + [_vp, _sz, _vp], _i),
     "wkv_decode_step": ([_i, _i, _i] + [_vp] * 17 + [_vp], _i),
     "wkv_forward_noalloc": ([_i, _i, _i, _i] + [_vp] * 6 + [_vp], _i),
     "wkv_debug_set_wait_budget_ns": ([_ll], _i),
@@ -371,6 +372,49 @@ def backward(w, u, k, v, gy, *, ckpt=None, gw=None, gu=None, gk=None, gv=None, w
     _check(_lib.wkv_backward(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(gy), _p(ckpt), _p(gw), _p(gu),
                              _p(gk), _p(gv), ws.ptr(), ws.nbytes, _stream(stream)), "wkv_backward")
     return gw, gu, gk, gv
+
+
+def backward_with_state(w, u, k, v, gy, state_in=None, gstate_end=None, *, ckpt=None, gw=None, gu=None, gk=None,
+                        gv=None, gstate_in=None, want_gstate_in: bool = True, workspace: Workspace | None = None,
+                        stream=None):
+    """``backward`` for a forward pass that started from ``state_in`` ([3, B,
+    C] or None) and whose end state feeds later tokens: ``gstate_end`` [3, B,
+    C] = (g_num, g_den, pp), the gradient with respect to the end state's
+    num, den written at scale pp (None: none).  Returns (gw, gu, gk, gv,
+    gstate_in), the last [3, B, C] = (g_num, g_den, pp) for state_in (None
+    when not wanted)."""
+    if k.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("k must be float32 or bfloat16")
+    B, T, C = k.shape
+    _need(k, "k", (k.dtype,))
+    _need(v, "v", (k.dtype,), k.shape)
+    _need(gy, "gy", (k.dtype,), k.shape)
+    _need(w, "w", shape=(C,))
+    _need(u, "u", shape=(C,))
+    for t, n in ((state_in, "state_in"), (gstate_end, "gstate_end")):
+        if t is not None:
+            _need(t, n, shape=(3, B, C))
+    if ckpt is not None:
+        _need(ckpt, "ckpt")
+        if ckpt.numel() < checkpoint_floats(B, T, C):
+            raise ValueError("ckpt is too small")
+    dev = k.device
+    gw = torch.empty(C, dtype=torch.float32, device=dev) if gw is None else gw
+    gu = torch.empty(C, dtype=torch.float32, device=dev) if gu is None else gu
+    gk = torch.empty((B, T, C), dtype=torch.float32, device=dev) if gk is None else gk
+    gv = torch.empty((B, T, C), dtype=torch.float32, device=dev) if gv is None else gv
+    if gstate_in is None and want_gstate_in:
+        gstate_in = torch.empty((3, B, C), dtype=torch.float32, device=dev)
+    for t, n, s in ((gw, "gw", (C,)), (gu, "gu", (C,)), (gk, "gk", (B, T, C)), (gv, "gv", (B, T, C))):
+        _need(t, n, shape=s)
+    if gstate_in is not None:
+        _need(gstate_in, "gstate_in", shape=(3, B, C))
+    ws = workspace or _workspace("bwd", backward_workspace_bytes(B, T, C), dev)
+    dt = WKV_BF16 if k.dtype == torch.bfloat16 else WKV_F32
+    _check(_lib.wkv_backward_with_state(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(gy), _p(state_in),
+                                        _p(gstate_end), _p(ckpt), _p(gw), _p(gu), _p(gk), _p(gv), _p(gstate_in),
+                                        ws.ptr(), ws.nbytes, _stream(stream)), "wkv_backward_with_state")
+    return gw, gu, gk, gv, gstate_in
 
 
 def backward_gated(w, u, k, v, r, gout, *, ckpt=None, gw=None, gu=None, gk=None, gv=None, gr=None,

@@ -174,8 +174,9 @@ namespace {
 // one gw, gu row per (run, batch row), then the reduction of those rows.
 wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int kv_dtype, const float* w,
                                const float* u, const void* k, const void* v, const void* gy, const void* r,
-                               const float* ckpt, float* gw, float* gu, float* gk, float* gv, float* gr,
-                               WsHeader* hdr, void* workspace, uint64_t budget, cudaStream_t s) {
+                               const float* state_in, const float* gstate_end, const float* ckpt, float* gw,
+                               float* gu, float* gk, float* gv, float* gr, float* gstate_in, WsHeader* hdr,
+                               void* workspace, uint64_t budget, cudaStream_t s) {
   const int B = g.B, T = g.T, C = g.C;
   const int eb = kv_dtype == WKV_F32 ? 4 : 2;
   const float* states = ckpt;
@@ -187,6 +188,7 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int kv
     f.k = k;
     f.v = v;
     f.y = nullptr;
+    f.state_in = state_in;
     f.ckpt = reinterpret_cast<float*>(bytes(workspace) + l.fwd + fwd_layout(g).ckpt);
     f.recs = reinterpret_cast<Rec*>(bytes(workspace) + l.fwd + fwd_layout(g).agg);
     f.exited = &hdr->exited[1];
@@ -210,6 +212,9 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int kv
   a.gy = gy;
   a.r = r;
   a.ckpt = states;
+  a.state_in = state_in;
+  a.gstate_end = gstate_end;
+  a.gstate_in = gstate_in;
   a.gk = gk;
   a.gv = gv;
   a.gr = gr;
@@ -317,11 +322,13 @@ wkv_status forward_impl(int B, int T, int C, int kv_dtype, const float* w, const
   return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
 }
 
-// wkv_backward, and wkv_backward_gated when r is non-null (then gy is the
-// gated output's gradient and gr receives r's).
+// wkv_backward, wkv_backward_gated when r is non-null (then gy is the
+// gated output's gradient and gr receives r's), and wkv_backward_with_state
+// (state_in, gstate_end, gstate_in).
 wkv_status backward_impl(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
-                         const void* v, const void* gy, const void* r, const float* ckpt, float* gw, float* gu,
-                         float* gk, float* gv, float* gr, void* workspace, size_t workspace_bytes, void* stream) {
+                         const void* v, const void* gy, const void* r, const float* state_in,
+                         const float* gstate_end, const float* ckpt, float* gw, float* gu, float* gk, float* gv,
+                         float* gr, float* gstate_in, void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
   if (!sizes_ok(B, T, C) || !w || !u || !k || !v || !gy || !gw || !gu || !gk || !gv) return WKV_ERR_INVALID_ARG;
   if (r && !gr) return WKV_ERR_INVALID_ARG;
@@ -337,8 +344,13 @@ wkv_status backward_impl(int B, int T, int C, int kv_dtype, const float* w, cons
   cudaError_t e = sequential_mode(g, seq);
   if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
   if (seq)
-    return backward_sequential(g, l, kv_dtype, w, u, k, v, gy, r, ckpt, gw, gu, gk, gv, gr, hdr, workspace, budget,
-                               s);
+    return backward_sequential(g, l, kv_dtype, w, u, k, v, gy, r, state_in, gstate_end, ckpt, gw, gu, gk, gv, gr,
+                               gstate_in, hdr, workspace, budget, s);
+  if (state_in || gstate_end || gstate_in) {
+    set_last_error("wkv_backward_with_state: carried states are taken by the sequential kernels only (the chunked "
+                   "scan is forced)");
+    return WKV_ERR_UNSUPPORTED;
+  }
   if (r) {
     set_last_error("wkv_backward_gated: the gated output's backward pass runs on the sequential kernels only (the "
                    "chunked scan is forced)");
@@ -508,8 +520,16 @@ wkv_status wkv_forward_gated(int B, int T, int C, int kv_dtype, const float* w, 
 wkv_status wkv_backward(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
                         const void* v, const void* gy, const float* ckpt, float* gw, float* gu, float* gk,
                         float* gv, void* workspace, size_t workspace_bytes, void* stream) {
-  return backward_impl(B, T, C, kv_dtype, w, u, k, v, gy, nullptr, ckpt, gw, gu, gk, gv, nullptr, workspace,
-                       workspace_bytes, stream);
+  return backward_impl(B, T, C, kv_dtype, w, u, k, v, gy, nullptr, nullptr, nullptr, ckpt, gw, gu, gk, gv, nullptr,
+                       nullptr, workspace, workspace_bytes, stream);
+}
+
+wkv_status wkv_backward_with_state(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
+                                   const void* v, const void* gy, const float* state_in, const float* gstate_end,
+                                   const float* ckpt, float* gw, float* gu, float* gk, float* gv, float* gstate_in,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_impl(B, T, C, kv_dtype, w, u, k, v, gy, nullptr, state_in, gstate_end, ckpt, gw, gu, gk, gv,
+                       nullptr, gstate_in, workspace, workspace_bytes, stream);
 }
 
 wkv_status wkv_backward_gated(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
@@ -517,8 +537,8 @@ wkv_status wkv_backward_gated(int B, int T, int C, int kv_dtype, const float* w,
                               float* gk, float* gv, float* gr, void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
   if (!r || !gr) return WKV_ERR_INVALID_ARG;
-  return backward_impl(B, T, C, kv_dtype, w, u, k, v, gout, r, ckpt, gw, gu, gk, gv, gr, workspace, workspace_bytes,
-                       stream);
+  return backward_impl(B, T, C, kv_dtype, w, u, k, v, gout, r, nullptr, nullptr, ckpt, gw, gu, gk, gv, gr, nullptr,
+                       workspace, workspace_bytes, stream);
 }
 
 wkv_status wkv_decode_step(int L, int B, int C, const float* x, const float* x_prev, const float* mu_k,

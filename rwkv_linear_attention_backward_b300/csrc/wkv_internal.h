@@ -146,6 +146,9 @@ struct SeqBwdArgs {
   const void* gy;  // with r: the gradient of the gated output sigmoid(r) wkv
   const void* r;   // null: ungated
   const float* ckpt;
+  const float* state_in;    // [3][B][C] state before the first token, or null (empty)
+  const float* gstate_end;  // [3][B][C] gradient of the last state's num, den at the given pp, or null
+  float* gstate_in;         // [3][B][C] out: gradient of state_in's num, den, and state_in's pp; or null
   float* gk;
   float* gv;
   float* gr;       // [B, T, C] (gated launches)

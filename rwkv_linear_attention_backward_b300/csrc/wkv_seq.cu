@@ -982,8 +982,8 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
   float xa[kChunk], xb[kChunk], xp[kChunk];  // per-token form's states (local memory)
   const size_t o0 = (size_t)col.b * g.C + col.cc;
   const size_t jstride = (size_t)g.B * g.C;
-  auto load_state = [&](int j) {  // the checkpoint before chunk j
-    if (j <= 0) return empty_state();
+  auto load_state = [&](int j) {  // the checkpoint before chunk j (the given start state before chunk 0)
+    if (j <= 0) return load_state_planes(a.state_in, jstride, o0);
     const size_t o = (size_t)(j - 1) * jstride + o0;
     return State{__ldg(a.ckpt + o), __ldg(a.ckpt + o + g.plane), __ldg(a.ckpt + o + 2 * g.plane)};
   };
@@ -1011,16 +1011,23 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
                     last - a.debug_skip_chunk < first + count;
   if (n1 > 0 && col.valid && !skip) rec_store(a.recs + (size_t)run * jstride + o0, L.tag, X.la, X.lb, X.f);
 
-  // the carry into this run's end (in time): the runs after it, nearest
-  // last (none for the run holding the last chunk)
+  // the carry into this run's end (in time): the gradient given on the
+  // state after the last token, if any (the num, den gradients of a state
+  // at the given pp: exactly the record form), then the runs after this
+  // one, nearest last.  Run 0 holds the last chunks, the only partial one
+  // among them, so its span is counted in tokens.
+  const bool has_end = a.gstate_end != nullptr;
   X = Adj{0.f, 0.f, 0.f};
+  if (has_end)
+    X = Adj{__ldg(a.gstate_end + o0), __ldg(a.gstate_end + jstride + o0), __ldg(a.gstate_end + 2 * jstride + o0)};
   for (int r = 0; r < run; ++r) {
     int fr, cr;
     segment_of(g.nchunks, nseg, r, fr, cr);
     Rec rec;
     if (!wait_rec(a.recs + (size_t)r * jstride + o0, col.valid, L, a.eh, a.budget_ns, rec)) return fail(it - 1);
     const Adj Ar{rec_x(rec), rec_y(rec), rec_z(rec)};
-    X = r == 0 ? Ar : fold_adj(Ar, (float)(cr * kChunk) * cw.w, X);
+    const int span = r == 0 ? g.T - (g.nchunks - cr) * kChunk : cr * kChunk;
+    X = (r == 0 && !has_end) ? Ar : fold_adj(Ar, (float)span * cw.w, X);
   }
 
   // phase 2: gk, gv, and this run's gw, gu
@@ -1034,15 +1041,23 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
     const int64_t row = ((int64_t)col.b * g.T + (int64_t)j * kChunk) * g.C + col.c;
     float gw_acc, gu_acc;
     float* grp = GATE ? a.gr + row : nullptr;
+    const bool has_succ = j < last || has_end;
     if (n == kChunk)
-      seq_bwd_chunk<true, KV, RP>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last, X,
+      seq_bwd_chunk<true, KV, RP>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, has_succ, X,
                                   a.gk + row, a.gv + row, grp, g.C, col.valid, gw_acc, gu_acc, xa, xb, xp);
     else
-      seq_bwd_chunk<false, KV, RP>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, j < last,
+      seq_bwd_chunk<false, KV, RP>(dk + lane, dk + kSeqTile + lane, dk + 2 * kSeqTile + lane, n, cw, P, has_succ,
                                    X, a.gk + row, a.gv + row, grp, g.C, col.valid, gw_acc, gu_acc, xa, xb, xp);
     kahan_add(cw.gw_s, cw.gw_k, gw_acc);
     kahan_add(cw.gu_s, cw.gu_k, gu_acc);
     release(it);
+  }
+  // the run holding chunk 0 ends at the sequence's start: X is then the
+  // gradient of the start state's num, den, in record form at its pp
+  if (run == nseg - 1 && a.gstate_in && col.valid) {
+    a.gstate_in[o0] = X.la;
+    a.gstate_in[jstride + o0] = X.lb;
+    a.gstate_in[2 * jstride + o0] = X.f;
   }
   // one gw, gu row per (run, batch row): row run * B + b of [2][nseg * B][C]
   // (added up in row order by the reduction kernel that follows)

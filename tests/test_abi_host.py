@@ -186,6 +186,27 @@ def test_state_fold_and_state_only_pass_reject_before_launch(lib):
                                       NULL) == 1
 
 
+def test_backward_with_state_rejects_before_launch(lib):
+    B, T, C = 2, 40, 64
+    wsb = ctypes.c_size_t(lib.wkv_backward_workspace_bytes(B, T, C))
+
+    def call(**nulls):
+        p = {n: FAKE for n in ("w", "u", "k", "v", "gy", "gw", "gu", "gk", "gv")}
+        p.update(nulls)
+        return lib.wkv_backward_with_state(B, T, C, 0, p["w"], p["u"], p["k"], p["v"], p["gy"], FAKE, FAKE, NULL,
+                                           p["gw"], p["gu"], p["gk"], p["gv"], FAKE, FAKE, wsb, NULL)
+
+    for name in ("w", "u", "k", "v", "gy", "gw", "gu", "gk", "gv"):
+        assert call(**{name: NULL}) == 1
+    # carried states are taken by the sequential kernels only
+    lib.wkv_debug_set_scan_mode(1)
+    try:
+        assert call() == 2
+        assert b"sequential" in lib.wkv_last_error_string()
+    finally:
+        lib.wkv_debug_set_scan_mode(0)
+
+
 def test_decode_rejects_before_launch(lib):
     args = [FAKE] * 17
     assert lib.wkv_decode_step(0, 1, 1, *args, NULL) == 1
