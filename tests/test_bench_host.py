@@ -1,0 +1,82 @@
+"""bench.py's host-side logic on the CPU: arguments, the whole-job
+aggregate, the traffic record gated on the kernel sources, and the clock
+record that decides whether a timed run is rejected."""
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_arguments():
+    a = bench.parse_args([])
+    assert (a.gpus, a.workload, a.impl, a.scan_mode) == (1, "l169m", "ours", "auto")
+    assert a.warmup >= 3
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--warmup", "2"])
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--workload", "nope"])
+    for w in ("tiny", "l169m", "l1b5", "long", "l169m_bf16", "l169m_gated", "decode", "shift", "cmix"):
+        assert bench.parse_args(["--workload", w]).workload == w
+        assert w in bench.DEFAULT_STEPS
+
+
+def test_aggregate_one_rank():
+    value, t = bench.aggregate(2.0, 100.0, 1)
+    assert (value, t) == (50.0, 2.0)
+
+
+def test_traffic_record_follows_the_sources(tmp_path, monkeypatch):
+    rec = {"seq_bwd_kernel@l169m": {"source_hash": "abc", "dram_bytes_per_launch": 123}}
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", tmp_path)
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc")
+    assert bench.ncu_traffic("seq_bwd_kernel", "l169m") == 123
+    assert bench.ncu_traffic("seq_fwd_kernel", "l169m") is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "changed")
+    assert bench.ncu_traffic("seq_bwd_kernel", "l169m") is None
+    (tmp_path / "profiles" / "ncu_traffic.json").unlink()
+    assert bench.ncu_traffic("seq_bwd_kernel", "l169m") is None
+
+
+def test_source_hash_covers_the_kernel_sources():
+    h = bench.kernel_source_hash()
+    assert len(h) == 16 and h == bench.kernel_source_hash()
+
+
+def _sampler(samples, reasons, max_mhz=2032.0):
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.samples, s.reasons, s.max_mhz, s.source, s.error = list(samples), set(reasons), max_mhz, "test", None
+    return s
+
+
+def test_clock_rejection():
+    assert not _sampler([2032] * 5, []).rejected()
+    assert not _sampler([1900] * 5, ["sw_power_cap"]).rejected()  # kept and noted
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert _sampler([2032] * 5, [r]).rejected()
+    assert _sampler([1000] * 5, []).rejected()  # stuck well below max with no reason: a clock lock
+    assert not _sampler([1000] * 5, ["sw_power_cap"]).rejected()
+    s = _sampler([2032, 2032, 1500], ["gpu_idle"]).summary()
+    assert s["sm_mhz"] == 2032 and s["reasons"] == []  # idle is not a reason
+
+
+def test_smi_lines_are_read():
+    class Proc:
+        stdout = ["2032, 2032, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n",
+                  "garbage\n",
+                  "1800, 2032, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+                  "1700, 2032, 0x0000000000000008, Active, Not Active, Not Active, Not Active\n"]
+
+    s = _sampler([], [])
+    s._proc = Proc()
+    s._run_smi()
+    assert s.samples == [2032.0, 1800.0, 1700.0]
+    assert {"sw_power_cap", "hw_slowdown"} <= s.reasons
+    assert s.rejected()
