@@ -710,7 +710,7 @@ def _oracle_pass(o, wl, w, u, k, v, gy, cs, r=None):
     ks, vs = k[:, :, cs], v[:, :, cs]
     if wl.gated:
         rs = r[:, :, cs]
-        o.forward_gated(w[cs], u[cs], ks, vs, rs)
+        o.forward_gated_recurrent(w[cs], u[cs], ks, vs, rs)
         o.backward_gated(w[cs], u[cs], ks, vs, rs, gy[:, :, cs])
         return
     o.forward_recurrent(w[cs], u[cs], ks, vs)
@@ -720,7 +720,7 @@ def _oracle_pass(o, wl, w, u, k, v, gy, cs, r=None):
 
 def _oracle_what(wl):
     if wl.gated:
-        return "gated direct forward + gated adjoint backward"
+        return "gated recurrent forward + gated adjoint backward"
     return "recurrent forward + adjoint backward" if wl.backward else "recurrent forward"
 
 

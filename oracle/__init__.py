@@ -55,6 +55,7 @@ class Oracle:
             "wkv_oracle_state": [i, i, i, p, p, p, i, p, p, p],
             "wkv_oracle_decode_step": [i, i, i] + [p] * 17,
             "wkv_oracle_forward_gated": [i, i, i] + [p] * 6,
+            "wkv_oracle_forward_gated_recurrent": [i, i, i] + [p] * 6,
             "wkv_oracle_backward_gated": [i, i, i] + [p] * 11,
             "wkv_oracle_state_fold": [i, i, p, i, p, ctypes.POINTER(ctypes.c_longlong), p],
             "wkv_oracle_sqrelu": [ctypes.c_size_t] + [p] * 2,
@@ -126,6 +127,15 @@ class Oracle:
         B, T, C = k.shape
         out = np.empty_like(k)
         self._lib.wkv_oracle_forward_gated(B, T, C, *map(self._ptr, (w, u, k, v, r, out)))
+        return out
+
+    def forward_gated_recurrent(self, w, u, k, v, r) -> np.ndarray:
+        """sigmoid(r) * wkv through the recurrent form (the O(T) form timed
+        as the CPU baseline)."""
+        w, u, k, v, r = map(self._in, (w, u, k, v, r))
+        B, T, C = k.shape
+        out = np.empty_like(k)
+        self._lib.wkv_oracle_forward_gated_recurrent(B, T, C, *map(self._ptr, (w, u, k, v, r, out)))
         return out
 
     def backward_gated(self, w, u, k, v, r, gout):

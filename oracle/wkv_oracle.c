@@ -442,6 +442,19 @@ void wkv_oracle_forward_gated(int B, int T, int C, const double *w, const double
         out[i] = out[i] / (1.0 + exp(-r[i]));
 }
 
+/* The same gated output through the recurrent form: sigmoid(r_t) times
+ * wkv_t of wkv_oracle_forward_recurrent.  O(T) per channel, so it is the
+ * form the CPU timing uses; it equals wkv_oracle_forward_gated (the direct
+ * O(T^2) sums) up to rounding. */
+void wkv_oracle_forward_gated_recurrent(int B, int T, int C, const double *w, const double *u, const double *k,
+                                        const double *v, const double *r, double *out)
+{
+    wkv_oracle_forward_recurrent(B, T, C, w, u, k, v, out);
+    size_t n = (size_t)B * (size_t)T * (size_t)C;
+    for (size_t i = 0; i < n; ++i)
+        out[i] = out[i] / (1.0 + exp(-r[i]));
+}
+
 /* Gradients of sum(gout * out) for the gated output above.  wkv_t reaches
  * the loss only through out_t, with factor sigmoid(r_t), so the gradient
  * that enters the recurrence's reverse mode is gy_t = gout_t sigmoid(r_t)

@@ -460,6 +460,21 @@ def pin_gate_special_values(o):
     assert np.all(np.abs(gr) <= 5e-18 * np.abs(g * y) + 1e-300), "r=40 gr"
 
 
+def pin_gate_recurrent_form(o):
+    """The gated output through the recurrent form (the form the CPU baseline
+    times) equals the gated direct sums, and at the exact sigmoid points the
+    pinned direct wkv times 3/4, 1/2, 1/4."""
+    for seed in (55, 56):
+        w, u, k, v, _ = _rand_inputs(seed, B=2, T=40, C=4, k_std=2.0)
+        r = _rng(seed + 7).normal(0, 2.0, k.shape)
+        _close(o.forward_gated_recurrent(w, u, k, v, r), o.forward_gated(w, u, k, v, r), 1e-12, 1e-13,
+               f"gated recurrent vs direct seed {seed}")
+    y = o.forward_direct(w, u, k, v)
+    for rv, s in ((np.log(3.0), 0.75), (0.0, 0.5), (-np.log(3.0), 0.25)):
+        _close(o.forward_gated_recurrent(w, u, k, v, np.full_like(k, rv)), s * y, 1e-12, 1e-13,
+               f"gated recurrent at r={rv:.3f}")
+
+
 def pin_gate_finite_differences(o):
     """Central differences of sum(gout * sigmoid(r) * wkv) in float64 on tiny
     inputs give all five gradients of the gated backward pass."""
@@ -548,6 +563,7 @@ ALL_PINS = [
     pin_decode_hand_values,
     pin_decode_matches_forward,
     pin_gate_special_values,
+    pin_gate_recurrent_form,
     pin_gate_finite_differences,
     pin_channel_mix,
 ]

@@ -42,6 +42,8 @@ MUTANTS = [
     ("state_pp_index", "wkv_oracle_state",
      "double ex = k[IDX(b, i, c)] - (double)(t - 1 - i) * w[c];",
      "double ex = k[IDX(b, i, c)] - (double)(t - i) * w[c];"),
+    ("gated_recurrent_gate_sign", "wkv_oracle_forward_gated_recurrent",
+     "out[i] = out[i] / (1.0 + exp(-r[i]));\n}\n\n/* Gradients", "out[i] = out[i] / (1.0 + exp(r[i]));\n}\n\n/* Gradients"),
     ("decode_mix_transposed", "wkv_oracle_decode_step",
      "mu_k[p] * x[o] + (1.0 - mu_k[p]) * x_prev[o]", "mu_k[p] * x_prev[o] + (1.0 - mu_k[p]) * x[o]"),
     ("decode_gate_sign", "wkv_oracle_decode_step",
