@@ -40,15 +40,17 @@ def oracle():
 
 
 def pytest_sessionfinish(session, exitstatus):
-    """Write every parity measurement of the run to gpurun_out/ when that
-    folder exists (GPU runs), for the records kept under profiles/."""
+    """Every parity comparison of the run (both gates' numbers), written as
+    JSON to the file named by WKV_PARITY_LOG when it is set."""
     import json
 
+    path = os.environ.get("WKV_PARITY_LOG")
+    if not path:
+        return
     try:
         from parity import PARITY_LOG
     except ImportError:
         return
-    out = os.path.join(ROOT, "gpurun_out")
-    if PARITY_LOG and os.path.isdir(out):
-        with open(os.path.join(out, "parity_errors.json"), "w") as f:
+    if PARITY_LOG:
+        with open(path, "w") as f:
             json.dump(PARITY_LOG, f, indent=0)

@@ -10,6 +10,7 @@ the full 169M-layer shapes."""
 import pytest
 import torch
 
+import fp32_emulation as emu
 from parity import TOL_Y, assert_close, cuda
 from rwkv_linear_attention_backward_b300 import inputs
 
@@ -34,14 +35,19 @@ def _all(wkv, k, ga, r, vk, gout):
     return a, gk, out, gr, gvk
 
 
+def _close(got, want, em, what, tol=TOL):
+    assert_close(got, want, tol, what, emu=em)
+
+
 def _check(oracle, got, k, ga, r, vk, gout, what):
     a, gk, out, gr, gvk = got
-    assert_close(a, oracle.sqrelu(k), TOL, f"{what} a")
-    assert_close(gk, oracle.sqrelu_backward(k, ga), TOL, f"{what} gk")
-    assert_close(out, oracle.cmix_gate(r, vk), TOL, f"{what} out")
+    _close(a, oracle.sqrelu(k), emu.sqrelu(k), f"{what} a")
+    _close(gk, oracle.sqrelu_backward(k, ga), emu.sqrelu_backward(k, ga), f"{what} gk")
+    _close(out, oracle.cmix_gate(r, vk), emu.cmix_gate(r, vk), f"{what} out")
     ogr, ogvk = oracle.cmix_gate_backward(r, vk, gout)
-    assert_close(gr, ogr, TOL, f"{what} gr")
-    assert_close(gvk, ogvk, TOL, f"{what} gvk")
+    egr, egvk = emu.cmix_gate_backward(r, vk, gout)
+    _close(gr, ogr, egr, f"{what} gr")
+    _close(gvk, ogvk, egvk, f"{what} gvk")
 
 
 SIZES = [1, 3, 4, 5, 7, 1000, 4097, (1 << 20) + 3]
@@ -103,4 +109,4 @@ def test_workload_cmix_full(oracle, wkv):
     k, ga, r, vk, gout = inputs.cmix_inputs(M.B, M.T, M.C, M.H, seed=M.seed)
     got = _all(wkv, *cuda(k, ga, r, vk, gout))
     _check(oracle, got, k, ga, r, vk, gout, "cmix")
-    assert_close(got[0].view(M.B, M.T, M.H), oracle.sqrelu(k), TOL_Y, "cmix a shape")
+    _close(got[0].view(M.B, M.T, M.H), oracle.sqrelu(k), emu.sqrelu(k), "cmix a shape", tol=TOL_Y)

@@ -12,6 +12,8 @@ import numpy as np
 import pytest
 import torch
 
+import fp32_emulation as emu
+from checks import check_pair_grads
 from parity import TOL_BF16, TOL_GRAD, TOL_Y, assert_close, cuda, to_np
 from rwkv_linear_attention_backward_b300 import inputs
 
@@ -39,15 +41,25 @@ def _run(wkv, w, u, k, v, r, gout, use_ckpt=True):
     return (out, ckpt) + grads
 
 
+GATED = ("gw", "gu", "gk", "gv", "gr")
+
+
+def _check_out(oracle, w, u, k, v, r, out, what, tol=TOL_Y):
+    assert_close(out, oracle.forward_gated(w, u, k, v, r), tol, f"{what} out", emu=emu.forward_gated(w, u, k, v, r))
+
+
+def _check_grads(oracle, w, u, k, v, r, gout, got, what):
+    """``got``: the GPU's (gw, gu, gk, gv, gr)."""
+    o = oracle.backward_gated(w, u, k, v, r, gout)
+    e = emu.backward_gated(w, u, k, v, r, gout)
+    for g, oo, ee, n in zip(got, o, e, GATED):
+        assert_close(g, oo, TOL_GRAD, f"{what} {n}", emu=ee)
+
+
 def _check(oracle, wkv, w, u, k, v, r, gout, what, tol_out=TOL_Y, use_ckpt=True):
     out, _, gw, gu, gk, gv, gr = _run(wkv, w, u, k, v, r, gout, use_ckpt)
-    assert_close(out, oracle.forward_gated(w, u, k, v, r), tol_out, f"{what} out")
-    ow, ou, ok, ov, orr = oracle.backward_gated(w, u, k, v, r, gout)
-    assert_close(gk, ok, TOL_GRAD, f"{what} gk")
-    assert_close(gv, ov, TOL_GRAD, f"{what} gv")
-    assert_close(gw, ow, TOL_GRAD, f"{what} gw")
-    assert_close(gu, ou, TOL_GRAD, f"{what} gu")
-    assert_close(gr, orr, TOL_GRAD, f"{what} gr")
+    _check_out(oracle, w, u, k, v, r, out, what, tol_out)
+    _check_grads(oracle, w, u, k, v, r, gout, (gw, gu, gk, gv, gr), what)
 
 
 def _refused(wkv, w, u, k, v, r, gout):
@@ -99,10 +111,10 @@ def test_gated_bf16(oracle, wkv, scan_mode):
         return
     _check(oracle, wkv, w, u, k, v, r, gout, "bf16", tol_out=TOL_BF16)
     out = _run(wkv, w, u, k, v, r, gout)[0]
-    assert_close(out, oracle.forward_gated(w, u, k, v, r), TOL_Y, "bf16 out (fp32-level)")
+    _check_out(oracle, w, u, k, v, r, out, "bf16 (fp32-level)")
 
 
-def test_gate_at_one_is_ungated(wkv):
+def test_gate_at_one_is_ungated(oracle, wkv):
     """r = 30: sigmoid(r) rounds to 1 in fp32, so the gated output is wkv bit
     for bit (one run per column, so both calls split the columns alike) and
     gr is exactly 0.  The gradients equal the ungated call's with gy = gout
@@ -122,8 +134,9 @@ def test_gate_at_one_is_ungated(wkv):
     assert torch.equal(out, y), "out vs y"
     assert torch.equal(ckpt, ckpt2), "ckpt"
     assert torch.count_nonzero(gr).item() == 0, "gr"
-    for a, b, n in zip((gw, gu, gk, gv), ref, ("gw", "gu", "gk", "gv")):
-        assert_close(a, b, 1e-6, f"r=30 {n} vs ungated")
+    names = ("gw", "gu", "gk", "gv")
+    check_pair_grads(oracle, w, u, k, v, gout, dict(zip(names, (gw, gu, gk, gv))), dict(zip(names, ref)),
+                     "r=30 vs ungated", tol=1e-6)
 
 
 def test_gated_state_in_out(oracle, wkv):
@@ -141,9 +154,10 @@ def test_gated_state_in_out(oracle, wkv):
     torch.cuda.synchronize()
     assert torch.equal(s2, s3), "state out"
     want = oracle.forward_gated(w, u, k, v, r)[:, 100:]
-    assert_close(out, want, TOL_Y, "gated continuation vs oracle")
+    e = emu.forward_gated(w, u, k, v, r)[:, 100:]
+    assert_close(out, want, TOL_Y, "gated continuation vs oracle", emu=e)
     sig = 1.0 / (1.0 + np.exp(-to_np(r[:, 100:])))
-    assert_close(out, sig * to_np(y2), TOL_Y, "gated continuation vs ungated")
+    assert_close(out, sig * to_np(y2), TOL_Y, "gated continuation vs ungated", emu=e, ref=want, pair=True)
 
 
 def test_autograd_wrapper(oracle, wkv):
@@ -153,9 +167,7 @@ def test_autograd_wrapper(oracle, wkv):
     out = wkv.wkv_gated(wc, uc, kc, vc, rc)
     out.backward(gc.detach())
     torch.cuda.synchronize()
-    ow, ou, ok, ov, orr = oracle.backward_gated(w, u, k, v, r, gout)
-    for t, o_, n in ((wc, ow, "gw"), (uc, ou, "gu"), (kc, ok, "gk"), (vc, ov, "gv"), (rc, orr, "gr")):
-        assert_close(t.grad, o_, TOL_GRAD, f"autograd {n}")
+    _check_grads(oracle, w, u, k, v, r, gout, tuple(t.grad for t in (wc, uc, kc, vc, rc)), "autograd")
 
 
 def test_workload_l169m_gated_full(oracle, wkv):

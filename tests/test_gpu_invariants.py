@@ -4,7 +4,9 @@ workspace reuse, streams, and the bounded-wait error report."""
 import pytest
 import torch
 
-from parity import TOL_GRAD, TOL_Y, assert_close, cuda
+import fp32_emulation as emu
+from checks import check_grads, check_pair_grads, check_pair_y, check_y
+from parity import assert_close, cuda
 from rwkv_linear_attention_backward_b300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -42,12 +44,13 @@ def test_checkpoint_and_recompute_agree_bitwise(wkv, scan_mode):
 
 
 @pytest.mark.parametrize("t0", [333, 320])
-def test_forward_causal(wkv, scan_mode, t0):
+def test_forward_causal(oracle, wkv, scan_mode, t0):
     """y_t depends on tokens <= t only.  Whole chunks before the change are
     bitwise unchanged.  Inside the chunk holding the change, earlier outputs
     share the chunk's exponent reference (its largest k) with the changed
     tokens, so they may move by rounding only."""
-    w, u, k, v, gy = cuda(*inputs.training_inputs(2, 777, 96, seed=23, k_std=2.0))
+    host = inputs.training_inputs(2, 777, 96, seed=23, k_std=2.0)
+    w, u, k, v, gy = cuda(*host)
     y = wkv.forward(w, u, k, v)
     k2, v2 = k.clone(), v.clone()
     k2[:, t0:] += 3.0
@@ -58,7 +61,10 @@ def test_forward_causal(wkv, scan_mode, t0):
     c0 = (t0 // L) * L  # first token of the chunk holding t0
     assert torch.equal(y[:, :c0], y2[:, :c0])
     if c0 < t0:
-        assert_close(y2[:, c0:t0], y[:, c0:t0], 1e-6, "same-chunk outputs before the change")
+        hw, hu, hk, hv = host[:4]
+        assert_close(y2[:, c0:t0], y[:, c0:t0], 1e-6, "same-chunk outputs before the change",
+                     emu=emu.forward_recurrent(hw, hu, hk, hv)[:, c0:t0],
+                     ref=oracle.forward_recurrent(hw, hu, hk, hv)[:, c0:t0], pair=True)
     assert not torch.equal(y[:, t0:], y2[:, t0:])
 
 
@@ -73,13 +79,14 @@ def test_backward_anticausal(wkv, scan_mode):
     assert torch.equal(gk[:, t0:], gk2[:, t0:]) and torch.equal(gv[:, t0:], gv2[:, t0:])
 
 
-def test_k_shift_invariance(wkv, scan_mode):
-    w, u, k, v, gy = cuda(*inputs.training_inputs(2, 600, 64, seed=25, k_std=2.0))
+def test_k_shift_invariance(oracle, wkv, scan_mode):
+    host = inputs.training_inputs(2, 600, 64, seed=25, k_std=2.0)
+    w, u, k, v, gy = cuda(*host)
     a = _run(wkv, w, u, k, v, gy)
     b = _run(wkv, w, u, k + 30.0, v, gy)
-    assert_close(b[0], a[0], TOL_Y, "y(k+30)")
-    for x, y_, n in zip(b[2:], a[2:], ("gw", "gu", "gk", "gv")):
-        assert_close(x, y_, TOL_GRAD, n)
+    check_pair_y(oracle, *host[:4], b[0], a[0], "y(k+30)")
+    names = ("gw", "gu", "gk", "gv")
+    check_pair_grads(oracle, *host, dict(zip(names, b[2:])), dict(zip(names, a[2:])), "k+30")
     s = a[4].double().sum(dim=1).abs().max().item()  # sum_t gk_t = 0 per (b, c)
     assert s <= 1e-4 * a[4].abs().max().item() * 600 ** 0.5
 
@@ -92,10 +99,8 @@ def test_workspace_reused_across_shapes(oracle, wkv, scan_mode):
         y = wkv.forward(wc, uc, kc, vc, workspace=ws)
         gw, gu, gk, gv = wkv.backward(wc, uc, kc, vc, gyc, workspace=ws)
         torch.cuda.synchronize()
-        assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "y")
-        ow, ou, ok, ov = oracle.backward_adjoint(w, u, k, v, gy)
-        assert_close(gk, ok, TOL_GRAD, "gk")
-        assert_close(gw, ow, TOL_GRAD, "gw")
+        check_y(oracle, w, u, k, v, y, "reused workspace")
+        check_grads(oracle, w, u, k, v, gy, dict(gk=gk, gw=gw), "reused workspace")
         wkv.workspace_check(ws)
 
 
@@ -107,8 +112,8 @@ def test_side_stream(oracle, wkv, scan_mode):
         y = wkv.forward(*tw[:4], stream=s)
         gw, gu, gk, gv = wkv.backward(*tw, stream=s)
     s.synchronize()
-    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "y")
-    assert_close(gv, oracle.backward_adjoint(w, u, k, v, gy)[3], TOL_GRAD, "gv")
+    check_y(oracle, w, u, k, v, y, "side stream")
+    check_grads(oracle, w, u, k, v, gy, dict(gv=gv), "side stream")
 
 
 @pytest.mark.parametrize("mode", ["chunked", "sequential", "sequential-chain3"])
@@ -136,19 +141,25 @@ def test_expired_wait_is_reported(oracle, wkv, which, mode):
         with pytest.raises(wkv.WKVError) as exc:
             wkv.workspace_check(ws)
         assert exc.value.status == 6
+        # the device-wide record reports it too, once
+        with pytest.raises(wkv.WKVError) as exc:
+            wkv.sync_status()
+        assert exc.value.status == 6
     finally:
         wkv.set_skip_chunk(-1)
         wkv.set_wait_budget_ns(0)
-    wkv.workspace_check(ws)  # the record was cleared
+    wkv.workspace_check(ws)  # the records were cleared
+    wkv.sync_status()
     try:
         y = wkv.forward(*tw[:4], workspace=ws)
         gw, gu, gk, gv = wkv.backward(*tw, workspace=ws)
         wkv.workspace_check(ws)
+        wkv.sync_status()
     finally:
         wkv.set_scan_mode("auto")
         wkv.set_chain_len(0)
-    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "y after timeout")
-    assert_close(gk, oracle.backward_adjoint(w, u, k, v, gy)[2], TOL_GRAD, "gk after timeout")
+    check_y(oracle, w, u, k, v, y, "after timeout")
+    check_grads(oracle, w, u, k, v, gy, dict(gk=gk), "after timeout")
 
 
 def test_graph_replay_with_new_inputs(wkv, scan_mode):

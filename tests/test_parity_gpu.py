@@ -11,6 +11,8 @@ import numpy as np
 import pytest
 import torch
 
+import fp32_emulation as emu
+from checks import check_grads, check_pair_grads, check_pair_y, check_y
 from parity import TOL_BF16, TOL_GRAD, TOL_Y, assert_close, assert_state_close, cuda, sample_channels, to_np
 from rwkv_linear_attention_backward_b300 import inputs
 
@@ -34,12 +36,8 @@ def run_fwd_bwd(wkv, w, u, k, v, gy, use_ckpt=True):
 
 def check_all(oracle, wkv, w, u, k, v, gy, use_ckpt=True, what=""):
     y, ckpt, gw, gu, gk, gv = run_fwd_bwd(wkv, w, u, k, v, gy, use_ckpt)
-    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, f"{what} y")
-    ow, ou, ok, ov = oracle.backward_adjoint(w, u, k, v, gy)
-    assert_close(gk, ok, TOL_GRAD, f"{what} gk")
-    assert_close(gv, ov, TOL_GRAD, f"{what} gv")
-    assert_close(gw, ow, TOL_GRAD, f"{what} gw")
-    assert_close(gu, ou, TOL_GRAD, f"{what} gu")
+    check_y(oracle, w, u, k, v, y, what)
+    check_grads(oracle, w, u, k, v, gy, dict(gk=gk, gv=gv, gw=gw, gu=gu), what)
     return y, ckpt
 
 
@@ -67,10 +65,11 @@ def test_checkpoint_is_the_carried_state(oracle, wkv, scan_mode):
     L = wkv.chunk_len()
     nch = -(-T // L)
     ck = to_np(ckpt).reshape(3, nch, B, C)
+    ends = [min((j + 1) * L, T) for j in range(nch)]
+    sums = emu.sums_after(w, k, v, ends)
     for j in range(nch):
-        t = min((j + 1) * L, T)
-        num, den, pp = oracle.state(w, k, v, t)
-        assert_state_close(ck[0, j], ck[1, j], ck[2, j], num, den, pp, TOL_Y, f"after chunk {j}")
+        num, den, pp = oracle.state(w, k, v, ends[j])
+        assert_state_close(ck[0, j], ck[1, j], ck[2, j], num, den, pp, TOL_Y, f"after chunk {j}", emu_sums=sums[j])
 
 
 @pytest.mark.parametrize("case", ["k_shift_64", "tiny_w", "huge_w", "big_u", "k_std_8"])
@@ -104,9 +103,9 @@ def test_bf16_forward(oracle, wkv, scan_mode):
     w, u, k, v, _ = inputs.training_inputs(B, T, C, seed=9, k_std=5.0, d_lo=-8.0, d_hi=1.0, kv_dtype="bf16")
     y = wkv.forward(*cuda(w, u, k, v))
     torch.cuda.synchronize()
-    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_BF16, "bf16 y")
+    check_y(oracle, w, u, k, v, y, "bf16", tol=TOL_BF16)
     # far inside the loose bf16 tolerance: the oracle sees the same rounded inputs
-    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "bf16 y (fp32-level)")
+    check_y(oracle, w, u, k, v, y, "bf16 (fp32-level)")
 
 
 BF16_SHAPES = [(1, 1, 8), (2, 33, 136), (3, 200, 96), (1, 1000, 40), (2, 513, 384)]
@@ -124,14 +123,7 @@ def test_bf16_backward(oracle, wkv, scan_mode, B, T, C):
         assert exc.value.status == 2
         return
     for use_ckpt in (True, False):
-        y, ckpt, gw, gu, gk, gv = run_fwd_bwd(wkv, w, u, k, v, gy, use_ckpt=use_ckpt)
-        ow, ou, ok, ov = oracle.backward_adjoint(w, u, k, v, gy)
-        what = f"bf16 ckpt={use_ckpt}"
-        assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, f"{what} y")
-        assert_close(gk, ok, TOL_GRAD, f"{what} gk")
-        assert_close(gv, ov, TOL_GRAD, f"{what} gv")
-        assert_close(gw, ow, TOL_GRAD, f"{what} gw")
-        assert_close(gu, ou, TOL_GRAD, f"{what} gu")
+        check_all(oracle, wkv, w, u, k, v, gy, use_ckpt=use_ckpt, what=f"bf16 ckpt={use_ckpt}")
 
 
 def test_bf16_backward_agrees_with_fp32_of_rounded_inputs(wkv):
@@ -162,7 +154,7 @@ def _both_modes(wkv, w, u, k, v, gy, max_runs=0):
     return res["chunked"], res["sequential"]
 
 
-def test_scan_modes_agree_bitwise(wkv):
+def test_scan_modes_agree_bitwise(oracle, wkv):
     """With one run per column, the sequential walk carries the state across
     chunk boundaries with the chunked scan's combine, in the same order, and
     computes a chunk's outputs with the same fixed-scale arithmetic: on
@@ -173,8 +165,15 @@ def test_scan_modes_agree_bitwise(wkv):
     a, b = _both_modes(wkv, w, u, k, v, gy, max_runs=1)
     assert torch.equal(a[0], b[0]), "y"
     assert torch.equal(a[1], b[1]), "ckpt"
-    for x, y_, n in zip(a[2:], b[2:], ("gw", "gu", "gk", "gv")):
-        assert_close(y_, x, TOL_GRAD, f"{n} sequential vs chunked")
+    _pairs(oracle, w, u, k, v, gy, a, b)
+
+
+def _pairs(oracle, w, u, k, v, gy, a, b):
+    """The two strategies' results against each other (both fp32
+    evaluations: the floor is twice the float32 evaluation's error)."""
+    check_pair_y(oracle, w, u, k, v, b[0], a[0], "y sequential vs chunked")
+    check_pair_grads(oracle, w, u, k, v, gy, dict(zip(("gw", "gu", "gk", "gv"), b[2:])),
+                     dict(zip(("gw", "gu", "gk", "gv"), a[2:])), "sequential vs chunked")
 
 
 def test_scan_modes_agree_runs(oracle, wkv):
@@ -184,25 +183,22 @@ def test_scan_modes_agree_runs(oracle, wkv):
     B, T, C = 8, 1000, 768
     w, u, k, v, gy = inputs.training_inputs(B, T, C, seed=41, k_std=3.0, d_lo=-6.0, d_hi=2.0)
     a, b = _both_modes(wkv, w, u, k, v, gy)
-    assert_close(b[0], a[0], TOL_Y, "y sequential vs chunked")
-    for x, y_, n in zip(a[2:], b[2:], ("gw", "gu", "gk", "gv")):
-        assert_close(y_, x, TOL_GRAD, f"{n} sequential vs chunked")
+    _pairs(oracle, w, u, k, v, gy, a, b)
     cs = sample_channels(C, 24, 41)
-    ks, vs = k[:, :, cs].contiguous(), v[:, :, cs].contiguous()
-    ow, ou, ok, ov = oracle.backward_adjoint(w[cs], u[cs], ks, vs, gy[:, :, cs].contiguous())
+    ws, us, ks, vs, gs = w[cs], u[cs], k[:, :, cs].contiguous(), v[:, :, cs].contiguous(), gy[:, :, cs].contiguous()
     cst = torch.as_tensor(cs, device="cuda")
-    assert_close(b[0].index_select(2, cst), oracle.forward_recurrent(w[cs], u[cs], ks, vs), TOL_Y, "sequential y")
-    assert_close(b[4].index_select(2, cst), ok, TOL_GRAD, "sequential gk")
-    assert_close(b[5].index_select(2, cst), ov, TOL_GRAD, "sequential gv")
-    assert_close(b[2].index_select(0, cst), ow, TOL_GRAD, "sequential gw")
-    assert_close(b[3].index_select(0, cst), ou, TOL_GRAD, "sequential gu")
+    check_y(oracle, ws, us, ks, vs, b[0].index_select(2, cst), "sequential")
+    check_grads(oracle, ws, us, ks, vs, gs, dict(gk=b[4].index_select(2, cst), gv=b[5].index_select(2, cst),
+                                                 gw=b[2].index_select(0, cst), gu=b[3].index_select(0, cst)),
+                "sequential")
 
 
 # ------------------------------------------------------------ named workloads
 def test_workload_tiny(oracle, wkv):
     w, u, k, v, gy = inputs.workload_inputs("tiny")
     y, _ = check_all(oracle, wkv, w, u, k, v, gy, what="tiny")
-    assert_close(y, oracle.forward_direct(w, u, k, v), TOL_Y, "tiny y vs direct form")
+    assert_close(y, oracle.forward_direct(w, u, k, v), TOL_Y, "tiny y vs direct form",
+                 emu=emu.forward_recurrent(w, u, k, v))
 
 
 def test_workload_l169m_full(oracle, wkv):
@@ -214,21 +210,17 @@ def _sampled(oracle, wkv, name, nchan, seed):
     w, u, k, v, gy = inputs.workload_inputs(name)
     wl = inputs.WORKLOADS[name]
     cs = sample_channels(wl.C, nchan, seed)
-    ks, vs = k[:, :, cs].contiguous(), v[:, :, cs].contiguous()
+    ws, us, ks, vs = w[cs], u[cs], k[:, :, cs].contiguous(), v[:, :, cs].contiguous()
+    cst = torch.as_tensor(cs, device="cuda")
     if wl.backward:
         y, _, gw, gu, gk, gv = run_fwd_bwd(wkv, w, u, k, v, gy)
-        ow, ou, ok, ov = oracle.backward_adjoint(w[cs], u[cs], ks, vs, gy[:, :, cs].contiguous())
-        cst = torch.as_tensor(cs, device="cuda")
-        assert_close(gk.index_select(2, cst), ok, TOL_GRAD, f"{name} gk")
-        assert_close(gv.index_select(2, cst), ov, TOL_GRAD, f"{name} gv")
-        assert_close(gw.index_select(0, cst), ow, TOL_GRAD, f"{name} gw")
-        assert_close(gu.index_select(0, cst), ou, TOL_GRAD, f"{name} gu")
+        check_grads(oracle, ws, us, ks, vs, gy[:, :, cs].contiguous(),
+                    dict(gk=gk.index_select(2, cst), gv=gv.index_select(2, cst), gw=gw.index_select(0, cst),
+                         gu=gu.index_select(0, cst)), name)
     else:
         y = wkv.forward(*cuda(w, u, k, v))
         torch.cuda.synchronize()
-        cst = torch.as_tensor(cs, device="cuda")
-    tol = TOL_BF16 if wl.kv_dtype == "bf16" else TOL_Y
-    assert_close(y.index_select(2, cst), oracle.forward_recurrent(w[cs], u[cs], ks, vs), tol, f"{name} y")
+    check_y(oracle, ws, us, ks, vs, y.index_select(2, cst), name, tol=TOL_BF16 if wl.kv_dtype == "bf16" else TOL_Y)
 
 
 def test_workload_l1b5_sampled(oracle, wkv):

@@ -9,6 +9,8 @@ import numpy as np
 import pytest
 import torch
 
+import fp32_emulation as emu
+from checks import check_grads, check_pair_grads
 from parity import TOL_GRAD, assert_close, cuda, to_np
 from rwkv_linear_attention_backward_b300 import inputs
 
@@ -50,21 +52,21 @@ def test_backward_with_state_vs_oracle(oracle, wkv, scan_mode, B, P, T, C):
                         s_out[2].cpu()])  # written at the end state's own scale
     sin64 = tuple(sin.double().numpy())
     ge = gend.double().numpy()
-    ow, ou, ok, ov, (ga, gb) = oracle.backward_state(w, u, ks, vs, gs, sin64,
-                                                     (ge[0] * np.exp(-ge[2]), ge[1] * np.exp(-ge[2])))
+    aend = (ge[0] * np.exp(-ge[2]), ge[1] * np.exp(-ge[2]))
+    ow, ou, ok, ov, (ga, gb) = oracle.backward_state(w, u, ks, vs, gs, sin64, aend)
+    eo = emu.backward(w, u, ks, vs, gs, state_in=sin64, adj_end=aend)
     for use_ckpt in (True, False):
         gw, gu, gk, gv, gin = wkv.backward_with_state(wc, uc, kc, vc, gc, sc, gend.cuda(),
                                                       ckpt=ckpt if use_ckpt else None)
         torch.cuda.synchronize()
         what = f"B{B}P{P}T{T}C{C} ckpt={use_ckpt}"
-        assert_close(gk, ok, TOL_GRAD, f"{what} gk")
-        assert_close(gv, ov, TOL_GRAD, f"{what} gv")
-        assert_close(gw, ow, TOL_GRAD, f"{what} gw")
-        assert_close(gu, ou, TOL_GRAD, f"{what} gu")
+        for g, o, n in ((gk, ok, "gk"), (gv, ov, "gv"), (gw, ow, "gw"), (gu, ou, "gu")):
+            assert_close(g, o, TOL_GRAD, f"{what} {n}", emu=eo[n])
         gi = to_np(gin)
         assert np.array_equal(gi[2], sin64[2]), f"{what}: pp plane of the start-state gradient"
-        assert_close(gi[0], ga * np.exp(sin64[2]), TOL_GRAD, f"{what} g_num of the start state")
-        assert_close(gi[1], gb * np.exp(sin64[2]), TOL_GRAD, f"{what} g_den of the start state")
+        sp = np.exp(sin64[2])
+        assert_close(gi[0], ga * sp, TOL_GRAD, f"{what} g_num of the start state", emu=eo["ga"] * sp)
+        assert_close(gi[1], gb * sp, TOL_GRAD, f"{what} g_den of the start state", emu=eo["gb"] * sp)
 
 
 def test_without_states_is_plain_backward(wkv, scan_mode):
@@ -108,11 +110,8 @@ def test_segments_backward_give_the_whole(oracle, wkv, tsplit, scan_mode, cuts):
         gw += w_r.double()
         gu += u_r.double()
     torch.cuda.synchronize()
-    ow, ou, ok, ov = oracle.backward_adjoint(w, u, k, v, gy)
-    assert_close(torch.cat(gks, dim=1), ok, TOL_GRAD, f"{cuts} gk")
-    assert_close(torch.cat(gvs, dim=1), ov, TOL_GRAD, f"{cuts} gv")
-    assert_close(gw, ow, TOL_GRAD, f"{cuts} gw")
-    assert_close(gu, ou, TOL_GRAD, f"{cuts} gu")
+    split = dict(gk=torch.cat(gks, dim=1), gv=torch.cat(gvs, dim=1), gw=gw, gu=gu)
+    check_grads(oracle, w, u, k, v, gy, split, f"{cuts}")
     whole = wkv.backward(wc, uc, kc, vc, gc)
     torch.cuda.synchronize()
-    assert_close(torch.cat(gks, dim=1), whole[2], TOL_GRAD, f"{cuts} gk vs one call")
+    check_pair_grads(oracle, w, u, k, v, gy, dict(gk=split["gk"]), dict(gk=whole[2]), f"{cuts} vs one call")

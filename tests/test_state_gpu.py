@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import fp32_emulation as emu
 from parity import TOL_BF16, TOL_Y, assert_close, assert_state_close, cuda, to_np
 from rwkv_linear_attention_backward_b300 import inputs
 
@@ -41,9 +42,10 @@ def test_forward_from_state(oracle, wkv, scan_mode, B, T, C):
     y, sout = wkv.forward_with_state(*cuda(w, u, k, v), state_in=cuda(_planes(sin))[0])
     torch.cuda.synchronize()
     yo, (no, do, po) = oracle.forward_state(w, u, k, v, sin)
-    assert_close(y, yo, TOL_Y, "y")
+    fe = emu.forward(w, u, k, v, state_in=sin)
+    assert_close(y, yo, TOL_Y, "y", emu=fe["y"])
     s = to_np(sout)
-    assert_state_close(s[0], s[1], s[2], no, do, po, TOL_Y, "state out")
+    assert_state_close(s[0], s[1], s[2], no, do, po, TOL_Y, "state out", emu_sums=(fe["a"], fe["b"]))
 
 
 def test_forward_from_state_bf16(oracle, wkv, scan_mode):
@@ -52,9 +54,10 @@ def test_forward_from_state_bf16(oracle, wkv, scan_mode):
     y, sout = wkv.forward_with_state(*cuda(w, u, k, v), state_in=cuda(_planes(sin))[0])
     torch.cuda.synchronize()
     yo, (no, do, po) = oracle.forward_state(w, u, k, v, sin)
-    assert_close(y, yo, TOL_BF16, "bf16 y")
+    fe = emu.forward(w, u, k, v, state_in=sin)
+    assert_close(y, yo, TOL_BF16, "bf16 y", emu=fe["y"])
     s = to_np(sout)
-    assert_state_close(s[0], s[1], s[2], no, do, po, TOL_Y, "bf16 state out")
+    assert_state_close(s[0], s[1], s[2], no, do, po, TOL_Y, "bf16 state out", emu_sums=(fe["a"], fe["b"]))
 
 
 @pytest.mark.parametrize("t0", [1, 32, 100, 699])
@@ -69,13 +72,16 @@ def test_split_matches_whole(oracle, wkv, scan_mode, t0):
     y1, s1 = wkv.forward_with_state(wc, uc, kc[:, :t0].contiguous(), vc[:, :t0].contiguous())
     y2, s2 = wkv.forward_with_state(wc, uc, kc[:, t0:].contiguous(), vc[:, t0:].contiguous(), state_in=s1)
     torch.cuda.synchronize()
-    assert_close(torch.cat([y1, y2], dim=1), y, TOL_Y, "split vs whole")
+    fe = emu.forward(w, u, k, v)
+    assert_close(torch.cat([y1, y2], dim=1), y, TOL_Y, "split vs whole", emu=fe["y"],
+                 ref=oracle.forward_recurrent(w, u, k, v), pair=True)
     nch = -(-T // wkv.chunk_len())
     last = to_np(ckpt).reshape(3, nch, B, C)[:, nch - 1]
     s = to_np(s2)
     assert_state_close(s[0], s[1], s[2], last[0], last[1], last[2], TOL_Y, "state after both calls")
     n, d, p = oracle.state(w, k, v, T)
-    assert_state_close(s[0], s[1], s[2], n, d, p, TOL_Y, "state after both calls vs oracle")
+    assert_state_close(s[0], s[1], s[2], n, d, p, TOL_Y, "state after both calls vs oracle",
+                       emu_sums=(fe["a"], fe["b"]))
 
 
 def test_empty_state_is_forward(wkv, scan_mode):
@@ -103,6 +109,7 @@ def test_prefill_then_decode(oracle, wkv):
     num, den, pp = (sout[i].clone().unsqueeze(0) for i in range(3))  # one layer: [1, B, C]
     g = torch.Generator().manual_seed(341)
     on, od, op = (a[None] for a in oracle.state(w, k, v, T))
+    ea, eb = (x[None] for x in emu.sums_after(w, k, v, [T])[0])
     for t in range(T, T + n):
         x, xp, r = (torch.randn(1, B, C, generator=g) for _ in range(3))
         mu = [torch.rand(1, C, generator=g) for _ in range(3)]
@@ -110,6 +117,8 @@ def test_prefill_then_decode(oracle, wkv):
         y, _, _, _ = wkv.decode_step(*cuda(x, xp, mu[0], mu[1], mu[2], r, kt, vt, w[None], u[None]), num, den, pp)
         yo, on, od, op, _, _, _ = oracle.decode_step(x, xp, mu[0], mu[1], mu[2], r, kt, vt, w[None], u[None],
                                                      on, od, op)
+        ye, ea, eb, _, _, _ = emu.decode_step(x, xp, mu[0], mu[1], mu[2], r, kt, vt, w[None], u[None], ea, eb)
         torch.cuda.synchronize()
-        assert_close(y, yo, TOL_Y, f"decode step {t - T}")
-    assert_state_close(to_np(num)[0], to_np(den)[0], to_np(pp)[0], on[0], od[0], op[0], TOL_Y, "final state")
+        assert_close(y, yo, TOL_Y, f"decode step {t - T}", emu=ye)
+    assert_state_close(to_np(num)[0], to_np(den)[0], to_np(pp)[0], on[0], od[0], op[0], TOL_Y, "final state",
+                       emu_sums=(ea[0], eb[0]))

@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import fp32_emulation as emu
 from parity import TOL_BF16, TOL_Y, assert_close, assert_state_close, cuda, to_np
 from rwkv_linear_attention_backward_b300 import inputs
 
@@ -55,11 +56,13 @@ def test_segments_give_the_whole_sequence(oracle, wkv, tsplit, scan_mode, cuts):
     y, ends = _segments(tsplit, wkv, wc, uc, kc, vc, cuts)
     y_whole, s_whole = wkv.forward_with_state(wc, uc, kc, vc)
     torch.cuda.synchronize()
-    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, f"{cuts} y vs oracle")
-    assert_close(y, y_whole, TOL_Y, f"{cuts} y vs one call")
+    fe = emu.forward(w, u, k, v)
+    yo = oracle.forward_recurrent(w, u, k, v)
+    assert_close(y, yo, TOL_Y, f"{cuts} y vs oracle", emu=fe["y"])
+    assert_close(y, y_whole, TOL_Y, f"{cuts} y vs one call", emu=fe["y"], ref=yo, pair=True)
     n, d, p = oracle.state(w, k, v, T)
     e = to_np(ends[-1])
-    assert_state_close(e[0], e[1], e[2], n, d, p, TOL_Y, f"{cuts} end state")
+    assert_state_close(e[0], e[1], e[2], n, d, p, TOL_Y, f"{cuts} end state", emu_sums=(fe["a"], fe["b"]))
 
 
 def test_segments_after_a_given_state(oracle, wkv, tsplit):
@@ -70,10 +73,12 @@ def test_segments_after_a_given_state(oracle, wkv, tsplit):
     sin = torch.tensor(np.stack(oracle.state(w, k[:, :P], v[:, :P], P)), dtype=torch.float32)
     wc, uc, kc, vc, sc = cuda(w, u, k[:, P:].contiguous(), v[:, P:].contiguous(), sin)
     y, ends = _segments(tsplit, wkv, wc, uc, kc, vc, [0, 250, 251, 900], state_in=sc)
-    assert_close(y, oracle.forward_recurrent(w, u, k, v)[:, P:], TOL_Y, "y after a given state")
+    fe = emu.forward(w, u, k[:, P:], v[:, P:], state_in=sin)
+    assert_close(y, oracle.forward_recurrent(w, u, k, v)[:, P:], TOL_Y, "y after a given state", emu=fe["y"])
     n, d, p = oracle.state(w, k, v, P + T)
     e = to_np(ends[-1])
-    assert_state_close(e[0], e[1], e[2], n, d, p, TOL_Y, "end state after a given state")
+    assert_state_close(e[0], e[1], e[2], n, d, p, TOL_Y, "end state after a given state",
+                       emu_sums=(fe["a"], fe["b"]))
 
 
 def test_segments_bf16(oracle, wkv, tsplit, scan_mode):
@@ -81,8 +86,9 @@ def test_segments_bf16(oracle, wkv, tsplit, scan_mode):
     w, u, k, v, _ = inputs.training_inputs(B, T, C, seed=730, k_std=4.0, kv_dtype="bf16")
     wc, uc, kc, vc = cuda(w, u, k, v)
     y, _ = _segments(tsplit, wkv, wc, uc, kc, vc, [0, 100, 400, 777])
-    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_BF16, "bf16 segments y")
-    assert_close(y, oracle.forward_recurrent(w, u, k, v), TOL_Y, "bf16 segments y (fp32-level)")
+    yo, ye = oracle.forward_recurrent(w, u, k, v), emu.forward_recurrent(w, u, k, v)
+    assert_close(y, yo, TOL_BF16, "bf16 segments y", emu=ye)
+    assert_close(y, yo, TOL_Y, "bf16 segments y (fp32-level)", emu=ye)
 
 
 def test_state_only_pass_matches_full_pass(oracle, wkv, scan_mode):
@@ -96,7 +102,8 @@ def test_state_only_pass_matches_full_pass(oracle, wkv, scan_mode):
     a, b = to_np(s_none), to_np(s_full)
     assert_state_close(a[0], a[1], a[2], b[0], b[1], b[2], TOL_Y, "state-only vs full pass")
     n, d, p = oracle.state(w, k, v, T)
-    assert_state_close(a[0], a[1], a[2], n, d, p, TOL_Y, "state-only vs oracle")
+    fe = emu.forward(w, u, k, v)
+    assert_state_close(a[0], a[1], a[2], n, d, p, TOL_Y, "state-only vs oracle", emu_sums=(fe["a"], fe["b"]))
     assert_close(ck_none, ck_full, TOL_Y, "checkpoints")
 
 
@@ -119,6 +126,7 @@ def test_state_fold_kernel(oracle, wkv):
     g = to_np(out)
     assert_state_close(g[0], g[1], g[2], n, d, p, TOL_Y, "fold vs oracle")
     n2, d2, p2 = oracle.state(w, k, v, T)
-    assert_state_close(g[0], g[1], g[2], n2, d2, p2, TOL_Y, "fold vs whole")
+    fe = emu.forward(w, u, k, v)
+    assert_state_close(g[0], g[1], g[2], n2, d2, p2, TOL_Y, "fold vs whole", emu_sums=(fe["a"], fe["b"]))
     e = to_np(empty)
     assert np.all(e[0] == 0) and np.all(e[1] == 0) and np.all(e[2] < -1e37)
