@@ -25,7 +25,9 @@
  * Conventions for every entry point
  *   - Tensor arguments are DEVICE pointers owned by the caller (no host
  *     pointers).  The library allocates nothing and keeps no per-call state;
- *     all scratch lives in the caller's workspace.
+ *     all scratch lives in the caller's workspace (wkv_forward_noalloc:
+ *     a fixed array in the library).  Its one device-side record is the
+ *     expired-wait flag that wkv_sync_status reads.
  *   - k, v, y, gy, gk, gv are [B, T, C] row-major, C fastest.  w, u, gw, gu
  *     are [C].  Decode tensors are [L, B, C]; decode parameters [L, C].
  *   - stream is a cudaStream_t cast to void*; NULL is the legacy default
@@ -57,7 +59,7 @@ typedef enum {
   WKV_ERR_MISALIGNED = 3,  /* reserved */
   WKV_ERR_WORKSPACE = 4,   /* workspace null or smaller than the *_workspace_bytes query */
   WKV_ERR_CUDA = 5,        /* a CUDA call failed; see wkv_last_error_string() */
-  WKV_ERR_TIMEOUT = 6      /* a bounded device-side wait expired (see wkv_workspace_check) */
+  WKV_ERR_TIMEOUT = 6      /* a bounded device-side wait expired (wkv_workspace_check, wkv_sync_status) */
 } wkv_status;
 
 typedef enum { WKV_F32 = 0, WKV_BF16 = 1 } wkv_dtype;
@@ -104,6 +106,16 @@ wkv_status wkv_workspace_init(void* workspace, size_t bytes, void* stream);
  * its outputs are then invalid) and clears that record.  WKV_OK otherwise. */
 wkv_status wkv_workspace_check(void* workspace, void* stream);
 
+/* Synchronises `stream` (WKV_ERR_CUDA with the runtime's message if the
+ * stream reports an error), then reports whether any kernel of this
+ * library on the current device gave up a bounded wait since the last
+ * wkv_sync_status: WKV_ERR_TIMEOUT (the outputs of that call are invalid),
+ * else WKV_OK.  The record is device-wide, not per stream or workspace
+ * (every workspace, and wkv_forward_noalloc's built-in scratch, feed it),
+ * and taking it clears it; wkv_workspace_check keeps its own record per
+ * workspace.  Call it from one host thread at a time per device. */
+wkv_status wkv_sync_status(void* stream);
+
 /*
  * wkv_forward -- the training (time-parallel) form: y[b,t,c] = wkv_t for all
  * t at once, by a chunked associative scan over T (chunk summaries combined
@@ -145,8 +157,8 @@ wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const 
  *              given), and no output is read back or stored.
  *   The other arguments are those of wkv_forward; ckpt and y describe the T
  *   tokens of this call.  wkv_backward differentiates the forward pass from
- *   the empty state only: the gradient with respect to a state_in is not
- *   computed.
+ *   the empty state; wkv_backward_with_state differentiates this call,
+ *   state_in included, and takes a gradient on state_out.
  * Errors: as wkv_forward (y, state_out and ckpt all NULL:
  * WKV_ERR_INVALID_ARG).
  */
@@ -325,6 +337,24 @@ wkv_status wkv_decode_step(int L, int B, int C, const float* x, const float* x_p
                            float* xv, float* xr, void* stream);
 
 /*
+ * wkv_decode_step_bf16 -- wkv_decode_step with bf16 token inputs: x, x_prev,
+ * r, k, v are [L, B, C] bf16 (the RNN mode of "RWKV についての調査記録",
+ * section "RWKVとは？": a token and a state in, an output and a new state
+ * out).  The parameters mu_k, mu_v, mu_r, w, u, the state num, den, pp and
+ * the outputs y, xk, xv, xr stay fp32, and every operation is the fp32
+ * arithmetic of wkv_decode_step on the widened inputs (a bf16 value widens
+ * to fp32 exactly), so for the same rounded inputs the two calls agree bit
+ * for bit.  50 bytes per element move with the mix outputs (60 with fp32
+ * inputs).  Any alignment is accepted; 8-byte aligned bf16 tensors and
+ * 16-byte aligned fp32 tensors with C % 4 == 0 take the vectorised path.
+ * Errors: as wkv_decode_step.
+ */
+wkv_status wkv_decode_step_bf16(int L, int B, int C, const void* x, const void* x_prev, const float* mu_k,
+                                const float* mu_v, const float* mu_r, const void* r, const void* k, const void* v,
+                                const float* w, const float* u, float* num, float* den, float* pp, float* y,
+                                float* xk, float* xv, float* xr, void* stream);
+
+/*
  * wkv_token_shift -- the token shift of the training path, eq. (7) of
  * "RWKV解读" section "3、RWKV的网络架构": the input of each projection is
  * a weighted sum of the current and the previous token.  Per (b, t, c),
@@ -376,6 +406,8 @@ wkv_status wkv_token_shift_backward(int B, int T, int C, const float* x, const f
  * library holds until the process exits.  Nothing is allocated.
  *   - Shapes whose wkv_forward_workspace_bytes exceed 32 MiB are rejected
  *     with WKV_ERR_WORKSPACE and a message in wkv_last_error_string().
+ *   - The array used is the current device's: make the device that holds
+ *     the tensors current before the call.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
@@ -385,8 +417,8 @@ wkv_status wkv_token_shift_backward(int B, int T, int C, const float* x, const f
  *     that an earlier call's are never taken for the current one's).  Calls
  *     that overlap on the GPU (different streams without ordering, or
  *     different host threads) race on the array: serialise them.
- *   - A bounded device-side wait that expires cannot be reported here (there
- *     is no workspace to check); use wkv_forward where that matters.
+ *   - A bounded device-side wait that expires is reported by
+ *     wkv_sync_status (there is no workspace to check).
  * Errors: as wkv_forward, plus WKV_ERR_WORKSPACE for shapes too large.
  */
 wkv_status wkv_forward_noalloc(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,

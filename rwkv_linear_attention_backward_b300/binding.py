@@ -40,6 +40,7 @@ _SIGNATURES = {
     "wkv_backward_workspace_bytes": ([_i, _i, _i], _sz),
     "wkv_workspace_init": ([_vp, _sz, _vp], _i),
     "wkv_workspace_check": ([_vp, _vp], _i),
+    "wkv_sync_status": ([_vp], _i),
     "wkv_forward": ([_i, _i, _i, _i] + [_vp] * 6 + [_vp, _sz, _vp], _i),
     "wkv_forward_with_state": ([_i, _i, _i, _i] + [_vp] * 8 + [_vp, _sz, _vp], _i),
     "wkv_backward": ([_i, _i, _i, _i] + [_vp] * 10 + [_vp, _sz, _vp], _i),
@@ -47,6 +48,7 @@ _SIGNATURES = {
     "wkv_backward_gated": ([_i, _i, _i, _i] + [_vp] * 12 + [_vp, _sz, _vp], _i),
     "wkv_backward_with_state": ([_i, _i, _i, _i] + [_vp] * 13 + [_vp, _sz, _vp], _i),
     "wkv_decode_step": ([_i, _i, _i] + [_vp] * 17 + [_vp], _i),
+    "wkv_decode_step_bf16": ([_i, _i, _i] + [_vp] * 17 + [_vp], _i),
     "wkv_forward_noalloc": ([_i, _i, _i, _i] + [_vp] * 6 + [_vp], _i),
     "wkv_debug_set_wait_budget_ns": ([_ll], _i),
     "wkv_debug_set_skip_chunk": ([_i], _i),
@@ -156,6 +158,13 @@ def _workspace(kind: str, nbytes: int, device: torch.device) -> Workspace:
 def workspace_check(ws: Workspace, stream=None) -> None:
     """Synchronise and raise WKVError if a bounded device wait expired."""
     _check(_lib.wkv_workspace_check(ws.ptr(), _stream(stream)), "wkv_workspace_check")
+
+
+def sync_status(stream=None) -> None:
+    """Synchronise ``stream`` and raise WKVError if any call of the library
+    on the current device gave up a bounded device wait since the last
+    check (device-wide; the record is cleared)."""
+    _check(_lib.wkv_sync_status(_stream(stream)), "wkv_sync_status")
 
 
 # ---------------------------------------------------------------- forward
@@ -327,19 +336,31 @@ def forward_noalloc(w, u, k, v, *, y=None, ckpt=None, stream=None):
     """wkv_forward with the library's built-in scratch instead of a
     workspace, for callers that cannot allocate device memory (see
     wkv_forward_noalloc in include/wkv.h).  Shapes needing more than 32 MiB
-    of scratch raise WKVError."""
+    of scratch raise WKVError.  Returns ``y``, or ``(y, ckpt)`` when a
+    ``ckpt`` buffer is given.  The call runs with the tensors' device
+    current (the scratch array is chosen by the current device)."""
+    if k.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("k must be float32 or bfloat16")
     B, T, C = k.shape
-    _need(k, "k", (torch.float32, torch.bfloat16))
+    _need(k, "k", (k.dtype,))
     _need(v, "v", (k.dtype,), k.shape)
     _need(w, "w", shape=(C,))
     _need(u, "u", shape=(C,))
     if y is None:
         y = torch.empty((B, T, C), dtype=torch.float32, device=k.device)
     _need(y, "y", shape=(B, T, C))
+    if ckpt is not None:
+        _need(ckpt, "ckpt")
+        if ckpt.numel() < checkpoint_floats(B, T, C):
+            raise ValueError("ckpt is too small")
+    for name, t in (("v", v), ("w", w), ("u", u), ("y", y), ("ckpt", ckpt)):
+        if t is not None and t.device != k.device:
+            raise ValueError(f"{name} is on {t.device}, k on {k.device}")
     dt = WKV_BF16 if k.dtype == torch.bfloat16 else WKV_F32
-    _check(_lib.wkv_forward_noalloc(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(y), _p(ckpt), _stream(stream)),
-           "wkv_forward_noalloc")
-    return y
+    with torch.cuda.device(k.device):
+        _check(_lib.wkv_forward_noalloc(B, T, C, dt, _p(w), _p(u), _p(k), _p(v), _p(y), _p(ckpt),
+                                        _stream(stream)), "wkv_forward_noalloc")
+    return (y, ckpt) if ckpt is not None else y
 
 
 # --------------------------------------------------------------- backward
@@ -503,26 +524,34 @@ def decode_step(x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u, num, den, pp, *, y=N
                 mix: bool = True, stream=None):
     """One fused RNN-mode step of L layers; num, den, pp [L, B, C] update in place.
 
+    The token inputs x, x_prev, r, k, v are all fp32 or all bf16
+    (wkv_decode_step_bf16); parameters, state and outputs are fp32.
     Returns (y, xk, xv, xr); the mix outputs are None when ``mix`` is False
     and no buffers are passed.
     """
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x must be float32 or bfloat16")
     L, B, C = x.shape
-    for t, n in ((x, "x"), (x_prev, "x_prev"), (r, "r"), (k, "k"), (v, "v"), (num, "num"), (den, "den"),
-                 (pp, "pp")):
+    for t, n in ((x, "x"), (x_prev, "x_prev"), (r, "r"), (k, "k"), (v, "v")):
+        _need(t, n, (x.dtype,), shape=(L, B, C))
+    for t, n in ((num, "num"), (den, "den"), (pp, "pp")):
         _need(t, n, shape=(L, B, C))
     for t, n in ((mu_k, "mu_k"), (mu_v, "mu_v"), (mu_r, "mu_r"), (w, "w"), (u, "u")):
         _need(t, n, shape=(L, C))
+    out = dict(dtype=torch.float32, device=x.device)
     if y is None:
-        y = torch.empty_like(x)
+        y = torch.empty((L, B, C), **out)
     if mix:
-        xk = torch.empty_like(x) if xk is None else xk
-        xv = torch.empty_like(x) if xv is None else xv
-        xr = torch.empty_like(x) if xr is None else xr
+        xk = torch.empty((L, B, C), **out) if xk is None else xk
+        xv = torch.empty((L, B, C), **out) if xv is None else xv
+        xr = torch.empty((L, B, C), **out) if xr is None else xr
     for t, n in ((y, "y"), (xk, "xk"), (xv, "xv"), (xr, "xr")):
         if t is not None:
             _need(t, n, shape=(L, B, C))
-    _check(_lib.wkv_decode_step(L, B, C, *map(_p, (x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u, num, den, pp, y, xk,
-                                                     xv, xr)), _stream(stream)), "wkv_decode_step")
+    fn, name = ((_lib.wkv_decode_step_bf16, "wkv_decode_step_bf16") if x.dtype == torch.bfloat16 else
+                (_lib.wkv_decode_step, "wkv_decode_step"))
+    _check(fn(L, B, C, *map(_p, (x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u, num, den, pp, y, xk, xv, xr)),
+              _stream(stream)), name)
     return y, xk, xv, xr
 
 

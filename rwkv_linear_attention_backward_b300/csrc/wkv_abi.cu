@@ -490,6 +490,23 @@ wkv_status wkv_workspace_check(void* workspace, void* stream) {
   return code == kDevErrTimeout ? WKV_ERR_TIMEOUT : WKV_ERR_CUDA;
 }
 
+wkv_status wkv_sync_status(void* stream) {
+  clear_error();
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wkv_sync_status: synchronize");
+  unsigned int first = 0;
+  cudaError_t (*const takers[])(unsigned int*) = {take_error_seq, take_error_fwd, take_error_bwd};
+  for (auto take : takers) {  // every record is taken (and cleared), the first one reported
+    unsigned int code = 0;
+    e = take(&code);
+    if (e != cudaSuccess) return cuda_fail(e, "wkv_sync_status: read");
+    if (first == 0) first = code;
+  }
+  if (first == 0) return WKV_OK;
+  set_last_error("wkv_sync_status: a bounded device-side wait expired; the outputs of that call are invalid");
+  return first == kDevErrTimeout ? WKV_ERR_TIMEOUT : WKV_ERR_CUDA;
+}
+
 wkv_status wkv_forward(int B, int T, int C, int kv_dtype, const float* w, const float* u, const void* k,
                        const void* v, float* y, float* ckpt, void* workspace, size_t workspace_bytes,
                        void* stream) {
@@ -541,22 +558,45 @@ wkv_status wkv_backward_gated(int B, int T, int C, int kv_dtype, const float* w,
                        workspace, workspace_bytes, stream);
 }
 
-wkv_status wkv_decode_step(int L, int B, int C, const float* x, const float* x_prev, const float* mu_k,
-                           const float* mu_v, const float* mu_r, const float* r, const float* k, const float* v,
-                           const float* w, const float* u, float* num, float* den, float* pp, float* y, float* xk,
-                           float* xv, float* xr, void* stream) {
+namespace {
+
+// The decode step with fp32 (token_dtype 0) or bf16 (1) token inputs.
+wkv_status decode_impl(int L, int B, int C, int token_dtype, const void* x, const void* x_prev, const float* mu_k,
+                       const float* mu_v, const float* mu_r, const void* r, const void* k, const void* v,
+                       const float* w, const float* u, float* num, float* den, float* pp, float* y, float* xk,
+                       float* xv, float* xr, void* stream, const char* where) {
   clear_error();
   if (L <= 0 || B <= 0 || C <= 0) return WKV_ERR_INVALID_ARG;
   if ((double)L * B * C >= 1099511627776.0) return WKV_ERR_INVALID_ARG;
   if (!x || !x_prev || !mu_k || !mu_v || !mu_r || !r || !k || !v || !w || !u || !num || !den || !pp || !y)
     return WKV_ERR_INVALID_ARG;
   DecodeArgs a{x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u, num, den, pp, y, xk, xv, xr, L, B, C};
-  auto al16 = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  const bool vec4 = (C % 4 == 0) && al16(x) && al16(x_prev) && al16(mu_k) && al16(mu_v) && al16(mu_r) && al16(r) &&
-                    al16(k) && al16(v) && al16(w) && al16(u) && al16(num) && al16(den) && al16(pp) && al16(y) &&
-                    al16(xk) && al16(xv) && al16(xr);
-  cudaError_t e = launch_decode(a, vec4, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_decode_step");
+  auto al = [](const void* p, unsigned m) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & m) == 0; };
+  // four channels per thread: 16-byte accesses of fp32 arrays, 8-byte of bf16 ones
+  const unsigned tm = token_dtype == 0 ? 15u : 7u;
+  const bool vec4 = (C % 4 == 0) && al(x, tm) && al(x_prev, tm) && al(r, tm) && al(k, tm) && al(v, tm) &&
+                    al(mu_k, 15u) && al(mu_v, 15u) && al(mu_r, 15u) && al(w, 15u) && al(u, 15u) && al(num, 15u) &&
+                    al(den, 15u) && al(pp, 15u) && al(y, 15u) && al(xk, 15u) && al(xv, 15u) && al(xr, 15u);
+  cudaError_t e = launch_decode(a, vec4, token_dtype, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WKV_OK : cuda_fail(e, where);
+}
+
+}  // namespace
+
+wkv_status wkv_decode_step(int L, int B, int C, const float* x, const float* x_prev, const float* mu_k,
+                           const float* mu_v, const float* mu_r, const float* r, const float* k, const float* v,
+                           const float* w, const float* u, float* num, float* den, float* pp, float* y, float* xk,
+                           float* xv, float* xr, void* stream) {
+  return decode_impl(L, B, C, 0, x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u, num, den, pp, y, xk, xv, xr, stream,
+                     "wkv_decode_step");
+}
+
+wkv_status wkv_decode_step_bf16(int L, int B, int C, const void* x, const void* x_prev, const float* mu_k,
+                                const float* mu_v, const float* mu_r, const void* r, const void* k, const void* v,
+                                const float* w, const float* u, float* num, float* den, float* pp, float* y,
+                                float* xk, float* xv, float* xr, void* stream) {
+  return decode_impl(L, B, C, 1, x, x_prev, mu_k, mu_v, mu_r, r, k, v, w, u, num, den, pp, y, xk, xv, xr, stream,
+                     "wkv_decode_step_bf16");
 }
 
 size_t wkv_token_shift_backward_workspace_bytes(int B, int T, int C) {

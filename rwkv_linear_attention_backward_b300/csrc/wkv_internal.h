@@ -93,13 +93,22 @@ struct ReduceArgs {
 };
 
 struct DecodeArgs {
-  const float *x, *x_prev, *mu_k, *mu_v, *mu_r, *r, *k, *v, *w, *u;
+  const void *x, *x_prev;           // token inputs [L, B, C]: float or bf16 (the launch's token dtype)
+  const float *mu_k, *mu_v, *mu_r;  // [L, C]
+  const void *r, *k, *v;            // token inputs, as x
+  const float *w, *u;               // [L, C]
   float *num, *den, *pp, *y, *xk, *xv, *xr;
   int L, B, C;
 };
 
 // Sets the text returned by wkv_last_error_string() on this thread.
 void set_last_error(const char* msg);
+
+// Each file's device-wide record of an expired wait on the current device:
+// read and cleared (wkv_sync_status).
+cudaError_t take_error_seq(unsigned int* code);
+cudaError_t take_error_fwd(unsigned int* code);
+cudaError_t take_error_bwd(unsigned int* code);
 
 // Rank-3 TMA descriptor of a [B, T, C] tensor with a {box_c, kChunk, 1} box
 // (elem_bytes 4 = fp32, 2 = bf16).  False when TMA cannot address it (the
@@ -215,7 +224,8 @@ cudaError_t launch_state_fold(const FoldArgs& a, cudaStream_t s);
 cudaError_t launch_forward(FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
 cudaError_t launch_backward(BwdArgs& a, cudaStream_t s);
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s);
-cudaError_t launch_decode(const DecodeArgs& a, bool vec4, cudaStream_t s);
+// token_dtype: 0 fp32 token inputs, 1 bf16.
+cudaError_t launch_decode(const DecodeArgs& a, bool vec4, int token_dtype, cudaStream_t s);
 
 // Row slices of the gw/gu reduction for `rows` partial rows over C channels
 // (a function of the shape only, so the summation order is fixed).

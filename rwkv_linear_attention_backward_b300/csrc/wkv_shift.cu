@@ -79,10 +79,12 @@ __global__ void __launch_bounds__(256) shift_fwd_kernel(const ShiftArgs a) {
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const float x = W::get(cur, i), p = W::get(prev, i);
-      // mu x + (1 - mu) p = p + mu (x - p)
-      W::set(ok, i, fmaf(W::get(mk, i), x - p, p));
-      W::set(ov, i, fmaf(W::get(mv, i), x - p, p));
-      W::set(orr, i, fmaf(W::get(mr, i), x - p, p));
+      // mu x + (1 - mu) x_prev as written in eq. (7): one rounding per
+      // product, where mu (x - x_prev) + x_prev would first round
+      // x - x_prev, a larger error wherever the two terms nearly cancel
+      W::set(ok, i, fmaf(W::get(mk, i), x, (1.f - W::get(mk, i)) * p));
+      W::set(ov, i, fmaf(W::get(mv, i), x, (1.f - W::get(mv, i)) * p));
+      W::set(orr, i, fmaf(W::get(mr, i), x, (1.f - W::get(mr, i)) * p));
     }
     W::store(a.xk + o, ok);
     W::store(a.xv + o, ov);

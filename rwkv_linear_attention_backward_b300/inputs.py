@@ -34,6 +34,8 @@ cmix       channel mixing's pointwise steps (squared ReLU, sigmoid gate)
 decode     RNN decode, L=32 layers, B=256, C=4096, 1024 steps; x, x_prev,
            r, k, v ~ N(0,1); mu_k, mu_v, mu_r ~ U(0,1); d ~ U(-6,2),
            u ~ U(-1,1) per layer; state starts at (0, 0, -1e38)
+decode_bf16 as decode, with x, x_prev, r, k, v rounded to bf16 (state,
+           parameters and outputs fp32)
 =========  ==========================================================
 """
 from __future__ import annotations
@@ -72,6 +74,7 @@ class DecodeWorkload:
     d_lo: float
     d_hi: float
     seed: int
+    token_dtype: str = "f32"  # x, x_prev, r, k, v: "f32" or "bf16" (state and outputs fp32)
 
     @property
     def elements_per_step(self) -> int:
@@ -87,6 +90,8 @@ WORKLOADS = {
     "l169m_gated": TrainingWorkload("l169m_gated", 8, 1024, 768, 3.0, -6.0, 2.0, "f32", True, 1008, gated=True),
 }
 DECODE = DecodeWorkload("decode", 32, 256, 4096, 1024, -6.0, 2.0, 1005)
+DECODE_BF16 = DecodeWorkload("decode_bf16", 32, 256, 4096, 1024, -6.0, 2.0, 1011, token_dtype="bf16")
+DECODES = {"decode": DECODE, "decode_bf16": DECODE_BF16}
 
 
 @dataclass(frozen=True)
@@ -217,16 +222,24 @@ def decode_params(L: int, C: int, *, seed: int, d_lo: float = -6.0, d_hi: float 
     return mu_k, mu_v, mu_r, torch.exp(d), u
 
 
-def decode_step_inputs(L: int, B: int, C: int, *, seed: int, step: int):
+def _token_dtype(ts, token_dtype: str):
+    if token_dtype == "bf16":
+        return tuple(t.to(torch.bfloat16) for t in ts)
+    if token_dtype != "f32":
+        raise ValueError(f"token_dtype must be 'f32' or 'bf16', got {token_dtype!r}")
+    return tuple(ts)
+
+
+def decode_step_inputs(L: int, B: int, C: int, *, seed: int, step: int, token_dtype: str = "f32"):
     """Per-step decode inputs, each [L, B, C]: (x, x_prev, r, k, v) ~ N(0,1).
 
     Each step index has its own generator (seed * 1_000_003 + step), so any
     step can be drawn without drawing the ones before it.  Draw order: x,
-    x_prev, r, k, v.
+    x_prev, r, k, v.  ``token_dtype="bf16"``: drawn in fp32, then rounded.
     """
     g = _gen(int(seed) * 1_000_003 + int(step))
     shape = (L, B, C)
-    return tuple(torch.randn(shape, generator=g, dtype=torch.float32) for _ in range(5))
+    return _token_dtype([torch.randn(shape, generator=g, dtype=torch.float32) for _ in range(5)], token_dtype)
 
 
 def initial_state(L: int, B: int, C: int):
@@ -235,13 +248,14 @@ def initial_state(L: int, B: int, C: int):
     return z.clone(), z.clone(), torch.full((L, B, C), -1e38, dtype=torch.float32)
 
 
-def decode_pool(L: int, B: int, C: int, *, seed: int, n_sets: int, device="cpu"):
+def decode_pool(L: int, B: int, C: int, *, seed: int, n_sets: int, device="cpu", token_dtype: str = "f32"):
     """A pool of ``n_sets`` per-step decode input sets (x, x_prev, r, k, v),
     each [L, B, C] ~ N(0,1), drawn directly on ``device`` from one generator
-    seeded with ``seed`` (set after set, in that order within a set).  A run
-    of more steps than sets uses set ``step % n_sets`` at each step."""
+    seeded with ``seed`` (set after set, in that order within a set; bf16:
+    each set drawn in fp32, then rounded).  A run of more steps than sets
+    uses set ``step % n_sets`` at each step."""
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     shape = (L, B, C)
-    return [tuple(torch.randn(shape, generator=g, dtype=torch.float32, device=device) for _ in range(5))
-            for _ in range(n_sets)]
+    return [_token_dtype([torch.randn(shape, generator=g, dtype=torch.float32, device=device) for _ in range(5)],
+                         token_dtype) for _ in range(n_sets)]
