@@ -621,4 +621,7 @@ cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// The device-wide error record of this file's kernels (wkv_sync_status).
+cudaError_t take_error_bwd(unsigned int* code) { return take_module_error(code); }
+
 }  // namespace wkv

@@ -186,11 +186,33 @@ __host__ __device__ __forceinline__ uint32_t tag_of(unsigned long long epoch) {
   return (uint32_t)((epoch - 1) % 0xFFFFFFFFull) + 1u;  // never 0: the tag of a zero-filled workspace
 }
 
-// Records that this launch (epoch) gave up: the code for the host, the epoch
-// so the launch's other waits stop at once.
+// The first device error code of any launch of this compilation unit's
+// kernels on a device since the host last took it (take_module_error):
+// what wkv_sync_status reports, whatever workspace the launch used.  One
+// copy per compilation unit (each .cu file is its own device module), zero
+// when the library loads.
+static __device__ unsigned int g_module_error;
+
+// Records that this launch (epoch) gave up: the code for the host (in the
+// workspace, and device-wide for wkv_sync_status), the epoch so the
+// launch's other waits stop at once.
 __device__ __forceinline__ void record_error(WsHeader* h, unsigned int code, uint64_t epoch) {
   atomicCAS(&h->error, 0u, code);
+  atomicCAS(&g_module_error, 0u, code);
   atomicExch(&h->abort, (unsigned long long)epoch);
+}
+
+// Host side: reads this compilation unit's g_module_error on the current
+// device into *code and clears it when set.  Synchronous.
+static inline cudaError_t take_module_error(unsigned int* code) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_module_error, sizeof(v));
+  if (e == cudaSuccess && v != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_module_error, &zero, sizeof(zero));
+  }
+  *code = v;
+  return e;
 }
 
 }  // namespace wkv
@@ -199,16 +221,32 @@ namespace wkv {
 
 // ------------------------------------------------------ tagged records
 // Chunk results pass between warps of different CTAs as 16-byte records, one
-// per channel: three values and the launch tag, read and written as single
-// 128-bit accesses (single-copy atomic), so a reader that sees its launch's
-// tag sees the values written with it: no fence and no separate flag is
-// needed.  The tag is derived from the launch epoch and is never 0 (the tag
-// of a zero-filled workspace); epochs increase from launch to launch on a
-// workspace, so records left by earlier launches never read as current.
+// per channel: three values and a check word, written and read as 128-bit
+// accesses with no fence and no separate flag.  The check word is the
+// launch tag mixed with the bits of the three values (rec_check), so a
+// reader accepts a record only when the values it holds are the ones the
+// current launch wrote with that word.  A read that saw part of a record
+// from one write and part from another (an older launch's record, the
+// zero-filled workspace, or a write not yet complete) fails the check and is
+// read again, so correctness does not rest on 128-bit accesses being
+// indivisible: should one be split, the pieces would not match (a random
+// match has probability 2^-31).  Tags come from the launch epoch and are
+// never 0; epochs increase from launch to launch on a workspace, so records
+// left by earlier launches never pass as current.
 struct Rec {
   unsigned long long lo;  // value 0 | value 1 << 32
-  unsigned long long hi;  // value 2 | tag << 32
+  unsigned long long hi;  // value 2 | check << 32
 };
+
+// The check word of a record: tag and value bits through a multiplicative
+// mix; odd, so never the 0 of a zero-filled workspace.
+__device__ __forceinline__ uint32_t rec_check(uint32_t tag, uint32_t x, uint32_t y, uint32_t z) {
+  uint32_t h = tag * 0x9E3779B1u;
+  h = (h ^ x) * 0x85EBCA77u;
+  h = (h ^ (h >> 15) ^ y) * 0xC2B2AE3Du;
+  h = (h ^ (h >> 13) ^ z) * 0x27D4EB2Fu;
+  return (h ^ (h >> 16)) | 1u;
+}
 
 __device__ __forceinline__ Rec rec_load(const Rec* p) {
   Rec r;
@@ -223,8 +261,9 @@ __device__ __forceinline__ Rec rec_load(const Rec* p) {
 }
 
 __device__ __forceinline__ void rec_store(Rec* p, uint32_t tag, float x, float y, float z) {
-  const unsigned long long lo = ((unsigned long long)__float_as_uint(y) << 32) | __float_as_uint(x);
-  const unsigned long long hi = ((unsigned long long)tag << 32) | __float_as_uint(z);
+  const uint32_t bx = __float_as_uint(x), by = __float_as_uint(y), bz = __float_as_uint(z);
+  const unsigned long long lo = ((unsigned long long)by << 32) | bx;
+  const unsigned long long hi = ((unsigned long long)rec_check(tag, bx, by, bz) << 32) | bz;
   asm volatile(
       "{\n\t.reg .b128 t;\n\t"
       "mov.b128 t, {%0, %1};\n\t"
@@ -233,7 +272,9 @@ __device__ __forceinline__ void rec_store(Rec* p, uint32_t tag, float x, float y
       : "memory");
 }
 
-__device__ __forceinline__ bool rec_ok(const Rec& r, uint32_t tag) { return (uint32_t)(r.hi >> 32) == tag; }
+__device__ __forceinline__ bool rec_ok(const Rec& r, uint32_t tag) {
+  return (uint32_t)(r.hi >> 32) == rec_check(tag, (uint32_t)r.lo, (uint32_t)(r.lo >> 32), (uint32_t)r.hi);
+}
 __device__ __forceinline__ float rec_x(const Rec& r) { return __uint_as_float((uint32_t)r.lo); }
 __device__ __forceinline__ float rec_y(const Rec& r) { return __uint_as_float((uint32_t)(r.lo >> 32)); }
 __device__ __forceinline__ float rec_z(const Rec& r) { return __uint_as_float((uint32_t)r.hi); }

@@ -499,4 +499,7 @@ cudaError_t launch_forward(FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t 
   return write_y ? launch_fwd_t<__nv_bfloat16, true>(a, s) : launch_fwd_t<__nv_bfloat16, false>(a, s);
 }
 
+// The device-wide error record of this file's kernels (wkv_sync_status).
+cudaError_t take_error_fwd(unsigned int* code) { return take_module_error(code); }
+
 }  // namespace wkv

@@ -1297,4 +1297,7 @@ cudaError_t launch_seq_backward(SeqBwdArgs& a, int kv_dtype, cudaStream_t s) {
   return kv_dtype == 0 ? launch_seq_bwd_t<float, false>(a, s) : launch_seq_bwd_t<__nv_bfloat16, false>(a, s);
 }
 
+// The device-wide error record of this file's kernels (wkv_sync_status).
+cudaError_t take_error_seq(unsigned int* code) { return take_module_error(code); }
+
 }  // namespace wkv

@@ -30,11 +30,29 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(wkv_[a-z0-9_]+)\s*\(", text)))
 
 
+# The boundary's calls: the forward and backward passes, the decode step, the
+# workspace size queries, the status text and the expired-wait report; plus
+# what this library adds around them.
+BOUNDARY = ("wkv_status_string", "wkv_forward_workspace_bytes", "wkv_backward_workspace_bytes", "wkv_forward",
+            "wkv_backward", "wkv_decode_step", "wkv_last_error_string", "wkv_sync_status")
+ADDED = ("wkv_checkpoint_floats", "wkv_workspace_init", "wkv_workspace_check", "wkv_forward_with_state",
+         "wkv_backward_with_state", "wkv_forward_gated", "wkv_backward_gated", "wkv_state_fold", "wkv_token_shift",
+         "wkv_token_shift_backward", "wkv_channel_mix_sqrelu", "wkv_channel_mix_gate", "wkv_forward_noalloc")
+
+
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("wkv_forward", "wkv_backward", "wkv_decode_step", "wkv_forward_workspace_bytes",
-              "wkv_backward_workspace_bytes", "wkv_checkpoint_floats", "wkv_workspace_check"):
-        assert n in names
+    for n in BOUNDARY + ADDED:
+        assert n in names, n
+
+
+def test_sync_status_without_work(lib):
+    """No launch has recorded anything: wkv_sync_status of the default
+    stream is WKV_OK (where no device exists it reports the CUDA error)."""
+    import torch
+
+    st = lib.wkv_sync_status(None)
+    assert st == (0 if torch.cuda.is_available() else 5)
 
 
 def test_every_declared_symbol_is_exported(lib):
