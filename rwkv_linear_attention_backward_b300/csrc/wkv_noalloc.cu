@@ -64,9 +64,16 @@ wkv_status scratch_address(void** out) {
 extern "C" wkv_status wkv_forward_noalloc(int B, int T, int C, int kv_dtype, const float* w, const float* u,
                                           const void* k, const void* v, float* y, float* ckpt, void* stream) {
   using namespace wkv;
-  if (!w || !u || !k || !v || !y || B <= 0 || T <= 0 || C <= 0) return WKV_ERR_INVALID_ARG;
+  set_last_error("");  // a rejection below must not leave an earlier call's message in place
+  if (!w || !u || !k || !v || !y || B <= 0 || T <= 0 || C <= 0) {
+    set_last_error("wkv_forward_noalloc: a required pointer is null or a size is not positive");
+    return WKV_ERR_INVALID_ARG;
+  }
   const size_t need = wkv_forward_workspace_bytes(B, T, C);
-  if (need == 0) return WKV_ERR_INVALID_ARG;
+  if (need == 0) {
+    set_last_error("wkv_forward_noalloc: B * T * C is beyond the sizes the library takes");
+    return WKV_ERR_INVALID_ARG;
+  }
   if (need > kNoAllocScratchBytes) {
     char msg[200];
     std::snprintf(msg, sizeof(msg),
