@@ -7,10 +7,13 @@ Prints ONE JSON line on rank 0.  A step is one pass of the training hot path
 over one batch of seeded synthetic input already resident in HBM: the
 forward call (which also writes the chunk checkpoints) followed by the
 backward call (gradients of w, u, k, v), for the named workload (default
-``l169m``: B=8, T=1024, C=768, fp32, one layer of a 169M RWKV-4).  Other
-workloads: ``tiny``, ``l1b5`` (B=16 T=4096 C=2048), ``long`` (forward only,
-bf16 k/v, B=1 T=131072 C=2560) and ``decode`` (one fused decode step of
-L=32 layers, B=256, C=4096, state carried across steps).
+``l1b5``: B=16, T=4096, C=2048, fp32, one layer of a 1.5B-class model, the
+largest forward+backward shape).  Other workloads: ``tiny``, ``l169m``
+(B=8 T=1024 C=768, one layer of a 169M RWKV-4), ``long`` (forward only,
+bf16 k/v, B=1 T=131072 C=2560), ``decode`` / ``decode_bf16`` (one fused
+decode step of L=32 layers, B=256, C=4096, fp32 / bf16 token inputs, state
+carried across steps), and the pointwise neighbours ``shift``, ``cmix``,
+``l169m_bf16``, ``l169m_gated``.
 
 Timing: W untimed warm-up steps; then the forward and the backward call are
 captured once as CUDA graphs (as a training loop would run them; ``--no-graph``
@@ -56,6 +59,7 @@ BYTES_FWD_BF16 = 8   # read bf16 k, v; write fp32 y
 BYTES_BWD = 20       # read k, v, gy; write gk, gv
 BYTES_BWD_BF16 = 14  # read bf16 k, v, gy; write fp32 gk, gv
 BYTES_DECODE = 60    # read x, x_prev, r, k, v; read+write num, den, pp; write y, xk, xv, xr
+BYTES_DECODE_BF16 = 50  # the same with bf16 x, x_prev, r, k, v
 BYTES_SHIFT_FWD = 16  # read x; write xk, xv, xr
 BYTES_SHIFT_BWD = 20  # read x, gxk, gxv, gxr; write gx
 BYTES_SQRELU_FWD = 8    # read k; write max(k, 0)^2                 (per hidden element)
@@ -73,8 +77,9 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default depends on the workload)")
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="l169m", choices=["tiny", "l169m", "l1b5", "long", "l169m_bf16",
-                                                              "l169m_gated", "decode", "shift", "cmix"])
+    ap.add_argument("--workload", default="l1b5", choices=["tiny", "l169m", "l1b5", "long", "l169m_bf16",
+                                                             "l169m_gated", "decode", "decode_bf16", "shift",
+                                                             "cmix"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -89,7 +94,8 @@ def parse_args(argv=None):
 
 
 DEFAULT_STEPS = {"tiny": 2000, "l169m": 4000, "l1b5": 200, "long": 200, "l169m_bf16": 4000, "l169m_gated": 4000,
-                 "decode": 256, "shift": 200, "cmix": 1000}
+                 "decode": 256, "decode_bf16": 256, "shift": 200, "cmix": 1000}
+DECODE_WORKLOADS = ("decode", "decode_bf16")
 
 
 # ------------------------------------------------------------------ ranks
@@ -245,10 +251,26 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- helpers
-def kernel_source_hash() -> str:
+# The source files each kernel is compiled from (its .cu file and the
+# headers that file includes): a traffic record stays valid while these are
+# unchanged.
+_HEADERS = ("wkv_common.cuh", "wkv_internal.h")
+KERNEL_FILES = {
+    "seq_": ("wkv_seq.cu", "wkv_adjoint.cuh", "wkv_pipe.cuh") + _HEADERS,
+    "decode_kernel": ("wkv_decode.cu",) + _HEADERS,
+    "shift_": ("wkv_shift.cu",) + _HEADERS,
+    "cmix_kernel": ("wkv_cmix.cu",) + _HEADERS,
+}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """Hash of the sources of `kernel` (by its name's prefix), or of every
+    file under csrc/ when the kernel is None or unlisted."""
     h = hashlib.sha256()
     csrc = ROOT / "rwkv_linear_attention_backward_b300" / "csrc"
-    for p in sorted(csrc.glob("*")):
+    files = next((f for pre, f in KERNEL_FILES.items() if kernel and kernel.startswith(pre)), None)
+    paths = sorted(csrc.glob("*")) if files is None else [csrc / n for n in sorted(files)]
+    for p in paths:
         h.update(p.name.encode())
         h.update(p.read_bytes())
     return h.hexdigest()[:16]
@@ -264,7 +286,7 @@ def ncu_traffic(kernel: str, workload: str):
         rec = json.loads(f.read_text()).get(f"{kernel}@{workload}")
     except ValueError:
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if not rec or rec.get("source_hash") != kernel_source_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -393,24 +415,24 @@ class TrainingRun:
 
 
 class DecodeRun:
-    def __init__(self, device):
+    def __init__(self, device, name="decode"):
         import torch
         from rwkv_linear_attention_backward_b300 import binding, inputs
 
         self.torch, self.wkv = torch, binding
-        D = inputs.DECODE
+        D = inputs.DECODES[name]
         self.D = D
         L, B, C = D.L, D.B, D.C
         self.elements = D.elements_per_step
         self.params = tuple(t.to(device) for t in inputs.decode_params(L, C, seed=D.seed, d_lo=D.d_lo, d_hi=D.d_hi))
-        self.pool = inputs.decode_pool(L, B, C, seed=D.seed, n_sets=16, device=device)
+        self.pool = inputs.decode_pool(L, B, C, seed=D.seed, n_sets=16, device=device, token_dtype=D.token_dtype)
         self.state = tuple(t.to(device) for t in inputs.initial_state(L, B, C))
         self.out = tuple(torch.empty(L, B, C, device=device) for _ in range(4))
         self.t = 0
-        self.bytes_fwd = BYTES_DECODE * self.elements
+        self.bytes_fwd = (BYTES_DECODE_BF16 if D.token_dtype == "bf16" else BYTES_DECODE) * self.elements
         self.bytes_bwd = 0
         self.launches_per_step = 1
-        self.dominant = "decode_kernel_vec4"
+        self.dominant = "decode_kernel_vec4<__nv_bfloat16>" if D.token_dtype == "bf16" else "decode_kernel_vec4<float>"
         self.dominant_bytes = self.bytes_fwd
 
     def step(self, ev=None):
@@ -613,12 +635,13 @@ def cpu_baseline(workload: str, target_s: float = 12.0):
     from rwkv_linear_attention_backward_b300 import inputs
 
     o = oracle.load()
-    if workload == "decode":
-        D = inputs.DECODE
+    if workload in DECODE_WORKLOADS:
+        D = inputs.DECODES[workload]
         L, B, C = D.L, D.B, D.C
         params = [p.numpy() for p in inputs.decode_params(L, C, seed=D.seed, d_lo=D.d_lo, d_hi=D.d_hi)]
         rows = 16
-        x, xp, r, k, v = (t.numpy()[:, :rows] for t in inputs.decode_step_inputs(L, B, C, seed=D.seed, step=0))
+        x, xp, r, k, v = (t.float().numpy()[:, :rows] for t in
+                          inputs.decode_step_inputs(L, B, C, seed=D.seed, step=0, token_dtype=D.token_dtype))
         st = [t.numpy()[:, :rows] for t in inputs.initial_state(L, B, C)]
         done, t0, steps = 0, time.perf_counter(), 0
         while time.perf_counter() - t0 < target_s:
@@ -743,8 +766,8 @@ def run_ours(args):
 
         binding.set_scan_mode(args.scan_mode)
     steps = args.steps or DEFAULT_STEPS[args.workload]
-    if args.workload == "decode":
-        run = DecodeRun(device)
+    if args.workload in DECODE_WORKLOADS:
+        run = DecodeRun(device, args.workload)
     elif args.workload == "shift":
         run = ShiftRun(device)
     elif args.workload == "cmix":
@@ -790,8 +813,9 @@ def run_ours(args):
     dom_avg = sum(dom_s) / len(dom_s)
     achieved = run.dominant_bytes / dom_avg / 1e9
     step_bytes = run.bytes_fwd + run.bytes_bwd
-    if args.workload == "decode":
-        wl_cfg = {"workload": "decode", "L": run.D.L, "B": run.D.B, "C": run.D.C, "state": "fp32"}
+    if args.workload in DECODE_WORKLOADS:
+        wl_cfg = {"workload": args.workload, "L": run.D.L, "B": run.D.B, "C": run.D.C,
+                  "token_inputs": run.D.token_dtype, "state": "fp32"}
     elif args.workload == "shift":
         wl_cfg = {"workload": "shift", "B": run.S.B, "T": run.S.T, "C": run.S.C, "pass": "forward+backward"}
     elif args.workload == "cmix":
@@ -802,14 +826,16 @@ def run_ours(args):
                   "kv_dtype": run.wl.kv_dtype, "pass": "forward+backward" if run.wl.backward else "forward"}
         if run.wl.gated:
             wl_cfg["output"] = "sigmoid(r) * wkv, the gate fused into the forward and backward kernels"
-    wl_cfg.update({"launch": "api calls per step" if (args.no_graph or args.workload in ("decode", "shift", "cmix")) else
+    pointwise = DECODE_WORKLOADS + ("shift", "cmix")
+    wl_cfg.update({"launch": "api calls per step" if (args.no_graph or args.workload in pointwise) else
                    "CUDA graphs of the forward and backward calls, captured once and replayed per step",
                    "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}",
                    "scan_mode": args.scan_mode,
                    "strategy": getattr(run, "strategy", "n/a"),
                    "checkpoints": "forward writes chunk checkpoints, backward reads them"
-                   if args.workload not in ("decode", "shift", "cmix") else "n/a"})
-    metric = {"long": METRIC_FWD, "decode": METRIC_DEC, "shift": METRIC_SHIFT, "cmix": METRIC_CMIX,
+                   if args.workload not in pointwise else "n/a"})
+    metric = {"long": METRIC_FWD, "decode": METRIC_DEC, "decode_bf16": METRIC_DEC, "shift": METRIC_SHIFT,
+              "cmix": METRIC_CMIX,
               "l169m_gated": METRIC_GATED}.get(args.workload, METRIC)
     out = {
         "metric": metric,
@@ -890,11 +916,12 @@ def run_reference(args):
     total_budget = 120.0  # seconds for warm-up + timed steps together
     per_step = total_budget / (steps + args.warmup)
     o = oracle.load()
-    if args.workload == "decode":
-        D = inputs.DECODE
+    if args.workload in DECODE_WORKLOADS:
+        D = inputs.DECODES[args.workload]
         L, B, C = D.L, D.B, D.C
         params = [p.numpy() for p in inputs.decode_params(L, C, seed=D.seed, d_lo=D.d_lo, d_hi=D.d_hi)]
-        x, xp, r, k, v = (t.numpy() for t in inputs.decode_step_inputs(L, B, C, seed=D.seed, step=0))
+        x, xp, r, k, v = (t.float().numpy() for t in
+                          inputs.decode_step_inputs(L, B, C, seed=D.seed, step=0, token_dtype=D.token_dtype))
         t0 = time.perf_counter()
         o.decode_step(x[:, :1], xp[:, :1], *params[:3], r[:, :1], k[:, :1], v[:, :1], *params[3:],
                       *[t.numpy()[:, :1] for t in inputs.initial_state(L, 1, C)])
@@ -955,7 +982,7 @@ def run_reference(args):
     done = sum(one() for _ in range(steps))
     el = time.perf_counter() - t0
     value = done / el
-    if args.workload == "decode":
+    if args.workload in DECODE_WORKLOADS:
         cfg = {"workload": args.workload}
     elif args.workload == "shift":
         cfg = {"workload": "shift", "B": inputs.SHIFT.B, "T": inputs.SHIFT.T, "C": inputs.SHIFT.C}

@@ -15,13 +15,13 @@ import bench  # noqa: E402
 
 def test_arguments():
     a = bench.parse_args([])
-    assert (a.gpus, a.workload, a.impl, a.scan_mode) == (1, "l169m", "ours", "auto")
+    assert (a.gpus, a.workload, a.impl, a.scan_mode) == (1, "l1b5", "ours", "auto")
     assert a.warmup >= 3
     with pytest.raises(SystemExit):
         bench.parse_args(["--warmup", "2"])
     with pytest.raises(SystemExit):
         bench.parse_args(["--workload", "nope"])
-    for w in ("tiny", "l169m", "l1b5", "long", "l169m_bf16", "l169m_gated", "decode", "shift", "cmix"):
+    for w in ("tiny", "l169m", "l1b5", "long", "l169m_bf16", "l169m_gated", "decode", "decode_bf16", "shift", "cmix"):
         assert bench.parse_args(["--workload", w]).workload == w
         assert w in bench.DEFAULT_STEPS
 
@@ -36,10 +36,10 @@ def test_traffic_record_follows_the_sources(tmp_path, monkeypatch):
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", tmp_path)
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc")
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel=None: "abc")
     assert bench.ncu_traffic("seq_bwd_kernel", "l169m") == 123
     assert bench.ncu_traffic("seq_fwd_kernel", "l169m") is None
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "changed")
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel=None: "changed")
     assert bench.ncu_traffic("seq_bwd_kernel", "l169m") is None
     (tmp_path / "profiles" / "ncu_traffic.json").unlink()
     assert bench.ncu_traffic("seq_bwd_kernel", "l169m") is None
@@ -48,6 +48,13 @@ def test_traffic_record_follows_the_sources(tmp_path, monkeypatch):
 def test_source_hash_covers_the_kernel_sources():
     h = bench.kernel_source_hash()
     assert len(h) == 16 and h == bench.kernel_source_hash()
+    # a kernel's hash covers its own files only: every listed file exists,
+    # and the sequential and decode kernels hash differently
+    csrc = bench.ROOT / "rwkv_linear_attention_backward_b300" / "csrc"
+    for files in bench.KERNEL_FILES.values():
+        assert all((csrc / f).exists() for f in files)
+    assert bench.kernel_source_hash("seq_bwd_kernel") == bench.kernel_source_hash("seq_fwd_kernel")
+    assert bench.kernel_source_hash("seq_bwd_kernel") != bench.kernel_source_hash("decode_kernel_vec4<float>")
 
 
 def _sampler(samples, reasons, max_mhz=2032.0):
