@@ -168,7 +168,7 @@ __device__ __forceinline__ void bwd_finish(const BwdArgs& a, const float* __rest
         const float gk = fmaf(fmaf(la, vv, lb), ek, cur);
         const float gv = fmaf(gi, ec, la * ek);
         gu_acc += cur;
-        gw_acc = fmaf(la, A[i], fmaf(lb, Bd[i], gw_acc));
+        gw_acc += fmaf(la, A[i], lb * Bd[i]);  // the two nearly cancelling terms first
         la = fmaf(la, p.ew, gi);
         lb = fmaf(lb, p.ew, -gi * (vv - vmy));
         if (valid) {

@@ -738,7 +738,6 @@ __device__ __forceinline__ void seq_bwd_chunk(const KV* __restrict__ sk, const K
     const float f = has_succ ? exp_nat(F - X.f) : 0.f;
     const float xla = X.la * f, xlb = X.lb * f;
     float la0 = 0.f, lb0 = 0.f, pw = 1.f;
-    float gwb = 0.f;  // gw's lb share: a second chain beside gw_acc's la share
     if constexpr (FULL) {
       // the per-token terms that need no adjoint, for the whole chunk first
       // (independent work), then the reverse sweep's chains
@@ -767,8 +766,10 @@ __device__ __forceinline__ void seq_bwd_chunk(const KV* __restrict__ sk, const K
         const float gk = fmaf(fmaf(la, vv, lb), ek, cur);
         const float gv = fmaf(gi, ec, la * ek);
         gu_acc += cur;
-        gw_acc = fmaf(la, A[i], gw_acc);
-        gwb = fmaf(lb, Bd[i], gwb);
+        // the token's two terms first: they nearly cancel (lb ~ -la wkv), so
+        // summing each over the chunk apart would round at ~32 times the size
+        // of what is left after the cancellation
+        gw_acc += fmaf(la, A[i], lb * Bd[i]);
         la0 = fmaf(la0, cw.ew, gi);
         lb0 = fmaf(lb0, cw.ew, -gi * (vv - VM[i]));
         pw *= cw.ew;
@@ -794,8 +795,10 @@ __device__ __forceinline__ void seq_bwd_chunk(const KV* __restrict__ sk, const K
         const float gk = fmaf(fmaf(la, vv, lb), ek, cur);
         const float gv = fmaf(gi, ec, la * ek);
         gu_acc += cur;
-        gw_acc = fmaf(la, A[i], gw_acc);
-        gwb = fmaf(lb, Bd[i], gwb);
+        // the token's two terms first: they nearly cancel (lb ~ -la wkv), so
+        // summing each over the chunk apart would round at ~32 times the size
+        // of what is left after the cancellation
+        gw_acc += fmaf(la, A[i], lb * Bd[i]);
         la0 = fmaf(la0, cw.ew, gi);
         lb0 = fmaf(lb0, cw.ew, -gi * (vv - vmy));
         pw *= cw.ew;
@@ -806,7 +809,7 @@ __device__ __forceinline__ void seq_bwd_chunk(const KV* __restrict__ sk, const K
         }
       }
     }
-    gw_acc = -cw.ew * (gw_acc + gwb);
+    gw_acc = -cw.ew * gw_acc;
     // the adjoint at the chunk start, at the scale of P (the record form)
     const Adj A0{la0 * s0, lb0 * s0, P.pp};
     X = has_succ ? fold_adj(A0, (float)n * cw.w, X) : A0;
