@@ -290,3 +290,34 @@ def cmix_gate_backward(r, vk, gout):
     s = _sigmoid(_f32(r))
     g = _f32(gout)
     return (g * _f32(vk) * s * (F32(1) - s)).astype(F32), (g * s).astype(F32)
+
+
+# ----------------------------------------------------------- perturbations
+def perturbed(arrays, seed: int):
+    """The float inputs moved by one unit in the last place of float32, up or
+    down at random per element (other arguments unchanged).  A float32
+    evaluation on these is as valid as one on the exact inputs: the inputs of
+    an fp32 pipeline carry that much rounding from upstream, and a kernel
+    rounds its intermediates as much.  The spread of the results measures how
+    sensitive each output is to fp32 rounding (see ``evaluations``)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for a in arrays:
+        if a is None or isinstance(a, (int, float, str)):
+            out.append(a)
+            continue
+        if isinstance(a, tuple):
+            out.append(tuple(perturbed(list(a), int(rng.integers(1 << 30)))))
+            continue
+        x = _f32(a)
+        up = rng.random(x.shape) < 0.5
+        out.append(np.where(up, np.nextafter(x, np.float32(np.inf)), np.nextafter(x, np.float32(-np.inf))))
+    return out
+
+
+def evaluations(fn, *args, n: int = 2):
+    """fn(*args) and fn on ``n`` one-ulp perturbations of the float inputs:
+    float32 evaluations of the same quantity, whose worst error against the
+    oracle is the floor the parity gate uses for gradients."""
+    return [fn(*args)] + [fn(*perturbed(list(args), 1000 + i)) for i in range(n)]
+

@@ -15,6 +15,15 @@ with r = want (the float64 oracle unless stated) and tau = 1e-3 max|r|:
    (``tests/fp32_emulation.py``: the plain recurrence, nothing rescaled or
    compensated) against the oracle, on the same inputs.
 
+For gradients ``emu`` is a list of float32 evaluations: one on the
+exact inputs and two on inputs moved by one ulp at random
+(``fp32_emulation.evaluations``), and f_i is the worst of their errors.
+One evaluation is a single sample of the fp32 rounding at an
+ill-conditioned output: on the gated stress input, gw of one channel
+(2.8e-3 of the largest) came out of two equally valid float32 evaluations
+with errors 3.9e-5 and 1.1e-4, which differ only in the float32 sigmoid
+that rounded the output gradient.
+
 Gate 2 without a float32 evaluation (``emu`` not given) is plain
 e_i <= tol.  Why the floor: an output that is near zero only by
 cancellation (a weighted average of O(1) values that happens to be small)
@@ -92,7 +101,8 @@ def rel_err(got, want) -> float:
 
 def assert_close(got, want, tol, what="", emu=None, ref=None, pair=False):
     """Both gates (module docstring).  ``emu``: the float32 evaluation of
-    ``want``'s quantity; ``ref``: the float64 value it is measured against
+    ``want``'s quantity (or a list of such evaluations: the worst error
+    counts); ``ref``: the float64 value it is measured against
     (default ``want``); ``pair``: got and want are both GPU results."""
     e, el = errors(got, want)
     g, r = to_np(got), to_np(want)
@@ -103,12 +113,14 @@ def assert_close(got, want, tol, what="", emu=None, ref=None, pair=False):
     eg = _elem(g, r, _scale(r))
     bound = tol
     if emu is not None:
-        m = to_np(emu)
         o = r if ref is None else to_np(ref)
-        assert m.shape == o.shape == r.shape, f"{what}: emulation shape {m.shape} vs {r.shape}"
-        assert np.all(np.isfinite(m)), f"{what}: the float32 evaluation left float32's range"
         so = _scale(o)
-        fe = _elem(m, o, so)
+        fe = None
+        for m in (emu if isinstance(emu, list) else [emu]):  # several evaluations: the worst error
+            m = to_np(m)
+            assert m.shape == o.shape == r.shape, f"{what}: emulation shape {m.shape} vs {r.shape}"
+            assert np.all(np.isfinite(m)), f"{what}: the float32 evaluation left float32's range"
+            fe = _elem(m, o, so) if fe is None else np.maximum(fe, _elem(m, o, so))
         k = K_EMU * (2.0 if pair else 1.0)
         bound = max(tol, k * float(fe.max()))
         entry["emu_elem"] = float(fe.max())

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import fp32_emulation as emu
-from checks import check_pair_grads
+from checks import check_pair_grads, grad_evaluations
 from parity import TOL_BF16, TOL_GRAD, TOL_Y, assert_close, cuda, to_np
 from rwkv_linear_attention_backward_b300 import inputs
 
@@ -51,9 +51,9 @@ def _check_out(oracle, w, u, k, v, r, out, what, tol=TOL_Y):
 def _check_grads(oracle, w, u, k, v, r, gout, got, what):
     """``got``: the GPU's (gw, gu, gk, gv, gr)."""
     o = oracle.backward_gated(w, u, k, v, r, gout)
-    e = emu.backward_gated(w, u, k, v, r, gout)
-    for g, oo, ee, n in zip(got, o, e, GATED):
-        assert_close(g, oo, TOL_GRAD, f"{what} {n}", emu=ee)
+    e = grad_evaluations(emu.backward_gated, w, u, k, v, r, gout, names=GATED)
+    for g, oo, n in zip(got, o, GATED):
+        assert_close(g, oo, TOL_GRAD, f"{what} {n}", emu=e[n])
 
 
 def _check(oracle, wkv, w, u, k, v, r, gout, what, tol_out=TOL_Y, use_ckpt=True):

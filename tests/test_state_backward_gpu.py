@@ -54,7 +54,9 @@ def test_backward_with_state_vs_oracle(oracle, wkv, scan_mode, B, P, T, C):
     ge = gend.double().numpy()
     aend = (ge[0] * np.exp(-ge[2]), ge[1] * np.exp(-ge[2]))
     ow, ou, ok, ov, (ga, gb) = oracle.backward_state(w, u, ks, vs, gs, sin64, aend)
-    eo = emu.backward(w, u, ks, vs, gs, state_in=sin64, adj_end=aend)
+    evs = emu.evaluations(lambda *x: emu.backward(*x[:5], state_in=x[5], adj_end=x[6]), w, u, ks, vs, gs, sin64,
+                          aend)
+    eo = {n: [e[n] for e in evs] for n in evs[0]}
     for use_ckpt in (True, False):
         gw, gu, gk, gv, gin = wkv.backward_with_state(wc, uc, kc, vc, gc, sc, gend.cuda(),
                                                       ckpt=ckpt if use_ckpt else None)
@@ -65,8 +67,8 @@ def test_backward_with_state_vs_oracle(oracle, wkv, scan_mode, B, P, T, C):
         gi = to_np(gin)
         assert np.array_equal(gi[2], sin64[2]), f"{what}: pp plane of the start-state gradient"
         sp = np.exp(sin64[2])
-        assert_close(gi[0], ga * sp, TOL_GRAD, f"{what} g_num of the start state", emu=eo["ga"] * sp)
-        assert_close(gi[1], gb * sp, TOL_GRAD, f"{what} g_den of the start state", emu=eo["gb"] * sp)
+        assert_close(gi[0], ga * sp, TOL_GRAD, f"{what} g_num of the start state", emu=[x * sp for x in eo["ga"]])
+        assert_close(gi[1], gb * sp, TOL_GRAD, f"{what} g_den of the start state", emu=[x * sp for x in eo["gb"]])
 
 
 def test_without_states_is_plain_backward(wkv, scan_mode):
