@@ -51,7 +51,9 @@ struct Adj {
 // forward states are running maxima), so one exponential of a non-positive
 // number.
 __device__ __forceinline__ Adj fold_adj(const Adj& A, float Lw, const Adj& X) {
-  const float e = exp_nat((A.f - Lw) - X.f);
+  // __fsub_rn: never fused with the multiply that formed Lw (same roundings
+  // in every kernel; see combine)
+  const float e = exp_nat(__fsub_rn(A.f, Lw) - X.f);
   return Adj{fmaf(e, X.la, A.la), fmaf(e, X.lb, A.lb), A.f};
 }
 

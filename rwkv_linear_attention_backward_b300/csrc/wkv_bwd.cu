@@ -514,6 +514,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2) bwd_scan_kernel(const __grid_
 __global__ void __launch_bounds__(256) reduce_kernel(const ReduceArgs a) {
   __shared__ float sw[8][32], su[8][32];
   __shared__ bool last;
+  // launched as a dependent of the backward scan: wait until the scan has
+  // completed and its writes (the partial rows, the sequence number) are
+  // visible; a no-op when launched without that dependency
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
   const int grp = blockIdx.x, sl = blockIdx.y;
   const int c = grp * 32 + lane;
@@ -616,9 +620,22 @@ cudaError_t launch_backward(BwdArgs& a, cudaStream_t s) {
   return launch_cooperative(bwd_scan_kernel, nblk, smem, s, a);
 }
 
+// The reduction is a programmatic dependent of the backward scan launched
+// just before it on the stream: it may be scheduled while the scan's last
+// CTAs finish (the scan signals griddepcontrol.launch_dependents at its
+// start), and its griddepcontrol.wait holds it until the scan is complete.
 cudaError_t launch_reduce(const ReduceArgs& a, cudaStream_t s) {
-  reduce_kernel<<<dim3((a.C + 31) / 32, a.nslice), dim3(256), 0, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.C + 31) / 32, a.nslice);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, reduce_kernel, a);
 }
 
 // The device-wide error record of this file's kernels (wkv_sync_status).

@@ -140,10 +140,13 @@ __device__ __forceinline__ float output(const State& s, float k, float v, float 
 // of chunk results (the decay is data independent, so a chunk's effect on
 // the carried state is "decay by its length, then add its own summary").
 // One exponential: the larger of the two scales gets exactly 1.  Written with
-// explicit fmaf so that every caller performs the same roundings (the
-// look-back relies on bitwise equal folds).
+// explicit roundings (fmaf, and __fsub_rn, which the compiler never fuses
+// with the multiply that formed `decay` at the call site) so that every
+// kernel performs the same roundings: the forward pass and the state-only
+// pass must give bitwise equal states, and the look-back relies on bitwise
+// equal folds.
 __device__ __forceinline__ State combine(const State& x, float decay, const State& y) {
-  const float px = x.pp - decay;
+  const float px = __fsub_rn(x.pp, decay);
   const float d = px - y.pp;
   const float e = exp_neg_abs(d);
   const bool keep = d >= 0.f;

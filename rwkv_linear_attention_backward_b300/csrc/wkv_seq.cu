@@ -525,14 +525,26 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
   const int last_len = g.nchunks - (R - 1) * len;
   int nitems = 0;
   for (int r = wi; r < R; r += W) nitems += r == R - 1 ? last_len : 2 * len;
+  // A position in the warp's item stream: m-th run of the warp, item off of
+  // that run; advanced one item at a time (no division per item).
+  struct Cur {
+    int m, off;
+  };
+  auto advance = [&](Cur& c) {
+    const int n = wi + c.m * W == R - 1 ? last_len : 2 * len;
+    if (++c.off == n) {
+      c.off = 0;
+      ++c.m;
+    }
+  };
   struct Item {
     int r, j;
     bool p1, first, last;  // phase 1 item; first / last item of its phase
   };
-  auto item = [&](int it) {
+  auto item = [&](const Cur& c) {
     Item o;
-    const int m = it / (2 * len), off = it - m * 2 * len;
-    o.r = wi + m * W;
+    const int off = c.off;
+    o.r = wi + c.m * W;
     if (o.r == R - 1) {
       o.p1 = false;
       o.j = o.r * len + off;
@@ -547,22 +559,26 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
     }
     return o;
   };
-  auto issue = [&](int it) {  // lane 0: item it into its stage
+  auto issue = [&](int it, const Cur& c) {  // lane 0: item it (at c) into its stage
     const int s = it % NS;
-    const int j = item(it).j;
+    const int j = item(c).j;
     KV* dk = ring + (size_t)(2 * s) * kSeqTile;
     mbar_arrive_expect_tx(&full[s], kStageBytes);
     tma_load_3d(dk, &a.tk, &full[s], col.c0, j * kChunk, col.b);
     tma_load_3d(dk + kSeqTile, &a.tv, &full[s], col.c0, j * kChunk, col.b);
   };
   int issued = 0;
+  Cur ahead{0, 0};  // the next item to stage
   if (tma) {
     if (lane == 0) {
       for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
       mbar_init_fence();
       tma_prefetch_desc(&a.tk);
       tma_prefetch_desc(&a.tv);
-      for (int it = 0; it < NS && it < nitems; ++it) issue(it);
+    }
+    for (int it = 0; it < NS && it < nitems; ++it) {
+      if (lane == 0) issue(it, ahead);
+      advance(ahead);
     }
     issued = min(NS, nitems);
     __syncwarp();
@@ -584,8 +600,9 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
   };
 
   State S = empty_state(), P = empty_state();
-  for (int it = 0; it < nitems; ++it) {
-    const Item m = item(it);
+  Cur cur{0, 0};
+  for (int it = 0; it < nitems; ++it, advance(cur)) {
+    const Item m = item(cur);
     const int s = it % NS;
     KV* dk = ring + (size_t)(2 * s) * kSeqTile;
     if (tma) {
@@ -622,7 +639,8 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
     // release the stage (only read: see seq_fwd_run)
     __syncwarp();
     if (tma && it + NS < nitems) {
-      if (lane == 0) issue(it + NS);
+      if (lane == 0) issue(it + NS, ahead);
+      advance(ahead);
       ++issued;
     }
     if (m.p1 && m.last) {
@@ -1074,6 +1092,9 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
 template <typename KV, int NS, bool GATE>
 __global__ void __launch_bounds__(kSeqChannels) seq_bwd_kernel(const __grid_constant__ SeqBwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
+  // the gw, gu reduction that follows may be launched now (its CTAs start as
+  // this launch's CTAs leave SMs, and wait for its completion before reading)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const Launch L = seq_launch(a.eh);
   seq_bwd_run<KV, NS, GATE>(a, L, smem);
   seq_exit(a.exited, a.eh, L.epoch);
