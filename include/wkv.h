@@ -192,6 +192,33 @@ wkv_status wkv_state_fold(int B, int C, const float* w, int n, const float* stat
                           float* out, void* stream);
 
 /*
+ * wkv_adjoint_fold -- the gradient of the start state of the first of n
+ * consecutive segments of one sequence, from each segment's own start-state
+ * gradient (wkv_backward_with_state with no gstate_end: what its own
+ * outputs' gradients put on it) and the gradient on the last segment's end
+ * state.  Through a segment of n tokens whose outputs carry no gradient the
+ * adjoint of the sums only decays, la <- e^{-n w} la (lb alike), the
+ * reverse of the state fold (eq. (8) written recursively, "RWKV解读" section
+ * "3、RWKV的网络架构"); so the start gradient of segment i is its own plus
+ * e^{-n_i w} times the start gradient of segment i + 1, folded from the last
+ * segment to the first.  A sequence split along time gives each segment's
+ * gstate_end this way from the later segments' summary passes.
+ *   w            [C] the decay.
+ *   adj          [n][3][B][C] planes (g_num, g_den, pp) per segment, in
+ *                sequence order, each at its own start state's pp.
+ *   lengths      [n] host array, tokens per segment (>= 0).
+ *   gstate_end   [3][B][C] or NULL: the gradient on the last segment's end
+ *                state, in the same planes (NULL: none).
+ *   out          [3][B][C] planes of the first segment's start gradient, at
+ *                its pp (gstate_end itself when n = 0).
+ * Errors: WKV_ERR_INVALID_ARG (B or C <= 0, n < 0 or n > 256, a negative
+ * length, w or out NULL, adj or lengths NULL with n > 0, n = 0 with no
+ * gstate_end), WKV_ERR_CUDA.
+ */
+wkv_status wkv_adjoint_fold(int B, int C, const float* w, int n, const float* adj, const long long* lengths,
+                            const float* gstate_end, float* out, void* stream);
+
+/*
  * wkv_backward -- gradients of sum(gy * wkv) with respect to w, u, k, v.
  *   kv_dtype    WKV_F32: k, v, gy are float; WKV_BF16: k, v, gy are bf16
  *               (halving the bytes read; the arithmetic stays fp32 and
@@ -303,6 +330,12 @@ wkv_status wkv_channel_mix_gate_backward(long long n, const float* r, const floa
  *               same state_in (or NULL: recomputed from state_in).
  *   The other arguments, and gw (which then includes the decay of state_in
  *   through the segment), are those of wkv_backward.
+ *   Summary pass: gk and gv both NULL (and gstate_in given) computes
+ *   gstate_in alone, from gy and gstate_end, without writing anything else
+ *   (gw, gu may be NULL and are not written).  It reads k, v, gy and the
+ *   checkpoints once; the segments of a sequence split along time use it to
+ *   exchange their start-state gradients before their full backward passes
+ *   (wkv_adjoint_fold), so that those run at the same time.
  * Errors: as wkv_backward; WKV_ERR_UNSUPPORTED while the chunked scan is
  * forced.
  */

@@ -60,6 +60,7 @@ _SIGNATURES = {
     "wkv_token_shift_backward_workspace_bytes": ([_i, _i, _i], _sz),
     "wkv_token_shift_backward": ([_i, _i, _i] + [_vp] * 13 + [_vp, _sz, _vp], _i),
     "wkv_state_fold": ([_i, _i, _vp, _i, _vp, ctypes.POINTER(_ll), _vp, _vp], _i),
+    "wkv_adjoint_fold": ([_i, _i, _vp, _i, _vp, ctypes.POINTER(_ll), _vp, _vp, _vp], _i),
     "wkv_channel_mix_sqrelu": ([_ll] + [_vp] * 2 + [_vp], _i),
     "wkv_channel_mix_sqrelu_backward": ([_ll] + [_vp] * 3 + [_vp], _i),
     "wkv_channel_mix_gate": ([_ll] + [_vp] * 3 + [_vp], _i),
@@ -291,6 +292,31 @@ def state_fold(w, states, lengths, *, out=None, stream=None):
     return out
 
 
+def adjoint_fold(w, adj, lengths, gstate_end=None, *, out=None, stream=None):
+    """The start-state gradient [3, B, C] = (g_num, g_den, pp) of the first
+    of n consecutive segments: ``adj`` fp32 [n, 3, B, C] is each segment's
+    own start-state gradient (its summary pass with no end gradient),
+    ``lengths`` their token counts, ``gstate_end`` [3, B, C] the gradient on
+    the last segment's end state (None: none; required when n = 0)."""
+    C = w.shape[0]
+    _need(w, "w", shape=(C,))
+    _need(adj, "adj")
+    if adj.dim() != 4 or adj.shape[1] != 3 or adj.shape[3] != C:
+        raise ValueError("adj must be [n, 3, B, C]")
+    n, B = adj.shape[0], adj.shape[2]
+    lengths = [int(x) for x in lengths]
+    if len(lengths) != n:
+        raise ValueError("one length per segment")
+    if gstate_end is not None:
+        _need(gstate_end, "gstate_end", shape=(3, B, C))
+    out = torch.empty((3, B, C), dtype=torch.float32, device=w.device) if out is None else out
+    _need(out, "out", shape=(3, B, C))
+    lens = (ctypes.c_longlong * max(n, 1))(*lengths)
+    _check(_lib.wkv_adjoint_fold(B, C, _p(w), n, _p(adj) if n else None, lens, _p(gstate_end), _p(out),
+                                 _stream(stream)), "wkv_adjoint_fold")
+    return out
+
+
 def token_shift(x, x0, mu_k, mu_v, mu_r, *, xk=None, xv=None, xr=None, stream=None):
     """(xk, xv, xr) = mu x_t + (1 - mu) x_{t-1} for x [B, T, C] (fp32); x0
     [B, C] is the token before the sequence (None: zeros)."""
@@ -396,14 +422,15 @@ def backward(w, u, k, v, gy, *, ckpt=None, gw=None, gu=None, gk=None, gv=None, w
 
 
 def backward_with_state(w, u, k, v, gy, state_in=None, gstate_end=None, *, ckpt=None, gw=None, gu=None, gk=None,
-                        gv=None, gstate_in=None, want_gstate_in: bool = True, workspace: Workspace | None = None,
-                        stream=None):
+                        gv=None, gstate_in=None, want_gstate_in: bool = True, summary: bool = False,
+                        workspace: Workspace | None = None, stream=None):
     """``backward`` for a forward pass that started from ``state_in`` ([3, B,
     C] or None) and whose end state feeds later tokens: ``gstate_end`` [3, B,
     C] = (g_num, g_den, pp), the gradient with respect to the end state's
     num, den written at scale pp (None: none).  Returns (gw, gu, gk, gv,
     gstate_in), the last [3, B, C] = (g_num, g_den, pp) for state_in (None
-    when not wanted)."""
+    when not wanted).  ``summary``: the summary pass, which computes
+    gstate_in alone (gw, gu, gk, gv are None)."""
     if k.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("k must be float32 or bfloat16")
     B, T, C = k.shape
@@ -420,14 +447,18 @@ def backward_with_state(w, u, k, v, gy, state_in=None, gstate_end=None, *, ckpt=
         if ckpt.numel() < checkpoint_floats(B, T, C):
             raise ValueError("ckpt is too small")
     dev = k.device
-    gw = torch.empty(C, dtype=torch.float32, device=dev) if gw is None else gw
-    gu = torch.empty(C, dtype=torch.float32, device=dev) if gu is None else gu
-    gk = torch.empty((B, T, C), dtype=torch.float32, device=dev) if gk is None else gk
-    gv = torch.empty((B, T, C), dtype=torch.float32, device=dev) if gv is None else gv
+    if summary:
+        gw = gu = gk = gv = None
+        want_gstate_in = True
+    else:
+        gw = torch.empty(C, dtype=torch.float32, device=dev) if gw is None else gw
+        gu = torch.empty(C, dtype=torch.float32, device=dev) if gu is None else gu
+        gk = torch.empty((B, T, C), dtype=torch.float32, device=dev) if gk is None else gk
+        gv = torch.empty((B, T, C), dtype=torch.float32, device=dev) if gv is None else gv
+        for t, n, s in ((gw, "gw", (C,)), (gu, "gu", (C,)), (gk, "gk", (B, T, C)), (gv, "gv", (B, T, C))):
+            _need(t, n, shape=s)
     if gstate_in is None and want_gstate_in:
         gstate_in = torch.empty((3, B, C), dtype=torch.float32, device=dev)
-    for t, n, s in ((gw, "gw", (C,)), (gu, "gu", (C,)), (gk, "gk", (B, T, C)), (gv, "gv", (B, T, C))):
-        _need(t, n, shape=s)
     if gstate_in is not None:
         _need(gstate_in, "gstate_in", shape=(3, B, C))
     ws = workspace or _workspace("bwd", backward_workspace_bytes(B, T, C), dev)

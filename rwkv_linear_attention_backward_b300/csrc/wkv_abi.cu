@@ -231,6 +231,7 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int kv
               (!r || make_tile_map(&a.tr, r, B, T, C, eb, kSeqChannels));
   cudaError_t e = launch_seq_backward(a, kv_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "wkv_backward");
+  if (!gk) return WKV_OK;  // a summary pass: no gw, gu to reduce
   const int rows = a.nseg * B;
   ReduceArgs red;
   red.part = a.part;
@@ -330,7 +331,10 @@ wkv_status backward_impl(int B, int T, int C, int kv_dtype, const float* w, cons
                          const float* gstate_end, const float* ckpt, float* gw, float* gu, float* gk, float* gv,
                          float* gr, float* gstate_in, void* workspace, size_t workspace_bytes, void* stream) {
   clear_error();
-  if (!sizes_ok(B, T, C) || !w || !u || !k || !v || !gy || !gw || !gu || !gk || !gv) return WKV_ERR_INVALID_ARG;
+  // gk, gv both NULL: the summary pass (the start state's gradient only)
+  const bool summary = !gk && !gv && gstate_in && !r;
+  if (!sizes_ok(B, T, C) || !w || !u || !k || !v || !gy) return WKV_ERR_INVALID_ARG;
+  if (!summary && (!gw || !gu || !gk || !gv)) return WKV_ERR_INVALID_ARG;
   if (r && !gr) return WKV_ERR_INVALID_ARG;
   if (kv_dtype != WKV_F32 && kv_dtype != WKV_BF16) return WKV_ERR_INVALID_ARG;
   const ScanGeometry g = make_geometry(B, T, C);
@@ -725,6 +729,30 @@ wkv_status wkv_state_fold(int B, int C, const float* w, int n, const float* stat
   a.n = n;
   cudaError_t e = launch_state_fold(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_state_fold");
+}
+
+wkv_status wkv_adjoint_fold(int B, int C, const float* w, int n, const float* adj, const long long* lengths,
+                            const float* gstate_end, float* out, void* stream) {
+  clear_error();
+  if (B <= 0 || C <= 0 || (double)B * C >= 1099511627776.0 || !w || !out || n < 0 || n > kMaxFoldSegments)
+    return WKV_ERR_INVALID_ARG;
+  if (n > 0 && (!adj || !lengths)) return WKV_ERR_INVALID_ARG;
+  if (n == 0 && !gstate_end) return WKV_ERR_INVALID_ARG;
+  AdjFoldArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int i = 0; i < n; ++i) {
+    if (lengths[i] < 0) return WKV_ERR_INVALID_ARG;
+    a.len[i] = lengths[i];
+  }
+  a.w = w;
+  a.adj = adj;
+  a.gend = gstate_end;
+  a.out = out;
+  a.B = B;
+  a.C = C;
+  a.n = n;
+  cudaError_t e = launch_adjoint_fold(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_adjoint_fold");
 }
 
 wkv_status wkv_debug_set_wait_budget_ns(long long ns) {

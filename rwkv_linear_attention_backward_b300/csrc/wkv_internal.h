@@ -220,6 +220,19 @@ struct FoldArgs {
 };
 cudaError_t launch_state_fold(const FoldArgs& a, cudaStream_t s);
 
+// Start-state gradients of consecutive segments (each with a zero gradient
+// on its end state), folded last to first after the gradient on the last
+// segment's end state (gend, or null): the start-state gradient of the first.
+struct AdjFoldArgs {
+  const float* w;
+  const float* adj;   // [n][3][B][C] planes (g_num, g_den, pp)
+  const float* gend;  // [3][B][C] or null
+  float* out;         // [3][B][C]
+  int B, C, n;
+  long long len[kMaxFoldSegments];
+};
+cudaError_t launch_adjoint_fold(const AdjFoldArgs& a, cudaStream_t s);
+
 // Grid of a persistent scan kernel: resident CTAs per SM x SMs, at most ntiles.
 cudaError_t launch_forward(FwdArgs& a, int kv_dtype, bool write_y, cudaStream_t s);
 cudaError_t launch_backward(BwdArgs& a, cudaStream_t s);

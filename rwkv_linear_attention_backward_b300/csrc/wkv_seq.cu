@@ -948,8 +948,12 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
 
   int first, count;  // in walk order: position p is chunk last - p
   segment_of(g.nchunks, nseg, run, first, count);
-  const int n1 = run < nseg - 1 ? count : 0;
-  const int nitems = n1 + count;
+  // A summary pass (no gk, gv): every run summarises its chunks, and the run
+  // holding chunk 0 folds the summaries and writes the start state's
+  // gradient; nothing else is computed.
+  const bool summary = a.gk == nullptr;
+  const int n1 = summary || run < nseg - 1 ? count : 0;
+  const int nitems = summary ? n1 : n1 + count;
   auto chunk_of = [&](int it) { return last - (first + (it < n1 ? it : it - n1)); };
   auto issue = [&](int it) {  // lane 0: item it into its stage
     const int s = it % NS;
@@ -1030,7 +1034,10 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
   // fault injection: the run holding this chunk never publishes
   const bool skip = a.debug_skip_chunk >= 0 && last - a.debug_skip_chunk >= first &&
                     last - a.debug_skip_chunk < first + count;
-  if (n1 > 0 && col.valid && !skip) rec_store(a.recs + (size_t)run * jstride + o0, L.tag, X.la, X.lb, X.f);
+  if (n1 > 0 && run < nseg - 1 && col.valid && !skip)
+    rec_store(a.recs + (size_t)run * jstride + o0, L.tag, X.la, X.lb, X.f);
+  if (summary && run < nseg - 1) return;
+  const Adj own = X;  // this run's summary (the summary pass's last run)
 
   // the carry into this run's end (in time): the gradient given on the
   // state after the last token, if any (the num, den gradients of a state
@@ -1072,6 +1079,16 @@ __device__ __forceinline__ void seq_bwd_run(const SeqBwdArgs& a, const Launch& L
     kahan_add(cw.gw_s, cw.gw_k, gw_acc);
     kahan_add(cw.gu_s, cw.gu_k, gu_acc);
     release(it);
+  }
+  if (summary) {  // the run holding chunk 0: its own summary after the carry
+    const int span = run == 0 ? g.T : count * kChunk;
+    X = (run == 0 && !has_end) ? own : fold_adj(own, (float)span * cw.w, X);
+    if (a.gstate_in && col.valid) {
+      a.gstate_in[o0] = X.la;
+      a.gstate_in[jstride + o0] = X.lb;
+      a.gstate_in[2 * jstride + o0] = X.f;
+    }
+    return;
   }
   // the run holding chunk 0 ends at the sequence's start: X is then the
   // gradient of the start state's num, den, in record form at its pp

@@ -17,12 +17,23 @@ torch.distributed moving 3·B·C floats per rank once:
 Each rank reads its k, v twice.
 
 The backward pass (``backward_tsplit``) needs, per rank, the gradient that
-the tokens after its segment put on its end state, so the ranks run in
-turn, last first: a rank receives that gradient from the next rank, runs
-``backward_with_state`` from its start state, and sends the gradient of its
-start state (3·B·C floats) to the previous rank; gw and gu are summed over
-the ranks by an all-reduce.  Its gk, gv are exact; the ranks' backward
-passes do not overlap.
+the tokens after its segment put on its end state.  Through tokens whose
+outputs carry no gradient that gradient only decays (la <- e^{-w} la, lb
+alike), so it is folded from the later segments' own start-state gradients
+the way states are folded forwards, and the ranks' backward passes run at
+the same time.  Per rank:
+
+5. its segment's start-state gradient from its own gy alone (the summary
+   pass of ``backward_with_state``: reads k, v, gy once, writes 3·B·C
+   floats);
+6. an all-gather of those gradients (3·B·C floats per rank);
+7. its end gradient: the fold of the later segments' gradients, after the
+   gradient given on the sequence's end state if any (``adjoint_fold``);
+8. its full backward pass from its start state with that end gradient;
+   gw and gu summed over the ranks by an all-reduce.
+
+Each rank reads its k, v, gy twice in the backward pass too; nothing waits
+on another rank's backward pass.
 """
 from __future__ import annotations
 
@@ -72,34 +83,43 @@ def forward_tsplit(w, u, k, v, state_in=None, *, group=None, ops=None, want_star
     return (y, end, start) if want_start else (y, end)
 
 
-def backward_tsplit(w, u, k, v, gy, start, *, group=None, ops=None):
+def end_gradient(w, starts_grads, lengths, rank: int, gstate_end=None, *, ops=None):
+    """Step 7: the gradient on segment ``rank``'s end state, [3, B, C] planes
+    (g_num, g_den, pp), or None when there is none.  ``starts_grads`` [world,
+    3, B, C] and ``lengths`` [world] are every segment's own start-state
+    gradient and tokens; ``gstate_end`` the gradient given on the whole
+    sequence's end state (None: none)."""
+    ops = _ops(ops)
+    lengths = [int(x) for x in lengths]
+    later = starts_grads[rank + 1:]
+    if later.shape[0] == 0:
+        return gstate_end
+    return ops.adjoint_fold(w, later.contiguous(), lengths[rank + 1:], gstate_end)
+
+
+def backward_tsplit(w, u, k, v, gy, start, gstate_end=None, *, group=None, ops=None):
     """Gradients of sum(gy * wkv) over the whole split sequence for this
     rank's segment: ``start`` is the state the segment started from
-    (``forward_tsplit(..., want_start=True)``).  Returns (gw, gu) summed over
-    all ranks, and this segment's (gk, gv), and the gradient of the state
-    before the whole sequence as (g_num, g_den, pp) on rank 0 (None
-    elsewhere)."""
+    (``forward_tsplit(..., want_start=True)``), ``gstate_end`` (the same on
+    every rank) the gradient on the state after the whole sequence, as
+    (g_num, g_den, pp) planes (None: none).  Returns (gw, gu) summed over all
+    ranks, and this segment's (gk, gv), and the gradient of the state before
+    the whole sequence as (g_num, g_den, pp) on rank 0 (None elsewhere)."""
     import torch.distributed as dist
 
     ops = _ops(ops)
     rank, world = dist.get_rank(group), dist.get_world_size(group)
     B, T, C = k.shape
-    g_end = None
-    if rank + 1 < world:
-        g_end = torch.empty((3, B, C), dtype=start.dtype, device=start.device)
-        dist.recv(g_end, src=_global(group, rank + 1), group=group)
+    own = ops.backward_with_state(w, u, k, v, gy, start, None, summary=True)[4]
+    grads = torch.empty((world,) + tuple(own.shape), dtype=own.dtype, device=own.device)
+    dist.all_gather(list(grads.unbind(0)), own.contiguous(), group=group)
+    lens = torch.empty((world, 1), dtype=torch.int64, device=own.device)
+    dist.all_gather(list(lens.unbind(0)), torch.full((1,), T, dtype=torch.int64, device=own.device), group=group)
+    g_end = end_gradient(w, grads, lens.flatten().tolist(), rank, gstate_end, ops=ops)
     gw, gu, gk, gv, g_start = ops.backward_with_state(w, u, k, v, gy, start, g_end)
-    if rank > 0:
-        dist.send(g_start.contiguous(), dst=_global(group, rank - 1), group=group)
     dist.all_reduce(gw, group=group)
     dist.all_reduce(gu, group=group)
     return gw, gu, gk, gv, (g_start if rank == 0 else None)
-
-
-def _global(group, r: int) -> int:
-    import torch.distributed as dist
-
-    return r if group is None else dist.get_global_rank(group, r)
 
 
 def _ops(ops):

@@ -292,6 +292,30 @@ def cmix_gate_backward(r, vk, gout):
     return (g * _f32(vk) * s * (F32(1) - s)).astype(F32), (g * s).astype(F32)
 
 
+# --------------------------------------------------------- adjoint fold
+def adjoint_fold(w, adj, lengths, gstate_end=None):
+    """The start-state gradient of the first of n segments in float32, from
+    their own start gradients ``adj`` [n, 3, B, C] planes (g_num, g_den, pp)
+    and the gradient on the last end state: in unscaled form (g e^{-pp}),
+    each segment's own plus e^{-n w} times the next one's, last to first;
+    returned as planes at the first segment's pp."""
+    w = _f32(w)
+    a = _f32(adj)
+    X = None
+    if gstate_end is not None:
+        g = _f32(gstate_end)
+        s = np.exp(-g[2])
+        X = (g[0] * s, g[1] * s)
+    for i in range(a.shape[0] - 1, -1, -1):
+        s = np.exp(-a[i, 2])
+        own = (a[i, 0] * s, a[i, 1] * s)
+        dec = np.exp(-(F32(lengths[i]) * w))
+        X = own if X is None else (own[0] + dec * X[0], own[1] + dec * X[1])
+    pp = a[0, 2]
+    e = np.exp(pp)
+    return np.stack([X[0] * e, X[1] * e, pp]).astype(F32)
+
+
 # ----------------------------------------------------------- perturbations
 def perturbed(arrays, seed: int):
     """The float inputs moved by one unit in the last place of float32, up or

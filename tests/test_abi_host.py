@@ -36,7 +36,8 @@ def declared_functions():
 BOUNDARY = ("wkv_status_string", "wkv_forward_workspace_bytes", "wkv_backward_workspace_bytes", "wkv_forward",
             "wkv_backward", "wkv_decode_step", "wkv_last_error_string", "wkv_sync_status")
 ADDED = ("wkv_checkpoint_floats", "wkv_workspace_init", "wkv_workspace_check", "wkv_forward_with_state",
-         "wkv_backward_with_state", "wkv_forward_gated", "wkv_backward_gated", "wkv_state_fold", "wkv_token_shift",
+         "wkv_backward_with_state", "wkv_forward_gated", "wkv_backward_gated", "wkv_state_fold", "wkv_adjoint_fold",
+         "wkv_decode_step_bf16", "wkv_token_shift",
          "wkv_token_shift_backward", "wkv_channel_mix_sqrelu", "wkv_channel_mix_gate", "wkv_forward_noalloc")
 
 
@@ -223,6 +224,26 @@ def test_backward_with_state_rejects_before_launch(lib):
         assert b"sequential" in lib.wkv_last_error_string()
     finally:
         lib.wkv_debug_set_scan_mode(0)
+
+
+def test_summary_pass_and_adjoint_fold_reject_before_launch(lib):
+    B, T, C = 2, 40, 64
+    wsb = ctypes.c_size_t(lib.wkv_backward_workspace_bytes(B, T, C))
+    # a summary pass (gk, gv NULL) must return the start state's gradient
+    assert lib.wkv_backward_with_state(B, T, C, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, NULL, NULL, NULL,
+                                       NULL, NULL, FAKE, wsb, NULL) == 1
+    lens = (ctypes.c_longlong * 3)(5, 0, 7)
+    bad = (ctypes.c_longlong * 3)(5, -1, 7)
+    fold = lib.wkv_adjoint_fold
+    assert fold(0, 4, FAKE, 3, FAKE, lens, FAKE, FAKE, NULL) == 1
+    assert fold(2, 4, NULL, 3, FAKE, lens, FAKE, FAKE, NULL) == 1
+    assert fold(2, 4, FAKE, 3, FAKE, lens, FAKE, NULL, NULL) == 1
+    assert fold(2, 4, FAKE, -1, FAKE, lens, FAKE, FAKE, NULL) == 1
+    assert fold(2, 4, FAKE, 257, FAKE, lens, FAKE, FAKE, NULL) == 1
+    assert fold(2, 4, FAKE, 3, NULL, lens, FAKE, FAKE, NULL) == 1
+    assert fold(2, 4, FAKE, 3, FAKE, NULL, FAKE, FAKE, NULL) == 1
+    assert fold(2, 4, FAKE, 3, FAKE, bad, FAKE, FAKE, NULL) == 1
+    assert fold(2, 4, FAKE, 0, NULL, lens, NULL, FAKE, NULL) == 1  # nothing to fold and no end gradient
 
 
 def test_decode_rejects_before_launch(lib):
