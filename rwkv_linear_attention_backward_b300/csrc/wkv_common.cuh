@@ -60,6 +60,33 @@ __device__ __forceinline__ float exp_neg_abs(float d) { return ex2(-fabsf(d) * k
 
 __device__ __forceinline__ float exp_nat(float x) { return ex2(x * kLog2e); }
 
+// Two fp32 values in one 64-bit register pair, for the packed fp32
+// instructions of sm_100 and later: one fma.rn.f32x2 is two IEEE fmas, lane
+// by lane, so a packed chain gives the scalar chain's values bit for bit.
+struct Pk2 {
+  unsigned long long v;
+};
+__device__ __forceinline__ Pk2 f2(float lo, float hi) {
+  Pk2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(Pk2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(Pk2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  return hi;
+}
+__device__ __forceinline__ Pk2 fma2(Pk2 a, Pk2 b, Pk2 c) {  // a * b + c, per lane
+  Pk2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return d;
+}
+
 // sigmoid(r) = 1 / (1 + e^{-r}), the receptance gate on the time-mixing
 // output: 0 once e^{-r} overflows (r below about -88), 1 once e^{-r} is
 // below half an ulp of 1.

@@ -128,11 +128,12 @@ __device__ __forceinline__ void fwd_rerun(const FwdArgs& a, const KV* __restrict
 #pragma unroll 8
       for (int i = 0; i < p.len; ++i) {
         const float ek = ex2(fmaf(to_f32<KV>(sk[i * S]), kLog2e, -F2));
-        const float vv = to_f32<KV>(sv[i * S]);
-        const float ec = ek * eu;
-        const float yv = fmaf(ec, vv, na) * rcp(nb + ec);
+        const float ekv = ek * to_f32<KV>(sv[i * S]);
+        // numerator e^{k-F} v e^u + a, denominator e^{k-F} e^u + b: the
+        // sequential kernels' arithmetic, so both give the same outputs
+        const float yv = fmaf(ekv, eu, na) * rcp(fmaf(ek, eu, nb));
         if (valid) __stcs(yp + (int64_t)i * g.C, yv);
-        na = fmaf(na, p.ew, ek * vv);
+        na = fmaf(na, p.ew, ekv);
         nb = fmaf(nb, p.ew, ek);
       }
     } else {

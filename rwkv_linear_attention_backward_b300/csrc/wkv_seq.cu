@@ -197,37 +197,39 @@ __device__ __forceinline__ void seq_fwd_full(const KV* __restrict__ sk, const KV
     // before each token (four chains); the outputs.
     const float F2 = F * kLog2e;
     const float s0 = exp_nat(P.pp - F);
-    float vr[L];
+    // per token the pair {e^{k-F} v, e^{k-F}}: the addends of both pairs of
+    // chains (the sums with P, for the outputs; the chunk's own, for the
+    // carried state) and, times e^u, of the output's numerator and
+    // denominator
+    Pk2 kv[L];
 #pragma unroll
     for (int i = 0; i < L; ++i) {
-      vr[i] = to_f32<KV>(sv[i * S]);
-      kr[i] = ex2(fmaf(kr[i], kLog2e, -F2));  // ek
+      const float ek = ex2(fmaf(kr[i], kLog2e, -F2));
+      kv[i] = f2(ek * to_f32<KV>(sv[i * S]), ek);
     }
-    float na = P.num * s0, nb = P.den * s0;
-    float on = 0.f, od = 0.f;
-    float A[L], Bd[L];  // sums with P before each token (for the outputs)
+    const Pk2 ew2 = f2(ew, ew);
+    Pk2 nab = f2(P.num * s0, P.den * s0);  // sums with P before each token
+    Pk2 own = f2(0.f, 0.f);                // the chunk's own sums
+    Pk2 AB[L];
 #pragma unroll
     for (int i = 0; i < L; ++i) {
-      const float ekv = kr[i] * vr[i];
       if constexpr (YM != kYNone) {
-        A[i] = na;
-        Bd[i] = nb;
-        na = fmaf(na, ew, ekv);
-        nb = fmaf(nb, ew, kr[i]);
+        AB[i] = nab;
+        nab = fma2(nab, ew2, kv[i]);
       }
-      on = fmaf(on, ew, ekv);
-      od = fmaf(od, ew, kr[i]);
+      own = fma2(own, ew2, kv[i]);
     }
     if constexpr (YM != kYNone) {
+      const Pk2 eu2 = f2(eu, eu);
 #pragma unroll
       for (int i = 0; i < L; ++i) {
-        const float ec = kr[i] * eu;
-        const float yv = fmaf(ec, vr[i], A[i]) * rcp(Bd[i] + ec);
+        const Pk2 nd = fma2(kv[i], eu2, AB[i]);  // {numerator, denominator}
+        const float yv = f2_lo(nd) * rcp(f2_hi(nd));
         put_y<YM>(yp, i, ystride, yv, YM == kYGated ? rg[i] : 0.f, valid);
       }
     }
     const float sc = exp_nat(F - r);
-    P = combine(P, (float)L * w, State{on * sc, od * sc, r});
+    P = combine(P, (float)L * w, State{f2_lo(own) * sc, f2_hi(own) * sc, r});
   } else {
 #pragma unroll 1
     for (int i = 0; i < L; ++i) {
@@ -270,8 +272,9 @@ __device__ __forceinline__ void seq_fwd_chunk(const KV* __restrict__ sk, const K
       const float vv = to_f32<KV>(sv[i * S]);
       const float ekv = ek * vv;
       if constexpr (YM != kYNone) {
-        const float ec = ek * eu;
-        const float yv = fmaf(ec, vv, na) * rcp(nb + ec);
+        // the full-chunk body's arithmetic (numerator e^{k-F} v e^u + a,
+        // denominator e^{k-F} e^u + b)
+        const float yv = fmaf(ekv, eu, na) * rcp(fmaf(ek, eu, nb));
         put_y<YM>(yp, i, ystride, yv, load_r<KV, YM>(rp, i, ystride, valid), valid);
         na = fmaf(na, ew, ekv);
         nb = fmaf(nb, ew, ek);
@@ -295,6 +298,54 @@ __device__ __forceinline__ void seq_fwd_chunk(const KV* __restrict__ sk, const K
       step(P, kk, vv, w);
     }
   }
+}
+
+// Phase 1 of the forward walk for one chunk of n tokens: S, the state a run
+// carries from the empty one, advanced past the chunk.  The chunk's own sums
+// are formed directly: token i enters the sums after the chunk with exponent
+// rr_i = k_i - (n-1-i) w; with r = max_i rr_i every weight e^{rr_i - r} is at
+// most 1 and their sum at least 1, so this form is exact in fp32 for any
+// finite input (no fixed scale to leave, no per-token fallback) and needs no
+// chain through the tokens.  S is then decayed over the chunk and combined
+// with the chunk's sums at scale e^{r}.  Phase 2 keeps the chained form,
+// which also yields the outputs, so the checkpoints of every kernel that
+// walks a chunk in phase 2 are the same bit for bit.
+template <bool FULL, typename KV>
+__device__ __forceinline__ void seq_fwd_summary(const KV* __restrict__ sk, const KV* __restrict__ sv, int n, float w,
+                                                State& S) {
+  constexpr int L = kChunk;
+  constexpr int Sd = kSeqChannels;
+  float r, on = 0.f, od = 0.f;
+  if constexpr (FULL) {
+    float rr[L];
+#pragma unroll
+    for (int i = 0; i < L; ++i) rr[i] = fmaf(-(float)(L - 1 - i), w, to_f32<KV>(sk[i * Sd]));
+    r = tree_max<L>(rr);
+    const float r2 = r * kLog2e;
+    float on1 = 0.f, od1 = 0.f;  // odd tokens: two chains per sum
+#pragma unroll
+    for (int i = 0; i < L; i += 2) {
+      const float e0 = ex2(fmaf(rr[i], kLog2e, -r2)), e1 = ex2(fmaf(rr[i + 1], kLog2e, -r2));
+      on = fmaf(e0, to_f32<KV>(sv[i * Sd]), on);
+      on1 = fmaf(e1, to_f32<KV>(sv[(i + 1) * Sd]), on1);
+      od += e0;
+      od1 += e1;
+    }
+    on += on1;
+    od += od1;
+  } else {
+    r = -3.0e38f;
+#pragma unroll 8
+    for (int i = 0; i < n; ++i) r = fmaxf(r, fmaf(-(float)(n - 1 - i), w, to_f32<KV>(sk[i * Sd])));
+    const float r2 = r * kLog2e;
+#pragma unroll 8
+    for (int i = 0; i < n; ++i) {
+      const float e = ex2(fmaf(fmaf(-(float)(n - 1 - i), w, to_f32<KV>(sk[i * Sd])), kLog2e, -r2));
+      on = fmaf(e, to_f32<KV>(sv[i * Sd]), on);
+      od += e;
+    }
+  }
+  S = combine(S, (float)n * w, State{on, od, r});
 }
 
 // Runs of a column's walk: the chunks in walk order (time order for the
@@ -446,9 +497,9 @@ __device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L
     const int j = chunk_of(it);
     const int n = min(kChunk, g.T - j * kChunk);
     if (n == kChunk)
-      seq_fwd_full<KV, kYNone>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, P, nullptr, nullptr, 0, false);
+      seq_fwd_summary<true, KV>(dk + lane, dk + kSeqTile + lane, n, w, P);
     else
-      seq_fwd_chunk<KV, kYNone>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, nullptr, nullptr, 0, false);
+      seq_fwd_summary<false, KV>(dk + lane, dk + kSeqTile + lane, n, w, P);
     release(it);
   }
   const bool skip = a.debug_skip_chunk >= first && a.debug_skip_chunk < first + count;  // fault injection
@@ -616,9 +667,9 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
     if (m.p1) {
       if (m.first) S = empty_state();
       if (n == kChunk)
-        seq_fwd_full<KV, kYNone>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, S, nullptr, nullptr, 0, false);
+        seq_fwd_summary<true, KV>(dk + lane, dk + kSeqTile + lane, n, w, S);
       else
-        seq_fwd_chunk<KV, kYNone>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, S, nullptr, nullptr, 0, false);
+        seq_fwd_summary<false, KV>(dk + lane, dk + kSeqTile + lane, n, w, S);
     } else {
       if (m.first && m.r == R - 1 && !carry_in(m.r, P)) return fail(it);
       const int64_t row = ((int64_t)col.b * g.T + (int64_t)m.j * kChunk) * g.C + col.c;

@@ -144,7 +144,7 @@ def emu_state_content(emu_sums, r_pp):
     return a * s, b * s
 
 
-def assert_state_close(num, den, pp, onum, oden, opp, tol, what="", pp_atol=5e-3, emu_sums=None):
+def assert_state_close(num, den, pp, onum, oden, opp, tol, what="", pp_atol=5e-3, emu_sums=None, oracle=None):
     """Compare a carried state (num, den, pp) with the oracle's.
 
     The state stands for the sums a = num e^{pp}, b = den e^{pp}; pp is only
@@ -153,7 +153,23 @@ def assert_state_close(num, den, pp, onum, oden, opp, tol, what="", pp_atol=5e-3
     num e^{pp - pp_ref}, den e^{pp - pp_ref}.  pp itself must stay a valid
     scale: within pp_atol of the running maximum, and den >= ~1.  Empty
     states (pp_ref = -1e38) must be empty on both sides.  ``emu_sums``: the
-    float32 evaluation's unscaled sums (a, b), for the element-wise floor."""
+    float32 evaluation's unscaled sums (a, b), for the element-wise floor.
+    ``oracle`` = (num, den, pp): (onum, oden, opp) is another GPU state and
+    this the oracle's; both are measured at the oracle's scale and compared
+    as a pair (``assert_close``)."""
+    if oracle is not None:
+        g_num, g_den, g_pp = to_np(num), to_np(den), to_np(pp)
+        o_num, o_den, o_pp = (to_np(x) for x in oracle)
+        b_num, b_den, b_pp = to_np(onum), to_np(oden), to_np(opp)
+        empty = o_pp < -1e37
+        assert np.all(g_pp[empty] < -1e37) and np.all(b_pp[empty] < -1e37), f"{what}: empty state not preserved"
+        fg, fb = np.ones_like(g_pp), np.ones_like(b_pp)
+        fg[~empty] = np.exp(g_pp[~empty] - o_pp[~empty])
+        fb[~empty] = np.exp(b_pp[~empty] - o_pp[~empty])
+        en, ed = emu_state_content(emu_sums, o_pp) if emu_sums is not None else (None, None)
+        assert_close(g_num * fg, b_num * fb, tol, f"{what} num e^pp", emu=en, ref=o_num, pair=True)
+        assert_close(g_den * fg, b_den * fb, tol, f"{what} den e^pp", emu=ed, ref=o_den, pair=True)
+        return
     g_num, g_den, g_pp = to_np(num), to_np(den), to_np(pp)
     r_num, r_den, r_pp = to_np(onum), to_np(oden), to_np(opp)
     empty = r_pp < -1e37

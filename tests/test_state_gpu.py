@@ -78,8 +78,9 @@ def test_split_matches_whole(oracle, wkv, scan_mode, t0):
     nch = -(-T // wkv.chunk_len())
     last = to_np(ckpt).reshape(3, nch, B, C)[:, nch - 1]
     s = to_np(s2)
-    assert_state_close(s[0], s[1], s[2], last[0], last[1], last[2], TOL_Y, "state after both calls")
     n, d, p = oracle.state(w, k, v, T)
+    assert_state_close(s[0], s[1], s[2], last[0], last[1], last[2], TOL_Y, "state after both calls",
+                       emu_sums=(fe["a"], fe["b"]), oracle=(n, d, p))
     assert_state_close(s[0], s[1], s[2], n, d, p, TOL_Y, "state after both calls vs oracle",
                        emu_sums=(fe["a"], fe["b"]))
 
