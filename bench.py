@@ -135,7 +135,7 @@ def aggregate(per_rank_seconds: float, units_per_rank: float, world: int, device
 class ClockSampler:
     """Samples the SM clock and clock-event reasons during a timed region
     (read only): through NVML when pynvml imports, else by running
-    ``nvidia-smi --query-gpu=... -lms 50`` and reading its output."""
+    ``nvidia-smi --query-gpu=... -lms 10`` and reading its output."""
 
     NAMES = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
@@ -146,7 +146,7 @@ class ClockSampler:
                   "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
                   "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int, period_s: float = 0.02):
+    def __init__(self, index: int, period_s: float = 0.002):
         self.index = index
         self.period = period_s
         self.samples = []
@@ -211,7 +211,7 @@ class ClockSampler:
         try:
             self._proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "10"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.source = "nvidia-smi"
         except OSError as e:
             self.error = f"{self.error}; nvidia-smi: {e}"
@@ -239,8 +239,11 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "source": self.source,
                     "error": self.error}
         reasons = sorted(self.reasons - {"gpu_idle"})
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": reasons,
-                "samples": len(self.samples), "source": self.source}
+        out = {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+               "samples": len(self.samples), "source": self.source}
+        if self.source != "nvml" and self.error:
+            out["nvml_error"] = self.error[:120]
+        return out
 
     def rejected(self) -> bool:
         s = self.summary()
