@@ -403,16 +403,18 @@ __device__ __forceinline__ void seq_exit(unsigned int* exited, WsHeader* h, unsi
 
 // Waits (bounded) until the record at p carries this launch's tag on every
 // valid lane.  False when the wait expired (recorded) or the launch gave up
-// elsewhere.
+// elsewhere.  The poll reloads the record back to back (one L2 round trip
+// per try, no sleep: the wait sits on the critical path of the runs that
+// follow) and looks at the abort flag and the clock every 16th try only.
 __device__ __forceinline__ bool wait_rec(const Rec* p, bool valid, const Launch& L, WsHeader* h, uint64_t budget_ns,
                                          Rec& r) {
   r = rec_load(p);
   if (__all_sync(0xffffffffu, !valid || rec_ok(r, L.tag))) return true;
   const uint64_t t0 = globaltimer();
-  while (true) {
-    __nanosleep(100);
+  for (unsigned int n = 1;; ++n) {
     r = rec_load(p);
     if (__all_sync(0xffffffffu, !valid || rec_ok(r, L.tag))) return true;
+    if ((n & 15u) != 0) continue;
     if (__shfl_sync(0xffffffffu, *(volatile const unsigned long long*)&h->abort, 0) == L.epoch) return false;
     if (__shfl_sync(0xffffffffu, globaltimer(), 0) - t0 > budget_ns) {
       if ((threadIdx.x & 31) == 0) record_error(h, kDevErrTimeout, L.epoch);
@@ -1297,9 +1299,10 @@ cudaError_t launch_planned(const DevInfo& d, Args& a, int arrays, size_t elem, s
     // forces chained runs of that length.
     forced = a.chain;
     chained = forced > 0 || ((long long)cols < d.sms && (double)input_bytes > 0.6 * (double)d.l2);
-    // chained runs re-read from L2, so they take more warps: 16 per SM
-    // (measured on the long-context forward: 0.73 ms at 16, 0.86 at 8, 0.9+ at 24)
-    if (chained && !forced) warps = 16;
+    // Chained runs take the caller's warps per SM too: on the long-context
+    // forward (B=1 T=131072 C=2560 bf16) 12 per SM give 22 runs per column
+    // of 6 chunks at 4 stages, 0.59-0.60 ms; 29 runs of 5 (16 per SM) took
+    // 0.65 ms, 23 or 24 runs 0.77-0.85 ms, 20 runs 0.66 ms (one GPU call).
   }
   // resident CTAs per SM of the kernel that will run, at two stages
   int per_sm2 = 0;

@@ -162,6 +162,33 @@ def test_expired_wait_is_reported(oracle, wkv, which, mode):
     check_grads(oracle, w, u, k, v, gy, dict(gk=gk), "after timeout")
 
 
+@pytest.mark.parametrize("kv_dtype", ["f32", "bf16"])
+def test_chained_runs_do_not_depend_on_the_warps(oracle, wkv, kv_dtype):
+    """Chained runs: the state before run r is the start state with the
+    summaries of runs 0..r-1 folded in left to right, whichever warp walks
+    which run, so one warp walking all 67 runs of a column and many warps
+    sharing them give the same bits; both match the oracle."""
+    B, T, C = 2, 32 * 200, 64
+    w, u, k, v, _ = inputs.training_inputs(B, T, C, seed=29, k_std=3.0, d_lo=-7.0, d_hi=1.0, kv_dtype=kv_dtype)
+    tw = cuda(w, u, k, v)
+    outs = []
+    try:
+        wkv.set_scan_mode("sequential")
+        wkv.set_chain_len(3)
+        for runs in (1, 5, 0):
+            wkv.set_max_runs(runs)
+            outs.append(wkv.forward(*tw, want_ckpt=True))
+            torch.cuda.synchronize()
+    finally:
+        wkv.set_scan_mode("auto")
+        wkv.set_chain_len(0)
+        wkv.set_max_runs(0)
+    for (y, ck), runs in zip(outs[1:], (5, 0)):
+        assert torch.equal(y, outs[0][0]), f"y, max runs {runs}"
+        assert torch.equal(ck, outs[0][1]), f"checkpoints, max runs {runs}"
+    check_y(oracle, w, u, k, v, outs[0][0], f"chained {kv_dtype}")
+
+
 def test_graph_replay_with_new_inputs(wkv, scan_mode):
     """Forward + backward captured once in a CUDA graph and replayed after the
     inputs change in place give the results of direct calls on the new
