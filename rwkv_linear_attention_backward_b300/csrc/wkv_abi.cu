@@ -147,14 +147,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace
 
-bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int elem_bytes, int box_c) {
+bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int elem_bytes, int box_c, int box_t) {
   if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
   if (((size_t)C * elem_bytes) % 16 != 0) return false;
   PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)T, (cuuint64_t)B};
   const cuuint64_t strides[2] = {(cuuint64_t)C * elem_bytes, (cuuint64_t)T * C * elem_bytes};
-  const cuuint32_t box[3] = {(cuuint32_t)box_c, (cuuint32_t)kChunk, 1u};
+  const cuuint32_t box[3] = {(cuuint32_t)box_c, (cuuint32_t)box_t, 1u};
   const cuuint32_t estride[3] = {1u, 1u, 1u};
   const CUresult r = fn(map, elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                         const_cast<void*>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -167,6 +167,16 @@ bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int 
 
 namespace wkv {
 namespace {
+
+// The tensor maps of the sequential forward walk: k and v in boxes of one
+// chunk, and in boxes of one chained item (chain_chunks chunks).  False when
+// the inputs do not allow TMA (the kernels then copy with plain loads).
+bool seq_forward_maps(SeqFwdArgs& a, const void* k, const void* v, int B, int T, int C, int eb) {
+  const int box_t = chain_chunks((size_t)eb) * kChunk;
+  return make_tile_map(&a.tk, k, B, T, C, eb, kSeqChannels) && make_tile_map(&a.tv, v, B, T, C, eb, kSeqChannels) &&
+         make_tile_map(&a.tk2, k, B, T, C, eb, kSeqChannels, box_t) &&
+         make_tile_map(&a.tv2, v, B, T, C, eb, kSeqChannels, box_t);
+}
 
 // The backward pass with the sequential column kernels: the checkpoints
 // (recomputed by a state-only forward walk when the caller has none), the
@@ -198,7 +208,7 @@ wkv_status backward_sequential(const ScanGeometry& g, const BwdLayout& l, int kv
     f.eh = hdr;
     f.g = g;
     f.budget_ns = budget;
-    f.use_tma = make_tile_map(&f.tk, k, B, T, C, eb, kSeqChannels) && make_tile_map(&f.tv, v, B, T, C, eb, kSeqChannels);
+    f.use_tma = seq_forward_maps(f, k, v, B, T, C, eb);
     cudaError_t e = launch_seq_forward(f, kv_dtype, false, s);
     if (e != cudaSuccess) return cuda_fail(e, "wkv_backward: state pass");
     states = f.ckpt;
@@ -296,7 +306,7 @@ wkv_status forward_impl(int B, int T, int C, int kv_dtype, const float* w, const
     q.debug_skip_chunk = g_skip_chunk.load();
     q.g = g;
     q.budget_ns = (uint64_t)g_budget_ns.load();
-    q.use_tma = make_tile_map(&q.tk, k, B, T, C, eb, kSeqChannels) && make_tile_map(&q.tv, v, B, T, C, eb, kSeqChannels);
+    q.use_tma = seq_forward_maps(q, k, v, B, T, C, eb);
     e = launch_seq_forward(q, kv_dtype, y != nullptr, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? WKV_OK : cuda_fail(e, "wkv_forward");
   }

@@ -114,7 +114,8 @@ cudaError_t take_error_bwd(unsigned int* code);
 // (elem_bytes 4 = fp32, 2 = bf16).  False when TMA cannot address it (the
 // base not 16-byte aligned or C * elem_bytes not a multiple of 16) or the
 // driver has no encoder; the kernels then stage tiles with plain loads.
-bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int elem_bytes, int box_c);
+bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int elem_bytes, int box_c,
+                   int box_t = kChunk);
 
 // Sequential column kernels (wkv_seq.cu): a column is one batch row and 32
 // channels; its chunks are walked in order (forward) or in reverse order
@@ -124,8 +125,14 @@ bool make_tile_map(CUtensorMap* map, const void* base, int B, int T, int C, int 
 constexpr int kSeqChannels = 32;
 constexpr int kSeqMaxRuns = 32;  // runs per column
 
+// Chunks per item of the chained forward walk (one stage and one TMA box
+// per array): two for 2-byte elements (a box row of 32 channels is then 128
+// bytes), one for 4-byte ones.
+__host__ __device__ constexpr int chain_chunks(size_t elem_bytes) { return elem_bytes == 2 ? 2 : 1; }
+
 struct SeqFwdArgs {
-  CUtensorMap tk, tv;  // box {32, kChunk, 1} (when use_tma)
+  CUtensorMap tk, tv;    // box {32, kChunk, 1} (when use_tma)
+  CUtensorMap tk2, tv2;  // box {32, chain_chunks(element size) * kChunk, 1}: the chained walk's items
   const float* w;
   const float* u;
   const void* k;

@@ -555,10 +555,21 @@ __device__ __forceinline__ void seq_fwd_run(const SeqFwdArgs& a, const Launch& L
 // which its warp reaches before any later run of its own, and every warp is
 // resident (cooperative launch), so the waits always end.  The last run
 // publishes nothing and needs no phase 1.
+//
+// The walk moves in items of chain_chunks(sizeof(KV)) chunks: one stage, one
+// TMA box per array and one wait per item.  With bf16 inputs an item is two
+// chunks, so a box row is 128 bytes (64 tokens x 32 channels) and the
+// per-item work of the pipeline (waits, copies issued, bookkeeping) is paid
+// once per 64 tokens.  The last item of a run's phase holds the run's last
+// chunk alone when the run has an odd length (its box then also carries the
+// next chunk, unused).  Each chunk is computed exactly as with one-chunk
+// items, so the results do not depend on the item size.
 template <typename KV, int NS, int YM>
 __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch& L, unsigned char* smem) {
-  KV* ring = reinterpret_cast<KV*>(smem);  // stage s: k at 2s*kSeqTile, v at (2s+1)*kSeqTile
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + seq_ring_elems<KV, NS>(2) * sizeof(KV));
+  constexpr int CP = chain_chunks(sizeof(KV));  // chunks per item
+  constexpr int kBox = CP * kSeqTile;           // elements of one array's box
+  KV* ring = reinterpret_cast<KV*>(smem);       // stage s: k at 2s*kBox, v at (2s+1)*kBox
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * 2 * kBox * sizeof(KV));
   const int lane = threadIdx.x;
   const ScanGeometry& g = a.g;
   const int W = a.nseg, len = a.chain;
@@ -568,57 +579,61 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
   const float w = __ldg(a.w + col.cc), u = __ldg(a.u + col.cc);
   const float ew = expf(-w), eu = expf(u);
   const bool tma = a.use_tma != 0;
-  constexpr uint32_t kStageBytes = 2 * kSeqTile * sizeof(KV);
+  constexpr uint32_t kStageBytes = 2 * kBox * sizeof(KV);
   const size_t rec0 = (size_t)col.b * g.C + col.cc;  // + run * B * C
   const size_t jstride = (size_t)g.B * g.C;
 
-  // The warp's item stream: per run, its chunks (phase 1) then the same
-  // chunks again (phase 2); the last run of the column has phase 2 only.
-  // Items per run: 2 len, except the last run (the warp's last).
+  // The warp's item stream: per run, its items (phase 1) then the same items
+  // again (phase 2); the last run of the column has phase 2 only.  Items
+  // per phase: ip for a full run, il for the last one.
   const int last_len = g.nchunks - (R - 1) * len;
+  const int ip = (len + CP - 1) / CP, il = (last_len + CP - 1) / CP;
   int nitems = 0;
-  for (int r = wi; r < R; r += W) nitems += r == R - 1 ? last_len : 2 * len;
+  for (int r = wi; r < R; r += W) nitems += r == R - 1 ? il : 2 * ip;
   // A position in the warp's item stream: m-th run of the warp, item off of
   // that run; advanced one item at a time (no division per item).
   struct Cur {
     int m, off;
   };
   auto advance = [&](Cur& c) {
-    const int n = wi + c.m * W == R - 1 ? last_len : 2 * len;
+    const int n = wi + c.m * W == R - 1 ? il : 2 * ip;
     if (++c.off == n) {
       c.off = 0;
       ++c.m;
     }
   };
   struct Item {
-    int r, j;
+    int r, j, nc;           // run; first chunk; chunks of the run in the item
     bool p1, first, last;  // phase 1 item; first / last item of its phase
   };
   auto item = [&](const Cur& c) {
     Item o;
-    const int off = c.off;
     o.r = wi + c.m * W;
+    int k, rl, np;  // item of the phase; chunks in the run; items in the phase
     if (o.r == R - 1) {
       o.p1 = false;
-      o.j = o.r * len + off;
-      o.first = off == 0;
-      o.last = off == last_len - 1;
+      k = c.off;
+      rl = last_len;
+      np = il;
     } else {
-      o.p1 = off < len;
-      const int k = o.p1 ? off : off - len;
-      o.j = o.r * len + k;
-      o.first = k == 0;
-      o.last = k == len - 1;
+      o.p1 = c.off < ip;
+      k = o.p1 ? c.off : c.off - ip;
+      rl = len;
+      np = ip;
     }
+    o.j = o.r * len + k * CP;
+    o.nc = min(CP, rl - k * CP);
+    o.first = k == 0;
+    o.last = k == np - 1;
     return o;
   };
   auto issue = [&](int it, const Cur& c) {  // lane 0: item it (at c) into its stage
     const int s = it % NS;
     const int j = item(c).j;
-    KV* dk = ring + (size_t)(2 * s) * kSeqTile;
+    KV* dk = ring + (size_t)(2 * s) * kBox;
     mbar_arrive_expect_tx(&full[s], kStageBytes);
-    tma_load_3d(dk, &a.tk, &full[s], col.c0, j * kChunk, col.b);
-    tma_load_3d(dk + kSeqTile, &a.tv, &full[s], col.c0, j * kChunk, col.b);
+    tma_load_3d(dk, &a.tk2, &full[s], col.c0, j * kChunk, col.b);
+    tma_load_3d(dk + kBox, &a.tv2, &full[s], col.c0, j * kChunk, col.b);
   };
   int issued = 0;
   Cur ahead{0, 0};  // the next item to stage
@@ -626,8 +641,8 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
     if (lane == 0) {
       for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
       mbar_init_fence();
-      tma_prefetch_desc(&a.tk);
-      tma_prefetch_desc(&a.tv);
+      tma_prefetch_desc(&a.tk2);
+      tma_prefetch_desc(&a.tv2);
     }
     for (int it = 0; it < NS && it < nitems; ++it) {
       if (lane == 0) issue(it, ahead);
@@ -657,36 +672,44 @@ __device__ __forceinline__ void seq_fwd_chain(const SeqFwdArgs& a, const Launch&
   for (int it = 0; it < nitems; ++it, advance(cur)) {
     const Item m = item(cur);
     const int s = it % NS;
-    KV* dk = ring + (size_t)(2 * s) * kSeqTile;
+    KV* dk = ring + (size_t)(2 * s) * kBox;
     if (tma) {
       if (!stage_wait(&full[s], (uint32_t)((it / NS) & 1), a.budget_ns)) return fail(it);
     } else {
-      copy_box_plain(dk, static_cast<const KV*>(a.k), g, col, m.j * kChunk);
-      copy_box_plain(dk + kSeqTile, static_cast<const KV*>(a.v), g, col, m.j * kChunk);
+      for (int h = 0; h < m.nc; ++h) {
+        copy_box_plain(dk + h * kSeqTile, static_cast<const KV*>(a.k), g, col, (m.j + h) * kChunk);
+        copy_box_plain(dk + kBox + h * kSeqTile, static_cast<const KV*>(a.v), g, col, (m.j + h) * kChunk);
+      }
       __syncwarp();
     }
-    const int n = min(kChunk, g.T - m.j * kChunk);
-    if (m.p1) {
-      if (m.first) S = empty_state();
-      if (n == kChunk)
-        seq_fwd_summary<true, KV>(dk + lane, dk + kSeqTile + lane, n, w, S);
-      else
-        seq_fwd_summary<false, KV>(dk + lane, dk + kSeqTile + lane, n, w, S);
-    } else {
-      if (m.first && m.r == R - 1 && !carry_in(m.r, P)) return fail(it);
-      const int64_t row = ((int64_t)col.b * g.T + (int64_t)m.j * kChunk) * g.C + col.c;
-      float* yp = YM != kYNone ? a.y + row : nullptr;
-      const KV* rp = YM == kYGated ? static_cast<const KV*>(a.r) + row : nullptr;
-      if (n == kChunk)
-        seq_fwd_full<KV, YM>(dk + lane, dk + kSeqTile + lane, w, u, ew, eu, P, yp, rp, g.C, col.valid);
-      else
-        seq_fwd_chunk<KV, YM>(dk + lane, dk + kSeqTile + lane, n, w, u, ew, eu, P, yp, rp, g.C, col.valid);
-      if (col.valid) {
-        const size_t o = (size_t)m.j * jstride + rec0;
-        a.ckpt[o] = P.num;
-        a.ckpt[o + g.plane] = P.den;
-        a.ckpt[o + 2 * g.plane] = P.pp;
-        if (m.j == g.nchunks - 1 && a.state_out) store_state_planes(a.state_out, jstride, rec0, P);
+    if (m.p1 && m.first) S = empty_state();
+    if (!m.p1 && m.first && m.r == R - 1 && !carry_in(m.r, P)) return fail(it);
+#pragma unroll 1
+    for (int h = 0; h < m.nc; ++h) {
+      const int j = m.j + h;
+      const KV* sk = dk + h * kSeqTile + lane;
+      const KV* sv = dk + kBox + h * kSeqTile + lane;
+      const int n = min(kChunk, g.T - j * kChunk);
+      if (m.p1) {
+        if (n == kChunk)
+          seq_fwd_summary<true, KV>(sk, sv, n, w, S);
+        else
+          seq_fwd_summary<false, KV>(sk, sv, n, w, S);
+      } else {
+        const int64_t row = ((int64_t)col.b * g.T + (int64_t)j * kChunk) * g.C + col.c;
+        float* yp = YM != kYNone ? a.y + row : nullptr;
+        const KV* rp = YM == kYGated ? static_cast<const KV*>(a.r) + row : nullptr;
+        if (n == kChunk)
+          seq_fwd_full<KV, YM>(sk, sv, w, u, ew, eu, P, yp, rp, g.C, col.valid);
+        else
+          seq_fwd_chunk<KV, YM>(sk, sv, n, w, u, ew, eu, P, yp, rp, g.C, col.valid);
+        if (col.valid) {
+          const size_t o = (size_t)j * jstride + rec0;
+          a.ckpt[o] = P.num;
+          a.ckpt[o + g.plane] = P.den;
+          a.ckpt[o + 2 * g.plane] = P.pp;
+          if (j == g.nchunks - 1 && a.state_out) store_state_planes(a.state_out, jstride, rec0, P);
+        }
       }
     }
     // release the stage (only read: see seq_fwd_run)
@@ -1300,13 +1323,15 @@ cudaError_t launch_planned(const DevInfo& d, Args& a, int arrays, size_t elem, s
     forced = a.chain;
     chained = forced > 0 || ((long long)cols < d.sms && (double)input_bytes > 0.6 * (double)d.l2);
     // Chained runs take the caller's warps per SM too: on the long-context
-    // forward (B=1 T=131072 C=2560 bf16) 12 per SM give 22 runs per column
-    // of 6 chunks at 4 stages, 0.59-0.60 ms; 29 runs of 5 (16 per SM) took
-    // 0.65 ms, 23 or 24 runs 0.77-0.85 ms, 20 runs 0.66 ms (one GPU call).
+    // forward (B=1 T=131072 C=2560 bf16) 12 per SM give 22 runs per column;
+    // 29 runs (16 per SM) were 8% slower, 23 or 24 runs 30-40%, 20 runs 10%
+    // (one GPU call, one-chunk items).
   }
+  // a stage of the chained walk holds chain_chunks(elem) chunks
+  const size_t cstage = chained ? stage * chain_chunks(elem) : stage;
   // resident CTAs per SM of the kernel that will run, at two stages
   int per_sm2 = 0;
-  cudaError_t e = chained ? resident_per_sm<Args, KernChain<2>::fn>(2 * stage + 128, per_sm2)
+  cudaError_t e = chained ? resident_per_sm<Args, KernChain<2>::fn>(2 * cstage + 128, per_sm2)
                           : resident_per_sm<Args, Kern<2>::fn>(2 * stage + 128, per_sm2);
   if (e != cudaSuccess) return e;
   a.nseg = choose_runs(d, a.g, per_sm2, input_bytes, warps, chained);
@@ -1314,13 +1339,15 @@ cudaError_t launch_planned(const DevInfo& d, Args& a, int arrays, size_t elem, s
   if constexpr (std::is_same<Args, SeqFwdArgs>::value) {
     a.chain = 0;
     if (chained) {
-      // runs of `len` chunks, the runs in flight (nseg per column) within 40%
+      // runs of `len` chunks, the runs in flight (nseg per column) within 35%
       // of L2 (longer runs fall out of L2 before phase 2; shorter ones make
-      // the chain of carried states the bound)
+      // the chain of carried states the bound).  Long-context forward, 22
+      // runs per column: 0.57 ms at 6 chunks (42 MB in flight), 0.60 at 5,
+      // 0.65 at 4, 0.68 at 8.
       long long len = forced;
       if (len <= 0) {
         const double per_run_chunk = (double)cols * a.nseg * stage;  // one chunk of every run in flight
-        len = (long long)(0.4 * (double)d.l2 / per_run_chunk);
+        len = (long long)(0.35 * (double)d.l2 / per_run_chunk);
         if (len < 4) len = 4;
         if (len > 64) len = 64;
       }
@@ -1331,7 +1358,7 @@ cudaError_t launch_planned(const DevInfo& d, Args& a, int arrays, size_t elem, s
   }
   const unsigned int nblk = cols * (unsigned int)a.nseg;
   const bool coop = a.nseg > 1;  // runs wait on each other
-  if (chained) return launch_staged<Args, KernChain>(d, a, nblk, stage, coop, s);
+  if (chained) return launch_staged<Args, KernChain>(d, a, nblk, cstage, coop, s);
   return launch_staged<Args, Kern>(d, a, nblk, stage, coop, s);
 }
 
