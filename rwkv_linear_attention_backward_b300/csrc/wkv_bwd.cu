@@ -507,10 +507,11 @@ __global__ void __launch_bounds__(kPipeThreads, 2) bwd_scan_kernel(const __grid_
 // gw[c] = sum over the partial rows of part[0][.][c], gu likewise from
 // part[1].  Block (g, sl) of 8 warps sums the rows of slice sl for the 32
 // channels of group g: warp q takes rows q, q+8, ... with compensated
-// (Kahan) summation, then the 8 warp sums are added in order.  The last
-// block of a group to finish (counted on a launch-tagged counter) adds the
-// slice sums in slice order.  Every
-// order is fixed by the shape, so the result is deterministic.
+// (Kahan) summation, then the 8 warp sums are added in order.  With one
+// slice those sums are gw, gu; with several, the last block of a group to
+// finish (counted on a launch-tagged counter) adds the slice sums in slice
+// order.  Every order is fixed by the shape, so the result is
+// deterministic.
 __global__ void __launch_bounds__(256) reduce_kernel(const ReduceArgs a) {
   __shared__ float sw[8][32], su[8][32];
   __shared__ bool last;
@@ -526,6 +527,7 @@ __global__ void __launch_bounds__(256) reduce_kernel(const ReduceArgs a) {
   float s1 = 0.f, k1 = 0.f, s2 = 0.f, k2 = 0.f;
   if (c < a.C) {
     const size_t P = (size_t)a.rows * a.C;
+#pragma unroll 4
     for (int r = r0 + q; r < r1; r += 8) {
       const size_t o = (size_t)r * a.C + c;
       const float y1 = a.part[o] - k1;
@@ -547,6 +549,13 @@ __global__ void __launch_bounds__(256) reduce_kernel(const ReduceArgs a) {
     for (int i = 0; i < 8; ++i) {
       t1 += sw[i][lane];
       t2 += su[i][lane];
+    }
+    if (a.nslice == 1) {  // the whole sum: no slices to combine
+      if (c < a.C) {
+        a.gw[c] = t1;
+        a.gu[c] = t2;
+      }
+      return;
     }
     if (c < a.C) {
       a.slices[((size_t)sl * 2) * a.C + c] = t1;
@@ -588,6 +597,9 @@ __global__ void __launch_bounds__(256) reduce_kernel(const ReduceArgs a) {
 }  // namespace
 
 int reduce_slices(int rows, int C) {
+  // up to 64 rows one block per channel group sums them all (8 rows a warp
+  // at most): a second pass over slices would cost more than it spreads
+  if (rows <= 64) return 1;
   const int groups = (C + 31) / 32;
   int ns = (rows + 31) / 32;
   int cap = 2 * 148 / groups;
