@@ -15,13 +15,17 @@ decode step of L=32 layers, B=256, C=4096, fp32 / bf16 token inputs, state
 carried across steps), and the pointwise neighbours ``shift``, ``cmix``,
 ``l169m_bf16``, ``l169m_gated``.
 
-Timing: W untimed warm-up steps; then the forward and the backward call are
-captured once as CUDA graphs (as a training loop would run them; ``--no-graph``
-calls the API every step instead) and K steps replay them.  L2 is flushed (a
-write of twice its size) before every timed step, outside the step's CUDA-event pair;
-the value is the elements of all ranks over the max over ranks of the summed
-per-step device times.  The dominant kernel's launches are timed with their
-own events on the launching stream for the roofline entry.  SM clocks and
+Timing: W untimed warm-up steps; then the step (the forward call, then the
+backward call) is captured once as a CUDA graph (as a training loop would run
+it; ``--no-graph`` calls the API every step instead) and K steps replay it.
+L2 is flushed before every timed step, outside the step's CUDA-event pair: a
+write of twice its size, then a read of another buffer of twice its size, so
+that the lines the write left dirty are written back before the step and not
+during it.  The value is the elements of all ranks over the max over ranks of
+the summed per-step device times.  For the roofline entry the dominant call
+is timed in K more steps, the forward and backward calls replayed as graphs
+of their own with CUDA events around the dominant one on the launching
+stream.  SM clocks and
 clock-event reasons are sampled (NVML, else nvidia-smi) during the timed steps.
 
 ``--impl reference`` times the float64 CPU oracle (oracle/) on this
@@ -366,14 +370,22 @@ class TrainingRun:
         with torch.cuda.graph(self.g_fwd):
             self._forward()
         self.g_bwd = None
+        self.g_step = self.g_fwd
         if self.wl.backward:
             self.g_bwd = torch.cuda.CUDAGraph()
             with torch.cuda.graph(self.g_bwd):
+                self._backward()
+            self.g_step = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.g_step):
+                self._forward()
                 self._backward()
         torch.cuda.synchronize()
 
     def step(self, ev=None):
         graphs = getattr(self, "g_fwd", None) is not None
+        if graphs and ev is None:
+            self.g_step.replay()  # the whole step as one graph
+            return
         self.g_fwd.replay() if graphs else self._forward()
         if self.wl.backward:
             if ev is not None:
@@ -612,15 +624,18 @@ class CmixRun:
 
 def time_steps(run, steps: int, flush, stream):
     """Per-step device times (s) of `steps` steps, L2 flushed before each;
-    also the dominant call's per-launch times."""
+    then, in `steps` more steps, the dominant call's per-launch times."""
     torch = run.torch
     ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     ev_dom = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for i in range(steps):
         flush()
         ev_step[i][0].record(stream)
-        run.step_dominant_events(ev_dom[i])
+        run.step()
         ev_step[i][1].record(stream)
+    for i in range(steps):
+        flush()
+        run.step_dominant_events(ev_dom[i])
     torch.cuda.synchronize()
     step_s = [a.elapsed_time(b) / 1e3 for a, b in ev_step]
     dom_s = [a.elapsed_time(b) / 1e3 for a, b in ev_dom]
@@ -780,7 +795,15 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     scratch = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
-    flush = lambda: scratch.fill_(1.0)  # noqa: E731  (a write larger than L2)
+    evict = torch.ones_like(scratch)
+    evict_sum = torch.empty((), dtype=torch.float32, device=device)
+
+    def flush():
+        # a write larger than L2, then a read of as much other memory: the
+        # read evicts the lines the write left dirty (their write-back happens
+        # here, not in the step) and leaves L2 holding none of the step's data
+        scratch.fill_(1.0)
+        torch.sum(evict, dim=0, out=evict_sum)
 
     for _ in range(args.warmup):
         flush()
@@ -831,8 +854,9 @@ def run_ours(args):
             wl_cfg["output"] = "sigmoid(r) * wkv, the gate fused into the forward and backward kernels"
     pointwise = DECODE_WORKLOADS + ("shift", "cmix")
     wl_cfg.update({"launch": "api calls per step" if (args.no_graph or args.workload in pointwise) else
-                   "CUDA graphs of the forward and backward calls, captured once and replayed per step",
-                   "l2": "flushed before every timed step (write of 2x L2)", "parallelism": f"replicas x{world}",
+                   "one CUDA graph of the step's calls, captured once and replayed per step",
+                   "l2": "flushed before every timed step (write of 2x L2, then a read of another 2x L2 buffer)",
+                   "parallelism": f"replicas x{world}",
                    "scan_mode": args.scan_mode,
                    "strategy": getattr(run, "strategy", "n/a"),
                    "checkpoints": "forward writes chunk checkpoints, backward reads them"
