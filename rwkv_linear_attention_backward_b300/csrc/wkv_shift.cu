@@ -99,12 +99,16 @@ __device__ __forceinline__ void kahan(float& s, float& k, float x) {
   s = t;
 }
 
-// Backward: block (channel group of 32 V channels, row slice); warp y takes
-// rows slice_start + y, + 8, ... (every row's loads independent of the other
-// rows', so a warp keeps them all in flight).  gmu partials of the slice go
-// to part[slice][3][C], reduced over the 8 warps in order.
+// Backward: block (channel group of 32 V channels, row slice); the slice's
+// rows are cut into 8 contiguous ranges, one per warp, and a warp walks its
+// range from the last row to the first.  Walking down, the mix gradients of
+// row t+1 (the "next" terms of row t) are the ones loaded one step before,
+// and the x_{t-1} loaded for row t is the x_t of the next step, so a row
+// costs four loads (gxk, gxv, gxr and x_{t-1}) instead of eight.  gmu
+// partials of the slice go to part[slice][3][C], the 8 warps' sums added in
+// warp order.
 template <int V>
-__global__ void __launch_bounds__(256, 3) shift_bwd_kernel(const ShiftArgs a) {
+__global__ void __launch_bounds__(256, 2) shift_bwd_kernel(const ShiftArgs a) {
   using W = Vec<V>;
   using VT = typename W::T;
   __shared__ float red[8][3][32 * V];
@@ -114,21 +118,28 @@ __global__ void __launch_bounds__(256, 3) shift_bwd_kernel(const ShiftArgs a) {
   const int64_t rows = (int64_t)a.B * a.T;
   const int64_t per = (rows + a.nslice - 1) / a.nslice;
   const int64_t r0 = (int64_t)blockIdx.y * per, r1 = r0 + per < rows ? r0 + per : rows;
+  const int64_t pw = r1 > r0 ? (r1 - r0 + 7) / 8 : 0;  // rows per warp
+  const int64_t w0 = r0 + wy * pw, w1 = w0 + pw < r1 ? w0 + pw : r1;
   float sk[V], kk[V], sv[V], kv[V], sr[V], kr[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) sk[i] = kk[i] = sv[i] = kv[i] = sr[i] = kr[i] = 0.f;
-  if (valid) {
+  if (valid && w0 < w1) {
     const VT mk = W::load(a.mu_k + c), mv = W::load(a.mu_v + c), mr = W::load(a.mu_r + c);
-    for (int64_t row = r0 + wy; row < r1; row += 8) {
-      const int b = (int)(row / a.T);
-      const int t = (int)(row - (int64_t)b * a.T);
+    int64_t row = w1 - 1;
+    int b = (int)(row / a.T);
+    int t = (int)(row - (int64_t)b * a.T);
+    // the row after the range (none past the end of a sequence)
+    VT nk = W::zero(), nv = W::zero(), nr = W::zero();
+    if (t + 1 < a.T) {
+      const int64_t o = (row + 1) * a.C + c;
+      nk = W::load(a.gxk + o);
+      nv = W::load(a.gxv + o);
+      nr = W::load(a.gxr + o);
+    }
+    VT cur = W::load(a.x + row * a.C + c);
+    for (; row >= w0; --row) {
       const int64_t o = row * a.C + c;
       const VT gk = W::load(a.gxk + o), gv = W::load(a.gxv + o), gr = W::load(a.gxr + o);
-      const bool has_next = t + 1 < a.T;
-      const VT nk = has_next ? W::load(a.gxk + o + a.C) : W::zero();
-      const VT nv = has_next ? W::load(a.gxv + o + a.C) : W::zero();
-      const VT nr = has_next ? W::load(a.gxr + o + a.C) : W::zero();
-      const VT cur = W::load(a.x + o);
       VT prev;
       if (t > 0) prev = W::load(a.x + o - a.C);
       else prev = a.x0 ? W::load(a.x0 + (int64_t)b * a.C + c) : W::zero();
@@ -150,6 +161,21 @@ __global__ void __launch_bounds__(256, 3) shift_bwd_kernel(const ShiftArgs a) {
       }
       W::store(a.gx + o, g);
       if (t == 0 && a.gx0) W::store(a.gx0 + (int64_t)b * a.C + c, g0);
+      // one row down: this row's mix gradients are the next terms of the
+      // row below, and its x_{t-1} is that row's x_t; below a sequence's
+      // first row lies the previous sequence's last row (no next terms)
+      if (t > 0) {
+        nk = gk;
+        nv = gv;
+        nr = gr;
+        cur = prev;
+        --t;
+      } else {
+        nk = nv = nr = W::zero();
+        t = a.T - 1;
+        --b;
+        if (row > w0) cur = W::load(a.x + (row - 1) * a.C + c);
+      }
     }
   }
 #pragma unroll
@@ -207,7 +233,7 @@ int shift_slices(int B, int T, int C, bool vec4) {
   const int per_group = vec4 ? 128 : 32;
   const int groups = (C + per_group - 1) / per_group;
   const int64_t rows = (int64_t)B * T;
-  int64_t ns = (2 * 148 + groups - 1) / groups;  // about two CTAs per SM
+  int64_t ns = (2 * 148) / groups;  // two CTAs per SM at most: one wave
   if (ns > (rows + 7) / 8) ns = (rows + 7) / 8;
   if (ns < 1) ns = 1;
   return (int)ns;
