@@ -409,24 +409,38 @@ class TrainingRun:
 
     # end to end through the public API with host buffers
     def e2e_setup(self):
+        """Pinned host buffers and two device slots of inputs and outputs
+        (slot 0: the timed run's own buffers)."""
         torch = self.torch
         self.pin_in = tuple(t.pin_memory() for t in self.host)
-        self.pin_out = tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in self._outputs())
+        self._slots = [(self.dev, tuple(self._outputs()))]
+        self._slots.append((tuple(torch.empty_like(t) for t in self.dev),
+                            tuple(torch.empty_like(t) for t in self._outputs())))
+        self.pin_out = [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in self._outputs())
+                        for _ in range(2)]
         self.h2d = sum(t.numel() * t.element_size() for t in self.pin_in)
-        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out[0])
 
     def _outputs(self):
         grads = [self.gk, self.gv, self.gw, self.gu] + ([self.gr] if self.wl.gated else [])
         return [self.y] + (grads if self.wl.backward else [])
 
-    def e2e_step(self):
-        for d, h in zip(self.dev, self.pin_in):
-            d.copy_(h, non_blocking=True)
+    def e2e_inputs(self, k):
+        return self._slots[k][0]
+
+    def e2e_compute(self, k):
+        """The step's calls on slot k's inputs into slot k's outputs."""
+        dev, outs = self._slots[k]
+        self.dev = dev
+        self.y = outs[0]
+        if self.wl.backward:
+            self.gk, self.gv, self.gw, self.gu = outs[1:5]
+            if self.wl.gated:
+                self.gr = outs[5]
         self._forward()
         if self.wl.backward:
             self._backward()
-        for h, d in zip(self.pin_out, self._outputs()):
-            h.copy_(d, non_blocking=True)
+        return outs
 
 
 class DecodeRun:
@@ -472,19 +486,20 @@ class DecodeRun:
     def e2e_setup(self):
         torch = self.torch
         self.pin_in = tuple(t.to("cpu").pin_memory() for t in self.pool[0])
-        self.pin_out = (torch.empty(self.out[0].shape, pin_memory=True),)
+        self._slots = [(self.pool[0], self.out[0]), (self.pool[1], torch.empty_like(self.out[0]))]
+        self.pin_out = [(torch.empty(self.out[0].shape, pin_memory=True),) for _ in range(2)]
         self.h2d = sum(t.numel() * t.element_size() for t in self.pin_in)
-        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out[0])
 
-    def e2e_step(self):
-        bufs = self.pool[0]
-        for d, h in zip(bufs, self.pin_in):
-            d.copy_(h, non_blocking=True)
-        x, xp, r, k, v = bufs
+    def e2e_inputs(self, k):
+        return self._slots[k][0]
+
+    def e2e_compute(self, k):
+        (x, xp, r, kk, v), y = self._slots[k]
         mk, mv, mr, w, u = self.params
-        y, xk, xv, xr = self.out
-        self.wkv.decode_step(x, xp, mk, mv, mr, r, k, v, w, u, *self.state, y=y, xk=xk, xv=xv, xr=xr)
-        self.pin_out[0].copy_(y, non_blocking=True)
+        _, xk, xv, xr = self.out
+        self.wkv.decode_step(x, xp, mk, mv, mr, r, kk, v, w, u, *self.state, y=y, xk=xk, xv=xv, xr=xr)
+        return (y,)
 
 
 class ShiftRun:
@@ -536,17 +551,21 @@ class ShiftRun:
     def e2e_setup(self):
         torch = self.torch
         self.pin_in = tuple(t.pin_memory() for t in self.host)
-        self.pin_out = tuple(torch.empty(self.S.B, self.S.T, self.S.C, pin_memory=True) for _ in range(4))
+        self._slots = [(self.dev, self.out), (tuple(torch.empty_like(t) for t in self.dev),
+                                              tuple(torch.empty_like(t) for t in self.out))]
+        self.pin_out = [tuple(torch.empty(self.S.B, self.S.T, self.S.C, pin_memory=True) for _ in range(4))
+                        for _ in range(2)]
         self.h2d = sum(t.numel() * t.element_size() for t in self.pin_in)
-        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out[0])
 
-    def e2e_step(self):
-        for d, h in zip(self.dev, self.pin_in):
-            d.copy_(h, non_blocking=True)
+    def e2e_inputs(self, k):
+        return self._slots[k][0]
+
+    def e2e_compute(self, k):
+        self.dev, self.out = self._slots[k]
         self._forward()
-        gx = self._backward()[0]
-        for h, d in zip(self.pin_out, self.out + (gx,)):
-            h.copy_(d, non_blocking=True)
+        gx = self._backward()[0]  # allocated by the call: the copy-out stream marks its use
+        return self.out + (gx,)
 
 
 # --------------------------------------------------------------- ours: run
@@ -608,18 +627,21 @@ class CmixRun:
     def e2e_setup(self):
         torch = self.torch
         self.pin_in = tuple(t.pin_memory() for t in self.host)
-        self.pin_out = tuple(torch.empty(t.shape, pin_memory=True) for t in self.out)
+        self._slots = [(self.dev, self.out), (tuple(torch.empty_like(t) for t in self.dev),
+                                              tuple(torch.empty_like(t) for t in self.out))]
+        self.pin_out = [tuple(torch.empty(t.shape, pin_memory=True) for t in self.out) for _ in range(2)]
         self.h2d = sum(t.numel() * t.element_size() for t in self.pin_in)
-        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.pin_out[0])
 
-    def e2e_step(self):
-        for d, h in zip(self.dev, self.pin_in):
-            d.copy_(h, non_blocking=True)
+    def e2e_inputs(self, k):
+        return self._slots[k][0]
+
+    def e2e_compute(self, k):
+        self.dev, self.out = self._slots[k]
         self._forward()
         self._gate_backward()
         self._sqrelu_backward()
-        for h, d in zip(self.pin_out, self.out):
-            h.copy_(d, non_blocking=True)
+        return self.out
 
 
 def time_steps(run, steps: int, flush, stream):
@@ -911,22 +933,59 @@ def run_ours(args):
 
 def e2e(run, steps: int):
     """Same metric through the public API with pinned host buffers: every
-    step copies its inputs host->device, runs the step, copies the results
-    device->host."""
+    step copies its inputs host->device, runs the step's calls and copies
+    its results device->host.  Steps are pipelined as a training loop's
+    data path would be: copies in on one stream, the calls on a second,
+    copies out on a third, over two slots of device buffers, so step i+1's
+    inputs and step i-1's results cross the host link (both directions at
+    once) while step i computes.  The time is the whole sequence's, from the
+    first copy in to the last copy out."""
     torch = run.torch
     run.e2e_setup()
-    for _ in range(2):
-        run.e2e_step()
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def issue(i):
+        k = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_comp[k])  # step i-2 has read slot k's inputs
+            for d, h in zip(run.e2e_inputs(k), run.pin_in):
+                d.copy_(h, non_blocking=True)
+            ev_in[k].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev_in[k])
+            if i >= 2:
+                s_comp.wait_event(ev_out[k])  # step i-2's results have left slot k
+            outs = run.e2e_compute(k)
+            ev_comp[k].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[k])
+            for h, d in zip(run.pin_out[k], outs):
+                d.record_stream(s_out)
+                h.copy_(d, non_blocking=True)
+            ev_out[k].record(s_out)
+
+    def sequence(n):
+        for i in range(n):
+            issue(i)
+        cur = torch.cuda.current_stream()
+        for e in ev_out[:min(n, 2)]:
+            cur.wait_event(e)
+
+    sequence(2)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        run.e2e_step()
+    a.record(s_in)
+    sequence(steps)
     b.record()
     torch.cuda.synchronize()
     dt = a.elapsed_time(b) / 1e3
     return {"value": run.elements * steps / dt, "unit": "elements/s", "h2d_bytes_per_step": run.h2d,
-            "d2h_bytes_per_step": run.d2h, "steps": steps}
+            "d2h_bytes_per_step": run.d2h, "steps": steps,
+            "pipeline": "copies in, calls and copies out on three streams over two buffer slots"}
 
 
 # -------------------------------------------------------------- reference
