@@ -136,9 +136,58 @@ def aggregate(per_rank_seconds: float, units_per_rank: float, world: int, device
 
 
 # ----------------------------------------------------------------- clocks
+class CtypesNvml:
+    """The few read-only NVML calls the clock sampler makes, through ctypes
+    on the driver's libnvidia-ml.so.1: for hosts where the pynvml module is
+    not installed.  `lib` stands in for the library in host tests."""
+
+    NVML_CLOCK_SM = 1  # nvmlClockType_t: the SM clock domain
+
+    def __init__(self, lib=None):
+        import ctypes
+
+        self._c = ctypes
+        self.lib = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+        self._check(self.lib.nvmlInit_v2(), "nvmlInit_v2")
+
+    @staticmethod
+    def _check(status, what):
+        if status != 0:
+            raise RuntimeError(f"{what} returned NVML status {status}")
+
+    def nvmlInit(self):
+        pass  # initialised in the constructor
+
+    def nvmlDeviceGetHandleByIndex(self, index):
+        h = self._c.c_void_p()
+        self._check(self.lib.nvmlDeviceGetHandleByIndex_v2(self._c.c_uint(index), self._c.byref(h)),
+                    "nvmlDeviceGetHandleByIndex_v2")
+        return h
+
+    def _clock(self, fn, name, h, domain):
+        v = self._c.c_uint()
+        self._check(fn(h, self._c.c_int(domain), self._c.byref(v)), name)
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, h, domain):
+        return self._clock(self.lib.nvmlDeviceGetClockInfo, "nvmlDeviceGetClockInfo", h, domain)
+
+    def nvmlDeviceGetMaxClockInfo(self, h, domain):
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo, "nvmlDeviceGetMaxClockInfo", h, domain)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        if fn is None:  # the older name of the same call
+            fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        v = self._c.c_ulonglong()
+        self._check(fn(h, self._c.byref(v)), "nvmlDeviceGetCurrentClocksEventReasons")
+        return v.value
+
+
 class ClockSampler:
     """Samples the SM clock and clock-event reasons during a timed region
-    (read only): through NVML when pynvml imports, else by running
+    (read only): through NVML (the pynvml module, else the driver's NVML
+    library through ctypes) every 2 ms, else by running
     ``nvidia-smi --query-gpu=... -lms 10`` and reading its output."""
 
     NAMES = {
@@ -161,17 +210,23 @@ class ClockSampler:
         self._stop = threading.Event()
         self._thread = None
         self._proc = None
-        try:
-            import pynvml
+        self.nv = None
+        errors = []
+        for source in ("nvml", "nvml (ctypes)"):
+            try:
+                if source == "nvml":
+                    import pynvml as nv
 
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.source = "nvml"
-        except Exception as e:
-            self.nv = None
-            self.error = f"pynvml: {e}"
+                    nv.nvmlInit()
+                else:
+                    nv = CtypesNvml()
+                self.h = nv.nvmlDeviceGetHandleByIndex(index)
+                self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
+                self.nv, self.source = nv, source
+                break
+            except Exception as e:
+                errors.append(f"{source}: {e}")
+        self.error = "; ".join(errors) or None
 
     def _run_nvml(self):
         nv = self.nv
@@ -245,8 +300,8 @@ class ClockSampler:
         reasons = sorted(self.reasons - {"gpu_idle"})
         out = {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": reasons,
                "samples": len(self.samples), "source": self.source}
-        if self.source != "nvml" and self.error:
-            out["nvml_error"] = self.error[:120]
+        if self.source == "nvidia-smi" and self.error:
+            out["nvml_error"] = self.error[:160]
         return out
 
     def rejected(self) -> bool:

@@ -87,3 +87,48 @@ def test_smi_lines_are_read():
     assert s.samples == [2032.0, 1800.0, 1700.0]
     assert {"sw_power_cap", "hw_slowdown"} <= s.reasons
     assert s.rejected()
+
+
+def test_ctypes_nvml_reads_through_the_library_calls():
+    """The ctypes NVML binding (hosts without pynvml) passes the SM clock
+    domain, returns what the library writes, takes the older name of the
+    clock-event call when the newer one is missing, and raises on a
+    non-zero status."""
+    calls = []
+
+    class FakeLib:
+        def nvmlInit_v2(self):
+            calls.append("init")
+            return 0
+
+        def nvmlDeviceGetHandleByIndex_v2(self, index, ref):
+            ref._obj.value = 0x1234 + index.value
+            return 0
+
+        def nvmlDeviceGetClockInfo(self, h, domain, ref):
+            assert h.value == 0x1234 and domain.value == 1
+            ref._obj.value = 1965
+            return 0
+
+        def nvmlDeviceGetMaxClockInfo(self, h, domain, ref):
+            ref._obj.value = 2032
+            return 0
+
+        def nvmlDeviceGetCurrentClocksThrottleReasons(self, h, ref):
+            ref._obj.value = 0x4 | 0x8
+            return 0
+
+    nv = bench.CtypesNvml(FakeLib())
+    assert calls == ["init"]
+    h = nv.nvmlDeviceGetHandleByIndex(0)
+    assert nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM) == 1965
+    assert nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM) == 2032
+    assert nv.nvmlDeviceGetCurrentClocksEventReasons(h) == 0xC
+
+    class Failing(FakeLib):
+        def nvmlDeviceGetClockInfo(self, h, domain, ref):
+            return 3
+
+    nv = bench.CtypesNvml(Failing())
+    with pytest.raises(RuntimeError, match="status 3"):
+        nv.nvmlDeviceGetClockInfo(nv.nvmlDeviceGetHandleByIndex(0), nv.NVML_CLOCK_SM)
