@@ -232,7 +232,7 @@ class ClockSampler:
         nv = self.nv
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                self.samples.append(float(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)))
                 mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
                 for bit, name in self.NAMES.items():
                     if mask & bit:
