@@ -970,6 +970,7 @@ def run_ours(args):
             "launch_ms": dom_avg * 1e3,
         },
         "gpu_launches": run.launches_per_step * steps,
+        "gpu_launches_roofline_pass": run.launches_per_step * steps,  # the dominant call's own K steps
         "clocks": clocks.summary(),
     }
     if len(attempts) > 1:
