@@ -6,7 +6,7 @@ import torch
 
 import fp32_emulation as emu
 from checks import check_grads, check_pair_grads, check_pair_y, check_y
-from parity import assert_close, cuda
+from parity import TOL_Y, assert_close, assert_state_close, cuda, to_np
 from rwkv_linear_attention_backward_b300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -187,6 +187,49 @@ def test_chained_runs_do_not_depend_on_the_warps(oracle, wkv, kv_dtype):
         assert torch.equal(y, outs[0][0]), f"y, max runs {runs}"
         assert torch.equal(ck, outs[0][1]), f"checkpoints, max runs {runs}"
     check_y(oracle, w, u, k, v, outs[0][0], f"chained {kv_dtype}")
+
+
+CHAIN_LENS = [1, 2, 4, 7]
+
+
+@pytest.mark.parametrize("kv_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("chain", CHAIN_LENS, ids=[f"len{n}" for n in CHAIN_LENS])
+def test_chained_run_lengths(oracle, wkv, kv_dtype, chain):
+    """Chained runs of 1, 2, 4 and 7 chunks over a ragged sequence (T not a
+    multiple of the chunk), with the column's warps each walking several
+    runs.  With bf16 inputs the walk moves two chunks per item: runs of one
+    chunk make every item a lone chunk, even lengths only full items, odd
+    ones a lone last item per phase.  The outputs, the checkpoints at the
+    first, a middle and the last chunk boundary, and the state after the
+    last token match the oracle."""
+    B, T, C = 2, 32 * 37 + 11, 96
+    w, u, k, v, _ = inputs.training_inputs(B, T, C, seed=31 + chain, k_std=3.0, d_lo=-7.0, d_hi=1.0,
+                                           kv_dtype=kv_dtype)
+    tw = cuda(w, u, k, v)
+    try:
+        wkv.set_scan_mode("sequential")
+        wkv.set_chain_len(chain)
+        wkv.set_max_runs(4)
+        y, ck = wkv.forward(*tw, want_ckpt=True)
+        _, state = wkv.forward_with_state(*tw)
+        torch.cuda.synchronize()
+    finally:
+        wkv.set_scan_mode("auto")
+        wkv.set_chain_len(0)
+        wkv.set_max_runs(0)
+    what = f"chained len {chain} {kv_dtype}"
+    check_y(oracle, w, u, k, v, y, what)
+    nch = -(-T // 32)
+    cks = to_np(ck).reshape(3, nch, B, C)
+    for j in (0, nch // 2, nch - 1):
+        t = min((j + 1) * 32, T)
+        ea, eb = emu.sums_after(w, k, v, [t])[0]
+        assert_state_close(cks[0, j], cks[1, j], cks[2, j], *oracle.state(w, k, v, t), TOL_Y,
+                           f"{what} checkpoint {j}", emu_sums=(ea, eb))
+    st = to_np(state)
+    ea, eb = emu.sums_after(w, k, v, [T])[0]
+    assert_state_close(st[0], st[1], st[2], *oracle.state(w, k, v, T), TOL_Y, f"{what} final state",
+                       emu_sums=(ea, eb))
 
 
 def test_graph_replay_with_new_inputs(wkv, scan_mode):
