@@ -975,8 +975,8 @@ def run_ours(args):
     }
     if len(attempts) > 1:
         out["clocks"]["remeasured"] = True
-    if world == 1 and not args.no_e2e:
-        out["e2e"] = e2e(run, steps=max(3, min(steps, 50)))
+    if not args.no_e2e:
+        out["e2e"] = e2e(run, steps=max(3, min(steps, 50)), world=world, device=device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.workload)
     if rank == 0:
@@ -987,7 +987,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def e2e(run, steps: int):
+def e2e(run, steps: int, world: int = 1, device=None):
     """Same metric through the public API with pinned host buffers: every
     step copies its inputs host->device, runs the step's calls and copies
     its results device->host.  Steps are pipelined as a training loop's
@@ -995,7 +995,9 @@ def e2e(run, steps: int):
     copies out on a third, over two slots of device buffers, so step i+1's
     inputs and step i-1's results cross the host link (both directions at
     once) while step i computes.  The time is the whole sequence's, from the
-    first copy in to the last copy out."""
+    first copy in to the last copy out; with several ranks (each its own
+    GPU and buffers) the value is all ranks' elements over the slowest
+    rank's time."""
     torch = run.torch
     run.e2e_setup()
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
@@ -1033,13 +1035,14 @@ def e2e(run, steps: int):
 
     sequence(2)
     torch.cuda.synchronize()
+    barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(s_in)
     sequence(steps)
     b.record()
     torch.cuda.synchronize()
-    dt = a.elapsed_time(b) / 1e3
-    return {"value": run.elements * steps / dt, "unit": "elements/s", "h2d_bytes_per_step": run.h2d,
+    value, _ = aggregate(a.elapsed_time(b) / 1e3, run.elements * steps, world, device)
+    return {"value": value, "unit": "elements/s", "h2d_bytes_per_step": run.h2d,
             "d2h_bytes_per_step": run.d2h, "steps": steps,
             "pipeline": "copies in, calls and copies out on three streams over two buffer slots"}
 
